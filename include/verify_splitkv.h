@@ -1,0 +1,160 @@
+/*
+ * verify_splitkv.h -- C ABI of the GB300 (sm_103a) split-KV verify attention.
+ *
+ * The operation (sglang "verify_splitkv.py" page: module docstring,
+ * "_verify_prefix_stage1", "_verify_combine_stage2", "verify_splitkv_fwd"):
+ * EAGLE speculative target-verify at topk = 1.  Sequence b owns l_ext draft
+ * query rows q[qo_indptr[b] + i] (i < l_ext) and a prefix of
+ * P_b = kv_indptr[b+1] - kv_indptr[b] tokens whose K/V rows live in a token
+ * pool, addressed through kv_indices[kv_indptr[b] + j].  Query head h reads
+ * KV head h / (h_q / h_kv).  Every draft row attends, under one softmax, over
+ *   - all P_b prefix keys: score sm_scale * k_scale * <q, K_pool[loc]>,
+ *     value v_scale * V_pool[loc];
+ *   - the drafts t <= i of its own sequence: score sm_scale * <q, k_ext[t]>,
+ *     value v_ext[t] (no k_scale / v_scale).
+ * The library computes this with split-KV (flash-decode) partial softmaxes
+ * over the prefix, merged by log-sum-exp with the causal draft block, and
+ * writes o[qo_indptr[b] + i, h, :] in bf16.  An empty prefix (P_b = 0) yields
+ * causal attention over the drafts alone.
+ *
+ * Threading and streams: every entry point may be called from any host
+ * thread.  verify_splitkv_fwd enqueues one kernel on the given stream and
+ * returns without synchronising and without reading device memory.
+ *
+ * Memory: all tensor pointers are DEVICE pointers owned by the caller.  The
+ * library never frees or retains them past the call.
+ */
+#ifndef VERIFY_SPLITKV_H
+#define VERIFY_SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of a vsk_tensor. */
+enum {
+  VSK_DTYPE_BF16 = 0,     /* bfloat16                                   */
+  VSK_DTYPE_FP8E4M3 = 1,  /* float8 e4m3 "fn" (no infinities)           */
+  VSK_DTYPE_I32 = 2,      /* int32                                      */
+  VSK_DTYPE_I64 = 3       /* int64                                      */
+};
+
+/* A strided view of device memory.  Strides and shape are in ELEMENTS.  For
+ * 3-d tensors the last dimension must be contiguous (stride[2] == 1); 1-d
+ * tensors must be contiguous.  Unused trailing entries are ignored. */
+typedef struct vsk_tensor {
+  const void* data;  /* device pointer (may be NULL only when the tensor is empty) */
+  int32_t dtype;     /* one of VSK_DTYPE_*                                          */
+  int32_t ndim;      /* 1 or 3                                                      */
+  int64_t shape[3];
+  int64_t stride[3];
+} vsk_tensor;
+
+/* Gate: returns 1 when verify_splitkv_fwd can serve this problem exactly,
+ * 0 otherwise (the caller then falls back to its prefill/extend kernel).
+ * Mirrors "can_handle" on the "verify_splitkv.py" page and adds this build's
+ * own limits.  It inspects shapes, dtypes, strides, pointer alignment and the
+ * scalar flags only: it never reads tensor VALUES.
+ *
+ *   q_extend   [B*l_ext, h_q, D]    bf16
+ *   k_extend   [B*l_ext, h_kv, D]   bf16   (draft keys)
+ *   v_extend   [B*l_ext, h_kv, Dv]  bf16   (draft values)
+ *   k_buffer   [pool, h_kv, D]      bf16 or fp8 e4m3 (prefix key pool)
+ *   v_buffer   [pool, h_kv, Dv]     same dtype as k_buffer
+ *   qo_indptr  [B+1] int32, kv_indptr [B+1] int32, kv_indices [n] int32|int64
+ *   is_causal  must be nonzero; max_len_extend (= l_ext) must be >= 1 and
+ *              q_extend must hold exactly B * max_len_extend rows.
+ *   sliding_window_size > 0, has_sinks != 0, logit_cap > 0 and
+ *   xai_temperature_len > 0 are features this kernel does not implement:
+ *   any of them makes the gate return 0.
+ * Build limits: D == Dv in {64, 128, 256}; (h_q/h_kv) * l_ext <= 128
+ * (<= 64 when D = 256); pool rows 16-byte aligned (data pointer and the
+ * byte strides of both leading dimensions); q/k_extend/v_extend 4-byte aligned
+ * with even strides.  On 0, vsk_last_error() names the first failed check. */
+int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
+                   const vsk_tensor* v_extend, const vsk_tensor* k_buffer,
+                   const vsk_tensor* v_buffer, const vsk_tensor* qo_indptr,
+                   const vsk_tensor* kv_indptr, const vsk_tensor* kv_indices,
+                   int is_causal, int64_t max_len_extend,
+                   int64_t sliding_window_size, int has_sinks, float logit_cap,
+                   int64_t xai_temperature_len);
+
+/* Split-KV verify attention ("verify_splitkv_fwd" on the "verify_splitkv.py"
+ * page, same tensor roles).  Returns 1 after enqueueing the work on `stream`
+ * (a cudaStream_t; NULL is the legacy default stream), or 0 having enqueued
+ * NOTHING: the gate failed, o_extend is not a bf16 [B*l_ext, h_q, Dv] tensor
+ * with a contiguous last dimension and even strides, the workspace is too
+ * small, or a CUDA call failed.  vsk_last_error() says which.
+ *
+ *   o_extend    output, written only at rows [0, B*l_ext) and all h_q heads.
+ *   k_scale, v_scale  dequantisation multipliers of the prefix pool (1.0 for
+ *               a bf16 pool); they do not apply to k_extend / v_extend.
+ *   sm_scale    softmax scale; a value <= 0 or NaN selects 1/sqrt(D).
+ *   workspace   device scratch of workspace_bytes bytes, zero-filled before
+ *               its first use (cudaMemset or vsk_workspace_init) and then
+ *               reused unchanged: every call leaves its counters at zero.  The
+ *               needed size is at most vsk_workspace_size(max_bs, ...) for any
+ *               B <= max_bs on the same device.  Concurrent calls (on
+ *               different streams) must not share one workspace.
+ *               workspace == NULL selects a library-owned per-device buffer
+ *               that grows on demand; growth allocates and synchronises the
+ *               device, so make the first such call outside graph capture.
+ * Device-side checks: kv_indices values outside [0, pool) and inconsistent
+ * indptr entries are never dereferenced; they set a bit in the workspace
+ * error word (see vsk_read_error_flags) and the affected rows are computed
+ * without those keys. */
+int verify_splitkv_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
+                       const vsk_tensor* v_extend, const vsk_tensor* o_extend,
+                       const vsk_tensor* k_buffer, const vsk_tensor* v_buffer,
+                       const vsk_tensor* qo_indptr, const vsk_tensor* kv_indptr,
+                       const vsk_tensor* kv_indices, int is_causal,
+                       int64_t max_len_extend, float k_scale, float v_scale,
+                       float sm_scale, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Upper bound, in bytes, of the workspace verify_splitkv_fwd needs for any
+ * batch of up to max_bs sequences with these head counts and sizes on the
+ * CURRENT CUDA device (its SM count sets the number of persistent CTAs).
+ * Returns 0 when the shapes are unsupported or no device is present. */
+size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv,
+                          int64_t head_dim, int64_t v_head_dim,
+                          int64_t max_len_extend);
+
+/* Same bound for an explicit SM count (no CUDA call; usable without a GPU). */
+size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q,
+                                  int64_t h_kv, int64_t head_dim,
+                                  int64_t v_head_dim, int64_t max_len_extend);
+
+/* Zero-fills `bytes` bytes of a workspace on `stream` (asynchronous).
+ * Returns 1 on success, 0 on a CUDA error. */
+int vsk_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Synchronises `stream`, then copies the device error word of `workspace`
+ * (NULL: the library-owned workspace of the current device) into *flags and
+ * clears it.  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
+ * not non-decreasing or beyond kv_indices; 4 = qo_indptr inconsistent with
+ * l_ext; 8 = a bounded wait inside the kernel timed out (the kernel returned
+ * early; outputs are incomplete).  Returns 1 on success, 0 on a CUDA error.
+ * Intended for tests and debugging: it blocks the host. */
+int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
+
+/* Tuning override for tests and sweeps: number of persistent CTAs (0 = the
+ * device's SM count times the CTAs that fit per SM) and the minimum prefix
+ * tokens per CTA (0 = default).  Affects the split of the prefix across CTAs,
+ * never the definition of the result.  Process-wide; not thread-safe. */
+void vsk_set_tuning(int num_ctas, int min_tokens_per_cta);
+
+/* Message of the most recent 0 return on this host thread ("" if none). */
+const char* vsk_last_error(void);
+
+/* Library version string. */
+const char* vsk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_SPLITKV_H */

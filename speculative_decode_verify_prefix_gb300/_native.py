@@ -1,0 +1,104 @@
+"""Build and load the in-tree CUDA library (libverify_splitkv.so, sm_103a).
+
+The library is compiled from ``csrc/verify_splitkv.cu`` with nvcc into
+``_build/`` next to this file.  Loading never falls back to anything: if the
+library is missing or fails to load, callers get an exception.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "csrc", "verify_splitkv.cu")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "verify_splitkv.h")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, f"libverify_splitkv_{platform.machine()}.so")
+NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc_path() -> str:
+    for cand in (os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc"), "nvcc"):
+        if os.path.sep not in cand or os.path.exists(cand):
+            return cand
+    return "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (no-op when up to date)."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    deps = [SRC, HEADER]
+    if not force and os.path.exists(LIB_PATH):
+        if os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps):
+            return LIB_PATH
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc_path(), *NVCC_ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-shared", SRC, "-o", tmp]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class VskTensor(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 3),
+        ("stride", ctypes.c_int64 * 3),
+    ]
+
+
+DTYPE_BF16, DTYPE_FP8E4M3, DTYPE_I32, DTYPE_I64 = 0, 1, 2, 3
+
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.POINTER(VskTensor)
+
+
+def _bind(lib):
+    lib.vsk_can_handle.restype = ctypes.c_int
+    lib.vsk_can_handle.argtypes = [_P] * 8 + [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                              ctypes.c_float, ctypes.c_int64]
+    lib.verify_splitkv_fwd.restype = ctypes.c_int
+    lib.verify_splitkv_fwd.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                                                  ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.vsk_workspace_size.restype = ctypes.c_size_t
+    lib.vsk_workspace_size.argtypes = [ctypes.c_int64] * 6
+    lib.vsk_workspace_size_for_sms.restype = ctypes.c_size_t
+    lib.vsk_workspace_size_for_sms.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6
+    lib.vsk_workspace_init.restype = ctypes.c_int
+    lib.vsk_workspace_init.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.vsk_read_error_flags.restype = ctypes.c_int
+    lib.vsk_read_error_flags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.vsk_set_tuning.restype = None
+    lib.vsk_set_tuning.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.vsk_last_error.restype = ctypes.c_char_p
+    lib.vsk_last_error.argtypes = []
+    lib.vsk_version.restype = ctypes.c_char_p
+    lib.vsk_version.argtypes = []
+    return lib
+
+
+def lib():
+    """The loaded CUDA library; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"CUDA library {LIB_PATH} is missing: run __graft_entry__.build() "
+                        "(there is no CPU fallback)")
+                _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def last_error() -> str:
+    return lib().vsk_last_error().decode()

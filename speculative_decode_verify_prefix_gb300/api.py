@@ -1,0 +1,153 @@
+"""Python binding of the C ABI in include/verify_splitkv.h.
+
+Argument marshalling only: torch tensors become ``vsk_tensor`` views (device
+pointer, dtype code, shape, strides) and the call goes straight to the CUDA
+library.  Every step of the computation runs in the library's kernel.
+
+``can_handle`` and ``verify_splitkv_fwd`` keep the positional signature of the
+sglang "verify_splitkv.py" page (``can_handle``, ``verify_splitkv_fwd``), so a
+caller of that module can switch by changing the import.  The workspace cache
+mirrors the page's ``_VK_CACHE``: one zero-initialised buffer per device, sized
+by ``max_bs`` and grown only, so its address stays fixed across batch sizes.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _native
+
+_DT = {
+    torch.bfloat16: _native.DTYPE_BF16,
+    torch.float8_e4m3fn: _native.DTYPE_FP8E4M3,
+    torch.int32: _native.DTYPE_I32,
+    torch.int64: _native.DTYPE_I64,
+}
+
+
+def as_vsk(t: torch.Tensor) -> _native.VskTensor:
+    """A vsk_tensor view of a torch tensor (no copy)."""
+    v = _native.VskTensor()
+    v.data = t.data_ptr() if t.numel() else 0
+    v.dtype = _DT.get(t.dtype, -1)
+    v.ndim = t.dim()
+    for i in range(min(3, t.dim())):
+        v.shape[i] = t.shape[i]
+        v.stride[i] = t.stride(i)
+    return v
+
+
+def _ref(t):
+    return ctypes.byref(as_vsk(t))
+
+
+def can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
+               custom_mask, is_causal, mask_indptr, max_len_extend, sliding_window_size=-1, sinks=None,
+               logit_cap=0.0, xai_temperature_len=-1) -> bool:
+    """True iff the split-KV verify kernel serves this problem (shape and flag
+    checks only; tensor values are never read).  ``custom_mask`` is not
+    inspected: the kernel computes pure causal attention, which equals the tree
+    mask only at speculative topk == 1, so the caller gates on topk == 1."""
+    try:
+        mle = int(max_len_extend)
+    except (TypeError, ValueError):
+        return False
+    for t in (q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices):
+        if not isinstance(t, torch.Tensor) or t.dtype not in _DT or t.dim() > 3:
+            return False
+    sw = -1 if sliding_window_size is None else int(sliding_window_size)
+    xai = -1 if xai_temperature_len is None else int(xai_temperature_len)
+    cap = float(logit_cap) if logit_cap else 0.0
+    return bool(_native.lib().vsk_can_handle(
+        _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(k_buffer), _ref(v_buffer),
+        _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), int(bool(is_causal)), mle,
+        sw, int(sinks is not None), cap, xai))
+
+
+_WS = {}
+_WS_LOCK = threading.Lock()
+
+
+def workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> int:
+    return int(_native.lib().vsk_workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext))
+
+
+def get_workspace(device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> torch.Tensor:
+    """Zero-filled per-device workspace, grown (never shrunk) to fit max_bs."""
+    device = torch.device(device)
+    with torch.cuda.device(device):
+        need = workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext)
+    if need == 0:
+        raise RuntimeError("workspace size query failed: " + _native.last_error())
+    with _WS_LOCK:
+        ws = _WS.get(device)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(need, dtype=torch.uint8, device=device)
+            _WS[device] = ws
+    return ws
+
+
+def _coerce(x) -> float:
+    try:
+        return float(x)
+    except (TypeError, ValueError):
+        return 1.0
+
+
+def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer, qo_indptr, kv_indptr,
+                       kv_indices, custom_mask, is_causal, mask_indptr, max_len_extend, k_scale, v_scale,
+                       sm_scale=None, logit_cap=0.0, skip_prefix_custom_mask=True, sliding_window_size=-1,
+                       sinks=None, window_kv_offsets=None, xai_temperature_len=-1, max_bs=None,
+                       workspace=None, stream=None) -> bool:
+    """Drop-in for the prefill/extend attention call on the EAGLE target-verify
+    (topk = 1) shape.  Returns True once the kernel is enqueued on the current
+    stream (o_extend will hold the result), False if the case is unsupported
+    (nothing was launched; the caller falls back)."""
+    if not can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
+                      custom_mask, is_causal, mask_indptr, max_len_extend,
+                      sliding_window_size=sliding_window_size, sinks=sinks, logit_cap=logit_cap,
+                      xai_temperature_len=xai_temperature_len):
+        return False
+    bs = qo_indptr.shape[0] - 1
+    mle = int(max_len_extend)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q_extend.device, mb, q_extend.shape[1], k_extend.shape[1],
+                                  q_extend.shape[2], v_extend.shape[2], mle)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_extend.device)
+    sm = 0.0 if sm_scale is None else float(sm_scale)
+    ok = _native.lib().verify_splitkv_fwd(
+        _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
+        _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), int(bool(is_causal)), mle,
+        _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if not ok:
+        raise RuntimeError("verify_splitkv_fwd failed after the gate passed: " + _native.last_error())
+    return True
+
+
+def read_error_flags(workspace=None, stream=None) -> int:
+    """Device error word of a workspace (synchronises; for tests/debugging)."""
+    if workspace is None:
+        with _WS_LOCK:
+            ws = next(iter(_WS.values()), None) if _WS else None
+        workspace = ws
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    flags = ctypes.c_uint32(0)
+    ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    if not _native.lib().vsk_read_error_flags(ptr, ctypes.c_void_p(stream.cuda_stream), ctypes.byref(flags)):
+        raise RuntimeError(_native.last_error())
+    return int(flags.value)
+
+
+def set_tuning(num_ctas: int = 0, min_tokens_per_cta: int = 0) -> None:
+    """Override the CTA count / minimum tokens per CTA (0 = defaults)."""
+    _native.lib().vsk_set_tuning(int(num_ctas), int(min_tokens_per_cta))
+
+
+def version() -> str:
+    return _native.lib().vsk_version().decode()

@@ -1,0 +1,1269 @@
+// Split-KV verify attention for EAGLE target-verify at topk = 1, for GB300
+// (sm_103a).  The operation is defined on the sglang "verify_splitkv.py" page
+// (module docstring; "_verify_prefix_stage1" computes per-split partial
+// softmaxes over the gathered prefix with qk *= sm_scale * k_scale and
+// acc *= v_scale; "_verify_combine_stage2" merges the splits by log-sum-exp,
+// adds the causal draft-draft block without scales and merges again).  The
+// C ABI is declared in include/verify_splitkv.h.
+//
+// GB300 design (not the page's two-kernel Triton layout):
+//   * ONE persistent, warp-specialised kernel per call.  The flattened work
+//     space (sequence b, KV-head group hg, prefix token t) is cut into equal
+//     contiguous shares, one per CTA; grid = SMs x CTAs-per-SM from static
+//     shapes, the split itself is computed on the device from kv_indptr, so no
+//     host synchronisation is needed.
+//   * A producer warp gathers whole token rows (all HC KV heads of the group,
+//     e.g. 8 x 128 x 2 B = 2 KB at serving scale) with cp.async.bulk (TMA) into
+//     a padded shared-memory ring, completing on mbarriers; indices are
+//     prefetched several stages ahead with cp.async.
+//   * Consumer warps, one per (KV head, 16-row tile) of the packed query tile
+//     (all h_q/h_kv query heads x l_ext draft rows of one KV head), run
+//     bf16 mma.sync m16n8k16 for QK and PV with an fp32 online softmax, so each
+//     K/V byte is read from HBM once.
+//   * The last CTA to finish a segment (atomic ticket, no spin-wait) merges
+//     the other CTAs' partials by log-sum-exp and continues the same online
+//     softmax over the causal draft keys, then writes bf16 output.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/verify_splitkv.h"
+
+#define VSK_VERSION "verify_splitkv-gb300 0.1"
+
+namespace vsk {
+
+// ---------------------------------------------------------------------------
+// Constants shared by the host plan and the kernel.
+// ---------------------------------------------------------------------------
+constexpr int kStageTokens = 16;     // prefix tokens per pipeline stage (one mma k-step)
+constexpr int kMaxStages = 16;       // ring depth cap
+constexpr int kIdxAhead = 4;         // stages of kv_indices prefetched ahead of the copies
+constexpr int kIdxRing = 8;          // index ring entries (> kIdxAhead)
+constexpr int kCtlBytes = 2048;      // control block before the ring (see smem map below)
+constexpr int kOffBars = 256;        // mbarriers: full[nst], empty[nst]
+constexpr int kOffIdx = 512;         // index ring: kIdxRing x 16 x 8 B
+constexpr int kOffMask = 1536;       // per-stage valid-token masks
+constexpr int kSmemPerSM = 233472;   // 228 KB per SM
+constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
+constexpr int kReservedPerCTA = 1024;
+constexpr long long kDefaultMinTokens = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+enum : unsigned {
+  kErrBadIndex = 1u,
+  kErrBadKvIndptr = 2u,
+  kErrBadQoIndptr = 4u,
+  kErrTimeout = 8u,
+};
+
+struct Params {
+  const __nv_bfloat16* q;  long long q_s0, q_s1;
+  const __nv_bfloat16* ke; long long ke_s0, ke_s1;
+  const __nv_bfloat16* ve; long long ve_s0, ve_s1;
+  __nv_bfloat16* o;        long long o_s0, o_s1;
+  const unsigned char* kb; long long kb_s0, kb_s1;  // byte strides
+  const unsigned char* vb; long long vb_s0, vb_s1;  // byte strides
+  const int* qo;
+  const int* kvp;
+  const void* kvi;
+  int idx64;
+  long long n_idx, pool, n_rows;
+  int B, L, gq, R, HC, MT, n_hg, nwc, nst;
+  int tsk, tsv, stage_bytes, ring_off, scratch_off;
+  int k_contig, v_contig;
+  float scale2, dscale2, v_scale;
+  long long w_min;
+  unsigned* err;
+  int* cnt;
+  float* plse;
+  float* po;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and raises the CTA abort
+// flag plus the timeout error bit) if the phase does not complete within
+// kWaitLimitNs, or immediately once another warp of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared (TMA), completing `bytes` on mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
+  return __bfloat1622float2(v);
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// e4m3 x2 -> bf16 x2, exactly (every e4m3 value is a bf16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(unsigned short two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  __half2 hv = *reinterpret_cast<__half2*>(&h);
+  float2 f = __half22float2(hv);
+  return pack_bf16(f.x, f.y);
+}
+
+// ---------------------------------------------------------------------------
+// Work schedule: segments (b, hg) of virtual length max(P_b, 1), laid end to
+// end; CTA c owns positions [c*W, c*W + W).  Both the producer and the
+// consumers walk the same sequence deterministically.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void load_seq(const Params& p, int b, int& P, long long& kv0) {
+  const int a = __ldg(p.kvp + b);
+  const int e = __ldg(p.kvp + b + 1);
+  const bool ok = a >= 0 && e >= a && static_cast<long long>(e) <= p.n_idx;
+  P = ok ? e - a : 0;
+  kv0 = ok ? a : 0;
+}
+
+struct Seg {
+  int b, hg, len, P;
+  long long kv0, off;  // off: flattened position of the segment's first token
+};
+
+__device__ __forceinline__ void seg_advance(const Params& p, Seg& s) {
+  s.off += s.len;
+  if (++s.hg == p.n_hg) {
+    s.hg = 0;
+    if (++s.b < p.B) {
+      load_seq(p, s.b, s.P, s.kv0);
+      s.len = max(s.P, 1);
+    }
+  }
+}
+
+__device__ __forceinline__ bool seg_live(const Params& p, const Seg& s, long long end) {
+  return s.b < p.B && s.off < end;
+}
+
+// Stage iterator (producer): successive groups of <= 16 real prefix tokens.
+struct StageIt {
+  Seg s;
+  int tok, te;
+  bool valid;
+};
+
+__device__ __forceinline__ int piece_real_end(const Seg& s, long long end) {
+  const long long t1 = min(end, s.off + s.len) - s.off;
+  return static_cast<int>(min(t1, static_cast<long long>(s.P)));
+}
+
+__device__ __forceinline__ void sit_settle(const Params& p, StageIt& it, long long end) {
+  while (seg_live(p, it.s, end) && it.tok >= it.te) {
+    seg_advance(p, it.s);
+    it.tok = 0;
+    if (seg_live(p, it.s, end)) it.te = piece_real_end(it.s, end);
+  }
+  it.valid = seg_live(p, it.s, end);
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// Shared memory map (bytes):
+//   [0,   128)  control: sched base (i64) @0, sched b @8, abort @12, last @16
+//   [128, 256)  block-scan scratch (up to 16 x i64)
+//   [256, 512)  mbarriers full[nst] then empty[nst]
+//   [512,1536)  kv_indices ring, kIdxRing x 16 x 8 B
+//   [1536,1600) per-stage masks of valid tokens
+//   [ring_off, ...)    nst stages: K rows 16 x tsk, then V rows 16 x tsv
+//   [scratch_off, ...) fp8 only: per consumer warp bf16 K and V, 16 x (D+8)
+// ---------------------------------------------------------------------------
+template <int D>
+struct MaxWarps {
+  static constexpr int value = (D > 128) ? 4 : 8;
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
+    vsk_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
+  constexpr int NT = D / 8;        // n-tiles of the output row
+  constexpr int KS = D / 16;       // k-steps of the QK contraction
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  long long* ctl_base = reinterpret_cast<long long*>(smem);
+  int* ctl_b = reinterpret_cast<int*>(smem + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 12);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);
+  long long* scan_ws = reinterpret_cast<long long*>(smem + 128);
+  unsigned* masks = reinterpret_cast<unsigned*>(smem + kOffMask);
+  const uint32_t bar0 = smem_u32(smem + kOffBars);
+  const int nst = p.nst;
+
+  // ---- prologue: total virtual length and this CTA's starting segment ----
+  if (tid == 0) {
+    *abort_flag = 0;
+    *ctl_b = -1;
+  }
+  const int nthreads = blockDim.x;
+  const int per = (p.B + nthreads - 1) / nthreads;
+  const int b_lo = min(p.B, tid * per);
+  const int b_hi = min(p.B, b_lo + per);
+  long long mysum = 0;
+  bool bad_kvp = false;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int a = __ldg(p.kvp + b), e = __ldg(p.kvp + b + 1);
+    const bool ok = a >= 0 && e >= a && static_cast<long long>(e) <= p.n_idx;
+    bad_kvp |= !ok;
+    mysum += max(ok ? e - a : 0, 1);
+  }
+  if (bad_kvp && blockIdx.x == 0) atomicOr(p.err, kErrBadKvIndptr);
+  long long incl = mysum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  const int nwarps = nthreads >> 5;
+  if (lane == 31) scan_ws[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nwarps ? scan_ws[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    if (lane < nwarps) scan_ws[lane] = w;
+  }
+  __syncthreads();
+  const long long excl = (warp > 0 ? scan_ws[warp - 1] : 0) + incl - mysum;
+  const long long tot = scan_ws[nwarps - 1] * p.n_hg;
+  long long W = (tot + gridDim.x - 1) / gridDim.x;
+  if (W < p.w_min) W = p.w_min;
+  const long long start = static_cast<long long>(blockIdx.x) * W;
+  if (start >= tot) return;  // uniform: the whole CTA has no work
+  const long long end = min(tot, start + W);
+  {
+    long long off = excl;
+    for (int b = b_lo; b < b_hi; ++b) {
+      int P;
+      long long kv0;
+      load_seq(p, b, P, kv0);
+      const long long len = max(P, 1);
+      const long long base = off * p.n_hg;
+      if (start >= base && start < base + len * p.n_hg) {
+        *ctl_b = b;
+        *ctl_base = base;
+      }
+      off += len;
+    }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(bar0 + 8 * i, 1);
+      mbar_init(bar0 + 8 * (nst + i), p.nwc);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  Seg seg0;
+  seg0.b = *ctl_b;
+  if (seg0.b < 0) return;  // unreachable for consistent inputs; guards the walk
+  load_seq(p, seg0.b, seg0.P, seg0.kv0);
+  seg0.len = max(seg0.P, 1);
+  seg0.hg = static_cast<int>((start - *ctl_base) / seg0.len);
+  seg0.off = *ctl_base + static_cast<long long>(seg0.hg) * seg0.len;
+
+  unsigned char* ring = smem + p.ring_off;
+  const int rowK = p.HC * D * EK;  // bytes of one token's K rows for the group
+  const int rowV = p.HC * D * EK;
+
+  if (warp == p.nwc) {
+    // =========================== producer warp ===========================
+    const uint64_t pol = policy_evict_first();
+    StageIt ii, ci;  // index iterator (ahead) and copy iterator
+    ii.s = seg0;
+    ii.tok = static_cast<int>(start - seg0.off);
+    ii.te = piece_real_end(seg0, end);
+    sit_settle(p, ii, end);
+    ci = ii;
+    const uint32_t idx_base = smem_u32(smem + kOffIdx);
+    auto issue_idx = [&](const StageIt& it, int entry) {
+      if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
+        const long long n = it.s.kv0 + it.tok + lane;
+        const uint32_t dst = idx_base + entry * 128 + lane * 8;
+        if (p.idx64)
+          cp_async_8(dst, static_cast<const long long*>(p.kvi) + n);
+        else
+          cp_async_4(dst, static_cast<const int*>(p.kvi) + n);
+      }
+      cp_async_commit();
+    };
+#pragma unroll 1
+    for (int a = 0; a < kIdxAhead; ++a) {
+      issue_idx(ii, a % kIdxRing);
+      if (ii.valid) {
+        ii.tok += kStageTokens;
+        sit_settle(p, ii, end);
+      }
+    }
+    long long k = 0;
+#pragma unroll 1
+    while (ci.valid) {
+      issue_idx(ii, static_cast<int>((k + kIdxAhead) % kIdxRing));
+      if (ii.valid) {
+        ii.tok += kStageTokens;
+        sit_settle(p, ii, end);
+      }
+      cp_async_wait<kIdxAhead>();
+      const int slot = static_cast<int>(k % nst);
+      if (k >= nst) {
+        if (!mbar_wait(bar0 + 8 * (nst + slot), static_cast<uint32_t>(((k / nst) + 1) & 1), abort_flag, p.err))
+          break;
+      }
+      const int n = min(kStageTokens, ci.te - ci.tok);
+      long long loc = -1;
+      if (lane < n) {
+        const unsigned char* e = smem + kOffIdx + static_cast<int>(k % kIdxRing) * 128 + lane * 8;
+        loc = p.idx64 ? *reinterpret_cast<const long long*>(e) : static_cast<long long>(*reinterpret_cast<const int*>(e));
+      }
+      const bool ok = lane < n && loc >= 0 && loc < p.pool;
+      const unsigned mask = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
+      if (lane < n && !ok) atomicOr(p.err, kErrBadIndex);
+      unsigned char* stage = ring + slot * p.stage_bytes;
+      unsigned inv = (~mask) & 0xFFFFu;
+      if (inv) {
+        // V rows of absent tokens must be finite zeros: their softmax weight
+        // is 0, and 0 * (stale NaN) would poison the PV accumulation.
+        while (inv) {
+          const int t = __ffs(inv) - 1;
+          inv &= inv - 1;
+          uint4* dst = reinterpret_cast<uint4*>(stage + 16 * p.tsk + t * p.tsv);
+          for (int c = lane; c < rowV / 16; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      if (lane == 0) masks[slot] = mask;
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_expect_tx(bar0 + 8 * slot, static_cast<uint32_t>(__popc(mask)) * static_cast<uint32_t>(rowK + rowV));
+      __syncwarp();
+      if (ok) {
+        const uint32_t full = bar0 + 8 * slot;
+        const unsigned char* srcK = p.kb + loc * p.kb_s0 + static_cast<long long>(ci.s.hg) * p.HC * p.kb_s1;
+        const unsigned char* srcV = p.vb + loc * p.vb_s0 + static_cast<long long>(ci.s.hg) * p.HC * p.vb_s1;
+        const uint32_t dK = smem_u32(stage + lane * p.tsk);
+        const uint32_t dV = smem_u32(stage + 16 * p.tsk + lane * p.tsv);
+        if (p.k_contig) {
+          bulk_g2s(dK, srcK, rowK, full, pol);
+        } else {
+          for (int h = 0; h < p.HC; ++h) bulk_g2s(dK + h * D * EK, srcK + h * p.kb_s1, D * EK, full, pol);
+        }
+        if (p.v_contig) {
+          bulk_g2s(dV, srcV, rowV, full, pol);
+        } else {
+          for (int h = 0; h < p.HC; ++h) bulk_g2s(dV + h * D * EK, srcV + h * p.vb_s1, D * EK, full, pol);
+        }
+      }
+      ci.tok += kStageTokens;
+      sit_settle(p, ci, end);
+      ++k;
+    }
+    cp_async_wait<0>();
+    if (*abort_flag) {
+      // Leave no bulk copy in flight into this CTA's shared memory: wait
+      // (bounded, short) for the last issued stages to land.
+      for (long long j = max(0LL, k - nst); j < k; ++j) {
+        const uint32_t full = bar0 + 8 * static_cast<int>(j % nst);
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(full, static_cast<uint32_t>((j / nst) & 1)) && global_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ============================ consumer warps ============================
+  const int hc = warp / p.MT;
+  const int mt = warp % p.MT;
+  const int g = lane >> 2;
+  const int j = lane & 3;
+  const int RM = 16 * p.MT;
+  const int r0 = 16 * mt + g;
+  const int r1 = r0 + 8;
+  const float NEG_INF = -INFINITY;
+
+  // ldmatrix lane offsets inside a stage (bytes)
+  const int k_key = ((lane >> 4) << 3) + (lane & 7);
+  const int k_col = ((lane >> 3) & 1) * 8;
+  const int v_key = (((lane >> 3) & 1) << 3) + (lane & 7);
+  const int v_col = (lane >> 4) * 8;
+  const int sk = FP8 ? (D + 8) * 2 : p.tsk;  // token stride of the bf16 K rows read by ldmatrix
+  const int sv = FP8 ? (D + 8) * 2 : p.tsv;
+  unsigned char* scratch = smem + p.scratch_off + warp * (2 * 16 * (D + 8) * 2);
+
+  Seg s = seg0;
+  long long k = 0;
+  const long long Wl = W;
+  const int c_self = blockIdx.x;
+
+#pragma unroll 1
+  while (seg_live(p, s, end)) {
+    const int kvh = s.hg * p.HC + hc;
+    const int t0 = static_cast<int>(max(start, s.off) - s.off);
+    const int te = piece_real_end(s, end);
+    // sequence row base, validated against l_ext
+    int s_b;
+    {
+      const int a = __ldg(p.qo + s.b), e = __ldg(p.qo + s.b + 1);
+      const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
+      if (!ok && lane == 0 && hc == 0 && mt == 0) atomicOr(p.err, kErrBadQoIndptr);
+      s_b = ok ? a : s.b * p.L;
+    }
+    // query fragments of rows r0, r1 of this warp's tile (zero beyond R)
+    uint32_t qf[KS][4];
+    {
+      const bool v0 = r0 < p.R, v1 = r1 < p.R;
+      const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
+                                static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
+      const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
+                                static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qf[kk][0] = v0 ? ld_u32(q0 + kk * 16 + 2 * j) : 0u;
+        qf[kk][1] = v1 ? ld_u32(q1 + kk * 16 + 2 * j) : 0u;
+        qf[kk][2] = v0 ? ld_u32(q0 + kk * 16 + 8 + 2 * j) : 0u;
+        qf[kk][3] = v1 ? ld_u32(q1 + kk * 16 + 8 + 2 * j) : 0u;
+      }
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+    // ---------------- prefix: online softmax over this CTA's piece ----------------
+#pragma unroll 1
+    for (int tok = t0; tok < te; tok += kStageTokens, ++k) {
+      const int slot = static_cast<int>(k % nst);
+      mbar_wait(bar0 + 8 * slot, static_cast<uint32_t>((k / nst) & 1), abort_flag, p.err);
+      const unsigned mask = masks[slot];
+      const unsigned char* stage = ring + slot * p.stage_bytes;
+      uint32_t kaddr, vaddr;
+      if (FP8) {
+        // widen this head's 16 K and V rows to bf16 in the warp's scratch
+        const unsigned char* srcK = stage + hc * D;
+        const unsigned char* srcV = stage + 16 * p.tsk + hc * D;
+        unsigned char* dK = scratch;
+        unsigned char* dV = scratch + 16 * (D + 8) * 2;
+        for (int c = lane; c < D; c += 32) {  // D chunks of 16 B per 16 tokens
+          const int t = c / (D / 16), cc = c % (D / 16);
+          const uint4 a = *reinterpret_cast<const uint4*>(srcK + t * p.tsk + cc * 16);
+          const uint4 b = *reinterpret_cast<const uint4*>(srcV + t * p.tsv + cc * 16);
+          uint4 o0, o1, o2, o3;
+          o0.x = e4m3x2_to_bf16x2(a.x & 0xFFFF); o0.y = e4m3x2_to_bf16x2(a.x >> 16);
+          o0.z = e4m3x2_to_bf16x2(a.y & 0xFFFF); o0.w = e4m3x2_to_bf16x2(a.y >> 16);
+          o1.x = e4m3x2_to_bf16x2(a.z & 0xFFFF); o1.y = e4m3x2_to_bf16x2(a.z >> 16);
+          o1.z = e4m3x2_to_bf16x2(a.w & 0xFFFF); o1.w = e4m3x2_to_bf16x2(a.w >> 16);
+          o2.x = e4m3x2_to_bf16x2(b.x & 0xFFFF); o2.y = e4m3x2_to_bf16x2(b.x >> 16);
+          o2.z = e4m3x2_to_bf16x2(b.y & 0xFFFF); o2.w = e4m3x2_to_bf16x2(b.y >> 16);
+          o3.x = e4m3x2_to_bf16x2(b.z & 0xFFFF); o3.y = e4m3x2_to_bf16x2(b.z >> 16);
+          o3.z = e4m3x2_to_bf16x2(b.w & 0xFFFF); o3.w = e4m3x2_to_bf16x2(b.w >> 16);
+          *reinterpret_cast<uint4*>(dK + t * (D + 8) * 2 + cc * 32) = o0;
+          *reinterpret_cast<uint4*>(dK + t * (D + 8) * 2 + cc * 32 + 16) = o1;
+          *reinterpret_cast<uint4*>(dV + t * (D + 8) * 2 + cc * 32) = o2;
+          *reinterpret_cast<uint4*>(dV + t * (D + 8) * 2 + cc * 32 + 16) = o3;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * (nst + slot));  // ring slot no longer needed
+        kaddr = smem_u32(dK);
+        vaddr = smem_u32(dV);
+      } else {
+        kaddr = smem_u32(stage + hc * D * 2);
+        vaddr = smem_u32(stage + 16 * p.tsk + hc * D * 2);
+      }
+
+      // S = Q K^T for 16 keys: two n-tiles of 8 keys
+      float sc[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kaddr + k_key * sk + (kk * 16 + k_col) * 2, b0, b1, b2, b3);
+        mma_bf16(sc[0], qf[kk], b0, b1);
+        mma_bf16(sc[1], qf[kk], b2, b3);
+      }
+      // mask absent keys, scale into the log2 domain
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = t * 8 + 2 * j + (e & 1);
+          sc[t][e] = ((mask >> key) & 1u) ? sc[t][e] * p.scale2 : NEG_INF;
+        }
+      }
+      const float mx0 = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
+      const float mx1 = quad_max(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
+      const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
+      const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
+      float pr[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        pr[t][0] = exp2f(sc[t][0] - ms0);
+        pr[t][1] = exp2f(sc[t][1] - ms0);
+        pr[t][2] = exp2f(sc[t][2] - ms1);
+        pr[t][3] = exp2f(sc[t][3] - ms1);
+      }
+      l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+      l1 = l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+      m0 = mn0;
+      m1 = mn1;
+      uint32_t pa[4];
+      pa[0] = pack_bf16(pr[0][0], pr[0][1]);
+      pa[1] = pack_bf16(pr[0][2], pr[0][3]);
+      pa[2] = pack_bf16(pr[1][0], pr[1][1]);
+      pa[3] = pack_bf16(pr[1][2], pr[1][3]);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        acc[n][0] *= al0;
+        acc[n][1] *= al0;
+        acc[n][2] *= al1;
+        acc[n][3] *= al1;
+      }
+      // O += P V for 16 keys
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vaddr + v_key * sv + (n2 * 16 + v_col) * 2, b0, b1, b2, b3);
+        mma_bf16(acc[2 * n2], pa, b0, b1);
+        mma_bf16(acc[2 * n2 + 1], pa, b2, b3);
+      }
+      __syncwarp();
+      if (!FP8 && lane == 0) mbar_arrive(bar0 + 8 * (nst + slot));
+    }
+
+    // ---------------- piece end: partial, ticket, log-sum-exp merge ----------------
+    l0 = quad_sum(l0);
+    l1 = quad_sum(l1);
+    const int s_idx = s.b * p.n_hg + s.hg;
+    const long long c_first = s.off / Wl;
+    const long long c_last = (s.off + s.len - 1) / Wl;
+    bool finisher = true;
+    if (c_last > c_first) {
+      const long long slot_self = c_self + s_idx;
+      float* lse_p = p.plse + (slot_self * p.HC + hc) * RM;
+      float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * D;
+      const float inv0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
+      const float inv1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
+      if (j == 0) {
+        lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
+        lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+        *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+      }
+      __threadfence();
+      named_bar_sync(1, p.nwc * 32);
+      if (tid == 0) {
+        const int expected = static_cast<int>(c_last - c_first + 1);
+        const int old = atomicAdd(p.cnt + s_idx, 1);
+        const int last = (old == expected - 1) ? 1 : 0;
+        if (last) {
+          p.cnt[s_idx] = 0;  // leave the ticket at zero for the next call
+          __threadfence();
+        }
+        *last_flag = last;
+      }
+      named_bar_sync(1, p.nwc * 32);
+      finisher = *last_flag != 0;
+      if (finisher) {
+        // own state -> v_scale-applied unnormalised form, then fold in the others
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[n][0] *= p.v_scale;
+          acc[n][1] *= p.v_scale;
+          acc[n][2] *= p.v_scale;
+          acc[n][3] *= p.v_scale;
+        }
+#pragma unroll 1
+        for (long long c = c_first; c <= c_last; ++c) {
+          if (c == c_self) continue;
+          const long long sl = c + s_idx;
+          const float* lq = p.plse + (sl * p.HC + hc) * RM;
+          const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
+          const float e0 = __ldcg(lq + r0), e1 = __ldcg(lq + r1);
+          const float mn0 = fmaxf(m0, e0), mn1 = fmaxf(m1, e1);
+          const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
+          const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
+          const float a0 = exp2f(m0 - ms0), a1 = exp2f(m1 - ms1);
+          const float w0 = exp2f(e0 - ms0), w1 = exp2f(e1 - ms1);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
+            const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
+            acc[n][0] = acc[n][0] * a0 + (w0 > 0.f ? x0.x * w0 : 0.f);
+            acc[n][1] = acc[n][1] * a0 + (w0 > 0.f ? x0.y * w0 : 0.f);
+            acc[n][2] = acc[n][2] * a1 + (w1 > 0.f ? x1.x * w1 : 0.f);
+            acc[n][3] = acc[n][3] * a1 + (w1 > 0.f ? x1.y * w1 : 0.f);
+          }
+          l0 = l0 * a0 + w0;
+          l1 = l1 * a1 + w1;
+          m0 = mn0;
+          m1 = mn1;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        acc[n][0] *= p.v_scale;
+        acc[n][1] *= p.v_scale;
+        acc[n][2] *= p.v_scale;
+        acc[n][3] *= p.v_scale;
+      }
+    }
+
+    if (finisher) {
+      // ------------- causal draft keys: continue the same online softmax -------------
+      const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
+#pragma unroll 1
+      for (int td = 0; td * 8 < p.L; ++td) {
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
+        const int tkey = td * 8 + g;  // key whose K row this lane supplies
+        const bool kv = tkey < p.L;
+        const __nv_bfloat16* kp = p.ke + (static_cast<long long>(s_b) + (kv ? tkey : 0)) * p.ke_s0 +
+                                  static_cast<long long>(kvh) * p.ke_s1;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t b0 = kv ? ld_u32(kp + kk * 16 + 2 * j) : 0u;
+          const uint32_t b1 = kv ? ld_u32(kp + kk * 16 + 8 + 2 * j) : 0u;
+          mma_bf16(sd, qf[kk], b0, b1);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = td * 8 + 2 * j + (e & 1);
+          const int irow = (e < 2) ? i0 : i1;
+          sd[e] = (key < p.L && key <= irow) ? sd[e] * p.dscale2 : NEG_INF;
+        }
+        const float mx0 = quad_max(fmaxf(sd[0], sd[1]));
+        const float mx1 = quad_max(fmaxf(sd[2], sd[3]));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
+        const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
+        const float a0 = exp2f(m0 - ms0), a1 = exp2f(m1 - ms1);
+        float pd[4];
+        pd[0] = exp2f(sd[0] - ms0);
+        pd[1] = exp2f(sd[1] - ms0);
+        pd[2] = exp2f(sd[2] - ms1);
+        pd[3] = exp2f(sd[3] - ms1);
+        l0 = l0 * a0 + quad_sum(pd[0] + pd[1]);
+        l1 = l1 * a1 + quad_sum(pd[2] + pd[3]);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[n][0] *= a0;
+          acc[n][1] *= a0;
+          acc[n][2] *= a1;
+          acc[n][3] *= a1;
+        }
+        // fp32 weighted sum of the draft values of this tile
+#pragma unroll
+        for (int js = 0; js < 4; ++js) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = td * 8 + 2 * js + e;
+            if (key >= p.L) continue;  // uniform across the warp
+            const float w0 = __shfl_sync(0xffffffffu, pd[e], g * 4 + js);
+            const float w1 = __shfl_sync(0xffffffffu, pd[2 + e], g * 4 + js);
+            const __nv_bfloat16* vp = p.ve + (static_cast<long long>(s_b) + key) * p.ve_s0 +
+                                      static_cast<long long>(kvh) * p.ve_s1 + 2 * j;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              const float2 v = unpack_bf16(ld_u32(vp + n * 8));
+              acc[n][0] = fmaf(w0, v.x, acc[n][0]);
+              acc[n][1] = fmaf(w0, v.y, acc[n][1]);
+              acc[n][2] = fmaf(w1, v.x, acc[n][2]);
+              acc[n][3] = fmaf(w1, v.y, acc[n][3]);
+            }
+          }
+        }
+      }
+      // ------------------------------ output ------------------------------
+      const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+      if (r0 < p.R) {
+        __nv_bfloat16* op = p.o + (static_cast<long long>(s_b) + r0 / p.gq) * p.o_s0 +
+                            static_cast<long long>(kvh * p.gq + r0 % p.gq) * p.o_s1 + 2 * j;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16(acc[n][0] * inv0, acc[n][1] * inv0);
+      }
+      if (r1 < p.R) {
+        __nv_bfloat16* op = p.o + (static_cast<long long>(s_b) + r1 / p.gq) * p.o_s0 +
+                            static_cast<long long>(kvh * p.gq + r1 % p.gq) * p.o_s1 + 2 * j;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16(acc[n][2] * inv1, acc[n][3] * inv1);
+      }
+    }
+    seg_advance(p, s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+thread_local std::string g_err;
+
+int fail(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return 0;
+}
+
+struct Plan {
+  int gq, R, MT, HC, n_hg, nwc, threads, ek;
+  int tsk, tsv, stage_bytes, nst, ring_off, scratch_off;
+  size_t smem;
+  int ctas_per_sm;
+};
+
+int floor_pow2(int x) {
+  int r = 1;
+  while (r * 2 <= x) r *= 2;
+  return r;
+}
+
+// Chooses the CTA shape: HC KV heads per CTA x MT 16-row tiles per head, one
+// consumer warp each; ring depth from the shared-memory budget.
+bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl) {
+  if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
+  const long long R = (h_q / h_kv) * L;
+  const int maxw = D > 128 ? 4 : 8;
+  if (R > 16LL * maxw) return fail("packed rows (h_q/h_kv)*l_ext = %lld exceed %d for head_dim %lld", R, 16 * maxw, D);
+  pl.gq = static_cast<int>(h_q / h_kv);
+  pl.R = static_cast<int>(R);
+  int mt = 1;
+  while (16 * mt < R) mt *= 2;
+  pl.MT = mt;
+  int hc = 1;
+  while (hc * 2 * mt <= maxw && h_kv % (hc * 2) == 0) hc *= 2;
+  pl.HC = hc;
+  pl.n_hg = static_cast<int>(h_kv / hc);
+  pl.nwc = hc * mt;
+  pl.threads = (pl.nwc + 1) * 32;
+  pl.ek = fp8 ? 1 : 2;
+  pl.tsk = hc * static_cast<int>(D) * pl.ek + 16;
+  pl.tsv = hc * static_cast<int>(D) * pl.ek + 16;
+  pl.stage_bytes = kStageTokens * (pl.tsk + pl.tsv);
+  const int scratch = fp8 ? pl.nwc * 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0;
+  int k = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
+  for (;;) {
+    const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
+    const int nst = std::min(kMaxStages, (budget - kCtlBytes - scratch) / pl.stage_bytes);
+    if (nst >= 2) {
+      pl.nst = nst;
+      pl.ctas_per_sm = k;
+      break;
+    }
+    if (k == 1) return fail("stage of %d bytes does not fit shared memory", pl.stage_bytes);
+    k /= 2;
+  }
+  pl.ring_off = kCtlBytes;
+  pl.scratch_off = pl.ring_off + pl.nst * pl.stage_bytes;
+  pl.smem = static_cast<size_t>(pl.scratch_off + scratch);
+  return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t cnt_off, lse_off, o_off, total;
+};
+
+WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
+  WsLayout w;
+  const long long segs = B * pl.n_hg;
+  const long long slots = n_cta + segs;
+  const long long rows = slots * pl.HC * 16LL * pl.MT;
+  w.cnt_off = 256;
+  w.lse_off = w.cnt_off + align256(4 * static_cast<size_t>(segs));
+  w.o_off = w.lse_off + align256(4 * static_cast<size_t>(rows));
+  w.total = w.o_off + 4 * static_cast<size_t>(rows) * static_cast<size_t>(D);
+  return w;
+}
+
+// process-wide tuning overrides
+int g_num_ctas = 0;
+long long g_min_tokens = 0;
+
+struct DevWs {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::vector<DevWs> g_ws;
+std::vector<int> g_sms;
+
+int device_sms(int dev) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  if (static_cast<int>(g_sms.size()) <= dev) g_sms.resize(dev + 1, 0);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+bool check_3d(const vsk_tensor* t, const char* name) {
+  if (!t) return fail("%s is NULL", name);
+  if (t->ndim != 3) return fail("%s must be 3-d (got ndim %d)", name, t->ndim);
+  for (int i = 0; i < 3; ++i)
+    if (t->shape[i] < 0) return fail("%s has a negative extent", name);
+  if (t->shape[0] > 0 && t->shape[1] > 0 && t->shape[2] > 1 && t->stride[2] != 1)
+    return fail("%s: last dimension must be contiguous", name);
+  const long long n = t->shape[0] * t->shape[1] * t->shape[2];
+  if (n > 0 && !t->data) return fail("%s: NULL data with %lld elements", name, n);
+  return true;
+}
+
+bool check_1d(const vsk_tensor* t, const char* name) {
+  if (!t) return fail("%s is NULL", name);
+  if (t->ndim != 1) return fail("%s must be 1-d (got ndim %d)", name, t->ndim);
+  if (t->shape[0] < 0) return fail("%s has a negative extent", name);
+  if (t->shape[0] > 1 && t->stride[0] != 1) return fail("%s must be contiguous", name);
+  if (t->shape[0] > 0 && !t->data) return fail("%s: NULL data", name);
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// can_handle of the "verify_splitkv.py" page plus this build's limits.
+bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* kb,
+          const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp, const vsk_tensor* kvi,
+          int is_causal, long long mle, long long sliding_window, int has_sinks, float logit_cap,
+          long long xai_len) {
+  // features the kernel does not implement
+  if (has_sinks) return fail("attention sinks are not supported");
+  if (sliding_window > 0) return fail("sliding_window_size > 0 is not supported");
+  if (logit_cap > 0.f) return fail("logit_cap > 0 is not supported");
+  if (xai_len > 0) return fail("xai_temperature_len > 0 is not supported");
+  if (!is_causal) return fail("only causal (topk = 1) verify is supported");
+  if (!check_3d(q, "q_extend") || !check_3d(ke, "k_extend") || !check_3d(ve, "v_extend") ||
+      !check_3d(kb, "k_buffer") || !check_3d(vb, "v_buffer"))
+    return false;
+  if (!check_1d(qo, "qo_indptr") || !check_1d(kvp, "kv_indptr") || !check_1d(kvi, "kv_indices")) return false;
+  const long long h_q = q->shape[1], h_kv = ke->shape[1];
+  if (h_kv == 0 || h_q % h_kv != 0) return fail("h_q (%lld) is not a multiple of h_kv (%lld)", h_q, h_kv);
+  if (kb->shape[1] != h_kv || vb->shape[1] != h_kv || ve->shape[1] != h_kv)
+    return fail("KV head count mismatch between k_extend, v_extend and the buffers");
+  const long long D = q->shape[2], Dv = ve->shape[2];
+  if (ke->shape[2] != D || kb->shape[2] != D) return fail("head_dim mismatch between q, k_extend and k_buffer");
+  if (vb->shape[2] != Dv) return fail("v_head_dim mismatch between v_extend and v_buffer");
+  const long long bs = qo->shape[0] - 1;
+  if (bs < 1) return fail("batch size must be >= 1");
+  if (kvp->shape[0] != bs + 1) return fail("kv_indptr must have B+1 entries");
+  if (mle < 1) return fail("max_len_extend must be >= 1");
+  if (q->shape[0] != bs * mle) return fail("ragged extend: q has %lld rows, expected B*max_len_extend = %lld", q->shape[0], bs * mle);
+  if (ke->shape[0] != q->shape[0] || ve->shape[0] != q->shape[0]) return fail("k_extend/v_extend rows differ from q_extend");
+  if (kb->shape[0] != vb->shape[0]) return fail("k_buffer and v_buffer pools differ in size");
+  // this build's limits
+  if (D != Dv) return fail("head_dim (%lld) != v_head_dim (%lld) is not built", D, Dv);
+  if (D != 64 && D != 128 && D != 256) return fail("head_dim %lld not in {64, 128, 256}", D);
+  if (q->dtype != VSK_DTYPE_BF16 || ke->dtype != VSK_DTYPE_BF16 || ve->dtype != VSK_DTYPE_BF16)
+    return fail("q_extend, k_extend and v_extend must be bf16");
+  if (kb->dtype != vb->dtype || (kb->dtype != VSK_DTYPE_BF16 && kb->dtype != VSK_DTYPE_FP8E4M3))
+    return fail("k_buffer and v_buffer must both be bf16 or both fp8 e4m3");
+  if (qo->dtype != VSK_DTYPE_I32 || kvp->dtype != VSK_DTYPE_I32) return fail("indptr arrays must be int32");
+  if (kvi->dtype != VSK_DTYPE_I32 && kvi->dtype != VSK_DTYPE_I64) return fail("kv_indices must be int32 or int64");
+  const long long R = (h_q / h_kv) * mle;
+  const long long maxR = D > 128 ? 64 : 128;
+  if (R > maxR) return fail("(h_q/h_kv)*max_len_extend = %lld exceeds %lld", R, maxR);
+  const size_t ek = kb->dtype == VSK_DTYPE_BF16 ? 2 : 1;
+  for (const vsk_tensor* t : {kb, vb}) {
+    if (!aligned(t->data, 16) || (t->stride[0] * ek) % 16 != 0 || (t->stride[1] * ek) % 16 != 0)
+      return fail("K/V pool rows must be 16-byte aligned");
+  }
+  for (const vsk_tensor* t : {q, ke, ve}) {
+    if (!aligned(t->data, 4) || (t->stride[0] % 2) != 0 || (t->stride[1] % 2) != 0)
+      return fail("q_extend/k_extend/v_extend must be 4-byte aligned with even strides");
+  }
+  return true;
+}
+
+using KernelFn = void (*)(Params);
+
+template <int D, bool FP8>
+KernelFn kernel_ptr() {
+  return vsk_kernel<D, FP8>;
+}
+
+KernelFn pick_kernel(int D, bool fp8) {
+  switch (D) {
+    case 64: return fp8 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
+    case 128: return fp8 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+    case 256: return fp8 ? kernel_ptr<256, true>() : kernel_ptr<256, false>();
+    default: return nullptr;
+  }
+}
+
+int prepare_kernel(KernelFn fn) {
+  // the attribute is per function and context; set it before every launch
+  // configuration query (cheap, idempotent)
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemPerCTAMax) == cudaSuccess;
+}
+
+void* internal_workspace(int dev, size_t need, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  if (static_cast<int>(g_ws.size()) <= dev) g_ws.resize(dev + 1);
+  DevWs& w = g_ws[dev];
+  if (w.bytes >= need) return w.ptr;
+  if (w.ptr) {
+    cudaStreamSynchronize(stream);
+    cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, need) != cudaSuccess) return nullptr;
+  if (cudaMemset(p, 0, need) != cudaSuccess) {
+    cudaFree(p);
+    return nullptr;
+  }
+  w.ptr = p;
+  w.bytes = need;
+  return p;
+}
+
+}  // namespace vsk
+
+using namespace vsk;
+
+extern "C" {
+
+int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend, const vsk_tensor* v_extend,
+                   const vsk_tensor* k_buffer, const vsk_tensor* v_buffer, const vsk_tensor* qo_indptr,
+                   const vsk_tensor* kv_indptr, const vsk_tensor* kv_indices, int is_causal,
+                   int64_t max_len_extend, int64_t sliding_window_size, int has_sinks, float logit_cap,
+                   int64_t xai_temperature_len) {
+  g_err.clear();
+  return gate(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices, is_causal,
+              max_len_extend, sliding_window_size, has_sinks, logit_cap, xai_temperature_len)
+             ? 1
+             : 0;
+}
+
+size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t head_dim,
+                                  int64_t v_head_dim, int64_t max_len_extend) {
+  if (num_sms <= 0 || max_bs < 1 || head_dim != v_head_dim || max_len_extend < 1) return 0;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
+  Plan pl;
+  if (!make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl)) return 0;
+  Plan pl8;
+  if (!make_plan(h_q, h_kv, head_dim, max_len_extend, true, pl8)) return 0;
+  const long long n_cta = static_cast<long long>(num_sms) * 4;  // bound on CTAs per SM
+  const size_t a = ws_layout(n_cta, max_bs, pl, head_dim).total;
+  const size_t b = ws_layout(n_cta, max_bs, pl8, head_dim).total;
+  return a > b ? a : b;
+}
+
+size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t v_head_dim,
+                          int64_t max_len_extend) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int sms = device_sms(dev);
+  if (sms <= 0) return 0;
+  size_t need = vsk_workspace_size_for_sms(sms, max_bs, h_q, h_kv, head_dim, v_head_dim, max_len_extend);
+  if (g_num_ctas > 4 * sms) {
+    Plan pl;
+    if (make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl)) {
+      const size_t t = ws_layout(g_num_ctas, max_bs, pl, head_dim).total;
+      if (t > need) need = t;
+    }
+  }
+  return need;
+}
+
+int vsk_workspace_init(void* workspace, size_t bytes, void* stream) {
+  g_err.clear();
+  if (!workspace || bytes == 0) return 1;
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail("cudaMemsetAsync: %s", cudaGetErrorString(e));
+  return 1;
+}
+
+int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags) {
+  g_err.clear();
+  if (!flags) return fail("flags is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail("cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  void* ws = workspace;
+  if (!ws) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail("no CUDA device");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (static_cast<int>(g_ws.size()) > dev) ws = g_ws[dev].ptr;
+  }
+  if (!ws) {
+    *flags = 0;
+    return 1;
+  }
+  e = cudaMemcpy(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail("cudaMemcpy: %s", cudaGetErrorString(e));
+  e = cudaMemset(ws, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return fail("cudaMemset: %s", cudaGetErrorString(e));
+  return 1;
+}
+
+void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
+  g_num_ctas = num_ctas > 0 ? num_ctas : 0;
+  g_min_tokens = min_tokens_per_cta > 0 ? min_tokens_per_cta : 0;
+}
+
+const char* vsk_last_error(void) { return g_err.c_str(); }
+
+const char* vsk_version(void) { return VSK_VERSION; }
+
+int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                       const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                       const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                       float sm_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
+  if (!check_3d(o, "o_extend")) return 0;
+  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
+      o->shape[2] != ve->shape[2])
+    return fail("o_extend must be bf16 [B*l_ext, h_q, v_head_dim]");
+  if (!aligned(o->data, 4) || (o->stride[0] % 2) != 0 || (o->stride[1] % 2) != 0)
+    return fail("o_extend must be 4-byte aligned with even strides");
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return fail("k_scale and v_scale must be finite");
+
+  const long long B = qo->shape[0] - 1;
+  const long long h_q = q->shape[1], h_kv = ke->shape[1], D = q->shape[2];
+  const bool fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
+  Plan pl;
+  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl)) return 0;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
+  const int sms = device_sms(dev);
+  if (sms <= 0) return fail("cannot query the SM count of device %d", dev);
+  KernelFn fn = pick_kernel(static_cast<int>(D), fp8);
+  if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);
+  if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
+  const int per_sm = std::min(occ, pl.ctas_per_sm);
+  const long long n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
+  const WsLayout wl = ws_layout(n_cta, B, pl, D);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (!ws) {
+    ws = static_cast<unsigned char*>(internal_workspace(dev, wl.total, st));
+    if (!ws) return fail("cannot allocate a %zu-byte workspace", wl.total);
+  } else if (workspace_bytes < wl.total) {
+    return fail("workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes, wl.total);
+  } else if (!aligned(ws, 256)) {
+    return fail("workspace must be 256-byte aligned");
+  }
+
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16*>(q->data);
+  p.q_s0 = q->stride[0];
+  p.q_s1 = q->stride[1];
+  p.ke = static_cast<const __nv_bfloat16*>(ke->data);
+  p.ke_s0 = ke->stride[0];
+  p.ke_s1 = ke->stride[1];
+  p.ve = static_cast<const __nv_bfloat16*>(ve->data);
+  p.ve_s0 = ve->stride[0];
+  p.ve_s1 = ve->stride[1];
+  p.o = static_cast<__nv_bfloat16*>(const_cast<void*>(o->data));
+  p.o_s0 = o->stride[0];
+  p.o_s1 = o->stride[1];
+  p.kb = static_cast<const unsigned char*>(kb->data);
+  p.kb_s0 = kb->stride[0] * pl.ek;
+  p.kb_s1 = kb->stride[1] * pl.ek;
+  p.vb = static_cast<const unsigned char*>(vb->data);
+  p.vb_s0 = vb->stride[0] * pl.ek;
+  p.vb_s1 = vb->stride[1] * pl.ek;
+  p.qo = static_cast<const int*>(qo->data);
+  p.kvp = static_cast<const int*>(kvp->data);
+  p.kvi = kvi->data;
+  p.idx64 = kvi->dtype == VSK_DTYPE_I64;
+  p.n_idx = kvi->shape[0];
+  p.pool = kb->shape[0];
+  p.n_rows = q->shape[0];
+  p.B = static_cast<int>(B);
+  p.L = static_cast<int>(max_len_extend);
+  p.gq = pl.gq;
+  p.R = pl.R;
+  p.HC = pl.HC;
+  p.MT = pl.MT;
+  p.n_hg = pl.n_hg;
+  p.nwc = pl.nwc;
+  p.nst = pl.nst;
+  p.tsk = pl.tsk;
+  p.tsv = pl.tsv;
+  p.stage_bytes = pl.stage_bytes;
+  p.ring_off = pl.ring_off;
+  p.scratch_off = pl.scratch_off;
+  p.k_contig = (kb->stride[1] == D) ? 1 : 0;
+  p.v_contig = (vb->stride[1] == D) ? 1 : 0;
+  const double sm = (sm_scale > 0.f && std::isfinite(sm_scale)) ? static_cast<double>(sm_scale)
+                                                                 : 1.0 / std::sqrt(static_cast<double>(D));
+  const double log2e = 1.4426950408889634;
+  p.scale2 = static_cast<float>(sm * static_cast<double>(k_scale) * log2e);
+  p.dscale2 = static_cast<float>(sm * log2e);
+  p.v_scale = v_scale;
+  p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
+  p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
+  p.po = reinterpret_cast<float*>(ws + wl.o_off);
+
+  void* args[] = {&p};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads), args,
+                       pl.smem, st);
+  if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
+  return 1;
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+"""Host-side boundary tests (no GPU needed).
+
+The gate follows ``can_handle`` on the "verify_splitkv.py" page and the
+fallback tests of the "test_verify_splitkv.py" page (non-causal, sinks,
+sliding window, logit cap, ragged extend); the build's own limits are checked
+too.  ``vsk_can_handle`` never dereferences tensor data, so CPU tensors stand
+in for device tensors here.
+"""
+import ctypes
+import re
+
+import pytest
+import torch
+
+import workloads
+import speculative_decode_verify_prefix_gb300 as vsk
+from speculative_decode_verify_prefix_gb300 import _native
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    vsk.build()
+
+
+def _inputs(**over):
+    spec = workloads.Spec("gate", (512, 512), 4, 16, 2, 256, 256, seed=3)
+    p = workloads.make_problem(spec, "cpu", **over)
+    return [p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"], p["kv_indptr"],
+            p["kv_indices"], None, True, None, p["max_len_extend"]]
+
+
+def test_accepts_the_verify_shape():
+    assert vsk.can_handle(*_inputs())
+
+
+def test_fallback_non_causal():
+    a = _inputs()
+    a[9] = False
+    assert not vsk.can_handle(*a)
+    assert "causal" in vsk.last_error()
+
+
+def test_fallback_exotic_features():
+    a = _inputs()
+    assert not vsk.can_handle(*a, sinks=torch.zeros(16))
+    assert not vsk.can_handle(*a, sliding_window_size=128)
+    assert not vsk.can_handle(*a, logit_cap=30.0)
+    assert not vsk.can_handle(*a, xai_temperature_len=4)
+    assert vsk.can_handle(*a, sliding_window_size=-1, logit_cap=0.0, xai_temperature_len=-1)
+
+
+def test_fallback_ragged_extend():
+    a = _inputs()
+    a[11] = a[11] + 1
+    assert not vsk.can_handle(*a)
+    assert "ragged" in vsk.last_error()
+    a[11] = "four"
+    assert not vsk.can_handle(*a)
+    a[11] = 0
+    assert not vsk.can_handle(*a)
+
+
+def test_rejects_shape_mismatches():
+    q, ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle = _inputs()
+    assert not vsk.can_handle(q[:, :15], ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle)  # 15 % 2
+    assert not vsk.can_handle(q, ke, ve, kb[:, :1], vb, qo, kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke, ve, kb, vb[:, :, :128], qo, kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke[:, :, :128], ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke, ve, kb, vb, qo[:1], kvp, kvi, cm, causal, mi, mle)  # bs < 1
+    assert not vsk.can_handle(q, ke, ve, kb, vb, qo, kvp[:2], kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q[0], ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle)  # not 3-d
+
+
+def test_rejects_unbuilt_dtypes_and_sizes():
+    q, ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle = _inputs()
+    assert not vsk.can_handle(q.half(), ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke, ve, kb, vb.to(torch.float8_e4m3fn), qo, kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke, ve, kb, vb, qo.long(), kvp, kvi, cm, causal, mi, mle)
+    assert not vsk.can_handle(q, ke, ve, kb, vb, qo, kvp, kvi.float(), cm, causal, mi, mle)
+    # head_dim not built
+    spec = workloads.Spec("d96", (20,), 4, 4, 1, 96, 96, seed=4)
+    p = workloads.make_problem(spec, "cpu")
+    assert not vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
+                              p["kv_indptr"], p["kv_indices"], None, True, None, 4)
+    # D != Dv
+    spec = workloads.Spec("dne", (20,), 4, 4, 1, 64, 128, seed=4)
+    p = workloads.make_problem(spec, "cpu")
+    assert not vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
+                              p["kv_indptr"], p["kv_indices"], None, True, None, 4)
+
+
+def test_packed_row_limit():
+    ok = workloads.Spec("r128", (20,), 8, 16, 1, 128, 128, seed=5)        # 16 * 8 = 128 rows
+    too = workloads.Spec("r256", (20,), 8, 32, 1, 128, 128, seed=5)       # 256 rows
+    d256 = workloads.Spec("r128d256", (20,), 8, 16, 1, 256, 256, seed=5)  # 128 rows at D=256
+    for spec, want in ((ok, True), (too, False), (d256, False)):
+        p = workloads.make_problem(spec, "cpu")
+        got = vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
+                             p["kv_indptr"], p["kv_indices"], None, True, None, 8)
+        assert got == want, spec.name
+
+
+def test_rejects_misaligned_pool():
+    q, ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle = _inputs()
+    flat = torch.zeros(kb.numel() + 8, dtype=torch.bfloat16)
+    shifted = flat[1:1 + kb.numel()].view(kb.shape)  # 2-byte offset
+    assert not vsk.can_handle(q, ke, ve, shifted, vb, qo, kvp, kvi, cm, causal, mi, mle)
+    assert "16-byte" in vsk.last_error()
+
+
+def test_fwd_returns_false_without_launch_when_gate_fails():
+    a = _inputs()
+    o = torch.empty(a[0].shape[0], 16, 256, dtype=torch.bfloat16)
+    a[9] = False
+    assert vsk.verify_splitkv_fwd(a[0], a[1], a[2], o, a[3], a[4], a[5], a[6], a[7], None, False, None, a[11],
+                                  1.0, 1.0) is False
+
+
+def test_c_fwd_rejects_bad_output_before_any_cuda_call():
+    lib = _native.lib()
+    q, ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle = _inputs()
+    o_bad = torch.empty(q.shape[0], 16, 128, dtype=torch.bfloat16)  # wrong Dv
+    r = vsk.api._ref
+    ok = lib.verify_splitkv_fwd(r(q), r(ke), r(ve), r(o_bad), r(kb), r(vb), r(qo), r(kvp), r(kvi), 1, mle,
+                                1.0, 1.0, 0.0, None, 0, None)
+    assert ok == 0 and "o_extend" in vsk.last_error()
+
+
+def test_workspace_bound_for_sms():
+    lib = _native.lib()
+    a = lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 128, 128, 4)
+    b = lib.vsk_workspace_size_for_sms(152, 128, 32, 8, 128, 128, 4)
+    assert 0 < a < b
+    # serving shape: partial slots (4 CTAs/SM bound + one per segment) x 8 heads x 16 rows x (128 + 1) fp32
+    slots = 4 * 152 + 64
+    assert a >= slots * 8 * 16 * 129 * 4
+    assert a < 64 * 2 ** 20
+    assert lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 96, 96, 4) == 0
+    assert lib.vsk_workspace_size_for_sms(0, 64, 32, 8, 128, 128, 4) == 0
+
+
+def _header_functions():
+    with open(_native.HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|void|char)\s*\*?\s*(\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _header_functions()
+    assert {"verify_splitkv_fwd", "vsk_can_handle", "vsk_workspace_size"} <= set(names)
+    lib = ctypes.CDLL(_native.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/verify_splitkv.h but not exported"
+
+
+def test_version_string():
+    assert vsk.version().startswith("verify_splitkv-gb300")

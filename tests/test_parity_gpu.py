@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerance: atol 2e-2, rtol 1e-2 on the bf16 output against the oracle's fp64
+value (the parity tolerance of the "test_verify_splitkv.py" page); integer
+index handling is checked bit-exactly (int32 vs int64 indices, pool-slot
+permutations, repeated calls).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module")
+def vsk():
+    import speculative_decode_verify_prefix_gb300 as m
+
+    m.build()
+    yield m
+    m.set_tuning(0, 0)
+
+
+def run_gpu(vsk, prob, o=None, **kw):
+    q = prob["q"]
+    if o is None:
+        o = torch.full((q.shape[0], q.shape[1], prob["v_ext"].shape[2]), float("nan"), dtype=torch.bfloat16,
+                       device=q.device)
+    ran = vsk.verify_splitkv_fwd(q, prob["k_ext"], prob["v_ext"], o, prob["k_buffer"], prob["v_buffer"],
+                                 prob["qo_indptr"], prob["kv_indptr"], prob["kv_indices"], None, True, None,
+                                 prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
+                                 sm_scale=prob["sm_scale"], **kw)
+    assert ran, vsk.last_error()
+    torch.cuda.synchronize()
+    return o
+
+
+def oracle_o(prob, **kw):
+    return oracle.verify_forward(workloads.to_oracle_arrays(prob), **kw)["o"]
+
+
+def check(got, ref, atol=ATOL, rtol=RTOL, rows=None):
+    g = got.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        g, ref = g[rows], ref[rows]
+    assert np.isfinite(g).all(), "non-finite output"
+    err = np.abs(g - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance; max abs err {err.max():.3e}"
+    return float(err.max())
+
+
+def gpu_problem(spec, **over):
+    return workloads.make_problem(spec, "cuda", **over)
+
+
+# ----------------------------------------------------------------- the five workloads
+def test_tiny(vsk):
+    p = gpu_problem(workloads.TINY)
+    err = check(run_gpu(vsk, p), oracle_o(p))
+    assert err < 2e-3
+    assert vsk.read_error_flags() == 0
+
+
+def test_head_dim_256(vsk):
+    p = gpu_problem(workloads.D256)
+    check(run_gpu(vsk, p), oracle_o(p))
+
+
+@pytest.mark.parametrize("spec", workloads.gqa_sweep(), ids=lambda s: s.name)
+def test_gqa_extend_sweep(vsk, spec):
+    p = gpu_problem(spec)
+    check(run_gpu(vsk, p), oracle_o(p))
+
+
+def test_fp8_pool_with_scales(vsk):
+    p = gpu_problem(workloads.FP8)
+    err = check(run_gpu(vsk, p), oracle_o(p))
+    assert err < 2e-3  # fp8 decode is exact on both sides; only bf16 rounding remains
+
+
+def _subproblem(prob, b):
+    """Sequence b alone, with its referenced pool rows gathered to the host."""
+    kvp, qo = prob["kv_indptr"].cpu(), prob["qo_indptr"].cpu()
+    s, e = int(qo[b]), int(qo[b + 1])
+    ps, pe = int(kvp[b]), int(kvp[b + 1])
+    loc = prob["kv_indices"][ps:pe].long()
+    uniq, inv = torch.unique(loc, return_inverse=True)
+    sub = {
+        "q": prob["q"][s:e].cpu(), "k_ext": prob["k_ext"][s:e].cpu(), "v_ext": prob["v_ext"][s:e].cpu(),
+        "k_buffer": prob["k_buffer"][uniq].cpu(), "v_buffer": prob["v_buffer"][uniq].cpu(),
+        "qo_indptr": torch.tensor([0, e - s], dtype=torch.int32),
+        "kv_indptr": torch.tensor([0, pe - ps], dtype=torch.int32),
+        "kv_indices": inv.cpu().to(torch.int64),
+        "sm_scale": prob["sm_scale"], "k_scale": prob["k_scale"], "v_scale": prob["v_scale"],
+    }
+    return sub, (s, e)
+
+
+def test_serving_scale_sampled(vsk):
+    """Full serving-scale batch in the benchmark's launch configuration; the
+    oracle checks three whole sequences (all heads, all draft rows)."""
+    p = gpu_problem(workloads.SERVING)
+    o = run_gpu(vsk, p)
+    g = o.float()
+    assert torch.isfinite(g).all()
+    for b in (0, 31, 63):
+        sub, (s, e) = _subproblem(p, b)
+        ref = oracle_o(sub, nthreads=0)
+        check(o[s:e], ref)
+    assert vsk.read_error_flags() == 0
+    del p
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------- edge cases
+EDGE = [
+    workloads.Spec("mixed_ragged_empty", (0, 1, 15, 16, 17, 300, 0, 1000), 3, 8, 2, 128, 128, perm=True,
+                   pool_extra=50, seed=101),
+    workloads.Spec("all_empty", (0, 0, 0), 4, 8, 4, 128, 128, seed=102),
+    workloads.Spec("l1_decode", (700, 33), 1, 32, 8, 128, 128, perm=True, seed=103),
+    workloads.Spec("rows128", (333, 1024), 8, 16, 1, 128, 128, perm=True, seed=104),
+    workloads.Spec("d256_rows64", (250, 517), 8, 16, 2, 256, 256, perm=True, seed=105),
+    workloads.Spec("d64_hkv8", (129, 77, 400), 4, 32, 8, 64, 64, perm=True, seed=106),
+    workloads.Spec("bf16_scales", (1024, 2048), 4, 16, 2, 256, 256, k_scale=0.5, v_scale=0.25, seed=107),
+    workloads.Spec("fp8_d64", (100, 257), 2, 8, 4, 64, 64, pool="e4m3", perm=True, k_scale=2.0, v_scale=0.5,
+                   seed=108),
+    workloads.Spec("fp8_d128_hkv8", (1000, 35, 513), 4, 32, 8, 128, 128, pool="e4m3", perm=True, k_scale=0.75,
+                   v_scale=1.5, seed=109),
+    workloads.Spec("hkv6", (200, 90), 3, 12, 6, 128, 128, perm=True, seed=110),
+    workloads.Spec("single_seq_long", (20000,), 4, 8, 2, 128, 128, perm=True, seed=111),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=lambda s: s.name)
+def test_edge_cases(vsk, spec):
+    p = gpu_problem(spec)
+    check(run_gpu(vsk, p), oracle_o(p))
+    assert vsk.read_error_flags() == 0
+
+
+def test_poisoned_unreferenced_slots(vsk):
+    spec = workloads.Spec("poison", (40, 0, 129), 4, 8, 2, 128, 128, perm=True, pool_extra=300, poison=True,
+                          seed=112)
+    p = gpu_problem(spec)
+    check(run_gpu(vsk, p), oracle_o(p))
+
+
+@pytest.mark.parametrize("num_ctas,min_tok", [(1, 0), (2, 16), (3, 16), (7, 16), (64, 16), (1000, 16), (0, 16)])
+def test_split_count_independence(vsk, num_ctas, min_tok):
+    spec = workloads.Spec("splits", (2000, 5, 0, 777, 64), 4, 16, 4, 128, 128, perm=True, seed=113)
+    p = gpu_problem(spec)
+    vsk.set_tuning(0, 0)
+    base = run_gpu(vsk, p).float()
+    vsk.set_tuning(num_ctas, min_tok)
+    try:
+        o = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
+    check(o, oracle_o(p))
+    assert (o.float() - base).abs().max().item() < 1e-3 * 8  # a few bf16 ulps at |o| < 1
+
+
+def test_int32_indices_bitwise_equal(vsk):
+    spec = workloads.Spec("idx", (500, 37, 1200), 4, 16, 2, 128, 128, perm=True, pool_extra=20, seed=114)
+    a = run_gpu(vsk, gpu_problem(spec))
+    b = run_gpu(vsk, gpu_problem(spec, idx_dtype="int32"))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_slot_permutation_bitwise_equal(vsk):
+    spec = workloads.Spec("slots", (300, 1000), 4, 8, 2, 128, 128, perm=True, pool_extra=7, seed=115)
+    p = gpu_problem(spec)
+    a = run_gpu(vsk, p)
+    n = p["k_buffer"].shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(9)).cuda()
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(n, device="cuda")
+    p2 = dict(p, k_buffer=p["k_buffer"][perm].contiguous(), v_buffer=p["v_buffer"][perm].contiguous(),
+              kv_indices=inv[p["kv_indices"]])
+    b = run_gpu(vsk, p2)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_repeated_calls_identical(vsk):
+    """Tickets are left at zero after each call: back-to-back calls agree bitwise."""
+    spec = workloads.Spec("repeat", (3000, 4000, 10), 4, 32, 8, 128, 128, perm=True, seed=116)
+    p = gpu_problem(spec)
+    vsk.set_tuning(16, 64)  # force multi-CTA segments
+    try:
+        a = run_gpu(vsk, p)
+        b = run_gpu(vsk, p)
+        c = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_strided_views(vsk):
+    """Pool heads not contiguous within a token and q/o as strided views."""
+    spec = workloads.Spec("strided", (300, 45), 4, 8, 2, 128, 128, perm=True, seed=117)
+    p = gpu_problem(spec)
+    ref = oracle_o(p)
+    big_k = torch.zeros(p["k_buffer"].shape[0], 2, 2 * 128, dtype=torch.bfloat16, device="cuda")
+    big_v = torch.zeros_like(big_k)
+    big_k[:, :, 64:192] = p["k_buffer"]
+    big_v[:, :, 128:256] = p["v_buffer"]
+    big_q = torch.zeros(p["q"].shape[0], 8, 3 * 128, dtype=torch.bfloat16, device="cuda")
+    big_q[:, :, 128:256] = p["q"]
+    big_o = torch.full((p["q"].shape[0], 8, 2 * 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    p2 = dict(p, k_buffer=big_k[:, :, 64:192], v_buffer=big_v[:, :, 128:256], q=big_q[:, :, 128:256])
+    run_gpu(vsk, p2, o=big_o[:, :, 0:128])
+    check(big_o[:, :, 0:128], ref)
+    assert (big_o[:, :, 128:] == 7.0).all()  # nothing written outside the view
+
+
+def test_out_of_range_index_is_flagged_not_read(vsk):
+    spec = workloads.Spec("badidx", (50, 60), 2, 4, 1, 64, 64, seed=118)
+    p = gpu_problem(spec)
+    ref_other = oracle_o(p)
+    kvi = p["kv_indices"].clone()
+    kvi[55] = p["k_buffer"].shape[0]      # one past the pool (sequence 1)
+    kvi[70] = -3                          # negative (sequence 1)
+    p2 = dict(p, kv_indices=kvi)
+    vsk.read_error_flags()
+    o = run_gpu(vsk, p2)
+    assert vsk.read_error_flags() & 1
+    assert torch.isfinite(o.float()).all()
+    check(o, ref_other, rows=slice(0, 2))  # sequence 0 untouched
+    # sequence 1 equals the definition with those two keys removed
+    keep = torch.ones(60, dtype=torch.bool)
+    keep[[5, 20]] = False
+    p3 = dict(p, kv_indices=torch.cat([kvi[:50], kvi[50:][keep.cuda()]]),
+              kv_indptr=torch.tensor([0, 50, 108], dtype=torch.int32, device="cuda"))
+    check(o, oracle_o(p3), rows=slice(2, 4))
+
+
+def test_cuda_graph_replay_matches_eager(vsk):
+    spec = workloads.Spec("graph", (900, 50, 2048), 4, 32, 8, 128, 128, perm=True, seed=119)
+    p = gpu_problem(spec)
+    eager = run_gpu(vsk, p)
+    ws = vsk.get_workspace("cuda", 3, 32, 8, 128, 128, 4)
+    o = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run_gpu(vsk, p, o=o, workspace=ws)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    o.fill_(0)
+    with torch.cuda.graph(g):
+        vsk.verify_splitkv_fwd(p["q"], p["k_ext"], p["v_ext"], o, p["k_buffer"], p["v_buffer"], p["qo_indptr"],
+                               p["kv_indptr"], p["kv_indices"], None, True, None, 4, 1.0, 1.0,
+                               sm_scale=p["sm_scale"], workspace=ws)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), eager.view(torch.int16))
