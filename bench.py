@@ -1,0 +1,482 @@
+"""Benchmark: split-KV verify attention on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one call of the whole hot path (one verify_splitkv_fwd launch) over
+the serving-scale verify batch: B = 64 sequences, prefix lengths drawn
+uniformly from [8192, 32768], l_ext = 4 draft rows, h_q = 32, h_kv = 8,
+head_dim 128, bf16 K/V pool addressed through a random permutation
+(page size 1).  Inputs are synthetic and seeded (workloads.py), resident in
+HBM when the timed region starts, and larger than L2 (5.4 GB pool vs 129 MB).
+
+value  = algorithmic bytes per call / mean device time per call (GB/s).
+e2e    = the same metric through the public API with pinned host inputs:
+         every step copies all inputs host->device and the output back.
+roofline.achieved = algorithmic bytes per launch / mean launch duration,
+         against the measured HBM copy peak.
+cpu_baseline = the fp64 CPU oracle on a bounded sample of the same workload.
+
+--impl reference times that oracle instead (the reference arm): each step is a
+bounded sample of the workload on the host cores, reported in the same metric.
+Under torchrun (N > 1) every rank runs an independent replica (the path
+shards by sequence with no exchange), timings are maxed over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verify-attn KV GB/s (fraction of GB300 HBM peak) and µs/call, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "speculative_decode_verify_prefix_gb300", "csrc", "verify_splitkv.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is for another workload or an older kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_sha256") != kernel_source_hash() or t.get("workload") != workload:
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+WORKLOADS = {
+    "serving": workloads.SERVING,
+    "tiny": workloads.TINY,
+    "d256": workloads.D256,
+    "fp8": workloads.FP8,
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="serving")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- ranks
+class Dist:
+    """Process layout: torchrun env vars when present, else a single process."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return reduce_max(x, self.pg)
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def reduce_max(x: float, pg) -> float:
+    """Max of a scalar over all ranks (identity on one process)."""
+    if pg is None:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() and \
+        pg.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput: units every rank processed over the slowest rank's time."""
+    return per_rank_units * world / max_seconds
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index):
+        self.index = str(index)
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        return parse_clock_rows(rows, self.REASONS)
+
+
+def parse_clock_rows(rows, reason_names) -> dict:
+    sm, smax, reasons = [], [], set()
+    for r in rows:
+        r = [x.strip() for x in r]
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+        except ValueError:
+            continue
+        for name, val in zip(reason_names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- accounting
+def seq_bytes(prob, b: int) -> int:
+    """Algorithmic bytes of sequence b: its prefix K/V rows once per KV head,
+    its indices, queries, drafts and output."""
+    q, ke, ve = prob["q"], prob["k_ext"], prob["v_ext"]
+    P = prob["prefix_lens"][b]
+    h_q, h_kv, d, dv = q.shape[1], ke.shape[1], ke.shape[2], ve.shape[2]
+    L = prob["max_len_extend"]
+    e = prob["k_buffer"].element_size()
+    idx = prob["kv_indices"].element_size()
+    return int(P * h_kv * (d + dv) * e + P * idx + L * (2 * h_q * d + 2 * h_kv * (d + dv) + 2 * h_q * dv))
+
+
+def sample_arrays(prob, seqs):
+    """Host arrays for the oracle holding only the listed sequences, with each
+    sequence's referenced pool rows gathered (in first-use order) to the host."""
+    kvp = prob["kv_indptr"].cpu().tolist()
+    qo = prob["qo_indptr"].cpu().tolist()
+    qs, ks, vs, locs, lens, rows = [], [], [], [], [], []
+    for b in seqs:
+        qs.append(prob["q"][qo[b]:qo[b + 1]])
+        ks.append(prob["k_ext"][qo[b]:qo[b + 1]])
+        vs.append(prob["v_ext"][qo[b]:qo[b + 1]])
+        locs.append(prob["kv_indices"][kvp[b]:kvp[b + 1]].long())
+        lens.append(kvp[b + 1] - kvp[b])
+        rows.append(qo[b + 1] - qo[b])
+    loc = torch.cat(locs)
+    uniq, inv = torch.unique(loc, return_inverse=True)
+    sub = {
+        "q": torch.cat(qs), "k_ext": torch.cat(ks), "v_ext": torch.cat(vs),
+        "k_buffer": prob["k_buffer"][uniq], "v_buffer": prob["v_buffer"][uniq],
+        "kv_indptr": torch.tensor([0] + np.cumsum(lens).tolist(), dtype=torch.int32),
+        "qo_indptr": torch.tensor([0] + np.cumsum(rows).tolist(), dtype=torch.int32),
+        "kv_indices": inv.to(torch.int64),
+        "sm_scale": prob["sm_scale"], "k_scale": prob["k_scale"], "v_scale": prob["v_scale"],
+    }
+    return workloads.to_oracle_arrays(sub)
+
+
+class OracleSampler:
+    """Times the fp64 oracle on (sequence, query-head block) units of a workload."""
+
+    def __init__(self, prob, seqs):
+        import oracle
+
+        self.oracle = oracle
+        self.prob = prob
+        self.cores = oracle.max_threads(0)
+        self.seqs = list(seqs)
+        self.arrays = sample_arrays(prob, self.seqs)
+        self.h_q = prob["q"].shape[1]
+        self.out = {}
+
+    def run(self, units):
+        """units: list of (local sequence index, h0, h1).  Returns (seconds, bytes)."""
+        t0 = time.perf_counter()
+        for (s, h0, h1) in units:
+            self.oracle.verify_forward(self.arrays, b_range=(s, s + 1), h_range=(h0, h1), out=self.out)
+        dt = time.perf_counter() - t0
+        nbytes = sum(seq_bytes(self.prob, self.seqs[s]) * (h1 - h0) / self.h_q for (s, h0, h1) in units)
+        return dt, nbytes
+
+
+def cpu_baseline(prob, target_s: float) -> dict:
+    """The oracle as it stands on the host cores, on whole sequences of the
+    workload until about target_s seconds of CPU work."""
+    B = len(prob["prefix_lens"])
+    cal = OracleSampler(prob, [0])
+    h_q = cal.h_q
+    t1, _ = cal.run([(0, 0, h_q)])
+    n = max(1, min(B - 1, 32, int(target_s / max(t1, 1e-6))))
+    samp = OracleSampler(prob, range(1, 1 + n))
+    dt, nbytes, passes = 0.0, 0.0, 0
+    while dt < target_s and passes < 64:
+        d, b = samp.run([(s, 0, h_q) for s in range(n)])
+        dt, nbytes, passes = dt + d, nbytes + b, passes + 1
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": samp.cores, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"{passes} pass(es) over {n} whole sequences (all {h_q} query heads, all draft rows) of "
+                      f"the same workload, fp64, OpenMP over (sequence, head); bytes counted as the "
+                      f"sequences' algorithmic bytes"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def _call(vsk, prob, o, ws):
+    return vsk.verify_splitkv_fwd(prob["q"], prob["k_ext"], prob["v_ext"], o, prob["k_buffer"], prob["v_buffer"],
+                                  prob["qo_indptr"], prob["kv_indptr"], prob["kv_indices"], None, True, None,
+                                  prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
+                                  sm_scale=prob["sm_scale"], workspace=ws)
+
+
+def time_kernel(vsk, prob, o, ws, steps: int, warmup: int, dist: Dist, gpu_index: int):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        assert _call(vsk, prob, o, ws), vsk.last_error()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        t0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            _call(vsk, prob, o, ws)
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    region_ms = t0.elapsed_time(t1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return region_ms, statistics.fmean(launch_ms), statistics.median(launch_ms), clk.summary()
+
+
+def time_e2e(vsk, prob, steps: int, warmup: int):
+    """Public API end to end: pinned host inputs copied in, result copied out."""
+    names = ["q", "k_ext", "v_ext", "k_buffer", "v_buffer", "qo_indptr", "kv_indptr", "kv_indices"]
+    host = {k: prob[k].cpu().pin_memory() for k in names}
+    dev = {k: torch.empty_like(prob[k]) for k in names}
+    o = torch.empty(prob["q"].shape[0], prob["q"].shape[1], prob["v_ext"].shape[2], dtype=torch.bfloat16,
+                    device=prob["q"].device)
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+    d = dict(prob, **dev)
+    ws = vsk.get_workspace(o.device, len(prob["prefix_lens"]), o.shape[1], prob["k_ext"].shape[1],
+                           prob["q"].shape[2], prob["v_ext"].shape[2], prob["max_len_extend"])
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        assert _call(vsk, d, o, ws), vsk.last_error()
+        o_host.copy_(o, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1))
+    del host, dev
+    return statistics.fmean(times), h2d, d2h
+
+
+def run_ours(args, dist: Dist) -> dict:
+    import speculative_decode_verify_prefix_gb300 as vsk
+
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    spec = WORKLOADS[args.workload]
+    prob = workloads.make_problem(spec, dev)
+    B = len(prob["prefix_lens"])
+    nbytes = workloads.algorithmic_bytes(prob)
+    o = torch.empty(prob["q"].shape[0], prob["q"].shape[1], prob["v_ext"].shape[2], dtype=torch.bfloat16,
+                    device=dev)
+    ws = vsk.get_workspace(dev, B, prob["q"].shape[1], prob["k_ext"].shape[1], prob["q"].shape[2],
+                           prob["v_ext"].shape[2], prob["max_len_extend"])
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    gpu_index = visible.split(",")[dist.local_rank].strip() if visible else str(dist.local_rank)
+    region_ms, launch_ms, launch_med_ms, clocks = time_kernel(vsk, prob, o, ws, args.steps, args.warmup, dist,
+                                                              gpu_index)
+    flags = vsk.read_error_flags(ws)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} after the timed region")
+    region_s = dist.max(region_ms / 1e3)
+    launch_s = dist.max(launch_ms / 1e3)
+    ms_per_step = region_s * 1e3 / args.steps
+    value = aggregate(nbytes * args.steps, region_s, dist.world) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / launch_s / 1e9
+    traffic = traffic_per_launch(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_call": round(ms_per_step * 1e3, 2), "frac_of_hbm_peak": round(value / peak, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; workloads.py)",
+        "config": workload_config(spec, prob, nbytes),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "vsk_kernel<128,false>" if spec.d == 128 and spec.pool == "bf16" else "vsk_kernel",
+                     "launch_us_mean": round(launch_s * 1e6, 2), "launch_us_median": round(launch_med_ms * 1e3, 2),
+                     "bytes_per_launch": nbytes},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(vsk, prob, args.e2e_steps, 2)
+        e2e_s = dist.max(e2e_ms / 1e3)
+        line["e2e"] = {"value": round(aggregate(nbytes, e2e_s, dist.world) / 1e9, 3), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3),
+                       "steps": args.e2e_steps}
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+    return line
+
+
+def workload_config(spec, prob, nbytes) -> dict:
+    lens = prob["prefix_lens"]
+    return {
+        "workload": spec.name, "batch": len(lens), "prefix_tokens": int(sum(lens)),
+        "prefix_len_min": int(min(lens)), "prefix_len_max": int(max(lens)),
+        "prefix_lens": (f"uniform int [{spec.len_range[0]}, {spec.len_range[1]}], seed {spec.seed}"
+                        if spec.prefix_lens is None else list(spec.prefix_lens)),
+        "l_ext": spec.l_ext, "h_q": spec.h_q, "h_kv": spec.h_kv, "head_dim": spec.d, "v_head_dim": spec.dv,
+        "kv_pool": spec.pool, "kv_indices": ("random permutation" if spec.perm else "arange") + f", {spec.idx_dtype}",
+        "k_scale": spec.k_scale, "v_scale": spec.v_scale, "page_size": 1,
+        "algorithmic_bytes_per_call": nbytes,
+        "l2": "inputs larger than L2 (no flush)" if nbytes > 129e6 else "inputs fit in L2 (L2-resident figure)",
+        "kernel_launches_per_step": 1,
+    }
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, dist: Dist) -> dict | None:
+    """The oracle, as it stands, on the host cores: each step computes a bounded
+    sample (one sequence x a block of query heads) of the same workload."""
+    if dist.rank != 0:
+        return None
+    dev = torch.device("cuda", dist.local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    spec = WORKLOADS[args.workload]
+    prob = workloads.make_problem(spec, dev)
+    B = len(prob["prefix_lens"])
+    n_seq = min(B, 8)
+    samp = OracleSampler(prob, range(n_seq))
+    h_q = samp.h_q
+    hb = max(1, min(h_q, samp.cores))  # one query head per core per step
+    units = [(s, h0, min(h_q, h0 + hb)) for s in range(n_seq) for h0 in range(0, h_q, hb)]
+    for i in range(args.warmup):
+        samp.run([units[i % len(units)]])
+    tot_s, tot_b = 0.0, 0.0
+    for i in range(args.steps):
+        dt, nb = samp.run([units[(args.warmup + i) % len(units)]])
+        tot_s += dt
+        tot_b += nb
+    value = tot_b / tot_s / 1e9
+    nbytes = workloads.algorithmic_bytes(prob)
+    sample = (f"per step: 1 sequence x {hb} query heads (all draft rows) of the {spec.name} workload, "
+              f"cycling over its first {n_seq} sequences; fp64 oracle, OpenMP over heads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; workloads.py)", "config": workload_config(spec, prob, nbytes),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": samp.cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, dist)
+        else:
+            line = run_ours(args, dist)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -706,17 +706,15 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
       named_bar_sync(1, p.nwc * 32);
       finisher = *last_flag != 0;
       if (finisher) {
-        // own state -> v_scale-applied unnormalised form, then fold in the others
+        // Fold every piece of the segment, this CTA's own included (read
+        // back), in CTA order: the result does not depend on which CTA
+        // happened to finish last.
+        m0 = m1 = NEG_INF;
+        l0 = l1 = 0.f;
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          acc[n][0] *= p.v_scale;
-          acc[n][1] *= p.v_scale;
-          acc[n][2] *= p.v_scale;
-          acc[n][3] *= p.v_scale;
-        }
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll 1
         for (long long c = c_first; c <= c_last; ++c) {
-          if (c == c_self) continue;
           const long long sl = c + s_idx;
           const float* lq = p.plse + (sl * p.HC + hc) * RM;
           const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;

@@ -62,8 +62,9 @@ def gpu_problem(spec, **over):
 # ----------------------------------------------------------------- the five workloads
 def test_tiny(vsk):
     p = gpu_problem(workloads.TINY)
-    err = check(run_gpu(vsk, p), oracle_o(p))
-    assert err < 2e-3
+    o, ref = run_gpu(vsk, p), oracle_o(p)
+    err = check(o, ref)
+    assert err < 4e-3  # bf16 output rounding plus bf16 softmax weights, nothing more
     assert vsk.read_error_flags() == 0
 
 
@@ -80,8 +81,9 @@ def test_gqa_extend_sweep(vsk, spec):
 
 def test_fp8_pool_with_scales(vsk):
     p = gpu_problem(workloads.FP8)
-    err = check(run_gpu(vsk, p), oracle_o(p))
-    assert err < 2e-3  # fp8 decode is exact on both sides; only bf16 rounding remains
+    o, ref = run_gpu(vsk, p), oracle_o(p)
+    err = check(o, ref)
+    assert err < 2e-3  # fp8 decode is exact on both sides; outputs are ~v_scale/sqrt(n)
 
 
 def _subproblem(prob, b):
@@ -188,7 +190,8 @@ def test_slot_permutation_bitwise_equal(vsk):
 
 
 def test_repeated_calls_identical(vsk):
-    """Tickets are left at zero after each call: back-to-back calls agree bitwise."""
+    """Tickets are left at zero after each call and pieces merge in a fixed
+    order: back-to-back calls agree bitwise."""
     spec = workloads.Spec("repeat", (3000, 4000, 10), 4, 32, 8, 128, 128, perm=True, seed=116)
     p = gpu_problem(spec)
     vsk.set_tuning(16, 64)  # force multi-CTA segments
