@@ -147,6 +147,41 @@ int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
  * never the definition of the result.  Process-wide; not thread-safe. */
 void vsk_set_tuning(int num_ctas, int min_tokens_per_cta);
 
+/* Size, in bytes, of the scratch array built into the library for
+ * verify_splitkv_fwd_noalloc (32 MiB). */
+#define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
+
+/* verify_splitkv_fwd for callers that must not allocate device memory.  The
+ * source pages have no counterpart: it is a deployment convenience of this
+ * library.  Some callers cannot call cudaMalloc: serving engines that give
+ * all free HBM to their own pool allocator up front (a stray allocation can
+ * fail, fragment that pool or stall the device while memory is mapped), and
+ * plugin hosts whose interface passes only input and output pointers.  This
+ * entry point takes the same tensors as verify_splitkv_fwd but no workspace:
+ * its scratch is a VSK_NOALLOC_SCRATCH_BYTES array in the library's device
+ * image, which every GPU that loads the library holds until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - Each call first clears the array's error word and per-segment tickets
+ *     on `stream` (cudaMemsetAsync), then enqueues the kernel; the error word
+ *     is therefore not reported through vsk_read_error_flags.
+ *   - Every call shares the one array: calls whose kernels may overlap on the
+ *     GPU (different streams, or different host threads) race and corrupt
+ *     each other's results.  Serialise them on one stream.
+ *   - A problem whose scratch exceeds VSK_NOALLOC_SCRATCH_BYTES (roughly, more
+ *     than a few hundred sequence x KV-head-group segments at head_dim 128)
+ *     is rejected: returns 0, nothing enqueued, and vsk_last_error() says so.
+ * Returns 1 once enqueued, 0 otherwise (see verify_splitkv_fwd). */
+int verify_splitkv_fwd_noalloc(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
+                               const vsk_tensor* v_extend, const vsk_tensor* o_extend,
+                               const vsk_tensor* k_buffer, const vsk_tensor* v_buffer,
+                               const vsk_tensor* qo_indptr, const vsk_tensor* kv_indptr,
+                               const vsk_tensor* kv_indices, int is_causal,
+                               int64_t max_len_extend, float k_scale, float v_scale,
+                               float sm_scale, void* stream);
+
 /* Message of the most recent 0 return on this host thread ("" if none). */
 const char* vsk_last_error(void);
 

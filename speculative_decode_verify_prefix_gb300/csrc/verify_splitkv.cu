@@ -1265,3 +1265,87 @@ int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tens
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc at all: engines that hand every free
+// byte of HBM to their own pool allocator at start-up and forbid stray device
+// allocations (a cudaMalloc there can fail, fragment the pool, or stall every
+// stream while the driver maps memory), and plugin hosts whose interface
+// passes only input and output pointers with no workspace.  For them the
+// scratch this kernel needs (one ticket per segment, the error word and the
+// per-CTA log-sum-exp partials) lives in the array below, which the driver
+// creates when the library's module is loaded on a GPU and keeps until the
+// process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_vsk_static_scratch[VSK_NOALLOC_SCRATCH_BYTES];
+
+namespace vsk {
+namespace {
+
+std::mutex g_static_mu;
+std::vector<void*> g_static_addr;  // per device: device address of g_vsk_static_scratch
+
+// Device address of the scratch array on the current device.  The host-side
+// name is only a stand-in, so the address is asked from the runtime once per
+// device (with that device current) and cached.
+void* static_scratch(int dev) {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (static_cast<int>(g_static_addr.size()) <= dev) g_static_addr.resize(dev + 1, nullptr);
+  if (!g_static_addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_vsk_static_scratch);
+    if (e != cudaSuccess) {
+      fail("cudaGetSymbolAddress of the built-in scratch failed: %s", cudaGetErrorString(e));
+      return nullptr;
+    }
+    g_static_addr[dev] = ptr;
+  }
+  return g_static_addr[dev];
+}
+
+}  // namespace
+}  // namespace vsk
+
+extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve,
+                                          const vsk_tensor* o, const vsk_tensor* kb, const vsk_tensor* vb,
+                                          const vsk_tensor* qo, const vsk_tensor* kvp, const vsk_tensor* kvi,
+                                          int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                                          float sm_scale, void* stream) {
+  g_err.clear();
+  if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
+  if (!check_3d(o, "o_extend")) return 0;
+  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
+      o->shape[2] != ve->shape[2])
+    return fail("o_extend must be bf16 [B*l_ext, h_q, v_head_dim]");
+  const long long B = qo->shape[0] - 1;
+  const long long h_q = q->shape[1], h_kv = ke->shape[1], D = q->shape[2];
+  const bool fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
+  Plan pl;
+  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl)) return 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
+  const int sms = device_sms(dev);
+  KernelFn fn = pick_kernel(static_cast<int>(D), fp8);
+  if (sms <= 0 || !fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);
+  if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
+  const long long n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * std::min(occ, pl.ctas_per_sm);
+  const size_t need = ws_layout(n_cta, B, pl, D).total;
+  if (need > static_cast<size_t>(VSK_NOALLOC_SCRATCH_BYTES))
+    return fail("this problem needs %zu bytes of scratch, more than the %d bytes built into the library for "
+                "verify_splitkv_fwd_noalloc; use verify_splitkv_fwd with a caller workspace",
+                need, VSK_NOALLOC_SCRATCH_BYTES);
+  unsigned char* scratch = static_cast<unsigned char*>(static_scratch(dev));
+  if (!scratch) return 0;
+  // The array keeps whatever the previous call left: zero the error word and
+  // the per-segment tickets before this call's kernel runs.
+  const size_t clear = 256 + 4 * static_cast<size_t>(B) * static_cast<size_t>(pl.n_hg);
+  e = cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail("cudaMemsetAsync on the built-in scratch: %s", cudaGetErrorString(e));
+  return verify_splitkv_fwd(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale,
+                            sm_scale, scratch, VSK_NOALLOC_SCRATCH_BYTES, stream);
+}
