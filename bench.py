@@ -78,6 +78,9 @@ def traffic_per_launch(workload: str):
 
 WORKLOADS = {
     "serving": workloads.SERVING,
+    # same length distribution, 8 sequences (~0.67 GB > L2): the case multi-pass
+    # ncu captures run on
+    "serving_b8": workloads.replace(workloads.SERVING, name="serving_b8_p8k_32k", batch=8),
     "tiny": workloads.TINY,
     "d256": workloads.D256,
     "fp8": workloads.FP8,

@@ -147,6 +147,13 @@ int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
  * never the definition of the result.  Process-wide; not thread-safe. */
 void vsk_set_tuning(int num_ctas, int min_tokens_per_cta);
 
+/* Tuning override of the CTA shape, for sweeps: at most `max_ring_stages`
+ * 16-token stages in the shared-memory ring (>= 2; 0 = as many as fit) and at
+ * most `max_kv_heads_per_cta` KV heads served by one CTA (a power of two;
+ * 0 = up to 8).  Fewer heads per CTA means more, smaller CTAs per SM.  Never
+ * changes the result beyond rounding order.  Process-wide; not thread-safe. */
+void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta);
+
 /* Size, in bytes, of the scratch array built into the library for
  * verify_splitkv_fwd_noalloc (32 MiB). */
 #define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)

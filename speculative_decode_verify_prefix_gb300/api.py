@@ -149,5 +149,10 @@ def set_tuning(num_ctas: int = 0, min_tokens_per_cta: int = 0) -> None:
     _native.lib().vsk_set_tuning(int(num_ctas), int(min_tokens_per_cta))
 
 
+def set_tuning_shape(max_ring_stages: int = 0, max_kv_heads_per_cta: int = 0) -> None:
+    """Override ring depth / KV heads per CTA (0 = defaults)."""
+    _native.lib().vsk_set_tuning_shape(int(max_ring_stages), int(max_kv_heads_per_cta))
+
+
 def version() -> str:
     return _native.lib().vsk_version().decode()

@@ -48,18 +48,14 @@ namespace vsk {
 // Constants shared by the host plan and the kernel.
 // ---------------------------------------------------------------------------
 constexpr int kStageTokens = 16;     // prefix tokens per pipeline stage (one mma k-step)
-constexpr int kMaxStages = 16;       // ring depth cap
+constexpr int kMaxStages = 5;        // ring depth cap (kIdxAhead >= stages - 1)
 constexpr int kIdxAhead = 4;         // stages of kv_indices prefetched ahead of the copies
-constexpr int kIdxRing = 8;          // index ring entries (> kIdxAhead)
-constexpr int kCtlBytes = 2048;      // control block before the ring (see smem map below)
-constexpr int kOffBars = 256;        // mbarriers: full[nst], empty[nst]
-constexpr int kOffIdx = 512;         // index ring: kIdxRing x 16 x 8 B
-constexpr int kOffMask = 1536;       // per-stage valid-token masks
+constexpr int kIdxRing = 8;          // per-warp index ring entries (> kIdxAhead)
+constexpr int kCtlBytes = 256;       // control block before the warp regions
 constexpr int kSmemPerSM = 233472;   // 228 KB per SM
 constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr long long kDefaultMinTokens = 256;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
 enum : unsigned {
   kErrBadIndex = 1u,
@@ -81,8 +77,7 @@ struct Params {
   int idx64;
   long long n_idx, pool, n_rows;
   int B, L, gq, R, HC, MT, n_hg, nwc, nst;
-  int tsk, tsv, stage_bytes, ring_off, scratch_off;
-  int k_contig, v_contig;
+  int ring_off, warp_bytes;
   float scale2, dscale2, v_scale;
   long long w_min;
   unsigned* err;
@@ -98,72 +93,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait on an mbarrier phase.  Returns false (and raises the CTA abort
-// flag plus the timeout error bit) if the phase does not complete within
-// kWaitLimitNs, or immediately once another warp of the CTA has aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (unsigned it = 1;; ++it) {
-    if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
-}
-
-// 1-D bulk copy global -> shared (TMA), completing `bytes` on mbarrier `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                         uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
 }
 
 __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
@@ -172,10 +105,26 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16-byte global -> shared copy through L2 only (zero-filled when !valid),
+// with an L2 eviction-priority hint.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, bool valid, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// wait_group with a run-time count (0..3)
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    default: cp_async_wait<3>(); break;
+  }
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -223,6 +172,13 @@ __device__ __forceinline__ float quad_max(float x) {
 __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
   return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// 2^x with the hardware approximation (ex2.approx.ftz: about 2 ulp, -inf -> +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // e4m3 x2 -> bf16 x2, exactly (every e4m3 value is a bf16 value).
@@ -287,16 +243,42 @@ __device__ __forceinline__ void sit_settle(const Params& p, StageIt& it, long lo
   it.valid = seg_live(p, it.s, end);
 }
 
+// Query fragments (mma A operand, rows r0 and r0 + 8 of the packed tile) of
+// one segment, straight from global memory; rows beyond R are zero.  Returns
+// the segment's first draft row (qo_indptr[b], validated against l_ext).
+template <int KS>
+__device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int r0, int r1, int j, bool flag_err,
+                                      uint32_t (&qf)[KS][4]) {
+  const int a = __ldg(p.qo + s.b), e = __ldg(p.qo + s.b + 1);
+  const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
+  if (!ok && flag_err) atomicOr(p.err, kErrBadQoIndptr);
+  const int s_b = ok ? a : s.b * p.L;
+  const int kvh = s.hg * p.HC + hc;
+  const bool v0 = r0 < p.R, v1 = r1 < p.R;
+  const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
+                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
+  const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
+                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    qf[kk][0] = v0 ? ld_u32(q0 + kk * 16 + 2 * j) : 0u;
+    qf[kk][1] = v1 ? ld_u32(q1 + kk * 16 + 2 * j) : 0u;
+    qf[kk][2] = v0 ? ld_u32(q0 + kk * 16 + 8 + 2 * j) : 0u;
+    qf[kk][3] = v1 ? ld_u32(q1 + kk * 16 + 8 + 2 * j) : 0u;
+  }
+  return s_b;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // Shared memory map (bytes):
-//   [0,   128)  control: sched base (i64) @0, sched b @8, abort @12, last @16
+//   [0,   128)  control: sched base (i64) @0, sched b @8, ticket flags [2] @16
 //   [128, 256)  block-scan scratch (up to 16 x i64)
-//   [256, 512)  mbarriers full[nst] then empty[nst]
-//   [512,1536)  kv_indices ring, kIdxRing x 16 x 8 B
-//   [1536,1600) per-stage masks of valid tokens
-//   [ring_off, ...)    nst stages: K rows 16 x tsk, then V rows 16 x tsv
-//   [scratch_off, ...) fp8 only: per consumer warp bf16 K and V, 16 x (D+8)
+//   [ring_off + w * warp_bytes, ...)  warp w's private region:
+//        nst stages of K rows [16][D*e] then V rows [16][D*e] (bf16 rows are
+//        XOR-swizzled in 16-byte chunks, chunk ^ (token & 7), so 8-row ldmatrix
+//        phases hit 8 distinct bank groups); kIdxRing x 16 x 8 B of kv_indices;
+//        16 x 4 B valid-token masks; fp8 only: bf16 K and V, 16 x (D+8) each.
 // ---------------------------------------------------------------------------
 template <int D>
 struct MaxWarps {
@@ -304,30 +286,27 @@ struct MaxWarps {
 };
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
+__global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
   constexpr int NT = D / 8;        // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
+  constexpr int ROWB = D * EK;     // bytes of one head's K (or V) row
+  constexpr int CPR = ROWB / 16;   // 16-byte chunks per row
+  constexpr int STAGE_B = 2 * kStageTokens * ROWB;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   long long* ctl_base = reinterpret_cast<long long*>(smem);
   int* ctl_b = reinterpret_cast<int*>(smem + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 12);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);  // [2]
   long long* scan_ws = reinterpret_cast<long long*>(smem + 128);
-  unsigned* masks = reinterpret_cast<unsigned*>(smem + kOffMask);
-  const uint32_t bar0 = smem_u32(smem + kOffBars);
   const int nst = p.nst;
 
   // ---- prologue: total virtual length and this CTA's starting segment ----
-  if (tid == 0) {
-    *abort_flag = 0;
-    *ctl_b = -1;
-  }
+  if (tid == 0) *ctl_b = -1;
   const int nthreads = blockDim.x;
   const int per = (p.B + nthreads - 1) / nthreads;
   const int b_lo = min(p.B, tid * per);
@@ -382,13 +361,6 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
       off += len;
     }
   }
-  if (tid == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(bar0 + 8 * i, 1);
-      mbar_init(bar0 + 8 * (nst + i), p.nwc);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
   __syncthreads();
 
   Seg seg0;
@@ -399,116 +371,11 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
   seg0.hg = static_cast<int>((start - *ctl_base) / seg0.len);
   seg0.off = *ctl_base + static_cast<long long>(seg0.hg) * seg0.len;
 
-  unsigned char* ring = smem + p.ring_off;
-  const int rowK = p.HC * D * EK;  // bytes of one token's K rows for the group
-  const int rowV = p.HC * D * EK;
-
-  if (warp == p.nwc) {
-    // =========================== producer warp ===========================
-    const uint64_t pol = policy_evict_first();
-    StageIt ii, ci;  // index iterator (ahead) and copy iterator
-    ii.s = seg0;
-    ii.tok = static_cast<int>(start - seg0.off);
-    ii.te = piece_real_end(seg0, end);
-    sit_settle(p, ii, end);
-    ci = ii;
-    const uint32_t idx_base = smem_u32(smem + kOffIdx);
-    auto issue_idx = [&](const StageIt& it, int entry) {
-      if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
-        const long long n = it.s.kv0 + it.tok + lane;
-        const uint32_t dst = idx_base + entry * 128 + lane * 8;
-        if (p.idx64)
-          cp_async_8(dst, static_cast<const long long*>(p.kvi) + n);
-        else
-          cp_async_4(dst, static_cast<const int*>(p.kvi) + n);
-      }
-      cp_async_commit();
-    };
-#pragma unroll 1
-    for (int a = 0; a < kIdxAhead; ++a) {
-      issue_idx(ii, a % kIdxRing);
-      if (ii.valid) {
-        ii.tok += kStageTokens;
-        sit_settle(p, ii, end);
-      }
-    }
-    long long k = 0;
-#pragma unroll 1
-    while (ci.valid) {
-      issue_idx(ii, static_cast<int>((k + kIdxAhead) % kIdxRing));
-      if (ii.valid) {
-        ii.tok += kStageTokens;
-        sit_settle(p, ii, end);
-      }
-      cp_async_wait<kIdxAhead>();
-      const int slot = static_cast<int>(k % nst);
-      if (k >= nst) {
-        if (!mbar_wait(bar0 + 8 * (nst + slot), static_cast<uint32_t>(((k / nst) + 1) & 1), abort_flag, p.err))
-          break;
-      }
-      const int n = min(kStageTokens, ci.te - ci.tok);
-      long long loc = -1;
-      if (lane < n) {
-        const unsigned char* e = smem + kOffIdx + static_cast<int>(k % kIdxRing) * 128 + lane * 8;
-        loc = p.idx64 ? *reinterpret_cast<const long long*>(e) : static_cast<long long>(*reinterpret_cast<const int*>(e));
-      }
-      const bool ok = lane < n && loc >= 0 && loc < p.pool;
-      const unsigned mask = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
-      if (lane < n && !ok) atomicOr(p.err, kErrBadIndex);
-      unsigned char* stage = ring + slot * p.stage_bytes;
-      unsigned inv = (~mask) & 0xFFFFu;
-      if (inv) {
-        // V rows of absent tokens must be finite zeros: their softmax weight
-        // is 0, and 0 * (stale NaN) would poison the PV accumulation.
-        while (inv) {
-          const int t = __ffs(inv) - 1;
-          inv &= inv - 1;
-          uint4* dst = reinterpret_cast<uint4*>(stage + 16 * p.tsk + t * p.tsv);
-          for (int c = lane; c < rowV / 16; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
-      }
-      if (lane == 0) masks[slot] = mask;
-      __syncwarp();
-      if (lane == 0)
-        mbar_arrive_expect_tx(bar0 + 8 * slot, static_cast<uint32_t>(__popc(mask)) * static_cast<uint32_t>(rowK + rowV));
-      __syncwarp();
-      if (ok) {
-        const uint32_t full = bar0 + 8 * slot;
-        const unsigned char* srcK = p.kb + loc * p.kb_s0 + static_cast<long long>(ci.s.hg) * p.HC * p.kb_s1;
-        const unsigned char* srcV = p.vb + loc * p.vb_s0 + static_cast<long long>(ci.s.hg) * p.HC * p.vb_s1;
-        const uint32_t dK = smem_u32(stage + lane * p.tsk);
-        const uint32_t dV = smem_u32(stage + 16 * p.tsk + lane * p.tsv);
-        if (p.k_contig) {
-          bulk_g2s(dK, srcK, rowK, full, pol);
-        } else {
-          for (int h = 0; h < p.HC; ++h) bulk_g2s(dK + h * D * EK, srcK + h * p.kb_s1, D * EK, full, pol);
-        }
-        if (p.v_contig) {
-          bulk_g2s(dV, srcV, rowV, full, pol);
-        } else {
-          for (int h = 0; h < p.HC; ++h) bulk_g2s(dV + h * D * EK, srcV + h * p.vb_s1, D * EK, full, pol);
-        }
-      }
-      ci.tok += kStageTokens;
-      sit_settle(p, ci, end);
-      ++k;
-    }
-    cp_async_wait<0>();
-    if (*abort_flag) {
-      // Leave no bulk copy in flight into this CTA's shared memory: wait
-      // (bounded, short) for the last issued stages to land.
-      for (long long j = max(0LL, k - nst); j < k; ++j) {
-        const uint32_t full = bar0 + 8 * static_cast<int>(j % nst);
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(full, static_cast<uint32_t>((j / nst) & 1)) && global_ns() - t0 < 100000000ull) {
-        }
-      }
-    }
-    return;
-  }
-
-  // ============================ consumer warps ============================
+  // ============================ per-warp pipeline ============================
+  // Warp w serves KV head hc = w / MT of the group and the 16-row tile mt of
+  // its packed query rows.  It streams its head's K and V rows itself with
+  // 16-byte cp.async into a private nst-deep ring: no producer warp, no
+  // cross-warp waits.  Indices come kIdxAhead stages ahead, also by cp.async.
   const int hc = warp / p.MT;
   const int mt = warp % p.MT;
   const int g = lane >> 2;
@@ -517,50 +384,119 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
   const int r0 = 16 * mt + g;
   const int r1 = r0 + 8;
   const float NEG_INF = -INFINITY;
-
-  // ldmatrix lane offsets inside a stage (bytes)
-  const int k_key = ((lane >> 4) << 3) + (lane & 7);
-  const int k_col = ((lane >> 3) & 1) * 8;
-  const int v_key = (((lane >> 3) & 1) << 3) + (lane & 7);
-  const int v_col = (lane >> 4) * 8;
-  const int sk = FP8 ? (D + 8) * 2 : p.tsk;  // token stride of the bf16 K rows read by ldmatrix
-  const int sv = FP8 ? (D + 8) * 2 : p.tsv;
-  unsigned char* scratch = smem + p.scratch_off + warp * (2 * 16 * (D + 8) * 2);
-
-  Seg s = seg0;
-  long long k = 0;
+  unsigned char* ring = smem + p.ring_off + warp * p.warp_bytes;
+  unsigned char* idx_ring = ring + nst * STAGE_B;
+  unsigned* mask_ring = reinterpret_cast<unsigned*>(idx_ring + kIdxRing * 128);
+  unsigned char* scratch = reinterpret_cast<unsigned char*>(mask_ring) + 128;  // fp8: bf16 K, V
+  const uint32_t ring_s = smem_u32(ring);
+  const uint32_t idx_s = smem_u32(idx_ring);
+  const uint64_t pol = policy_evict_first();
   const long long Wl = W;
   const int c_self = blockIdx.x;
+  const bool flagger = (warp == 0 && lane == 0);
+
+  auto issue_idx = [&](const StageIt& it, long long job) {
+    if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
+      const long long n = it.s.kv0 + it.tok + lane;
+      const uint32_t dst = idx_s + static_cast<uint32_t>(job % kIdxRing) * 128u + lane * 8u;
+      if (p.idx64)
+        cp_async_8(dst, static_cast<const long long*>(p.kvi) + n);
+      else
+        cp_async_4(dst, static_cast<const int*>(p.kvi) + n);
+    }
+  };
+  auto issue_data = [&](const StageIt& it, long long job) {
+    if (!it.valid) return;
+    const int n = min(kStageTokens, it.te - it.tok);
+    const unsigned char* ie = idx_ring + static_cast<int>(job % kIdxRing) * 128;
+    long long myloc = -1;
+    if (lane < n)
+      myloc = p.idx64 ? *reinterpret_cast<const long long*>(ie + lane * 8)
+                      : static_cast<long long>(*reinterpret_cast<const int*>(ie + lane * 8));
+    const bool ok = lane < n && myloc >= 0 && myloc < p.pool;
+    const unsigned mask = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
+    if (lane < n && !ok && hc == 0 && mt == 0) atomicOr(p.err, kErrBadIndex);
+    if (lane == 0) mask_ring[job % 16] = mask;
+    const long long head = static_cast<long long>(it.s.hg) * p.HC + hc;
+    const unsigned char* kbase = p.kb + head * p.kb_s1;
+    const unsigned char* vbase = p.vb + head * p.vb_s1;
+    const uint32_t slot = ring_s + static_cast<uint32_t>(job % nst) * STAGE_B;
+#pragma unroll
+    for (int i = 0; i < CPR; ++i) {
+      const int c = lane + 32 * i;
+      const int row = c / CPR;  // 0..15 K rows, 16..31 V rows
+      const int t = row & 15;
+      const int cir = c % CPR;
+      const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+      const bool v = (mask >> t) & 1u;
+      // an absent token is zero-filled (nothing read); q is a valid, never-empty address
+      const void* src = v ? static_cast<const void*>(((row >> 4) ? vbase + loc * p.vb_s0 : kbase + loc * p.kb_s0) + cir * 16)
+                          : static_cast<const void*>(p.q);
+      const int pc = FP8 ? cir : (cir ^ (t & 7));
+      cp_async_16_zfill(slot + static_cast<uint32_t>((row >> 4) * (16 * ROWB) + t * ROWB + pc * 16), src, v, pol);
+    }
+  };
+
+  StageIt ii, di;
+  ii.s = seg0;
+  ii.tok = static_cast<int>(start - seg0.off);
+  ii.te = piece_real_end(seg0, end);
+  sit_settle(p, ii, end);
+  di = ii;
+  long long job_i = 0, job_d = 0;
+  auto step_idx = [&]() {
+    issue_idx(ii, job_i);
+    ++job_i;
+    if (ii.valid) {
+      ii.tok += kStageTokens;
+      sit_settle(p, ii, end);
+    }
+  };
+  auto step_data = [&]() {
+    issue_data(di, job_d);
+    ++job_d;
+    if (di.valid) {
+      di.tok += kStageTokens;
+      sit_settle(p, di, end);
+    }
+  };
+#pragma unroll 1
+  for (int a = 0; a < kIdxAhead; ++a) step_idx();
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+#pragma unroll 1
+  for (int a = 0; a < nst - 1; ++a) {
+    step_data();
+    step_idx();
+    cp_async_commit();
+  }
+
+  // ldmatrix lane roles (token row within the 16-token stage, 16-byte chunk)
+  const int k_key = ((lane >> 4) << 3) + (lane & 7);
+  const int k_chk = (lane >> 3) & 1;
+  const int v_key = (((lane >> 3) & 1) << 3) + (lane & 7);
+  const int v_chk = lane >> 4;
+
+  // The next piece's query fragments are loaded into registers while the
+  // current piece streams (head_dim <= 128), so a piece boundary costs no
+  // global round trip.
+  constexpr bool kQAhead = D <= 128;
+  uint32_t qf[KS][4];
+  uint32_t qn[kQAhead ? KS : 1][4];
+  Seg s = seg0;
+  load_q<KS>(p, s, hc, r0, r1, j, flagger, qf);
+  Seg sn = s;
+  seg_advance(p, sn);
+  if constexpr (kQAhead) {
+    if (seg_live(p, sn, end)) load_q<KS>(p, sn, hc, r0, r1, j, false, qn);
+  }
+  long long k = 0;
 
 #pragma unroll 1
   while (seg_live(p, s, end)) {
-    const int kvh = s.hg * p.HC + hc;
     const int t0 = static_cast<int>(max(start, s.off) - s.off);
     const int te = piece_real_end(s, end);
-    // sequence row base, validated against l_ext
-    int s_b;
-    {
-      const int a = __ldg(p.qo + s.b), e = __ldg(p.qo + s.b + 1);
-      const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
-      if (!ok && lane == 0 && hc == 0 && mt == 0) atomicOr(p.err, kErrBadQoIndptr);
-      s_b = ok ? a : s.b * p.L;
-    }
-    // query fragments of rows r0, r1 of this warp's tile (zero beyond R)
-    uint32_t qf[KS][4];
-    {
-      const bool v0 = r0 < p.R, v1 = r1 < p.R;
-      const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
-                                static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
-      const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
-                                static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qf[kk][0] = v0 ? ld_u32(q0 + kk * 16 + 2 * j) : 0u;
-        qf[kk][1] = v1 ? ld_u32(q1 + kk * 16 + 2 * j) : 0u;
-        qf[kk][2] = v0 ? ld_u32(q0 + kk * 16 + 8 + 2 * j) : 0u;
-        qf[kk][3] = v1 ? ld_u32(q1 + kk * 16 + 8 + 2 * j) : 0u;
-      }
-    }
     float acc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
@@ -569,21 +505,23 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
     // ---------------- prefix: online softmax over this CTA's piece ----------------
 #pragma unroll 1
     for (int tok = t0; tok < te; tok += kStageTokens, ++k) {
-      const int slot = static_cast<int>(k % nst);
-      mbar_wait(bar0 + 8 * slot, static_cast<uint32_t>((k / nst) & 1), abort_flag, p.err);
-      const unsigned mask = masks[slot];
-      const unsigned char* stage = ring + slot * p.stage_bytes;
-      uint32_t kaddr, vaddr;
-      if (FP8) {
-        // widen this head's 16 K and V rows to bf16 in the warp's scratch
-        const unsigned char* srcK = stage + hc * D;
-        const unsigned char* srcV = stage + 16 * p.tsk + hc * D;
+      cp_async_wait_dyn(nst - 2);  // stage k has landed (this lane's copies)
+      __syncwarp();                // ... and every other lane's
+      step_data();                 // refill the slot stage k-1 used
+      step_idx();
+      cp_async_commit();
+      const unsigned mask = mask_ring[k % 16];
+      unsigned char* slotp = ring + static_cast<int>(k % nst) * STAGE_B;
+      uint32_t kaddr0, kaddr1, vaddr0;
+      int kstride;
+      if constexpr (FP8) {
+        // widen the 16 K and V rows to bf16 (exact) in the warp's scratch
         unsigned char* dK = scratch;
         unsigned char* dV = scratch + 16 * (D + 8) * 2;
-        for (int c = lane; c < D; c += 32) {  // D chunks of 16 B per 16 tokens
+        for (int c = lane; c < D; c += 32) {  // D chunks of 16 B per 16 rows
           const int t = c / (D / 16), cc = c % (D / 16);
-          const uint4 a = *reinterpret_cast<const uint4*>(srcK + t * p.tsk + cc * 16);
-          const uint4 b = *reinterpret_cast<const uint4*>(srcV + t * p.tsv + cc * 16);
+          const uint4 a = *reinterpret_cast<const uint4*>(slotp + t * ROWB + cc * 16);
+          const uint4 b = *reinterpret_cast<const uint4*>(slotp + 16 * ROWB + t * ROWB + cc * 16);
           uint4 o0, o1, o2, o3;
           o0.x = e4m3x2_to_bf16x2(a.x & 0xFFFF); o0.y = e4m3x2_to_bf16x2(a.x >> 16);
           o0.z = e4m3x2_to_bf16x2(a.y & 0xFFFF); o0.w = e4m3x2_to_bf16x2(a.y >> 16);
@@ -599,13 +537,17 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
           *reinterpret_cast<uint4*>(dV + t * (D + 8) * 2 + cc * 32 + 16) = o3;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8 * (nst + slot));  // ring slot no longer needed
-        kaddr = smem_u32(dK);
-        vaddr = smem_u32(dV);
+        kstride = (D + 8) * 2;
+        kaddr0 = smem_u32(dK) + k_key * kstride + k_chk * 16;
+        vaddr0 = smem_u32(dV) + v_key * kstride + v_chk * 16;
+        kaddr1 = 0;
       } else {
-        kaddr = smem_u32(stage + hc * D * 2);
-        vaddr = smem_u32(stage + 16 * p.tsk + hc * D * 2);
+        kstride = ROWB;
+        kaddr0 = smem_u32(slotp) + k_key * ROWB;
+        vaddr0 = smem_u32(slotp) + 16 * ROWB + v_key * ROWB;
+        kaddr1 = 0;
       }
+      (void)kaddr1;
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys
       float sc[2][4];
@@ -614,17 +556,27 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kaddr + k_key * sk + (kk * 16 + k_col) * 2, b0, b1, b2, b3);
+        const int lc = kk * 2 + k_chk;
+        const uint32_t addr = FP8 ? kaddr0 + kk * 32 : kaddr0 + ((lc ^ (k_key & 7)) << 4);
+        ldsm_x4(addr, b0, b1, b2, b3);
         mma_bf16(sc[0], qf[kk], b0, b1);
         mma_bf16(sc[1], qf[kk], b2, b3);
       }
-      // mask absent keys, scale into the log2 domain
+      // scale into the log2 domain; mask absent keys (tail / dropped) only
+      // when the stage is not full (the mask is uniform across the warp)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = t * 8 + 2 * j + (e & 1);
-          sc[t][e] = ((mask >> key) & 1u) ? sc[t][e] * p.scale2 : NEG_INF;
+        for (int e = 0; e < 4; ++e) sc[t][e] *= p.scale2;
+      }
+      if (mask != 0xFFFFu) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = t * 8 + 2 * j + (e & 1);
+            if (!((mask >> key) & 1u)) sc[t][e] = NEG_INF;
+          }
         }
       }
       const float mx0 = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
@@ -632,17 +584,32 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
       const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
-      const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
       float pr[2][4];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        pr[t][0] = exp2f(sc[t][0] - ms0);
-        pr[t][1] = exp2f(sc[t][1] - ms0);
-        pr[t][2] = exp2f(sc[t][2] - ms1);
-        pr[t][3] = exp2f(sc[t][3] - ms1);
+        pr[t][0] = fast_exp2(sc[t][0] - ms0);
+        pr[t][1] = fast_exp2(sc[t][1] - ms0);
+        pr[t][2] = fast_exp2(sc[t][2] - ms1);
+        pr[t][3] = fast_exp2(sc[t][3] - ms1);
       }
-      l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-      l1 = l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+      const float ps0 = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+      const float ps1 = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+      // rescale only when some row's running maximum moved (rare once the
+      // maximum has settled); otherwise alpha is exactly 1
+      if (__any_sync(0xffffffffu, (mn0 != m0) || (mn1 != m1))) {
+        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[n][0] *= al0;
+          acc[n][1] *= al0;
+          acc[n][2] *= al1;
+          acc[n][3] *= al1;
+        }
+      }
+      l0 += ps0;
+      l1 += ps1;
       m0 = mn0;
       m1 = mn1;
       uint32_t pa[4];
@@ -650,34 +617,24 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
       pa[1] = pack_bf16(pr[0][2], pr[0][3]);
       pa[2] = pack_bf16(pr[1][0], pr[1][1]);
       pa[3] = pack_bf16(pr[1][2], pr[1][3]);
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        acc[n][0] *= al0;
-        acc[n][1] *= al0;
-        acc[n][2] *= al1;
-        acc[n][3] *= al1;
-      }
       // O += P V for 16 keys
 #pragma unroll
       for (int n2 = 0; n2 < NT / 2; ++n2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vaddr + v_key * sv + (n2 * 16 + v_col) * 2, b0, b1, b2, b3);
+        const int lc = n2 * 2 + v_chk;
+        const uint32_t addr = FP8 ? vaddr0 + n2 * 32 : vaddr0 + ((lc ^ (v_key & 7)) << 4);
+        ldsm_x4_t(addr, b0, b1, b2, b3);
         mma_bf16(acc[2 * n2], pa, b0, b1);
         mma_bf16(acc[2 * n2 + 1], pa, b2, b3);
       }
-      __syncwarp();
-      if (!FP8 && lane == 0) mbar_arrive(bar0 + 8 * (nst + slot));
     }
 
-    // ---------------- piece end: partial, ticket, log-sum-exp merge ----------------
+    // ---------------- piece end: write the partial and keep streaming ----------------
+    // (tickets, merges, drafts and output wait until the whole range is streamed)
     l0 = quad_sum(l0);
     l1 = quad_sum(l1);
-    const int s_idx = s.b * p.n_hg + s.hg;
-    const long long c_first = s.off / Wl;
-    const long long c_last = (s.off + s.len - 1) / Wl;
-    bool finisher = true;
-    if (c_last > c_first) {
-      const long long slot_self = c_self + s_idx;
+    {
+      const long long slot_self = c_self + static_cast<long long>(s.b) * p.n_hg + s.hg;
       float* lse_p = p.plse + (slot_self * p.HC + hc) * RM;
       float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * D;
       const float inv0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
@@ -691,8 +648,40 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
         *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
         *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
       }
-      __threadfence();
-      named_bar_sync(1, p.nwc * 32);
+    }
+    s = sn;
+    if (seg_live(p, s, end)) {
+      seg_advance(p, sn);
+      if constexpr (kQAhead) {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          qf[kk][0] = qn[kk][0];
+          qf[kk][1] = qn[kk][1];
+          qf[kk][2] = qn[kk][2];
+          qf[kk][3] = qn[kk][3];
+        }
+        if (seg_live(p, sn, end)) load_q<KS>(p, sn, hc, r0, r1, j, false, qn);
+      } else {
+        load_q<KS>(p, s, hc, r0, r1, j, false, qf);
+      }
+    }
+  }
+
+  // ================= epilogue: tickets, log-sum-exp merges, drafts, output =================
+  // No copy is left in flight, and every partial this thread wrote is made
+  // visible device-wide before any ticket of this CTA is taken.
+  cp_async_wait<0>();
+  __threadfence();
+  named_bar_sync(1, p.nwc * 32);
+  Seg sg = seg0;
+  int nbar = 0;  // ticket rounds so far: selects the flag slot (two slots, one barrier per round)
+#pragma unroll 1
+  while (seg_live(p, sg, end)) {
+    const long long s_idx = static_cast<long long>(sg.b) * p.n_hg + sg.hg;
+    const long long c_first = sg.off / Wl;
+    const long long c_last = (sg.off + sg.len - 1) / Wl;
+    bool finisher = true;
+    if (c_last > c_first) {
       if (tid == 0) {
         const int expected = static_cast<int>(c_last - c_first + 1);
         const int old = atomicAdd(p.cnt + s_idx, 1);
@@ -701,55 +690,46 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
           p.cnt[s_idx] = 0;  // leave the ticket at zero for the next call
           __threadfence();
         }
-        *last_flag = last;
+        last_flag[nbar & 1] = last;
       }
       named_bar_sync(1, p.nwc * 32);
-      finisher = *last_flag != 0;
-      if (finisher) {
-        // Fold every piece of the segment, this CTA's own included (read
-        // back), in CTA order: the result does not depend on which CTA
-        // happened to finish last.
-        m0 = m1 = NEG_INF;
-        l0 = l1 = 0.f;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll 1
-        for (long long c = c_first; c <= c_last; ++c) {
-          const long long sl = c + s_idx;
-          const float* lq = p.plse + (sl * p.HC + hc) * RM;
-          const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
-          const float e0 = __ldcg(lq + r0), e1 = __ldcg(lq + r1);
-          const float mn0 = fmaxf(m0, e0), mn1 = fmaxf(m1, e1);
-          const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
-          const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
-          const float a0 = exp2f(m0 - ms0), a1 = exp2f(m1 - ms1);
-          const float w0 = exp2f(e0 - ms0), w1 = exp2f(e1 - ms1);
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
-            const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
-            acc[n][0] = acc[n][0] * a0 + (w0 > 0.f ? x0.x * w0 : 0.f);
-            acc[n][1] = acc[n][1] * a0 + (w0 > 0.f ? x0.y * w0 : 0.f);
-            acc[n][2] = acc[n][2] * a1 + (w1 > 0.f ? x1.x * w1 : 0.f);
-            acc[n][3] = acc[n][3] * a1 + (w1 > 0.f ? x1.y * w1 : 0.f);
-          }
-          l0 = l0 * a0 + w0;
-          l1 = l1 * a1 + w1;
-          m0 = mn0;
-          m1 = mn1;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        acc[n][0] *= p.v_scale;
-        acc[n][1] *= p.v_scale;
-        acc[n][2] *= p.v_scale;
-        acc[n][3] *= p.v_scale;
-      }
+      finisher = last_flag[nbar & 1] != 0;
+      ++nbar;
     }
-
     if (finisher) {
+      const int kvh = sg.hg * p.HC + hc;
+      // Fold every piece of the segment in CTA order: the result does not
+      // depend on which CTA happened to finish last.
+      float acc[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+#pragma unroll 1
+      for (long long c = c_first; c <= c_last; ++c) {
+        const long long sl = c + s_idx;
+        const float* lq = p.plse + (sl * p.HC + hc) * RM;
+        const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
+        const float e0 = __ldcg(lq + r0), e1 = __ldcg(lq + r1);
+        const float mn0 = fmaxf(m0, e0), mn1 = fmaxf(m1, e1);
+        const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
+        const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
+        const float a0 = exp2f(m0 - ms0), a1 = exp2f(m1 - ms1);
+        const float w0 = exp2f(e0 - ms0), w1 = exp2f(e1 - ms1);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
+          const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
+          acc[n][0] = acc[n][0] * a0 + (w0 > 0.f ? x0.x * w0 : 0.f);
+          acc[n][1] = acc[n][1] * a0 + (w0 > 0.f ? x0.y * w0 : 0.f);
+          acc[n][2] = acc[n][2] * a1 + (w1 > 0.f ? x1.x * w1 : 0.f);
+          acc[n][3] = acc[n][3] * a1 + (w1 > 0.f ? x1.y * w1 : 0.f);
+        }
+        l0 = l0 * a0 + w0;
+        l1 = l1 * a1 + w1;
+        m0 = mn0;
+        m1 = mn1;
+      }
+      const int s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
 #pragma unroll 1
@@ -832,7 +812,7 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
           *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16(acc[n][2] * inv1, acc[n][3] * inv1);
       }
     }
-    seg_advance(p, s);
+    seg_advance(p, sg);
   }
 }
 
@@ -851,9 +831,15 @@ int fail(const char* fmt, ...) {
   return 0;
 }
 
+// process-wide tuning overrides (0 = default)
+int g_num_ctas = 0;
+long long g_min_tokens = 0;
+int g_max_stages = 0;
+int g_max_heads = 0;
+
 struct Plan {
   int gq, R, MT, HC, n_hg, nwc, threads, ek;
-  int tsk, tsv, stage_bytes, nst, ring_off, scratch_off;
+  int stage_bytes, nst, ring_off, warp_bytes;
   size_t smem;
   int ctas_per_sm;
 };
@@ -877,20 +863,22 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   while (16 * mt < R) mt *= 2;
   pl.MT = mt;
   int hc = 1;
-  while (hc * 2 * mt <= maxw && h_kv % (hc * 2) == 0) hc *= 2;
+  const int hc_cap = g_max_heads > 0 ? g_max_heads : maxw;
+  while (hc * 2 * mt <= maxw && hc * 2 <= hc_cap && h_kv % (hc * 2) == 0) hc *= 2;
   pl.HC = hc;
   pl.n_hg = static_cast<int>(h_kv / hc);
   pl.nwc = hc * mt;
-  pl.threads = (pl.nwc + 1) * 32;
+  pl.threads = pl.nwc * 32;
   pl.ek = fp8 ? 1 : 2;
-  pl.tsk = hc * static_cast<int>(D) * pl.ek + 16;
-  pl.tsv = hc * static_cast<int>(D) * pl.ek + 16;
-  pl.stage_bytes = kStageTokens * (pl.tsk + pl.tsv);
-  const int scratch = fp8 ? pl.nwc * 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0;
+  // per warp: nst stages of 16 K rows + 16 V rows of one head, the index ring,
+  // the mask ring and (fp8) the bf16 widening scratch
+  pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
+  const int fixed = kIdxRing * 128 + 128 + (fp8 ? 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0);
   int k = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
   for (;;) {
     const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
-    const int nst = std::min(kMaxStages, (budget - kCtlBytes - scratch) / pl.stage_bytes);
+    const int cap = g_max_stages > 0 ? std::min(g_max_stages, kMaxStages) : kMaxStages;
+    const int nst = std::min(cap, ((budget - kCtlBytes) / pl.nwc - fixed) / pl.stage_bytes);
     if (nst >= 2) {
       pl.nst = nst;
       pl.ctas_per_sm = k;
@@ -899,9 +887,9 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
     if (k == 1) return fail("stage of %d bytes does not fit shared memory", pl.stage_bytes);
     k /= 2;
   }
+  pl.warp_bytes = ((pl.nst * pl.stage_bytes + fixed) + 127) & ~127;
   pl.ring_off = kCtlBytes;
-  pl.scratch_off = pl.ring_off + pl.nst * pl.stage_bytes;
-  pl.smem = static_cast<size_t>(pl.scratch_off + scratch);
+  pl.smem = static_cast<size_t>(pl.ring_off) + static_cast<size_t>(pl.nwc) * pl.warp_bytes;
   return true;
 }
 
@@ -923,9 +911,7 @@ WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
   return w;
 }
 
-// process-wide tuning overrides
-int g_num_ctas = 0;
-long long g_min_tokens = 0;
+
 
 struct DevWs {
   void* ptr = nullptr;
@@ -1153,6 +1139,11 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
   g_min_tokens = min_tokens_per_cta > 0 ? min_tokens_per_cta : 0;
 }
 
+void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta) {
+  g_max_stages = max_ring_stages >= 2 ? max_ring_stages : 0;
+  g_max_heads = max_kv_heads_per_cta > 0 ? max_kv_heads_per_cta : 0;
+}
+
 const char* vsk_last_error(void) { return g_err.c_str(); }
 
 const char* vsk_version(void) { return VSK_VERSION; }
@@ -1238,13 +1229,8 @@ int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tens
   p.n_hg = pl.n_hg;
   p.nwc = pl.nwc;
   p.nst = pl.nst;
-  p.tsk = pl.tsk;
-  p.tsv = pl.tsv;
-  p.stage_bytes = pl.stage_bytes;
   p.ring_off = pl.ring_off;
-  p.scratch_off = pl.scratch_off;
-  p.k_contig = (kb->stride[1] == D) ? 1 : 0;
-  p.v_contig = (vb->stride[1] == D) ? 1 : 0;
+  p.warp_bytes = pl.warp_bytes;
   const double sm = (sm_scale > 0.f && std::isfinite(sm_scale)) ? static_cast<double>(sm_scale)
                                                                  : 1.0 / std::sqrt(static_cast<double>(D));
   const double log2e = 1.4426950408889634;

@@ -16,7 +16,7 @@ rows ``l_ext`` per sequence with ``qo_indptr = arange(0, B*l_ext + 1, l_ext)``
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 
 import numpy as np
 import torch
