@@ -7,22 +7,22 @@
 // C ABI is declared in include/verify_splitkv.h.
 //
 // GB300 design (not the page's two-kernel Triton layout):
-//   * ONE persistent, warp-specialised kernel per call.  The flattened work
-//     space (sequence b, KV-head group hg, prefix token t) is cut into equal
-//     contiguous shares, one per CTA; grid = SMs x CTAs-per-SM from static
-//     shapes, the split itself is computed on the device from kv_indptr, so no
-//     host synchronisation is needed.
-//   * A producer warp gathers whole token rows (all HC KV heads of the group,
-//     e.g. 8 x 128 x 2 B = 2 KB at serving scale) with cp.async.bulk (TMA) into
-//     a padded shared-memory ring, completing on mbarriers; indices are
-//     prefetched several stages ahead with cp.async.
-//   * Consumer warps, one per (KV head, 16-row tile) of the packed query tile
-//     (all h_q/h_kv query heads x l_ext draft rows of one KV head), run
-//     bf16 mma.sync m16n8k16 for QK and PV with an fp32 online softmax, so each
-//     K/V byte is read from HBM once.
-//   * The last CTA to finish a segment (atomic ticket, no spin-wait) merges
-//     the other CTAs' partials by log-sum-exp and continues the same online
-//     softmax over the causal draft keys, then writes bf16 output.
+//   * ONE persistent kernel per call.  The flattened work space (sequence b,
+//     KV-head group hg, prefix token t) is cut into equal contiguous shares,
+//     one per CTA; grid = SMs x CTAs-per-SM from static shapes, the split
+//     itself is computed on the device from kv_indptr, so no host
+//     synchronisation is needed.
+//   * Warp (hc, mt) of a CTA owns one KV head of the group and one 16-row tile
+//     of its packed queries (all h_q/h_kv query heads x l_ext draft rows), so
+//     each K/V byte is read from HBM once.  It streams its head's K and V row
+//     slices itself with 16-byte cp.async into a private XOR-swizzled ring
+//     (indices prefetched by cp.async, completion by wait_group: no producer
+//     warp, no mbarrier, no spin-wait) and runs bf16 mma.sync m16n8k16 for QK
+//     and PV with an fp32 online softmax.
+//   * Piece ends only write log-sum-exp partials.  After streaming, the CTA
+//     that draws a segment's last ticket (atomic, no wait) merges the pieces
+//     in CTA order and continues the same online softmax over the causal
+//     draft keys, then writes bf16 output.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
