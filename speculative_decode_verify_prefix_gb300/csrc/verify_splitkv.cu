@@ -421,19 +421,27 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     const unsigned char* kbase = p.kb + head * p.kb_s1;
     const unsigned char* vbase = p.vb + head * p.vb_s1;
     const uint32_t slot = ring_s + static_cast<uint32_t>(job % nst) * STAGE_B;
+    // lane -> (token group, 16-byte chunk): LPT lanes cover one row, so each
+    // lane computes a token's K and V addresses once and issues both copies
+    constexpr int LPT = CPR < 32 ? CPR : 32;  // lanes per row
+    constexpr int TSTEP = 32 / LPT;          // tokens covered per pass of the warp
+    constexpr int CPL = CPR / LPT;           // chunks of a row per lane
+    const int cl = lane % LPT;
 #pragma unroll
-    for (int i = 0; i < CPR; ++i) {
-      const int c = lane + 32 * i;
-      const int row = c / CPR;  // 0..15 K rows, 16..31 V rows
-      const int t = row & 15;
-      const int cir = c % CPR;
+    for (int t = lane / LPT; t < kStageTokens; t += TSTEP) {
       const long long loc = __shfl_sync(0xffffffffu, myloc, t);
       const bool v = (mask >> t) & 1u;
       // an absent token is zero-filled (nothing read); q is a valid, never-empty address
-      const void* src = v ? static_cast<const void*>(((row >> 4) ? vbase + loc * p.vb_s0 : kbase + loc * p.kb_s0) + cir * 16)
-                          : static_cast<const void*>(p.q);
-      const int pc = FP8 ? cir : (cir ^ (t & 7));
-      cp_async_16_zfill(slot + static_cast<uint32_t>((row >> 4) * (16 * ROWB) + t * ROWB + pc * 16), src, v, pol);
+      const unsigned char* ks = v ? kbase + loc * p.kb_s0 : reinterpret_cast<const unsigned char*>(p.q);
+      const unsigned char* vs = v ? vbase + loc * p.vb_s0 : reinterpret_cast<const unsigned char*>(p.q);
+#pragma unroll
+      for (int cj = 0; cj < CPL; ++cj) {
+        const int cir = cl + LPT * cj;
+        const int pc = FP8 ? cir : (cir ^ (t & 7));
+        const uint32_t d = slot + static_cast<uint32_t>(t * ROWB + pc * 16);
+        cp_async_16_zfill(d, v ? ks + cir * 16 : ks, v, pol);
+        cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
+      }
     }
   };
 
@@ -550,17 +558,32 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       (void)kaddr1;
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys
-      float sc[2][4];
+      // two independent accumulator chains per n-tile (even / odd k-steps)
+      // halve the dependent mma latency; summed afterwards
+      float sc[2][4], sc2[2][4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+      for (int t = 0; t < 2; ++t) {
+        sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+        sc2[t][0] = sc2[t][1] = sc2[t][2] = sc2[t][3] = 0.f;
+      }
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         uint32_t b0, b1, b2, b3;
         const int lc = kk * 2 + k_chk;
         const uint32_t addr = FP8 ? kaddr0 + kk * 32 : kaddr0 + ((lc ^ (k_key & 7)) << 4);
         ldsm_x4(addr, b0, b1, b2, b3);
-        mma_bf16(sc[0], qf[kk], b0, b1);
-        mma_bf16(sc[1], qf[kk], b2, b3);
+        if (kk & 1) {
+          mma_bf16(sc2[0], qf[kk], b0, b1);
+          mma_bf16(sc2[1], qf[kk], b2, b3);
+        } else {
+          mma_bf16(sc[0], qf[kk], b0, b1);
+          mma_bf16(sc[1], qf[kk], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[t][e] += sc2[t][e];
       }
       // scale into the log2 domain; mask absent keys (tail / dropped) only
       // when the stage is not full (the mask is uniform across the warp)
