@@ -395,6 +395,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int c_self = blockIdx.x;
   const bool flagger = (warp == 0 && lane == 0);
 
+  int dslot = 0;  // ring slot of the next data job (job % nst, kept without a division)
   auto issue_idx = [&](const StageIt& it, long long job) {
     if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
       const long long n = it.s.kv0 + it.tok + lane;
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     const long long head = static_cast<long long>(it.s.hg) * p.HC + hc;
     const unsigned char* kbase = p.kb + head * p.kb_s1;
     const unsigned char* vbase = p.vb + head * p.vb_s1;
-    const uint32_t slot = ring_s + static_cast<uint32_t>(job % nst) * STAGE_B;
+    const uint32_t slot = ring_s + static_cast<uint32_t>(dslot) * STAGE_B;
     // lane -> (token group, 16-byte chunk): LPT lanes cover one row, so each
     // lane computes a token's K and V addresses once and issues both copies
     constexpr int LPT = CPR < 32 ? CPR : 32;  // lanes per row
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   auto step_data = [&]() {
     issue_data(di, job_d);
     ++job_d;
+    if (++dslot == nst) dslot = 0;
     if (di.valid) {
       di.tok += kStageTokens;
       sit_settle(p, di, end);
@@ -500,6 +502,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     if (seg_live(p, sn, end)) load_q<KS>(p, sn, hc, r0, r1, j, false, qn);
   }
   long long k = 0;
+  int kslot = 0;  // ring slot of stage k (k % nst, kept without a division)
 
 #pragma unroll 1
   while (seg_live(p, s, end)) {
@@ -512,14 +515,14 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 
     // ---------------- prefix: online softmax over this CTA's piece ----------------
 #pragma unroll 1
-    for (int tok = t0; tok < te; tok += kStageTokens, ++k) {
+    for (int tok = t0; tok < te; tok += kStageTokens, ++k, kslot = (kslot + 1 == nst) ? 0 : kslot + 1) {
       cp_async_wait_dyn(nst - 2);  // stage k has landed (this lane's copies)
       __syncwarp();                // ... and every other lane's
       step_data();                 // refill the slot stage k-1 used
       step_idx();
       cp_async_commit();
       const unsigned mask = mask_ring[k % 16];
-      unsigned char* slotp = ring + static_cast<int>(k % nst) * STAGE_B;
+      unsigned char* slotp = ring + kslot * STAGE_B;
       uint32_t kaddr0, kaddr1, vaddr0;
       int kstride;
       if constexpr (FP8) {
@@ -558,13 +561,17 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       (void)kaddr1;
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys
-      // two independent accumulator chains per n-tile (even / odd k-steps)
-      // halve the dependent mma latency; summed afterwards
-      float sc[2][4], sc2[2][4];
+      // four independent accumulator chains per n-tile (k-step mod 4) cut the
+      // dependent mma latency; summed afterwards
+      float sc[2][4];
+      float sx[3][2][4];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-        sc2[t][0] = sc2[t][1] = sc2[t][2] = sc2[t][3] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sc[t][e] = 0.f;
+          sx[0][t][e] = sx[1][t][e] = sx[2][t][e] = 0.f;
+        }
       }
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
@@ -572,18 +579,18 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         const int lc = kk * 2 + k_chk;
         const uint32_t addr = FP8 ? kaddr0 + kk * 32 : kaddr0 + ((lc ^ (k_key & 7)) << 4);
         ldsm_x4(addr, b0, b1, b2, b3);
-        if (kk & 1) {
-          mma_bf16(sc2[0], qf[kk], b0, b1);
-          mma_bf16(sc2[1], qf[kk], b2, b3);
-        } else {
+        if ((kk & 3) == 0) {
           mma_bf16(sc[0], qf[kk], b0, b1);
           mma_bf16(sc[1], qf[kk], b2, b3);
+        } else {
+          mma_bf16(sx[(kk & 3) - 1][0], qf[kk], b0, b1);
+          mma_bf16(sx[(kk & 3) - 1][1], qf[kk], b2, b3);
         }
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[t][e] += sc2[t][e];
+        for (int e = 0; e < 4; ++e) sc[t][e] += (sx[0][t][e] + sx[1][t][e]) + sx[2][t][e];
       }
       // scale into the log2 domain; mask absent keys (tail / dropped) only
       // when the stage is not full (the mask is uniform across the warp)
