@@ -55,6 +55,8 @@ class _Problem(ctypes.Structure):
         ("sm_scale", ctypes.c_double),
         ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double),
+        ("custom_mask", ctypes.c_void_p),
+        ("mask_indptr", ctypes.c_void_p),
     ]
 
 
@@ -140,7 +142,10 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
     ``k_pool``, ``v_pool`` (uint16 bf16 bits or uint8 e4m3 codes, [pool_tokens,
     h_kv, d|dv]); ``pool_dtype`` ("bf16" | "e4m3"); ``qo_indptr``,
     ``kv_indptr`` (int32 [B+1]); ``kv_indices`` (int32 or int64);
-    ``sm_scale``, ``k_scale``, ``v_scale`` (floats).
+    ``sm_scale``, ``k_scale``, ``v_scale`` (floats); optionally
+    ``custom_mask`` (uint8, flattened per-sequence [L, P+L] row-major draft
+    visibility, nonzero = visible) with ``mask_indptr`` (int64 [B+1]) for tree
+    verify; without them the drafts are causal.
 
     Returns ``{"o": float64 [n_rows, h_q, dv]}`` (NaN where not computed) and,
     with ``debug``, ``o_prefix``, ``lse_prefix``, ``o_draft``, ``lse_draft``.
@@ -177,6 +182,12 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
     P.sm_scale = float(prob["sm_scale"])
     P.k_scale = float(prob.get("k_scale", 1.0))
     P.v_scale = float(prob.get("v_scale", 1.0))
+    cm = prob.get("custom_mask")
+    mi = None
+    if cm is not None:
+        cm = np.ascontiguousarray(cm).view(np.uint8) if cm.dtype == np.bool_ else np.ascontiguousarray(cm, dtype=np.uint8)
+        mi = np.ascontiguousarray(prob["mask_indptr"], dtype=np.int64)
+        P.custom_mask, P.mask_indptr = (_ptr(cm) if cm.size else 0), _ptr(mi)
 
     b0, b1 = b_range if b_range is not None else (0, B)
     h0, h1 = h_range if h_range is not None else (0, h_q)
@@ -190,7 +201,7 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
             if k not in res:
                 res[k] = np.full(shp, np.nan, dtype=np.float64)
         dbg = [_ptr(res["o_prefix"]), _ptr(res["lse_prefix"]), _ptr(res["o_draft"]), _ptr(res["lse_draft"])]
-    keep = (q, ke, ve, kp, vp, qo, kvp, kvi)  # noqa: F841  (alive across the call)
+    keep = (q, ke, ve, kp, vp, qo, kvp, kvi, cm, mi)  # noqa: F841  (alive across the call)
     rc = lib.orc_verify_forward(ctypes.byref(P), b0, b1, h0, h1, _ptr(res["o"]), *dbg, int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected the requested ranges or head counts")

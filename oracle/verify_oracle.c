@@ -27,7 +27,18 @@
  *     prefix values only;
  *   - an fp8 pool is decoded exactly (e4m3 "fn" variant: bias 7, no infinity,
  *     S.1111.111 is NaN, largest finite 448); q is used unquantised;
- *   - L_b = qo_indptr[b+1] - qo_indptr[b] rows per sequence.
+ *   - L_b = qo_indptr[b+1] - qo_indptr[b] rows per sequence;
+ *   - tree verify (speculative topk > 1), when a custom mask is given: the
+ *     mask of sequence b is an L_b x (P_b + L_b) byte matrix stored row-major
+ *     from mask_indptr[b] (row i = draft query i, column j = prefix keys then
+ *     draft keys, nonzero = visible), the layout the "aiter_backend.py" page
+ *     builds for target verify (seq_mask_len = draft_num * (seq_len +
+ *     draft_num), mask_indptr = its running sum).  With the prefix part of
+ *     the mask skipped (skip_prefix_custom_mask, the verify default), every
+ *     prefix key stays visible and only the draft columns are read; draft key
+ *     t is visible to row i iff mask[mask_indptr[b] + i*(P_b+L_b) + P_b + t];
+ *   - a row that sees no key at all (empty prefix and no visible draft) has
+ *     output 0 and lse -inf.
  *
  * Debug outputs (optional) split the same sum into its prefix part and its
  * draft part: o_prefix / lse_prefix over the prefix keys only (lse = -inf and
@@ -69,6 +80,8 @@ typedef struct {
   const int32_t* kv_indptr;  /* [B+1] */
   const void* kv_indices;    /* int32 or int64, per idx_dtype */
   double sm_scale, k_scale, v_scale;
+  const uint8_t* custom_mask;   /* NULL: causal drafts (t <= i) */
+  const int64_t* mask_indptr;   /* [B+1], used with custom_mask  */
 } orc_problem;
 
 /* bf16 is the upper half of an IEEE-754 binary32: widen the bit pattern. */
@@ -113,6 +126,12 @@ static int64_t kv_index(const orc_problem* p, int64_t n) {
   return (int64_t)((const int32_t*)p->kv_indices)[n];
 }
 
+/* Is draft key t visible to draft row i of sequence b? */
+static int draft_visible(const orc_problem* p, int64_t b, int64_t i, int64_t t, int64_t P_b, int64_t L_b) {
+  if (!p->custom_mask) return t <= i;
+  return p->custom_mask[p->mask_indptr[b] + i * (P_b + L_b) + P_b + t] != 0;
+}
+
 /* One (sequence b, query head h): every draft row of b.  Scratch holds the
    decoded q row, the score row and a value accumulator.                     */
 static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
@@ -142,13 +161,13 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
       for (int64_t c = 0; c < D; ++c) dot += qrow[c] * pool_elem(p, p->k_pool, loc * p->kp_s0 + kvh * p->kp_s1 + c);
       score[j] = p->sm_scale * p->k_scale * dot;
     }
-    for (int64_t t = 0; t <= i; ++t) {
+    for (int64_t t = 0; t < L_b; ++t) {
       double dot = 0.0;
       for (int64_t c = 0; c < D; ++c)
         dot += qrow[c] * orc_bf16_to_f64(p->k_ext[(s_b + t) * p->ke_s0 + kvh * p->ke_s1 + c]);
-      score[P_b + t] = p->sm_scale * dot;
+      score[P_b + t] = draft_visible(p, b, i, t, P_b, L_b) ? p->sm_scale * dot : -INFINITY;
     }
-    const int64_t n_keys = P_b + i + 1;
+    const int64_t n_keys = P_b + L_b;
 
     /* full softmax over the whole row */
     double mx = -INFINITY;
@@ -156,7 +175,7 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
     double denom = 0.0;
     for (int64_t c = 0; c < DV; ++c) acc[c] = 0.0;
     for (int64_t j = 0; j < n_keys; ++j) {
-      const double w = exp(score[j] - mx);
+      const double w = (score[j] == -INFINITY) ? 0.0 : exp(score[j] - mx);
       denom += w;
       if (j < P_b) {
         const int64_t loc = kv_index(p, p_b + j);
@@ -169,7 +188,7 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
       }
     }
     double* o = out + (row * p->h_q + h) * DV;
-    for (int64_t c = 0; c < DV; ++c) o[c] = acc[c] / denom;
+    for (int64_t c = 0; c < DV; ++c) o[c] = (mx == -INFINITY) ? 0.0 : acc[c] / denom;
 
     if (o_prefix) {
       /* prefix keys alone */
@@ -195,17 +214,18 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
       /* causal drafts alone */
       double* od = o_draft + (row * p->h_q + h) * DV;
       double dm = -INFINITY;
-      for (int64_t t = 0; t <= i; ++t) if (score[P_b + t] > dm) dm = score[P_b + t];
+      for (int64_t t = 0; t < L_b; ++t) if (score[P_b + t] > dm) dm = score[P_b + t];
       double dd = 0.0;
       for (int64_t c = 0; c < DV; ++c) acc2[c] = 0.0;
-      for (int64_t t = 0; t <= i; ++t) {
+      for (int64_t t = 0; t < L_b; ++t) {
+        if (score[P_b + t] == -INFINITY) continue;
         const double w = exp(score[P_b + t] - dm);
         dd += w;
         for (int64_t c = 0; c < DV; ++c)
           acc2[c] += w * orc_bf16_to_f64(p->v_ext[(s_b + t) * p->ve_s0 + kvh * p->ve_s1 + c]);
       }
-      for (int64_t c = 0; c < DV; ++c) od[c] = acc2[c] / dd;
-      lse_draft[row * p->h_q + h] = dm + log(dd);
+      for (int64_t c = 0; c < DV; ++c) od[c] = (dm == -INFINITY) ? 0.0 : acc2[c] / dd;
+      lse_draft[row * p->h_q + h] = (dm == -INFINITY) ? -INFINITY : dm + log(dd);
     }
   }
   free(qrow);

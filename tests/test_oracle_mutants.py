@@ -17,12 +17,14 @@ from test_oracle_pins import _golden_cases, _sdpa_reference, run_golden
 SRC = os.path.join(os.path.dirname(oracle.__file__), "verify_oracle.c")
 
 MUTANTS = {
-    "drop_own_draft_key": ("const int64_t n_keys = P_b + i + 1;", "const int64_t n_keys = P_b + i;"),
-    "k_scale_on_drafts": ("score[P_b + t] = p->sm_scale * dot;", "score[P_b + t] = p->sm_scale * p->k_scale * dot;"),
+    "drop_own_draft_key": ("if (!p->custom_mask) return t <= i;", "if (!p->custom_mask) return t < i;"),
+    "k_scale_on_drafts": ("? p->sm_scale * dot : -INFINITY", "? p->sm_scale * p->k_scale * dot : -INFINITY"),
+    "tree_mask_transposed": ("p->mask_indptr[b] + i * (P_b + L_b) + P_b + t]", "p->mask_indptr[b] + t * (P_b + L_b) + P_b + i]"),
+    "tree_mask_prefix_offset": ("i * (P_b + L_b) + P_b + t]", "i * (P_b + L_b) + t]"),
     "v_scale_dropped": ("acc[c] += w * p->v_scale * pool_elem(p, p->v_pool", "acc[c] += w * pool_elem(p, p->v_pool"),
     "gqa_modulo": ("const int64_t kvh = h / group;", "const int64_t kvh = h % p->h_kv;"),
     "no_indirection": ("const int64_t loc = kv_index(p, p_b + j);", "const int64_t loc = p_b + j;"),
-    "softmax_sign": ("const double w = exp(score[j] - mx);", "const double w = exp(mx - score[j]);"),
+    "softmax_sign": ("exp(score[j] - mx)", "exp(mx - score[j])"),
     "pool_strides_transposed": ("loc * p->kp_s0 + kvh * p->kp_s1", "loc * p->kp_s1 + kvh * p->kp_s0"),
     "draft_value_row": ("p->v_ext[(s_b + t) * p->ve_s0", "p->v_ext[(s_b + i) * p->ve_s0"),
 }

@@ -89,6 +89,8 @@ def _golden_arrays(fx, pool_dtype):
         "kv_indptr": np.array(fx["kv_indptr"], dtype=np.int32),
         "kv_indices": np.array(fx["kv_indices"], dtype=np.int64),
         "sm_scale": _parse_value(fx["sm_scale"]), "k_scale": fx["k_scale"], "v_scale": fx["v_scale"],
+        **({"custom_mask": np.array(fx["custom_mask"], dtype=np.uint8),
+            "mask_indptr": np.array(fx["mask_indptr"], dtype=np.int64)} if "custom_mask" in fx else {}),
     }
 
 
@@ -122,7 +124,7 @@ def test_golden(fn, pool_dtype):
 
 def test_golden_fixtures_present():
     names = {f for f in os.listdir(GOLDEN) if f.endswith(".json")}
-    assert {"scales_causal.json", "gqa_mapping.json", "indptr_empty_prefix.json"} <= names
+    assert {"scales_causal.json", "gqa_mapping.json", "indptr_empty_prefix.json", "tree_mask.json"} <= names
 
 
 # ---------------------------------------------------------------- library cross-check
@@ -144,7 +146,12 @@ def _sdpa_reference(prob):
         kcat = torch.cat([prob["k_scale"] * kb[loc], ke[s:e]], 0)       # [P+L, h_kv, d]
         vcat = torch.cat([prob["v_scale"] * vb[loc], ve[s:e]], 0)
         mask = torch.ones(L, P + L, dtype=torch.bool)
-        mask[:, P:] = torch.tril(torch.ones(L, L, dtype=torch.bool))
+        if prob.get("custom_mask") is not None:
+            mi = prob["mask_indptr"]
+            m = prob["custom_mask"][int(mi[b]):int(mi[b + 1])].view(L, P + L).bool()
+            mask[:, P:] = m[:, P:]  # prefix columns are not applied
+        else:
+            mask[:, P:] = torch.tril(torch.ones(L, L, dtype=torch.bool))
         qh = q[s:e].transpose(0, 1)                                     # [h_q, L, d]
         kh = kcat.transpose(0, 1).repeat_interleave(g, 0)               # [h_q, P+L, d]
         vh = vcat.transpose(0, 1).repeat_interleave(g, 0)
@@ -161,6 +168,9 @@ SDPA_CASES = [
     workloads.Spec("l1_decode", (50, 17), 1, 8, 8, 64, 64, seed=9, idx_dtype="int32"),
     workloads.Spec("d_ne_dv", (33, 20), 2, 4, 2, 64, 128, seed=10),
     workloads.Spec("long_chain", (16,), 8, 4, 1, 64, 64, seed=11),
+    workloads.Spec("tree_random", (0, 23, 40), 6, 8, 2, 64, 64, perm=True, tree="random", seed=12),
+    workloads.Spec("tree_star_fp8", (30, 9), 5, 4, 2, 64, 64, pool="e4m3", tree="star", k_scale=0.5, v_scale=2.0,
+                   seed=13),
 ]
 
 
@@ -327,3 +337,34 @@ def test_thread_count_does_not_change_results():
     a = oracle.verify_forward(workloads.to_oracle_arrays(prob), nthreads=1)["o"]
     b = oracle.verify_forward(workloads.to_oracle_arrays(prob), nthreads=4)["o"]
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- tree verify (custom mask)
+def test_chain_tree_mask_equals_causal():
+    spec = workloads.Spec("chain", (0, 31, 64), 6, 8, 2, 64, 64, perm=True, seed=41)
+    causal = _run(workloads.make_problem(spec, "cpu"))["o"]
+    chain = _run(workloads.make_problem(spec, "cpu", tree="chain"))["o"]
+    assert np.array_equal(causal, chain)
+
+
+def test_tree_mask_prefix_columns_are_not_applied():
+    spec = workloads.Spec("prefcols", (17, 40), 5, 4, 1, 64, 64, perm=True, tree="random", seed=42)
+    prob = workloads.make_problem(spec, "cpu")
+    a = _run(prob)["o"]
+    cm = prob["custom_mask"].clone()
+    mi = prob["mask_indptr"]
+    for b, P in enumerate(prob["prefix_lens"]):
+        m = cm[int(mi[b]):int(mi[b + 1])].view(5, P + 5)
+        m[:, :P] = 0
+    b_ = _run(dict(prob, custom_mask=cm))["o"]
+    assert np.array_equal(a, b_)
+
+
+def test_tree_mask_row_with_nothing_visible_is_zero():
+    spec = workloads.Spec("empty_row", (0,), 3, 2, 1, 64, 64, tree="chain", seed=43)
+    prob = workloads.make_problem(spec, "cpu")
+    cm = prob["custom_mask"].clone()
+    cm[3:6] = 0  # row 1 sees nothing (no prefix, no draft)
+    r = _run(dict(prob, custom_mask=cm), debug=True)
+    assert np.array_equal(r["o"][1], np.zeros_like(r["o"][1]))
+    assert np.isfinite(r["o"]).all() and np.isneginf(r["lse_draft"][1]).all()

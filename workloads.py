@@ -40,6 +40,7 @@ class Spec:
     idx_dtype: str = "int64"
     pool_extra: int = 0         # unreferenced pool slots beyond sum(prefix_lens)
     poison: bool = False        # fill unreferenced pool slots with NaN
+    tree: str = ""              # "" causal drafts; "chain" | "star" | "random": tree-verify mask
     seed: int = 0
 
     @property
@@ -115,7 +116,11 @@ def make_problem(spec: Spec, device="cpu", **overrides) -> dict:
     qo_indptr = torch.arange(0, n_ext + 1, spec.l_ext, dtype=torch.int32)
     if spec.idx_dtype == "int32":
         kv_indices = kv_indices.to(torch.int32)
-    return {
+    extra = {}
+    if spec.tree:
+        cm, mi = tree_mask([int(x) for x in lens.tolist()], spec.l_ext, spec.tree, spec.seed + 7, device)
+        extra = {"custom_mask": cm, "mask_indptr": mi}
+    return {**extra,
         "spec": spec,
         "q": q, "k_ext": k_ext, "v_ext": v_ext,
         "k_buffer": k_buffer, "v_buffer": v_buffer,
@@ -126,6 +131,39 @@ def make_problem(spec: Spec, device="cpu", **overrides) -> dict:
         "prefix_lens": [int(x) for x in lens.tolist()],
         "pool_dtype": spec.pool,
     }
+
+
+def tree_parents(kind: str, L: int, gen: torch.Generator) -> list:
+    """Parent of each draft node of a speculation tree (node 0 is the root):
+    a chain (i -> i-1), a star (every node under the root) or a random tree."""
+    if kind == "chain":
+        return [-1] + list(range(L - 1))
+    if kind == "star":
+        return [-1] + [0] * (L - 1)
+    return [-1] + [int(torch.randint(0, i, (1,), generator=gen)) for i in range(1, L)]
+
+
+def tree_mask(prefix_lens, L: int, kind: str, seed: int, device="cpu"):
+    """Target-verify mask of speculation trees, in the layout the
+    "aiter_backend.py" page builds: per sequence an L x (P_b + L) uint8 matrix,
+    row-major, prefix columns all visible, draft column t visible to row i iff
+    t is i or an ancestor of i; ``mask_indptr`` (int64) holds the running
+    offsets."""
+    gen = torch.Generator().manual_seed(seed)
+    parts, offs = [], [0]
+    for P in prefix_lens:
+        par = tree_parents(kind, L, gen)
+        m = torch.zeros(L, P + L, dtype=torch.uint8)
+        m[:, :P] = 1
+        for i in range(L):
+            a = i
+            while a >= 0:
+                m[i, P + a] = 1
+                a = par[a]
+        parts.append(m.flatten())
+        offs.append(offs[-1] + m.numel())
+    cm = torch.cat(parts) if parts else torch.zeros(0, dtype=torch.uint8)
+    return cm.to(device), torch.tensor(offs, dtype=torch.int64, device=device)
 
 
 def _bits(t: torch.Tensor) -> np.ndarray:
@@ -148,6 +186,8 @@ def to_oracle_arrays(prob: dict) -> dict:
         "kv_indptr": prob["kv_indptr"].cpu().numpy(),
         "kv_indices": prob["kv_indices"].cpu().numpy(),
         "sm_scale": prob["sm_scale"], "k_scale": prob["k_scale"], "v_scale": prob["v_scale"],
+        **({"custom_mask": prob["custom_mask"].cpu().numpy(), "mask_indptr": prob["mask_indptr"].cpu().numpy()}
+           if prob.get("custom_mask") is not None else {}),
     }
 
 
