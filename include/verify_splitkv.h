@@ -39,7 +39,8 @@ enum {
   VSK_DTYPE_BF16 = 0,     /* bfloat16                                   */
   VSK_DTYPE_FP8E4M3 = 1,  /* float8 e4m3 "fn" (no infinities)           */
   VSK_DTYPE_I32 = 2,      /* int32                                      */
-  VSK_DTYPE_I64 = 3       /* int64                                      */
+  VSK_DTYPE_I64 = 3,      /* int64                                      */
+  VSK_DTYPE_U8 = 4        /* uint8 (also used for bool masks)           */
 };
 
 /* A strided view of device memory.  Strides and shape are in ELEMENTS.  For
@@ -115,6 +116,30 @@ int verify_splitkv_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
                        float sm_scale, void* workspace, size_t workspace_bytes,
                        void* stream);
 
+/* Tree verify (speculative topk > 1): verify_splitkv_fwd with the draft
+ * block under a custom mask instead of the causal rule (the case the
+ * "verify_splitkv.py" page leaves to its fallback).  The mask layout is the
+ * target-verify one of the "aiter_backend.py" page: for sequence b an
+ * l_ext x (P_b + l_ext) uint8 matrix, row-major from custom_mask[mask_indptr[b]]
+ * (row i = draft query i; columns = the P_b prefix keys, then the l_ext draft
+ * keys; nonzero = visible).  Only the draft columns are read: every prefix
+ * key stays visible (skip_prefix_custom_mask = True, the verify default).
+ * A row with no visible key at all (empty prefix, no visible draft) gets 0.
+ *   custom_mask  [n] uint8 (bool bytes accepted), device memory
+ *   mask_indptr  [B+1] int32 or int64, device memory
+ * Everything else, the return value and the workspace rules are those of
+ * verify_splitkv_fwd (is_causal is implied).  mask_indptr entries whose rows
+ * would fall outside custom_mask are not dereferenced: that sequence's
+ * drafts fall back to the causal rule and error bit 16 is set. */
+int verify_splitkv_tree_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
+                            const vsk_tensor* v_extend, const vsk_tensor* o_extend,
+                            const vsk_tensor* k_buffer, const vsk_tensor* v_buffer,
+                            const vsk_tensor* qo_indptr, const vsk_tensor* kv_indptr,
+                            const vsk_tensor* kv_indices, const vsk_tensor* custom_mask,
+                            const vsk_tensor* mask_indptr, int64_t max_len_extend,
+                            float k_scale, float v_scale, float sm_scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* Upper bound, in bytes, of the workspace verify_splitkv_fwd needs for any
  * batch of up to max_bs sequences with these head counts and sizes on the
  * CURRENT CUDA device (its SM count sets the number of persistent CTAs).
@@ -137,7 +162,8 @@ int vsk_workspace_init(void* workspace, size_t bytes, void* stream);
  * clears it.  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
  * not non-decreasing or beyond kv_indices; 4 = qo_indptr inconsistent with
  * l_ext; 8 = reserved for a timed-out wait inside the kernel (this build's
- * kernel has no waits that can time out and never sets it).  Returns 1 on success, 0 on a CUDA error.
+ * kernel has no waits that can time out and never sets it); 16 = a
+ * mask_indptr entry of verify_splitkv_tree_fwd outside custom_mask.  Returns 1 on success, 0 on a CUDA error.
  * Intended for tests and debugging: it blocks the host. */
 int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
 

@@ -54,7 +54,7 @@ class VskTensor(ctypes.Structure):
     ]
 
 
-DTYPE_BF16, DTYPE_FP8E4M3, DTYPE_I32, DTYPE_I64 = 0, 1, 2, 3
+DTYPE_BF16, DTYPE_FP8E4M3, DTYPE_I32, DTYPE_I64, DTYPE_U8 = 0, 1, 2, 3, 4
 
 _lib = None
 _lock = threading.Lock()
@@ -69,6 +69,9 @@ def _bind(lib):
     lib.verify_splitkv_fwd.restype = ctypes.c_int
     lib.verify_splitkv_fwd.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                                                   ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.verify_splitkv_tree_fwd.restype = ctypes.c_int
+    lib.verify_splitkv_tree_fwd.argtypes = [_P] * 11 + [ctypes.c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     lib.vsk_workspace_size.restype = ctypes.c_size_t
     lib.vsk_workspace_size.argtypes = [ctypes.c_int64] * 6
     lib.vsk_workspace_size_for_sms.restype = ctypes.c_size_t

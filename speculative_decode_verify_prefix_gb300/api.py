@@ -24,6 +24,8 @@ _DT = {
     torch.float8_e4m3fn: _native.DTYPE_FP8E4M3,
     torch.int32: _native.DTYPE_I32,
     torch.int64: _native.DTYPE_I64,
+    torch.uint8: _native.DTYPE_U8,
+    torch.bool: _native.DTYPE_U8,
 }
 
 
@@ -102,14 +104,22 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
                        sinks=None, window_kv_offsets=None, xai_temperature_len=-1, max_bs=None,
                        workspace=None, stream=None) -> bool:
     """Drop-in for the prefill/extend attention call on the EAGLE target-verify
-    (topk = 1) shape.  Returns True once the kernel is enqueued on the current
-    stream (o_extend will hold the result), False if the case is unsupported
-    (nothing was launched; the caller falls back)."""
+    shape.  Returns True once the kernel is enqueued on the current stream
+    (o_extend will hold the result), False if the case is unsupported
+    (nothing was launched; the caller falls back).
+
+    Without ``custom_mask`` the drafts are causal (topk = 1).  With
+    ``custom_mask`` / ``mask_indptr`` (the target-verify layout: per sequence
+    an l_ext x (prefix + l_ext) uint8 matrix) the draft block follows the
+    mask, which serves tree verify (topk > 1); the prefix part of the mask is
+    not applied, so ``skip_prefix_custom_mask`` must be True."""
     if not can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
                       custom_mask, is_causal, mask_indptr, max_len_extend,
                       sliding_window_size=sliding_window_size, sinks=sinks, logit_cap=logit_cap,
                       xai_temperature_len=xai_temperature_len):
         return False
+    if custom_mask is not None and (not skip_prefix_custom_mask or mask_indptr is None):
+        return False  # the prefix part of a tree mask is not applied by this kernel
     bs = qo_indptr.shape[0] - 1
     mle = int(max_len_extend)
     if workspace is None:
@@ -119,6 +129,16 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
     if stream is None:
         stream = torch.cuda.current_stream(q_extend.device)
     sm = 0.0 if sm_scale is None else float(sm_scale)
+    if custom_mask is not None:
+        cm = custom_mask if custom_mask.dtype == torch.uint8 else custom_mask.view(torch.uint8)
+        ok = _native.lib().verify_splitkv_tree_fwd(
+            _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
+            _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), _ref(cm.reshape(-1)), _ref(mask_indptr), mle,
+            _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+            ctypes.c_void_p(stream.cuda_stream))
+        if not ok:
+            raise RuntimeError("verify_splitkv_tree_fwd failed after the gate passed: " + _native.last_error())
+        return True
     ok = _native.lib().verify_splitkv_fwd(
         _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
         _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), int(bool(is_causal)), mle,

@@ -62,6 +62,7 @@ enum : unsigned {
   kErrBadKvIndptr = 2u,
   kErrBadQoIndptr = 4u,
   kErrTimeout = 8u,
+  kErrBadMaskIndptr = 16u,
 };
 
 struct Params {
@@ -80,6 +81,10 @@ struct Params {
   int ring_off, warp_bytes;
   float scale2, dscale2, v_scale;
   long long w_min;
+  const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
+  const void* mindptr;
+  int mindptr64;
+  long long n_mask;
   unsigned* err;
   int* cnt;
   float* plse;
@@ -762,6 +767,24 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       const int s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
+      // tree verify: this sequence's mask rows (row-major [L][P+L], only the
+      // draft columns are read); inconsistent offsets fall back to causal
+      long long mbase = -1;
+      if (p.cmask) {
+        const long long m0 = p.mindptr64 ? static_cast<const long long*>(p.mindptr)[sg.b]
+                                         : static_cast<long long>(static_cast<const int*>(p.mindptr)[sg.b]);
+        const long long span = static_cast<long long>(p.L) * (sg.P + p.L);
+        if (m0 >= 0 && m0 + span <= p.n_mask) {
+          mbase = m0;
+        } else if (flagger) {
+          atomicOr(p.err, kErrBadMaskIndptr);
+        }
+      }
+      auto visible = [&](int key, int irow) -> bool {
+        if (key >= p.L || irow >= p.L) return false;
+        if (mbase < 0) return key <= irow;
+        return __ldg(p.cmask + mbase + static_cast<long long>(irow) * (sg.P + p.L) + sg.P + key) != 0;
+      };
 #pragma unroll 1
       for (int td = 0; td * 8 < p.L; ++td) {
         float sd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -779,7 +802,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         for (int e = 0; e < 4; ++e) {
           const int key = td * 8 + 2 * j + (e & 1);
           const int irow = (e < 2) ? i0 : i1;
-          sd[e] = (key < p.L && key <= irow) ? sd[e] * p.dscale2 : NEG_INF;
+          sd[e] = visible(key, irow) ? sd[e] * p.dscale2 : NEG_INF;
         }
         const float mx0 = quad_max(fmaxf(sd[0], sd[1]));
         const float mx1 = quad_max(fmaxf(sd[2], sd[3]));
@@ -826,7 +849,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         }
       }
       // ------------------------------ output ------------------------------
-      const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+      // a row with nothing visible (empty prefix, no visible draft) is 0
+      const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
       if (r0 < p.R) {
         __nv_bfloat16* op = p.o + (static_cast<long long>(s_b) + r0 / p.gq) * p.o_s0 +
                             static_cast<long long>(kvh * p.gq + r0 % p.gq) * p.o_s1 + 2 * j;
@@ -1178,11 +1202,15 @@ const char* vsk_last_error(void) { return g_err.c_str(); }
 
 const char* vsk_version(void) { return VSK_VERSION; }
 
-int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
-                       const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
-                       const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
-                       float sm_scale, void* workspace, size_t workspace_bytes, void* stream) {
-  g_err.clear();
+}  // extern "C"
+
+namespace vsk {
+// Shared body of the entry points; cm / mi select tree verify (both null: causal drafts).
+static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                      const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                      const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                      float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
+                      const vsk_tensor* mi) {
   if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
   if (!check_3d(o, "o_extend")) return 0;
   if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
@@ -1268,6 +1296,11 @@ int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tens
   p.dscale2 = static_cast<float>(sm * log2e);
   p.v_scale = v_scale;
   p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
+  p.cmask = cm ? static_cast<const unsigned char*>(cm->data) : nullptr;
+  p.mindptr = mi ? mi->data : nullptr;
+  p.mindptr64 = (mi && mi->dtype == VSK_DTYPE_I64) ? 1 : 0;
+  p.n_mask = cm ? cm->shape[0] : 0;
+  if (p.cmask == nullptr) p.mindptr = nullptr;
   p.err = reinterpret_cast<unsigned*>(ws);
   p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
   p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
@@ -1278,6 +1311,33 @@ int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tens
                        pl.smem, st);
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
   return 1;
+}
+}  // namespace vsk
+
+extern "C" {
+
+int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                       const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                       const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                       float sm_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  return run_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale, sm_scale,
+                    workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int verify_splitkv_tree_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                            const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                            const vsk_tensor* kvi, const vsk_tensor* custom_mask, const vsk_tensor* mask_indptr,
+                            int64_t max_len_extend, float k_scale, float v_scale, float sm_scale, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (!check_1d(custom_mask, "custom_mask") || !check_1d(mask_indptr, "mask_indptr")) return 0;
+  if (custom_mask->dtype != VSK_DTYPE_U8) return fail("custom_mask must be uint8 (or bool)");
+  if (mask_indptr->dtype != VSK_DTYPE_I32 && mask_indptr->dtype != VSK_DTYPE_I64)
+    return fail("mask_indptr must be int32 or int64");
+  if (!qo || mask_indptr->shape[0] != qo->shape[0]) return fail("mask_indptr must have B+1 entries");
+  return run_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, 1, max_len_extend, k_scale, v_scale, sm_scale, workspace,
+                    workspace_bytes, stream, custom_mask, mask_indptr);
 }
 
 }  // extern "C"

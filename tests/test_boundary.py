@@ -156,3 +156,26 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_string():
     assert vsk.version().startswith("verify_splitkv-gb300")
+
+
+def test_tree_entry_rejects_bad_mask_arguments():
+    lib = _native.lib()
+    q, ke, ve, kb, vb, qo, kvp, kvi, cm, causal, mi, mle = _inputs()
+    o = torch.empty(q.shape[0], 16, 256, dtype=torch.bfloat16)
+    r = vsk.api._ref
+    good_mask = torch.ones(2 * 4 * (512 + 4), dtype=torch.uint8)
+    good_ind = torch.tensor([0, 4 * 516, 8 * 516], dtype=torch.int64)
+    for mask, ind, msg in ((good_mask.float(), good_ind, "uint8"), (good_mask, good_ind.float(), "int32 or int64"),
+                           (good_mask, good_ind[:2], "B+1")):
+        ok = lib.verify_splitkv_tree_fwd(r(q), r(ke), r(ve), r(o), r(kb), r(vb), r(qo), r(kvp), r(kvi), r(mask),
+                                         r(ind), mle, 1.0, 1.0, 0.0, None, 0, None)
+        assert ok == 0 and msg in vsk.last_error()
+
+
+def test_python_tree_path_needs_skip_prefix():
+    a = _inputs()
+    o = torch.empty(a[0].shape[0], 16, 256, dtype=torch.bfloat16)
+    mask = torch.ones(2 * 4 * 516, dtype=torch.uint8)
+    ind = torch.tensor([0, 4 * 516, 8 * 516], dtype=torch.int64)
+    assert vsk.verify_splitkv_fwd(a[0], a[1], a[2], o, a[3], a[4], a[5], a[6], a[7], mask, True, ind, a[11], 1.0, 1.0,
+                                  skip_prefix_custom_mask=False) is False

@@ -31,8 +31,10 @@ def run_gpu(vsk, prob, o=None, **kw):
     if o is None:
         o = torch.full((q.shape[0], q.shape[1], prob["v_ext"].shape[2]), float("nan"), dtype=torch.bfloat16,
                        device=q.device)
+    cm = kw.pop("custom_mask", None)
+    mi = kw.pop("mask_indptr", None)
     ran = vsk.verify_splitkv_fwd(q, prob["k_ext"], prob["v_ext"], o, prob["k_buffer"], prob["v_buffer"],
-                                 prob["qo_indptr"], prob["kv_indptr"], prob["kv_indices"], None, True, None,
+                                 prob["qo_indptr"], prob["kv_indptr"], prob["kv_indices"], cm, True, mi,
                                  prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
                                  sm_scale=prob["sm_scale"], **kw)
     assert ran, vsk.last_error()
@@ -265,3 +267,69 @@ def test_cuda_graph_replay_matches_eager(vsk):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), eager.view(torch.int16))
+
+
+# ----------------------------------------------------------------- tree verify (custom mask)
+TREES = [
+    workloads.Spec("tree_rand_l8", (0, 17, 300, 1024), 8, 16, 2, 128, 128, perm=True, tree="random", seed=201),
+    workloads.Spec("tree_star_l4", (2000, 33), 4, 32, 8, 128, 128, perm=True, tree="star", seed=202),
+    workloads.Spec("tree_rand_d256_fp8", (700, 90), 6, 16, 2, 256, 256, pool="e4m3", perm=True, tree="random",
+                   k_scale=0.5, v_scale=0.25, seed=203),
+    workloads.Spec("tree_rand_d64_l16", (129, 64), 16, 8, 1, 64, 64, perm=True, tree="random", seed=204),
+]
+
+
+def run_tree(vsk, prob, o=None, **kw):
+    return run_gpu(vsk, prob, o=o, custom_mask=prob["custom_mask"], mask_indptr=prob["mask_indptr"], **kw)
+
+
+@pytest.mark.parametrize("spec", TREES, ids=lambda s: s.name)
+def test_tree_verify_matches_oracle(vsk, spec):
+    p = gpu_problem(spec)
+    check(run_tree(vsk, p), oracle_o(p))
+    assert vsk.read_error_flags() == 0
+
+
+def test_chain_tree_is_bitwise_the_causal_path(vsk):
+    spec = workloads.Spec("chain", (500, 0, 1200), 4, 32, 8, 128, 128, perm=True, tree="chain", seed=205)
+    p = gpu_problem(spec)
+    a = run_gpu(vsk, p)
+    b = run_tree(vsk, p)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_tree_prefix_columns_and_indptr_dtype(vsk):
+    spec = workloads.Spec("cols", (77, 300), 5, 8, 2, 128, 128, perm=True, tree="random", seed=206)
+    p = gpu_problem(spec)
+    a = run_tree(vsk, p)
+    cm = p["custom_mask"].clone()
+    mi = p["mask_indptr"].cpu()
+    for b, P in enumerate(p["prefix_lens"]):
+        cm[int(mi[b]):int(mi[b + 1])].view(5, P + 5)[:, :P] = 0
+    b_ = run_gpu(vsk, p, custom_mask=cm.bool(), mask_indptr=p["mask_indptr"].to(torch.int32))
+    assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
+
+
+def test_tree_row_with_nothing_visible_is_zero(vsk):
+    spec = workloads.Spec("emptyrow", (0, 40), 3, 4, 1, 64, 64, tree="chain", seed=207)
+    p = gpu_problem(spec)
+    cm = p["custom_mask"].clone()
+    cm[3:6] = 0  # sequence 0, draft row 1: no prefix and no visible draft
+    p2 = dict(p, custom_mask=cm)
+    o = run_tree(vsk, p2)
+    ref = oracle_o(p2)
+    check(o, ref)
+    assert (o[1].float() == 0).all()
+
+
+def test_tree_bad_mask_indptr_is_flagged_not_read(vsk):
+    spec = workloads.Spec("badmask", (50, 60), 4, 8, 2, 128, 128, tree="random", seed=208)
+    p = gpu_problem(spec)
+    mi = p["mask_indptr"].clone()
+    mi[1] = p["custom_mask"].numel()  # sequence 1's rows would start past the end
+    vsk.read_error_flags()
+    o = run_gpu(vsk, p, custom_mask=p["custom_mask"], mask_indptr=mi)
+    assert vsk.read_error_flags() & 16
+    causal = oracle_o({k: v for k, v in p.items() if k not in ("custom_mask", "mask_indptr")})
+    check(o, causal, rows=slice(4, 8))              # sequence 1 fell back to causal drafts
+    check(o, oracle_o(p), rows=slice(0, 4))         # sequence 0 kept its tree
