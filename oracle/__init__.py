@@ -57,6 +57,11 @@ class _Problem(ctypes.Structure):
         ("v_scale", ctypes.c_double),
         ("custom_mask", ctypes.c_void_p),
         ("mask_indptr", ctypes.c_void_p),
+        ("paged", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p),
+        ("bt_s0", ctypes.c_int64),
+        ("page_size", ctypes.c_int64),
+        ("seq_lens", ctypes.c_void_p),
     ]
 
 
@@ -145,7 +150,11 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
     ``sm_scale``, ``k_scale``, ``v_scale`` (floats); optionally
     ``custom_mask`` (uint8, flattened per-sequence [L, P+L] row-major draft
     visibility, nonzero = visible) with ``mask_indptr`` (int64 [B+1]) for tree
-    verify; without them the drafts are causal.
+    verify; without them the drafts are causal.  A paged problem (drafts
+    already in the cache) instead gives ``block_table`` (int32 [B, max_blocks]),
+    ``page_size`` and ``seq_lens`` (int32 [B], cached tokens before the
+    drafts); its ``kv_indptr`` / ``kv_indices`` / ``k_ext`` / ``v_ext`` are
+    not read (``k_ext`` / ``v_ext`` may be empty [n_rows, h_kv, d] arrays).
 
     Returns ``{"o": float64 [n_rows, h_q, dv]}`` (NaN where not computed) and,
     with ``debug``, ``o_prefix``, ``lse_prefix``, ``o_draft``, ``lse_draft``.
@@ -154,8 +163,8 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
     q, ke, ve = prob["q"], prob["k_ext"], prob["v_ext"]
     kp, vp = prob["k_pool"], prob["v_pool"]
     qo = np.ascontiguousarray(prob["qo_indptr"], dtype=np.int32)
-    kvp = np.ascontiguousarray(prob["kv_indptr"], dtype=np.int32)
-    kvi = np.ascontiguousarray(prob["kv_indices"])
+    kvp = np.ascontiguousarray(prob.get("kv_indptr", np.zeros(1, dtype=np.int32)), dtype=np.int32)
+    kvi = np.ascontiguousarray(prob.get("kv_indices", np.zeros(0, dtype=np.int64)))
     if kvi.dtype not in (np.int32, np.int64):
         raise TypeError("kv_indices must be int32 or int64")
     for name, a in (("q", q), ("k_ext", ke), ("v_ext", ve)):
@@ -201,7 +210,12 @@ def verify_forward(prob: dict, b_range=None, h_range=None, debug: bool = False,
             if k not in res:
                 res[k] = np.full(shp, np.nan, dtype=np.float64)
         dbg = [_ptr(res["o_prefix"]), _ptr(res["lse_prefix"]), _ptr(res["o_draft"]), _ptr(res["lse_draft"])]
-    keep = (q, ke, ve, kp, vp, qo, kvp, kvi, cm, mi)  # noqa: F841  (alive across the call)
+    bt = sl = None
+    if prob.get("block_table") is not None:
+        bt = np.ascontiguousarray(prob["block_table"], dtype=np.int32)
+        sl = np.ascontiguousarray(prob["seq_lens"], dtype=np.int32)
+        P.paged, P.block_table, P.bt_s0, P.page_size, P.seq_lens = 1, _ptr(bt), bt.shape[1], int(prob["page_size"]), _ptr(sl)
+    keep = (q, ke, ve, kp, vp, qo, kvp, kvi, cm, mi, bt, sl)  # noqa: F841  (alive across the call)
     rc = lib.orc_verify_forward(ctypes.byref(P), b0, b1, h0, h1, _ptr(res["o"]), *dbg, int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected the requested ranges or head counts")

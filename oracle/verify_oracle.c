@@ -38,7 +38,15 @@
  *     prefix key stays visible and only the draft columns are read; draft key
  *     t is visible to row i iff mask[mask_indptr[b] + i*(P_b+L_b) + P_b + t];
  *   - a row that sees no key at all (empty prefix and no visible draft) has
- *     output 0 and lse -inf.
+ *     output 0 and lse -inf;
+ *   - drafts already in a paged cache (the unified target-verify path of the
+ *     "aiter_backend.py" page: block_table [B, max_blocks] of page ids over a
+ *     pool of pages of page_size tokens, seqused_k = seq_lens + draft_num,
+ *     causal): the keys of sequence b are cache positions 0 .. P_b + L_b - 1,
+ *     position j at pool row block_table[b][j / page_size] * page_size +
+ *     j % page_size; positions < P_b = seq_lens[b] are the prefix, the next
+ *     L_b are the drafts (row i sees drafts t <= i); every key is a cache
+ *     entry, so k_scale and v_scale apply to the drafts too.
  *
  * Debug outputs (optional) split the same sum into its prefix part and its
  * draft part: o_prefix / lse_prefix over the prefix keys only (lse = -inf and
@@ -82,6 +90,12 @@ typedef struct {
   double sm_scale, k_scale, v_scale;
   const uint8_t* custom_mask;   /* NULL: causal drafts (t <= i) */
   const int64_t* mask_indptr;   /* [B+1], used with custom_mask  */
+  /* drafts in a paged cache (kv_indptr / kv_indices / k_ext / v_ext unused) */
+  int32_t paged;
+  const int32_t* block_table;   /* [B, bt_s0] page ids */
+  int64_t bt_s0;
+  int64_t page_size;
+  const int32_t* seq_lens;      /* [B] cached tokens before the drafts */
 } orc_problem;
 
 /* bf16 is the upper half of an IEEE-754 binary32: widen the bit pattern. */
@@ -121,9 +135,27 @@ static double pool_elem(const orc_problem* p, const void* pool, int64_t off) {
   return orc_bf16_to_f64(((const uint16_t*)pool)[off]);
 }
 
+/* Pool row of cache position j of sequence b (paged problems). */
+static int64_t paged_row(const orc_problem* p, int64_t b, int64_t j) {
+  return (int64_t)p->block_table[b * p->bt_s0 + j / p->page_size] * p->page_size + j % p->page_size;
+}
+
 static int64_t kv_index(const orc_problem* p, int64_t n) {
   if (p->idx_dtype == ORC_IDX_I64) return ((const int64_t*)p->kv_indices)[n];
   return (int64_t)((const int32_t*)p->kv_indices)[n];
+}
+
+/* Pool row of prefix key j of sequence b (p_b = kv_indptr[b]). */
+static int64_t prefix_row(const orc_problem* p, int64_t b, int64_t p_b, int64_t j) {
+  return p->paged ? paged_row(p, b, j) : kv_index(p, p_b + j);
+}
+
+/* Value element c of draft key t of sequence b (KV head kvh). */
+static double draft_value(const orc_problem* p, int64_t b, int64_t s_b, int64_t P_b, int64_t t, int64_t kvh,
+                          int64_t c) {
+  if (p->paged)
+    return p->v_scale * pool_elem(p, p->v_pool, paged_row(p, b, P_b + t) * p->vp_s0 + kvh * p->vp_s1 + c);
+  return orc_bf16_to_f64(p->v_ext[(s_b + t) * p->ve_s0 + kvh * p->ve_s1 + c]);
 }
 
 /* Is draft key t visible to draft row i of sequence b? */
@@ -141,8 +173,8 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
   const int64_t kvh = h / group;
   const int64_t s_b = p->qo_indptr[b];
   const int64_t L_b = (int64_t)p->qo_indptr[b + 1] - s_b;
-  const int64_t p_b = p->kv_indptr[b];
-  const int64_t P_b = (int64_t)p->kv_indptr[b + 1] - p_b;
+  const int64_t p_b = p->paged ? 0 : p->kv_indptr[b];
+  const int64_t P_b = p->paged ? (int64_t)p->seq_lens[b] : (int64_t)p->kv_indptr[b + 1] - p_b;
   const int64_t D = p->d, DV = p->dv;
 
   double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
@@ -156,15 +188,21 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
 
     /* scores: prefix keys first, then the visible drafts t <= i */
     for (int64_t j = 0; j < P_b; ++j) {
-      const int64_t loc = kv_index(p, p_b + j);
+      const int64_t loc = prefix_row(p, b, p_b, j);
       double dot = 0.0;
       for (int64_t c = 0; c < D; ++c) dot += qrow[c] * pool_elem(p, p->k_pool, loc * p->kp_s0 + kvh * p->kp_s1 + c);
       score[j] = p->sm_scale * p->k_scale * dot;
     }
     for (int64_t t = 0; t < L_b; ++t) {
       double dot = 0.0;
-      for (int64_t c = 0; c < D; ++c)
-        dot += qrow[c] * orc_bf16_to_f64(p->k_ext[(s_b + t) * p->ke_s0 + kvh * p->ke_s1 + c]);
+      if (p->paged) {
+        const int64_t loc = paged_row(p, b, P_b + t);
+        for (int64_t c = 0; c < D; ++c) dot += qrow[c] * pool_elem(p, p->k_pool, loc * p->kp_s0 + kvh * p->kp_s1 + c);
+        dot *= p->k_scale;
+      } else {
+        for (int64_t c = 0; c < D; ++c)
+          dot += qrow[c] * orc_bf16_to_f64(p->k_ext[(s_b + t) * p->ke_s0 + kvh * p->ke_s1 + c]);
+      }
       score[P_b + t] = draft_visible(p, b, i, t, P_b, L_b) ? p->sm_scale * dot : -INFINITY;
     }
     const int64_t n_keys = P_b + L_b;
@@ -178,13 +216,13 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
       const double w = (score[j] == -INFINITY) ? 0.0 : exp(score[j] - mx);
       denom += w;
       if (j < P_b) {
-        const int64_t loc = kv_index(p, p_b + j);
+        const int64_t loc = prefix_row(p, b, p_b, j);
         for (int64_t c = 0; c < DV; ++c)
           acc[c] += w * p->v_scale * pool_elem(p, p->v_pool, loc * p->vp_s0 + kvh * p->vp_s1 + c);
       } else {
         const int64_t t = j - P_b;
         for (int64_t c = 0; c < DV; ++c)
-          acc[c] += w * orc_bf16_to_f64(p->v_ext[(s_b + t) * p->ve_s0 + kvh * p->ve_s1 + c]);
+          acc[c] += w * draft_value(p, b, s_b, P_b, t, kvh, c);
       }
     }
     double* o = out + (row * p->h_q + h) * DV;
@@ -203,7 +241,7 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
         for (int64_t c = 0; c < DV; ++c) acc2[c] = 0.0;
         for (int64_t j = 0; j < P_b; ++j) {
           const double w = exp(score[j] - pm);
-          const int64_t loc = kv_index(p, p_b + j);
+          const int64_t loc = prefix_row(p, b, p_b, j);
           pd += w;
           for (int64_t c = 0; c < DV; ++c)
             acc2[c] += w * p->v_scale * pool_elem(p, p->v_pool, loc * p->vp_s0 + kvh * p->vp_s1 + c);
@@ -222,7 +260,7 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
         const double w = exp(score[P_b + t] - dm);
         dd += w;
         for (int64_t c = 0; c < DV; ++c)
-          acc2[c] += w * orc_bf16_to_f64(p->v_ext[(s_b + t) * p->ve_s0 + kvh * p->ve_s1 + c]);
+          acc2[c] += w * draft_value(p, b, s_b, P_b, t, kvh, c);
       }
       for (int64_t c = 0; c < DV; ++c) od[c] = (dm == -INFINITY) ? 0.0 : acc2[c] / dd;
       lse_draft[row * p->h_q + h] = (dm == -INFINITY) ? -INFINITY : dm + log(dd);

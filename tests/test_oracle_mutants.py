@@ -23,10 +23,13 @@ MUTANTS = {
     "tree_mask_prefix_offset": ("i * (P_b + L_b) + P_b + t]", "i * (P_b + L_b) + t]"),
     "v_scale_dropped": ("acc[c] += w * p->v_scale * pool_elem(p, p->v_pool", "acc[c] += w * pool_elem(p, p->v_pool"),
     "gqa_modulo": ("const int64_t kvh = h / group;", "const int64_t kvh = h % p->h_kv;"),
-    "no_indirection": ("const int64_t loc = kv_index(p, p_b + j);", "const int64_t loc = p_b + j;"),
+    "no_indirection": ("return p->paged ? paged_row(p, b, j) : kv_index(p, p_b + j);",
+                       "return p->paged ? paged_row(p, b, j) : p_b + j;"),
+    "paged_page_offset": ("* p->page_size + j % p->page_size;", "* p->page_size + j / p->page_size;"),
+    "paged_draft_unscaled": ("return p->v_scale * pool_elem(p, p->v_pool, paged_row", "return pool_elem(p, p->v_pool, paged_row"),
     "softmax_sign": ("exp(score[j] - mx)", "exp(mx - score[j])"),
     "pool_strides_transposed": ("loc * p->kp_s0 + kvh * p->kp_s1", "loc * p->kp_s1 + kvh * p->kp_s0"),
-    "draft_value_row": ("p->v_ext[(s_b + t) * p->ve_s0", "p->v_ext[(s_b + i) * p->ve_s0"),
+    "draft_value_row": ("p->v_ext[(s_b + t) * p->ve_s0", "p->v_ext[(s_b + 0) * p->ve_s0"),
 }
 
 

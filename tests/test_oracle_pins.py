@@ -82,12 +82,19 @@ def _golden_arrays(fx, pool_dtype):
         assert torch.equal(f8.to(torch.float64).nan_to_num(7.5), t.nan_to_num(7.5)), "fixture value not exact in e4m3"
         return f8.view(torch.uint8).numpy()
 
+    if fx.get("paged"):
+        n, hq = len(fx["q"]), len(fx["q"][0])
+        hkv, d = len(fx["k_pool"][0]), len(fx["k_pool"][0][0])
+        dv = len(fx["v_pool"][0][0])
+        fx = dict(fx, k_ext=[[[0] * d] * hkv] * n, v_ext=[[[0] * dv] * hkv] * n)
     return {
+        **({"block_table": np.array(fx["block_table"], dtype=np.int32), "page_size": fx["page_size"],
+            "seq_lens": np.array(fx["seq_lens"], dtype=np.int32)} if fx.get("paged") else
+           {"kv_indptr": np.array(fx["kv_indptr"], dtype=np.int32),
+            "kv_indices": np.array(fx["kv_indices"], dtype=np.int64)}),
         "q": bits16(fx["q"]), "k_ext": bits16(fx["k_ext"]), "v_ext": bits16(fx["v_ext"]),
         "k_pool": pool(fx["k_pool"]), "v_pool": pool(fx["v_pool"]), "pool_dtype": pool_dtype,
         "qo_indptr": np.array(fx["qo_indptr"], dtype=np.int32),
-        "kv_indptr": np.array(fx["kv_indptr"], dtype=np.int32),
-        "kv_indices": np.array(fx["kv_indices"], dtype=np.int64),
         "sm_scale": _parse_value(fx["sm_scale"]), "k_scale": fx["k_scale"], "v_scale": fx["v_scale"],
         **({"custom_mask": np.array(fx["custom_mask"], dtype=np.uint8),
             "mask_indptr": np.array(fx["mask_indptr"], dtype=np.int64)} if "custom_mask" in fx else {}),
@@ -124,7 +131,8 @@ def test_golden(fn, pool_dtype):
 
 def test_golden_fixtures_present():
     names = {f for f in os.listdir(GOLDEN) if f.endswith(".json")}
-    assert {"scales_causal.json", "gqa_mapping.json", "indptr_empty_prefix.json", "tree_mask.json"} <= names
+    assert {"scales_causal.json", "gqa_mapping.json", "indptr_empty_prefix.json", "tree_mask.json",
+            "paged_drafts_in_cache.json"} <= names
 
 
 # ---------------------------------------------------------------- library cross-check
@@ -368,3 +376,59 @@ def test_tree_mask_row_with_nothing_visible_is_zero():
     r = _run(dict(prob, custom_mask=cm), debug=True)
     assert np.array_equal(r["o"][1], np.zeros_like(r["o"][1]))
     assert np.isfinite(r["o"]).all() and np.isneginf(r["lse_draft"][1]).all()
+
+
+# ---------------------------------------------------------------- drafts in a paged cache
+def _sdpa_paged(prob):
+    """fp64 SDPA over each sequence's cache positions 0 .. P+L-1 (scaled keys
+    and values), prefix visible, drafts causal."""
+    d64 = torch.float64
+    q = prob["q"].to(d64)
+    kc, vc = prob["k_buffer"].to(d64), prob["v_buffer"].to(d64)
+    bt, ps = prob["block_table"].long(), prob["page_size"]
+    h_q, h_kv = q.shape[1], kc.shape[1]
+    g = h_q // h_kv
+    L = prob["max_len_extend"]
+    out = torch.empty(q.shape[0], h_q, vc.shape[2], dtype=d64)
+    for b, P in enumerate(prob["seq_lens"].tolist()):
+        j = torch.arange(P + L)
+        rows = bt[b, j // ps] * ps + j % ps
+        k = prob["k_scale"] * kc[rows]
+        v = prob["v_scale"] * vc[rows]
+        mask = torch.ones(L, P + L, dtype=torch.bool)
+        mask[:, P:] = torch.tril(torch.ones(L, L, dtype=torch.bool))
+        qh = q[b * L:(b + 1) * L].transpose(0, 1)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qh, k.transpose(0, 1).repeat_interleave(g, 0), v.transpose(0, 1).repeat_interleave(g, 0),
+            attn_mask=mask, scale=prob["sm_scale"])
+        out[b * L:(b + 1) * L] = o.transpose(0, 1)
+    return out.numpy()
+
+
+PAGED_CASES = [
+    workloads.Spec("paged_ps16", (100, 0, 37), 4, 8, 2, 64, 64, perm=True, page_size=16, pool_extra=40, seed=51),
+    workloads.Spec("paged_ps1_fp8", (30, 61), 3, 4, 2, 64, 64, pool="e4m3", perm=True, page_size=1, k_scale=0.5,
+                   v_scale=2.0, seed=52),
+    workloads.Spec("paged_decode_ps64", (200, 129, 5), 1, 8, 8, 64, 64, perm=True, page_size=64, seed=53),
+]
+
+
+@pytest.mark.parametrize("spec", PAGED_CASES, ids=lambda s: s.name)
+def test_paged_sdpa_crosscheck(spec):
+    prob = workloads.make_problem(spec, "cpu")
+    got = _run(prob)["o"]
+    np.testing.assert_allclose(got, _sdpa_paged(prob), rtol=1e-11, atol=1e-12)
+
+
+def test_paged_equals_flat_when_scales_are_one():
+    spec = workloads.Spec("paged_eq", (70, 3, 0), 4, 8, 4, 64, 64, perm=True, page_size=8, pool_extra=24, seed=54)
+    prob = workloads.make_problem(spec, "cpu")
+    paged = _run(prob)["o"]
+    flat = {k: v for k, v in prob.items() if k not in ("block_table", "page_size", "seq_lens")}
+    assert np.array_equal(paged, _run(flat)["o"])
+
+
+def test_paged_poisoned_pages_are_never_read():
+    spec = workloads.Spec("paged_poison", (50, 9), 4, 4, 1, 64, 64, perm=True, page_size=4, pool_extra=64,
+                          poison=True, seed=55)
+    assert np.isfinite(_run(workloads.make_problem(spec, "cpu"))["o"]).all()

@@ -41,6 +41,7 @@ class Spec:
     pool_extra: int = 0         # unreferenced pool slots beyond sum(prefix_lens)
     poison: bool = False        # fill unreferenced pool slots with NaN
     tree: str = ""              # "" causal drafts; "chain" | "star" | "random": tree-verify mask
+    page_size: int = 0          # > 0: drafts already in a paged cache, addressed by a block table
     seed: int = 0
 
     @property
@@ -73,6 +74,59 @@ def _gen(device, seed: int) -> torch.Generator:
     return g
 
 
+def _make_paged(spec: Spec, device, g, lens) -> dict:
+    """Drafts-in-cache problem: every sequence's prefix and drafts occupy
+    ceil((P_b + l_ext) / page_size) pages of a shared cache, listed in a
+    zero-padded int32 block table (the unified target-verify layout)."""
+    ps, L, B = spec.page_size, spec.l_ext, int(lens.numel())
+    npages = [-(-(int(P) + L) // ps) for P in lens.tolist()]
+    used = sum(npages)
+    num_pages = used + -(-int(spec.pool_extra) // ps)
+    bf16 = torch.bfloat16
+    k_cache = torch.randn(num_pages * ps, spec.h_kv, spec.d, generator=g, device=device, dtype=bf16)
+    v_cache = torch.randn(num_pages * ps, spec.h_kv, spec.dv, generator=g, device=device, dtype=bf16)
+    order = (torch.randperm(num_pages, generator=g, device=device) if spec.perm
+             else torch.arange(num_pages, device=device)).to(torch.int32).cpu()
+    max_pages = max(npages) if npages else 1
+    bt = torch.zeros(B, max_pages, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(npages):
+        bt[b, :n] = order[pos:pos + n]
+        pos += n
+    n_ext = B * L
+    q = torch.randn(n_ext, spec.h_q, spec.d, generator=g, device=device, dtype=bf16)
+    rows = []  # pool row of every cache position, per sequence
+    for b, P in enumerate(lens.tolist()):
+        j = torch.arange(int(P) + L)
+        rows.append((bt[b, j // ps].long() * ps + j % ps))
+    if spec.poison:
+        unref = torch.ones(num_pages * ps, dtype=torch.bool)
+        if rows:
+            unref[torch.cat(rows)] = False
+        k_cache[unref.to(device)] = float("nan")
+        v_cache[unref.to(device)] = float("nan")
+    if spec.pool == "e4m3":
+        k_cache = k_cache.to(torch.float8_e4m3fn)
+        v_cache = v_cache.to(torch.float8_e4m3fn)
+    # flat equivalents (prefix through kv_indices, drafts as k_ext / v_ext), for comparisons
+    pre = [r[:int(P)] for r, P in zip(rows, lens.tolist())]
+    drf = torch.cat([r[int(P):] for r, P in zip(rows, lens.tolist())]) if rows else torch.zeros(0, dtype=torch.long)
+    kv_indices = (torch.cat(pre) if pre else torch.zeros(0, dtype=torch.long)).to(torch.int64)
+    kv_indptr = torch.zeros(B + 1, dtype=torch.int32)
+    kv_indptr[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    d_dev = drf.to(device)
+    k_ext = k_cache[d_dev].to(bf16) if n_ext else torch.zeros(0, spec.h_kv, spec.d, dtype=bf16, device=device)
+    v_ext = v_cache[d_dev].to(bf16) if n_ext else torch.zeros(0, spec.h_kv, spec.dv, dtype=bf16, device=device)
+    return {
+        "spec": spec, "q": q, "k_ext": k_ext, "v_ext": v_ext, "k_buffer": k_cache, "v_buffer": v_cache,
+        "block_table": bt.to(device), "page_size": ps, "seq_lens": lens.to(torch.int32).to(device),
+        "qo_indptr": torch.arange(0, n_ext + 1, L, dtype=torch.int32).to(device),
+        "kv_indptr": kv_indptr.to(device), "kv_indices": kv_indices.to(device),
+        "max_len_extend": L, "sm_scale": spec.sm_scale, "k_scale": spec.k_scale, "v_scale": spec.v_scale,
+        "prefix_lens": [int(x) for x in lens.tolist()], "pool_dtype": spec.pool,
+    }
+
+
 def make_problem(spec: Spec, device="cpu", **overrides) -> dict:
     """Draw one problem.  Every tensor lives on ``device``; draws are seeded by
     ``spec.seed`` in a fixed order, so a (spec, device) pair is reproducible."""
@@ -85,6 +139,8 @@ def make_problem(spec: Spec, device="cpu", **overrides) -> dict:
     else:
         lo, hi = spec.len_range
         lens = torch.randint(lo, hi + 1, (spec.batch,), generator=g, device=device).cpu()
+    if spec.page_size > 0:
+        return _make_paged(spec, device, g, lens)
     B = int(lens.numel())
     T = int(lens.sum())
     pool_tokens = T + int(spec.pool_extra)
@@ -188,6 +244,8 @@ def to_oracle_arrays(prob: dict) -> dict:
         "sm_scale": prob["sm_scale"], "k_scale": prob["k_scale"], "v_scale": prob["v_scale"],
         **({"custom_mask": prob["custom_mask"].cpu().numpy(), "mask_indptr": prob["mask_indptr"].cpu().numpy()}
            if prob.get("custom_mask") is not None else {}),
+        **({"block_table": prob["block_table"].cpu().numpy(), "page_size": prob["page_size"],
+            "seq_lens": prob["seq_lens"].cpu().numpy()} if prob.get("block_table") is not None else {}),
     }
 
 
