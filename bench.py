@@ -84,6 +84,9 @@ WORKLOADS = {
     "tiny": workloads.TINY,
     "d256": workloads.D256,
     "fp8": workloads.FP8,
+    # the same batch with the drafts already in a 16-token-page cache
+    # (verify_splitkv_paged_fwd)
+    "serving_paged": workloads.replace(workloads.SERVING, name="serving_paged16_b64_p8k_32k", page_size=16),
 }
 
 
@@ -223,6 +226,9 @@ def seq_bytes(prob, b: int) -> int:
     h_q, h_kv, d, dv = q.shape[1], ke.shape[1], ke.shape[2], ve.shape[2]
     L = prob["max_len_extend"]
     e = prob["k_buffer"].element_size()
+    if prob.get("block_table") is not None:
+        pages = -(-(P + L) // prob["page_size"])
+        return int((P + L) * h_kv * (d + dv) * e + 4 * pages + 4 + L * (2 * h_q * d + 2 * h_q * dv))
     idx = prob["kv_indices"].element_size()
     return int(P * h_kv * (d + dv) * e + P * idx + L * (2 * h_q * d + 2 * h_kv * (d + dv) + 2 * h_q * dv))
 
@@ -299,6 +305,11 @@ def cpu_baseline(prob, target_s: float) -> dict:
 
 # ----------------------------------------------------------------------------- our arm
 def _call(vsk, prob, o, ws):
+    if prob.get("block_table") is not None:
+        vsk.verify_splitkv_paged_fwd(prob["q"], o, prob["k_buffer"], prob["v_buffer"], prob["block_table"],
+                                     prob["seq_lens"], prob["page_size"], prob["max_len_extend"], prob["k_scale"],
+                                     prob["v_scale"], sm_scale=prob["sm_scale"], workspace=ws)
+        return True
     return vsk.verify_splitkv_fwd(prob["q"], prob["k_ext"], prob["v_ext"], o, prob["k_buffer"], prob["v_buffer"],
                                   prob["qo_indptr"], prob["kv_indptr"], prob["kv_indices"], None, True, None,
                                   prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
@@ -331,7 +342,10 @@ def time_kernel(vsk, prob, o, ws, steps: int, warmup: int, dist: Dist, gpu_index
 
 def time_e2e(vsk, prob, steps: int, warmup: int):
     """Public API end to end: pinned host inputs copied in, result copied out."""
-    names = ["q", "k_ext", "v_ext", "k_buffer", "v_buffer", "qo_indptr", "kv_indptr", "kv_indices"]
+    if prob.get("block_table") is not None:
+        names = ["q", "k_buffer", "v_buffer", "block_table", "seq_lens"]
+    else:
+        names = ["q", "k_ext", "v_ext", "k_buffer", "v_buffer", "qo_indptr", "kv_indptr", "kv_indices"]
     host = {k: prob[k].cpu().pin_memory() for k in names}
     dev = {k: torch.empty_like(prob[k]) for k in names}
     o = torch.empty(prob["q"].shape[0], prob["q"].shape[1], prob["v_ext"].shape[2], dtype=torch.bfloat16,
@@ -422,8 +436,11 @@ def workload_config(spec, prob, nbytes) -> dict:
         "prefix_lens": (f"uniform int [{spec.len_range[0]}, {spec.len_range[1]}], seed {spec.seed}"
                         if spec.prefix_lens is None else list(spec.prefix_lens)),
         "l_ext": spec.l_ext, "h_q": spec.h_q, "h_kv": spec.h_kv, "head_dim": spec.d, "v_head_dim": spec.dv,
-        "kv_pool": spec.pool, "kv_indices": ("random permutation" if spec.perm else "arange") + f", {spec.idx_dtype}",
-        "k_scale": spec.k_scale, "v_scale": spec.v_scale, "page_size": 1,
+        "kv_pool": spec.pool,
+        "kv_indices": (("random page permutation, int32 block table" if spec.page_size > 0 else
+                        ("random permutation" if spec.perm else "arange") + f", {spec.idx_dtype}")),
+        "k_scale": spec.k_scale, "v_scale": spec.v_scale, "page_size": max(1, spec.page_size),
+        "drafts": "in the paged cache (block table)" if spec.page_size > 0 else "k_extend / v_extend",
         "algorithmic_bytes_per_call": nbytes,
         "l2": "inputs larger than L2 (no flush)" if nbytes > 129e6 else "inputs fit in L2 (L2-resident figure)",
         "kernel_launches_per_step": 1,

@@ -140,6 +140,38 @@ int verify_splitkv_tree_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_exte
                             float k_scale, float v_scale, float sm_scale,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Verify with the drafts already written to a paged KV cache (the unified
+ * target-verify path of the "aiter_backend.py" page: the drafts' K/V are
+ * stored before attention runs, the block table maps cache positions to
+ * pages, and the key length of sequence b is seq_lens[b] + l_ext).  Cache
+ * position t of sequence b lives in pool row
+ *     block_table[b][t / page_size] * page_size + t % page_size;
+ * positions [0, seq_lens[b]) are the prefix and [seq_lens[b], seq_lens[b] +
+ * l_ext) the drafts, which see the whole prefix and, causally, the drafts up
+ * to themselves.  k_scale / v_scale multiply EVERY cached key and value,
+ * drafts included (they come from the same cache).  With l_ext = 1 this is
+ * the plain paged decode step.
+ *   q            [B*l_ext, h_q, D] bf16, sequence b's drafts at rows b*l_ext ..
+ *   o            [B*l_ext, h_q, D] bf16 output (written, never read)
+ *   k_cache, v_cache  [n_pages*page_size, h_kv, D] bf16 or fp8 e4m3 (same
+ *                dtype), rows 16-byte aligned
+ *   block_table  [B, max_blocks] int32 page ids, rows contiguous; only the
+ *                columns covering positions < seq_lens[b] + l_ext are read
+ *   seq_lens     [B] int32 cached tokens before the drafts
+ *   page_size    tokens per page (>= 1); max_blocks*page_size must cover l_ext
+ * D in {64, 128, 256}; (h_q/h_kv)*l_ext within the limits of
+ * verify_splitkv_fwd, whose workspace rules, workspace size and return value
+ * apply unchanged.  Device-side checks: a page id whose rows fall outside the
+ * cache sets error bit 1 and those keys are left out; seq_lens[b] < 0 or
+ * seq_lens[b] + l_ext beyond max_blocks*page_size sets bit 2 and sequence b
+ * is computed with an empty prefix. */
+int verify_splitkv_paged_fwd(const vsk_tensor* q, const vsk_tensor* o,
+                             const vsk_tensor* k_cache, const vsk_tensor* v_cache,
+                             const vsk_tensor* block_table, const vsk_tensor* seq_lens,
+                             int64_t page_size, int64_t max_len_extend, float k_scale,
+                             float v_scale, float sm_scale, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Upper bound, in bytes, of the workspace verify_splitkv_fwd needs for any
  * batch of up to max_bs sequences with these head counts and sizes on the
  * CURRENT CUDA device (its SM count sets the number of persistent CTAs).

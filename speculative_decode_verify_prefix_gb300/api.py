@@ -149,6 +149,34 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
     return True
 
 
+def verify_splitkv_paged_fwd(q, o, k_cache, v_cache, block_table, seq_lens, page_size, max_len_extend,
+                             k_scale=1.0, v_scale=1.0, sm_scale=None, max_bs=None, workspace=None,
+                             stream=None) -> None:
+    """Verify with the drafts already stored in a paged KV cache.
+
+    ``q`` / ``o``: [B*l_ext, h_q, D] bf16; ``k_cache`` / ``v_cache``:
+    [n_pages*page_size, h_kv, D] bf16 or fp8 e4m3; ``block_table``: [B,
+    max_blocks] int32 page ids; ``seq_lens``: [B] int32 cached tokens before
+    the drafts (the drafts occupy cache positions seq_lens[b] ..
+    seq_lens[b] + l_ext - 1).  ``k_scale`` / ``v_scale`` apply to every cached
+    key and value, drafts included.  Enqueues the kernel on the current stream;
+    raises ValueError when the library rejects the arguments."""
+    bs = seq_lens.shape[0]
+    mle = int(max_len_extend)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sm = 0.0 if sm_scale is None else float(sm_scale)
+    ok = _native.lib().verify_splitkv_paged_fwd(
+        _ref(q), _ref(o), _ref(k_cache), _ref(v_cache), _ref(block_table), _ref(seq_lens), int(page_size), mle,
+        _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+        ctypes.c_void_p(stream.cuda_stream))
+    if not ok:
+        raise ValueError("verify_splitkv_paged_fwd: " + _native.last_error())
+
+
 def read_error_flags(workspace=None, stream=None) -> int:
     """Device error word of a workspace (synchronises; for tests/debugging)."""
     if workspace is None:

@@ -29,6 +29,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -80,6 +81,15 @@ struct Params {
   int B, L, gq, R, HC, MT, n_hg, nwc, nst;
   int ring_off, warp_bytes;
   float scale2, dscale2, v_scale;
+  float dvs;  // multiplier of draft values (v_scale when drafts come from the cache)
+  // drafts already in a paged cache: block table of page ids, prefix lengths
+  int paged;
+  const int* bt;
+  long long bt_s0;
+  int bt_cols, page;
+  unsigned pg_m;  // division by page: t / page == (umulhi(t, pg_m) + t) >> pg_l for 0 <= t < 2^31
+  int pg_l;
+  const int* slens;
   long long w_min;
   const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
   const void* mindptr;
@@ -199,12 +209,40 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(unsigned short two) {
 // end; CTA c owns positions [c*W, c*W + W).  Both the producer and the
 // consumers walk the same sequence deterministically.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void load_seq(const Params& p, int b, int& P, long long& kv0) {
+// Prefix length (and kv_indices base) of sequence b; inconsistent entries
+// give an empty prefix and return false.
+__device__ __forceinline__ bool seq_info(const Params& p, int b, int& P, long long& kv0) {
+  if (p.paged) {
+    const int n = __ldg(p.slens + b);
+    const bool ok = n >= 0 && static_cast<long long>(n) + p.L <= static_cast<long long>(p.bt_cols) * p.page;
+    P = ok ? n : 0;
+    kv0 = 0;
+    return ok;
+  }
   const int a = __ldg(p.kvp + b);
   const int e = __ldg(p.kvp + b + 1);
   const bool ok = a >= 0 && e >= a && static_cast<long long>(e) <= p.n_idx;
   P = ok ? e - a : 0;
   kv0 = ok ? a : 0;
+  return ok;
+}
+
+__device__ __forceinline__ void load_seq(const Params& p, int b, int& P, long long& kv0) { seq_info(p, b, P, kv0); }
+
+// Block-table column of cache position t >= 0: multiply-high division by a
+// constant (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994), exact for every t < 2^31.
+__device__ __forceinline__ int page_of(const Params& p, int t) {
+  const unsigned u = static_cast<unsigned>(t);
+  return static_cast<int>((__umulhi(u, p.pg_m) + u) >> p.pg_l);
+}
+
+// Pool row of cache position pos of sequence b (paged problems), or -1.
+__device__ __forceinline__ long long paged_row(const Params& p, int b, int pos) {
+  const int col = page_of(p, pos);
+  const long long pid = __ldg(p.bt + static_cast<long long>(b) * p.bt_s0 + col);
+  const long long r = pid * p.page + (pos - col * p.page);
+  return (pid >= 0 && r < p.pool) ? r : -1;
 }
 
 struct Seg {
@@ -254,7 +292,7 @@ __device__ __forceinline__ void sit_settle(const Params& p, StageIt& it, long lo
 template <int KS>
 __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int r0, int r1, int j, bool flag_err,
                                       uint32_t (&qf)[KS][4]) {
-  const int a = __ldg(p.qo + s.b), e = __ldg(p.qo + s.b + 1);
+  const int a = p.qo ? __ldg(p.qo + s.b) : s.b * p.L, e = p.qo ? __ldg(p.qo + s.b + 1) : (s.b + 1) * p.L;
   const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
   if (!ok && flag_err) atomicOr(p.err, kErrBadQoIndptr);
   const int s_b = ok ? a : s.b * p.L;
@@ -319,10 +357,10 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   long long mysum = 0;
   bool bad_kvp = false;
   for (int b = b_lo; b < b_hi; ++b) {
-    const int a = __ldg(p.kvp + b), e = __ldg(p.kvp + b + 1);
-    const bool ok = a >= 0 && e >= a && static_cast<long long>(e) <= p.n_idx;
-    bad_kvp |= !ok;
-    mysum += max(ok ? e - a : 0, 1);
+    int P;
+    long long kv0;
+    bad_kvp |= !seq_info(p, b, P, kv0);
+    mysum += max(P, 1);
   }
   if (bad_kvp && blockIdx.x == 0) atomicOr(p.err, kErrBadKvIndptr);
   long long incl = mysum;
@@ -405,7 +443,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
       const long long n = it.s.kv0 + it.tok + lane;
       const uint32_t dst = idx_s + static_cast<uint32_t>(job % kIdxRing) * 128u + lane * 8u;
-      if (p.idx64)
+      if (p.paged)  // page id of cache position tok + lane
+        cp_async_4(dst, p.bt + static_cast<long long>(it.s.b) * p.bt_s0 + page_of(p, it.tok + lane));
+      else if (p.idx64)
         cp_async_8(dst, static_cast<const long long*>(p.kvi) + n);
       else
         cp_async_4(dst, static_cast<const int*>(p.kvi) + n);
@@ -416,9 +456,16 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     const int n = min(kStageTokens, it.te - it.tok);
     const unsigned char* ie = idx_ring + static_cast<int>(job % kIdxRing) * 128;
     long long myloc = -1;
-    if (lane < n)
-      myloc = p.idx64 ? *reinterpret_cast<const long long*>(ie + lane * 8)
-                      : static_cast<long long>(*reinterpret_cast<const int*>(ie + lane * 8));
+    if (lane < n) {
+      if (p.paged) {
+        const long long pid = *reinterpret_cast<const int*>(ie + lane * 8);
+        const int t = it.tok + lane;
+        myloc = pid >= 0 ? pid * p.page + (t - page_of(p, t) * p.page) : -1;
+      } else {
+        myloc = p.idx64 ? *reinterpret_cast<const long long*>(ie + lane * 8)
+                        : static_cast<long long>(*reinterpret_cast<const int*>(ie + lane * 8));
+      }
+    }
     const bool ok = lane < n && myloc >= 0 && myloc < p.pool;
     const unsigned mask = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
     if (lane < n && !ok && hc == 0 && mt == 0) atomicOr(p.err, kErrBadIndex);
@@ -789,20 +836,45 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       for (int td = 0; td * 8 < p.L; ++td) {
         float sd[4] = {0.f, 0.f, 0.f, 0.f};
         const int tkey = td * 8 + g;  // key whose K row this lane supplies
-        const bool kv = tkey < p.L;
-        const __nv_bfloat16* kp = p.ke + (static_cast<long long>(s_b) + (kv ? tkey : 0)) * p.ke_s0 +
-                                  static_cast<long long>(kvh) * p.ke_s1;
+        bool kv = tkey < p.L;
+        unsigned kvm = 0xFFFFFFFFu;  // lane (g, 0) bit set: key td*8+g has a valid row
+        if (p.paged) {
+          // drafts are cache positions P + t, dequantised like the prefix
+          const long long krow = kv ? paged_row(p, sg.b, sg.P + tkey) : -1;
+          if (tkey < p.L && krow < 0) atomicOr(p.err, kErrBadIndex);
+          kv = krow >= 0;
+          kvm = __ballot_sync(0xffffffffu, kv);
+          const unsigned char* kr = p.kb + (kv ? krow : 0) * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t b0 = kv ? ld_u32(kp + kk * 16 + 2 * j) : 0u;
-          const uint32_t b1 = kv ? ld_u32(kp + kk * 16 + 8 + 2 * j) : 0u;
-          mma_bf16(sd, qf[kk], b0, b1);
+          for (int kk = 0; kk < KS; ++kk) {
+            uint32_t b0 = 0u, b1 = 0u;
+            if (kv) {
+              if constexpr (FP8) {
+                b0 = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(kr + kk * 16 + 2 * j));
+                b1 = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(kr + kk * 16 + 8 + 2 * j));
+              } else {
+                b0 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 2 * j) * 2);
+                b1 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2);
+              }
+            }
+            mma_bf16(sd, qf[kk], b0, b1);
+          }
+        } else {
+          const __nv_bfloat16* kp = p.ke + (static_cast<long long>(s_b) + (kv ? tkey : 0)) * p.ke_s0 +
+                                    static_cast<long long>(kvh) * p.ke_s1;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t b0 = kv ? ld_u32(kp + kk * 16 + 2 * j) : 0u;
+            const uint32_t b1 = kv ? ld_u32(kp + kk * 16 + 8 + 2 * j) : 0u;
+            mma_bf16(sd, qf[kk], b0, b1);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = td * 8 + 2 * j + (e & 1);
           const int irow = (e < 2) ? i0 : i1;
-          sd[e] = visible(key, irow) ? sd[e] * p.dscale2 : NEG_INF;
+          const bool rowok = (kvm >> (((key - td * 8) & 7) * 4)) & 1u;
+          sd[e] = (visible(key, irow) && rowok) ? sd[e] * p.dscale2 : NEG_INF;
         }
         const float mx0 = quad_max(fmaxf(sd[0], sd[1]));
         const float mx1 = quad_max(fmaxf(sd[2], sd[3]));
@@ -833,8 +905,27 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           for (int e = 0; e < 2; ++e) {
             const int key = td * 8 + 2 * js + e;
             if (key >= p.L) continue;  // uniform across the warp
-            const float w0 = __shfl_sync(0xffffffffu, pd[e], g * 4 + js);
-            const float w1 = __shfl_sync(0xffffffffu, pd[2 + e], g * 4 + js);
+            const float w0 = __shfl_sync(0xffffffffu, pd[e], g * 4 + js) * p.dvs;
+            const float w1 = __shfl_sync(0xffffffffu, pd[2 + e], g * 4 + js) * p.dvs;
+            if (p.paged) {
+              const long long vrow = paged_row(p, sg.b, sg.P + key);  // uniform across the warp
+              if (vrow < 0) continue;                                   // its weight is 0: never read
+              const unsigned char* vr = p.vb + vrow * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+                float2 v;
+                if constexpr (FP8) {
+                  v = unpack_bf16(e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(vr + n * 8 + 2 * j)));
+                } else {
+                  v = unpack_bf16(*reinterpret_cast<const uint32_t*>(vr + (n * 8 + 2 * j) * 2));
+                }
+                acc[n][0] = fmaf(w0, v.x, acc[n][0]);
+                acc[n][1] = fmaf(w0, v.y, acc[n][1]);
+                acc[n][2] = fmaf(w1, v.x, acc[n][2]);
+                acc[n][3] = fmaf(w1, v.y, acc[n][3]);
+              }
+              continue;
+            }
             const __nv_bfloat16* vp = p.ve + (static_cast<long long>(s_b) + key) * p.ve_s0 +
                                       static_cast<long long>(kvh) * p.ve_s1 + 2 * j;
 #pragma unroll
@@ -1205,27 +1296,12 @@ const char* vsk_version(void) { return VSK_VERSION; }
 }  // extern "C"
 
 namespace vsk {
-// Shared body of the entry points; cm / mi select tree verify (both null: causal drafts).
-static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
-                      const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
-                      const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
-                      float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
-                      const vsk_tensor* mi) {
-  if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
-  if (!check_3d(o, "o_extend")) return 0;
-  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
-      o->shape[2] != ve->shape[2])
-    return fail("o_extend must be bf16 [B*l_ext, h_q, v_head_dim]");
-  if (!aligned(o->data, 4) || (o->stride[0] % 2) != 0 || (o->stride[1] % 2) != 0)
-    return fail("o_extend must be 4-byte aligned with even strides");
-  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return fail("k_scale and v_scale must be finite");
-
-  const long long B = qo->shape[0] - 1;
-  const long long h_q = q->shape[1], h_kv = ke->shape[1], D = q->shape[2];
-  const bool fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
+// Plans the CTA shape for these sizes, sizes and checks the workspace, fills
+// the plan-dependent fields of p and launches the kernel.
+static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   Plan pl;
-  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl)) return 0;
-
+  if (!make_plan(h_q, h_kv, D, L, fp8, pl)) return 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
@@ -1251,6 +1327,44 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
     return fail("workspace must be 256-byte aligned");
   }
 
+  p.B = static_cast<int>(B);
+  p.L = static_cast<int>(L);
+  p.gq = pl.gq;
+  p.R = pl.R;
+  p.HC = pl.HC;
+  p.MT = pl.MT;
+  p.n_hg = pl.n_hg;
+  p.nwc = pl.nwc;
+  p.nst = pl.nst;
+  p.ring_off = pl.ring_off;
+  p.warp_bytes = pl.warp_bytes;
+  p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
+  p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
+  p.po = reinterpret_cast<float*>(ws + wl.o_off);
+  void* args[] = {&p};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads), args,
+                       pl.smem, st);
+  if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
+  return 1;
+}
+
+// Shared body of the entry points; cm / mi select tree verify (both null: causal drafts).
+static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                      const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                      const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                      float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
+                      const vsk_tensor* mi) {
+  if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
+  if (!check_3d(o, "o_extend")) return 0;
+  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
+      o->shape[2] != ve->shape[2])
+    return fail("o_extend must be bf16 [B*l_ext, h_q, v_head_dim]");
+  if (!aligned(o->data, 4) || (o->stride[0] % 2) != 0 || (o->stride[1] % 2) != 0)
+    return fail("o_extend must be 4-byte aligned with even strides");
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return fail("k_scale and v_scale must be finite");
+
   Params p;
   memset(&p, 0, sizeof p);
   p.q = static_cast<const __nv_bfloat16*>(q->data);
@@ -1266,11 +1380,12 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
   p.o_s0 = o->stride[0];
   p.o_s1 = o->stride[1];
   p.kb = static_cast<const unsigned char*>(kb->data);
-  p.kb_s0 = kb->stride[0] * pl.ek;
-  p.kb_s1 = kb->stride[1] * pl.ek;
+  const int ek = kb->dtype == VSK_DTYPE_FP8E4M3 ? 1 : 2;
+  p.kb_s0 = kb->stride[0] * ek;
+  p.kb_s1 = kb->stride[1] * ek;
   p.vb = static_cast<const unsigned char*>(vb->data);
-  p.vb_s0 = vb->stride[0] * pl.ek;
-  p.vb_s1 = vb->stride[1] * pl.ek;
+  p.vb_s0 = vb->stride[0] * ek;
+  p.vb_s1 = vb->stride[1] * ek;
   p.qo = static_cast<const int*>(qo->data);
   p.kvp = static_cast<const int*>(kvp->data);
   p.kvi = kvi->data;
@@ -1278,43 +1393,133 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
   p.n_idx = kvi->shape[0];
   p.pool = kb->shape[0];
   p.n_rows = q->shape[0];
-  p.B = static_cast<int>(B);
-  p.L = static_cast<int>(max_len_extend);
-  p.gq = pl.gq;
-  p.R = pl.R;
-  p.HC = pl.HC;
-  p.MT = pl.MT;
-  p.n_hg = pl.n_hg;
-  p.nwc = pl.nwc;
-  p.nst = pl.nst;
-  p.ring_off = pl.ring_off;
-  p.warp_bytes = pl.warp_bytes;
+  const long long D = q->shape[2];
   const double sm = (sm_scale > 0.f && std::isfinite(sm_scale)) ? static_cast<double>(sm_scale)
                                                                  : 1.0 / std::sqrt(static_cast<double>(D));
   const double log2e = 1.4426950408889634;
   p.scale2 = static_cast<float>(sm * static_cast<double>(k_scale) * log2e);
   p.dscale2 = static_cast<float>(sm * log2e);
+  p.dvs = 1.f;
   p.v_scale = v_scale;
-  p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
   p.cmask = cm ? static_cast<const unsigned char*>(cm->data) : nullptr;
   p.mindptr = mi ? mi->data : nullptr;
   p.mindptr64 = (mi && mi->dtype == VSK_DTYPE_I64) ? 1 : 0;
   p.n_mask = cm ? cm->shape[0] : 0;
   if (p.cmask == nullptr) p.mindptr = nullptr;
-  p.err = reinterpret_cast<unsigned*>(ws);
-  p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
-  p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
-  p.po = reinterpret_cast<float*>(ws + wl.o_off);
+  return launch_with_plan(p, qo->shape[0] - 1, q->shape[1], ke->shape[1], D, max_len_extend,
+                          kb->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes, stream);
+}
 
-  void* args[] = {&p};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads), args,
-                       pl.smem, st);
-  if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
-  return 1;
+bool check_2d(const vsk_tensor* t, const char* name) {
+  if (!t) return fail("%s is NULL", name);
+  if (t->ndim != 2) return fail("%s must be 2-d (got ndim %d)", name, t->ndim);
+  if (t->shape[0] < 0 || t->shape[1] < 0) return fail("%s has a negative extent", name);
+  if (t->shape[0] > 0 && t->shape[1] > 1 && t->stride[1] != 1) return fail("%s: rows must be contiguous", name);
+  if (t->shape[0] * t->shape[1] > 0 && !t->data) return fail("%s: NULL data", name);
+  return true;
+}
+
+// Drafts already written to a paged cache (the unified verify of the
+// "aiter_backend.py" page): sequence b's cache position t lives in pool row
+// block_table[b][t / page_size] * page_size + t % page_size, its prefix is
+// positions [0, seq_lens[b]) and its drafts [seq_lens[b], seq_lens[b] + L).
+static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor* kc, const vsk_tensor* vc,
+                     const vsk_tensor* bt, const vsk_tensor* sl, int64_t page_size, int64_t mle, float k_scale,
+                     float v_scale, float sm_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!check_3d(q, "q") || !check_3d(o, "o") || !check_3d(kc, "k_cache") || !check_3d(vc, "v_cache")) return 0;
+  if (!check_2d(bt, "block_table") || !check_1d(sl, "seq_lens")) return 0;
+  if (page_size < 1) return fail("page_size must be >= 1");
+  if (mle < 1) return fail("max_len_extend must be >= 1");
+  const long long bs = sl->shape[0];
+  if (bs < 1) return fail("batch size must be >= 1");
+  if (bt->shape[0] != bs) return fail("block_table must have one row per sequence (B = %lld)", bs);
+  if (bt->shape[1] < 1) return fail("block_table has no columns");
+  if (bt->shape[1] * page_size > INT_MAX) return fail("block_table columns x page_size exceeds 2^31 - 1");
+  if (bt->shape[1] * page_size < mle) return fail("block_table covers fewer than max_len_extend positions");
+  if (bt->dtype != VSK_DTYPE_I32 || sl->dtype != VSK_DTYPE_I32) return fail("block_table and seq_lens must be int32");
+  if (q->shape[0] != bs * mle)
+    return fail("ragged extend: q has %lld rows, expected B*max_len_extend = %lld", q->shape[0], bs * mle);
+  const long long h_q = q->shape[1], h_kv = kc->shape[1], D = q->shape[2];
+  if (h_kv == 0 || h_q % h_kv != 0) return fail("h_q (%lld) is not a multiple of h_kv (%lld)", h_q, h_kv);
+  if (vc->shape[1] != h_kv) return fail("KV head count mismatch between k_cache and v_cache");
+  if (kc->shape[2] != D) return fail("head_dim mismatch between q and k_cache");
+  if (vc->shape[2] != D) return fail("v_head_dim (%lld) != head_dim (%lld) is not built", vc->shape[2], D);
+  if (D != 64 && D != 128 && D != 256) return fail("head_dim %lld not in {64, 128, 256}", D);
+  if (kc->shape[0] != vc->shape[0]) return fail("k_cache and v_cache pools differ in size");
+  if (kc->shape[0] % page_size != 0) return fail("cache rows (%lld) are not a whole number of pages", kc->shape[0]);
+  if (q->dtype != VSK_DTYPE_BF16) return fail("q must be bf16");
+  if (kc->dtype != vc->dtype || (kc->dtype != VSK_DTYPE_BF16 && kc->dtype != VSK_DTYPE_FP8E4M3))
+    return fail("k_cache and v_cache must both be bf16 or both fp8 e4m3");
+  const long long R = (h_q / h_kv) * mle;
+  const long long maxR = D > 128 ? 64 : 128;
+  if (R > maxR) return fail("(h_q/h_kv)*max_len_extend = %lld exceeds %lld", R, maxR);
+  const size_t ek = kc->dtype == VSK_DTYPE_BF16 ? 2 : 1;
+  for (const vsk_tensor* t : {kc, vc}) {
+    if (!aligned(t->data, 16) || (t->stride[0] * ek) % 16 != 0 || (t->stride[1] * ek) % 16 != 0)
+      return fail("K/V cache rows must be 16-byte aligned");
+  }
+  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != h_q || o->shape[2] != D)
+    return fail("o must be bf16 [B*l_ext, h_q, head_dim]");
+  for (const vsk_tensor* t : {q, o}) {
+    if (!aligned(t->data, 4) || (t->stride[0] % 2) != 0 || (t->stride[1] % 2) != 0)
+      return fail("q and o must be 4-byte aligned with even strides");
+  }
+  if (!aligned(bt->data, 4) || !aligned(sl->data, 4)) return fail("block_table and seq_lens must be 4-byte aligned");
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return fail("k_scale and v_scale must be finite");
+
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16*>(q->data);
+  p.q_s0 = q->stride[0];
+  p.q_s1 = q->stride[1];
+  p.o = static_cast<__nv_bfloat16*>(const_cast<void*>(o->data));
+  p.o_s0 = o->stride[0];
+  p.o_s1 = o->stride[1];
+  p.kb = static_cast<const unsigned char*>(kc->data);
+  p.kb_s0 = kc->stride[0] * static_cast<long long>(ek);
+  p.kb_s1 = kc->stride[1] * static_cast<long long>(ek);
+  p.vb = static_cast<const unsigned char*>(vc->data);
+  p.vb_s0 = vc->stride[0] * static_cast<long long>(ek);
+  p.vb_s1 = vc->stride[1] * static_cast<long long>(ek);
+  p.pool = kc->shape[0];
+  p.n_rows = q->shape[0];
+  p.paged = 1;
+  p.bt = static_cast<const int*>(bt->data);
+  p.bt_s0 = bt->stride[0];
+  p.bt_cols = static_cast<int>(bt->shape[1]);
+  p.page = static_cast<int>(page_size);
+  {
+    int l = 0;
+    while ((1LL << l) < page_size) ++l;
+    p.pg_l = l;
+    p.pg_m = static_cast<unsigned>(((1ULL << (32 + l)) + static_cast<unsigned long long>(page_size) - 1) /
+                                       static_cast<unsigned long long>(page_size) -
+                                   (1ULL << 32));
+  }
+  p.slens = static_cast<const int*>(sl->data);
+  const double sm = (sm_scale > 0.f && std::isfinite(sm_scale)) ? static_cast<double>(sm_scale)
+                                                                 : 1.0 / std::sqrt(static_cast<double>(D));
+  const double log2e = 1.4426950408889634;
+  // every cached key, drafts included, carries the cache's scales
+  p.scale2 = static_cast<float>(sm * static_cast<double>(k_scale) * log2e);
+  p.dscale2 = p.scale2;
+  p.dvs = v_scale;
+  p.v_scale = v_scale;
+  return launch_with_plan(p, bs, h_q, h_kv, D, mle, kc->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes,
+                          stream);
 }
 }  // namespace vsk
 
 extern "C" {
+
+int verify_splitkv_paged_fwd(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor* k_cache,
+                             const vsk_tensor* v_cache, const vsk_tensor* block_table, const vsk_tensor* seq_lens,
+                             int64_t page_size, int64_t max_len_extend, float k_scale, float v_scale, float sm_scale,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  return run_paged(q, o, k_cache, v_cache, block_table, seq_lens, page_size, max_len_extend, k_scale, v_scale,
+                   sm_scale, workspace, workspace_bytes, stream);
+}
 
 int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
                        const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,

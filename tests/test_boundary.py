@@ -179,3 +179,52 @@ def test_python_tree_path_needs_skip_prefix():
     ind = torch.tensor([0, 4 * 516, 8 * 516], dtype=torch.int64)
     assert vsk.verify_splitkv_fwd(a[0], a[1], a[2], o, a[3], a[4], a[5], a[6], a[7], mask, True, ind, a[11], 1.0, 1.0,
                                   skip_prefix_custom_mask=False) is False
+
+
+def _paged_inputs(**over):
+    spec = workloads.Spec("gate_paged", (100, 37), 4, 16, 2, 128, 128, page_size=16, seed=6)
+    p = workloads.make_problem(spec, "cpu", **over)
+    o = torch.empty(p["q"].shape, dtype=torch.bfloat16)
+    return dict(q=p["q"], o=o, kc=p["k_buffer"], vc=p["v_buffer"], bt=p["block_table"], sl=p["seq_lens"],
+                ps=16, mle=4)
+
+
+def _paged_call(a):
+    r = vsk.api._ref
+    return _native.lib().verify_splitkv_paged_fwd(r(a["q"]), r(a["o"]), r(a["kc"]), r(a["vc"]), r(a["bt"]),
+                                                  r(a["sl"]), a["ps"], a["mle"], 1.0, 1.0, 0.0, None, 0, None)
+
+
+@pytest.mark.parametrize("change,msg", [
+    (dict(ps=0), "page_size"),
+    (dict(mle=3), "ragged"),
+    (dict(bt="long"), "int32"),
+    (dict(sl="long"), "int32"),
+    (dict(bt="drop_row"), "one row per sequence"),
+    (dict(kc="drop_rows"), "k_cache and v_cache"),
+    (dict(kc="odd_pages", vc="odd_pages"), "whole number of pages"),
+    (dict(o="short"), "o must be"),
+    (dict(vc="fp8"), "both be bf16 or both fp8"),
+    (dict(bt="one_col", ps=2), "fewer than max_len_extend"),
+])
+def test_paged_entry_rejects_bad_arguments(change, msg):
+    a = _paged_inputs()
+    for k, v in change.items():
+        if v == "long":
+            a[k] = a[k].long()
+        elif v == "drop_row":
+            a[k] = a[k][:1]
+        elif v == "drop_rows":
+            a[k] = a[k][:-16]
+        elif v == "odd_pages":
+            a[k] = a[k][:-1]
+        elif v == "short":
+            a[k] = a[k][:, :, :64]
+        elif v == "fp8":
+            a[k] = a[k].to(torch.float8_e4m3fn)
+        elif v == "one_col":
+            a[k] = a[k][:, :1].contiguous()
+        else:
+            a[k] = v
+    assert _paged_call(a) == 0
+    assert msg in vsk.last_error(), vsk.last_error()

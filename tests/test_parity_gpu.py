@@ -333,3 +333,119 @@ def test_tree_bad_mask_indptr_is_flagged_not_read(vsk):
     causal = oracle_o({k: v for k, v in p.items() if k not in ("custom_mask", "mask_indptr")})
     check(o, causal, rows=slice(4, 8))              # sequence 1 fell back to causal drafts
     check(o, oracle_o(p), rows=slice(0, 4))         # sequence 0 kept its tree
+
+
+# ----------------------------------------------------------------- drafts already in a paged cache
+PAGED = [
+    workloads.Spec("paged_ps1", (0, 17, 300, 1024), 4, 16, 2, 128, 128, perm=True, page_size=1, pool_extra=33,
+                   seed=301),
+    workloads.Spec("paged_ps16_fp8", (700, 5, 90), 4, 32, 8, 128, 128, pool="e4m3", perm=True, page_size=16,
+                   k_scale=0.5, v_scale=0.25, seed=302),
+    workloads.Spec("paged_ps64_d256", (1000, 63, 64, 0), 6, 16, 2, 256, 256, perm=True, page_size=64,
+                   k_scale=1.5, v_scale=0.75, seed=303),
+    workloads.Spec("paged_decode_ps16", (2000, 1, 0, 513, 16), 1, 32, 8, 128, 128, perm=True, page_size=16,
+                   seed=304),
+    workloads.Spec("paged_ps32_d64_l8", (129, 4000), 8, 8, 1, 64, 64, pool="e4m3", perm=True, page_size=32,
+                   k_scale=2.0, v_scale=0.5, seed=305),
+    # page sizes that are not powers of two (the page division is a multiply-high)
+    workloads.Spec("paged_ps3", (1, 2, 3, 1000), 3, 16, 4, 128, 128, perm=True, page_size=3, seed=311),
+    workloads.Spec("paged_ps24_fp8", (23, 24, 25, 3000), 4, 8, 2, 128, 128, pool="e4m3", perm=True, page_size=24,
+                   k_scale=0.75, v_scale=1.25, seed=312),
+    workloads.Spec("paged_ps100_d64", (99, 100, 101, 1234), 5, 16, 8, 64, 64, perm=True, page_size=100, seed=313),
+]
+
+
+def run_paged(vsk, prob, o=None, **kw):
+    q = prob["q"]
+    if o is None:
+        o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=q.device)
+    vsk.verify_splitkv_paged_fwd(q, o, prob["k_buffer"], prob["v_buffer"], prob["block_table"], prob["seq_lens"],
+                                 prob["page_size"], prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
+                                 sm_scale=prob["sm_scale"], **kw)
+    torch.cuda.synchronize()
+    return o
+
+
+@pytest.mark.parametrize("spec", PAGED, ids=lambda s: s.name)
+def test_paged_drafts_match_oracle(vsk, spec):
+    p = gpu_problem(spec)
+    vsk.read_error_flags()
+    check(run_paged(vsk, p), oracle_o(p))
+    assert vsk.read_error_flags() == 0
+
+
+def test_paged_poisoned_pages(vsk):
+    spec = workloads.Spec("paged_poison", (40, 0, 129), 4, 8, 2, 128, 128, perm=True, page_size=16, pool_extra=200,
+                          poison=True, seed=306)
+    p = gpu_problem(spec)
+    check(run_paged(vsk, p), oracle_o(p))
+
+
+def test_paged_bf16_unit_scales_is_bitwise_the_flat_path(vsk):
+    """With a bf16 cache and unit scales the paged call and the flat call
+    (prefix through kv_indices, drafts gathered into k_extend / v_extend) see
+    the same keys in the same order and must agree bit for bit."""
+    spec = workloads.Spec("paged_vs_flat", (900, 3, 0, 2500), 4, 32, 8, 128, 128, perm=True, page_size=16, seed=307)
+    p = gpu_problem(spec)
+    a = run_paged(vsk, p)
+    b = run_gpu(vsk, p)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_paged_split_count_independence(vsk):
+    spec = workloads.Spec("paged_splits", (2000, 5, 777), 4, 16, 4, 128, 128, perm=True, page_size=8, seed=308)
+    p = gpu_problem(spec)
+    ref = oracle_o(p)
+    for n in (1, 7, 1000):
+        vsk.set_tuning(n, 16)
+        try:
+            o = run_paged(vsk, p)
+        finally:
+            vsk.set_tuning(0, 0)
+        check(o, ref)
+
+
+def test_paged_bad_page_and_length_are_flagged_not_read(vsk):
+    spec = workloads.Spec("paged_bad", (50, 60, 70), 2, 4, 1, 64, 64, page_size=16, seed=309)
+    p = gpu_problem(spec)
+    ref = oracle_o(p)
+    n_pages = p["k_buffer"].shape[0] // 16
+    bt = p["block_table"].clone()
+    bt[1, 1] = n_pages          # one past the cache: positions 16..31 of sequence 1
+    sl = p["seq_lens"].clone()
+    sl[2] = -5                  # sequence 2: negative length
+    vsk.read_error_flags()
+    o = run_paged(vsk, dict(p, block_table=bt, seq_lens=sl))
+    flags = vsk.read_error_flags()
+    assert flags & 1 and flags & 2
+    assert torch.isfinite(o.float()).all()
+    check(o, ref, rows=slice(0, 2))  # sequence 0 untouched
+    # sequence 1 equals the definition with positions 16..31 of its prefix removed
+    keep = torch.ones(60, dtype=torch.bool)
+    keep[16:32] = False
+    kvi = p["kv_indices"].cpu()
+    p3 = dict(p, kv_indices=torch.cat([kvi[:50], kvi[50:110][keep]]).cuda(),
+              kv_indptr=torch.tensor([0, 50, 94, 94], dtype=torch.int32, device="cuda"))
+    p3.pop("block_table")
+    check(o, oracle_o(p3), rows=slice(2, 4))
+
+
+def test_paged_cuda_graph_replay(vsk):
+    spec = workloads.Spec("paged_graph", (900, 50, 2048), 4, 32, 8, 128, 128, perm=True, page_size=16, seed=310)
+    p = gpu_problem(spec)
+    eager = run_paged(vsk, p)
+    ws = vsk.get_workspace("cuda", 3, 32, 8, 128, 128, 4)
+    o = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run_paged(vsk, p, o=o, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    o.fill_(0)
+    with torch.cuda.graph(g):
+        vsk.verify_splitkv_paged_fwd(p["q"], o, p["k_buffer"], p["v_buffer"], p["block_table"], p["seq_lens"], 16, 4,
+                                     sm_scale=p["sm_scale"], workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), eager.view(torch.int16))

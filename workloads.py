@@ -259,5 +259,11 @@ def algorithmic_bytes(prob: dict) -> int:
     e = prob["k_buffer"].element_size()
     idx = prob["kv_indices"].element_size()
     n_rows, h_q = q.shape[0], q.shape[1]
+    if prob.get("block_table") is not None:
+        # drafts come from the cache too; one page id per page and one length per sequence
+        ps, L = prob["page_size"], prob["max_len_extend"]
+        pages = sum(-(-(P + L) // ps) for P in prob["prefix_lens"])
+        return int((T + n_rows) * h_kv * (d + dv) * e + 4 * pages + 4 * len(prob["prefix_lens"])
+                   + 2 * n_rows * h_q * d + 2 * n_rows * h_q * dv)
     kv = T * h_kv * (d + dv) * e
     return int(kv + T * idx + 2 * n_rows * h_q * d + 2 * n_rows * h_kv * (d + dv) + 2 * n_rows * h_q * dv)
