@@ -90,6 +90,12 @@ def _bind(lib):
     lib.orc_decode_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
     lib.orc_decode_e4m3.restype = None
     lib.orc_decode_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    lib.orc_quantize.restype = None
+    lib.orc_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+    lib.orc_encode_e4m3.restype = None
+    lib.orc_encode_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    lib.orc_encode_bf16.restype = None
+    lib.orc_encode_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
     return lib
 
 
@@ -130,6 +136,47 @@ def decode_e4m3(codes: np.ndarray, lib=None) -> np.ndarray:
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     out = np.empty(codes.shape, dtype=np.float64)
     lib.orc_decode_e4m3(_ptr(codes), _ptr(out), codes.size)
+    return out
+
+
+def encode_e4m3(values: np.ndarray, lib=None) -> np.ndarray:
+    """e4m3 codes of binary32 values (nearest, ties to even, saturating)."""
+    lib = lib or load()
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib.orc_encode_e4m3(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def encode_bf16(values: np.ndarray, lib=None) -> np.ndarray:
+    """bf16 bit patterns of binary32 values (nearest, ties to even)."""
+    lib = lib or load()
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib.orc_encode_bf16(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def quantize(bits: np.ndarray, scale: float, pool_dtype: str, lib=None) -> np.ndarray:
+    """Cache codes of bf16 values (uint16 bit patterns) stored with a
+    dequantisation scale: the cache dtype's nearest value to x / scale
+    (binary32 quotient).  ``pool_dtype`` "e4m3" gives uint8 codes, "bf16"
+    uint16 bit patterns."""
+    lib = lib or load()
+    src = np.ascontiguousarray(bits, dtype=np.uint16)
+    e4m3 = pool_dtype == "e4m3"
+    out = np.empty(src.shape, dtype=np.uint8 if e4m3 else np.uint16)
+    lib.orc_quantize(_ptr(src), src.size, float(scale), POOL_E4M3 if e4m3 else POOL_BF16, _ptr(out))
+    return out
+
+
+def write_rows(pool: np.ndarray, rows: np.ndarray, new_bits: np.ndarray, scale: float, pool_dtype: str,
+               lib=None) -> np.ndarray:
+    """A copy of ``pool`` [n, h_kv, d] with rows ``rows`` replaced by the
+    quantised ``new_bits`` [len(rows), h_kv, d] (the cache after a K or V
+    store of new tokens)."""
+    out = np.array(pool, copy=True)
+    out[np.asarray(rows, dtype=np.int64)] = quantize(new_bits, scale, pool_dtype, lib=lib)
     return out
 
 

@@ -48,6 +48,15 @@
  *     L_b are the drafts (row i sees drafts t <= i); every key is a cache
  *     entry, so k_scale and v_scale apply to the drafts too.
  *
+ * Writing new K/V rows into the cache (the draft K/V store that precedes
+ * unified verify on the "aiter_backend.py" page, where the bf16 -> fp8 cast
+ * and the paged write are one kernel, given the cache's k_scale / v_scale as
+ * descales): the stored code of a bf16 value x is the cache dtype's
+ * round-to-nearest-even of the binary32 quotient x / scale; an e4m3 cache
+ * saturates finite quotients beyond +-448 to +-448 (the saturating fp8 cast
+ * such kernels use), a NaN stays NaN.  Reading it back multiplies by the same
+ * scale, so a write followed by paged verify sees the dequantised value.
+ *
  * Debug outputs (optional) split the same sum into its prefix part and its
  * draft part: o_prefix / lse_prefix over the prefix keys only (lse = -inf and
  * o = 0 when P_b = 0) and o_draft / lse_draft over the causal drafts only.
@@ -314,4 +323,74 @@ void orc_decode_bf16(const uint16_t* in, double* out, int64_t n) {
 
 void orc_decode_e4m3(const uint8_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_to_f64(in[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * Quantised store of new K/V values (see the header comment).
+ * ------------------------------------------------------------------------- */
+
+/* e4m3 "fn" code nearest to y, ties to the code with an even mantissa, finite
+   values beyond the largest finite code (448) saturating to it; NaN -> the
+   NaN code.  Written as a search over the 127 non-negative finite codes,
+   whose values increase with the code.                                       */
+static uint8_t encode_e4m3_satfinite(float y) {
+  if (isnan(y)) return 0x7F;
+  const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  const double a = fabs((double)y);
+  uint8_t best = 0;
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double lo = orc_e4m3_to_f64((uint8_t)(c - 1)), hi = orc_e4m3_to_f64((uint8_t)c);
+    if (a >= hi) {
+      best = (uint8_t)c;  /* at or above this code: keep climbing */
+      continue;
+    }
+    /* lo <= a < hi: nearer of the two, a tie goes to the even code */
+    const double dl = a - lo, dh = hi - a;
+    if (dh < dl || (dh == dl && (c & 1) == 0)) best = (uint8_t)c;
+    else best = (uint8_t)(c - 1);
+    break;
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* bf16 nearest to y (ties to even), i.e. the binary32 values whose low 16
+   bits are zero; beyond the largest finite bf16 plus half an ulp -> infinity. */
+static uint16_t encode_bf16_rne(float y) {
+  uint32_t w;
+  memcpy(&w, &y, sizeof w);
+  if (isnan(y)) return (uint16_t)((w >> 16) | 0x40);
+  const uint32_t lo = w & 0xFFFF0000u;
+  if (lo == w) return (uint16_t)(w >> 16);
+  const uint32_t hi = lo + 0x10000u;  /* next value away from zero */
+  float flo, fhi;
+  memcpy(&flo, &lo, sizeof flo);
+  memcpy(&fhi, &hi, sizeof fhi);
+  const double vy = fabs((double)y), vlo = fabs((double)flo);
+  /* past the largest finite value the next step is 2^128 (infinity) */
+  const double vhi = isinf(fhi) ? ldexp(1.0, 128) : fabs((double)fhi);
+  const double dl = vy - vlo, dh = vhi - vy;
+  if (dh < dl || (dh == dl && ((hi >> 16) & 1u) == 0)) return (uint16_t)(hi >> 16);
+  return (uint16_t)(lo >> 16);
+}
+
+/* dst[i] = code of bf16 src[i] / scale in the cache dtype (ORC_POOL_BF16:
+   uint16 bits, ORC_POOL_E4M3: uint8 codes); the quotient is binary32.       */
+void orc_quantize(const uint16_t* src, int64_t n, float scale, int dst_dtype, void* dst) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float x = (float)orc_bf16_to_f64(src[i]);
+    const float y = x / scale;
+    if (dst_dtype == ORC_POOL_E4M3)
+      ((uint8_t*)dst)[i] = encode_e4m3_satfinite(y);
+    else
+      ((uint16_t*)dst)[i] = encode_bf16_rne(y);
+  }
+}
+
+/* Element-wise encoders alone (binary32 in), for the tests. */
+void orc_encode_e4m3(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = encode_e4m3_satfinite(in[i]);
+}
+
+void orc_encode_bf16(const float* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = encode_bf16_rne(in[i]);
 }

@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import workloads
-from test_oracle_pins import _golden_cases, _sdpa_reference, run_golden
+from test_oracle_pins import _golden_cases, _sdpa_reference, quantize_pins, run_golden
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "verify_oracle.c")
 
@@ -30,6 +30,10 @@ MUTANTS = {
     "softmax_sign": ("exp(score[j] - mx)", "exp(mx - score[j])"),
     "pool_strides_transposed": ("loc * p->kp_s0 + kvh * p->kp_s1", "loc * p->kp_s1 + kvh * p->kp_s0"),
     "draft_value_row": ("p->v_ext[(s_b + t) * p->ve_s0", "p->v_ext[(s_b + 0) * p->ve_s0"),
+    "store_multiplies_scale": ("const float y = x / scale;", "const float y = x * scale;"),
+    "e4m3_ties_away": ("(dh == dl && (c & 1) == 0)", "(dh == dl)"),
+    "e4m3_sign_dropped": ("const uint8_t sign = signbit(y) ? 0x80 : 0x00;", "const uint8_t sign = 0x00;"),
+    "bf16_truncates": ("if (dh < dl || (dh == dl && ((hi >> 16) & 1u) == 0)) return (uint16_t)(hi >> 16);", ""),
 }
 
 
@@ -45,6 +49,10 @@ def _build_mutant(name, tmp_path):
 
 
 def _detected(lib):
+    try:
+        quantize_pins(lib)
+    except AssertionError:
+        return True
     for case in _golden_cases():
         fn, pd = case.values
         try:

@@ -432,3 +432,87 @@ def test_paged_poisoned_pages_are_never_read():
     spec = workloads.Spec("paged_poison", (50, 9), 4, 4, 1, 64, 64, perm=True, page_size=4, pool_extra=64,
                           poison=True, seed=55)
     assert np.isfinite(_run(workloads.make_problem(spec, "cpu"))["o"]).all()
+
+
+# ---------------------------------------------------------------- quantised store of new K/V rows
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _e4m3_midpoints():
+    """Every value halfway between two adjacent non-negative finite e4m3 codes."""
+    vals = np.array([oracle.decode_e4m3(np.array([c], dtype=np.uint8))[0] for c in range(0x7F)])
+    return (vals[:-1] + vals[1:]) / 2
+
+
+def quantize_pins(lib=None):
+    """Every check of the quantised store; raises AssertionError on a miss.
+    Pinned to: the e4m3 and bf16 format definitions (round trip of every
+    code, the tie rule, saturation) and torch's own round-to-nearest-even
+    float8 / bfloat16 casts (a library routine the oracle does not use)."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.decode_e4m3(codes, lib=lib)
+    finite = ~np.isnan(vals)
+    # 1. decode -> store at scale 1 returns every finite code (both zeros included)
+    rt = oracle.quantize(_bf16_bits(torch.tensor(vals[finite])), 1.0, "e4m3", lib=lib)
+    np.testing.assert_array_equal(rt, codes[finite])
+    # 2. torch's cast on in-range binary32 values: random magnitudes and every midpoint, both signs
+    g = torch.Generator().manual_seed(71)
+    mag = torch.exp2(torch.empty(20000).uniform_(-12, 8.85, generator=g))
+    mid = torch.tensor(_e4m3_midpoints(), dtype=torch.float32)
+    v = torch.cat([mag, -mag, mid, -mid, torch.tensor([0.0, -0.0, 448.0, -448.0, 463.0])])
+    want = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.encode_e4m3(v.numpy(), lib=lib), want)
+    # 3. ties go to the even code; beyond 448 (and infinity) saturates; NaN stays NaN
+    got = oracle.encode_e4m3(np.array([1.0625, 1.1875, 3 * 2.0 ** -10, 2.0 ** -10, 464.0, 465.0, 1e30,
+                                       -1e30, np.inf, np.nan], dtype=np.float32), lib=lib)
+    assert got.tolist() == [0x38, 0x3A, 0x02, 0x00, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0x7F]
+    # 4. bf16 store: torch's cast on random binary32 values and exact ties
+    f = torch.randn(20000, generator=g) * torch.exp2(torch.empty(20000).uniform_(-30, 30, generator=g))
+    w = torch.randint(0, 2 ** 16, (4000,), generator=g, dtype=torch.int32) << 16 | 0x8000
+    ties = w.view(torch.float32)
+    ties = ties[torch.isfinite(ties)]
+    for x in (f, ties):
+        want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(oracle.encode_bf16(x.numpy(), lib=lib), want)
+    # 5. the scale divides, in binary32, before the cast (both cache dtypes)
+    x = torch.randn(4096, generator=g).to(torch.bfloat16)
+    for s in (0.5, 0.75, 2.0, 1.3):
+        q = (x.float() / s)
+        keep = q.abs() < 464
+        want8 = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        got8 = oracle.quantize(_bf16_bits(x), s, "e4m3", lib=lib)
+        np.testing.assert_array_equal(got8[keep.numpy()], want8[keep.numpy()])
+        want16 = q.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(oracle.quantize(_bf16_bits(x), s, "bf16", lib=lib), want16)
+
+
+def test_quantised_store_pins():
+    quantize_pins()
+
+
+def test_store_then_read_is_within_half_a_step():
+    """decode(store(x, s)) * s is the nearest representable value: relative
+    error at most 2^-4 for normal e4m3 values, 2^-8 for bf16."""
+    g = torch.Generator().manual_seed(72)
+    x = (torch.randn(8192, generator=g) * 4).to(torch.bfloat16)
+    xd = x.double().numpy()
+    for s in (0.25, 1.0, 3.0):
+        back = oracle.decode_e4m3(oracle.quantize(_bf16_bits(x), s, "e4m3")) * s
+        normal = np.abs(xd / s) >= 2.0 ** -6
+        assert np.all(np.abs(back - xd)[normal] <= 2.0 ** -4 * np.abs(xd)[normal] + 1e-300)
+        back16 = oracle.decode_bf16(oracle.quantize(_bf16_bits(x), s, "bf16")) * s
+        assert np.all(np.abs(back16 - xd) <= 2.0 ** -8 * np.abs(xd))
+
+
+def test_write_rows_replaces_only_the_named_rows():
+    g = torch.Generator().manual_seed(73)
+    pool = _bf16_bits(torch.randn(10, 2, 8, generator=g))
+    new = _bf16_bits(torch.randn(3, 2, 8, generator=g))
+    out = oracle.write_rows(pool, [7, 1, 4], new, 1.0, "bf16")
+    np.testing.assert_array_equal(out[[7, 1, 4]], new)
+    keep = [0, 2, 3, 5, 6, 8, 9]
+    np.testing.assert_array_equal(out[keep], pool[keep])
+    pool8 = np.zeros((10, 2, 8), dtype=np.uint8)
+    out8 = oracle.write_rows(pool8, [2, 9, 0], new, 0.5, "e4m3")
+    np.testing.assert_array_equal(out8[[2, 9, 0]], oracle.quantize(new, 0.5, "e4m3"))
