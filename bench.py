@@ -87,6 +87,11 @@ WORKLOADS = {
     # the same batch with the drafts already in a 16-token-page cache
     # (verify_splitkv_paged_fwd)
     "serving_paged": workloads.replace(workloads.SERVING, name="serving_paged16_b64_p8k_32k", page_size=16),
+    # the head_dim 256 and fp8-pool shapes at the serving batch and length mix
+    "d256_long": workloads.Spec("d256_b64_p8k_32k", None, 4, 16, 2, 256, 256, perm=True, batch=64,
+                                len_range=(8192, 32768), seed=1239),
+    "fp8_long": workloads.Spec("fp8_b64_p8k_32k", None, 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
+                               v_scale=0.25, batch=64, len_range=(8192, 32768), seed=1240),
 }
 
 

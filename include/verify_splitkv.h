@@ -172,6 +172,50 @@ int verify_splitkv_paged_fwd(const vsk_tensor* q, const vsk_tensor* o,
                              float v_scale, float sm_scale, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* verify_splitkv_fwd that also stores the new draft K/V into the cache in
+ * the same launch (the draft K/V store that precedes attention on the
+ * "aiter_backend.py" page, where the bf16 -> fp8 cast and the cache write are
+ * one kernel).  Row t of sequence b (k_extend / v_extend row s_b + t) is
+ * written to pool row out_cache_loc[s_b + t] of k_buffer / v_buffer as the
+ * cache dtype's round-to-nearest-even of x / k_scale (x / v_scale for V) in
+ * binary32, e4m3 saturating to +-448.  The attention itself is exactly that
+ * of verify_splitkv_fwd: the drafts enter it as the fresh bf16 k_extend /
+ * v_extend rows, without scales.
+ *   out_cache_loc  [B*l_ext] int32 or int64 device array, one pool row per
+ *                  q_extend row; those rows must not be prefix rows of any
+ *                  sequence of the batch (they are written while the prefix
+ *                  is being read).  A value outside [0, pool) is not written
+ *                  and sets error bit 1.
+ *   k_scale, v_scale  must be > 0 (they divide).
+ * k_buffer / v_buffer are written through their (const-qualified) views.
+ * Everything else as verify_splitkv_fwd (is_causal is implied). */
+int verify_splitkv_write_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
+                             const vsk_tensor* v_extend, const vsk_tensor* o_extend,
+                             const vsk_tensor* k_buffer, const vsk_tensor* v_buffer,
+                             const vsk_tensor* qo_indptr, const vsk_tensor* kv_indptr,
+                             const vsk_tensor* kv_indices, const vsk_tensor* out_cache_loc,
+                             int64_t max_len_extend, float k_scale, float v_scale,
+                             float sm_scale, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* verify_splitkv_paged_fwd with the drafts' K/V stored by the same launch:
+ * k_new / v_new row b*l_ext + t ([B*l_ext, h_kv, D] bf16) goes to cache
+ * position seq_lens[b] + t of k_cache / v_cache (block-table addressing as in
+ * verify_splitkv_paged_fwd), stored as the cache dtype's round-to-nearest-even
+ * of x / k_scale (x / v_scale) in binary32, e4m3 saturating to +-448.  The
+ * attention then equals verify_splitkv_paged_fwd run after that store: the
+ * drafts enter it as stored (dequantised with k_scale / v_scale).  The draft
+ * positions must not be prefix positions of any sequence of the batch; a
+ * draft position whose page id is outside the cache is neither written nor
+ * attended and sets error bit 1.  k_scale, v_scale must be > 0. */
+int verify_splitkv_paged_write_fwd(const vsk_tensor* q, const vsk_tensor* k_new,
+                                   const vsk_tensor* v_new, const vsk_tensor* o,
+                                   const vsk_tensor* k_cache, const vsk_tensor* v_cache,
+                                   const vsk_tensor* block_table, const vsk_tensor* seq_lens,
+                                   int64_t page_size, int64_t max_len_extend, float k_scale,
+                                   float v_scale, float sm_scale, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Upper bound, in bytes, of the workspace verify_splitkv_fwd needs for any
  * batch of up to max_bs sequences with these head counts and sizes on the
  * CURRENT CUDA device (its SM count sets the number of persistent CTAs).

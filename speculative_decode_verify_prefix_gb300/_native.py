@@ -76,6 +76,13 @@ def _bind(lib):
     lib.verify_splitkv_paged_fwd.argtypes = [_P] * 6 + [ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                                                         ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
                                                         ctypes.c_void_p]
+    lib.verify_splitkv_write_fwd.restype = ctypes.c_int
+    lib.verify_splitkv_write_fwd.argtypes = [_P] * 10 + [ctypes.c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.verify_splitkv_paged_write_fwd.restype = ctypes.c_int
+    lib.verify_splitkv_paged_write_fwd.argtypes = [_P] * 8 + [ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                                              ctypes.c_float, ctypes.c_float, ctypes.c_void_p,
+                                                              ctypes.c_size_t, ctypes.c_void_p]
     lib.vsk_workspace_size.restype = ctypes.c_size_t
     lib.vsk_workspace_size.argtypes = [ctypes.c_int64] * 6
     lib.vsk_workspace_size_for_sms.restype = ctypes.c_size_t

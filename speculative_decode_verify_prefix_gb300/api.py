@@ -177,6 +177,53 @@ def verify_splitkv_paged_fwd(q, o, k_cache, v_cache, block_table, seq_lens, page
         raise ValueError("verify_splitkv_paged_fwd: " + _native.last_error())
 
 
+def verify_splitkv_write_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer, qo_indptr, kv_indptr,
+                             kv_indices, out_cache_loc, max_len_extend, k_scale=1.0, v_scale=1.0, sm_scale=None,
+                             max_bs=None, workspace=None, stream=None) -> None:
+    """``verify_splitkv_fwd`` (causal drafts) that also stores k_extend /
+    v_extend into rows ``out_cache_loc`` of k_buffer / v_buffer (quantised
+    as x / scale in the pool dtype), in the same launch.  Raises ValueError
+    when the library rejects the arguments."""
+    bs = qo_indptr.shape[0] - 1
+    mle = int(max_len_extend)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q_extend.device, mb, q_extend.shape[1], k_extend.shape[1], q_extend.shape[2],
+                                  v_extend.shape[2], mle)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_extend.device)
+    sm = 0.0 if sm_scale is None else float(sm_scale)
+    ok = _native.lib().verify_splitkv_write_fwd(
+        _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
+        _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), _ref(out_cache_loc), mle, _coerce(k_scale),
+        _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+        ctypes.c_void_p(stream.cuda_stream))
+    if not ok:
+        raise ValueError("verify_splitkv_write_fwd: " + _native.last_error())
+
+
+def verify_splitkv_paged_write_fwd(q, k_new, v_new, o, k_cache, v_cache, block_table, seq_lens, page_size,
+                                   max_len_extend, k_scale=1.0, v_scale=1.0, sm_scale=None, max_bs=None,
+                                   workspace=None, stream=None) -> None:
+    """``verify_splitkv_paged_fwd`` that first stores the drafts' k_new /
+    v_new ([B*l_ext, h_kv, D] bf16) into cache positions seq_lens[b] + t, in
+    the same launch; the attention uses the stored values."""
+    bs = seq_lens.shape[0]
+    mle = int(max_len_extend)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sm = 0.0 if sm_scale is None else float(sm_scale)
+    ok = _native.lib().verify_splitkv_paged_write_fwd(
+        _ref(q), _ref(k_new), _ref(v_new), _ref(o), _ref(k_cache), _ref(v_cache), _ref(block_table), _ref(seq_lens),
+        int(page_size), mle, _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if not ok:
+        raise ValueError("verify_splitkv_paged_write_fwd: " + _native.last_error())
+
+
 def read_error_flags(workspace=None, stream=None) -> int:
     """Device error word of a workspace (synchronises; for tests/debugging)."""
     if workspace is None:

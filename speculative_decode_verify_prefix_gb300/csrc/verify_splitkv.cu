@@ -90,6 +90,15 @@ struct Params {
   unsigned pg_m;  // division by page: t / page == (umulhi(t, pg_m) + t) >> pg_l for 0 <= t < 2^31
   int pg_l;
   const int* slens;
+  // fused store of the new draft K/V (ke / ve) into the cache: 0 none,
+  // 1 rows out_cache_loc[s_b + t], 2 paged positions P + t (attention then
+  // uses the stored, dequantised values)
+  int wmode;
+  const void* ocl;
+  int ocl64;
+  unsigned char* kw;  // the same caches as kb / vb, writable
+  unsigned char* vw;
+  float kq, vq;       // dequantisation scales the stored codes are divided by
   long long w_min;
   const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
   const void* mindptr;
@@ -202,6 +211,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(unsigned short two) {
   __half2 hv = *reinterpret_cast<__half2*>(&h);
   float2 f = __half22float2(hv);
   return pack_bf16(f.x, f.y);
+}
+
+// Cache code of two values stored with dequantisation scale sc: the nearest
+// e4m3 (saturating) / bf16 value of the binary32 quotient x / sc.
+__device__ __forceinline__ unsigned short store_e4m3x2(float a, float b, float sc) {
+  const unsigned lo = __nv_cvt_float_to_fp8(__fdiv_rn(a, sc), __NV_SATFINITE, __NV_E4M3);
+  const unsigned hi = __nv_cvt_float_to_fp8(__fdiv_rn(b, sc), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<unsigned short>(lo | (hi << 8));
+}
+__device__ __forceinline__ uint32_t store_bf16x2(float a, float b, float sc) {
+  return pack_bf16(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
 }
 
 // ---------------------------------------------------------------------------
@@ -834,11 +854,67 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       };
 #pragma unroll 1
       for (int td = 0; td * 8 < p.L; ++td) {
+        // fused store (paged): quantise this tile's new draft K and V rows
+        // once, store the codes into the cache (warp mt == 0 of the head) and
+        // keep the dequantised values in the warp's idle ring, where the
+        // fragment loads below read them
+        unsigned char* stK = ring;
+        unsigned char* stV = ring + 8 * D * 2;
+        if (p.wmode == 2) {
+          constexpr int PR = D / 2;  // bf16 pairs per row
+#pragma unroll 1
+          for (int idx = lane; idx < 8 * PR; idx += 32) {
+            const int kl = idx / PR, c = (idx % PR) * 2;
+            const int key = td * 8 + kl;
+            if (key >= p.L) continue;
+            const long long row = paged_row(p, sg.b, sg.P + key);
+            if (row < 0) continue;
+            const long long src = static_cast<long long>(s_b) + key;
+            const float2 xk = unpack_bf16(ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + c));
+            const float2 xv = unpack_bf16(ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c));
+            unsigned char* kd = p.kw + row * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+            unsigned char* vd = p.vw + row * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+            uint32_t dk, dv;
+            if constexpr (FP8) {
+              const unsigned short ck = store_e4m3x2(xk.x, xk.y, p.kq);
+              const unsigned short cv = store_e4m3x2(xv.x, xv.y, p.vq);
+              dk = e4m3x2_to_bf16x2(ck);
+              dv = e4m3x2_to_bf16x2(cv);
+              if (mt == 0) {
+                *reinterpret_cast<unsigned short*>(kd + c) = ck;
+                *reinterpret_cast<unsigned short*>(vd + c) = cv;
+              }
+            } else {
+              dk = store_bf16x2(xk.x, xk.y, p.kq);
+              dv = store_bf16x2(xv.x, xv.y, p.vq);
+              if (mt == 0) {
+                *reinterpret_cast<uint32_t*>(kd + c * 2) = dk;
+                *reinterpret_cast<uint32_t*>(vd + c * 2) = dv;
+              }
+            }
+            *reinterpret_cast<uint32_t*>(stK + (kl * D + c) * 2) = dk;
+            *reinterpret_cast<uint32_t*>(stV + (kl * D + c) * 2) = dv;
+          }
+          __syncwarp();
+        }
         float sd[4] = {0.f, 0.f, 0.f, 0.f};
         const int tkey = td * 8 + g;  // key whose K row this lane supplies
         bool kv = tkey < p.L;
         unsigned kvm = 0xFFFFFFFFu;  // lane (g, 0) bit set: key td*8+g has a valid row
-        if (p.paged) {
+        if (p.wmode == 2) {
+          // the new drafts as stored (staged above)
+          const long long krow = kv ? paged_row(p, sg.b, sg.P + tkey) : -1;
+          if (tkey < p.L && krow < 0) atomicOr(p.err, kErrBadIndex);
+          kv = krow >= 0;
+          kvm = __ballot_sync(0xffffffffu, kv);
+          const unsigned char* kr = stK + g * D * 2;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t b0 = kv ? *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 2 * j) * 2) : 0u;
+            const uint32_t b1 = kv ? *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2) : 0u;
+            mma_bf16(sd, qf[kk], b0, b1);
+          }
+        } else if (p.paged) {
           // drafts are cache positions P + t, dequantised like the prefix
           const long long krow = kv ? paged_row(p, sg.b, sg.P + tkey) : -1;
           if (tkey < p.L && krow < 0) atomicOr(p.err, kErrBadIndex);
@@ -867,6 +943,25 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             const uint32_t b0 = kv ? ld_u32(kp + kk * 16 + 2 * j) : 0u;
             const uint32_t b1 = kv ? ld_u32(kp + kk * 16 + 8 + 2 * j) : 0u;
             mma_bf16(sd, qf[kk], b0, b1);
+          }
+          if (p.wmode == 1 && mt == 0 && kv) {
+            // side store of the fresh drafts into rows out_cache_loc[s_b + t]
+            const long long dst = p.ocl64 ? static_cast<const long long*>(p.ocl)[s_b + tkey]
+                                          : static_cast<long long>(static_cast<const int*>(p.ocl)[s_b + tkey]);
+            if (dst >= 0 && dst < p.pool) {
+              unsigned char* kr = p.kw + dst * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+#pragma unroll 1
+              for (int c2 = 0; c2 < 2 * KS; ++c2) {
+                const int c = c2 * 8 + 2 * j;
+                const float2 x = unpack_bf16(ld_u32(kp + c));
+                if constexpr (FP8)
+                  *reinterpret_cast<unsigned short*>(kr + c) = store_e4m3x2(x.x, x.y, p.kq);
+                else
+                  *reinterpret_cast<uint32_t*>(kr + c * 2) = store_bf16x2(x.x, x.y, p.kq);
+              }
+            } else if (j == 0) {
+              atomicOr(p.err, kErrBadIndex);
+            }
           }
         }
 #pragma unroll
@@ -907,6 +1002,19 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             if (key >= p.L) continue;  // uniform across the warp
             const float w0 = __shfl_sync(0xffffffffu, pd[e], g * 4 + js) * p.dvs;
             const float w1 = __shfl_sync(0xffffffffu, pd[2 + e], g * 4 + js) * p.dvs;
+            if (p.wmode == 2) {
+              if (paged_row(p, sg.b, sg.P + key) < 0) continue;  // uniform; its weight is 0
+              const unsigned char* vr = stV + ((key - td * 8) * D + 2 * j) * 2;
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+                const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(vr + n * 16));
+                acc[n][0] = fmaf(w0, v.x, acc[n][0]);
+                acc[n][1] = fmaf(w0, v.y, acc[n][1]);
+                acc[n][2] = fmaf(w1, v.x, acc[n][2]);
+                acc[n][3] = fmaf(w1, v.y, acc[n][3]);
+              }
+              continue;
+            }
             if (p.paged) {
               const long long vrow = paged_row(p, sg.b, sg.P + key);  // uniform across the warp
               if (vrow < 0) continue;                                   // its weight is 0: never read
@@ -928,6 +1036,13 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             }
             const __nv_bfloat16* vp = p.ve + (static_cast<long long>(s_b) + key) * p.ve_s0 +
                                       static_cast<long long>(kvh) * p.ve_s1 + 2 * j;
+            long long vdst = -1;
+            if (p.wmode == 1 && mt == 0 && g == 0) {
+              const long long d = p.ocl64 ? static_cast<const long long*>(p.ocl)[s_b + key]
+                                          : static_cast<long long>(static_cast<const int*>(p.ocl)[s_b + key]);
+              vdst = (d >= 0 && d < p.pool) ? d : -1;  // an out-of-range row is flagged by the K store
+            }
+            unsigned char* vr = p.vw + (vdst >= 0 ? vdst : 0) * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
               const float2 v = unpack_bf16(ld_u32(vp + n * 8));
@@ -935,6 +1050,16 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
               acc[n][1] = fmaf(w0, v.y, acc[n][1]);
               acc[n][2] = fmaf(w1, v.x, acc[n][2]);
               acc[n][3] = fmaf(w1, v.y, acc[n][3]);
+            }
+            if (vdst >= 0) {
+#pragma unroll 1
+              for (int n = 0; n < NT; ++n) {
+                const float2 v = unpack_bf16(ld_u32(vp + n * 8));
+                if constexpr (FP8)
+                  *reinterpret_cast<unsigned short*>(vr + n * 8 + 2 * j) = store_e4m3x2(v.x, v.y, p.vq);
+                else
+                  *reinterpret_cast<uint32_t*>(vr + (n * 8 + 2 * j) * 2) = store_bf16x2(v.x, v.y, p.vq);
+              }
             }
           }
         }
@@ -1355,7 +1480,7 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
                       const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
                       const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
                       float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
-                      const vsk_tensor* mi) {
+                      const vsk_tensor* mi, const vsk_tensor* ocl = nullptr) {
   if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
   if (!check_3d(o, "o_extend")) return 0;
   if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
@@ -1406,6 +1531,19 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
   p.mindptr64 = (mi && mi->dtype == VSK_DTYPE_I64) ? 1 : 0;
   p.n_mask = cm ? cm->shape[0] : 0;
   if (p.cmask == nullptr) p.mindptr = nullptr;
+  if (ocl) {
+    if (!check_1d(ocl, "out_cache_loc")) return 0;
+    if (ocl->dtype != VSK_DTYPE_I32 && ocl->dtype != VSK_DTYPE_I64) return fail("out_cache_loc must be int32 or int64");
+    if (ocl->shape[0] != q->shape[0]) return fail("out_cache_loc must have one entry per q_extend row");
+    if (!(k_scale > 0.f) || !(v_scale > 0.f)) return fail("storing into the cache needs k_scale > 0 and v_scale > 0");
+    p.wmode = 1;
+    p.ocl = ocl->data;
+    p.ocl64 = ocl->dtype == VSK_DTYPE_I64;
+    p.kw = static_cast<unsigned char*>(const_cast<void*>(kb->data));
+    p.vw = static_cast<unsigned char*>(const_cast<void*>(vb->data));
+    p.kq = k_scale;
+    p.vq = v_scale;
+  }
   return launch_with_plan(p, qo->shape[0] - 1, q->shape[1], ke->shape[1], D, max_len_extend,
                           kb->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes, stream);
 }
@@ -1425,7 +1563,8 @@ bool check_2d(const vsk_tensor* t, const char* name) {
 // positions [0, seq_lens[b]) and its drafts [seq_lens[b], seq_lens[b] + L).
 static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor* kc, const vsk_tensor* vc,
                      const vsk_tensor* bt, const vsk_tensor* sl, int64_t page_size, int64_t mle, float k_scale,
-                     float v_scale, float sm_scale, void* workspace, size_t workspace_bytes, void* stream) {
+                     float v_scale, float sm_scale, void* workspace, size_t workspace_bytes, void* stream,
+                     const vsk_tensor* k_new = nullptr, const vsk_tensor* v_new = nullptr) {
   if (!check_3d(q, "q") || !check_3d(o, "o") || !check_3d(kc, "k_cache") || !check_3d(vc, "v_cache")) return 0;
   if (!check_2d(bt, "block_table") || !check_1d(sl, "seq_lens")) return 0;
   if (page_size < 1) return fail("page_size must be >= 1");
@@ -1505,6 +1644,29 @@ static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor*
   p.dscale2 = p.scale2;
   p.dvs = v_scale;
   p.v_scale = v_scale;
+  if (k_new || v_new) {
+    if (!check_3d(k_new, "k_new") || !check_3d(v_new, "v_new")) return 0;
+    if (k_new->dtype != VSK_DTYPE_BF16 || v_new->dtype != VSK_DTYPE_BF16) return fail("k_new and v_new must be bf16");
+    if (k_new->shape[0] != q->shape[0] || v_new->shape[0] != q->shape[0] || k_new->shape[1] != h_kv ||
+        v_new->shape[1] != h_kv || k_new->shape[2] != D || v_new->shape[2] != D)
+      return fail("k_new / v_new must be [B*l_ext, h_kv, head_dim]");
+    for (const vsk_tensor* t : {k_new, v_new}) {
+      if (!aligned(t->data, 4) || (t->stride[0] % 2) != 0 || (t->stride[1] % 2) != 0)
+        return fail("k_new and v_new must be 4-byte aligned with even strides");
+    }
+    if (!(k_scale > 0.f) || !(v_scale > 0.f)) return fail("storing into the cache needs k_scale > 0 and v_scale > 0");
+    p.ke = static_cast<const __nv_bfloat16*>(k_new->data);
+    p.ke_s0 = k_new->stride[0];
+    p.ke_s1 = k_new->stride[1];
+    p.ve = static_cast<const __nv_bfloat16*>(v_new->data);
+    p.ve_s0 = v_new->stride[0];
+    p.ve_s1 = v_new->stride[1];
+    p.wmode = 2;
+    p.kw = static_cast<unsigned char*>(const_cast<void*>(kc->data));
+    p.vw = static_cast<unsigned char*>(const_cast<void*>(vc->data));
+    p.kq = k_scale;
+    p.vq = v_scale;
+  }
   return launch_with_plan(p, bs, h_q, h_kv, D, mle, kc->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes,
                           stream);
 }
@@ -1519,6 +1681,28 @@ int verify_splitkv_paged_fwd(const vsk_tensor* q, const vsk_tensor* o, const vsk
   g_err.clear();
   return run_paged(q, o, k_cache, v_cache, block_table, seq_lens, page_size, max_len_extend, k_scale, v_scale,
                    sm_scale, workspace, workspace_bytes, stream);
+}
+
+int verify_splitkv_paged_write_fwd(const vsk_tensor* q, const vsk_tensor* k_new, const vsk_tensor* v_new,
+                                   const vsk_tensor* o, const vsk_tensor* k_cache, const vsk_tensor* v_cache,
+                                   const vsk_tensor* block_table, const vsk_tensor* seq_lens, int64_t page_size,
+                                   int64_t max_len_extend, float k_scale, float v_scale, float sm_scale,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (!k_new || !v_new) return fail("k_new and v_new are required");
+  return run_paged(q, o, k_cache, v_cache, block_table, seq_lens, page_size, max_len_extend, k_scale, v_scale,
+                   sm_scale, workspace, workspace_bytes, stream, k_new, v_new);
+}
+
+int verify_splitkv_write_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                             const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                             const vsk_tensor* kvi, const vsk_tensor* out_cache_loc, int64_t max_len_extend,
+                             float k_scale, float v_scale, float sm_scale, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  g_err.clear();
+  if (!out_cache_loc) return fail("out_cache_loc is NULL");
+  return run_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, 1, max_len_extend, k_scale, v_scale, sm_scale, workspace,
+                    workspace_bytes, stream, nullptr, nullptr, out_cache_loc);
 }
 
 int verify_splitkv_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,

@@ -449,3 +449,108 @@ def test_paged_cuda_graph_replay(vsk):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), eager.view(torch.int16))
+
+
+# ----------------------------------------------------------------- fused store of the new drafts
+def _bits_np(t):
+    return workloads._bits(t)
+
+
+def _pool_np(t):
+    a = t.cpu().contiguous()
+    return a.view(torch.uint8).numpy() if a.dtype == torch.float8_e4m3fn else a.view(torch.int16).numpy().view(np.uint16)
+
+
+WRITE_FLAT = [
+    workloads.Spec("write_bf16", (300, 0, 1000), 4, 16, 2, 128, 128, perm=True, pool_extra=64, seed=401),
+    workloads.Spec("write_fp8_d256", (700, 90), 4, 16, 2, 256, 256, pool="e4m3", perm=True, pool_extra=32,
+                   k_scale=0.5, v_scale=0.25, seed=402),
+    workloads.Spec("write_fp8_d64_l8", (129, 64, 5), 8, 8, 1, 64, 64, pool="e4m3", perm=True, pool_extra=48,
+                   k_scale=2.0, v_scale=0.75, seed=403),
+    workloads.Spec("write_bf16_scaled", (500,), 3, 32, 8, 128, 128, perm=True, pool_extra=8, k_scale=1.5,
+                   v_scale=0.5, seed=404),
+]
+
+
+def _free_rows(p, n, seed):
+    """n distinct pool rows that no prefix references, in random order."""
+    used = torch.zeros(p["k_buffer"].shape[0], dtype=torch.bool)
+    used[p["kv_indices"].cpu()] = True
+    free = torch.nonzero(~used).flatten()
+    assert free.numel() >= n
+    return free[torch.randperm(free.numel(), generator=torch.Generator().manual_seed(seed))[:n]]
+
+
+@pytest.mark.parametrize("spec", WRITE_FLAT, ids=lambda s: s.name)
+@pytest.mark.parametrize("loc_dtype", [torch.int64, torch.int32])
+def test_fused_store_flat(vsk, spec, loc_dtype):
+    p = gpu_problem(spec)
+    plain = run_gpu(vsk, p)
+    n = p["q"].shape[0]
+    loc = _free_rows(p, n, spec.seed).to(loc_dtype)
+    kb, vb = p["k_buffer"].clone(), p["v_buffer"].clone()
+    o = torch.full_like(plain, float("nan"))
+    vsk.read_error_flags()
+    vsk.verify_splitkv_write_fwd(p["q"], p["k_ext"], p["v_ext"], o, kb, vb, p["qo_indptr"], p["kv_indptr"],
+                                 p["kv_indices"], loc.cuda(), p["max_len_extend"], p["k_scale"], p["v_scale"],
+                                 sm_scale=p["sm_scale"])
+    torch.cuda.synchronize()
+    assert vsk.read_error_flags() == 0
+    assert torch.equal(o.view(torch.int16), plain.view(torch.int16))  # the attention is untouched
+    dt = "e4m3" if spec.pool == "e4m3" else "bf16"
+    rows = loc.long().numpy()
+    for pool, new, sc in ((kb, p["k_ext"], p["k_scale"]), (vb, p["v_ext"], p["v_scale"])):
+        old = p["k_buffer"] if pool is kb else p["v_buffer"]
+        want = oracle.write_rows(_pool_np(old), rows, _bits_np(new), sc, dt)
+        np.testing.assert_array_equal(_pool_np(pool), want)  # exactly those rows, exactly those codes
+
+
+PAGED_WRITE = [
+    workloads.Spec("pwrite_ps16_fp8", (700, 5, 90, 0), 4, 32, 8, 128, 128, pool="e4m3", perm=True, page_size=16,
+                   k_scale=0.5, v_scale=0.25, seed=411),
+    workloads.Spec("pwrite_ps1_bf16", (0, 17, 300), 4, 16, 2, 128, 128, perm=True, page_size=1, seed=412),
+    workloads.Spec("pwrite_ps3_d256_fp8", (23, 1000), 6, 16, 2, 256, 256, pool="e4m3", perm=True, page_size=3,
+                   k_scale=1.5, v_scale=0.75, seed=413),
+    workloads.Spec("pwrite_decode_ps64_d64", (2000, 1, 63), 1, 8, 8, 64, 64, perm=True, page_size=64, k_scale=0.8,
+                   v_scale=1.25, seed=414),
+    workloads.Spec("pwrite_ps16_bf16_poison", (40, 0, 129), 4, 8, 2, 128, 128, perm=True, page_size=16,
+                   pool_extra=200, poison=True, k_scale=1.25, v_scale=2.0, seed=415),
+]
+
+
+def _draft_rows(p):
+    bt, ps, L = p["block_table"].cpu().numpy(), p["page_size"], p["max_len_extend"]
+    rows = []
+    for b, P in enumerate(p["prefix_lens"]):
+        j = np.arange(P, P + L)
+        rows.append(bt[b, j // ps].astype(np.int64) * ps + j % ps)
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("spec", PAGED_WRITE, ids=lambda s: s.name)
+def test_fused_store_paged(vsk, spec):
+    p = gpu_problem(spec)
+    g = torch.Generator(device="cuda").manual_seed(spec.seed + 1000)
+    k_new = torch.randn(p["k_ext"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    v_new = torch.randn(p["v_ext"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    kc, vc = p["k_buffer"].clone(), p["v_buffer"].clone()
+    o = torch.full(p["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vsk.read_error_flags()
+    vsk.verify_splitkv_paged_write_fwd(p["q"], k_new, v_new, o, kc, vc, p["block_table"], p["seq_lens"],
+                                       p["page_size"], p["max_len_extend"], p["k_scale"], p["v_scale"],
+                                       sm_scale=p["sm_scale"])
+    torch.cuda.synchronize()
+    assert vsk.read_error_flags() == 0
+    dt = "e4m3" if spec.pool == "e4m3" else "bf16"
+    rows = _draft_rows(p)
+    want_k = oracle.write_rows(_pool_np(p["k_buffer"]), rows, _bits_np(k_new), p["k_scale"], dt)
+    want_v = oracle.write_rows(_pool_np(p["v_buffer"]), rows, _bits_np(v_new), p["v_scale"], dt)
+    np.testing.assert_array_equal(_pool_np(kc), want_k)
+    np.testing.assert_array_equal(_pool_np(vc), want_v)
+    # attention = the definition over the cache as stored
+    arrays = workloads.to_oracle_arrays(p)
+    arrays["k_pool"], arrays["v_pool"] = want_k, want_v
+    check(o, oracle.verify_forward(arrays)["o"])
+    # ... and bit for bit what the plain paged call computes on that cache
+    again = run_paged(vsk, dict(p, k_buffer=kc, v_buffer=vc))
+    assert torch.equal(o.view(torch.int16), again.view(torch.int16))
