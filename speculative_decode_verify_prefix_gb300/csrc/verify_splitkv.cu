@@ -79,7 +79,8 @@ struct Params {
   int idx64;
   long long n_idx, pool, n_rows;
   int B, L, gq, R, HC, MT, n_hg, nwc, nst;
-  int ring_off, warp_bytes;
+  int ring_off, head_bytes;  // ring of KV head hc at ring_off + hc * head_bytes
+  int misc_off, misc_bytes;  // warp w's index / mask rings (and fp8 scratch) at misc_off + w * misc_bytes
   float scale2, dscale2, v_scale;
   float dvs;  // multiplier of draft values (v_scale when drafts come from the cache)
   // drafts already in a paged cache: block table of page ids, prefix lengths
@@ -337,11 +338,15 @@ __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int
 // Shared memory map (bytes):
 //   [0,   128)  control: sched base (i64) @0, sched b @8, ticket flags [2] @16
 //   [128, 256)  block-scan scratch (up to 16 x i64)
-//   [ring_off + w * warp_bytes, ...)  warp w's private region:
+//   [ring_off + hc * head_bytes, ...)  the ring of KV head hc, shared by the
+//        MT warps that serve it (each copies 16/MT of every stage's tokens):
 //        nst stages of K rows [16][D*e] then V rows [16][D*e] (bf16 rows are
 //        XOR-swizzled in 16-byte chunks, chunk ^ (token & 7), so 8-row ldmatrix
-//        phases hit 8 distinct bank groups); kIdxRing x 16 x 8 B of kv_indices;
-//        16 x 4 B valid-token masks; fp8 only: bf16 K and V, 16 x (D+8) each.
+//        phases hit 8 distinct bank groups).  After streaming, the first
+//        nwc * 32 * D bytes hold each warp's staged new drafts (fused store).
+//   [misc_off + w * misc_bytes, ...)  warp w's own kIdxRing x 16 x 8 B of
+//        kv_indices, 16 x 4 B valid-token masks and, fp8 only, bf16 K and V
+//        rows, 16 x (D+8) each.
 // ---------------------------------------------------------------------------
 template <int D>
 struct MaxWarps {
@@ -436,9 +441,11 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 
   // ============================ per-warp pipeline ============================
   // Warp w serves KV head hc = w / MT of the group and the 16-row tile mt of
-  // its packed query rows.  It streams its head's K and V rows itself with
-  // 16-byte cp.async into a private nst-deep ring: no producer warp, no
-  // cross-warp waits.  Indices come kIdxAhead stages ahead, also by cp.async.
+  // its packed query rows.  The MT warps of a head stream its K and V rows
+  // themselves with 16-byte cp.async into the head's nst-deep ring, each
+  // copying 16/MT tokens of every stage; with MT > 1 they meet at a named
+  // barrier once per stage.  No producer warp.  Indices come kIdxAhead stages
+  // ahead, also by cp.async, into each warp's own index ring.
   const int hc = warp / p.MT;
   const int mt = warp % p.MT;
   const int g = lane >> 2;
@@ -447,8 +454,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int r0 = 16 * mt + g;
   const int r1 = r0 + 8;
   const float NEG_INF = -INFINITY;
-  unsigned char* ring = smem + p.ring_off + warp * p.warp_bytes;
-  unsigned char* idx_ring = ring + nst * STAGE_B;
+  unsigned char* ring = smem + p.ring_off + hc * p.head_bytes;
+  unsigned char* idx_ring = smem + p.misc_off + warp * p.misc_bytes;
   unsigned* mask_ring = reinterpret_cast<unsigned*>(idx_ring + kIdxRing * 128);
   unsigned char* scratch = reinterpret_cast<unsigned char*>(mask_ring) + 128;  // fp8: bf16 K, V
   const uint32_t ring_s = smem_u32(ring);
@@ -500,9 +507,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     constexpr int TSTEP = 32 / LPT;          // tokens covered per pass of the warp
     constexpr int CPL = CPR / LPT;           // chunks of a row per lane
     const int cl = lane % LPT;
-#pragma unroll
-    for (int t = lane / LPT; t < kStageTokens; t += TSTEP) {
-      const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+    auto copy_token = [&](int t, long long loc) {
       const bool v = (mask >> t) & 1u;
       // an absent token is zero-filled (nothing read); q is a valid, never-empty address
       const unsigned char* ks = v ? kbase + loc * p.kb_s0 : reinterpret_cast<const unsigned char*>(p.q);
@@ -514,6 +519,23 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         const uint32_t d = slot + static_cast<uint32_t>(t * ROWB + pc * 16);
         cp_async_16_zfill(d, v ? ks + cir * 16 : ks, v, pol);
         cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
+      }
+    };
+    if (p.MT == 1) {
+      // the warp copies the whole stage (token indices known at compile time)
+#pragma unroll
+      for (int t = lane / LPT; t < kStageTokens; t += TSTEP) copy_token(t, __shfl_sync(0xffffffffu, myloc, t));
+    } else {
+      // the MT warps of the head split the stage: tokens [mt * tpw, mt * tpw + tpw)
+      const int tpw = kStageTokens / p.MT;
+#pragma unroll
+      for (int i = 0; i < kStageTokens / TSTEP; ++i) {
+        if (i * TSTEP >= tpw) break;  // uniform across the warp
+        const int tw = lane / LPT + i * TSTEP;
+        const bool act = tw < tpw;    // false only when fewer tokens than one pass of the warp
+        const int t = mt * tpw + (act ? tw : 0);
+        const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+        if (act) copy_token(t, loc);
       }
     }
   };
@@ -590,6 +612,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     for (int tok = t0; tok < te; tok += kStageTokens, ++k, kslot = (kslot + 1 == nst) ? 0 : kslot + 1) {
       cp_async_wait_dyn(nst - 2);  // stage k has landed (this lane's copies)
       __syncwarp();                // ... and every other lane's
+      // ... and the other warps' of this head: after this barrier no warp of
+      // the head still reads the slot of stage k - 1, which step_data refills
+      if (p.MT > 1) named_bar_sync(2 + hc, p.MT * 32);
       step_data();                 // refill the slot stage k-1 used
       step_idx();
       cp_async_commit();
@@ -858,8 +883,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         // once, store the codes into the cache (warp mt == 0 of the head) and
         // keep the dequantised values in the warp's idle ring, where the
         // fragment loads below read them
-        unsigned char* stK = ring;
-        unsigned char* stV = ring + 8 * D * 2;
+        unsigned char* stK = smem + p.ring_off + warp * (32 * D);
+        unsigned char* stV = stK + 8 * D * 2;
         if (p.wmode == 2) {
           constexpr int PR = D / 2;  // bf16 pairs per row
 #pragma unroll 1
@@ -1109,7 +1134,7 @@ int g_max_heads = 0;
 
 struct Plan {
   int gq, R, MT, HC, n_hg, nwc, threads, ek;
-  int stage_bytes, nst, ring_off, warp_bytes;
+  int stage_bytes, nst, ring_off, head_bytes, misc_off, misc_bytes;
   size_t smem;
   int ctas_per_sm;
 };
@@ -1140,15 +1165,15 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.nwc = hc * mt;
   pl.threads = pl.nwc * 32;
   pl.ek = fp8 ? 1 : 2;
-  // per warp: nst stages of 16 K rows + 16 V rows of one head, the index ring,
+  // per head: nst stages of 16 K rows + 16 V rows; per warp: the index ring,
   // the mask ring and (fp8) the bf16 widening scratch
   pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
-  const int fixed = kIdxRing * 128 + 128 + (fp8 ? 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0);
+  const int fixed = (kIdxRing * 128 + 128 + (fp8 ? 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0) + 127) & ~127;
   int k = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
   for (;;) {
     const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
     const int cap = g_max_stages > 0 ? std::min(g_max_stages, kMaxStages) : kMaxStages;
-    const int nst = std::min(cap, ((budget - kCtlBytes) / pl.nwc - fixed) / pl.stage_bytes);
+    const int nst = std::min(cap, (budget - kCtlBytes - pl.nwc * fixed) / (pl.HC * pl.stage_bytes));
     if (nst >= 2) {
       pl.nst = nst;
       pl.ctas_per_sm = k;
@@ -1157,9 +1182,14 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
     if (k == 1) return fail("stage of %d bytes does not fit shared memory", pl.stage_bytes);
     k /= 2;
   }
-  pl.warp_bytes = ((pl.nst * pl.stage_bytes + fixed) + 127) & ~127;
+  pl.head_bytes = pl.nst * pl.stage_bytes;
+  pl.misc_bytes = fixed;
   pl.ring_off = kCtlBytes;
-  pl.smem = static_cast<size_t>(pl.ring_off) + static_cast<size_t>(pl.nwc) * pl.warp_bytes;
+  // the ring region also holds each warp's staged drafts (32 * D bytes) after streaming
+  const int rings = std::max(pl.HC * pl.head_bytes, pl.nwc * 32 * static_cast<int>(D));
+  pl.misc_off = pl.ring_off + rings;
+  pl.smem = static_cast<size_t>(pl.misc_off) + static_cast<size_t>(pl.nwc) * pl.misc_bytes;
+  if (pl.smem > static_cast<size_t>(kSmemPerCTAMax)) return fail("shared memory plan of %zu bytes too large", pl.smem);
   return true;
 }
 
@@ -1462,7 +1492,9 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.nwc = pl.nwc;
   p.nst = pl.nst;
   p.ring_off = pl.ring_off;
-  p.warp_bytes = pl.warp_bytes;
+  p.head_bytes = pl.head_bytes;
+  p.misc_off = pl.misc_off;
+  p.misc_bytes = pl.misc_bytes;
   p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
   p.err = reinterpret_cast<unsigned*>(ws);
   p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
