@@ -163,6 +163,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// D(16x8 fp32) += A(16x16 f16, row) * B(16x8 f16, col)
+__device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
 __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -204,6 +213,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// e4m3 x2 -> f16 x2, exactly (every e4m3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(unsigned short two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // e4m3 x2 -> bf16 x2, exactly (every e4m3 value is a bf16 value).
@@ -333,6 +353,58 @@ __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int
   return s_b;
 }
 
+// Query fragments for an e4m3 pool: f16 operands whose contraction index is
+// permuted within each 16-wide block (logical k 2j, 2j+1 -> d 4j, 4j+1 and
+// k 2j+8, 2j+9 -> d 4j+2, 4j+3), the order in which K fragments come straight
+// out of e4m3 rows.  The tile is scaled by 2^-sh (exact), sh chosen so that
+// its largest |q| stays below 2^15, inside the f16 range; returns 2^sh.
+template <int KS>
+__device__ __forceinline__ float load_q_f16(const Params& p, const Seg& s, int hc, int r0, int r1, int j,
+                                             bool flag_err, uint32_t (&qf)[KS][4]) {
+  const int a = p.qo ? __ldg(p.qo + s.b) : s.b * p.L, e = p.qo ? __ldg(p.qo + s.b + 1) : (s.b + 1) * p.L;
+  const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
+  if (!ok && flag_err) atomicOr(p.err, kErrBadQoIndptr);
+  const int s_b = ok ? a : s.b * p.L;
+  const int kvh = s.hg * p.HC + hc;
+  const bool v0 = r0 < p.R, v1 = r1 < p.R;
+  const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
+                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
+  const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
+                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
+  unsigned mx = 0;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    qf[kk][0] = v0 ? ld_u32(q0 + kk * 16 + 4 * j) : 0u;
+    qf[kk][2] = v0 ? ld_u32(q0 + kk * 16 + 4 * j + 2) : 0u;
+    qf[kk][1] = v1 ? ld_u32(q1 + kk * 16 + 4 * j) : 0u;
+    qf[kk][3] = v1 ? ld_u32(q1 + kk * 16 + 4 * j + 2) : 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = max(mx, max(qf[kk][i] & 0x7FFFu, (qf[kk][i] >> 16) & 0x7FFFu));
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  const int ex = static_cast<int>(mx >> 7) - 127;  // exponent of the largest |q|
+  const int sh = ex > 14 ? ex - 14 : 0;
+  const float down = __int_as_float((127 - sh) << 23);
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_bf16(qf[kk][i]);
+      qf[kk][i] = pack_f16(f.x * down, f.y * down);
+    }
+  }
+  return __int_as_float((127 + sh) << 23);
+}
+
+// 16-byte chunk swizzle of a K / V row in a stage: rows of 128 bytes or more
+// XOR their chunk index with (token & 7); 64-byte rows (4 chunks) with
+// ((token >> 1) & 3).  Either way the 8 rows of an ldmatrix phase hit 8
+// distinct bank groups.
+template <int CPR>
+__device__ __forceinline__ int chunk_swz(int t) {
+  return CPR >= 8 ? (t & 7) : ((t >> 1) & 3);
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // Shared memory map (bytes):
@@ -457,7 +529,6 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   unsigned char* ring = smem + p.ring_off + hc * p.head_bytes;
   unsigned char* idx_ring = smem + p.misc_off + warp * p.misc_bytes;
   unsigned* mask_ring = reinterpret_cast<unsigned*>(idx_ring + kIdxRing * 128);
-  unsigned char* scratch = reinterpret_cast<unsigned char*>(mask_ring) + 128;  // fp8: bf16 K, V
   const uint32_t ring_s = smem_u32(ring);
   const uint32_t idx_s = smem_u32(idx_ring);
   const uint64_t pol = policy_evict_first();
@@ -515,7 +586,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 #pragma unroll
       for (int cj = 0; cj < CPL; ++cj) {
         const int cir = cl + LPT * cj;
-        const int pc = FP8 ? cir : (cir ^ (t & 7));
+        const int pc = cir ^ chunk_swz<CPR>(t);
         const uint32_t d = slot + static_cast<uint32_t>(t * ROWB + pc * 16);
         cp_async_16_zfill(d, v ? ks + cir * 16 : ks, v, pol);
         cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
@@ -581,6 +652,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int k_chk = (lane >> 3) & 1;
   const int v_key = (((lane >> 3) & 1) << 3) + (lane & 7);
   const int v_chk = lane >> 4;
+  const int f_key = lane & 15;  // e4m3 pools: key row of this lane's ldmatrix address
 
   // The next piece's query fragments are loaded into registers while the
   // current piece streams (head_dim <= 128), so a piece boundary costs no
@@ -588,12 +660,47 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   constexpr bool kQAhead = D <= 128;
   uint32_t qf[KS][4];
   uint32_t qn[kQAhead ? KS : 1][4];
+  // bf16 pool: bf16 q fragments; e4m3 pool: f16 q fragments scaled by 2^-sh
+  // (qmul = 2^sh is folded back into the score scale)
+  auto load_piece_q = [&](const Seg& sq, bool flag, uint32_t (&dst)[KS][4]) -> float {
+    if constexpr (FP8) {
+      return load_q_f16<KS>(p, sq, hc, r0, r1, j, flag, dst);
+    } else {
+      load_q<KS>(p, sq, hc, r0, r1, j, flag, dst);
+      return 1.f;
+    }
+  };
+  // e4m3 pools at head_dim 256: the piece's query fragments wait in the
+  // warp's shared memory (16 rows x D, 16-byte chunks XOR-swizzled by row)
+  // and are re-read by ldmatrix each stage, which frees 64 registers for the
+  // e4m3 conversions.
+  constexpr bool kQSmem = FP8 && D == 256;
+  unsigned char* qsm = reinterpret_cast<unsigned char*>(mask_ring) + 128;
+  auto q_to_smem = [&]() {
+    if constexpr (kQSmem) {
+      __syncwarp();  // the previous piece's ldmatrix reads are done
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = g + ((i & 1) << 3);
+          const int e = kk * 16 + ((i >> 1) << 3) + 2 * j;
+          *reinterpret_cast<uint32_t*>(qsm + row * (2 * D) + (((e >> 3) ^ (row & 7)) << 4) + (e & 7) * 2) = qf[kk][i];
+        }
+      }
+      __syncwarp();
+    }
+  };
+  const int q_row = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const uint32_t q_lane = smem_u32(qsm) + q_row * (2 * D);
   Seg s = seg0;
-  load_q<KS>(p, s, hc, r0, r1, j, flagger, qf);
+  float qsc = p.scale2 * load_piece_q(s, flagger, qf);
+  q_to_smem();
+  float qsc_n = p.scale2;
   Seg sn = s;
   seg_advance(p, sn);
   if constexpr (kQAhead) {
-    if (seg_live(p, sn, end)) load_q<KS>(p, sn, hc, r0, r1, j, false, qn);
+    if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, qn);
   }
   long long k = 0;
   int kslot = 0;  // ring slot of stage k (k % nst, kept without a division)
@@ -620,42 +727,12 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       cp_async_commit();
       const unsigned mask = mask_ring[k % 16];
       unsigned char* slotp = ring + kslot * STAGE_B;
-      uint32_t kaddr0, kaddr1, vaddr0;
-      int kstride;
-      if constexpr (FP8) {
-        // widen the 16 K and V rows to bf16 (exact) in the warp's scratch
-        unsigned char* dK = scratch;
-        unsigned char* dV = scratch + 16 * (D + 8) * 2;
-        for (int c = lane; c < D; c += 32) {  // D chunks of 16 B per 16 rows
-          const int t = c / (D / 16), cc = c % (D / 16);
-          const uint4 a = *reinterpret_cast<const uint4*>(slotp + t * ROWB + cc * 16);
-          const uint4 b = *reinterpret_cast<const uint4*>(slotp + 16 * ROWB + t * ROWB + cc * 16);
-          uint4 o0, o1, o2, o3;
-          o0.x = e4m3x2_to_bf16x2(a.x & 0xFFFF); o0.y = e4m3x2_to_bf16x2(a.x >> 16);
-          o0.z = e4m3x2_to_bf16x2(a.y & 0xFFFF); o0.w = e4m3x2_to_bf16x2(a.y >> 16);
-          o1.x = e4m3x2_to_bf16x2(a.z & 0xFFFF); o1.y = e4m3x2_to_bf16x2(a.z >> 16);
-          o1.z = e4m3x2_to_bf16x2(a.w & 0xFFFF); o1.w = e4m3x2_to_bf16x2(a.w >> 16);
-          o2.x = e4m3x2_to_bf16x2(b.x & 0xFFFF); o2.y = e4m3x2_to_bf16x2(b.x >> 16);
-          o2.z = e4m3x2_to_bf16x2(b.y & 0xFFFF); o2.w = e4m3x2_to_bf16x2(b.y >> 16);
-          o3.x = e4m3x2_to_bf16x2(b.z & 0xFFFF); o3.y = e4m3x2_to_bf16x2(b.z >> 16);
-          o3.z = e4m3x2_to_bf16x2(b.w & 0xFFFF); o3.w = e4m3x2_to_bf16x2(b.w >> 16);
-          *reinterpret_cast<uint4*>(dK + t * (D + 8) * 2 + cc * 32) = o0;
-          *reinterpret_cast<uint4*>(dK + t * (D + 8) * 2 + cc * 32 + 16) = o1;
-          *reinterpret_cast<uint4*>(dV + t * (D + 8) * 2 + cc * 32) = o2;
-          *reinterpret_cast<uint4*>(dV + t * (D + 8) * 2 + cc * 32 + 16) = o3;
-        }
-        __syncwarp();
-        kstride = (D + 8) * 2;
-        kaddr0 = smem_u32(dK) + k_key * kstride + k_chk * 16;
-        vaddr0 = smem_u32(dV) + v_key * kstride + v_chk * 16;
-        kaddr1 = 0;
-      } else {
-        kstride = ROWB;
-        kaddr0 = smem_u32(slotp) + k_key * ROWB;
-        vaddr0 = smem_u32(slotp) + 16 * ROWB + v_key * ROWB;
-        kaddr1 = 0;
-      }
-      (void)kaddr1;
+      // ldmatrix row addresses.  bf16: lanes 0-15 / 16-31 take keys 0-7, 8-15
+      // of k-chunk 2kk / 2kk+1 ... (k_key, k_chk); e4m3: lane takes key
+      // (lane & 15) and chunk 2kk2 + (lane >> 4), so one x4 load gives both
+      // 8-key tiles of two 16-wide d blocks.
+      const uint32_t kbase = smem_u32(slotp) + (FP8 ? f_key : k_key) * ROWB;
+      const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * ROWB;
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys
       // four independent accumulator chains per n-tile (k-step mod 4) cut the
@@ -670,18 +747,42 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           sx[0][t][e] = sx[1][t][e] = sx[2][t][e] = 0.f;
         }
       }
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        const int lc = kk * 2 + k_chk;
-        const uint32_t addr = FP8 ? kaddr0 + kk * 32 : kaddr0 + ((lc ^ (k_key & 7)) << 4);
-        ldsm_x4(addr, b0, b1, b2, b3);
-        if ((kk & 3) == 0) {
-          mma_bf16(sc[0], qf[kk], b0, b1);
-          mma_bf16(sc[1], qf[kk], b2, b3);
+      auto qk_step = [&](int kk, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+        float* c0 = (kk & 3) == 0 ? sc[0] : sx[((kk & 3) + 2) % 3][0];
+        float* c1 = (kk & 3) == 0 ? sc[1] : sx[((kk & 3) + 2) % 3][1];
+        if constexpr (kQSmem) {
+          uint32_t a[4];
+          ldsm_x4(q_lane + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+          mma_f16(c0, a, b0, b1);
+          mma_f16(c1, a, b2, b3);
+        } else if constexpr (FP8) {
+          mma_f16(c0, qf[kk], b0, b1);
+          mma_f16(c1, qf[kk], b2, b3);
         } else {
-          mma_bf16(sx[(kk & 3) - 1][0], qf[kk], b0, b1);
-          mma_bf16(sx[(kk & 3) - 1][1], qf[kk], b2, b3);
+          mma_bf16(c0, qf[kk], b0, b1);
+          mma_bf16(c1, qf[kk], b2, b3);
+        }
+      };
+      if constexpr (FP8) {
+        // each 32-bit register holds 4 consecutive e4m3 d values of one key:
+        // low pair -> b0, high pair -> b1 of the permuted contraction order
+#pragma unroll
+        for (int kk2 = 0; kk2 < KS / 2; ++kk2) {
+          const int c = 2 * kk2 + (lane >> 4);
+          uint32_t r0k, r1k, r2k, r3k;
+          ldsm_x4(kbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r0k, r1k, r2k, r3k);
+          qk_step(2 * kk2, e4m3x2_to_f16x2(r0k & 0xFFFF), e4m3x2_to_f16x2(r0k >> 16), e4m3x2_to_f16x2(r1k & 0xFFFF),
+                  e4m3x2_to_f16x2(r1k >> 16));
+          qk_step(2 * kk2 + 1, e4m3x2_to_f16x2(r2k & 0xFFFF), e4m3x2_to_f16x2(r2k >> 16),
+                  e4m3x2_to_f16x2(r3k & 0xFFFF), e4m3x2_to_f16x2(r3k >> 16));
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          const int lc = kk * 2 + k_chk;
+          ldsm_x4(kbase + ((lc ^ (k_key & 7)) << 4), b0, b1, b2, b3);
+          qk_step(kk, b0, b1, b2, b3);
         }
       }
 #pragma unroll
@@ -694,7 +795,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[t][e] *= p.scale2;
+        for (int e = 0; e < 4; ++e) sc[t][e] *= qsc;
       }
       if (mask != 0xFFFFu) {
 #pragma unroll
@@ -740,19 +841,44 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       m0 = mn0;
       m1 = mn1;
       uint32_t pa[4];
-      pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-      pa[1] = pack_bf16(pr[0][2], pr[0][3]);
-      pa[2] = pack_bf16(pr[1][0], pr[1][1]);
-      pa[3] = pack_bf16(pr[1][2], pr[1][3]);
-      // O += P V for 16 keys
+      if constexpr (FP8) {
+        pa[0] = pack_f16(pr[0][0], pr[0][1]);
+        pa[1] = pack_f16(pr[0][2], pr[0][3]);
+        pa[2] = pack_f16(pr[1][0], pr[1][1]);
+        pa[3] = pack_f16(pr[1][2], pr[1][3]);
+        // O += P V for 16 keys.  A transposing x4 load of e4m3 rows gives lane
+        // (g, j) the d pair (2g, 2g+1) of keys 2j and 2j+1; a byte permute
+        // regroups them by d, so each register feeds two n-tiles: E (even d,
+        // column g <-> d 2g) and O (odd d, column g <-> d 2g+1) of a 16-wide
+        // block.  acc[2*blk] is E, acc[2*blk+1] is O.
 #pragma unroll
-      for (int n2 = 0; n2 < NT / 2; ++n2) {
-        uint32_t b0, b1, b2, b3;
-        const int lc = n2 * 2 + v_chk;
-        const uint32_t addr = FP8 ? vaddr0 + n2 * 32 : vaddr0 + ((lc ^ (v_key & 7)) << 4);
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma_bf16(acc[2 * n2], pa, b0, b1);
-        mma_bf16(acc[2 * n2 + 1], pa, b2, b3);
+        for (int c2 = 0; c2 < KS / 2; ++c2) {
+          const int c = 2 * c2 + (lane >> 4);
+          uint32_t r[4];
+          ldsm_x4_t(vbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);      // keys 2j, 2j+1
+            const uint32_t x1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);  // keys 2j+8, 2j+9
+            const int blk = 2 * c2 + h;
+            mma_f16(acc[2 * blk], pa, e4m3x2_to_f16x2(x0 & 0xFFFF), e4m3x2_to_f16x2(x1 & 0xFFFF));
+            mma_f16(acc[2 * blk + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+          }
+        }
+      } else {
+        pa[0] = pack_bf16(pr[0][0], pr[0][1]);
+        pa[1] = pack_bf16(pr[0][2], pr[0][3]);
+        pa[2] = pack_bf16(pr[1][0], pr[1][1]);
+        pa[3] = pack_bf16(pr[1][2], pr[1][3]);
+        // O += P V for 16 keys
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t b0, b1, b2, b3;
+          const int lc = n2 * 2 + v_chk;
+          ldsm_x4_t(vbase + ((lc ^ (v_key & 7)) << 4), b0, b1, b2, b3);
+          mma_bf16(acc[2 * n2], pa, b0, b1);
+          mma_bf16(acc[2 * n2 + 1], pa, b2, b3);
+        }
       }
     }
 
@@ -770,10 +896,23 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
         lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
       }
+      if constexpr (FP8) {
+        // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
-        *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+        for (int blk = 0; blk < KS; ++blk) {
+          const float* e = acc[2 * blk];
+          const float* o = acc[2 * blk + 1];
+          *reinterpret_cast<float4*>(o_p + r0 * D + blk * 16 + 4 * j) =
+              make_float4(e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0);
+          *reinterpret_cast<float4*>(o_p + r1 * D + blk * 16 + 4 * j) =
+              make_float4(e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1);
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+          *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+        }
       }
     }
     s = sn;
@@ -787,9 +926,11 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           qf[kk][2] = qn[kk][2];
           qf[kk][3] = qn[kk][3];
         }
-        if (seg_live(p, sn, end)) load_q<KS>(p, sn, hc, r0, r1, j, false, qn);
+        qsc = qsc_n;
+        if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, qn);
       } else {
-        load_q<KS>(p, s, hc, r0, r1, j, false, qf);
+        qsc = p.scale2 * load_piece_q(s, false, qf);
+        q_to_smem();
       }
     }
   }
@@ -1168,7 +1309,7 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   // per head: nst stages of 16 K rows + 16 V rows; per warp: the index ring,
   // the mask ring and (fp8) the bf16 widening scratch
   pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
-  const int fixed = (kIdxRing * 128 + 128 + (fp8 ? 2 * 16 * (static_cast<int>(D) + 8) * 2 : 0) + 127) & ~127;
+  const int fixed = kIdxRing * 128 + 128 + (fp8 && D == 256 ? 16 * static_cast<int>(D) * 2 : 0);
   int k = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
   for (;;) {
     const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
