@@ -118,6 +118,28 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// L2 policy for the per-piece partials: kept in L2 until the segment's
+// finisher reads them back, while the K/V stream is marked evict-first.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_keep(float* a, float x, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(x), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep2(float* a, float x, float y, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(a), "f"(x), "f"(y), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep4(float* a, float x, float y, float z, float w, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(a), "f"(x), "f"(y), "f"(z), "f"(w),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -892,9 +914,10 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * D;
       const float inv0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
       const float inv1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
+      const uint64_t keep = policy_evict_last();
       if (j == 0) {
-        lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
-        lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
+        st_keep(lse_p + r0, l0 > 0.f ? m0 + log2f(l0) : NEG_INF, keep);
+        st_keep(lse_p + r1, l1 > 0.f ? m1 + log2f(l1) : NEG_INF, keep);
       }
       if constexpr (FP8) {
         // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
@@ -902,16 +925,14 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         for (int blk = 0; blk < KS; ++blk) {
           const float* e = acc[2 * blk];
           const float* o = acc[2 * blk + 1];
-          *reinterpret_cast<float4*>(o_p + r0 * D + blk * 16 + 4 * j) =
-              make_float4(e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0);
-          *reinterpret_cast<float4*>(o_p + r1 * D + blk * 16 + 4 * j) =
-              make_float4(e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1);
+          st_keep4(o_p + r0 * D + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
+          st_keep4(o_p + r1 * D + blk * 16 + 4 * j, e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1, keep);
         }
       } else {
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
-          *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+          st_keep2(o_p + r0 * D + n * 8 + 2 * j, acc[n][0] * inv0, acc[n][1] * inv0, keep);
+          st_keep2(o_p + r1 * D + n * 8 + 2 * j, acc[n][2] * inv1, acc[n][3] * inv1, keep);
         }
       }
     }
@@ -972,6 +993,22 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 #pragma unroll
       for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
       float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+      // the draft rows come from HBM: start them towards L2 now, and (head_dim
+      // <= 128) load the query fragments, so both overlap the fold below
+      if (mt == 0 && !p.paged) {
+        const int a = p.qo ? __ldg(p.qo + sg.b) : sg.b * p.L;
+        if (a >= 0 && static_cast<long long>(a) + p.L <= p.n_rows) {
+          constexpr int LINES = D * 2 / 128;  // 128-byte lines per row
+          for (int i = lane; i < p.L * LINES * 2; i += 32) {
+            const int t = i / (2 * LINES), rest = i % (2 * LINES);
+            const __nv_bfloat16* base = (rest < LINES) ? p.ke + (static_cast<long long>(a) + t) * p.ke_s0
+                                                       : p.ve + (static_cast<long long>(a) + t) * p.ve_s0;
+            prefetch_l2(base + static_cast<long long>(kvh) * (rest < LINES ? p.ke_s1 : p.ve_s1) + (rest % LINES) * 64);
+          }
+        }
+      }
+      int s_b = 0;
+      if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
 #pragma unroll 1
       for (long long c = c_first; c <= c_last; ++c) {
         const long long sl = c + s_idx;
@@ -997,7 +1034,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         m0 = mn0;
         m1 = mn1;
       }
-      const int s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
+      if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
       // tree verify: this sequence's mask rows (row-major [L][P+L], only the
