@@ -64,16 +64,16 @@ def hbm_peak():
 
 
 def traffic_per_launch(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    summary is for another workload or an older kernel source."""
+    """DRAM bytes per launch from the committed ncu summaries, or None when
+    there is none for this workload or it was taken on another kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("kernel_source_sha256") != kernel_source_hash() or t.get("workload") != workload:
+    if t.get("kernel_source_sha256") != kernel_source_hash():
         return None
-    return t.get("dram_bytes_per_launch")
+    return t.get("workloads", {}).get(workload, {}).get("dram_bytes_per_launch")
 
 
 WORKLOADS = {
