@@ -1009,30 +1009,40 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       }
       int s_b = 0;
       if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
-#pragma unroll 1
+      // Fold the pieces in CTA order.  Pass 1 finds the largest log-sum-exp
+      // of each row, pass 2 sums 2^(lse_c - max) o_c; two pieces per trip of
+      // pass 2 at head_dim <= 128 keep two pieces' loads in flight.
+#pragma unroll 4
       for (long long c = c_first; c <= c_last; ++c) {
-        const long long sl = c + s_idx;
-        const float* lq = p.plse + (sl * p.HC + hc) * RM;
-        const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
-        const float e0 = __ldcg(lq + r0), e1 = __ldcg(lq + r1);
-        const float mn0 = fmaxf(m0, e0), mn1 = fmaxf(m1, e1);
-        const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
-        const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
-        const float a0 = exp2f(m0 - ms0), a1 = exp2f(m1 - ms1);
-        const float w0 = exp2f(e0 - ms0), w1 = exp2f(e1 - ms1);
+        const float* lq = p.plse + ((c + s_idx) * p.HC + hc) * RM;
+        m0 = fmaxf(m0, __ldcg(lq + r0));
+        m1 = fmaxf(m1, __ldcg(lq + r1));
+      }
+      {
+        const float ms0 = (m0 == NEG_INF) ? 0.f : m0;
+        const float ms1 = (m1 == NEG_INF) ? 0.f : m1;
+#pragma unroll(D <= 128 ? 2 : 1)
+        for (long long c = c_first; c <= c_last; ++c) {
+          const long long sl = c + s_idx;
+          const float* lq = p.plse + (sl * p.HC + hc) * RM;
+          const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
+          const float w0 = exp2f(__ldcg(lq + r0) - ms0), w1 = exp2f(__ldcg(lq + r1) - ms1);
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
-          const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
-          acc[n][0] = acc[n][0] * a0 + (w0 > 0.f ? x0.x * w0 : 0.f);
-          acc[n][1] = acc[n][1] * a0 + (w0 > 0.f ? x0.y * w0 : 0.f);
-          acc[n][2] = acc[n][2] * a1 + (w1 > 0.f ? x1.x * w1 : 0.f);
-          acc[n][3] = acc[n][3] * a1 + (w1 > 0.f ? x1.y * w1 : 0.f);
+          for (int n = 0; n < NT; ++n) {
+            const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
+            const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
+            if (w0 > 0.f) {
+              acc[n][0] = fmaf(x0.x, w0, acc[n][0]);
+              acc[n][1] = fmaf(x0.y, w0, acc[n][1]);
+            }
+            if (w1 > 0.f) {
+              acc[n][2] = fmaf(x1.x, w1, acc[n][2]);
+              acc[n][3] = fmaf(x1.y, w1, acc[n][3]);
+            }
+          }
+          l0 += w0;
+          l1 += w1;
         }
-        l0 = l0 * a0 + w0;
-        l1 = l1 * a1 + w1;
-        m0 = mn0;
-        m1 = mn1;
       }
       if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
       // ------------- causal draft keys: continue the same online softmax -------------
@@ -1197,8 +1207,44 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           acc[n][3] *= a1;
         }
         // fp32 weighted sum of the draft values of this tile
+        bool v_done = false;
+        if constexpr (D <= 128) {
+          if (!p.paged && p.wmode == 0) {
+            // drafts from v_extend: four keys' value rows per load round trip
 #pragma unroll
-        for (int js = 0; js < 4; ++js) {
+            for (int kg = 0; kg < 2; ++kg) {
+              if (td * 8 + kg * 4 >= p.L) break;  // uniform across the warp
+              uint32_t vv[4][NT];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int key = td * 8 + kg * 4 + q4;
+                const bool ok = key < p.L;
+                const __nv_bfloat16* vp = p.ve + (static_cast<long long>(s_b) + (ok ? key : 0)) * p.ve_s0 +
+                                          static_cast<long long>(kvh) * p.ve_s1 + 2 * j;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) vv[q4][n] = ok ? ld_u32(vp + n * 8) : 0u;
+              }
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int kl = kg * 4 + q4;
+                const float w0 = __shfl_sync(0xffffffffu, pd[kl & 1], g * 4 + (kl >> 1)) * p.dvs;
+                const float w1 = __shfl_sync(0xffffffffu, pd[2 + (kl & 1)], g * 4 + (kl >> 1)) * p.dvs;
+                if (td * 8 + kl >= p.L) continue;  // uniform across the warp
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                  const float2 v = unpack_bf16(vv[q4][n]);
+                  acc[n][0] = fmaf(w0, v.x, acc[n][0]);
+                  acc[n][1] = fmaf(w0, v.y, acc[n][1]);
+                  acc[n][2] = fmaf(w1, v.x, acc[n][2]);
+                  acc[n][3] = fmaf(w1, v.y, acc[n][3]);
+                }
+              }
+            }
+            v_done = true;
+          }
+        }
+#pragma unroll
+        for (int js = 0; js < (v_done ? 0 : 4); ++js) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int key = td * 8 + 2 * js + e;
