@@ -106,6 +106,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--report-configs", action="store_true",
+                    help="print a per-configuration table (tiny, d256, GQA sweep, fp8, serving) instead of the JSON line")
     return ap.parse_args(argv)
 
 
@@ -489,8 +491,71 @@ def run_reference(args, dist: Dist) -> dict | None:
     }
 
 
+def report_configs(args) -> str:
+    """Per-configuration timings: median of >= 100 launches after 10 warm-up
+    launches, each launch timed alone with CUDA events; cold = the L2 flushed
+    before every launch by reading a 512 MB buffer (clean lines, so no write
+    back lands inside the timed launch), warm = back-to-back launches with the
+    inputs L2-resident when they fit.  Eager launches and CUDA-graph replays."""
+    import speculative_decode_verify_prefix_gb300 as vsk
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = hbm_peak()
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)  # 512 MB
+    specs = [workloads.TINY, workloads.D256] + workloads.gqa_sweep() + [workloads.FP8, workloads.SERVING]
+    rows = ["| config | B | R | D | pool | bytes / call | us / call cold (eager) | us / call cold (graph) | "
+            "us / call warm (graph) | GB/s cold (graph) | K/V-only GB/s cold | of measured peak (cold) |",
+            "|" + "---|" * 12]
+    for spec in specs:
+        prob = workloads.make_problem(spec, dev)
+        B = len(prob["prefix_lens"])
+        nbytes = workloads.algorithmic_bytes(prob)
+        kv = int(sum(prob["prefix_lens"])) * spec.h_kv * (spec.d + spec.dv) * prob["k_buffer"].element_size()
+        o = torch.empty(prob["q"].shape[0], spec.h_q, spec.dv, dtype=torch.bfloat16, device=dev)
+        ws = vsk.get_workspace(dev, B, spec.h_q, spec.h_kv, spec.d, spec.dv, spec.l_ext)
+        n = 100 if nbytes > 129e6 else 200
+
+        def timed(run, cold=True):
+            ts = []
+            for i in range(10 + n):
+                if cold:
+                    flush.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                run()
+                e1.record()
+                ts.append((e0, e1))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ts[10:]) * 1e3
+
+        eager = timed(lambda: _call(vsk, prob, o, ws))
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            _call(vsk, prob, o, ws)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            _call(vsk, prob, o, ws)
+        graph = timed(g.replay)
+        warm = timed(g.replay, cold=False)
+        if vsk.read_error_flags(ws):
+            raise RuntimeError(f"device error flags after {spec.name}")
+        rows.append(f"| {spec.name} | {B} | {(spec.h_q // spec.h_kv) * spec.l_ext} | {spec.d} | {spec.pool} | {nbytes:,} | "
+                    f"{eager:.2f} | {graph:.2f} | {warm:.2f} | {nbytes / graph / 1e3:.0f} | {kv / graph / 1e3:.0f} | "
+                    f"{nbytes / graph / 1e3 / peak:.3f} |")
+        del prob, o, g
+        torch.cuda.empty_cache()
+    rows.append(f"\npeak: {peak} GB/s ({peak_kind}); cold: L2 flushed by reading 512 MB before every launch")
+    return "\n".join(rows)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.report_configs:
+        print(report_configs(args), flush=True)
+        return
     dist = Dist()
     try:
         if args.impl == "reference":

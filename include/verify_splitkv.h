@@ -96,9 +96,12 @@ int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
  *   sm_scale    softmax scale; a value <= 0 or NaN selects 1/sqrt(D).
  *   workspace   device scratch of workspace_bytes bytes, zero-filled before
  *               its first use (cudaMemset or vsk_workspace_init) and then
- *               reused unchanged: every call leaves its counters at zero.  The
- *               needed size is at most vsk_workspace_size(max_bs, ...) for any
- *               B <= max_bs on the same device.  Concurrent calls (on
+ *               reused unchanged: every call leaves its counters (tickets,
+ *               kept in the last 64 KiB of the buffer, or more for very large
+ *               batches) at zero, so one buffer serves calls of any shapes
+ *               that fit it.  The needed size is at most
+ *               vsk_workspace_size(max_bs, ...) for any B <= max_bs on the
+ *               same device.  Concurrent calls (on
  *               different streams) must not share one workspace.
  *               workspace == NULL selects a library-owned per-device buffer
  *               that grows on demand; growth allocates and synchronises the

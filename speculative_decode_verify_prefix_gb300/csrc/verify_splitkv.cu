@@ -56,6 +56,9 @@ constexpr int kCtlBytes = 256;       // control block before the warp regions
 constexpr int kSmemPerSM = 233472;   // 228 KB per SM
 constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
+constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
+constexpr int kGroup = 4;             // pieces per group of a two-level merge
+constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 256;
 
 enum : unsigned {
@@ -106,7 +109,8 @@ struct Params {
   int mindptr64;
   long long n_mask;
   unsigned* err;
-  int* cnt;
+  int* cnt;       // [nseg] segment tickets, then [n_cta + nseg] group tickets (one per slot)
+  long long nseg;
   float* plse;
   float* po;
 };
@@ -964,35 +968,110 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   named_bar_sync(1, p.nwc * 32);
   Seg sg = seg0;
   int nbar = 0;  // ticket rounds so far: selects the flag slot (two slots, one barrier per round)
+  // One ticket round: tid 0 draws from ctr; the CTA learns whether it came
+  // last (then the ticket is reset to zero for the next call).
+  auto take_ticket = [&](int* ctr, int expected) -> bool {
+    if (tid == 0) {
+      const int old = atomicAdd(ctr, 1);
+      const int last = (old == expected - 1) ? 1 : 0;
+      if (last) {
+        *ctr = 0;
+        __threadfence();
+      }
+      last_flag[nbar & 1] = last;
+    }
+    named_bar_sync(1, p.nwc * 32);
+    const bool r = last_flag[nbar & 1] != 0;
+    ++nbar;
+    return r;
+  };
+  float acc[NT][4];
+  float m0, m1, l0, l1;
+  // Fold `count` partials (slots slot0, slot0 + stride, ...) of this warp's
+  // rows in slot order: pass 1 finds each row's largest log-sum-exp, pass 2
+  // sums 2^(lse - max) o; two partials per trip of pass 2 at head_dim <= 128
+  // keep two partials' loads in flight.
+  auto fold = [&](long long slot0, long long stride, long long count) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    m0 = NEG_INF;
+    m1 = NEG_INF;
+    l0 = 0.f;
+    l1 = 0.f;
+#pragma unroll 4
+    for (long long i = 0; i < count; ++i) {
+      const float* lq = p.plse + ((slot0 + i * stride) * p.HC + hc) * RM;
+      m0 = fmaxf(m0, __ldcg(lq + r0));
+      m1 = fmaxf(m1, __ldcg(lq + r1));
+    }
+    const float ms0 = (m0 == NEG_INF) ? 0.f : m0;
+    const float ms1 = (m1 == NEG_INF) ? 0.f : m1;
+#pragma unroll(D <= 128 ? 2 : 1)
+    for (long long i = 0; i < count; ++i) {
+      const long long sl = slot0 + i * stride;
+      const float* lq = p.plse + (sl * p.HC + hc) * RM;
+      const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
+      const float w0 = exp2f(__ldcg(lq + r0) - ms0), w1 = exp2f(__ldcg(lq + r1) - ms1);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
+        const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
+        if (w0 > 0.f) {
+          acc[n][0] = fmaf(x0.x, w0, acc[n][0]);
+          acc[n][1] = fmaf(x0.y, w0, acc[n][1]);
+        }
+        if (w1 > 0.f) {
+          acc[n][2] = fmaf(x1.x, w1, acc[n][2]);
+          acc[n][3] = fmaf(x1.y, w1, acc[n][3]);
+        }
+      }
+      l0 += w0;
+      l1 += w1;
+    }
+  };
 #pragma unroll 1
   while (seg_live(p, sg, end)) {
     const long long s_idx = static_cast<long long>(sg.b) * p.n_hg + sg.hg;
     const long long c_first = sg.off / Wl;
     const long long c_last = (sg.off + sg.len - 1) / Wl;
+    const long long npc = c_last - c_first + 1;  // pieces of the segment
+    // Segments of more than kTreeMin pieces merge in two levels: groups of
+    // kGroup consecutive pieces are folded by their group's last arriver into
+    // the slot of the group's first piece, then the last group folds the
+    // group partials.  Every level folds in slot order, so the result does not
+    // depend on which CTA arrived last.
+    const bool tree = npc > kTreeMin;
+    const long long ng = tree ? (npc + kGroup - 1) / kGroup : npc;
     bool finisher = true;
-    if (c_last > c_first) {
-      if (tid == 0) {
-        const int expected = static_cast<int>(c_last - c_first + 1);
-        const int old = atomicAdd(p.cnt + s_idx, 1);
-        const int last = (old == expected - 1) ? 1 : 0;
-        if (last) {
-          p.cnt[s_idx] = 0;  // leave the ticket at zero for the next call
-          __threadfence();
+    if (tree) {
+      const long long gfirst = c_first + ((c_self - c_first) / kGroup) * kGroup;
+      const long long gcount = min(static_cast<long long>(kGroup), c_last - gfirst + 1);
+      finisher = gcount == 1 || take_ticket(p.cnt + p.nseg + gfirst + s_idx, static_cast<int>(gcount));
+      if (finisher) {
+        fold(gfirst + s_idx, 1, gcount);
+        // the group partial replaces the partial of the group's first piece
+        const long long sl = gfirst + s_idx;
+        float* lse_p = p.plse + (sl * p.HC + hc) * RM;
+        float* o_p = p.po + ((sl * p.HC + hc) * RM) * D;
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        if (j == 0) {
+          lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
+          lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
         }
-        last_flag[nbar & 1] = last;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+          *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+        }
+        __threadfence();
+        named_bar_sync(1, p.nwc * 32);
+        finisher = take_ticket(p.cnt + s_idx, static_cast<int>(ng));
       }
-      named_bar_sync(1, p.nwc * 32);
-      finisher = last_flag[nbar & 1] != 0;
-      ++nbar;
+    } else if (npc > 1) {
+      finisher = take_ticket(p.cnt + s_idx, static_cast<int>(npc));
     }
     if (finisher) {
       const int kvh = sg.hg * p.HC + hc;
-      // Fold every piece of the segment in CTA order: the result does not
-      // depend on which CTA happened to finish last.
-      float acc[NT][4];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
       // the draft rows come from HBM: start them towards L2 now, and (head_dim
       // <= 128) load the query fragments, so both overlap the fold below
       if (mt == 0 && !p.paged) {
@@ -1009,41 +1088,11 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       }
       int s_b = 0;
       if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
-      // Fold the pieces in CTA order.  Pass 1 finds the largest log-sum-exp
-      // of each row, pass 2 sums 2^(lse_c - max) o_c; two pieces per trip of
-      // pass 2 at head_dim <= 128 keep two pieces' loads in flight.
-#pragma unroll 4
-      for (long long c = c_first; c <= c_last; ++c) {
-        const float* lq = p.plse + ((c + s_idx) * p.HC + hc) * RM;
-        m0 = fmaxf(m0, __ldcg(lq + r0));
-        m1 = fmaxf(m1, __ldcg(lq + r1));
-      }
-      {
-        const float ms0 = (m0 == NEG_INF) ? 0.f : m0;
-        const float ms1 = (m1 == NEG_INF) ? 0.f : m1;
-#pragma unroll(D <= 128 ? 2 : 1)
-        for (long long c = c_first; c <= c_last; ++c) {
-          const long long sl = c + s_idx;
-          const float* lq = p.plse + (sl * p.HC + hc) * RM;
-          const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
-          const float w0 = exp2f(__ldcg(lq + r0) - ms0), w1 = exp2f(__ldcg(lq + r1) - ms1);
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
-            const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
-            if (w0 > 0.f) {
-              acc[n][0] = fmaf(x0.x, w0, acc[n][0]);
-              acc[n][1] = fmaf(x0.y, w0, acc[n][1]);
-            }
-            if (w1 > 0.f) {
-              acc[n][2] = fmaf(x1.x, w1, acc[n][2]);
-              acc[n][3] = fmaf(x1.y, w1, acc[n][3]);
-            }
-          }
-          l0 += w0;
-          l1 += w1;
-        }
-      }
+      // the pieces (or, for a two-level merge, the group partials) in slot order
+      if (tree)
+        fold(c_first + s_idx, kGroup, ng);
+      else
+        fold(c_first + s_idx, 1, npc);
       if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
@@ -1419,8 +1468,13 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace: the error word at offset 0, the partials from offset 256 up,
+// and the tickets in the LAST cnt_bytes of the buffer, at least 64 KiB.  The
+// tickets' place is then the same for every call on a given buffer whatever
+// its shapes (up to 16,384 tickets), so the zero tickets a call leaves are the
+// ones the next call finds, and no call's partials reach them.
 struct WsLayout {
-  size_t cnt_off, lse_off, o_off, total;
+  size_t lse_off, o_off, cnt_bytes, total;
 };
 
 WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
@@ -1428,10 +1482,10 @@ WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
   const long long segs = B * pl.n_hg;
   const long long slots = n_cta + segs;
   const long long rows = slots * pl.HC * 16LL * pl.MT;
-  w.cnt_off = 256;
-  w.lse_off = w.cnt_off + align256(4 * static_cast<size_t>(segs));
+  w.lse_off = 256;
   w.o_off = w.lse_off + align256(4 * static_cast<size_t>(rows));
-  w.total = w.o_off + 4 * static_cast<size_t>(rows) * static_cast<size_t>(D);
+  w.cnt_bytes = std::max(static_cast<size_t>(kTicketBytes), align256(4 * static_cast<size_t>(segs + slots)));
+  w.total = align256(w.o_off + 4 * static_cast<size_t>(rows) * static_cast<size_t>(D)) + w.cnt_bytes;
   return w;
 }
 
@@ -1555,11 +1609,14 @@ int prepare_kernel(KernelFn fn) {
                               kSmemPerCTAMax) == cudaSuccess;
 }
 
-void* internal_workspace(int dev, size_t need, cudaStream_t stream) {
+void* internal_workspace(int dev, size_t need, cudaStream_t stream, size_t* bytes) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
   if (static_cast<int>(g_ws.size()) <= dev) g_ws.resize(dev + 1);
   DevWs& w = g_ws[dev];
-  if (w.bytes >= need) return w.ptr;
+  if (w.bytes >= need) {
+    *bytes = w.bytes;
+    return w.ptr;
+  }
   if (w.ptr) {
     cudaStreamSynchronize(stream);
     cudaFree(w.ptr);
@@ -1574,6 +1631,7 @@ void* internal_workspace(int dev, size_t need, cudaStream_t stream) {
   }
   w.ptr = p;
   w.bytes = need;
+  *bytes = need;
   return p;
 }
 
@@ -1697,8 +1755,9 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  size_t ws_bytes = workspace_bytes;
   if (!ws) {
-    ws = static_cast<unsigned char*>(internal_workspace(dev, wl.total, st));
+    ws = static_cast<unsigned char*>(internal_workspace(dev, wl.total, st, &ws_bytes));
     if (!ws) return fail("cannot allocate a %zu-byte workspace", wl.total);
   } else if (workspace_bytes < wl.total) {
     return fail("workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes, wl.total);
@@ -1721,7 +1780,8 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.misc_bytes = pl.misc_bytes;
   p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
   p.err = reinterpret_cast<unsigned*>(ws);
-  p.cnt = reinterpret_cast<int*>(ws + wl.cnt_off);
+  p.cnt = reinterpret_cast<int*>(ws + ((ws_bytes & ~static_cast<size_t>(255)) - wl.cnt_bytes));
+  p.nseg = B * pl.n_hg;
   p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
   p.po = reinterpret_cast<float*>(ws + wl.o_off);
   void* args[] = {&p};
@@ -2064,8 +2124,11 @@ extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor*
   if (!scratch) return 0;
   // The array keeps whatever the previous call left: zero the error word and
   // the per-segment tickets before this call's kernel runs.
-  const size_t clear = 256 + 4 * static_cast<size_t>(B) * static_cast<size_t>(pl.n_hg);
-  e = cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream));
+  const WsLayout wl = ws_layout(n_cta, B, pl, D);
+  e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));  // the error word
+  if (e == cudaSuccess)  // the tickets, at the end of the array
+    e = cudaMemsetAsync(scratch + VSK_NOALLOC_SCRATCH_BYTES - wl.cnt_bytes, 0, wl.cnt_bytes,
+                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail("cudaMemsetAsync on the built-in scratch: %s", cudaGetErrorString(e));
   return verify_splitkv_fwd(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale,
                             sm_scale, scratch, VSK_NOALLOC_SCRATCH_BYTES, stream);

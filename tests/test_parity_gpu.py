@@ -554,3 +554,27 @@ def test_fused_store_paged(vsk, spec):
     # ... and bit for bit what the plain paged call computes on that cache
     again = run_paged(vsk, dict(p, k_buffer=kc, v_buffer=vc))
     assert torch.equal(o.view(torch.int16), again.view(torch.int16))
+
+
+def test_one_workspace_serves_calls_of_any_shape(vsk):
+    """Tickets sit at a fixed place at the end of the buffer: calls of
+    different batch sizes, head counts and CTA counts sharing one caller
+    workspace agree bitwise with calls on a fresh zeroed workspace."""
+    specs = [
+        workloads.Spec("ws_a", (3000, 200, 4000, 17, 900, 1200, 5, 2500), 4, 32, 8, 128, 128, perm=True, seed=501),
+        workloads.Spec("ws_b", (5000, 64), 4, 16, 2, 256, 256, perm=True, seed=502),
+        workloads.Spec("ws_c", (2000, 5, 0, 777, 64), 4, 16, 4, 128, 128, perm=True, seed=503),
+    ]
+    shared = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    plan = [(0, 0), (1000, 16), (64, 16), (0, 0), (7, 16), (300, 16)]
+    for i, (nc, mt) in enumerate(plan):
+        for spec in specs:
+            p = gpu_problem(spec)
+            vsk.set_tuning(nc, mt)
+            try:
+                got = run_gpu(vsk, p, workspace=shared)
+                fresh = run_gpu(vsk, p, workspace=torch.zeros_like(shared))
+            finally:
+                vsk.set_tuning(0, 0)
+            assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (i, spec.name)
+    assert vsk.read_error_flags(shared) == 0
