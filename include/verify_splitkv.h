@@ -248,8 +248,11 @@ int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
 
 /* Tuning override for tests and sweeps: number of persistent CTAs (0 = the
  * device's SM count times the CTAs that fit per SM) and the minimum prefix
- * tokens per CTA (0 = default).  Affects the split of the prefix across CTAs,
- * never the definition of the result.  Process-wide; not thread-safe. */
+ * tokens per CTA (0 = default: at least 64 tokens and at least the mean
+ * prefix length / 24 from static shapes (kv_indices entries per sequence, or
+ * the block table's capacity), which bounds the pieces a segment's finisher
+ * merges; a nonzero value is used alone).  Affects the split of the prefix across
+ * CTAs, never the definition of the result.  Process-wide; not thread-safe. */
 void vsk_set_tuning(int num_ctas, int min_tokens_per_cta);
 
 /* Tuning override of the CTA shape, for sweeps: at most `max_ring_stages`

@@ -45,6 +45,14 @@ def _ref(t):
     return ctypes.byref(as_vsk(t))
 
 
+def _gate(views, is_causal, mle, sliding_window_size, sinks, logit_cap, xai_temperature_len) -> bool:
+    sw = -1 if sliding_window_size is None else int(sliding_window_size)
+    xai = -1 if xai_temperature_len is None else int(xai_temperature_len)
+    cap = float(logit_cap) if logit_cap else 0.0
+    return bool(_native.lib().vsk_can_handle(*[ctypes.byref(v) for v in views], int(bool(is_causal)), mle, sw,
+                                             int(sinks is not None), cap, xai))
+
+
 def can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
                custom_mask, is_causal, mask_indptr, max_len_extend, sliding_window_size=-1, sinks=None,
                logit_cap=0.0, xai_temperature_len=-1) -> bool:
@@ -56,19 +64,16 @@ def can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_i
         mle = int(max_len_extend)
     except (TypeError, ValueError):
         return False
-    for t in (q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices):
+    ts = (q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices)
+    for t in ts:
         if not isinstance(t, torch.Tensor) or t.dtype not in _DT or t.dim() > 3:
             return False
-    sw = -1 if sliding_window_size is None else int(sliding_window_size)
-    xai = -1 if xai_temperature_len is None else int(xai_temperature_len)
-    cap = float(logit_cap) if logit_cap else 0.0
-    return bool(_native.lib().vsk_can_handle(
-        _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(k_buffer), _ref(v_buffer),
-        _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), int(bool(is_causal)), mle,
-        sw, int(sinks is not None), cap, xai))
+    return _gate([as_vsk(t) for t in ts], is_causal, mle, sliding_window_size, sinks, logit_cap,
+                 xai_temperature_len)
 
 
 _WS = {}
+_WS_SIZE = {}  # (device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> bytes
 _WS_LOCK = threading.Lock()
 
 
@@ -79,8 +84,12 @@ def workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> int:
 def get_workspace(device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> torch.Tensor:
     """Zero-filled per-device workspace, grown (never shrunk) to fit max_bs."""
     device = torch.device(device)
-    with torch.cuda.device(device):
-        need = workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext)
+    key = (device, int(max_bs), int(h_q), int(h_kv), int(head_dim), int(v_head_dim), int(l_ext))
+    need = _WS_SIZE.get(key)
+    if need is None:
+        with torch.cuda.device(device):
+            need = workspace_size(*key[1:])
+        _WS_SIZE[key] = need
     if need == 0:
         raise RuntimeError("workspace size query failed: " + _native.last_error())
     with _WS_LOCK:
@@ -113,15 +122,20 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
     an l_ext x (prefix + l_ext) uint8 matrix) the draft block follows the
     mask, which serves tree verify (topk > 1); the prefix part of the mask is
     not applied, so ``skip_prefix_custom_mask`` must be True."""
-    if not can_handle(q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
-                      custom_mask, is_causal, mask_indptr, max_len_extend,
-                      sliding_window_size=sliding_window_size, sinks=sinks, logit_cap=logit_cap,
-                      xai_temperature_len=xai_temperature_len):
+    try:
+        mle = int(max_len_extend)
+    except (TypeError, ValueError):
+        return False
+    ts = (q_extend, k_extend, v_extend, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices)
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or t.dtype not in _DT or t.dim() > 3:
+            return False
+    views = [as_vsk(t) for t in ts]
+    if not _gate(views, is_causal, mle, sliding_window_size, sinks, logit_cap, xai_temperature_len):
         return False
     if custom_mask is not None and (not skip_prefix_custom_mask or mask_indptr is None):
         return False  # the prefix part of a tree mask is not applied by this kernel
     bs = qo_indptr.shape[0] - 1
-    mle = int(max_len_extend)
     if workspace is None:
         mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
         workspace = get_workspace(q_extend.device, mb, q_extend.shape[1], k_extend.shape[1],
@@ -131,17 +145,17 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
     sm = 0.0 if sm_scale is None else float(sm_scale)
     if custom_mask is not None:
         cm = custom_mask if custom_mask.dtype == torch.uint8 else custom_mask.view(torch.uint8)
+        r = [ctypes.byref(v) for v in views]
         ok = _native.lib().verify_splitkv_tree_fwd(
-            _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
-            _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), _ref(cm.reshape(-1)), _ref(mask_indptr), mle,
+            r[0], r[1], r[2], _ref(o_extend), r[3], r[4], r[5], r[6], r[7], _ref(cm.reshape(-1)), _ref(mask_indptr), mle,
             _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
             ctypes.c_void_p(stream.cuda_stream))
         if not ok:
             raise RuntimeError("verify_splitkv_tree_fwd failed after the gate passed: " + _native.last_error())
         return True
+    r = [ctypes.byref(v) for v in views]
     ok = _native.lib().verify_splitkv_fwd(
-        _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
-        _ref(qo_indptr), _ref(kv_indptr), _ref(kv_indices), int(bool(is_causal)), mle,
+        r[0], r[1], r[2], _ref(o_extend), r[3], r[4], r[5], r[6], r[7], int(bool(is_causal)), mle,
         _coerce(k_scale), _coerce(v_scale), sm, ctypes.c_void_p(workspace.data_ptr()),
         workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
     if not ok:

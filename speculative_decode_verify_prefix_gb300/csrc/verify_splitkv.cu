@@ -59,7 +59,8 @@ constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
-constexpr long long kDefaultMinTokens = 256;
+constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
+constexpr long long kPiecesPerSegment = 24;    // ... and at least the mean prefix over this many
 
 enum : unsigned {
   kErrBadIndex = 1u,
@@ -1736,7 +1737,7 @@ namespace vsk {
 // Plans the CTA shape for these sizes, sizes and checks the workspace, fills
 // the plan-dependent fields of p and launches the kernel.
 static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+                            void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
   Plan pl;
   if (!make_plan(h_q, h_kv, D, L, fp8, pl)) return 0;
   int dev = 0;
@@ -1778,7 +1779,16 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.head_bytes = pl.head_bytes;
   p.misc_off = pl.misc_off;
   p.misc_bytes = pl.misc_bytes;
-  p.w_min = g_min_tokens > 0 ? g_min_tokens : kDefaultMinTokens;
+  // Smallest CTA share, from static shapes only (no device read, graph
+  // safe): at least 64 tokens and, for small batches where the shares get
+  // short, at least the mean prefix / 24 in whole stages, which bounds the
+  // pieces a segment's finisher merges.
+  if (g_min_tokens > 0) {
+    p.w_min = g_min_tokens;
+  } else {
+    const long long wp = (mean_len / kPiecesPerSegment + kStageTokens - 1) / kStageTokens * kStageTokens;
+    p.w_min = std::max(kDefaultMinTokens, wp);
+  }
   p.err = reinterpret_cast<unsigned*>(ws);
   p.cnt = reinterpret_cast<int*>(ws + ((ws_bytes & ~static_cast<size_t>(255)) - wl.cnt_bytes));
   p.nseg = B * pl.n_hg;
@@ -1860,8 +1870,9 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
     p.kq = k_scale;
     p.vq = v_scale;
   }
-  return launch_with_plan(p, qo->shape[0] - 1, q->shape[1], ke->shape[1], D, max_len_extend,
-                          kb->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes, stream);
+  const long long B = qo->shape[0] - 1;
+  return launch_with_plan(p, B, q->shape[1], ke->shape[1], D, max_len_extend, kb->dtype == VSK_DTYPE_FP8E4M3,
+                          workspace, workspace_bytes, stream, kvi->shape[0] / B);
 }
 
 bool check_2d(const vsk_tensor* t, const char* name) {
@@ -1983,8 +1994,9 @@ static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor*
     p.kq = k_scale;
     p.vq = v_scale;
   }
+  // the block table bounds every sequence's length: its capacity stands in for the mean
   return launch_with_plan(p, bs, h_q, h_kv, D, mle, kc->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes,
-                          stream);
+                          stream, bt->shape[1] * page_size);
 }
 }  // namespace vsk
 

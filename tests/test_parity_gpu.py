@@ -387,8 +387,12 @@ def test_paged_bf16_unit_scales_is_bitwise_the_flat_path(vsk):
     the same keys in the same order and must agree bit for bit."""
     spec = workloads.Spec("paged_vs_flat", (900, 3, 0, 2500), 4, 32, 8, 128, 128, perm=True, page_size=16, seed=307)
     p = gpu_problem(spec)
-    a = run_paged(vsk, p)
-    b = run_gpu(vsk, p)
+    vsk.set_tuning(0, 256)  # the same split for both (their default floors come from different static shapes)
+    try:
+        a = run_paged(vsk, p)
+        b = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
