@@ -262,6 +262,13 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta);
  * changes the result beyond rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta);
 
+/* Tuning override, for sweeps and tests: 16-row query tiles per consumer warp
+ * (1 or 2; 0 = default: 2 at head_dim <= 128 when a KV head has more than 16
+ * packed rows and the call's prefix holds at least 65,536 tokens (from static
+ * shapes), else 1).  Affects the CTA shape, never the definition of the
+ * result.  Process-wide; not thread-safe. */
+void vsk_set_tuning_tiles(int tiles_per_warp);
+
 /* Size, in bytes, of the scratch array built into the library for
  * verify_splitkv_fwd_noalloc (32 MiB). */
 #define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)

@@ -93,6 +93,8 @@ def _bind(lib):
     lib.vsk_read_error_flags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.vsk_set_tuning.restype = None
     lib.vsk_set_tuning.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.vsk_set_tuning_tiles.restype = None
+    lib.vsk_set_tuning_tiles.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_shape.restype = None
     lib.vsk_set_tuning_shape.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.vsk_last_error.restype = ctypes.c_char_p

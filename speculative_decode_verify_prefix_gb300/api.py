@@ -263,5 +263,10 @@ def set_tuning_shape(max_ring_stages: int = 0, max_kv_heads_per_cta: int = 0) ->
     _native.lib().vsk_set_tuning_shape(int(max_ring_stages), int(max_kv_heads_per_cta))
 
 
+def set_tuning_tiles(tiles_per_warp: int = 0) -> None:
+    """Override the 16-row query tiles per consumer warp (1 or 2; 0 = default)."""
+    _native.lib().vsk_set_tuning_tiles(int(tiles_per_warp))
+
+
 def version() -> str:
     return _native.lib().vsk_version().decode()

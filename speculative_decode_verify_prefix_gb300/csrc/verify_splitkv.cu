@@ -57,6 +57,7 @@ constexpr int kSmemPerSM = 233472;   // 228 KB per SM
 constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
+constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
@@ -452,7 +453,7 @@ struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, int MTW>
 __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -545,13 +546,18 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   // copying 16/MT tokens of every stage; with MT > 1 they meet at a named
   // barrier once per stage.  No producer warp.  Indices come kIdxAhead stages
   // ahead, also by cp.async, into each warp's own index ring.
-  const int hc = warp / p.MT;
-  const int mt = warp % p.MT;
+  const int WPH = p.MT / MTW;  // warps per KV head; each owns MTW 16-row tiles
+  const int hc = warp / WPH;
+  const int mt = warp % WPH;
   const int g = lane >> 2;
   const int j = lane & 3;
   const int RM = 16 * p.MT;
-  const int r0 = 16 * mt + g;
-  const int r1 = r0 + 8;
+  int r0s[MTW], r1s[MTW];  // the packed rows of this lane in each of the warp's tiles
+#pragma unroll
+  for (int t = 0; t < MTW; ++t) {
+    r0s[t] = 16 * (mt * MTW + t) + g;
+    r1s[t] = r0s[t] + 8;
+  }
   const float NEG_INF = -INFINITY;
   unsigned char* ring = smem + p.ring_off + hc * p.head_bytes;
   unsigned char* idx_ring = smem + p.misc_off + warp * p.misc_bytes;
@@ -619,13 +625,13 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
       }
     };
-    if (p.MT == 1) {
+    if (WPH == 1) {
       // the warp copies the whole stage (token indices known at compile time)
 #pragma unroll
       for (int t = lane / LPT; t < kStageTokens; t += TSTEP) copy_token(t, __shfl_sync(0xffffffffu, myloc, t));
     } else {
-      // the MT warps of the head split the stage: tokens [mt * tpw, mt * tpw + tpw)
-      const int tpw = kStageTokens / p.MT;
+      // the warps of the head split the stage: tokens [mt * tpw, mt * tpw + tpw)
+      const int tpw = kStageTokens / WPH;
 #pragma unroll
       for (int i = 0; i < kStageTokens / TSTEP; ++i) {
         if (i * TSTEP >= tpw) break;  // uniform across the warp
@@ -682,37 +688,42 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int f_key = lane & 15;  // e4m3 pools: key row of this lane's ldmatrix address
 
   // The next piece's query fragments are loaded into registers while the
-  // current piece streams (head_dim <= 128), so a piece boundary costs no
-  // global round trip.
-  constexpr bool kQAhead = D <= 128;
-  uint32_t qf[KS][4];
+  // current piece streams (head_dim <= 128, one tile per warp), so a piece
+  // boundary costs no global round trip.
+  constexpr bool kQAhead = D <= 128 && MTW == 1;
+  uint32_t qf[MTW][KS][4];
   uint32_t qn[kQAhead ? KS : 1][4];
   // bf16 pool: bf16 q fragments; e4m3 pool: f16 q fragments scaled by 2^-sh
   // (qmul = 2^sh is folded back into the score scale)
-  auto load_piece_q = [&](const Seg& sq, bool flag, uint32_t (&dst)[KS][4]) -> float {
+  auto load_piece_q = [&](const Seg& sq, bool flag, int ra, int rb, uint32_t (&dst)[KS][4]) -> float {
     if constexpr (FP8) {
-      return load_q_f16<KS>(p, sq, hc, r0, r1, j, flag, dst);
+      return load_q_f16<KS>(p, sq, hc, ra, rb, j, flag, dst);
     } else {
-      load_q<KS>(p, sq, hc, r0, r1, j, flag, dst);
+      load_q<KS>(p, sq, hc, ra, rb, j, flag, dst);
       return 1.f;
     }
   };
-  // e4m3 pools at head_dim 256: the piece's query fragments wait in the
-  // warp's shared memory (16 rows x D, 16-byte chunks XOR-swizzled by row)
-  // and are re-read by ldmatrix each stage, which frees 64 registers for the
-  // e4m3 conversions.
-  constexpr bool kQSmem = FP8 && D == 256;
+  // e4m3 pools at head_dim 256, and warps with two tiles: the piece's query
+  // fragments wait in the warp's shared memory (per tile 16 rows x D,
+  // 16-byte chunks XOR-swizzled by row) and are re-read by ldmatrix each
+  // stage, which frees their registers (for the e4m3 conversions, or for the
+  // second tile's accumulators).
+  constexpr bool kQSmem = (FP8 && D == 256) || MTW == 2;
   unsigned char* qsm = reinterpret_cast<unsigned char*>(mask_ring) + 128;
   auto q_to_smem = [&]() {
     if constexpr (kQSmem) {
       __syncwarp();  // the previous piece's ldmatrix reads are done
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
+      for (int t = 0; t < MTW; ++t) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = g + ((i & 1) << 3);
-          const int e = kk * 16 + ((i >> 1) << 3) + 2 * j;
-          *reinterpret_cast<uint32_t*>(qsm + row * (2 * D) + (((e >> 3) ^ (row & 7)) << 4) + (e & 7) * 2) = qf[kk][i];
+        for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = g + ((i & 1) << 3);
+            const int e = kk * 16 + ((i >> 1) << 3) + 2 * j;
+            *reinterpret_cast<uint32_t*>(qsm + t * 32 * D + row * (2 * D) + (((e >> 3) ^ (row & 7)) << 4) +
+                                         (e & 7) * 2) = qf[t][kk][i];
+          }
         }
       }
       __syncwarp();
@@ -721,13 +732,15 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int q_row = (lane & 7) + (((lane >> 3) & 1) << 3);
   const uint32_t q_lane = smem_u32(qsm) + q_row * (2 * D);
   Seg s = seg0;
-  float qsc = p.scale2 * load_piece_q(s, flagger, qf);
+  float qsc[MTW];
+#pragma unroll
+  for (int t = 0; t < MTW; ++t) qsc[t] = p.scale2 * load_piece_q(s, flagger && t == 0, r0s[t], r1s[t], qf[t]);
   q_to_smem();
   float qsc_n = p.scale2;
   Seg sn = s;
   seg_advance(p, sn);
   if constexpr (kQAhead) {
-    if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, qn);
+    if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, r0s[0], r1s[0], qn);
   }
   long long k = 0;
   int kslot = 0;  // ring slot of stage k (k % nst, kept without a division)
@@ -736,10 +749,17 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   while (seg_live(p, s, end)) {
     const int t0 = static_cast<int>(max(start, s.off) - s.off);
     const int te = piece_real_end(s, end);
-    float acc[NT][4];
+    float acc[MTW][NT][4];
+    float m0[MTW], m1[MTW], l0[MTW], l1[MTW];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+    for (int t = 0; t < MTW; ++t) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = acc[t][n][2] = acc[t][n][3] = 0.f;
+      m0[t] = NEG_INF;
+      m1[t] = NEG_INF;
+      l0[t] = 0.f;
+      l1[t] = 0.f;
+    }
 
     // ---------------- prefix: online softmax over this CTA's piece ----------------
 #pragma unroll 1
@@ -748,7 +768,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       __syncwarp();                // ... and every other lane's
       // ... and the other warps' of this head: after this barrier no warp of
       // the head still reads the slot of stage k - 1, which step_data refills
-      if (p.MT > 1) named_bar_sync(2 + hc, p.MT * 32);
+      if (WPH > 1) named_bar_sync(2 + hc, WPH * 32);
       step_data();                 // refill the slot stage k-1 used
       step_idx();
       cp_async_commit();
@@ -761,33 +781,48 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       const uint32_t kbase = smem_u32(slotp) + (FP8 ? f_key : k_key) * ROWB;
       const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * ROWB;
 
-      // S = Q K^T for 16 keys: two n-tiles of 8 keys
-      // four independent accumulator chains per n-tile (k-step mod 4) cut the
-      // dependent mma latency; summed afterwards
-      float sc[2][4];
-      float sx[3][2][4];
+      // S = Q K^T for 16 keys: two n-tiles of 8 keys per 16-row tile.
+      // Independent accumulator chains per n-tile (k-step mod NCH) cut the
+      // dependent mma latency; summed afterwards.  With two tiles per warp the
+      // tiles themselves are independent chains.
+      constexpr int NCH = MTW == 1 ? 4 : 1;
+      float sc[MTW][2][4];
+      float sx[MTW][NCH > 1 ? NCH - 1 : 1][2][4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < MTW; ++t) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sc[t][e] = 0.f;
-          sx[0][t][e] = sx[1][t][e] = sx[2][t][e] = 0.f;
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[t][u][e] = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH - 1; ++c) sx[t][c][u][e] = 0.f;
+          }
         }
       }
       auto qk_step = [&](int kk, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-        float* c0 = (kk & 3) == 0 ? sc[0] : sx[((kk & 3) + 2) % 3][0];
-        float* c1 = (kk & 3) == 0 ? sc[1] : sx[((kk & 3) + 2) % 3][1];
-        if constexpr (kQSmem) {
-          uint32_t a[4];
-          ldsm_x4(q_lane + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
-          mma_f16(c0, a, b0, b1);
-          mma_f16(c1, a, b2, b3);
-        } else if constexpr (FP8) {
-          mma_f16(c0, qf[kk], b0, b1);
-          mma_f16(c1, qf[kk], b2, b3);
-        } else {
-          mma_bf16(c0, qf[kk], b0, b1);
-          mma_bf16(c1, qf[kk], b2, b3);
+        const int ch = kk % NCH;
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) {
+          float* c0 = ch == 0 ? sc[t][0] : sx[t][ch - 1][0];
+          float* c1 = ch == 0 ? sc[t][1] : sx[t][ch - 1][1];
+          if constexpr (kQSmem) {
+            uint32_t a[4];
+            ldsm_x4(q_lane + t * 32 * D + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+            if constexpr (FP8) {
+              mma_f16(c0, a, b0, b1);
+              mma_f16(c1, a, b2, b3);
+            } else {
+              mma_bf16(c0, a, b0, b1);
+              mma_bf16(c1, a, b2, b3);
+            }
+          } else if constexpr (FP8) {
+            mma_f16(c0, qf[t][kk], b0, b1);
+            mma_f16(c1, qf[t][kk], b2, b3);
+          } else {
+            mma_bf16(c0, qf[t][kk], b0, b1);
+            mma_bf16(c1, qf[t][kk], b2, b3);
+          }
         }
       };
       if constexpr (FP8) {
@@ -812,67 +847,82 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           qk_step(kk, b0, b1, b2, b3);
         }
       }
+      uint32_t pa[MTW][4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < MTW; ++t) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[t][e] += (sx[0][t][e] + sx[1][t][e]) + sx[2][t][e];
-      }
-      // scale into the log2 domain; mask absent keys (tail / dropped) only
-      // when the stage is not full (the mask is uniform across the warp)
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[t][e] *= qsc;
-      }
-      if (mask != 0xFFFFu) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int u = 0; u < 2; ++u) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int key = t * 8 + 2 * j + (e & 1);
-            if (!((mask >> key) & 1u)) sc[t][e] = NEG_INF;
+            float x = sc[t][u][e];
+            if constexpr (NCH == 4) {
+              x += (sx[t][0][u][e] + sx[t][1][u][e]) + sx[t][2][u][e];
+            } else {
+#pragma unroll
+              for (int c = 0; c < NCH - 1; ++c) x += sx[t][c][u][e];
+            }
+            // scale into the log2 domain
+            sc[t][u][e] = x * qsc[t];
           }
         }
-      }
-      const float mx0 = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
-      const float mx1 = quad_max(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
-      const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
-      float pr[2][4];
+        // mask absent keys (tail / dropped) only when the stage is not full
+        // (the mask is uniform across the warp)
+        if (mask != 0xFFFFu) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        pr[t][0] = fast_exp2(sc[t][0] - ms0);
-        pr[t][1] = fast_exp2(sc[t][1] - ms0);
-        pr[t][2] = fast_exp2(sc[t][2] - ms1);
-        pr[t][3] = fast_exp2(sc[t][3] - ms1);
-      }
-      const float ps0 = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-      const float ps1 = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-      // rescale only when some row's running maximum moved (rare once the
-      // maximum has settled); otherwise alpha is exactly 1
-      if (__any_sync(0xffffffffu, (mn0 != m0) || (mn1 != m1))) {
-        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
-        l0 *= al0;
-        l1 *= al1;
+          for (int u = 0; u < 2; ++u) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          acc[n][0] *= al0;
-          acc[n][1] *= al0;
-          acc[n][2] *= al1;
-          acc[n][3] *= al1;
+            for (int e = 0; e < 4; ++e) {
+              const int key = u * 8 + 2 * j + (e & 1);
+              if (!((mask >> key) & 1u)) sc[t][u][e] = NEG_INF;
+            }
+          }
+        }
+        const float mx0 = quad_max(fmaxf(fmaxf(sc[t][0][0], sc[t][0][1]), fmaxf(sc[t][1][0], sc[t][1][1])));
+        const float mx1 = quad_max(fmaxf(fmaxf(sc[t][0][2], sc[t][0][3]), fmaxf(sc[t][1][2], sc[t][1][3])));
+        const float mn0 = fmaxf(m0[t], mx0), mn1 = fmaxf(m1[t], mx1);
+        const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
+        const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
+        float pr[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          pr[u][0] = fast_exp2(sc[t][u][0] - ms0);
+          pr[u][1] = fast_exp2(sc[t][u][1] - ms0);
+          pr[u][2] = fast_exp2(sc[t][u][2] - ms1);
+          pr[u][3] = fast_exp2(sc[t][u][3] - ms1);
+        }
+        const float ps0 = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+        const float ps1 = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+        // rescale only when some row's running maximum moved (rare once the
+        // maximum has settled); otherwise alpha is exactly 1
+        if (__any_sync(0xffffffffu, (mn0 != m0[t]) || (mn1 != m1[t]))) {
+          const float al0 = fast_exp2(m0[t] - ms0), al1 = fast_exp2(m1[t] - ms1);
+          l0[t] *= al0;
+          l1[t] *= al1;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[t][n][0] *= al0;
+            acc[t][n][1] *= al0;
+            acc[t][n][2] *= al1;
+            acc[t][n][3] *= al1;
+          }
+        }
+        l0[t] += ps0;
+        l1[t] += ps1;
+        m0[t] = mn0;
+        m1[t] = mn1;
+        if constexpr (FP8) {
+          pa[t][0] = pack_f16(pr[0][0], pr[0][1]);
+          pa[t][1] = pack_f16(pr[0][2], pr[0][3]);
+          pa[t][2] = pack_f16(pr[1][0], pr[1][1]);
+          pa[t][3] = pack_f16(pr[1][2], pr[1][3]);
+        } else {
+          pa[t][0] = pack_bf16(pr[0][0], pr[0][1]);
+          pa[t][1] = pack_bf16(pr[0][2], pr[0][3]);
+          pa[t][2] = pack_bf16(pr[1][0], pr[1][1]);
+          pa[t][3] = pack_bf16(pr[1][2], pr[1][3]);
         }
       }
-      l0 += ps0;
-      l1 += ps1;
-      m0 = mn0;
-      m1 = mn1;
-      uint32_t pa[4];
       if constexpr (FP8) {
-        pa[0] = pack_f16(pr[0][0], pr[0][1]);
-        pa[1] = pack_f16(pr[0][2], pr[0][3]);
-        pa[2] = pack_f16(pr[1][0], pr[1][1]);
-        pa[3] = pack_f16(pr[1][2], pr[1][3]);
         // O += P V for 16 keys.  A transposing x4 load of e4m3 rows gives lane
         // (g, j) the d pair (2g, 2g+1) of keys 2j and 2j+1; a byte permute
         // regroups them by d, so each register feeds two n-tiles: E (even d,
@@ -888,56 +938,63 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);      // keys 2j, 2j+1
             const uint32_t x1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);  // keys 2j+8, 2j+9
             const int blk = 2 * c2 + h;
-            mma_f16(acc[2 * blk], pa, e4m3x2_to_f16x2(x0 & 0xFFFF), e4m3x2_to_f16x2(x1 & 0xFFFF));
-            mma_f16(acc[2 * blk + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+            const uint32_t e0 = e4m3x2_to_f16x2(x0 & 0xFFFF), e1 = e4m3x2_to_f16x2(x1 & 0xFFFF);
+            const uint32_t o0 = e4m3x2_to_f16x2(x0 >> 16), o1 = e4m3x2_to_f16x2(x1 >> 16);
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+              mma_f16(acc[t][2 * blk], pa[t], e0, e1);
+              mma_f16(acc[t][2 * blk + 1], pa[t], o0, o1);
+            }
           }
         }
       } else {
-        pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-        pa[1] = pack_bf16(pr[0][2], pr[0][3]);
-        pa[2] = pack_bf16(pr[1][0], pr[1][1]);
-        pa[3] = pack_bf16(pr[1][2], pr[1][3]);
         // O += P V for 16 keys
 #pragma unroll
         for (int n2 = 0; n2 < NT / 2; ++n2) {
           uint32_t b0, b1, b2, b3;
           const int lc = n2 * 2 + v_chk;
           ldsm_x4_t(vbase + ((lc ^ (v_key & 7)) << 4), b0, b1, b2, b3);
-          mma_bf16(acc[2 * n2], pa, b0, b1);
-          mma_bf16(acc[2 * n2 + 1], pa, b2, b3);
+#pragma unroll
+          for (int t = 0; t < MTW; ++t) {
+            mma_bf16(acc[t][2 * n2], pa[t], b0, b1);
+            mma_bf16(acc[t][2 * n2 + 1], pa[t], b2, b3);
+          }
         }
       }
     }
 
     // ---------------- piece end: write the partial and keep streaming ----------------
     // (tickets, merges, drafts and output wait until the whole range is streamed)
-    l0 = quad_sum(l0);
-    l1 = quad_sum(l1);
     {
       const long long slot_self = c_self + static_cast<long long>(s.b) * p.n_hg + s.hg;
       float* lse_p = p.plse + (slot_self * p.HC + hc) * RM;
       float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * D;
-      const float inv0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
-      const float inv1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
       const uint64_t keep = policy_evict_last();
-      if (j == 0) {
-        st_keep(lse_p + r0, l0 > 0.f ? m0 + log2f(l0) : NEG_INF, keep);
-        st_keep(lse_p + r1, l1 > 0.f ? m1 + log2f(l1) : NEG_INF, keep);
-      }
-      if constexpr (FP8) {
-        // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
 #pragma unroll
-        for (int blk = 0; blk < KS; ++blk) {
-          const float* e = acc[2 * blk];
-          const float* o = acc[2 * blk + 1];
-          st_keep4(o_p + r0 * D + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
-          st_keep4(o_p + r1 * D + blk * 16 + 4 * j, e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1, keep);
+      for (int t = 0; t < MTW; ++t) {
+        const int r0 = r0s[t], r1 = r1s[t];
+        const float s0 = quad_sum(l0[t]), s1 = quad_sum(l1[t]);
+        const float inv0 = s0 > 0.f ? p.v_scale / s0 : 0.f;
+        const float inv1 = s1 > 0.f ? p.v_scale / s1 : 0.f;
+        if (j == 0) {
+          st_keep(lse_p + r0, s0 > 0.f ? m0[t] + log2f(s0) : NEG_INF, keep);
+          st_keep(lse_p + r1, s1 > 0.f ? m1[t] + log2f(s1) : NEG_INF, keep);
         }
-      } else {
+        if constexpr (FP8) {
+          // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          st_keep2(o_p + r0 * D + n * 8 + 2 * j, acc[n][0] * inv0, acc[n][1] * inv0, keep);
-          st_keep2(o_p + r1 * D + n * 8 + 2 * j, acc[n][2] * inv1, acc[n][3] * inv1, keep);
+          for (int blk = 0; blk < KS; ++blk) {
+            const float* e = acc[t][2 * blk];
+            const float* o = acc[t][2 * blk + 1];
+            st_keep4(o_p + r0 * D + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
+            st_keep4(o_p + r1 * D + blk * 16 + 4 * j, e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1, keep);
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            st_keep2(o_p + r0 * D + n * 8 + 2 * j, acc[t][n][0] * inv0, acc[t][n][1] * inv0, keep);
+            st_keep2(o_p + r1 * D + n * 8 + 2 * j, acc[t][n][2] * inv1, acc[t][n][3] * inv1, keep);
+          }
         }
       }
     }
@@ -947,15 +1004,16 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       if constexpr (kQAhead) {
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-          qf[kk][0] = qn[kk][0];
-          qf[kk][1] = qn[kk][1];
-          qf[kk][2] = qn[kk][2];
-          qf[kk][3] = qn[kk][3];
+          qf[0][kk][0] = qn[kk][0];
+          qf[0][kk][1] = qn[kk][1];
+          qf[0][kk][2] = qn[kk][2];
+          qf[0][kk][3] = qn[kk][3];
         }
-        qsc = qsc_n;
-        if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, qn);
+        qsc[0] = qsc_n;
+        if (seg_live(p, sn, end)) qsc_n = p.scale2 * load_piece_q(sn, false, r0s[0], r1s[0], qn);
       } else {
-        qsc = p.scale2 * load_piece_q(s, false, qf);
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) qsc[t] = p.scale2 * load_piece_q(s, false, r0s[t], r1s[t], qf[t]);
         q_to_smem();
       }
     }
@@ -992,7 +1050,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   // rows in slot order: pass 1 finds each row's largest log-sum-exp, pass 2
   // sums 2^(lse - max) o; two partials per trip of pass 2 at head_dim <= 128
   // keep two partials' loads in flight.
-  auto fold = [&](long long slot0, long long stride, long long count) {
+  auto fold = [&](long long slot0, long long stride, long long count, int r0, int r1) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
     m0 = NEG_INF;
@@ -1049,20 +1107,24 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       const long long gcount = min(static_cast<long long>(kGroup), c_last - gfirst + 1);
       finisher = gcount == 1 || take_ticket(p.cnt + p.nseg + gfirst + s_idx, static_cast<int>(gcount));
       if (finisher) {
-        fold(gfirst + s_idx, 1, gcount);
         // the group partial replaces the partial of the group's first piece
         const long long sl = gfirst + s_idx;
         float* lse_p = p.plse + (sl * p.HC + hc) * RM;
         float* o_p = p.po + ((sl * p.HC + hc) * RM) * D;
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-        if (j == 0) {
-          lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
-          lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
-        }
+#pragma unroll 1
+        for (int t = 0; t < MTW; ++t) {
+          const int r0 = r0s[t], r1 = r1s[t];
+          fold(gfirst + s_idx, 1, gcount, r0, r1);
+          const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+          if (j == 0) {
+            lse_p[r0] = l0 > 0.f ? m0 + log2f(l0) : NEG_INF;
+            lse_p[r1] = l1 > 0.f ? m1 + log2f(l1) : NEG_INF;
+          }
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
-          *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+          for (int n = 0; n < NT; ++n) {
+            *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+            *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+          }
         }
         __threadfence();
         named_bar_sync(1, p.nwc * 32);
@@ -1072,10 +1134,13 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       finisher = take_ticket(p.cnt + s_idx, static_cast<int>(npc));
     }
     if (finisher) {
+      // one 16-row tile of the warp at a time: merge, drafts, output
+      auto finish_tile = [&](const int r0, const int r1, const bool first_tile) {
+        uint32_t qe[KS][4];  // this tile's query fragments (bf16) for the draft block
       const int kvh = sg.hg * p.HC + hc;
       // the draft rows come from HBM: start them towards L2 now, and (head_dim
       // <= 128) load the query fragments, so both overlap the fold below
-      if (mt == 0 && !p.paged) {
+      if (first_tile && !p.paged) {
         const int a = p.qo ? __ldg(p.qo + sg.b) : sg.b * p.L;
         if (a >= 0 && static_cast<long long>(a) + p.L <= p.n_rows) {
           constexpr int LINES = D * 2 / 128;  // 128-byte lines per row
@@ -1088,13 +1153,13 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         }
       }
       int s_b = 0;
-      if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
+      if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
       // the pieces (or, for a two-level merge, the group partials) in slot order
       if (tree)
-        fold(c_first + s_idx, kGroup, ng);
+        fold(c_first + s_idx, kGroup, ng, r0, r1);
       else
-        fold(c_first + s_idx, 1, npc);
-      if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger, qf);
+        fold(c_first + s_idx, 1, npc, r0, r1);
+      if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
       // tree verify: this sequence's mask rows (row-major [L][P+L], only the
@@ -1118,7 +1183,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 #pragma unroll 1
       for (int td = 0; td * 8 < p.L; ++td) {
         // fused store (paged): quantise this tile's new draft K and V rows
-        // once, store the codes into the cache (warp mt == 0 of the head) and
+        // once, store the codes into the cache (the head's first tile) and
         // keep the dequantised values in the warp's idle ring, where the
         // fragment loads below read them
         unsigned char* stK = smem + p.ring_off + warp * (32 * D);
@@ -1143,14 +1208,14 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
               const unsigned short cv = store_e4m3x2(xv.x, xv.y, p.vq);
               dk = e4m3x2_to_bf16x2(ck);
               dv = e4m3x2_to_bf16x2(cv);
-              if (mt == 0) {
+              if (first_tile) {
                 *reinterpret_cast<unsigned short*>(kd + c) = ck;
                 *reinterpret_cast<unsigned short*>(vd + c) = cv;
               }
             } else {
               dk = store_bf16x2(xk.x, xk.y, p.kq);
               dv = store_bf16x2(xv.x, xv.y, p.vq);
-              if (mt == 0) {
+              if (first_tile) {
                 *reinterpret_cast<uint32_t*>(kd + c * 2) = dk;
                 *reinterpret_cast<uint32_t*>(vd + c * 2) = dv;
               }
@@ -1175,7 +1240,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           for (int kk = 0; kk < KS; ++kk) {
             const uint32_t b0 = kv ? *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 2 * j) * 2) : 0u;
             const uint32_t b1 = kv ? *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2) : 0u;
-            mma_bf16(sd, qf[kk], b0, b1);
+            mma_bf16(sd, qe[kk], b0, b1);
           }
         } else if (p.paged) {
           // drafts are cache positions P + t, dequantised like the prefix
@@ -1196,7 +1261,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
                 b1 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2);
               }
             }
-            mma_bf16(sd, qf[kk], b0, b1);
+            mma_bf16(sd, qe[kk], b0, b1);
           }
         } else {
           const __nv_bfloat16* kp = p.ke + (static_cast<long long>(s_b) + (kv ? tkey : 0)) * p.ke_s0 +
@@ -1205,9 +1270,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           for (int kk = 0; kk < KS; ++kk) {
             const uint32_t b0 = kv ? ld_u32(kp + kk * 16 + 2 * j) : 0u;
             const uint32_t b1 = kv ? ld_u32(kp + kk * 16 + 8 + 2 * j) : 0u;
-            mma_bf16(sd, qf[kk], b0, b1);
+            mma_bf16(sd, qe[kk], b0, b1);
           }
-          if (p.wmode == 1 && mt == 0 && kv) {
+          if (p.wmode == 1 && first_tile && kv) {
             // side store of the fresh drafts into rows out_cache_loc[s_b + t]
             const long long dst = p.ocl64 ? static_cast<const long long*>(p.ocl)[s_b + tkey]
                                           : static_cast<long long>(static_cast<const int*>(p.ocl)[s_b + tkey]);
@@ -1336,7 +1401,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             const __nv_bfloat16* vp = p.ve + (static_cast<long long>(s_b) + key) * p.ve_s0 +
                                       static_cast<long long>(kvh) * p.ve_s1 + 2 * j;
             long long vdst = -1;
-            if (p.wmode == 1 && mt == 0 && g == 0) {
+            if (p.wmode == 1 && first_tile && g == 0) {
               const long long d = p.ocl64 ? static_cast<const long long*>(p.ocl)[s_b + key]
                                           : static_cast<long long>(static_cast<const int*>(p.ocl)[s_b + key]);
               vdst = (d >= 0 && d < p.pool) ? d : -1;  // an out-of-range row is flagged by the K store
@@ -1380,6 +1445,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         for (int n = 0; n < NT; ++n)
           *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16(acc[n][2] * inv1, acc[n][3] * inv1);
       }
+      };
+#pragma unroll 1
+      for (int t = 0; t < MTW; ++t) finish_tile(r0s[t], r1s[t], mt == 0 && t == 0);
     }
     seg_advance(p, sg);
   }
@@ -1405,9 +1473,10 @@ int g_num_ctas = 0;
 long long g_min_tokens = 0;
 int g_max_stages = 0;
 int g_max_heads = 0;
+int g_tiles = 0;  // tiles per warp override (0 = default)
 
 struct Plan {
-  int gq, R, MT, HC, n_hg, nwc, threads, ek;
+  int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
   int stage_bytes, nst, ring_off, head_bytes, misc_off, misc_bytes;
   size_t smem;
   int ctas_per_sm;
@@ -1419,9 +1488,12 @@ int floor_pow2(int x) {
   return r;
 }
 
-// Chooses the CTA shape: HC KV heads per CTA x MT 16-row tiles per head, one
-// consumer warp each; ring depth from the shared-memory budget.
-bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl) {
+// Chooses the CTA shape: HC KV heads per CTA x MT 16-row tiles per head; a
+// consumer warp owns MTW tiles (two at head_dim <= 128 when a head has more
+// than one tile, so its K / V fragments feed both); ring depth from the
+// shared-memory budget.
+bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl,
+               long long total_tokens, int tiles) {
   if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
   const long long R = (h_q / h_kv) * L;
   const int maxw = D > 128 ? 4 : 8;
@@ -1431,31 +1503,42 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   int mt = 1;
   while (16 * mt < R) mt *= 2;
   pl.MT = mt;
+  // two tiles per warp pay off once there is enough prefix to stream;
+  // small problems are latency bound and want more, lighter warps
+  if (tiles == 0) tiles = g_tiles;
+  if (tiles == 0) tiles = total_tokens >= kTwoTileMinTokens ? 2 : 1;
+  pl.MTW = (D <= 128 && mt >= 2 && tiles == 2) ? 2 : 1;
+  const int wph = mt / pl.MTW;  // warps per head
   int hc = 1;
   const int hc_cap = g_max_heads > 0 ? g_max_heads : maxw;
-  while (hc * 2 * mt <= maxw && hc * 2 <= hc_cap && h_kv % (hc * 2) == 0) hc *= 2;
+  while (hc * 2 * wph <= maxw && hc * 2 <= hc_cap && h_kv % (hc * 2) == 0) hc *= 2;
   pl.HC = hc;
   pl.n_hg = static_cast<int>(h_kv / hc);
-  pl.nwc = hc * mt;
+  pl.nwc = hc * wph;
   pl.threads = pl.nwc * 32;
   pl.ek = fp8 ? 1 : 2;
   // per head: nst stages of 16 K rows + 16 V rows; per warp: the index ring,
   // the mask ring and (fp8) the bf16 widening scratch
   pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
-  const int fixed = kIdxRing * 128 + 128 + (fp8 && D == 256 ? 16 * static_cast<int>(D) * 2 : 0);
-  int k = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
-  for (;;) {
-    const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
-    const int cap = g_max_stages > 0 ? std::min(g_max_stages, kMaxStages) : kMaxStages;
-    const int nst = std::min(cap, (budget - kCtlBytes - pl.nwc * fixed) / (pl.HC * pl.stage_bytes));
-    if (nst >= 2) {
-      pl.nst = nst;
-      pl.ctas_per_sm = k;
-      break;
+  const int qsm_tiles = (fp8 && D == 256) ? 1 : (pl.MTW == 2 ? 2 : 0);  // query tiles kept in shared memory
+  const int fixed = kIdxRing * 128 + 128 + qsm_tiles * 16 * static_cast<int>(D) * 2;
+  // CTAs per SM: as many as keep about 8 warps per SM with a ring of at
+  // least 3 stages (2 if nothing better fits)
+  const int kmax = pl.nwc >= 8 ? 1 : (pl.nwc >= 4 ? 2 : 4);
+  const int cap = g_max_stages > 0 ? std::min(g_max_stages, kMaxStages) : kMaxStages;
+  pl.nst = 0;
+  for (int want = 3; want >= 2 && pl.nst == 0; --want) {
+    for (int k = kmax; k >= 1; --k) {
+      const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / k - kReservedPerCTA);
+      const int nst = std::min(cap, (budget - kCtlBytes - pl.nwc * fixed) / (pl.HC * pl.stage_bytes));
+      if (nst >= std::min(want, cap)) {
+        pl.nst = nst;
+        pl.ctas_per_sm = k;
+        break;
+      }
     }
-    if (k == 1) return fail("stage of %d bytes does not fit shared memory", pl.stage_bytes);
-    k /= 2;
   }
+  if (pl.nst < 2) return fail("stage of %d bytes does not fit shared memory", pl.stage_bytes);
   pl.head_bytes = pl.nst * pl.stage_bytes;
   pl.misc_bytes = fixed;
   pl.ring_off = kCtlBytes;
@@ -1589,16 +1672,23 @@ bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const
 
 using KernelFn = void (*)(Params);
 
-template <int D, bool FP8>
+template <int D, bool FP8, int MTW>
 KernelFn kernel_ptr() {
-  return vsk_kernel<D, FP8>;
+  return vsk_kernel<D, FP8, MTW>;
 }
 
-KernelFn pick_kernel(int D, bool fp8) {
+KernelFn pick_kernel(int D, bool fp8, int mtw) {
+  if (mtw == 2) {
+    switch (D) {
+      case 64: return fp8 ? kernel_ptr<64, true, 2>() : kernel_ptr<64, false, 2>();
+      case 128: return fp8 ? kernel_ptr<128, true, 2>() : kernel_ptr<128, false, 2>();
+      default: return nullptr;
+    }
+  }
   switch (D) {
-    case 64: return fp8 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
-    case 128: return fp8 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
-    case 256: return fp8 ? kernel_ptr<256, true>() : kernel_ptr<256, false>();
+    case 64: return fp8 ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
+    case 128: return fp8 ? kernel_ptr<128, true, 1>() : kernel_ptr<128, false, 1>();
+    case 256: return fp8 ? kernel_ptr<256, true, 1>() : kernel_ptr<256, false, 1>();
     default: return nullptr;
   }
 }
@@ -1658,14 +1748,16 @@ size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q, int6
                                   int64_t v_head_dim, int64_t max_len_extend) {
   if (num_sms <= 0 || max_bs < 1 || head_dim != v_head_dim || max_len_extend < 1) return 0;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
-  Plan pl;
-  if (!make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl)) return 0;
-  Plan pl8;
-  if (!make_plan(h_q, h_kv, head_dim, max_len_extend, true, pl8)) return 0;
   const long long n_cta = static_cast<long long>(num_sms) * 4;  // bound on CTAs per SM
-  const size_t a = ws_layout(n_cta, max_bs, pl, head_dim).total;
-  const size_t b = ws_layout(n_cta, max_bs, pl8, head_dim).total;
-  return a > b ? a : b;
+  size_t need = 0;
+  for (int fp8 = 0; fp8 < 2; ++fp8) {
+    for (int tiles = 1; tiles <= 2; ++tiles) {
+      Plan pl;
+      if (!make_plan(h_q, h_kv, head_dim, max_len_extend, fp8 != 0, pl, 0, tiles)) return 0;
+      need = std::max(need, ws_layout(n_cta, max_bs, pl, head_dim).total);
+    }
+  }
+  return need;
 }
 
 size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t v_head_dim,
@@ -1676,10 +1768,12 @@ size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t hea
   if (sms <= 0) return 0;
   size_t need = vsk_workspace_size_for_sms(sms, max_bs, h_q, h_kv, head_dim, v_head_dim, max_len_extend);
   if (g_num_ctas > 4 * sms) {
-    Plan pl;
-    if (make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl)) {
-      const size_t t = ws_layout(g_num_ctas, max_bs, pl, head_dim).total;
-      if (t > need) need = t;
+    for (int tiles = 1; tiles <= 2; ++tiles) {
+      Plan pl;
+      if (make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl, 0, tiles)) {
+        const size_t t = ws_layout(g_num_ctas, max_bs, pl, head_dim).total;
+        if (t > need) need = t;
+      }
     }
   }
   return need;
@@ -1722,6 +1816,8 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
   g_min_tokens = min_tokens_per_cta > 0 ? min_tokens_per_cta : 0;
 }
 
+void vsk_set_tuning_tiles(int tiles_per_warp) { g_tiles = tiles_per_warp == 1 || tiles_per_warp == 2 ? tiles_per_warp : 0; }
+
 void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta) {
   g_max_stages = max_ring_stages >= 2 ? max_ring_stages : 0;
   g_max_heads = max_kv_heads_per_cta > 0 ? max_kv_heads_per_cta : 0;
@@ -1739,13 +1835,13 @@ namespace vsk {
 static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
                             void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
   Plan pl;
-  if (!make_plan(h_q, h_kv, D, L, fp8, pl)) return 0;
+  if (!make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0)) return 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
   const int sms = device_sms(dev);
   if (sms <= 0) return fail("cannot query the SM count of device %d", dev);
-  KernelFn fn = pick_kernel(static_cast<int>(D), fp8);
+  KernelFn fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
   if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);
@@ -2116,12 +2212,12 @@ extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor*
   const long long h_q = q->shape[1], h_kv = ke->shape[1], D = q->shape[2];
   const bool fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
   Plan pl;
-  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl)) return 0;
+  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl, (kvi->shape[0] / B) * B, 0)) return 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
   const int sms = device_sms(dev);
-  KernelFn fn = pick_kernel(static_cast<int>(D), fp8);
+  KernelFn fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
   if (sms <= 0 || !fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);

@@ -582,3 +582,34 @@ def test_one_workspace_serves_calls_of_any_shape(vsk):
                 vsk.set_tuning(0, 0)
             assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (i, spec.name)
     assert vsk.read_error_flags(shared) == 0
+
+
+TILES = [
+    workloads.Spec("tiles_r32", (700, 0, 2100), 4, 16, 2, 128, 128, perm=True, seed=601),
+    workloads.Spec("tiles_r64_fp8", (333, 1500), 8, 8, 1, 128, 128, pool="e4m3", perm=True, k_scale=0.5,
+                   v_scale=0.75, seed=602),
+    workloads.Spec("tiles_r128_d64", (90, 1200), 8, 16, 1, 64, 64, perm=True, seed=603),
+    workloads.Spec("tiles_r32_tree", (40, 900), 4, 8, 1, 128, 128, perm=True, tree="random", seed=604),
+    workloads.Spec("tiles_r32_paged_fp8", (17, 1000), 4, 16, 2, 128, 128, pool="e4m3", perm=True, page_size=16,
+                   k_scale=1.5, v_scale=0.5, seed=605),
+]
+
+
+@pytest.mark.parametrize("tiles", [1, 2])
+@pytest.mark.parametrize("spec", TILES, ids=lambda s: s.name)
+def test_one_or_two_tiles_per_warp(vsk, spec, tiles):
+    """Packed rows > 16 at head_dim <= 128: each consumer warp serves one or
+    two 16-row tiles; both CTA shapes match the oracle."""
+    p = gpu_problem(spec)
+    vsk.set_tuning_tiles(tiles)
+    try:
+        if spec.tree:
+            o = run_tree(vsk, p)
+        elif spec.page_size:
+            o = run_paged(vsk, p)
+        else:
+            o = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning_tiles(0)
+    check(o, oracle_o(p))
+    assert vsk.read_error_flags() == 0
