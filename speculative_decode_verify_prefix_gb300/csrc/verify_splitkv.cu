@@ -10,19 +10,23 @@
 //   * ONE persistent kernel per call.  The flattened work space (sequence b,
 //     KV-head group hg, prefix token t) is cut into equal contiguous shares,
 //     one per CTA; grid = SMs x CTAs-per-SM from static shapes, the split
-//     itself is computed on the device from kv_indptr, so no host
-//     synchronisation is needed.
-//   * Warp (hc, mt) of a CTA owns one KV head of the group and one 16-row tile
-//     of its packed queries (all h_q/h_kv query heads x l_ext draft rows), so
-//     each K/V byte is read from HBM once.  It streams its head's K and V row
-//     slices itself with 16-byte cp.async into a private XOR-swizzled ring
-//     (indices prefetched by cp.async, completion by wait_group: no producer
-//     warp, no mbarrier, no spin-wait) and runs bf16 mma.sync m16n8k16 for QK
-//     and PV with an fp32 online softmax.
+//     itself is computed on the device from kv_indptr (or seq_lens), so no
+//     host synchronisation is needed.
+//   * A CTA serves a group of KV heads.  The packed queries of a head (all
+//     h_q/h_kv query heads x l_ext draft rows) form 16-row tiles; a warp owns
+//     one head and one or two tiles, so each K/V byte is read from HBM once.
+//     The warps of a head stream its K and V row slices themselves with
+//     16-byte cp.async into the head's XOR-swizzled ring (indices or page ids
+//     prefetched by cp.async, completion by wait_group: no producer warp, no
+//     mbarrier, no spin-wait) and run mma.sync m16n8k16 for QK and PV (bf16;
+//     f16 straight from e4m3 rows for an fp8 pool) with an fp32 online
+//     softmax.
 //   * Piece ends only write log-sum-exp partials.  After streaming, the CTA
 //     that draws a segment's last ticket (atomic, no wait) merges the pieces
-//     in CTA order and continues the same online softmax over the causal
-//     draft keys, then writes bf16 output.
+//     in CTA order (in two levels for long segments) and continues the same
+//     online softmax over the draft keys (causal, tree mask, or drafts read
+//     from a paged cache; optionally storing new drafts into the cache), then
+//     writes bf16 output.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -85,7 +89,7 @@ struct Params {
   long long n_idx, pool, n_rows;
   int B, L, gq, R, HC, MT, n_hg, nwc, nst;
   int ring_off, head_bytes;  // ring of KV head hc at ring_off + hc * head_bytes
-  int misc_off, misc_bytes;  // warp w's index / mask rings (and fp8 scratch) at misc_off + w * misc_bytes
+  int misc_off, misc_bytes;  // warp w's index / mask rings (and query tiles) at misc_off + w * misc_bytes
   float scale2, dscale2, v_scale;
   float dvs;  // multiplier of draft values (v_scale when drafts come from the cache)
   // drafts already in a paged cache: block table of page ids, prefix lengths
@@ -439,14 +443,14 @@ __device__ __forceinline__ int chunk_swz(int t) {
 //   [0,   128)  control: sched base (i64) @0, sched b @8, ticket flags [2] @16
 //   [128, 256)  block-scan scratch (up to 16 x i64)
 //   [ring_off + hc * head_bytes, ...)  the ring of KV head hc, shared by the
-//        MT warps that serve it (each copies 16/MT of every stage's tokens):
-//        nst stages of K rows [16][D*e] then V rows [16][D*e] (bf16 rows are
-//        XOR-swizzled in 16-byte chunks, chunk ^ (token & 7), so 8-row ldmatrix
-//        phases hit 8 distinct bank groups).  After streaming, the first
-//        nwc * 32 * D bytes hold each warp's staged new drafts (fused store).
+//        warps that serve it (each copies its share of every stage's tokens):
+//        nst stages of K rows [16][D*e] then V rows [16][D*e], XOR-swizzled in
+//        16-byte chunks (chunk_swz) so 8-row ldmatrix phases hit 8 distinct
+//        bank groups.  After streaming, the first nwc * 32 * D bytes hold each
+//        warp's staged new drafts (fused store).
 //   [misc_off + w * misc_bytes, ...)  warp w's own kIdxRing x 16 x 8 B of
-//        kv_indices, 16 x 4 B valid-token masks and, fp8 only, bf16 K and V
-//        rows, 16 x (D+8) each.
+//        kv_indices, 16 x 4 B valid-token masks and, for two-tile warps and
+//        e4m3 pools at head_dim 256, its query tiles (16 x D x 2 B each).
 // ---------------------------------------------------------------------------
 template <int D>
 struct MaxWarps {
@@ -540,12 +544,13 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   seg0.off = *ctl_base + static_cast<long long>(seg0.hg) * seg0.len;
 
   // ============================ per-warp pipeline ============================
-  // Warp w serves KV head hc = w / MT of the group and the 16-row tile mt of
-  // its packed query rows.  The MT warps of a head stream its K and V rows
-  // themselves with 16-byte cp.async into the head's nst-deep ring, each
-  // copying 16/MT tokens of every stage; with MT > 1 they meet at a named
-  // barrier once per stage.  No producer warp.  Indices come kIdxAhead stages
-  // ahead, also by cp.async, into each warp's own index ring.
+  // Warp w serves KV head hc = w / WPH of the group and MTW 16-row tiles
+  // (from tile mt * MTW) of its packed query rows.  The WPH warps of a head
+  // stream its K and V rows themselves with 16-byte cp.async into the head's
+  // nst-deep ring, each copying 16/WPH tokens of every stage; with WPH > 1
+  // they meet at a named barrier once per stage.  No producer warp.  Indices
+  // come kIdxAhead stages ahead, also by cp.async, into each warp's own index
+  // ring.
   const int WPH = p.MT / MTW;  // warps per KV head; each owns MTW 16-row tiles
   const int hc = warp / WPH;
   const int mt = warp % WPH;
@@ -1518,7 +1523,7 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.threads = pl.nwc * 32;
   pl.ek = fp8 ? 1 : 2;
   // per head: nst stages of 16 K rows + 16 V rows; per warp: the index ring,
-  // the mask ring and (fp8) the bf16 widening scratch
+  // the mask ring and (two-tile warps; e4m3 pools at head_dim 256) the query tiles
   pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
   const int qsm_tiles = (fp8 && D == 256) ? 1 : (pl.MTW == 2 ? 2 : 0);  // query tiles kept in shared memory
   const int fixed = kIdxRing * 128 + 128 + qsm_tiles * 16 * static_cast<int>(D) * 2;
