@@ -269,6 +269,16 @@ void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta);
  * result.  Process-wide; not thread-safe. */
 void vsk_set_tuning_tiles(int tiles_per_warp);
 
+/* Tuning switch, for A/B runs and tests: mode 1 sends head_dim 256 calls with
+ * at most 32 packed query rows per KV head ((h_q / h_kv) * max_len_extend <=
+ * 32) through the tensor-memory form of the prefix stream (tcgen05.mma with
+ * accumulators in TMEM, one launch) followed by the epilogue of the mma.sync
+ * kernel (a second launch on the same stream); any other value (and the
+ * default) keeps every call on the mma.sync kernel, which is the faster of the
+ * two on GB300 at these shapes.  Both forms compute the same result up to
+ * rounding order.  Process-wide; not thread-safe. */
+void vsk_set_tuning_tc(int mode);
+
 /* Size, in bytes, of the scratch array built into the library for
  * verify_splitkv_fwd_noalloc (32 MiB). */
 #define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)

@@ -30,7 +30,8 @@ def nvcc_path() -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the CUDA library for sm_103a (no-op when up to date)."""
     os.makedirs(BUILD_DIR, exist_ok=True)
-    deps = [SRC, HEADER]
+    deps = [SRC, HEADER] + [os.path.join(_HERE, "csrc", n) for n in os.listdir(os.path.join(_HERE, "csrc"))
+                            if n.endswith((".cu", ".cuh"))]
     if not force and os.path.exists(LIB_PATH):
         if os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps):
             return LIB_PATH
@@ -95,6 +96,8 @@ def _bind(lib):
     lib.vsk_set_tuning.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.vsk_set_tuning_tiles.restype = None
     lib.vsk_set_tuning_tiles.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_tc.restype = None
+    lib.vsk_set_tuning_tc.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_shape.restype = None
     lib.vsk_set_tuning_shape.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.vsk_last_error.restype = ctypes.c_char_p

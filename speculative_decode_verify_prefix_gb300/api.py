@@ -268,5 +268,12 @@ def set_tuning_tiles(tiles_per_warp: int = 0) -> None:
     _native.lib().vsk_set_tuning_tiles(int(tiles_per_warp))
 
 
+def set_tuning_tc(enabled: bool = False) -> None:
+    """Route head_dim 256 calls (at most 32 packed rows per KV head) through the
+    tensor-memory stream (``enabled=True``) or through the mma.sync kernel (the
+    default, faster on GB300 at these shapes); for A/B runs and tests."""
+    _native.lib().vsk_set_tuning_tc(1 if enabled else 0)
+
+
 def version() -> str:
     return _native.lib().vsk_version().decode()

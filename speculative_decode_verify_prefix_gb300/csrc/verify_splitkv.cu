@@ -457,7 +457,9 @@ struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
 
-template <int D, bool FP8, int MTW>
+// EPI: the epilogue alone, after vtc_kernel has written every piece's
+// partial (same grid, share floor and plan fields, so the same pieces).
+template <int D, bool FP8, int MTW, bool EPI>
 __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -574,6 +576,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   const int c_self = blockIdx.x;
   const bool flagger = (warp == 0 && lane == 0);
 
+  if constexpr (!EPI) {
   int dslot = 0;  // ring slot of the next data job (job % nst, kept without a division)
   auto issue_idx = [&](const StageIt& it, long long job) {
     if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
@@ -1023,6 +1026,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       }
     }
   }
+  }  // !EPI
 
   // ================= epilogue: tickets, log-sum-exp merges, drafts, output =================
   // No copy is left in flight, and every partial this thread wrote is made
@@ -1458,6 +1462,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   }
 }
 
+#include "verify_tc.cuh"
+
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
@@ -1479,6 +1485,7 @@ long long g_min_tokens = 0;
 int g_max_stages = 0;
 int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
+int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
 
 struct Plan {
   int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
@@ -1552,6 +1559,40 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.misc_off = pl.ring_off + rings;
   pl.smem = static_cast<size_t>(pl.misc_off) + static_cast<size_t>(pl.nwc) * pl.misc_bytes;
   if (pl.smem > static_cast<size_t>(kSmemPerCTAMax)) return fail("shared memory plan of %zu bytes too large", pl.smem);
+  return true;
+}
+
+// The tensor-memory stream (vtc_kernel) serves head_dim 256 with at most 32
+// packed query rows per KV head.
+bool tc_eligible(long long h_q, long long h_kv, long long D, long long L) {
+  if (g_tc != 1 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
+  return (h_q / h_kv) * L <= 32;
+}
+
+// Plan fields of a tensor-memory call: one KV head per segment, RM = 16 or
+// 32 packed rows (MT = RM / 16 tiles); the epilogue kernel runs MT warps
+// and keeps its staged drafts (paged fused store) after the control block.
+bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl) {
+  if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
+  const long long R = (h_q / h_kv) * L;
+  if (R > 32) return fail("packed rows %lld exceed 32", R);
+  pl.gq = static_cast<int>(h_q / h_kv);
+  pl.R = static_cast<int>(R);
+  pl.MT = R <= 16 ? 1 : 2;
+  pl.MTW = 1;
+  pl.HC = 1;
+  pl.n_hg = static_cast<int>(h_kv);
+  pl.nwc = pl.MT;
+  pl.threads = pl.nwc * 32;
+  pl.ek = fp8 ? 1 : 2;
+  pl.stage_bytes = 0;
+  pl.nst = 0;
+  pl.ring_off = kCtlBytes;
+  pl.head_bytes = 0;
+  pl.misc_bytes = 0;
+  pl.misc_off = kCtlBytes + pl.nwc * 32 * static_cast<int>(D);
+  pl.smem = static_cast<size_t>(pl.misc_off);
+  pl.ctas_per_sm = 1;
   return true;
 }
 
@@ -1679,7 +1720,7 @@ using KernelFn = void (*)(Params);
 
 template <int D, bool FP8, int MTW>
 KernelFn kernel_ptr() {
-  return vsk_kernel<D, FP8, MTW>;
+  return vsk_kernel<D, FP8, MTW, false>;
 }
 
 KernelFn pick_kernel(int D, bool fp8, int mtw) {
@@ -1696,6 +1737,25 @@ KernelFn pick_kernel(int D, bool fp8, int mtw) {
     case 256: return fp8 ? kernel_ptr<256, true, 1>() : kernel_ptr<256, false, 1>();
     default: return nullptr;
   }
+}
+
+KernelFn pick_tc_kernel(bool fp8, int rm) {
+  if (rm == 16) return fp8 ? static_cast<KernelFn>(vtc_kernel<256, true, 16>) : static_cast<KernelFn>(vtc_kernel<256, false, 16>);
+  return fp8 ? static_cast<KernelFn>(vtc_kernel<256, true, 32>) : static_cast<KernelFn>(vtc_kernel<256, false, 32>);
+}
+
+KernelFn pick_epi_kernel(bool fp8) {
+  return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, true>) : static_cast<KernelFn>(vsk_kernel<256, false, 1, true>);
+}
+
+// Ring entries and shared memory of vtc_kernel (e4m3 pools: an even number
+// of entries, so that V rows always sit in odd entries).
+template <bool FP8, int RM>
+void tc_smem(int& ne, size_t& smem) {
+  using G = tc::Geo<256, FP8, RM>;
+  ne = std::min(tc::kMaxNE, (kSmemPerCTAMax - G::ring_off) / G::ENT);
+  if (FP8) ne &= ~1;
+  smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::ENT;
 }
 
 int prepare_kernel(KernelFn fn) {
@@ -1762,6 +1822,9 @@ size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q, int6
       need = std::max(need, ws_layout(n_cta, max_bs, pl, head_dim).total);
     }
   }
+  Plan tp;
+  if (head_dim == 256 && (h_q / h_kv) * max_len_extend <= 32 && make_tc_plan(h_q, h_kv, head_dim, max_len_extend, false, tp))
+    need = std::max(need, ws_layout(n_cta, max_bs, tp, head_dim).total);
   return need;
 }
 
@@ -1779,6 +1842,12 @@ size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t hea
         const size_t t = ws_layout(g_num_ctas, max_bs, pl, head_dim).total;
         if (t > need) need = t;
       }
+    }
+    Plan tp;
+    if (head_dim == 256 && h_kv > 0 && h_q % h_kv == 0 && (h_q / h_kv) * max_len_extend <= 32 &&
+        make_tc_plan(h_q, h_kv, head_dim, max_len_extend, false, tp)) {
+      const size_t t = ws_layout(g_num_ctas, max_bs, tp, head_dim).total;
+      if (t > need) need = t;
     }
   }
   return need;
@@ -1823,6 +1892,8 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
 
 void vsk_set_tuning_tiles(int tiles_per_warp) { g_tiles = tiles_per_warp == 1 || tiles_per_warp == 2 ? tiles_per_warp : 0; }
 
+void vsk_set_tuning_tc(int mode) { g_tc = mode == 1 ? 1 : 0; }
+
 void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta) {
   g_max_stages = max_ring_stages >= 2 ? max_ring_stages : 0;
   g_max_heads = max_kv_heads_per_cta > 0 ? max_kv_heads_per_cta : 0;
@@ -1839,19 +1910,42 @@ namespace vsk {
 // the plan-dependent fields of p and launches the kernel.
 static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
                             void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
+  const bool use_tc = tc_eligible(h_q, h_kv, D, L);
   Plan pl;
-  if (!make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0)) return 0;
+  if (use_tc ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl) : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0))
+    return 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
   const int sms = device_sms(dev);
   if (sms <= 0) return fail("cannot query the SM count of device %d", dev);
-  KernelFn fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
-  if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
+  // the streaming kernel (the whole call on the mma.sync path; the prefix
+  // stream on the tensor-memory path, followed by the epilogue kernel)
+  KernelFn fn = nullptr, fn_epi = nullptr;
+  int threads = pl.threads;
+  size_t smem = pl.smem;
+  int per_sm = pl.ctas_per_sm;
+  if (use_tc) {
+    const int rm = 16 * pl.MT;
+    fn = pick_tc_kernel(fp8, rm);
+    fn_epi = pick_epi_kernel(fp8);
+    if (!prepare_kernel(fn) || !prepare_kernel(fn_epi)) return fail("tensor-memory kernels unavailable");
+    int ne = 0;
+    if (fp8)
+      rm == 16 ? tc_smem<true, 16>(ne, smem) : tc_smem<true, 32>(ne, smem);
+    else
+      rm == 16 ? tc_smem<false, 16>(ne, smem) : tc_smem<false, 32>(ne, smem);
+    if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
+    pl.nst = ne;
+    threads = tc::kThreads;
+  } else {
+    fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
+    if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
+  }
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), threads, smem);
   if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
-  const int per_sm = std::min(occ, pl.ctas_per_sm);
+  per_sm = std::min(occ, per_sm);
   const long long n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
   const WsLayout wl = ws_layout(n_cta, B, pl, D);
 
@@ -1896,9 +1990,15 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
   p.po = reinterpret_cast<float*>(ws + wl.o_off);
   void* args[] = {&p};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads), args,
-                       pl.smem, st);
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(threads), args,
+                       smem, st);
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
+  if (fn_epi) {
+    // same grid and share floor: the epilogue kernel finds the same pieces
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_epi), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads),
+                         args, pl.smem, st);
+    if (e != cudaSuccess) return fail("epilogue kernel launch failed: %s", cudaGetErrorString(e));
+  }
   return 1;
 }
 
