@@ -289,3 +289,45 @@ def test_tc_fp8_long_sampled(vsk):
     assert vsk.read_error_flags() == 0
     del p
     torch.cuda.empty_cache()
+
+
+def _tc_cases(n=24, seed=2025):
+    """Seeded random head_dim 256 problems the tensor-memory stream serves
+    (at most 32 packed rows per KV head): lengths, head layouts, pools, scales,
+    index dtypes, forms (causal, tree, paged) and CTA splits."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        h_kv = int(rng.choice([1, 2, 4, 8]))
+        L = int(rng.integers(1, 9))
+        gq = int(rng.choice([g for g in (1, 2, 4, 8) if g * L <= 32]))
+        B = int(rng.integers(1, 6))
+        kind = rng.choice(["empty", "short", "mid", "long"], size=B, p=[0.1, 0.3, 0.4, 0.2])
+        lens = tuple(int({"empty": 0, "short": rng.integers(1, 70), "mid": rng.integers(70, 700),
+                          "long": rng.integers(700, 3000)}[k]) for k in kind)
+        form = str(rng.choice(["flat", "tree", "paged"], p=[0.5, 0.2, 0.3]))
+        pool = str(rng.choice(["bf16", "e4m3"]))
+        ks = float(rng.choice([1.0, 0.5, 1.5])) if pool == "e4m3" else float(rng.choice([1.0, 0.75]))
+        vs = float(rng.choice([1.0, 0.5, 2.0])) if pool == "e4m3" else float(rng.choice([1.0, 1.25]))
+        spec = S(f"tcfuzz{i}_{form}", lens, L, gq * h_kv, h_kv, 256, 256, pool=pool, perm=bool(rng.integers(0, 2)),
+                 k_scale=ks, v_scale=vs, idx_dtype=str(rng.choice(["int32", "int64"])),
+                 pool_extra=int(rng.integers(0, 64)), poison=bool(rng.integers(0, 2)),
+                 tree="random" if form == "tree" else "",
+                 page_size=int(rng.choice([1, 3, 16, 64])) if form == "paged" else 0, seed=4000 + i)
+        tuning = (0, 0) if rng.random() < 0.6 else (int(rng.integers(1, 400)), 16)
+        out.append((spec, form, tuning))
+    return out
+
+
+@pytest.mark.parametrize("case", _tc_cases(), ids=lambda c: c[0].name)
+def test_tc_random_problem_matches_oracle(vsk, case):
+    spec, form, (nc, mt) = case
+    p = workloads.make_problem(spec, "cuda")
+    vsk.read_error_flags()
+    vsk.set_tuning(nc, mt)
+    try:
+        o = run_tree(vsk, p) if form == "tree" else run_paged(vsk, p) if form == "paged" else run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
+    check(o, oracle_o(p))
+    assert vsk.read_error_flags() == 0
