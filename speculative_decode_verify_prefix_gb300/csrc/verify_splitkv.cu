@@ -438,48 +438,20 @@ __device__ __forceinline__ int chunk_swz(int t) {
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.
-// Shared memory map (bytes):
-//   [0,   128)  control: sched base (i64) @0, sched b @8, ticket flags [2] @16
-//   [128, 256)  block-scan scratch (up to 16 x i64)
-//   [ring_off + hc * head_bytes, ...)  the ring of KV head hc, shared by the
-//        warps that serve it (each copies its share of every stage's tokens):
-//        nst stages of K rows [16][D*e] then V rows [16][D*e], XOR-swizzled in
-//        16-byte chunks (chunk_swz) so 8-row ldmatrix phases hit 8 distinct
-//        bank groups.  After streaming, the first nwc * 32 * D bytes hold each
-//        warp's staged new drafts (fused store).
-//   [misc_off + w * misc_bytes, ...)  warp w's own kIdxRing x 16 x 8 B of
-//        kv_indices, 16 x 4 B valid-token masks and, for two-tile warps and
-//        e4m3 pools at head_dim 256, its query tiles (16 x D x 2 B each).
+// This CTA's share of the work: the segments (b, hg) of virtual length
+// max(P_b, 1) are laid end to end and CTA c owns positions [c W, c W + W),
+// W = max(ceil(total / gridDim.x), w_min).  A block scan of the prefix lengths
+// (kv_indptr or seq_lens) gives the total and the segment holding `start`; no
+// host synchronisation.  Every kernel that writes or reads a call's pieces
+// cuts the space this way.  All threads of the block call it (it uses
+// __syncthreads and shared memory [0, 256)); false: the CTA has no work.
 // ---------------------------------------------------------------------------
-template <int D>
-struct MaxWarps {
-  static constexpr int value = (D > 128) ? 4 : 8;
-};
-
-// EPI: the epilogue alone, after vtc_kernel has written every piece's
-// partial (same grid, share floor and plan fields, so the same pieces).
-template <int D, bool FP8, int MTW, bool EPI>
-__global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
-    vsk_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(1024) unsigned char smem[];
-  constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
-  constexpr int NT = D / 8;        // n-tiles of the output row
-  constexpr int KS = D / 16;       // k-steps of the QK contraction
-  constexpr int ROWB = D * EK;     // bytes of one head's K (or V) row
-  constexpr int CPR = ROWB / 16;   // 16-byte chunks per row
-  constexpr int STAGE_B = 2 * kStageTokens * ROWB;
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
+__device__ __forceinline__ bool cta_share(const Params& p, unsigned char* smem, long long& start, long long& end,
+                                          long long& W, Seg& seg0) {
   long long* ctl_base = reinterpret_cast<long long*>(smem);
   int* ctl_b = reinterpret_cast<int*>(smem + 8);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);  // [2]
   long long* scan_ws = reinterpret_cast<long long*>(smem + 128);
-  const int nst = p.nst;
-
-  // ---- prologue: total virtual length and this CTA's starting segment ----
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) *ctl_b = -1;
   const int nthreads = blockDim.x;
   const int per = (p.B + nthreads - 1) / nthreads;
@@ -515,11 +487,11 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   __syncthreads();
   const long long excl = (warp > 0 ? scan_ws[warp - 1] : 0) + incl - mysum;
   const long long tot = scan_ws[nwarps - 1] * p.n_hg;
-  long long W = (tot + gridDim.x - 1) / gridDim.x;
+  W = (tot + gridDim.x - 1) / gridDim.x;
   if (W < p.w_min) W = p.w_min;
-  const long long start = static_cast<long long>(blockIdx.x) * W;
-  if (start >= tot) return;  // uniform: the whole CTA has no work
-  const long long end = min(tot, start + W);
+  start = static_cast<long long>(blockIdx.x) * W;
+  if (start >= tot) return false;  // uniform
+  end = min(tot, start + W);
   {
     long long off = excl;
     for (int b = b_lo; b < b_hi; ++b) {
@@ -536,14 +508,58 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     }
   }
   __syncthreads();
-
-  Seg seg0;
   seg0.b = *ctl_b;
-  if (seg0.b < 0) return;  // unreachable for consistent inputs; guards the walk
+  if (seg0.b < 0) return false;  // unreachable for consistent inputs; guards the walk
   load_seq(p, seg0.b, seg0.P, seg0.kv0);
   seg0.len = max(seg0.P, 1);
   seg0.hg = static_cast<int>((start - *ctl_base) / seg0.len);
   seg0.off = *ctl_base + static_cast<long long>(seg0.hg) * seg0.len;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// Shared memory map (bytes):
+//   [0,   128)  control: sched base (i64) @0, sched b @8, ticket flags [2] @16
+//   [128, 256)  block-scan scratch (up to 16 x i64)
+//   [ring_off + hc * head_bytes, ...)  the ring of KV head hc, shared by the
+//        warps that serve it (each copies its share of every stage's tokens):
+//        nst stages of K rows [16][D*e] then V rows [16][D*e], XOR-swizzled in
+//        16-byte chunks (chunk_swz) so 8-row ldmatrix phases hit 8 distinct
+//        bank groups.  After streaming, the first nwc * 32 * D bytes hold each
+//        warp's staged new drafts (fused store).
+//   [misc_off + w * misc_bytes, ...)  warp w's own kIdxRing x 16 x 8 B of
+//        kv_indices, 16 x 4 B valid-token masks and, for two-tile warps and
+//        e4m3 pools at head_dim 256, its query tiles (16 x D x 2 B each).
+// ---------------------------------------------------------------------------
+template <int D>
+struct MaxWarps {
+  static constexpr int value = (D > 128) ? 4 : 8;
+};
+
+// EPI: the epilogue alone, after vtc_kernel has written every piece's
+// partial (same grid, share floor and plan fields, so the same pieces).
+template <int D, bool FP8, int MTW, bool EPI>
+__global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
+    vsk_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
+  constexpr int NT = D / 8;        // n-tiles of the output row
+  constexpr int KS = D / 16;       // k-steps of the QK contraction
+  constexpr int ROWB = D * EK;     // bytes of one head's K (or V) row
+  constexpr int CPR = ROWB / 16;   // 16-byte chunks per row
+  constexpr int STAGE_B = 2 * kStageTokens * ROWB;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);  // [2]
+  const int nst = p.nst;
+
+  // ---- prologue: this CTA's share of the flattened space and its first segment ----
+  long long start, end, W;
+  Seg seg0;
+  if (!cta_share(p, smem, start, end, W, seg0)) return;  // uniform: the whole CTA has no work
 
   // ============================ per-warp pipeline ============================
   // Warp w serves KV head hc = w / WPH of the group and MTW 16-row tiles

@@ -315,80 +315,6 @@ __device__ __forceinline__ int warp_rows_reduce(float (&v)[N], int lane) {
 
 }  // namespace tc
 
-// Finds this CTA's share of the flattened (segment, token) space, exactly as
-// vsk_kernel does (the two kernels of a call must cut it identically).
-// All threads of the block call it; false: the CTA has no work.
-__device__ __forceinline__ bool tc_share(const Params& p, unsigned char* smem, long long& start, long long& end,
-                                          Seg& seg0) {
-  long long* ctl_base = reinterpret_cast<long long*>(smem);
-  int* ctl_b = reinterpret_cast<int*>(smem + 8);
-  long long* scan_ws = reinterpret_cast<long long*>(smem + 128);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) *ctl_b = -1;
-  const int nthreads = blockDim.x;
-  const int per = (p.B + nthreads - 1) / nthreads;
-  const int b_lo = min(p.B, tid * per);
-  const int b_hi = min(p.B, b_lo + per);
-  long long mysum = 0;
-  bool bad_kvp = false;
-  for (int b = b_lo; b < b_hi; ++b) {
-    int P;
-    long long kv0;
-    bad_kvp |= !seq_info(p, b, P, kv0);
-    mysum += max(P, 1);
-  }
-  if (bad_kvp && blockIdx.x == 0) atomicOr(p.err, kErrBadKvIndptr);
-  long long incl = mysum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  const int nwarps = nthreads >> 5;
-  if (lane == 31) scan_ws[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    long long w = lane < nwarps ? scan_ws[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w += y;
-    }
-    if (lane < nwarps) scan_ws[lane] = w;
-  }
-  __syncthreads();
-  const long long excl = (warp > 0 ? scan_ws[warp - 1] : 0) + incl - mysum;
-  const long long tot = scan_ws[nwarps - 1] * p.n_hg;
-  long long W = (tot + gridDim.x - 1) / gridDim.x;
-  if (W < p.w_min) W = p.w_min;
-  start = static_cast<long long>(blockIdx.x) * W;
-  if (start >= tot) return false;
-  end = min(tot, start + W);
-  {
-    long long off = excl;
-    for (int b = b_lo; b < b_hi; ++b) {
-      int P;
-      long long kv0;
-      load_seq(p, b, P, kv0);
-      const long long len = max(P, 1);
-      const long long base = off * p.n_hg;
-      if (start >= base && start < base + len * p.n_hg) {
-        *ctl_b = b;
-        *ctl_base = base;
-      }
-      off += len;
-    }
-  }
-  __syncthreads();
-  seg0.b = *ctl_b;
-  if (seg0.b < 0) return false;
-  load_seq(p, seg0.b, seg0.P, seg0.kv0);
-  seg0.len = max(seg0.P, 1);
-  seg0.hg = static_cast<int>((start - *ctl_base) / seg0.len);
-  seg0.off = *ctl_base + static_cast<long long>(seg0.hg) * seg0.len;
-  return true;
-}
-
 // Successive 64-key tiles of this CTA's share (pieces without a real token
 // are skipped): segment, first token, end of the piece's real tokens.
 struct TileIt {
@@ -533,10 +459,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1) vtc_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NE = p.nst;
 
-  long long start, end;
+  long long start, end, W;
   Seg seg0;
-  if (!tc_share(p, smem, start, end, seg0)) return;  // uniform: no work
-  if ((smem_u32(smem) & 1023u) != 0u) {               // the swizzled layouts need 1024-byte alignment
+  if (!cta_share(p, smem, start, end, W, seg0)) return;  // uniform: no work
+  // The 128-byte swizzled layouts need a 1024-byte aligned base.  Dynamic
+  // shared memory of a kernel without static shared memory starts there; were
+  // it not so, the CTA reports the pipeline error bit and writes nothing.
+  if ((smem_u32(smem) & 1023u) != 0u) {
     if (tid == 0) atomicOr(p.err, kErrTimeout);
     return;
   }
