@@ -240,9 +240,13 @@ int vsk_workspace_init(void* workspace, size_t bytes, void* stream);
  * (NULL: the library-owned workspace of the current device) into *flags and
  * clears it.  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
  * not non-decreasing or beyond kv_indices; 4 = qo_indptr inconsistent with
- * l_ext; 8 = reserved for a timed-out wait inside the kernel (this build's
- * kernel has no waits that can time out and never sets it); 16 = a
- * mask_indptr entry of verify_splitkv_tree_fwd outside custom_mask.  Returns 1 on success, 0 on a CUDA error.
+ * l_ext; 8 = a pipeline wait that gave up after one second (only the
+ * tensor-memory form of the stream, selected by vsk_set_tuning_tc(1), has
+ * such waits: its CTA then stops streaming, frees its tensor memory and
+ * exits, and that call's output is not valid; the default kernel has no
+ * waits that can time out); 16 = a mask_indptr entry of
+ * verify_splitkv_tree_fwd outside custom_mask.  Returns 1 on success, 0 on a
+ * CUDA error.
  * Intended for tests and debugging: it blocks the host. */
 int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags);
 

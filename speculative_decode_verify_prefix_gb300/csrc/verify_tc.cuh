@@ -31,7 +31,7 @@
 //              cp.async.mbarrier.arrive.noinc (seven warps, since the copies a
 //              single warp keeps in flight are limited).
 // Operands in shared memory use the 128-byte swizzled canonical layouts:
-//   K tile, Q          K-major   [64-element column block][row][128 B]
+//   K tile, Q          K-major   [128-byte column block][row][128 B]
 //   V tile (A = V^T)   MN-major  [64-dv block][key][128 B]   (same bytes as
 //                      a K-major row store: one loader code serves both)
 //   P^T (B)            MN-major  [key][128 B] (RM <= 64 rows in one block)

@@ -138,6 +138,10 @@ EDGE = [
                    v_scale=1.5, seed=109),
     workloads.Spec("hkv6", (200, 90), 3, 12, 6, 128, 128, perm=True, seed=110),
     workloads.Spec("single_seq_long", (20000,), 4, 8, 2, 128, 128, perm=True, seed=111),
+    # 600 short sequences: the block scan gives each thread several sequences
+    workloads.Spec("many_short_seqs", None, 2, 8, 2, 64, 64, perm=True, batch=600, len_range=(0, 40), seed=119),
+    # one 200k-token prefix: a long segment merged in two levels
+    workloads.Spec("one_200k_prefix", (200000,), 4, 16, 2, 128, 128, perm=True, seed=120),
 ]
 
 
