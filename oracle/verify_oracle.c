@@ -20,7 +20,7 @@
  *   merges of the method only reorder this sum, so the oracle materialises the
  *   whole score row instead and never splits.
  *
- * Readings taken where the page is silent (each one restated in the design doc):
+ * Readings taken where the page is silent:
  *   - empty prefix (P_b = 0): the output is causal attention over the drafts
  *     alone (the page's stage-2 merge would produce NaN there);
  *   - k_scale and v_scale are dequantisation multipliers on prefix scores and
