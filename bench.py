@@ -426,7 +426,13 @@ def run_ours(args, dist: Dist) -> dict:
     peak, peak_kind = hbm_peak()
     achieved = nbytes / launch_s / 1e9
     traffic = traffic_per_launch(args.workload + ("_tc" if tc else ""))
+    if prob.get("block_table") is not None:
+        tokens = B * prob["block_table"].shape[1] * prob["page_size"]
+    else:
+        tokens = prob["kv_indices"].shape[0]
+    launches = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, prob["max_len_extend"], tokens)
     kernel = ("vtc_kernel (+ vsk_kernel epilogue)" if tc else
+              "vsk_kernel column-split stream (+ vsk_kernel epilogue)" if launches == 2 else
               "vsk_kernel<128,false>" if spec.d == 128 and spec.pool == "bf16" else "vsk_kernel")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
@@ -442,10 +448,10 @@ def run_ours(args, dist: Dist) -> dict:
                      "kernel": kernel,
                      "launch_us_mean": round(launch_s * 1e6, 2), "launch_us_median": round(launch_med_ms * 1e3, 2),
                      "bytes_per_launch": nbytes},
-        "gpu_launches": args.steps * (2 if tc else 1),
+        "gpu_launches": args.steps * launches,
         "clocks": clocks,
     }
-    line["config"]["kernel_launches_per_step"] = 2 if tc else 1
+    line["config"]["kernel_launches_per_step"] = launches
     if not args.no_e2e:
         e2e_ms, h2d, d2h = time_e2e(vsk, prob, args.e2e_steps, 3)
         e2e_s = dist.max(e2e_ms / 1e3)

@@ -283,6 +283,29 @@ void vsk_set_tuning_tiles(int tiles_per_warp);
  * rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_tc(int mode);
 
+/* Tuning switch, for A/B runs and tests, over head_dim 256 calls with at most
+ * 32 packed query rows per KV head.  Such a call can stream its prefix with
+ * the column-split form of the mma.sync kernel (two warps share each 16-row
+ * query tile, each holding half of the head dimension: half the accumulator
+ * registers, so three CTAs of 2 to 4 warps fit an SM) and fold the partials in
+ * a second launch on the same stream.  Mode 1 (the default) takes that form
+ * when the call's prefix tokens (kv_indices entries, or block-table capacity
+ * for the paged entry points) times h_kv are at most 655,360, where it is the
+ * faster one on GB300; mode 2 always takes it; mode 0 never does (one launch).
+ * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
+ * up to rounding order.  Process-wide; not thread-safe. */
+void vsk_set_tuning_colsplit(int mode);
+
+/* Kernel launches a call of these static shapes makes on its stream under the
+ * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
+ * then the epilogue kernel); 0 for shapes no entry point accepts.
+ * `prefix_tokens` is what the entry point sees: the length of kv_indices for
+ * the flat entry points, batch x block-table columns x page_size for the paged
+ * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch
+ * counts. */
+int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
+                          int64_t prefix_tokens);
+
 /* Size, in bytes, of the scratch array built into the library for
  * verify_splitkv_fwd_noalloc (32 MiB). */
 #define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)

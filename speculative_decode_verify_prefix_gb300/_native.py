@@ -98,6 +98,10 @@ def _bind(lib):
     lib.vsk_set_tuning_tiles.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_tc.restype = None
     lib.vsk_set_tuning_tc.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_colsplit.restype = None
+    lib.vsk_set_tuning_colsplit.argtypes = [ctypes.c_int]
+    lib.vsk_launches_per_call.restype = ctypes.c_int
+    lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
     lib.vsk_set_tuning_shape.restype = None
     lib.vsk_set_tuning_shape.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.vsk_last_error.restype = ctypes.c_char_p

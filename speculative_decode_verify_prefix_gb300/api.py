@@ -275,5 +275,21 @@ def set_tuning_tc(enabled: bool = False) -> None:
     _native.lib().vsk_set_tuning_tc(1 if enabled else 0)
 
 
+def set_tuning_colsplit(mode: int = 1) -> None:
+    """Head_dim 256 calls (at most 32 packed rows per KV head): stream with the
+    column-split mma.sync kernel plus an epilogue launch for small calls (1, the
+    default), always (2) or never (0); for A/B runs and tests."""
+    _native.lib().vsk_set_tuning_colsplit(int(mode))
+
+
+def launches_per_call(batch: int, h_q: int, h_kv: int, head_dim: int, max_len_extend: int,
+                      prefix_tokens: int) -> int:
+    """Kernel launches one call of these shapes makes (1 or 2; 0 if no entry
+    point accepts them); ``prefix_tokens`` = len(kv_indices), or batch x
+    block-table columns x page_size for the paged entry points."""
+    return int(_native.lib().vsk_launches_per_call(int(batch), int(h_q), int(h_kv), int(head_dim),
+                                                   int(max_len_extend), int(prefix_tokens)))
+
+
 def version() -> str:
     return _native.lib().vsk_version().decode()

@@ -62,6 +62,7 @@ constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
+constexpr long long kColSplitMaxWork = 655360;  // prefix tokens x KV heads up to which head_dim 256 splits columns
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
@@ -364,7 +365,7 @@ __device__ __forceinline__ void sit_settle(const Params& p, StageIt& it, long lo
 // the segment's first draft row (qo_indptr[b], validated against l_ext).
 template <int KS>
 __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int r0, int r1, int j, bool flag_err,
-                                      uint32_t (&qf)[KS][4]) {
+                                      uint32_t (&qf)[KS][4], int d0 = 0) {
   const int a = p.qo ? __ldg(p.qo + s.b) : s.b * p.L, e = p.qo ? __ldg(p.qo + s.b + 1) : (s.b + 1) * p.L;
   const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
   if (!ok && flag_err) atomicOr(p.err, kErrBadQoIndptr);
@@ -372,9 +373,9 @@ __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int
   const int kvh = s.hg * p.HC + hc;
   const bool v0 = r0 < p.R, v1 = r1 < p.R;
   const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
-                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
+                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1 + d0;
   const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
-                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
+                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1 + d0;
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
     qf[kk][0] = v0 ? ld_u32(q0 + kk * 16 + 2 * j) : 0u;
@@ -392,7 +393,7 @@ __device__ __forceinline__ int load_q(const Params& p, const Seg& s, int hc, int
 // its largest |q| stays below 2^15, inside the f16 range; returns 2^sh.
 template <int KS>
 __device__ __forceinline__ float load_q_f16(const Params& p, const Seg& s, int hc, int r0, int r1, int j,
-                                             bool flag_err, uint32_t (&qf)[KS][4]) {
+                                             bool flag_err, uint32_t (&qf)[KS][4], int d0 = 0) {
   const int a = p.qo ? __ldg(p.qo + s.b) : s.b * p.L, e = p.qo ? __ldg(p.qo + s.b + 1) : (s.b + 1) * p.L;
   const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
   if (!ok && flag_err) atomicOr(p.err, kErrBadQoIndptr);
@@ -400,9 +401,9 @@ __device__ __forceinline__ float load_q_f16(const Params& p, const Seg& s, int h
   const int kvh = s.hg * p.HC + hc;
   const bool v0 = r0 < p.R, v1 = r1 < p.R;
   const __nv_bfloat16* q0 = p.q + (static_cast<long long>(s_b) + (v0 ? r0 / p.gq : 0)) * p.q_s0 +
-                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1;
+                            static_cast<long long>(kvh * p.gq + (v0 ? r0 % p.gq : 0)) * p.q_s1 + d0;
   const __nv_bfloat16* q1 = p.q + (static_cast<long long>(s_b) + (v1 ? r1 / p.gq : 0)) * p.q_s0 +
-                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1;
+                            static_cast<long long>(kvh * p.gq + (v1 ? r1 % p.gq : 0)) * p.q_s1 + d0;
   unsigned mx = 0;
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
@@ -530,22 +531,33 @@ __device__ __forceinline__ bool cta_share(const Params& p, unsigned char* smem, 
 //        warp's staged new drafts (fused store).
 //   [misc_off + w * misc_bytes, ...)  warp w's own kIdxRing x 16 x 8 B of
 //        kv_indices, 16 x 4 B valid-token masks and, for two-tile warps and
-//        e4m3 pools at head_dim 256, its query tiles (16 x D x 2 B each).
+//        e4m3 pools at head_dim 256, its query tiles (16 x D x 2 B each; its
+//        half, 16 x D/2 x 2 B, in the column-split stream, which then adds two
+//        1 KB score-exchange slots).
 // ---------------------------------------------------------------------------
 template <int D>
 struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
 
-// EPI: the epilogue alone, after vtc_kernel has written every piece's
-// partial (same grid, share floor and plan fields, so the same pieces).
-template <int D, bool FP8, int MTW, bool EPI>
-__global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
+// EPI: the epilogue alone, after a stream-only launch has written every
+// piece's partial (same grid, share floor and plan fields, so the same pieces).
+// CS = 2 (head_dim 256, one KV head per CTA, at most two 16-row tiles): the
+// stream alone, each 16-row tile shared by a pair of warps that split the QK
+// contraction (exchanging their scaled partial scores through shared memory)
+// and own half of the output columns each; the epilogue then runs in an EPI
+// launch.  Half the accumulator registers per warp, so three CTAs per SM.
+template <int D, bool FP8, int MTW, bool EPI, int CS = 1>
+__global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
   constexpr int NT = D / 8;        // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
+  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1 && !EPI), "column split: head_dim 256 stream only");
+  constexpr int DH = D / CS;       // output columns (and contraction length) of one warp
+  constexpr int NTH = NT / CS;     // its n-tiles
+  constexpr int KSH = KS / CS;     // its k-steps
   constexpr int ROWB = D * EK;     // bytes of one head's K (or V) row
   constexpr int CPR = ROWB / 16;   // 16-byte chunks per row
   constexpr int STAGE_B = 2 * kStageTokens * ROWB;
@@ -569,9 +581,12 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   // they meet at a named barrier once per stage.  No producer warp.  Indices
   // come kIdxAhead stages ahead, also by cp.async, into each warp's own index
   // ring.
-  const int WPH = p.MT / MTW;  // warps per KV head; each owns MTW 16-row tiles
-  const int hc = warp / WPH;
-  const int mt = warp % WPH;
+  const int WPH = p.MT / MTW;  // warp groups per KV head; each owns MTW 16-row tiles
+  const int WPHC = WPH * CS;   // warps per KV head
+  const int hc = warp / WPHC;
+  const int mt = (warp / CS) % WPH;
+  const int csi = CS == 2 ? (warp & 1) : 0;  // column half of this warp
+  const int cw = warp % WPHC;                // this warp's share of the head's copies
   const int g = lane >> 2;
   const int j = lane & 3;
   const int RM = 16 * p.MT;
@@ -623,7 +638,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     }
     const bool ok = lane < n && myloc >= 0 && myloc < p.pool;
     const unsigned mask = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
-    if (lane < n && !ok && hc == 0 && mt == 0) atomicOr(p.err, kErrBadIndex);
+    if (lane < n && !ok && hc == 0 && cw == 0) atomicOr(p.err, kErrBadIndex);
     if (lane == 0) mask_ring[job % 16] = mask;
     const long long head = static_cast<long long>(it.s.hg) * p.HC + hc;
     const unsigned char* kbase = p.kb + head * p.kb_s1;
@@ -649,19 +664,19 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
       }
     };
-    if (WPH == 1) {
+    if (WPHC == 1) {
       // the warp copies the whole stage (token indices known at compile time)
 #pragma unroll
       for (int t = lane / LPT; t < kStageTokens; t += TSTEP) copy_token(t, __shfl_sync(0xffffffffu, myloc, t));
     } else {
-      // the warps of the head split the stage: tokens [mt * tpw, mt * tpw + tpw)
-      const int tpw = kStageTokens / WPH;
+      // the warps of the head split the stage: tokens [cw * tpw, cw * tpw + tpw)
+      const int tpw = kStageTokens / WPHC;
 #pragma unroll
       for (int i = 0; i < kStageTokens / TSTEP; ++i) {
         if (i * TSTEP >= tpw) break;  // uniform across the warp
         const int tw = lane / LPT + i * TSTEP;
         const bool act = tw < tpw;    // false only when fewer tokens than one pass of the warp
-        const int t = mt * tpw + (act ? tw : 0);
+        const int t = cw * tpw + (act ? tw : 0);
         const long long loc = __shfl_sync(0xffffffffu, myloc, t);
         if (act) copy_token(t, loc);
       }
@@ -715,15 +730,15 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   // current piece streams (head_dim <= 128, one tile per warp), so a piece
   // boundary costs no global round trip.
   constexpr bool kQAhead = D <= 128 && MTW == 1;
-  uint32_t qf[MTW][KS][4];
-  uint32_t qn[kQAhead ? KS : 1][4];
+  uint32_t qf[MTW][KSH][4];  // this warp's columns of the query (all of them unless CS = 2)
+  uint32_t qn[kQAhead ? KSH : 1][4];
   // bf16 pool: bf16 q fragments; e4m3 pool: f16 q fragments scaled by 2^-sh
   // (qmul = 2^sh is folded back into the score scale)
-  auto load_piece_q = [&](const Seg& sq, bool flag, int ra, int rb, uint32_t (&dst)[KS][4]) -> float {
+  auto load_piece_q = [&](const Seg& sq, bool flag, int ra, int rb, uint32_t (&dst)[KSH][4]) -> float {
     if constexpr (FP8) {
-      return load_q_f16<KS>(p, sq, hc, ra, rb, j, flag, dst);
+      return load_q_f16<KSH>(p, sq, hc, ra, rb, j, flag, dst, csi * DH);
     } else {
-      load_q<KS>(p, sq, hc, ra, rb, j, flag, dst);
+      load_q<KSH>(p, sq, hc, ra, rb, j, flag, dst, csi * DH);
       return 1.f;
     }
   };
@@ -740,12 +755,12 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
 #pragma unroll
       for (int t = 0; t < MTW; ++t) {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
+        for (int kk = 0; kk < KSH; ++kk) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int row = g + ((i & 1) << 3);
             const int e = kk * 16 + ((i >> 1) << 3) + 2 * j;
-            *reinterpret_cast<uint32_t*>(qsm + t * 32 * D + row * (2 * D) + (((e >> 3) ^ (row & 7)) << 4) +
+            *reinterpret_cast<uint32_t*>(qsm + t * 32 * DH + row * (2 * DH) + (((e >> 3) ^ (row & 7)) << 4) +
                                          (e & 7) * 2) = qf[t][kk][i];
           }
         }
@@ -754,7 +769,11 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     }
   };
   const int q_row = (lane & 7) + (((lane >> 3) & 1) << 3);
-  const uint32_t q_lane = smem_u32(qsm) + q_row * (2 * D);
+  const uint32_t q_lane = smem_u32(qsm) + q_row * (2 * DH);
+  // CS = 2: this warp's score exchange buffer (after its query tiles) and the
+  // offset, in floats, to its partner's
+  float* xbuf = reinterpret_cast<float*>(qsm + (kQSmem ? MTW * 32 * DH : 0));
+  const int xpair = (csi ? -1 : 1) * (p.misc_bytes / 4);
   Seg s = seg0;
   float qsc[MTW];
 #pragma unroll
@@ -773,12 +792,12 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
   while (seg_live(p, s, end)) {
     const int t0 = static_cast<int>(max(start, s.off) - s.off);
     const int te = piece_real_end(s, end);
-    float acc[MTW][NT][4];
+    float acc[MTW][NTH][4];  // this warp's output columns
     float m0[MTW], m1[MTW], l0[MTW], l1[MTW];
 #pragma unroll
     for (int t = 0; t < MTW; ++t) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = acc[t][n][2] = acc[t][n][3] = 0.f;
+      for (int n = 0; n < NTH; ++n) acc[t][n][0] = acc[t][n][1] = acc[t][n][2] = acc[t][n][3] = 0.f;
       m0[t] = NEG_INF;
       m1[t] = NEG_INF;
       l0[t] = 0.f;
@@ -792,7 +811,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       __syncwarp();                // ... and every other lane's
       // ... and the other warps' of this head: after this barrier no warp of
       // the head still reads the slot of stage k - 1, which step_data refills
-      if (WPH > 1) named_bar_sync(2 + hc, WPH * 32);
+      if (WPHC > 1) named_bar_sync(2 + hc, WPHC * 32);
       step_data();                 // refill the slot stage k-1 used
       step_idx();
       cp_async_commit();
@@ -832,7 +851,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           float* c1 = ch == 0 ? sc[t][1] : sx[t][ch - 1][1];
           if constexpr (kQSmem) {
             uint32_t a[4];
-            ldsm_x4(q_lane + t * 32 * D + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+            ldsm_x4(q_lane + t * 32 * DH + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
             if constexpr (FP8) {
               mma_f16(c0, a, b0, b1);
               mma_f16(c1, a, b2, b3);
@@ -853,8 +872,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         // each 32-bit register holds 4 consecutive e4m3 d values of one key:
         // low pair -> b0, high pair -> b1 of the permuted contraction order
 #pragma unroll
-        for (int kk2 = 0; kk2 < KS / 2; ++kk2) {
-          const int c = 2 * kk2 + (lane >> 4);
+        for (int kk2 = 0; kk2 < KSH / 2; ++kk2) {
+          const int c = 2 * (csi * (KSH / 2) + kk2) + (lane >> 4);
           uint32_t r0k, r1k, r2k, r3k;
           ldsm_x4(kbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r0k, r1k, r2k, r3k);
           qk_step(2 * kk2, e4m3x2_to_f16x2(r0k & 0xFFFF), e4m3x2_to_f16x2(r0k >> 16), e4m3x2_to_f16x2(r1k & 0xFFFF),
@@ -864,9 +883,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         }
       } else {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
+        for (int kk = 0; kk < KSH; ++kk) {
           uint32_t b0, b1, b2, b3;
-          const int lc = kk * 2 + k_chk;
+          const int lc = (csi * KSH + kk) * 2 + k_chk;
           ldsm_x4(kbase + ((lc ^ (k_key & 7)) << 4), b0, b1, b2, b3);
           qk_step(kk, b0, b1, b2, b3);
         }
@@ -888,6 +907,24 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
             // scale into the log2 domain
             sc[t][u][e] = x * qsc[t];
           }
+        }
+        if constexpr (CS == 2) {
+          // the pair's partial scores (each in the log2 domain already) summed
+          // by both warps alike; the buffer alternates with the stage parity
+          float* xo = xbuf + static_cast<int>(k & 1) * 256 + lane * 8;
+          *reinterpret_cast<float4*>(xo) = make_float4(sc[t][0][0], sc[t][0][1], sc[t][0][2], sc[t][0][3]);
+          *reinterpret_cast<float4*>(xo + 4) = make_float4(sc[t][1][0], sc[t][1][1], sc[t][1][2], sc[t][1][3]);
+          named_bar_sync(10 + (warp >> 1), 64);
+          const float* xp = xo + xpair;
+          const float4 y0 = *reinterpret_cast<const float4*>(xp), y1 = *reinterpret_cast<const float4*>(xp + 4);
+          sc[t][0][0] += y0.x;
+          sc[t][0][1] += y0.y;
+          sc[t][0][2] += y0.z;
+          sc[t][0][3] += y0.w;
+          sc[t][1][0] += y1.x;
+          sc[t][1][1] += y1.y;
+          sc[t][1][2] += y1.z;
+          sc[t][1][3] += y1.w;
         }
         // mask absent keys (tail / dropped) only when the stage is not full
         // (the mask is uniform across the warp)
@@ -923,7 +960,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
           l0[t] *= al0;
           l1[t] *= al1;
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
+          for (int n = 0; n < NTH; ++n) {
             acc[t][n][0] *= al0;
             acc[t][n][1] *= al0;
             acc[t][n][2] *= al1;
@@ -953,8 +990,8 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         // column g <-> d 2g) and O (odd d, column g <-> d 2g+1) of a 16-wide
         // block.  acc[2*blk] is E, acc[2*blk+1] is O.
 #pragma unroll
-        for (int c2 = 0; c2 < KS / 2; ++c2) {
-          const int c = 2 * c2 + (lane >> 4);
+        for (int c2 = 0; c2 < KSH / 2; ++c2) {
+          const int c = 2 * (csi * (KSH / 2) + c2) + (lane >> 4);
           uint32_t r[4];
           ldsm_x4_t(vbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
@@ -974,9 +1011,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       } else {
         // O += P V for 16 keys
 #pragma unroll
-        for (int n2 = 0; n2 < NT / 2; ++n2) {
+        for (int n2 = 0; n2 < NTH / 2; ++n2) {
           uint32_t b0, b1, b2, b3;
-          const int lc = n2 * 2 + v_chk;
+          const int lc = (csi * (NTH / 2) + n2) * 2 + v_chk;
           ldsm_x4_t(vbase + ((lc ^ (v_key & 7)) << 4), b0, b1, b2, b3);
 #pragma unroll
           for (int t = 0; t < MTW; ++t) {
@@ -1000,24 +1037,26 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
         const float s0 = quad_sum(l0[t]), s1 = quad_sum(l1[t]);
         const float inv0 = s0 > 0.f ? p.v_scale / s0 : 0.f;
         const float inv1 = s1 > 0.f ? p.v_scale / s1 : 0.f;
-        if (j == 0) {
+        if (j == 0 && csi == 0) {
           st_keep(lse_p + r0, s0 > 0.f ? m0[t] + log2f(s0) : NEG_INF, keep);
           st_keep(lse_p + r1, s1 > 0.f ? m1[t] + log2f(s1) : NEG_INF, keep);
         }
+        float* o0p = o_p + r0 * D + csi * DH;  // this warp's columns
+        float* o1p = o_p + r1 * D + csi * DH;
         if constexpr (FP8) {
           // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
 #pragma unroll
-          for (int blk = 0; blk < KS; ++blk) {
+          for (int blk = 0; blk < KSH; ++blk) {
             const float* e = acc[t][2 * blk];
             const float* o = acc[t][2 * blk + 1];
-            st_keep4(o_p + r0 * D + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
-            st_keep4(o_p + r1 * D + blk * 16 + 4 * j, e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1, keep);
+            st_keep4(o0p + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
+            st_keep4(o1p + blk * 16 + 4 * j, e[2] * inv1, o[2] * inv1, e[3] * inv1, o[3] * inv1, keep);
           }
         } else {
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            st_keep2(o_p + r0 * D + n * 8 + 2 * j, acc[t][n][0] * inv0, acc[t][n][1] * inv0, keep);
-            st_keep2(o_p + r1 * D + n * 8 + 2 * j, acc[t][n][2] * inv1, acc[t][n][3] * inv1, keep);
+          for (int n = 0; n < NTH; ++n) {
+            st_keep2(o0p + n * 8 + 2 * j, acc[t][n][0] * inv0, acc[t][n][1] * inv0, keep);
+            st_keep2(o1p + n * 8 + 2 * j, acc[t][n][2] * inv1, acc[t][n][3] * inv1, keep);
           }
         }
       }
@@ -1027,7 +1066,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
       seg_advance(p, sn);
       if constexpr (kQAhead) {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
+        for (int kk = 0; kk < KSH; ++kk) {
           qf[0][kk][0] = qn[kk][0];
           qf[0][kk][1] = qn[kk][1];
           qf[0][kk][2] = qn[kk][2];
@@ -1043,6 +1082,9 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     }
   }
   }  // !EPI
+  if constexpr (CS == 2) {
+    cp_async_wait<0>();  // stream only: the epilogue runs in its own launch
+  } else {
 
   // ================= epilogue: tickets, log-sum-exp merges, drafts, output =================
   // No copy is left in flight, and every partial this thread wrote is made
@@ -1476,6 +1518,7 @@ __global__ void __launch_bounds__(MaxWarps<D>::value * 32, 1)
     }
     seg_advance(p, sg);
   }
+  }  // CS == 1
 }
 
 #include "verify_tc.cuh"
@@ -1502,6 +1545,7 @@ int g_max_stages = 0;
 int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
 int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
+int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
 
 struct Plan {
   int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
@@ -1609,6 +1653,39 @@ bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool 
   pl.misc_off = kCtlBytes + pl.nwc * 32 * static_cast<int>(D);
   pl.smem = static_cast<size_t>(pl.misc_off);
   pl.ctas_per_sm = 1;
+  return true;
+}
+
+// Column-split stream (vsk_kernel<256, ., 1, false, 2>): head_dim 256 with at
+// most 32 packed rows per KV head.  The workspace / epilogue plan is the
+// tensor-memory one (one KV head per segment, MT = RM / 16, the epilogue in
+// MT warps); the stream runs 2 MT warps per CTA, three CTAs per SM.  Lighter
+// warps and more CTAs shorten small calls; on long ones the pair exchange and
+// the second launch cost more than they save, so by default only calls of at
+// most kColSplitMaxWork prefix tokens x KV heads (from static shapes) take it.
+bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
+  if (g_cs == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0 || (h_q / h_kv) * L > 32) return false;
+  return g_cs == 2 || total_tokens * h_kv <= kColSplitMaxWork;
+}
+struct StreamPlan {
+  int threads, nst, ring_off, head_bytes, misc_off, misc_bytes, per_sm;
+  size_t smem;
+};
+bool make_cs_stream_plan(const Plan& pl, long long D, bool fp8, StreamPlan& sp) {
+  const int nwc = 2 * pl.MT;
+  sp.threads = nwc * 32;
+  sp.per_sm = 3;
+  const int stage_bytes = 2 * kStageTokens * static_cast<int>(D) * (fp8 ? 1 : 2);
+  // per warp: index ring, mask ring, query tile (e4m3 pools: 16 rows x D/2 f16), score exchange buffer (2 x 1 KB)
+  sp.misc_bytes = kIdxRing * 128 + 128 + (fp8 ? 16 * static_cast<int>(D / 2) * 2 : 0) + 2048;
+  const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / sp.per_sm - kReservedPerCTA);
+  sp.nst = std::min(kMaxStages, (budget - kCtlBytes - nwc * sp.misc_bytes) / stage_bytes);
+  if (g_max_stages > 0) sp.nst = std::min(sp.nst, g_max_stages);
+  if (sp.nst < 2) return fail("column-split stage of %d bytes does not fit shared memory", stage_bytes);
+  sp.ring_off = kCtlBytes;
+  sp.head_bytes = sp.nst * stage_bytes;
+  sp.misc_off = sp.ring_off + sp.head_bytes;
+  sp.smem = static_cast<size_t>(sp.misc_off) + static_cast<size_t>(nwc) * sp.misc_bytes;
   return true;
 }
 
@@ -1758,6 +1835,11 @@ KernelFn pick_kernel(int D, bool fp8, int mtw) {
 KernelFn pick_tc_kernel(bool fp8, int rm) {
   if (rm == 16) return fp8 ? static_cast<KernelFn>(vtc_kernel<256, true, 16>) : static_cast<KernelFn>(vtc_kernel<256, false, 16>);
   return fp8 ? static_cast<KernelFn>(vtc_kernel<256, true, 32>) : static_cast<KernelFn>(vtc_kernel<256, false, 32>);
+}
+
+KernelFn pick_cs_kernel(bool fp8) {
+  return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, false, 2>)
+             : static_cast<KernelFn>(vsk_kernel<256, false, 1, false, 2>);
 }
 
 KernelFn pick_epi_kernel(bool fp8) {
@@ -1910,6 +1992,19 @@ void vsk_set_tuning_tiles(int tiles_per_warp) { g_tiles = tiles_per_warp == 1 ||
 
 void vsk_set_tuning_tc(int mode) { g_tc = mode == 1 ? 1 : 0; }
 
+void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode : 1; }
+
+int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
+                          int64_t prefix_tokens) {
+  if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
+  const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
+  return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) ||
+          cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
+             ? 2
+             : 1;
+}
+
 void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta) {
   g_max_stages = max_ring_stages >= 2 ? max_ring_stages : 0;
   g_max_heads = max_kv_heads_per_cta > 0 ? max_kv_heads_per_cta : 0;
@@ -1927,9 +2022,13 @@ namespace vsk {
 static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
                             void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
   const bool use_tc = tc_eligible(h_q, h_kv, D, L);
+  const bool use_cs = !use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan pl;
-  if (use_tc ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl) : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0))
+  if ((use_tc || use_cs) ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
+                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0))
     return 0;
+  StreamPlan sp{};
+  if (use_cs && !make_cs_stream_plan(pl, D, fp8, sp)) return 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
@@ -1954,6 +2053,13 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
     if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
     pl.nst = ne;
     threads = tc::kThreads;
+  } else if (use_cs) {
+    fn = pick_cs_kernel(fp8);
+    fn_epi = pick_epi_kernel(fp8);
+    if (!prepare_kernel(fn) || !prepare_kernel(fn_epi)) return fail("column-split kernels unavailable");
+    threads = sp.threads;
+    smem = sp.smem;
+    per_sm = sp.per_sm;
   } else {
     fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
     if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
@@ -2006,13 +2112,23 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
   p.po = reinterpret_cast<float*>(ws + wl.o_off);
   void* args[] = {&p};
+  Params pe = p;  // the epilogue launch keeps the plan's own fields
+  if (use_cs) {
+    p.nwc = 2 * pl.MT;
+    p.nst = sp.nst;
+    p.ring_off = sp.ring_off;
+    p.head_bytes = sp.head_bytes;
+    p.misc_off = sp.misc_off;
+    p.misc_bytes = sp.misc_bytes;
+  }
   e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(threads), args,
                        smem, st);
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
   if (fn_epi) {
+    void* args_e[] = {use_cs ? static_cast<void*>(&pe) : static_cast<void*>(&p)};
     // same grid and share floor: the epilogue kernel finds the same pieces
     e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_epi), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads),
-                         args, pl.smem, st);
+                         args_e, pl.smem, st);
     if (e != cudaSuccess) return fail("epilogue kernel launch failed: %s", cudaGetErrorString(e));
   }
   return 1;

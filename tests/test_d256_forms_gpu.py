@@ -1,11 +1,15 @@
-"""GPU parity of the tensor-memory stream (tcgen05.mma, accumulators in TMEM):
-head_dim 256 with at most 32 packed query rows per KV head, against the fp64
-oracle, with the mma.sync kernel it replaces checked beside it.
+"""GPU parity of the two alternative head_dim 256 streams, against the fp64
+oracle, with the one-launch mma.sync kernel checked beside each:
 
-Same tolerance as the other parity tests (atol 2e-2, rtol 1e-2 on the bf16
-output); stored cache codes and repeated / graph-replayed calls are compared
-bit for bit.  Every call also checks the device error word, whose timeout bit
-would report a pipeline wait that gave up.
+- "tc": the tensor-memory stream (tcgen05.mma, accumulators in TMEM);
+- "colsplit": the column-split mma.sync stream (two warps per 16-row query
+  tile, each holding half the head dimension).
+
+Both serve head_dim 256 with at most 32 packed query rows per KV head and fold
+their partials in a second launch.  Same tolerance as the other parity tests
+(atol 2e-2, rtol 1e-2 on the bf16 output); stored cache codes and repeated /
+graph-replayed calls are compared bit for bit.  Every call also checks the
+device error word, whose timeout bit would report a pipeline wait that gave up.
 """
 import numpy as np
 import pytest
@@ -20,25 +24,32 @@ pytestmark = pytest.mark.gpu
 S = workloads.Spec
 
 
-@pytest.fixture(scope="module")
-def vsk():
+def _select(m, form):
+    m.set_tuning_tc(form == "tc")
+    m.set_tuning_colsplit(2 if form == "colsplit" else 0)
+
+
+@pytest.fixture(scope="module", params=["tc", "colsplit"])
+def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 
     m.build()
-    m.set_tuning_tc(True)
+    m.form = request.param
+    _select(m, m.form)
     yield m
     m.set_tuning(0, 0)
     m.set_tuning_tc(False)
+    m.set_tuning_colsplit(1)
 
 
 def both(vsk, fn):
-    """fn() on the tensor-memory path, then on the mma.sync path."""
+    """fn() on the form under test, then on the one-launch mma.sync kernel."""
     a = fn()
-    vsk.set_tuning_tc(False)
+    _select(vsk, "one_launch")
     try:
         b = fn()
     finally:
-        vsk.set_tuning_tc(True)
+        _select(vsk, vsk.form)
     return a, b
 
 
@@ -61,7 +72,7 @@ TC = [
 
 
 @pytest.mark.parametrize("spec", TC, ids=lambda s: s.name)
-def test_tc_matches_oracle(vsk, spec):
+def test_form_matches_oracle(vsk, spec):
     p = gpu_problem(spec)
     ref = oracle_o(p)
     vsk.read_error_flags()
@@ -89,7 +100,7 @@ def _scale_k_rows(p, factor_of_position):
 
 
 @pytest.mark.parametrize("pool", ["bf16", "e4m3"])
-def test_tc_rising_scores_rescale_the_accumulator(vsk, pool):
+def test_form_rising_scores_rescale_the_accumulator(vsk, pool):
     """K rows grow with their position, so scores keep rising along each
     prefix and the running maximum is raised (O rescaled in TMEM) many times
     inside a piece."""
@@ -103,7 +114,7 @@ def test_tc_rising_scores_rescale_the_accumulator(vsk, pool):
     check(b, ref)
 
 
-def test_tc_single_dominant_key(vsk):
+def test_form_single_dominant_key(vsk):
     """One key per sequence with a huge K row (scores of either sign, far
     beyond the others) late in the prefix: the maximum jumps once by a lot."""
     spec = S("tc_spike", (2000, 700), 4, 16, 2, 256, 256, perm=True, seed=712)
@@ -126,7 +137,7 @@ TC_PAGED = [
 
 
 @pytest.mark.parametrize("spec", TC_PAGED, ids=lambda s: s.name)
-def test_tc_paged_matches_oracle(vsk, spec):
+def test_form_paged_matches_oracle(vsk, spec):
     p = gpu_problem(spec)
     ref = oracle_o(p)
     vsk.read_error_flags()
@@ -144,7 +155,7 @@ TC_TREE = [
 
 
 @pytest.mark.parametrize("spec", TC_TREE, ids=lambda s: s.name)
-def test_tc_tree_matches_oracle(vsk, spec):
+def test_form_tree_matches_oracle(vsk, spec):
     p = gpu_problem(spec)
     ref = oracle_o(p)
     a, b = both(vsk, lambda: run_tree(vsk, p))
@@ -154,7 +165,7 @@ def test_tc_tree_matches_oracle(vsk, spec):
 
 
 @pytest.mark.parametrize("pool", ["bf16", "e4m3"])
-def test_tc_fused_store_flat(vsk, pool):
+def test_form_fused_store_flat(vsk, pool):
     spec = S("tcw_flat", (700, 90, 0), 4, 16, 2, 256, 256, pool=pool, perm=True, pool_extra=32, k_scale=0.5,
              v_scale=0.25, seed=741)
     p = gpu_problem(spec)
@@ -177,7 +188,7 @@ def test_tc_fused_store_flat(vsk, pool):
 
 
 @pytest.mark.parametrize("pool", ["bf16", "e4m3"])
-def test_tc_fused_store_paged(vsk, pool):
+def test_form_fused_store_paged(vsk, pool):
     spec = S("tcw_paged", (23, 1000, 0, 64), 4, 16, 2, 256, 256, pool=pool, perm=True, page_size=16,
              k_scale=1.5, v_scale=0.75, seed=742)
     p = gpu_problem(spec)
@@ -203,7 +214,7 @@ def test_tc_fused_store_paged(vsk, pool):
 
 
 @pytest.mark.parametrize("num_ctas,min_tok", [(1, 0), (3, 16), (150, 16), (1000, 16), (0, 64)])
-def test_tc_split_count_independence(vsk, num_ctas, min_tok):
+def test_form_split_count_independence(vsk, num_ctas, min_tok):
     spec = S("tc_splits", (2000, 5, 0, 777, 64), 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
              v_scale=1.5, seed=751)
     p = gpu_problem(spec)
@@ -216,7 +227,7 @@ def test_tc_split_count_independence(vsk, num_ctas, min_tok):
     assert vsk.read_error_flags() == 0
 
 
-def test_tc_repeated_calls_and_graph_replay_identical(vsk):
+def test_form_repeated_calls_and_graph_replay_identical(vsk):
     """Two launches per call (stream, then epilogue): tickets are left at zero,
     so repeated calls and CUDA-graph replays agree bit for bit."""
     spec = S("tc_repeat", (3000, 4000, 10), 4, 16, 2, 256, 256, perm=True, seed=752)
@@ -248,14 +259,14 @@ def test_tc_repeated_calls_and_graph_replay_identical(vsk):
     check(a, oracle_o(p))
 
 
-def test_tc_poisoned_unreferenced_slots(vsk):
+def test_form_poisoned_unreferenced_slots(vsk):
     spec = S("tc_poison", (40, 0, 129, 64), 4, 16, 2, 256, 256, perm=True, pool_extra=300, poison=True, seed=753)
     p = gpu_problem(spec)
     check(run_gpu(vsk, p), oracle_o(p))
     assert vsk.read_error_flags() == 0
 
 
-def test_tc_out_of_range_index_is_flagged_not_read(vsk):
+def test_form_out_of_range_index_is_flagged_not_read(vsk):
     spec = S("tc_badidx", (50, 130), 4, 16, 2, 256, 256, seed=754)
     p = gpu_problem(spec)
     ref_other = oracle_o(p)
@@ -274,7 +285,7 @@ def test_tc_out_of_range_index_is_flagged_not_read(vsk):
     check(o, oracle_o(p3), rows=slice(4, 8))  # sequence 1 without those two keys
 
 
-def test_tc_fp8_long_sampled(vsk):
+def test_form_fp8_long_sampled(vsk):
     """The e4m3 head_dim 256 benchmark shape (64 sequences, prefixes
     U[8192, 32768]) in its launch configuration; the oracle checks three
     whole sequences."""
@@ -320,7 +331,7 @@ def _tc_cases(n=24, seed=2025):
 
 
 @pytest.mark.parametrize("case", _tc_cases(), ids=lambda c: c[0].name)
-def test_tc_random_problem_matches_oracle(vsk, case):
+def test_form_random_problem_matches_oracle(vsk, case):
     spec, form, (nc, mt) = case
     p = workloads.make_problem(spec, "cuda")
     vsk.read_error_flags()
