@@ -119,7 +119,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tc", action="store_true",
                     help="head_dim 256 calls stream the prefix with the tensor-memory kernel (tcgen05; "
-                         "two launches per call: vtc_kernel, then the epilogue)")
+                         "two launches per call: vtc_kernel, then the combine kernel)")
     ap.add_argument("--report-configs", action="store_true",
                     help="print a per-configuration table (tiny, d256, GQA sweep, fp8, serving) instead of the JSON line")
     return ap.parse_args(argv)
@@ -431,8 +431,8 @@ def run_ours(args, dist: Dist) -> dict:
     else:
         tokens = prob["kv_indices"].shape[0]
     launches = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, prob["max_len_extend"], tokens)
-    kernel = ("vtc_kernel (+ vsk_kernel epilogue)" if tc else
-              "vsk_kernel column-split stream (+ vsk_kernel epilogue)" if launches == 2 else
+    kernel = ("vtc_kernel (+ vsk_combine_kernel)" if tc else
+              "vsk_kernel column-split stream (+ vsk_combine_kernel)" if launches == 2 else
               "vsk_kernel<128,false>" if spec.d == 128 and spec.pool == "bf16" else "vsk_kernel")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,

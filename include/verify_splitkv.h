@@ -276,8 +276,9 @@ void vsk_set_tuning_tiles(int tiles_per_warp);
 /* Tuning switch, for A/B runs and tests: mode 1 sends head_dim 256 calls with
  * at most 32 packed query rows per KV head ((h_q / h_kv) * max_len_extend <=
  * 32) through the tensor-memory form of the prefix stream (tcgen05.mma with
- * accumulators in TMEM, one launch) followed by the epilogue of the mma.sync
- * kernel (a second launch on the same stream); any other value (and the
+ * accumulators in TMEM, one launch) followed by the combine kernel (a second
+ * launch on the same stream: it folds the per-piece partials, adds the draft
+ * block and writes o); any other value (and the
  * default) keeps every call on the mma.sync kernel, which is the faster of the
  * two on GB300 at these shapes.  Both forms compute the same result up to
  * rounding order.  Process-wide; not thread-safe. */
@@ -288,17 +289,18 @@ void vsk_set_tuning_tc(int mode);
  * the column-split form of the mma.sync kernel (two warps share each 16-row
  * query tile, each holding half of the head dimension: half the accumulator
  * registers, so three CTAs of 2 to 4 warps fit an SM) and fold the partials in
- * a second launch on the same stream.  Mode 1 (the default) takes that form
- * when the call's prefix tokens (kv_indices entries, or block-table capacity
- * for the paged entry points) times h_kv are at most 655,360, where it is the
- * faster one on GB300; mode 2 always takes it; mode 0 never does (one launch).
+ * a second launch on the same stream (the combine kernel: one CTA per
+ * segment, 16-row tile and 32-column slice).  Mode 1 (the default) takes that
+ * form when the call's prefix tokens (kv_indices entries, or block-table
+ * capacity for the paged entry points) times h_kv are at most 1,048,576, where
+ * it is the faster one on GB300; mode 2 always takes it; mode 0 never does.
  * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
 
 /* Kernel launches a call of these static shapes makes on its stream under the
  * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
- * then the epilogue kernel); 0 for shapes no entry point accepts.
+ * then the combine kernel); 0 for shapes no entry point accepts.
  * `prefix_tokens` is what the entry point sees: the length of kv_indices for
  * the flat entry points, batch x block-table columns x page_size for the paged
  * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch

@@ -277,7 +277,7 @@ def set_tuning_tc(enabled: bool = False) -> None:
 
 def set_tuning_colsplit(mode: int = 1) -> None:
     """Head_dim 256 calls (at most 32 packed rows per KV head): stream with the
-    column-split mma.sync kernel plus an epilogue launch for small calls (1, the
+    column-split mma.sync kernel plus a combine launch for small calls (1, the
     default), always (2) or never (0); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_colsplit(int(mode))
 

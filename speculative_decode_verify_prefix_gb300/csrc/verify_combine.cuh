@@ -1,0 +1,355 @@
+// ---------------------------------------------------------------------------
+// Combine kernel of the two-launch forms (head_dim 256: the column-split and
+// the tensor-memory streams).  Split-KV (flash-decode) attention computes one
+// (o, log-sum-exp) partial per CTA piece of a sequence's prefix and merges
+// them with the log-sum-exp rule; the verify step then continues the same
+// softmax over the causal draft-draft block (verify_splitkv.py page,
+// `_verify_prefix_stage1` / `_verify_merge_with_extend`: the prefix partials
+// are merged with the extend block's scores).
+//
+// When this kernel starts, the stream launch before it on the same stream has
+// written every piece's partial, so no ticket or arrival order is needed: one
+// CTA per (segment, 16-row query tile, 32-column slice of the output) reads
+// the segment's pieces straight away.  Its four warps split the pieces (each
+// keeps a running maximum, sum and weighted 16 x 32 block), meet in shared
+// memory, and then compute the draft scores of the tile (each warp a 64-wide
+// part of the head dimension, summed in a fixed order), continue the softmax
+// and write their 16 x 32 block of o.  The fused-store forms store the new
+// draft rows here too: tile 0's CTAs, each its 32-column slice of every row,
+// so every stored element has exactly one writer.
+//
+// The pieces of segment s = (b, hg) are found the way every kernel of a call
+// cuts the work: segments of virtual length max(P_b, 1) laid end to end, CTA
+// c of the stream grid (p.n_stream CTAs) owning [c W, c W + W) with
+// W = max(ceil(total / n_stream), w_min); piece c of s sits in slot c + s.
+// ---------------------------------------------------------------------------
+namespace cmb {
+constexpr int kD = 256;                    // head_dim served
+constexpr int kThreads = 128;              // four warps
+constexpr int kCols = 32;                  // output columns per CTA
+constexpr int kSlices = kD / kCols;
+constexpr int kMaxL = 32;                  // draft keys (at most 32 packed rows)
+constexpr int kKPitch = kD * 2 + 16;       // bytes per staged K row (padded: conflict-free fragment reads)
+constexpr int kScanOff = 0;                // 2 x 4 x i64 block sums
+constexpr int kSrcOff = 128;               // [kMaxL] i64: row the draft is read from (-1: no row)
+constexpr int kDstOff = kSrcOff + kMaxL * 8;  // [kMaxL] i64: row it is stored to (-1: none)
+constexpr int kKOff = kDstOff + kMaxL * 8;    // [kMaxL][kKPitch] draft K rows, bf16
+constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] fp32 draft V slice
+constexpr int kFoldOff = kVOff + kMaxL * kCols * 4;  // per warp m[16], then l[16]
+constexpr int kAccOff = kFoldOff + 4 * 32 * 4;       // per warp [16][kCols] weighted sums
+constexpr int kScPitch = kMaxL + 1;
+constexpr int kScOff = kAccOff + 4 * 16 * kCols * 4;  // per warp [16][kScPitch] partial scores
+constexpr int kSmem = kScOff + 4 * 16 * kScPitch * 4;
+static_assert(kSmem <= 48 * 1024, "combine kernel fits the default shared-memory window");
+static_assert(kKOff % 16 == 0 && kVOff % 16 == 0 && kAccOff % 16 == 0, "16-byte aligned regions");
+}  // namespace cmb
+
+template <bool FP8>
+__global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid_constant__ Params p) {
+  using namespace cmb;
+  constexpr int D = kD;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, j = lane & 3;
+  const int ch = static_cast<int>(blockIdx.x % kSlices);
+  const int tile = static_cast<int>((blockIdx.x / kSlices) % p.MT);
+  const long long s_idx = static_cast<long long>(blockIdx.x) / (kSlices * p.MT);
+  const int RM = 16 * p.MT;
+  const float NEG_INF = -INFINITY;
+  Seg sg;
+  sg.b = static_cast<int>(s_idx / p.n_hg);
+  sg.hg = static_cast<int>(s_idx % p.n_hg);
+  load_seq(p, sg.b, sg.P, sg.kv0);
+  sg.len = max(sg.P, 1);
+  const int kvh = sg.hg;  // one KV head per segment in the two-launch forms
+  const int col0 = ch * kCols;
+  const bool writer = tile == 0;  // stores this CTA's column slice of the new drafts
+  const bool flagger = tid == 0 && ch == 0 && tile == 0;
+
+  // the sequence's draft rows in q / k_ext / v_ext / o (qo_indptr, validated)
+  int s_b;
+  {
+    const int a = p.qo ? __ldg(p.qo + sg.b) : sg.b * p.L, e = p.qo ? __ldg(p.qo + sg.b + 1) : (sg.b + 1) * p.L;
+    const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
+    if (!ok && flagger) atomicOr(p.err, kErrBadQoIndptr);
+    s_b = ok ? a : sg.b * p.L;
+  }
+  // per draft key: the row it is read from and the row it is stored to
+  long long* ksrc = reinterpret_cast<long long*>(smem + kSrcOff);
+  long long* kdst = reinterpret_cast<long long*>(smem + kDstOff);
+  if (tid < p.L) {
+    const int key = tid;
+    long long src = static_cast<long long>(s_b) + key, dst = -1;
+    if (p.paged) {
+      // drafts at cache positions P + key (the paged store puts them there)
+      const long long row = paged_row(p, sg.b, sg.P + key);
+      if (row < 0 && writer && ch == 0) atomicOr(p.err, kErrBadIndex);
+      if (p.wmode == 2) {
+        dst = row;
+        if (row < 0) src = -1;
+      } else {
+        src = row;
+      }
+    } else if (p.wmode == 1) {
+      const long long d = p.ocl64 ? static_cast<const long long*>(p.ocl)[s_b + key]
+                                  : static_cast<long long>(static_cast<const int*>(p.ocl)[s_b + key]);
+      dst = (d >= 0 && d < p.pool) ? d : -1;
+      if (dst < 0 && writer && ch == 0) atomicOr(p.err, kErrBadIndex);
+    }
+    ksrc[key] = src;
+    kdst[key] = dst;
+  }
+  // block sums of the virtual segment lengths: all of them and those before b
+  long long* scan = reinterpret_cast<long long*>(smem + kScanOff);
+  {
+    long long tot_t = 0, bef_t = 0;
+    for (int bb = tid; bb < p.B; bb += kThreads) {
+      int P_;
+      long long k_;
+      seq_info(p, bb, P_, k_);
+      const long long ln = max(P_, 1);
+      tot_t += ln;
+      if (bb < sg.b) bef_t += ln;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot_t += __shfl_xor_sync(0xffffffffu, tot_t, o);
+      bef_t += __shfl_xor_sync(0xffffffffu, bef_t, o);
+    }
+    if (lane == 0) {
+      scan[warp] = tot_t;
+      scan[4 + warp] = bef_t;
+    }
+  }
+  __syncthreads();  // also publishes ksrc / kdst
+  const long long tot = (scan[0] + scan[1] + scan[2] + scan[3]) * p.n_hg;
+  const long long before = scan[4] + scan[5] + scan[6] + scan[7];
+  long long W = (tot + p.n_stream - 1) / p.n_stream;
+  if (W < p.w_min) W = p.w_min;
+  const long long off = before * p.n_hg + static_cast<long long>(sg.hg) * sg.len;
+  const long long c_first = off / W, c_last = (off + sg.len - 1) / W;
+  const long long npc = c_last - c_first + 1;  // pieces of the segment
+  const long long slot0 = c_first + s_idx;
+
+  // ---- stage the draft K rows (whole head dimension) and this slice of V ----
+  const int LK = (p.L + 7) & ~7;  // whole 8-key groups (keys past L staged as zero)
+  unsigned char* kst = smem + kKOff;
+  float* vst = reinterpret_cast<float*>(smem + kVOff);
+  for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
+    const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
+    uint32_t val = 0u;
+    const long long src = key < p.L ? ksrc[key] : -1;
+    if (src >= 0) {
+      if (p.paged && p.wmode != 2) {
+        const unsigned char* kr = p.kb + src * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+        if constexpr (FP8)
+          val = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(kr + d));
+        else
+          val = *reinterpret_cast<const uint32_t*>(kr + d * 2);
+      } else {
+        val = ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + d);
+        const long long dst = kdst[key];
+        const bool mine = writer && dst >= 0 && d >= col0 && d < col0 + kCols;
+        if (p.wmode != 0) {
+          const float2 x = unpack_bf16(val);
+          unsigned char* kd = p.kw + (dst >= 0 ? dst : 0) * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+          if constexpr (FP8) {
+            const unsigned short c = store_e4m3x2(x.x, x.y, p.kq);
+            if (mine) *reinterpret_cast<unsigned short*>(kd + d) = c;
+            if (p.wmode == 2) val = e4m3x2_to_bf16x2(c);  // attend over the stored values
+          } else {
+            const uint32_t c = store_bf16x2(x.x, x.y, p.kq);
+            if (mine) *reinterpret_cast<uint32_t*>(kd + d * 2) = c;
+            if (p.wmode == 2) val = c;
+          }
+        }
+      }
+    }
+    *reinterpret_cast<uint32_t*>(kst + key * kKPitch + d * 2) = val;
+  }
+  for (int idx = tid; idx < p.L * (kCols / 2); idx += kThreads) {
+    const int key = idx / (kCols / 2), c = col0 + (idx % (kCols / 2)) * 2;
+    float2 v = make_float2(0.f, 0.f);
+    const long long src = ksrc[key];
+    if (src >= 0) {
+      if (p.paged && p.wmode != 2) {
+        const unsigned char* vr = p.vb + src * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+        if constexpr (FP8)
+          v = unpack_bf16(e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(vr + c)));
+        else
+          v = unpack_bf16(*reinterpret_cast<const uint32_t*>(vr + c * 2));
+      } else {
+        v = unpack_bf16(ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c));
+        const long long dst = kdst[key];
+        if (p.wmode != 0) {
+          unsigned char* vd = p.vw + (dst >= 0 ? dst : 0) * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+          const bool mine = writer && dst >= 0;
+          if constexpr (FP8) {
+            const unsigned short cv = store_e4m3x2(v.x, v.y, p.vq);
+            if (mine) *reinterpret_cast<unsigned short*>(vd + c) = cv;
+            if (p.wmode == 2) v = unpack_bf16(e4m3x2_to_bf16x2(cv));
+          } else {
+            const uint32_t cv = store_bf16x2(v.x, v.y, p.vq);
+            if (mine) *reinterpret_cast<uint32_t*>(vd + c * 2) = cv;
+            if (p.wmode == 2) v = unpack_bf16(cv);
+          }
+        }
+      }
+    }
+    vst[key * kCols + (c - col0)] = v.x;
+    vst[key * kCols + (c - col0) + 1] = v.y;
+  }
+
+  // ---- this warp's query fragments: rows of the tile, head dims [64 warp, 64 warp + 64) ----
+  uint32_t qf[4][4];
+  {
+    const int r0 = 16 * tile + g;
+    load_q<4>(p, sg, 0, r0, r0 + 8, j, false, qf, 64 * warp);
+  }
+
+  // ---- fold: warp w takes pieces w, w + 4, ...; lane = (row, 16 columns) ----
+  const int fr = lane >> 1, fc = (lane & 1) * 16;
+  float fm = NEG_INF, fl = 0.f, fa[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) fa[k] = 0.f;
+  auto fold_one = [&](float x, const float4 (&v)[4]) {
+    if (x == NEG_INF) return;  // a piece with nothing visible
+    const float mn = fmaxf(fm, x);
+    const float sc = exp2f(fm - mn);  // 0 while fm is -inf
+    const float w = exp2f(x - mn);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      fa[4 * k + 0] = fmaf(fa[4 * k + 0], sc, w * v[k].x);
+      fa[4 * k + 1] = fmaf(fa[4 * k + 1], sc, w * v[k].y);
+      fa[4 * k + 2] = fmaf(fa[4 * k + 2], sc, w * v[k].z);
+      fa[4 * k + 3] = fmaf(fa[4 * k + 3], sc, w * v[k].w);
+    }
+    fl = fmaf(fl, sc, w);
+    fm = mn;
+  };
+  {
+    const int prow = 16 * tile + fr;
+#pragma unroll 1
+    for (long long i = warp; i < npc; i += 8) {
+      const bool two = i + 4 < npc;  // uniform across the warp
+      const long long sa = slot0 + i, sb = slot0 + (two ? i + 4 : i);
+      const float xa = __ldcg(p.plse + sa * RM + prow);
+      const float xb = __ldcg(p.plse + sb * RM + prow);
+      const float4* oa = reinterpret_cast<const float4*>(p.po + (sa * RM + prow) * D + col0 + fc);
+      const float4* ob = reinterpret_cast<const float4*>(p.po + (sb * RM + prow) * D + col0 + fc);
+      float4 va[4], vb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        va[k] = __ldcg(oa + k);
+        vb[k] = __ldcg(ob + k);
+      }
+      fold_one(xa, va);
+      if (two) fold_one(xb, vb);
+    }
+  }
+  float* sm_m = reinterpret_cast<float*>(smem + kFoldOff) + warp * 32;
+  float* sm_a = reinterpret_cast<float*>(smem + kAccOff) + warp * 16 * kCols;
+  if ((lane & 1) == 0) {
+    sm_m[fr] = fm;
+    sm_m[16 + fr] = fl;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<float4*>(sm_a + fr * kCols + fc + 4 * k) =
+        make_float4(fa[4 * k], fa[4 * k + 1], fa[4 * k + 2], fa[4 * k + 3]);
+  __syncthreads();  // staged drafts, fold partials
+
+  // ---- draft scores: this warp's 64-wide part of q . k for every 8-key group ----
+  float* scp = reinterpret_cast<float*>(smem + kScOff) + warp * 16 * kScPitch;
+#pragma unroll 1
+  for (int nt = 0; nt * 8 < p.L; ++nt) {
+    float sd[4] = {0.f, 0.f, 0.f, 0.f};
+    const unsigned char* kr = kst + (nt * 8 + g) * kKPitch + (64 * warp) * 2;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 2 * j) * 2);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2);
+      mma_bf16(sd, qf[kk], b0, b1);
+    }
+    scp[g * kScPitch + nt * 8 + 2 * j] = sd[0];
+    scp[g * kScPitch + nt * 8 + 2 * j + 1] = sd[1];
+    scp[(g + 8) * kScPitch + nt * 8 + 2 * j] = sd[2];
+    scp[(g + 8) * kScPitch + nt * 8 + 2 * j + 1] = sd[3];
+  }
+  __syncthreads();
+
+  // ---- per thread: row r of the tile, 4 output columns ----
+  const int r = tid >> 3, c4 = (tid & 7) * 4;
+  const int prow = 16 * tile + r;
+  const float* fm_all = reinterpret_cast<const float*>(smem + kFoldOff);
+  const float* fa_all = reinterpret_cast<const float*>(smem + kAccOff);
+  float M = NEG_INF;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) M = fmaxf(M, fm_all[w * 32 + r]);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float l = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float mw = fm_all[w * 32 + r];
+    if (mw == NEG_INF) continue;
+    const float s = exp2f(mw - M);
+    l = fmaf(fm_all[w * 32 + 16 + r], s, l);
+    const float4 a = *reinterpret_cast<const float4*>(fa_all + (w * 16 + r) * kCols + c4);
+    acc[0] = fmaf(a.x, s, acc[0]);
+    acc[1] = fmaf(a.y, s, acc[1]);
+    acc[2] = fmaf(a.z, s, acc[2]);
+    acc[3] = fmaf(a.w, s, acc[3]);
+  }
+  // draft visibility: causal, or the tree mask rows (row-major [L][P+L], only
+  // the draft columns are read; inconsistent offsets fall back to causal)
+  long long mbase = -1;
+  if (p.cmask) {
+    const long long m0 = p.mindptr64 ? static_cast<const long long*>(p.mindptr)[sg.b]
+                                     : static_cast<long long>(static_cast<const int*>(p.mindptr)[sg.b]);
+    const long long span = static_cast<long long>(p.L) * (sg.P + p.L);
+    if (m0 >= 0 && m0 + span <= p.n_mask)
+      mbase = m0;
+    else if (flagger)
+      atomicOr(p.err, kErrBadMaskIndptr);
+  }
+  const int irow = prow / p.gq;  // draft index of the row
+  const float* sc_all = reinterpret_cast<const float*>(smem + kScOff);
+  auto score = [&](int key) -> float {
+    if (key >= p.L || irow >= p.L || ksrc[key] < 0) return NEG_INF;
+    const bool vis = mbase < 0 ? key <= irow
+                               : __ldg(p.cmask + mbase + static_cast<long long>(irow) * (sg.P + p.L) + sg.P + key) != 0;
+    if (!vis) return NEG_INF;
+    float x = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) x += sc_all[(w * 16 + r) * kScPitch + key];
+    return x * p.dscale2;
+  };
+  float mx = M;
+#pragma unroll 1
+  for (int key = 0; key < p.L; ++key) mx = fmaxf(mx, score(key));
+  const float ms = (mx == NEG_INF) ? 0.f : mx;
+  const float a = exp2f(M - ms);  // 0 when no piece had a visible key
+  l *= a;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] *= a;
+#pragma unroll 1
+  for (int key = 0; key < p.L; ++key) {
+    const float pk = exp2f(score(key) - ms);
+    if (pk == 0.f) continue;
+    l += pk;
+    const float wv = pk * p.dvs;
+    const float4 v = *reinterpret_cast<const float4*>(vst + key * kCols + c4);
+    acc[0] = fmaf(wv, v.x, acc[0]);
+    acc[1] = fmaf(wv, v.y, acc[1]);
+    acc[2] = fmaf(wv, v.z, acc[2]);
+    acc[3] = fmaf(wv, v.w, acc[3]);
+  }
+  // a row with nothing visible (empty prefix, no visible draft) is 0
+  if (prow < p.R) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* op = p.o + (static_cast<long long>(s_b) + prow / p.gq) * p.o_s0 +
+                        static_cast<long long>(kvh * p.gq + prow % p.gq) * p.o_s1 + col0 + c4;
+    *reinterpret_cast<uint32_t*>(op) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    *reinterpret_cast<uint32_t*>(op + 2) = pack_bf16(acc[2] * inv, acc[3] * inv);
+  }
+}

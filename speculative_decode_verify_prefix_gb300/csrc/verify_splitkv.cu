@@ -62,11 +62,12 @@ constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
-constexpr long long kColSplitMaxWork = 655360;  // prefix tokens x KV heads up to which head_dim 256 splits columns
+constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
 constexpr long long kPiecesPerSegment = 24;    // ... and at least the mean prefix over this many
+constexpr long long kPiecesPerSegmentColSplit = 48;  // ... this many for the column-split stream
 
 enum : unsigned {
   kErrBadIndex = 1u,
@@ -111,6 +112,7 @@ struct Params {
   unsigned char* vw;
   float kq, vq;       // dequantisation scales the stored codes are divided by
   long long w_min;
+  int n_stream;  // CTAs of the stream launch (read by the combine kernel of the two-launch forms)
   const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
   const void* mindptr;
   int mindptr64;
@@ -540,21 +542,20 @@ struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
 
-// EPI: the epilogue alone, after a stream-only launch has written every
-// piece's partial (same grid, share floor and plan fields, so the same pieces).
 // CS = 2 (head_dim 256, one KV head per CTA, at most two 16-row tiles): the
 // stream alone, each 16-row tile shared by a pair of warps that split the QK
 // contraction (exchanging their scaled partial scores through shared memory)
-// and own half of the output columns each; the epilogue then runs in an EPI
-// launch.  Half the accumulator registers per warp, so three CTAs per SM.
-template <int D, bool FP8, int MTW, bool EPI, int CS = 1>
+// and own half of the output columns each; the combine kernel then folds the
+// partials in its own launch.  Half the accumulator registers per warp, so
+// three CTAs per SM.
+template <int D, bool FP8, int MTW, int CS = 1>
 __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
   constexpr int NT = D / 8;        // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
-  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1 && !EPI), "column split: head_dim 256 stream only");
+  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1), "column split: head_dim 256 stream only");
   constexpr int DH = D / CS;       // output columns (and contraction length) of one warp
   constexpr int NTH = NT / CS;     // its n-tiles
   constexpr int KSH = KS / CS;     // its k-steps
@@ -607,7 +608,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
   const int c_self = blockIdx.x;
   const bool flagger = (warp == 0 && lane == 0);
 
-  if constexpr (!EPI) {
+  {
   int dslot = 0;  // ring slot of the next data job (job % nst, kept without a division)
   auto issue_idx = [&](const StageIt& it, long long job) {
     if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
@@ -1081,9 +1082,9 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
       }
     }
   }
-  }  // !EPI
+  }  // streaming
   if constexpr (CS == 2) {
-    cp_async_wait<0>();  // stream only: the epilogue runs in its own launch
+    cp_async_wait<0>();  // stream only: the partials are folded by the combine kernel
   } else {
 
   // ================= epilogue: tickets, log-sum-exp merges, drafts, output =================
@@ -1522,6 +1523,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
 }
 
 #include "verify_tc.cuh"
+#include "verify_combine.cuh"
 
 // ---------------------------------------------------------------------------
 // Host side.
@@ -1629,9 +1631,9 @@ bool tc_eligible(long long h_q, long long h_kv, long long D, long long L) {
   return (h_q / h_kv) * L <= 32;
 }
 
-// Plan fields of a tensor-memory call: one KV head per segment, RM = 16 or
-// 32 packed rows (MT = RM / 16 tiles); the epilogue kernel runs MT warps
-// and keeps its staged drafts (paged fused store) after the control block.
+// Plan fields of a two-launch call (tensor-memory or column-split stream,
+// then the combine kernel): one KV head per segment, RM = 16 or 32 packed
+// rows (MT = RM / 16 tiles).  The stream kernel sets its own launch shape.
 bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl) {
   if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
   const long long R = (h_q / h_kv) * L;
@@ -1660,9 +1662,10 @@ bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool 
 // most 32 packed rows per KV head.  The workspace / epilogue plan is the
 // tensor-memory one (one KV head per segment, MT = RM / 16, the epilogue in
 // MT warps); the stream runs 2 MT warps per CTA, three CTAs per SM.  Lighter
-// warps and more CTAs shorten small calls; on long ones the pair exchange and
-// the second launch cost more than they save, so by default only calls of at
-// most kColSplitMaxWork prefix tokens x KV heads (from static shapes) take it.
+// warps, more CTAs and the ticket-free combine launch shorten small calls; on
+// long ones the pair exchange costs more than it saves, so by default only
+// calls of at most kColSplitMaxWork prefix tokens x KV heads (from static
+// shapes) take it.
 bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
   if (g_cs == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0 || (h_q / h_kv) * L > 32) return false;
   return g_cs == 2 || total_tokens * h_kv <= kColSplitMaxWork;
@@ -1813,7 +1816,7 @@ using KernelFn = void (*)(Params);
 
 template <int D, bool FP8, int MTW>
 KernelFn kernel_ptr() {
-  return vsk_kernel<D, FP8, MTW, false>;
+  return vsk_kernel<D, FP8, MTW>;
 }
 
 KernelFn pick_kernel(int D, bool fp8, int mtw) {
@@ -1838,13 +1841,13 @@ KernelFn pick_tc_kernel(bool fp8, int rm) {
 }
 
 KernelFn pick_cs_kernel(bool fp8) {
-  return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, false, 2>)
-             : static_cast<KernelFn>(vsk_kernel<256, false, 1, false, 2>);
+  return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 2>) : static_cast<KernelFn>(vsk_kernel<256, false, 1, 2>);
 }
 
-KernelFn pick_epi_kernel(bool fp8) {
-  return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, true>) : static_cast<KernelFn>(vsk_kernel<256, false, 1, true>);
+KernelFn pick_combine_kernel(bool fp8) {
+  return fp8 ? static_cast<KernelFn>(vsk_combine_kernel<true>) : static_cast<KernelFn>(vsk_combine_kernel<false>);
 }
+
 
 // Ring entries and shared memory of vtc_kernel (e4m3 pools: an even number
 // of entries, so that V rows always sit in odd entries).
@@ -2034,17 +2037,17 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
   const int sms = device_sms(dev);
   if (sms <= 0) return fail("cannot query the SM count of device %d", dev);
-  // the streaming kernel (the whole call on the mma.sync path; the prefix
-  // stream on the tensor-memory path, followed by the epilogue kernel)
-  KernelFn fn = nullptr, fn_epi = nullptr;
+  // the streaming kernel (the whole call on the one-launch path; the prefix
+  // stream on the two-launch paths, followed by the combine kernel)
+  KernelFn fn = nullptr, fn_comb = nullptr;
   int threads = pl.threads;
   size_t smem = pl.smem;
   int per_sm = pl.ctas_per_sm;
   if (use_tc) {
     const int rm = 16 * pl.MT;
     fn = pick_tc_kernel(fp8, rm);
-    fn_epi = pick_epi_kernel(fp8);
-    if (!prepare_kernel(fn) || !prepare_kernel(fn_epi)) return fail("tensor-memory kernels unavailable");
+    fn_comb = pick_combine_kernel(fp8);
+    if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("tensor-memory kernels unavailable");
     int ne = 0;
     if (fp8)
       rm == 16 ? tc_smem<true, 16>(ne, smem) : tc_smem<true, 32>(ne, smem);
@@ -2055,8 +2058,8 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
     threads = tc::kThreads;
   } else if (use_cs) {
     fn = pick_cs_kernel(fp8);
-    fn_epi = pick_epi_kernel(fp8);
-    if (!prepare_kernel(fn) || !prepare_kernel(fn_epi)) return fail("column-split kernels unavailable");
+    fn_comb = pick_combine_kernel(fp8);
+    if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("column-split kernels unavailable");
     threads = sp.threads;
     smem = sp.smem;
     per_sm = sp.per_sm;
@@ -2099,11 +2102,14 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   // Smallest CTA share, from static shapes only (no device read, graph
   // safe): at least 64 tokens and, for small batches where the shares get
   // short, at least the mean prefix / 24 in whole stages, which bounds the
-  // pieces a segment's finisher merges.
+  // pieces a segment's finisher merges.  The column-split stream (three CTAs
+  // per SM, partials folded by a separate launch) does best with every CTA
+  // busy: mean prefix / 48.
   if (g_min_tokens > 0) {
     p.w_min = g_min_tokens;
   } else {
-    const long long wp = (mean_len / kPiecesPerSegment + kStageTokens - 1) / kStageTokens * kStageTokens;
+    const long long per = use_cs ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
+    const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
     p.w_min = std::max(kDefaultMinTokens, wp);
   }
   p.err = reinterpret_cast<unsigned*>(ws);
@@ -2111,8 +2117,8 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.nseg = B * pl.n_hg;
   p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
   p.po = reinterpret_cast<float*>(ws + wl.o_off);
+  p.n_stream = static_cast<int>(n_cta);
   void* args[] = {&p};
-  Params pe = p;  // the epilogue launch keeps the plan's own fields
   if (use_cs) {
     p.nwc = 2 * pl.MT;
     p.nst = sp.nst;
@@ -2124,12 +2130,14 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(threads), args,
                        smem, st);
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
-  if (fn_epi) {
-    void* args_e[] = {use_cs ? static_cast<void*>(&pe) : static_cast<void*>(&p)};
-    // same grid and share floor: the epilogue kernel finds the same pieces
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_epi), dim3(static_cast<unsigned>(n_cta)), dim3(pl.threads),
-                         args_e, pl.smem, st);
-    if (e != cudaSuccess) return fail("epilogue kernel launch failed: %s", cudaGetErrorString(e));
+  if (fn_comb) {
+    // one CTA per (segment, 16-row tile, 32-column slice); the share floor and
+    // n_stream let it find the pieces the stream launch wrote
+    const long long n_comb = B * pl.n_hg * pl.MT * cmb::kSlices;
+    if (n_comb > 0x7FFFFFFFLL) return fail("combine grid of %lld CTAs too large", n_comb);
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_comb), dim3(static_cast<unsigned>(n_comb)),
+                         dim3(cmb::kThreads), args, cmb::kSmem, st);
+    if (e != cudaSuccess) return fail("combine kernel launch failed: %s", cudaGetErrorString(e));
   }
   return 1;
 }

@@ -6,8 +6,8 @@
 // v_scale), with the two contractions on the 5th-generation tensor cores and
 // their accumulators in tensor memory, so that no thread holds a 16 x 256
 // accumulator tile in registers.  It writes the per-piece (o, log-sum-exp)
-// partials in vsk_kernel's workspace format; vsk_kernel<.., true> then runs
-// the tickets, merges, draft block and output (its epilogue-only form).
+// partials in vsk_kernel's workspace format; vsk_combine_kernel then folds
+// them, adds the draft block and writes the output (a second launch).
 //
 // One CTA per SM, one KV head per segment (heads per CTA HC = 1), 64-key tiles.
 // Keys are the M dimension of both products, so the packed query rows (RM =

@@ -232,7 +232,7 @@ def test_paged_entry_rejects_bad_arguments(change, msg):
 
 def test_launches_per_call_follows_the_form_switches():
     """Head_dim 256 with at most 32 packed rows per KV head takes the
-    column-split stream plus the epilogue launch up to 655,360 prefix tokens x
+    column-split stream plus the combine launch up to 1,048,576 prefix tokens x
     KV heads (mode 1), always (mode 2) or never (mode 0); the tensor-memory
     switch takes precedence.  Everything else is one launch."""
     f = vsk.launches_per_call
@@ -241,8 +241,8 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1                 # head_dim 128
         assert f(3, 16, 2, 256, 4, 1536) == 2                       # R = 32, 3,072 token-heads
         assert f(8, 8, 2, 256, 4, 8 * 20000) == 2                   # R = 16
-        assert f(16, 16, 2, 256, 4, 327680) == 2                    # exactly 655,360 token-heads
-        assert f(16, 16, 2, 256, 4, 327696) == 1                    # one token past it per sequence
+        assert f(16, 16, 2, 256, 4, 524288) == 2                    # exactly 1,048,576 token-heads
+        assert f(16, 16, 2, 256, 4, 524304) == 1                    # one token past it per sequence
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 1                # the long batch
         assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: no column split
         vsk.set_tuning_colsplit(2)

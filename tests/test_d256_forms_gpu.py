@@ -68,6 +68,9 @@ TC = [
       seed=707),                                                                          # one KV head, R = 32
     S("tc_int32_idx", (700, 64, 1), 4, 16, 2, 256, 256, perm=True, idx_dtype="int32", seed=708),
     S("tc_bf16_scales", (1024, 2048), 3, 16, 2, 256, 256, k_scale=0.5, v_scale=0.25, seed=709),
+    # more sequences than a block has threads (the combine kernel's length scan loops)
+    S("tc_300_short", tuple(int(x) for x in np.random.default_rng(761).integers(0, 41, 300)), 4, 16, 2, 256, 256,
+      perm=True, seed=761),
 ]
 
 
@@ -227,8 +230,24 @@ def test_form_split_count_independence(vsk, num_ctas, min_tok):
     assert vsk.read_error_flags() == 0
 
 
+@pytest.mark.parametrize("pool", ["bf16", "e4m3"])
+def test_form_one_segment_many_pieces(vsk, pool):
+    """One sequence and one KV head cut into 1000 pieces (1000 stream CTAs of
+    50 tokens): the combine step folds them all."""
+    spec = S(f"tc_one_long_{pool}", (50000,), 4, 8, 1, 256, 256, pool=pool, perm=True,
+             k_scale=0.5 if pool == "e4m3" else 1.0, seed=762)
+    p = gpu_problem(spec)
+    vsk.set_tuning(1000, 16)
+    try:
+        o = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
+    check(o, oracle_o(p))
+    assert vsk.read_error_flags() == 0
+
+
 def test_form_repeated_calls_and_graph_replay_identical(vsk):
-    """Two launches per call (stream, then epilogue): tickets are left at zero,
+    """Two launches per call (stream, then combine): no state is left behind,
     so repeated calls and CUDA-graph replays agree bit for bit."""
     spec = S("tc_repeat", (3000, 4000, 10), 4, 16, 2, 256, 256, perm=True, seed=752)
     p = gpu_problem(spec)
