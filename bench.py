@@ -117,6 +117,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--one-launch", action="store_true",
+                    help="keep every call on the one-launch kernel (no column split, no stream + combine launches)")
     ap.add_argument("--tc", action="store_true",
                     help="head_dim 256 calls stream the prefix with the tensor-memory kernel (tcgen05; "
                          "two launches per call: vtc_kernel, then the combine kernel)")
@@ -405,6 +407,8 @@ def run_ours(args, dist: Dist) -> dict:
     # the tensor-memory stream serves head_dim 256 with at most 32 packed rows per KV head
     tc = bool(args.tc) and spec.d == 256 and (spec.h_q // spec.h_kv) * spec.l_ext <= 32
     vsk.set_tuning_tc(tc)
+    vsk.set_tuning_colsplit(0 if args.one_launch else 1)
+    vsk.set_tuning_split_launch(0 if args.one_launch else 1)
     prob = workloads.make_problem(spec, dev)
     B = len(prob["prefix_lens"])
     nbytes = workloads.algorithmic_bytes(prob)
@@ -432,7 +436,8 @@ def run_ours(args, dist: Dist) -> dict:
         tokens = prob["kv_indices"].shape[0]
     launches = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, prob["max_len_extend"], tokens)
     kernel = ("vtc_kernel (+ vsk_combine_kernel)" if tc else
-              "vsk_kernel column-split stream (+ vsk_combine_kernel)" if launches == 2 else
+              "vsk_kernel column-split stream (+ vsk_combine_kernel)" if launches == 2 and spec.d == 256 else
+              "vsk_kernel stream only (+ vsk_combine_kernel)" if launches == 2 else
               "vsk_kernel<128,false>" if spec.d == 128 and spec.pool == "bf16" else "vsk_kernel")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,

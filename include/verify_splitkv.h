@@ -305,6 +305,19 @@ void vsk_set_tuning_colsplit(int mode);
  * the flat entry points, batch x block-table columns x page_size for the paged
  * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch
  * counts. */
+/* Tuning switch, for A/B runs and tests, over head_dim 64 and 128 calls with at
+ * most 32 draft rows per sequence: the prefix is streamed by a stream-only
+ * instance of the mma.sync kernel and the per-piece partials are folded, the
+ * draft block added and o written by the combine kernel in a second launch on
+ * the same stream (instead of the one-launch kernel's ticketed tail).  Mode 1
+ * (the default) takes that form when the call's prefix tokens times h_kv are
+ * at least 2,048 and at most 1,048,576 (4,194,304 when (h_q / h_kv) *
+ * max_len_extend <= 16), where it measured faster on GB300; mode 2 always
+ * takes it; mode 0 never does.  All forms
+ * compute the same result up to rounding order.  Process-wide; not
+ * thread-safe. */
+void vsk_set_tuning_split_launch(int mode);
+
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens);
 

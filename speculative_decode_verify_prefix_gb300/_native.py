@@ -100,6 +100,8 @@ def _bind(lib):
     lib.vsk_set_tuning_tc.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_colsplit.restype = None
     lib.vsk_set_tuning_colsplit.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_split_launch.restype = None
+    lib.vsk_set_tuning_split_launch.argtypes = [ctypes.c_int]
     lib.vsk_launches_per_call.restype = ctypes.c_int
     lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
     lib.vsk_set_tuning_shape.restype = None

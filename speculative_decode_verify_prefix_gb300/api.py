@@ -282,6 +282,13 @@ def set_tuning_colsplit(mode: int = 1) -> None:
     _native.lib().vsk_set_tuning_colsplit(int(mode))
 
 
+def set_tuning_split_launch(mode: int = 1) -> None:
+    """Head_dim 64 / 128 calls (at most 32 drafts): stream-only kernel plus a
+    combine launch for small calls (1, the default), always (2) or never (0);
+    for A/B runs and tests."""
+    _native.lib().vsk_set_tuning_split_launch(int(mode))
+
+
 def launches_per_call(batch: int, h_q: int, h_kv: int, head_dim: int, max_len_extend: int,
                       prefix_tokens: int) -> int:
     """Kernel launches one call of these shapes makes (1 or 2; 0 if no entry

@@ -1,6 +1,6 @@
 // ---------------------------------------------------------------------------
-// Combine kernel of the two-launch forms (head_dim 256: the column-split and
-// the tensor-memory streams).  Split-KV (flash-decode) attention computes one
+// Combine kernel of the two-launch forms (the column-split and tensor-memory
+// streams at head_dim 256, the stream-only vsk_kernel at 64 / 128).  Split-KV (flash-decode) attention computes one
 // (o, log-sum-exp) partial per CTA piece of a sequence's prefix and merges
 // them with the log-sum-exp rule; the verify step then continues the same
 // softmax over the causal draft-draft block (verify_splitkv.py page,
@@ -9,51 +9,61 @@
 //
 // When this kernel starts, the stream launch before it on the same stream has
 // written every piece's partial, so no ticket or arrival order is needed: one
-// CTA per (segment, 16-row query tile, 32-column slice of the output) reads
-// the segment's pieces straight away.  Its four warps split the pieces (each
-// keeps a running maximum, sum and weighted 16 x 32 block), meet in shared
-// memory, and then compute the draft scores of the tile (each warp a 64-wide
-// part of the head dimension, summed in a fixed order), continue the softmax
-// and write their 16 x 32 block of o.  The fused-store forms store the new
+// CTA per (segment, KV head of the segment, 16-row query tile, 32-column
+// slice of the output) reads the segment's pieces straight away.  Its four
+// warps split the pieces (each keeps a running maximum, sum and weighted
+// 16 x 32 block), meet in shared memory, and then compute the draft scores of
+// the tile (each warp a quarter of the head dimension, summed in a fixed
+// order), continue the softmax and write their 16 x 32 block of o.  The fused-store forms store the new
 // draft rows here too: tile 0's CTAs, each its 32-column slice of every row,
 // so every stored element has exactly one writer.
 //
 // The pieces of segment s = (b, hg) are found the way every kernel of a call
 // cuts the work: segments of virtual length max(P_b, 1) laid end to end, CTA
 // c of the stream grid (p.n_stream CTAs) owning [c W, c W + W) with
-// W = max(ceil(total / n_stream), w_min); piece c of s sits in slot c + s.
+// W = max(ceil(total / n_stream), w_min); piece c of s sits in slot c + s,
+// KV head hc of the segment's HC at partial (slot HC + hc).
 // ---------------------------------------------------------------------------
 namespace cmb {
-constexpr int kD = 256;                    // head_dim served
 constexpr int kThreads = 128;              // four warps
 constexpr int kCols = 32;                  // output columns per CTA
-constexpr int kSlices = kD / kCols;
-constexpr int kMaxL = 32;                  // draft keys (at most 32 packed rows)
-constexpr int kKPitch = kD * 2 + 16;       // bytes per staged K row (padded: conflict-free fragment reads)
-constexpr int kScanOff = 0;                // 2 x 4 x i64 block sums
-constexpr int kSrcOff = 128;               // [kMaxL] i64: row the draft is read from (-1: no row)
-constexpr int kDstOff = kSrcOff + kMaxL * 8;  // [kMaxL] i64: row it is stored to (-1: none)
-constexpr int kKOff = kDstOff + kMaxL * 8;    // [kMaxL][kKPitch] draft K rows, bf16
-constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] fp32 draft V slice
-constexpr int kFoldOff = kVOff + kMaxL * kCols * 4;  // per warp m[16], then l[16]
-constexpr int kAccOff = kFoldOff + 4 * 32 * 4;       // per warp [16][kCols] weighted sums
+constexpr int kMaxL = 32;                  // draft keys served
 constexpr int kScPitch = kMaxL + 1;
-constexpr int kScOff = kAccOff + 4 * 16 * kCols * 4;  // per warp [16][kScPitch] partial scores
-constexpr int kSmem = kScOff + 4 * 16 * kScPitch * 4;
-static_assert(kSmem <= 48 * 1024, "combine kernel fits the default shared-memory window");
-static_assert(kKOff % 16 == 0 && kVOff % 16 == 0 && kAccOff % 16 == 0, "16-byte aligned regions");
+// Shared-memory map of the head_dim D instance (bytes).
+template <int D>
+struct Geo {
+  static constexpr int kSlices = D / kCols;
+  static constexpr int kKPitch = D * 2 + 16;  // staged K row, bf16 (padded: conflict-free fragment reads)
+  static constexpr int kScanOff = 0;          // 2 x 4 x i64 block sums
+  static constexpr int kSrcOff = 128;         // [kMaxL] i64: row the draft is read from (-1: no row)
+  static constexpr int kDstOff = kSrcOff + kMaxL * 8;    // [kMaxL] i64: row it is stored to (-1: none)
+  static constexpr int kKOff = kDstOff + kMaxL * 8;      // [kMaxL][kKPitch] draft K rows
+  static constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] fp32 draft V slice
+  static constexpr int kFoldOff = kVOff + kMaxL * kCols * 4;  // per warp m[16], then l[16]
+  static constexpr int kAccOff = kFoldOff + 4 * 32 * 4;       // per warp [16][kCols] weighted sums
+  static constexpr int kScOff = kAccOff + 4 * 16 * kCols * 4;  // per warp [16][kScPitch] partial scores
+  static constexpr int kSmem = kScOff + 4 * 16 * kScPitch * 4;
+  static_assert(kSmem <= 48 * 1024, "combine kernel fits the default shared-memory window");
+  static_assert(kKOff % 16 == 0 && kVOff % 16 == 0 && kAccOff % 16 == 0, "16-byte aligned regions");
+};
 }  // namespace cmb
 
-template <bool FP8>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid_constant__ Params p) {
   using namespace cmb;
-  constexpr int D = kD;
+  using G = Geo<D>;
+  constexpr int kSlices = G::kSlices, kKPitch = G::kKPitch;
+  constexpr int kScanOff = G::kScanOff, kSrcOff = G::kSrcOff, kDstOff = G::kDstOff, kKOff = G::kKOff;
+  constexpr int kVOff = G::kVOff, kFoldOff = G::kFoldOff, kAccOff = G::kAccOff, kScOff = G::kScOff;
+  constexpr int DW = D / 4;    // head dimensions of one warp's part of the draft scores
+  constexpr int KSW = DW / 16;  // its k-steps
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, j = lane & 3;
   const int ch = static_cast<int>(blockIdx.x % kSlices);
   const int tile = static_cast<int>((blockIdx.x / kSlices) % p.MT);
-  const long long s_idx = static_cast<long long>(blockIdx.x) / (kSlices * p.MT);
+  const int hc = static_cast<int>((blockIdx.x / (kSlices * p.MT)) % p.HC);
+  const long long s_idx = static_cast<long long>(blockIdx.x) / (kSlices * p.MT * p.HC);
   const int RM = 16 * p.MT;
   const float NEG_INF = -INFINITY;
   Seg sg;
@@ -61,10 +71,10 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   sg.hg = static_cast<int>(s_idx % p.n_hg);
   load_seq(p, sg.b, sg.P, sg.kv0);
   sg.len = max(sg.P, 1);
-  const int kvh = sg.hg;  // one KV head per segment in the two-launch forms
+  const int kvh = sg.hg * p.HC + hc;
   const int col0 = ch * kCols;
   const bool writer = tile == 0;  // stores this CTA's column slice of the new drafts
-  const bool flagger = tid == 0 && ch == 0 && tile == 0;
+  const bool flagger = tid == 0 && ch == 0 && tile == 0 && hc == 0;
 
   // the sequence's draft rows in q / k_ext / v_ext / o (qo_indptr, validated)
   int s_b;
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   const long long off = before * p.n_hg + static_cast<long long>(sg.hg) * sg.len;
   const long long c_first = off / W, c_last = (off + sg.len - 1) / W;
   const long long npc = c_last - c_first + 1;  // pieces of the segment
-  const long long slot0 = c_first + s_idx;
+  const long long slot0 = c_first + s_idx;  // partial of piece i, this head: (slot0 + i) HC + hc
 
   // ---- stage the draft K rows (whole head dimension) and this slice of V ----
   const int LK = (p.L + 7) & ~7;  // whole 8-key groups (keys past L staged as zero)
@@ -200,11 +210,11 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     vst[key * kCols + (c - col0) + 1] = v.y;
   }
 
-  // ---- this warp's query fragments: rows of the tile, head dims [64 warp, 64 warp + 64) ----
-  uint32_t qf[4][4];
+  // ---- this warp's query fragments: rows of the tile, head dims [DW warp, DW warp + DW) ----
+  uint32_t qf[KSW][4];
   {
     const int r0 = 16 * tile + g;
-    load_q<4>(p, sg, 0, r0, r0 + 8, j, false, qf, 64 * warp);
+    load_q<KSW>(p, sg, hc, r0, r0 + 8, j, false, qf, DW * warp);
   }
 
   // ---- fold: warp w takes pieces w, w + 4, ...; lane = (row, 16 columns) ----
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
 #pragma unroll 1
     for (long long i = warp; i < npc; i += 8) {
       const bool two = i + 4 < npc;  // uniform across the warp
-      const long long sa = slot0 + i, sb = slot0 + (two ? i + 4 : i);
+      const long long sa = (slot0 + i) * p.HC + hc, sb = (slot0 + (two ? i + 4 : i)) * p.HC + hc;
       const float xa = __ldcg(p.plse + sa * RM + prow);
       const float xb = __ldcg(p.plse + sb * RM + prow);
       const float4* oa = reinterpret_cast<const float4*>(p.po + (sa * RM + prow) * D + col0 + fc);
@@ -259,14 +269,14 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
         make_float4(fa[4 * k], fa[4 * k + 1], fa[4 * k + 2], fa[4 * k + 3]);
   __syncthreads();  // staged drafts, fold partials
 
-  // ---- draft scores: this warp's 64-wide part of q . k for every 8-key group ----
+  // ---- draft scores: this warp's DW-wide part of q . k for every 8-key group ----
   float* scp = reinterpret_cast<float*>(smem + kScOff) + warp * 16 * kScPitch;
 #pragma unroll 1
   for (int nt = 0; nt * 8 < p.L; ++nt) {
     float sd[4] = {0.f, 0.f, 0.f, 0.f};
-    const unsigned char* kr = kst + (nt * 8 + g) * kKPitch + (64 * warp) * 2;
+    const unsigned char* kr = kst + (nt * 8 + g) * kKPitch + (DW * warp) * 2;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < KSW; ++kk) {
       const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 2 * j) * 2);
       const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + (kk * 16 + 8 + 2 * j) * 2);
       mma_bf16(sd, qf[kk], b0, b1);

@@ -63,6 +63,9 @@ constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
 constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
+constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
+constexpr long long kSplitLaunchMaxWork = 1LL << 20;   // ... up to which they do (more than 16 packed rows)
+constexpr long long kSplitLaunchMaxWork16 = 1LL << 22;  // ... up to which they do (at most 16 packed rows)
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
@@ -542,20 +545,20 @@ struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
 
-// CS = 2 (head_dim 256, one KV head per CTA, at most two 16-row tiles): the
-// stream alone, each 16-row tile shared by a pair of warps that split the QK
-// contraction (exchanging their scaled partial scores through shared memory)
-// and own half of the output columns each; the combine kernel then folds the
-// partials in its own launch.  Half the accumulator registers per warp, so
-// three CTAs per SM.
-template <int D, bool FP8, int MTW, int CS = 1>
+// SO (stream only): the kernel ends once its pieces' partials are written; the
+// combine kernel folds them in its own launch.  CS = 2 (head_dim 256, one KV
+// head per CTA, at most two 16-row tiles; stream only): each 16-row tile is
+// shared by a pair of warps that split the QK contraction (exchanging their
+// scaled partial scores through shared memory) and own half of the output
+// columns each.  Half the accumulator registers per warp, so three CTAs per SM.
+template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2)>
 __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
   constexpr int NT = D / 8;        // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
-  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1), "column split: head_dim 256 stream only");
+  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1 && SO), "column split: head_dim 256 stream only");
   constexpr int DH = D / CS;       // output columns (and contraction length) of one warp
   constexpr int NTH = NT / CS;     // its n-tiles
   constexpr int KSH = KS / CS;     // its k-steps
@@ -1083,7 +1086,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
     }
   }
   }  // streaming
-  if constexpr (CS == 2) {
+  if constexpr (SO) {
     cp_async_wait<0>();  // stream only: the partials are folded by the combine kernel
   } else {
 
@@ -1519,7 +1522,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
     }
     seg_advance(p, sg);
   }
-  }  // CS == 1
+  }  // !SO
 }
 
 #include "verify_tc.cuh"
@@ -1548,6 +1551,7 @@ int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
 int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
+int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 
 struct Plan {
   int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
@@ -1669,6 +1673,20 @@ bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool 
 bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
   if (g_cs == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0 || (h_q / h_kv) * L > 32) return false;
   return g_cs == 2 || total_tokens * h_kv <= kColSplitMaxWork;
+}
+// Stream-only vsk_kernel then the combine kernel, for head_dim 64 / 128 calls
+// with at most cmb::kMaxL drafts: small and mid-size calls, where the
+// one-launch kernel's tail (tickets, a two-level fold of the pieces, the
+// draft block) is a chain of memory round trips that the combine launch
+// shortens.  Not for the very smallest (the second launch costs more than it
+// saves), nor for long batches, where the one-launch kernel's two tiles per
+// warp (more than 16 packed rows) or its full occupancy win.
+bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
+  if (g_sl == 0 || (D != 64 && D != 128) || h_kv <= 0 || h_q % h_kv != 0 || L > cmb::kMaxL) return false;
+  if (g_sl == 2) return true;
+  const long long work = total_tokens * h_kv;
+  const long long cap = (h_q / h_kv) * L <= 16 ? kSplitLaunchMaxWork16 : kSplitLaunchMaxWork;
+  return work >= kSplitLaunchMinWork && work <= cap;
 }
 struct StreamPlan {
   int threads, nst, ring_off, head_bytes, misc_off, misc_bytes, per_sm;
@@ -1844,8 +1862,30 @@ KernelFn pick_cs_kernel(bool fp8) {
   return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 2>) : static_cast<KernelFn>(vsk_kernel<256, false, 1, 2>);
 }
 
-KernelFn pick_combine_kernel(bool fp8) {
-  return fp8 ? static_cast<KernelFn>(vsk_combine_kernel<true>) : static_cast<KernelFn>(vsk_combine_kernel<false>);
+KernelFn pick_so_kernel(int D, bool fp8) {
+  switch (D) {
+    case 64: return fp8 ? static_cast<KernelFn>(vsk_kernel<64, true, 1, 1, true>)
+                        : static_cast<KernelFn>(vsk_kernel<64, false, 1, 1, true>);
+    case 128: return fp8 ? static_cast<KernelFn>(vsk_kernel<128, true, 1, 1, true>)
+                         : static_cast<KernelFn>(vsk_kernel<128, false, 1, 1, true>);
+    default: return nullptr;
+  }
+}
+
+KernelFn pick_combine_kernel(int D, bool fp8) {
+  switch (D) {
+    case 64: return fp8 ? static_cast<KernelFn>(vsk_combine_kernel<64, true>)
+                        : static_cast<KernelFn>(vsk_combine_kernel<64, false>);
+    case 128: return fp8 ? static_cast<KernelFn>(vsk_combine_kernel<128, true>)
+                         : static_cast<KernelFn>(vsk_combine_kernel<128, false>);
+    case 256: return fp8 ? static_cast<KernelFn>(vsk_combine_kernel<256, true>)
+                         : static_cast<KernelFn>(vsk_combine_kernel<256, false>);
+    default: return nullptr;
+  }
+}
+
+int combine_smem(int D) {
+  return D == 64 ? cmb::Geo<64>::kSmem : D == 128 ? cmb::Geo<128>::kSmem : cmb::Geo<256>::kSmem;
 }
 
 
@@ -1997,13 +2037,16 @@ void vsk_set_tuning_tc(int mode) { g_tc = mode == 1 ? 1 : 0; }
 
 void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode : 1; }
 
+void vsk_set_tuning_split_launch(int mode) { g_sl = (mode == 0 || mode == 2) ? mode : 1; }
+
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens) {
   if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
   const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
   return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) ||
-          cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
+          cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens) ||
+          sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
              ? 2
              : 1;
 }
@@ -2026,9 +2069,10 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
                             void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
   const bool use_tc = tc_eligible(h_q, h_kv, D, L);
   const bool use_cs = !use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  const bool use_sl = !use_tc && !use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan pl;
   if ((use_tc || use_cs) ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
-                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 0))
+                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, use_sl ? 1 : 0))
     return 0;
   StreamPlan sp{};
   if (use_cs && !make_cs_stream_plan(pl, D, fp8, sp)) return 0;
@@ -2046,7 +2090,7 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   if (use_tc) {
     const int rm = 16 * pl.MT;
     fn = pick_tc_kernel(fp8, rm);
-    fn_comb = pick_combine_kernel(fp8);
+    fn_comb = pick_combine_kernel(256, fp8);
     if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("tensor-memory kernels unavailable");
     int ne = 0;
     if (fp8)
@@ -2058,11 +2102,16 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
     threads = tc::kThreads;
   } else if (use_cs) {
     fn = pick_cs_kernel(fp8);
-    fn_comb = pick_combine_kernel(fp8);
+    fn_comb = pick_combine_kernel(256, fp8);
     if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("column-split kernels unavailable");
     threads = sp.threads;
     smem = sp.smem;
     per_sm = sp.per_sm;
+  } else if (use_sl) {
+    fn = pick_so_kernel(static_cast<int>(D), fp8);
+    fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
+    if (!fn || !fn_comb || !prepare_kernel(fn) || !prepare_kernel(fn_comb))
+      return fail("stream-only kernels for head_dim %lld unavailable", D);
   } else {
     fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
     if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
@@ -2102,13 +2151,12 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   // Smallest CTA share, from static shapes only (no device read, graph
   // safe): at least 64 tokens and, for small batches where the shares get
   // short, at least the mean prefix / 24 in whole stages, which bounds the
-  // pieces a segment's finisher merges.  The column-split stream (three CTAs
-  // per SM, partials folded by a separate launch) does best with every CTA
-  // busy: mean prefix / 48.
+  // pieces a segment's finisher merges.  The two-launch forms (partials
+  // folded by the combine launch) do best with every CTA busy: mean prefix / 48.
   if (g_min_tokens > 0) {
     p.w_min = g_min_tokens;
   } else {
-    const long long per = use_cs ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
+    const long long per = (use_cs || use_sl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
     const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
     p.w_min = std::max(kDefaultMinTokens, wp);
   }
@@ -2133,10 +2181,10 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   if (fn_comb) {
     // one CTA per (segment, 16-row tile, 32-column slice); the share floor and
     // n_stream let it find the pieces the stream launch wrote
-    const long long n_comb = B * pl.n_hg * pl.MT * cmb::kSlices;
+    const long long n_comb = B * pl.n_hg * pl.HC * pl.MT * (D / cmb::kCols);
     if (n_comb > 0x7FFFFFFFLL) return fail("combine grid of %lld CTAs too large", n_comb);
     e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_comb), dim3(static_cast<unsigned>(n_comb)),
-                         dim3(cmb::kThreads), args, cmb::kSmem, st);
+                         dim3(cmb::kThreads), args, combine_smem(static_cast<int>(D)), st);
     if (e != cudaSuccess) return fail("combine kernel launch failed: %s", cudaGetErrorString(e));
   }
   return 1;

@@ -234,7 +234,9 @@ def test_launches_per_call_follows_the_form_switches():
     """Head_dim 256 with at most 32 packed rows per KV head takes the
     column-split stream plus the combine launch up to 1,048,576 prefix tokens x
     KV heads (mode 1), always (mode 2) or never (mode 0); the tensor-memory
-    switch takes precedence.  Everything else is one launch."""
+    switch takes precedence.  Head_dim 64 / 128 with at most 32 drafts takes the
+    stream-only kernel plus the combine launch inside its own size window.
+    Everything else is one launch."""
     f = vsk.launches_per_call
     try:
         vsk.set_tuning_colsplit(1)
@@ -245,6 +247,19 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(16, 16, 2, 256, 4, 524304) == 1                    # one token past it per sequence
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 1                # the long batch
         assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: no column split
+        # head_dim 64 / 128: stream + combine from 2,048 token-heads up to 2^20 (R > 16) or 2^22 (R <= 16)
+        assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
+        assert f(2, 16, 2, 128, 4, 1024) == 2                       # exactly 2,048 token-heads
+        assert f(16, 16, 2, 128, 4, 524288) == 2                    # R = 32, 2^20
+        assert f(16, 16, 2, 128, 4, 524304) == 1
+        assert f(16, 32, 8, 128, 4, 524288) == 2                    # R = 16, 2^22
+        assert f(16, 32, 8, 128, 4, 524304) == 1
+        assert f(2, 64, 2, 128, 33, 4000) == 1                      # 33 drafts: beyond the combine kernel
+        vsk.set_tuning_split_launch(0)
+        assert f(16, 32, 8, 128, 4, 524288) == 1
+        vsk.set_tuning_split_launch(2)
+        assert f(64, 32, 8, 128, 4, 64 * 20000) == 2
+        vsk.set_tuning_split_launch(1)
         vsk.set_tuning_colsplit(2)
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1
@@ -255,6 +270,7 @@ def test_launches_per_call_follows_the_form_switches():
     finally:
         vsk.set_tuning_tc(False)
         vsk.set_tuning_colsplit(1)
+        vsk.set_tuning_split_launch(1)
     assert f(0, 16, 2, 256, 4, 10) == 0                             # no sequences
     assert f(2, 15, 2, 256, 4, 10) == 0                             # h_q not a multiple of h_kv
     assert f(2, 16, 2, 96, 4, 10) == 0                              # head_dim not built

@@ -1,12 +1,15 @@
-"""GPU parity of the two alternative head_dim 256 streams, against the fp64
-oracle, with the one-launch mma.sync kernel checked beside each:
+"""GPU parity of the two-launch forms (a prefix stream, then the combine
+kernel), against the fp64 oracle, with the one-launch mma.sync kernel checked
+beside each:
 
-- "tc": the tensor-memory stream (tcgen05.mma, accumulators in TMEM);
+- "tc": the tensor-memory stream (tcgen05.mma, accumulators in TMEM), head_dim 256;
 - "colsplit": the column-split mma.sync stream (two warps per 16-row query
-  tile, each holding half the head dimension).
+  tile, each holding half the head dimension), head_dim 256;
+- "split": the stream-only mma.sync kernel at head_dim 64 and 128 (every case
+  below rewritten to one of them, chosen by a hash of its name).
 
-Both serve head_dim 256 with at most 32 packed query rows per KV head and fold
-their partials in a second launch.  Same tolerance as the other parity tests
+All serve at most 32 packed query rows per KV head (head_dim 256) or 32 drafts
+(64 / 128) and fold their partials in a second launch.  Same tolerance as the other parity tests
 (atol 2e-2, rtol 1e-2 on the bf16 output); stored cache codes and repeated /
 graph-replayed calls are compared bit for bit.  Every call also checks the
 device error word, whose timeout bit would report a pipeline wait that gave up.
@@ -15,31 +18,54 @@ import numpy as np
 import pytest
 import torch
 
+import zlib
+
 import oracle
 import workloads
-from test_parity_gpu import (_bits_np, _draft_rows, _free_rows, _pool_np, _subproblem, check, gpu_problem,
+from test_parity_gpu import gpu_problem as _gpu_problem
+from test_parity_gpu import (_bits_np, _draft_rows, _free_rows, _pool_np, _subproblem, check,
                              oracle_o, run_gpu, run_paged, run_tree)
 
 pytestmark = pytest.mark.gpu
 S = workloads.Spec
 
 
+FORM = {"name": "tc"}
+
+
+def _adapt(spec):
+    """The case as the form under test serves it: the "split" form runs it at
+    head_dim 64 or 128."""
+    if FORM["name"] != "split":
+        return spec
+    d = 64 if zlib.crc32(spec.name.encode()) % 3 == 0 else 128
+    return workloads.replace(spec, d=d, dv=d)
+
+
+def gpu_problem(spec, **over):
+    return _gpu_problem(_adapt(spec), **over)
+
+
 def _select(m, form):
     m.set_tuning_tc(form == "tc")
     m.set_tuning_colsplit(2 if form == "colsplit" else 0)
+    m.set_tuning_split_launch(2 if form == "split" else 0)
 
 
-@pytest.fixture(scope="module", params=["tc", "colsplit"])
+@pytest.fixture(scope="module", params=["tc", "colsplit", "split"])
 def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 
     m.build()
     m.form = request.param
+    FORM["name"] = m.form
     _select(m, m.form)
     yield m
     m.set_tuning(0, 0)
     m.set_tuning_tc(False)
     m.set_tuning_colsplit(1)
+    m.set_tuning_split_launch(1)
+    FORM["name"] = "tc"
 
 
 def both(vsk, fn):
@@ -255,7 +281,7 @@ def test_form_repeated_calls_and_graph_replay_identical(vsk):
     try:
         a = run_gpu(vsk, p)
         b = run_gpu(vsk, p)
-        ws = vsk.get_workspace("cuda", 3, 16, 2, 256, 256, 4)
+        ws = vsk.get_workspace("cuda", 3, 16, 2, p["q"].shape[2], p["v_ext"].shape[2], 4)
         o = torch.empty_like(a)
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -352,7 +378,7 @@ def _tc_cases(n=24, seed=2025):
 @pytest.mark.parametrize("case", _tc_cases(), ids=lambda c: c[0].name)
 def test_form_random_problem_matches_oracle(vsk, case):
     spec, form, (nc, mt) = case
-    p = workloads.make_problem(spec, "cuda")
+    p = workloads.make_problem(_adapt(spec), "cuda")
     vsk.read_error_flags()
     vsk.set_tuning(nc, mt)
     try:
