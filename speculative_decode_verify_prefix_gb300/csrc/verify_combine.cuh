@@ -38,8 +38,8 @@ struct Geo {
   static constexpr int kSrcOff = 128;         // [kMaxL] i64: row the draft is read from (-1: no row)
   static constexpr int kDstOff = kSrcOff + kMaxL * 8;    // [kMaxL] i64: row it is stored to (-1: none)
   static constexpr int kKOff = kDstOff + kMaxL * 8;      // [kMaxL][kKPitch] draft K rows
-  static constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] fp32 draft V slice
-  static constexpr int kFoldOff = kVOff + kMaxL * kCols * 4;  // per warp m[16], then l[16]
+  static constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] bf16 draft V slice
+  static constexpr int kFoldOff = kVOff + kMaxL * kCols * 2;  // per warp m[16], then l[16]
   static constexpr int kAccOff = kFoldOff + 4 * 32 * 4;       // per warp [16][kCols] weighted sums
   static constexpr int kScOff = kAccOff + 4 * 16 * kCols * 4;  // per warp [16][kScPitch] partial scores
   static constexpr int kSmem = kScOff + 4 * 16 * kScPitch * 4;
@@ -76,6 +76,29 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   const bool writer = tile == 0;  // stores this CTA's column slice of the new drafts
   const bool flagger = tid == 0 && ch == 0 && tile == 0 && hc == 0;
 
+  // block sums of the virtual segment lengths: all of them and those before b
+  // (issued first: nothing else waits on fewer loads)
+  long long* scan = reinterpret_cast<long long*>(smem + kScanOff);
+  {
+    long long tot_t = 0, bef_t = 0;
+    for (int bb = tid; bb < p.B; bb += kThreads) {
+      int P_;
+      long long k_;
+      seq_info(p, bb, P_, k_);
+      const long long ln = max(P_, 1);
+      tot_t += ln;
+      if (bb < sg.b) bef_t += ln;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot_t += __shfl_xor_sync(0xffffffffu, tot_t, o);
+      bef_t += __shfl_xor_sync(0xffffffffu, bef_t, o);
+    }
+    if (lane == 0) {
+      scan[warp] = tot_t;
+      scan[4 + warp] = bef_t;
+    }
+  }
   // the sequence's draft rows in q / k_ext / v_ext / o (qo_indptr, validated)
   int s_b;
   {
@@ -109,28 +132,6 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     ksrc[key] = src;
     kdst[key] = dst;
   }
-  // block sums of the virtual segment lengths: all of them and those before b
-  long long* scan = reinterpret_cast<long long*>(smem + kScanOff);
-  {
-    long long tot_t = 0, bef_t = 0;
-    for (int bb = tid; bb < p.B; bb += kThreads) {
-      int P_;
-      long long k_;
-      seq_info(p, bb, P_, k_);
-      const long long ln = max(P_, 1);
-      tot_t += ln;
-      if (bb < sg.b) bef_t += ln;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tot_t += __shfl_xor_sync(0xffffffffu, tot_t, o);
-      bef_t += __shfl_xor_sync(0xffffffffu, bef_t, o);
-    }
-    if (lane == 0) {
-      scan[warp] = tot_t;
-      scan[4 + warp] = bef_t;
-    }
-  }
   __syncthreads();  // also publishes ksrc / kdst
   const long long tot = (scan[0] + scan[1] + scan[2] + scan[3]) * p.n_hg;
   const long long before = scan[4] + scan[5] + scan[6] + scan[7];
@@ -142,72 +143,91 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   const long long slot0 = c_first + s_idx;  // partial of piece i, this head: (slot0 + i) HC + hc
 
   // ---- stage the draft K rows (whole head dimension) and this slice of V ----
+  // Plain drafts (k_extend / v_extend, no store) go by cp.async and land while
+  // the pieces are folded; the cache and store forms convert in registers.
   const int LK = (p.L + 7) & ~7;  // whole 8-key groups (keys past L staged as zero)
   unsigned char* kst = smem + kKOff;
-  float* vst = reinterpret_cast<float*>(smem + kVOff);
-  for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
-    const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
-    uint32_t val = 0u;
-    const long long src = key < p.L ? ksrc[key] : -1;
-    if (src >= 0) {
-      if (p.paged && p.wmode != 2) {
-        const unsigned char* kr = p.kb + src * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
-        if constexpr (FP8)
-          val = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(kr + d));
-        else
-          val = *reinterpret_cast<const uint32_t*>(kr + d * 2);
-      } else {
-        val = ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + d);
-        const long long dst = kdst[key];
-        const bool mine = writer && dst >= 0 && d >= col0 && d < col0 + kCols;
-        if (p.wmode != 0) {
-          const float2 x = unpack_bf16(val);
-          unsigned char* kd = p.kw + (dst >= 0 ? dst : 0) * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
-          if constexpr (FP8) {
-            const unsigned short c = store_e4m3x2(x.x, x.y, p.kq);
-            if (mine) *reinterpret_cast<unsigned short*>(kd + d) = c;
-            if (p.wmode == 2) val = e4m3x2_to_bf16x2(c);  // attend over the stored values
-          } else {
-            const uint32_t c = store_bf16x2(x.x, x.y, p.kq);
-            if (mine) *reinterpret_cast<uint32_t*>(kd + d * 2) = c;
-            if (p.wmode == 2) val = c;
+  unsigned char* vst = smem + kVOff;
+  if (!p.paged && p.wmode == 0) {
+    for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
+      const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
+      unsigned char* dk = kst + key * kKPitch + d * 2;
+      if (key < p.L)
+        cp_async_4(smem_u32(dk), p.ke + ksrc[key] * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + d);
+      else
+        *reinterpret_cast<uint32_t*>(dk) = 0u;
+    }
+    for (int idx = tid; idx < p.L * (kCols / 2); idx += kThreads) {
+      const int key = idx / (kCols / 2), c = (idx % (kCols / 2)) * 2;
+      cp_async_4(smem_u32(vst + (key * kCols + c) * 2),
+                 p.ve + ksrc[key] * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + col0 + c);
+    }
+    cp_async_commit();
+  } else {
+    for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
+      const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
+      uint32_t val = 0u;
+      const long long src = key < p.L ? ksrc[key] : -1;
+      if (src >= 0) {
+        if (p.paged && p.wmode != 2) {
+          const unsigned char* kr = p.kb + src * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+          if constexpr (FP8)
+            val = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(kr + d));
+          else
+            val = *reinterpret_cast<const uint32_t*>(kr + d * 2);
+        } else {
+          val = ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + d);
+          const long long dst = kdst[key];
+          const bool mine = writer && dst >= 0 && d >= col0 && d < col0 + kCols;
+          if (p.wmode != 0) {
+            const float2 x = unpack_bf16(val);
+            unsigned char* kd = p.kw + (dst >= 0 ? dst : 0) * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
+            if constexpr (FP8) {
+              const unsigned short c = store_e4m3x2(x.x, x.y, p.kq);
+              if (mine) *reinterpret_cast<unsigned short*>(kd + d) = c;
+              if (p.wmode == 2) val = e4m3x2_to_bf16x2(c);  // attend over the stored values
+            } else {
+              const uint32_t c = store_bf16x2(x.x, x.y, p.kq);
+              if (mine) *reinterpret_cast<uint32_t*>(kd + d * 2) = c;
+              if (p.wmode == 2) val = c;
+            }
           }
         }
       }
+      *reinterpret_cast<uint32_t*>(kst + key * kKPitch + d * 2) = val;
     }
-    *reinterpret_cast<uint32_t*>(kst + key * kKPitch + d * 2) = val;
-  }
-  for (int idx = tid; idx < p.L * (kCols / 2); idx += kThreads) {
-    const int key = idx / (kCols / 2), c = col0 + (idx % (kCols / 2)) * 2;
-    float2 v = make_float2(0.f, 0.f);
-    const long long src = ksrc[key];
-    if (src >= 0) {
-      if (p.paged && p.wmode != 2) {
-        const unsigned char* vr = p.vb + src * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
-        if constexpr (FP8)
-          v = unpack_bf16(e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(vr + c)));
-        else
-          v = unpack_bf16(*reinterpret_cast<const uint32_t*>(vr + c * 2));
-      } else {
-        v = unpack_bf16(ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c));
-        const long long dst = kdst[key];
-        if (p.wmode != 0) {
-          unsigned char* vd = p.vw + (dst >= 0 ? dst : 0) * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
-          const bool mine = writer && dst >= 0;
-          if constexpr (FP8) {
-            const unsigned short cv = store_e4m3x2(v.x, v.y, p.vq);
-            if (mine) *reinterpret_cast<unsigned short*>(vd + c) = cv;
-            if (p.wmode == 2) v = unpack_bf16(e4m3x2_to_bf16x2(cv));
-          } else {
-            const uint32_t cv = store_bf16x2(v.x, v.y, p.vq);
-            if (mine) *reinterpret_cast<uint32_t*>(vd + c * 2) = cv;
-            if (p.wmode == 2) v = unpack_bf16(cv);
+    for (int idx = tid; idx < p.L * (kCols / 2); idx += kThreads) {
+      const int key = idx / (kCols / 2), c = col0 + (idx % (kCols / 2)) * 2;
+      uint32_t val = 0u;  // bf16 x2 (every staged value is a bf16 value)
+      const long long src = ksrc[key];
+      if (src >= 0) {
+        if (p.paged && p.wmode != 2) {
+          const unsigned char* vr = p.vb + src * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+          if constexpr (FP8)
+            val = e4m3x2_to_bf16x2(*reinterpret_cast<const unsigned short*>(vr + c));
+          else
+            val = *reinterpret_cast<const uint32_t*>(vr + c * 2);
+        } else {
+          val = ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c);
+          const long long dst = kdst[key];
+          if (p.wmode != 0) {
+            const float2 v = unpack_bf16(val);
+            unsigned char* vd = p.vw + (dst >= 0 ? dst : 0) * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+            const bool mine = writer && dst >= 0;
+            if constexpr (FP8) {
+              const unsigned short cv = store_e4m3x2(v.x, v.y, p.vq);
+              if (mine) *reinterpret_cast<unsigned short*>(vd + c) = cv;
+              if (p.wmode == 2) val = e4m3x2_to_bf16x2(cv);
+            } else {
+              const uint32_t cv = store_bf16x2(v.x, v.y, p.vq);
+              if (mine) *reinterpret_cast<uint32_t*>(vd + c * 2) = cv;
+              if (p.wmode == 2) val = cv;
+            }
           }
         }
       }
+      *reinterpret_cast<uint32_t*>(vst + (key * kCols + (c - col0)) * 2) = val;
     }
-    vst[key * kCols + (c - col0)] = v.x;
-    vst[key * kCols + (c - col0) + 1] = v.y;
   }
 
   // ---- this warp's query fragments: rows of the tile, head dims [DW warp, DW warp + DW) ----
@@ -267,6 +287,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   for (int k = 0; k < 4; ++k)
     *reinterpret_cast<float4*>(sm_a + fr * kCols + fc + 4 * k) =
         make_float4(fa[4 * k], fa[4 * k + 1], fa[4 * k + 2], fa[4 * k + 3]);
+  cp_async_wait<0>();
   __syncthreads();  // staged drafts, fold partials
 
   // ---- draft scores: this warp's DW-wide part of q . k for every 8-key group ----
@@ -348,11 +369,12 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     if (pk == 0.f) continue;
     l += pk;
     const float wv = pk * p.dvs;
-    const float4 v = *reinterpret_cast<const float4*>(vst + key * kCols + c4);
-    acc[0] = fmaf(wv, v.x, acc[0]);
-    acc[1] = fmaf(wv, v.y, acc[1]);
-    acc[2] = fmaf(wv, v.z, acc[2]);
-    acc[3] = fmaf(wv, v.w, acc[3]);
+    const uint2 vv = *reinterpret_cast<const uint2*>(vst + (key * kCols + c4) * 2);
+    const float2 v0 = unpack_bf16(vv.x), v1 = unpack_bf16(vv.y);
+    acc[0] = fmaf(wv, v0.x, acc[0]);
+    acc[1] = fmaf(wv, v0.y, acc[1]);
+    acc[2] = fmaf(wv, v1.x, acc[2]);
+    acc[3] = fmaf(wv, v1.y, acc[3]);
   }
   // a row with nothing visible (empty prefix, no visible draft) is 0
   if (prow < p.R) {
