@@ -45,17 +45,21 @@ import workloads  # noqa: E402
 
 METRIC = "verify-attn KV GB/s (fraction of GB300 HBM peak) and µs/call, 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decode_verify_prefix_gb300", "csrc", "verify_splitkv.cu")
+KERNEL_DIR = os.path.join(ROOT, "speculative_decode_verify_prefix_gb300", "csrc")
+KERNEL_SRCS = ("verify_splitkv.cu", "verify_combine.cuh", "verify_tc.cuh")  # every kernel of a call
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
 def kernel_source_hash() -> str:
-    """Hash of the kernel source's code: comments and blank space are left
-    out, so an edit of comments alone keeps the ncu figures valid."""
+    """Hash of the kernel sources' code (every file a call's kernels come
+    from): comments and blank space are left out, so an edit of comments
+    alone keeps the ncu figures valid."""
     import re
 
-    with open(KERNEL_SRC) as f:
-        src = f.read()
+    src = ""
+    for name in KERNEL_SRCS:
+        with open(os.path.join(KERNEL_DIR, name)) as f:
+            src += f.read() + "\n"
     src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
     src = re.sub(r"//[^\n]*", " ", src)
     src = " ".join(src.split())
