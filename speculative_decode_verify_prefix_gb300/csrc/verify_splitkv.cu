@@ -65,7 +65,7 @@ constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from 
 constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
 constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
 constexpr long long kSplitLaunchMaxWork = 1LL << 20;   // ... up to which they do (more than 16 packed rows)
-constexpr long long kSplitLaunchMaxWork16 = 1LL << 22;  // ... up to which they do (at most 16 packed rows)
+constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... up to which they do (at most 16 packed rows)
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
