@@ -1,0 +1,66 @@
+"""The launch count a call reports (vsk_launches_per_call, which bench.py's
+gpu_launches uses) against the kernels the CUDA profiler sees for the call:
+one launch for the one-launch kernel, two for the stream + combine forms."""
+import pytest
+import torch
+
+import workloads
+from test_parity_gpu import gpu_problem, run_gpu
+
+pytestmark = pytest.mark.gpu
+S = workloads.Spec
+
+
+@pytest.fixture(scope="module")
+def vsk():
+    import speculative_decode_verify_prefix_gb300 as m
+    from torch.profiler import ProfilerActivity, profile
+
+    m.build()
+    # the first profiling session of a process can come back empty while the
+    # CUDA activity tracer starts: run one on a throwaway kernel
+    with profile(activities=[ProfilerActivity.CUDA]):
+        torch.ones(1024, device="cuda").sum()
+        torch.cuda.synchronize()
+    yield m
+    m.set_tuning_colsplit(1)
+    m.set_tuning_split_launch(1)
+
+
+def _kernels_of_one_call(vsk, p):
+    from torch.profiler import ProfilerActivity, profile
+
+    run_gpu(vsk, p)  # warm (library load, workspace)
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        run_gpu(vsk, p)
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    if not names:
+        pytest.skip("the CUDA profiler recorded no kernels here")
+    return [n for n in names if "vsk_" in n]
+
+
+CASES = [
+    # (spec, colsplit mode, split-launch mode)
+    (workloads.TINY, 1, 1),                                                   # tiny: one launch
+    (workloads.D256, 1, 1),                                                   # column split + combine
+    (workloads.D256, 0, 1),                                                   # forced one launch
+    (S("lc_gqa", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 1),  # stream + combine
+    (S("lc_gqa_one", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}_cs{c[1]}_sl{c[2]}")
+def test_reported_launches_match_the_profiled_kernels(vsk, case):
+    spec, cs, sl = case
+    vsk.set_tuning_colsplit(cs)
+    vsk.set_tuning_split_launch(sl)
+    p = gpu_problem(spec)
+    B = len(p["prefix_lens"])
+    want = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, p["max_len_extend"], p["kv_indices"].shape[0])
+    got = _kernels_of_one_call(vsk, p)
+    assert want in (1, 2)
+    assert len(got) == want, got
+    if want == 2:
+        assert any("vsk_combine_kernel" in n for n in got)
