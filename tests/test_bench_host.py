@@ -93,3 +93,20 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_form_flags_and_traffic_lookup():
+    """--one-launch / --tc parse; the committed ncu traffic figures are found
+    for the workloads they were taken on only while the kernel sources match
+    the hash they were taken with."""
+    a = bench.parse_args(["--one-launch", "--tc", "--workload", "d256_b8"])
+    assert a.one_launch and a.tc and a.workload == "d256_b8"
+    d = bench.parse_args([])
+    assert not d.one_launch and not d.tc and d.workload == "serving"
+    with open(bench.TRAFFIC_FILE) as f:
+        t = json.load(f)
+    if t.get("kernel_source_sha256") == bench.kernel_source_hash():
+        for w, e in t["workloads"].items():
+            assert bench.traffic_per_launch(w) == e["dram_bytes_per_launch"]
+    else:
+        assert bench.traffic_per_launch("serving") is None
