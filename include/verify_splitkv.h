@@ -311,7 +311,7 @@ void vsk_set_tuning_colsplit(int mode);
  * draft block added and o written by the combine kernel in a second launch on
  * the same stream (instead of the one-launch kernel's ticketed tail).  Mode 1
  * (the default) takes that form when the call's prefix tokens times h_kv are
- * at least 2,048 and at most 1,048,576 (8,388,608 when (h_q / h_kv) *
+ * at least 2,048 and at most 4,194,304 (8,388,608 when (h_q / h_kv) *
  * max_len_extend <= 16), where it measured faster on GB300; mode 2 always
  * takes it; mode 0 never does.  All forms
  * compute the same result up to rounding order.  Process-wide; not

@@ -64,7 +64,8 @@ constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a w
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
 constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
 constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
-constexpr long long kSplitLaunchMaxWork = 1LL << 20;   // ... up to which they do (more than 16 packed rows)
+constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
+constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
 constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... up to which they do (at most 16 packed rows)
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
@@ -1679,8 +1680,9 @@ bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long l
 // one-launch kernel's tail (tickets, a two-level fold of the pieces, the
 // draft block) is a chain of memory round trips that the combine launch
 // shortens.  Not for the very smallest (the second launch costs more than it
-// saves), nor for long batches, where the one-launch kernel's two tiles per
-// warp (more than 16 packed rows) or its full occupancy win.
+// saves), nor for long batches, where the one-launch kernel's finishers hide
+// its tail behind other CTAs' streaming.  Warps take two tiles (more than 16
+// packed rows) from kSplitTwoTileMinTokens prefix tokens.
 bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
   if (g_sl == 0 || (D != 64 && D != 128) || h_kv <= 0 || h_q % h_kv != 0 || L > cmb::kMaxL) return false;
   if (g_sl == 2) return true;
@@ -1862,7 +1864,16 @@ KernelFn pick_cs_kernel(bool fp8) {
   return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 2>) : static_cast<KernelFn>(vsk_kernel<256, false, 1, 2>);
 }
 
-KernelFn pick_so_kernel(int D, bool fp8) {
+KernelFn pick_so_kernel(int D, bool fp8, int mtw) {
+  if (mtw == 2) {
+    switch (D) {
+      case 64: return fp8 ? static_cast<KernelFn>(vsk_kernel<64, true, 2, 1, true>)
+                          : static_cast<KernelFn>(vsk_kernel<64, false, 2, 1, true>);
+      case 128: return fp8 ? static_cast<KernelFn>(vsk_kernel<128, true, 2, 1, true>)
+                           : static_cast<KernelFn>(vsk_kernel<128, false, 2, 1, true>);
+      default: return nullptr;
+    }
+  }
   switch (D) {
     case 64: return fp8 ? static_cast<KernelFn>(vsk_kernel<64, true, 1, 1, true>)
                         : static_cast<KernelFn>(vsk_kernel<64, false, 1, 1, true>);
@@ -2072,7 +2083,8 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   const bool use_sl = !use_tc && !use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan pl;
   if ((use_tc || use_cs) ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
-                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, use_sl ? 1 : 0))
+                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
+                                      use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0))
     return 0;
   StreamPlan sp{};
   if (use_cs && !make_cs_stream_plan(pl, D, fp8, sp)) return 0;
@@ -2108,7 +2120,7 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
     smem = sp.smem;
     per_sm = sp.per_sm;
   } else if (use_sl) {
-    fn = pick_so_kernel(static_cast<int>(D), fp8);
+    fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW);
     fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
     if (!fn || !fn_comb || !prepare_kernel(fn) || !prepare_kernel(fn_comb))
       return fail("stream-only kernels for head_dim %lld unavailable", D);

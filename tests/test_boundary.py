@@ -247,11 +247,11 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(16, 16, 2, 256, 4, 524304) == 1                    # one token past it per sequence
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 1                # the long batch
         assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: no column split
-        # head_dim 64 / 128: stream + combine from 2,048 token-heads up to 2^20 (R > 16) or 2^23 (R <= 16)
+        # head_dim 64 / 128: stream + combine from 2,048 token-heads up to 2^22 (R > 16) or 2^23 (R <= 16)
         assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
         assert f(2, 16, 2, 128, 4, 1024) == 2                       # exactly 2,048 token-heads
-        assert f(16, 16, 2, 128, 4, 524288) == 2                    # R = 32, 2^20
-        assert f(16, 16, 2, 128, 4, 524304) == 1
+        assert f(16, 16, 2, 128, 4, 2097152) == 2                   # R = 32, 2^22
+        assert f(16, 16, 2, 128, 4, 2097168) == 1
         assert f(16, 32, 8, 128, 4, 1048576) == 2                   # R = 16, 2^23
         assert f(16, 32, 8, 128, 4, 1048592) == 1
         assert f(64, 32, 8, 128, 4, 64 * 20480) == 1                # the serving batch: one launch

@@ -94,6 +94,8 @@ TC = [
       seed=707),                                                                          # one KV head, R = 32
     S("tc_int32_idx", (700, 64, 1), 4, 16, 2, 256, 256, perm=True, idx_dtype="int32", seed=708),
     S("tc_bf16_scales", (1024, 2048), 3, 16, 2, 256, 256, k_scale=0.5, v_scale=0.25, seed=709),
+    # 70,000 prefix tokens: at head_dim 64 / 128 warps take two 16-row tiles
+    S("tc_two_tiles", (40000, 30000), 4, 16, 2, 256, 256, perm=True, seed=770),
     # more sequences than a block has threads (the combine kernel's length scan loops)
     S("tc_300_short", tuple(int(x) for x in np.random.default_rng(761).integers(0, 41, 300)), 4, 16, 2, 256, 256,
       perm=True, seed=761),
@@ -252,6 +254,23 @@ def test_form_split_count_independence(vsk, num_ctas, min_tok):
         o = run_gpu(vsk, p)
     finally:
         vsk.set_tuning(0, 0)
+    check(o, oracle_o(p))
+    assert vsk.read_error_flags() == 0
+
+
+@pytest.mark.parametrize("pool", ["bf16", "e4m3"])
+def test_form_two_tiles_per_warp(vsk, pool):
+    """Warps with two 16-row tiles (forced; at head_dim 64 / 128 the stream-only
+    kernel takes them from 2^18 prefix tokens): no effect on the head_dim 256
+    forms."""
+    spec = S(f"tc_two_tiles_forced_{pool}", (9000, 0, 4097, 700), 4, 16, 2, 256, 256, pool=pool, perm=True,
+             k_scale=0.5 if pool == "e4m3" else 1.0, v_scale=0.75, seed=771)
+    p = gpu_problem(spec)
+    vsk.set_tuning_tiles(2)
+    try:
+        o = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning_tiles(0)
     check(o, oracle_o(p))
     assert vsk.read_error_flags() == 0
 
