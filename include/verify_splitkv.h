@@ -18,8 +18,10 @@
  * causal attention over the drafts alone.
  *
  * Threading and streams: every entry point may be called from any host
- * thread.  verify_splitkv_fwd enqueues one kernel on the given stream and
- * returns without synchronising and without reading device memory.
+ * thread.  verify_splitkv_fwd enqueues one kernel on the given stream (two
+ * for the small and mid-size shapes served by a prefix stream and a combine
+ * kernel; vsk_launches_per_call tells which) and returns without
+ * synchronising and without reading device memory.
  *
  * Memory: all tensor pointers are DEVICE pointers owned by the caller.  The
  * library never frees or retains them past the call.
@@ -298,13 +300,6 @@ void vsk_set_tuning_tc(int mode);
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
 
-/* Kernel launches a call of these static shapes makes on its stream under the
- * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
- * then the combine kernel); 0 for shapes no entry point accepts.
- * `prefix_tokens` is what the entry point sees: the length of kv_indices for
- * the flat entry points, batch x block-table columns x page_size for the paged
- * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch
- * counts. */
 /* Tuning switch, for A/B runs and tests, over head_dim 64 and 128 calls with at
  * most 32 draft rows per sequence: the prefix is streamed by a stream-only
  * instance of the mma.sync kernel and the per-piece partials are folded, the
@@ -313,11 +308,17 @@ void vsk_set_tuning_colsplit(int mode);
  * (the default) takes that form when the call's prefix tokens times h_kv are
  * at least 2,048 and at most 4,194,304 (8,388,608 when (h_q / h_kv) *
  * max_len_extend <= 16), where it measured faster on GB300; mode 2 always
- * takes it; mode 0 never does.  All forms
- * compute the same result up to rounding order.  Process-wide; not
- * thread-safe. */
+ * takes it; mode 0 never does.  All forms compute the same result up to
+ * rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_split_launch(int mode);
 
+/* Kernel launches a call of these static shapes makes on its stream under the
+ * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
+ * then the combine kernel); 0 for shapes no entry point accepts.
+ * `prefix_tokens` is what the entry point sees: the length of kv_indices for
+ * the flat entry points, batch x block-table columns x page_size for the paged
+ * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch
+ * counts. */
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens);
 
