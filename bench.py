@@ -330,6 +330,36 @@ def cpu_baseline(prob, target_s: float) -> dict:
                       f"sequences' algorithmic bytes"}
 
 
+def oracle_config_times(min_seconds: float = 0.25) -> list:
+    """The oracle as it stands on the four small configurations (tiny, head_dim
+    256, the GQA / draft-length sweep, the e4m3 pool), whole problems on the
+    host: one thread, and all cores.  Each figure is the mean over repeats
+    filling at least min_seconds.  A reported baseline, not a target."""
+    import oracle
+
+    specs = [workloads.TINY, workloads.D256] + workloads.gqa_sweep() + [workloads.FP8]
+    cores = oracle.max_threads(0)
+    rows = []
+    for spec in specs:
+        prob = workloads.make_problem(spec, "cpu")
+        arrays = workloads.to_oracle_arrays(prob)
+        nbytes = workloads.algorithmic_bytes(prob)
+        row = {"config": spec.name, "bytes_per_call": nbytes}
+        for label, nt in (("1thread", 1), ("all_cores", 0)):
+            oracle.verify_forward(arrays, nthreads=nt)
+            n, t0 = 0, time.perf_counter()
+            while True:
+                oracle.verify_forward(arrays, nthreads=nt)
+                n += 1
+                dt = time.perf_counter() - t0
+                if dt >= min_seconds:
+                    break
+            row[f"us_per_call_{label}"] = round(dt / n * 1e6, 1)
+            row[f"gbs_{label}"] = round(nbytes / (dt / n) / 1e9, 4)
+        rows.append(row)
+    return [{"cores_all": cores}] + rows
+
+
 # ----------------------------------------------------------------------------- our arm
 def _call(vsk, prob, o, ws):
     if prob.get("block_table") is not None:
@@ -469,6 +499,7 @@ def run_ours(args, dist: Dist) -> dict:
                        "steps": args.e2e_steps, "statistic": "median of the timed steps after 3 warm-up steps"}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+        line["cpu_baseline"]["small_configs"] = oracle_config_times()
     return line
 
 

@@ -96,18 +96,22 @@ int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
  *   k_scale, v_scale  dequantisation multipliers of the prefix pool (1.0 for
  *               a bf16 pool); they do not apply to k_extend / v_extend.
  *   sm_scale    softmax scale; a value <= 0 or NaN selects 1/sqrt(D).
- *   workspace   device scratch of workspace_bytes bytes, zero-filled before
- *               its first use (cudaMemset or vsk_workspace_init) and then
- *               reused unchanged: every call leaves its counters (tickets,
- *               kept in the last 64 KiB of the buffer, or more for very large
- *               batches) at zero, so one buffer serves calls of any shapes
- *               that fit it.  The needed size is at most
+ *   workspace   device scratch of workspace_bytes bytes, 256-byte aligned,
+ *               zero-filled before its first use (cudaMemset or
+ *               vsk_workspace_init) and then reused unchanged.  The call's
+ *               counters (tickets) sit at the END of the buffer: the last
+ *               64 KiB, which every call leaves at zero, or for very large
+ *               batches (more than 16,384 tickets) a larger region, whose
+ *               part beyond those 64 KiB the call clears on `stream` before
+ *               its kernel (one cudaMemsetAsync).  So one buffer serves calls
+ *               of any shapes that fit it.  The needed size is at most
  *               vsk_workspace_size(max_bs, ...) for any B <= max_bs on the
- *               same device.  Concurrent calls (on
- *               different streams) must not share one workspace.
+ *               same device.
  *               workspace == NULL selects a library-owned per-device buffer
  *               that grows on demand; growth allocates and synchronises the
  *               device, so make the first such call outside graph capture.
+ *               Calls whose kernels may overlap on the GPU (different
+ *               streams) must each have their own workspace.
  * Device-side checks: kv_indices values outside [0, pool) and inconsistent
  * indptr entries are never dereferenced; they set a bit in the workspace
  * error word (see vsk_read_error_flags) and the affected rows are computed
@@ -239,8 +243,10 @@ size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q,
 int vsk_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* Synchronises `stream`, then copies the device error word of `workspace`
- * (NULL: the library-owned workspace of the current device) into *flags and
- * clears it.  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
+ * into *flags and clears it.  workspace == NULL selects the library-owned
+ * workspace of the current device, workspace == VSK_NOALLOC_SCRATCH the
+ * built-in scratch of verify_splitkv_fwd_noalloc on the current device (its
+ * word holds the flags of the most recent such call there).  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
  * not non-decreasing or beyond kv_indices; 4 = qo_indptr inconsistent with
  * l_ext; 8 = a pipeline wait that gave up after one second (only the
  * tensor-memory form of the stream, selected by vsk_set_tuning_tc(1), has
@@ -326,6 +332,11 @@ int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
  * verify_splitkv_fwd_noalloc (32 MiB). */
 #define VSK_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
 
+/* Passed as the `workspace` argument of vsk_read_error_flags: selects the
+ * built-in scratch of verify_splitkv_fwd_noalloc (a selector, never
+ * dereferenced). */
+#define VSK_NOALLOC_SCRATCH ((void*)1)
+
 /* verify_splitkv_fwd for callers that must not allocate device memory.  The
  * source pages have no counterpart: it is a deployment convenience of this
  * library.  Some callers cannot call cudaMalloc: serving engines that give
@@ -339,9 +350,12 @@ int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
  *     stream capture on that device.
- *   - Each call first clears the array's error word and per-segment tickets
- *     on `stream` (cudaMemsetAsync), then enqueues the kernel; the error word
- *     is therefore not reported through vsk_read_error_flags.
+ *   - The call plans exactly as verify_splitkv_fwd does (the same form: one
+ *     launch, or a prefix stream then the combine kernel) and checks that
+ *     plan's scratch against the array.  It then clears the array's error
+ *     word and its ticket region on `stream` (cudaMemsetAsync) and enqueues
+ *     the kernels.  vsk_read_error_flags(VSK_NOALLOC_SCRATCH, ...) reads
+ *     (and clears) the error word of the most recent call on the device.
  *   - Every call shares the one array: calls whose kernels may overlap on the
  *     GPU (different streams, or different host threads) race and corrupt
  *     each other's results.  Serialise them on one stream.

@@ -284,7 +284,8 @@ static void one_head(const orc_problem* p, int64_t b, int64_t h, double* out,
 /* Output rows for sequences [b0, b1) and query heads [h0, h1).
    out (and the optional debug arrays) are dense [n_rows, h_q, dv] / [n_rows,
    h_q]; rows and heads outside the requested ranges are left untouched.
-   nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad ranges.  */
+   nthreads <= 0 uses every processor (whatever an earlier call asked for).
+   Returns 0, or -1 on bad ranges.  */
 int orc_verify_forward(const orc_problem* p, int64_t b0, int64_t b1, int64_t h0, int64_t h1,
                        double* out, double* o_prefix, double* lse_prefix, double* o_draft,
                        double* lse_draft, int nthreads) {
@@ -294,7 +295,7 @@ int orc_verify_forward(const orc_problem* p, int64_t b0, int64_t b1, int64_t h0,
   const int64_t nb = b1 - b0, nh = h1 - h0;
   const int64_t n_work = nb * nh;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  omp_set_num_threads(nthreads > 0 ? nthreads : omp_get_num_procs());
 #pragma omp parallel for schedule(dynamic, 1)
 #endif
   for (int64_t w = 0; w < n_work; ++w) {
@@ -308,7 +309,7 @@ int orc_verify_forward(const orc_problem* p, int64_t b0, int64_t b1, int64_t h0,
 /* Threads an OpenMP parallel region would use (1 without OpenMP). */
 int orc_max_threads(int nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  omp_set_num_threads(nthreads > 0 ? nthreads : omp_get_num_procs());
   return omp_get_max_threads();
 #else
   (void)nthreads;

@@ -7,8 +7,11 @@ library.  Every step of the computation runs in the library's kernel.
 ``can_handle`` and ``verify_splitkv_fwd`` keep the positional signature of the
 sglang "verify_splitkv.py" page (``can_handle``, ``verify_splitkv_fwd``), so a
 caller of that module can switch by changing the import.  The workspace cache
-mirrors the page's ``_VK_CACHE``: one zero-initialised buffer per device, sized
-by ``max_bs`` and grown only, so its address stays fixed across batch sizes.
+mirrors the page's ``_VK_CACHE``: one zero-initialised buffer per (device,
+stream), sized by ``max_bs`` and grown only, so its address stays fixed across
+batch sizes.  Calls on different streams get different buffers, so they may
+overlap on the GPU; calls on one stream are ordered by the stream and share its
+buffer.
 """
 from __future__ import annotations
 
@@ -81,9 +84,21 @@ def workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> int:
     return int(_native.lib().vsk_workspace_size(max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext))
 
 
-def get_workspace(device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> torch.Tensor:
-    """Zero-filled per-device workspace, grown (never shrunk) to fit max_bs."""
+def _stream_key(device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def get_workspace(device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext, stream=None) -> torch.Tensor:
+    """Zero-filled workspace of ``stream`` (default: the device's current
+    stream) on ``device``, grown (never shrunk) to fit max_bs.  One buffer per
+    (device, stream): a buffer is never shared by calls that may overlap on the
+    GPU.  Growing allocates a new buffer; the old one is released by torch's
+    caching allocator on the current stream, after the calls queued on it."""
     device = torch.device(device)
+    if device.index is None:
+        device = torch.device(device.type, torch.cuda.current_device())
     key = (device, int(max_bs), int(h_q), int(h_kv), int(head_dim), int(v_head_dim), int(l_ext))
     need = _WS_SIZE.get(key)
     if need is None:
@@ -92,11 +107,12 @@ def get_workspace(device, max_bs, h_q, h_kv, head_dim, v_head_dim, l_ext) -> tor
         _WS_SIZE[key] = need
     if need == 0:
         raise RuntimeError("workspace size query failed: " + _native.last_error())
+    wkey = (device, _stream_key(device, stream))
     with _WS_LOCK:
-        ws = _WS.get(device)
+        ws = _WS.get(wkey)
         if ws is None or ws.numel() < need:
             ws = torch.zeros(need, dtype=torch.uint8, device=device)
-            _WS[device] = ws
+            _WS[wkey] = ws
     return ws
 
 
@@ -136,12 +152,12 @@ def verify_splitkv_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffe
     if custom_mask is not None and (not skip_prefix_custom_mask or mask_indptr is None):
         return False  # the prefix part of a tree mask is not applied by this kernel
     bs = qo_indptr.shape[0] - 1
+    if stream is None:
+        stream = torch.cuda.current_stream(q_extend.device)
     if workspace is None:
         mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
         workspace = get_workspace(q_extend.device, mb, q_extend.shape[1], k_extend.shape[1],
-                                  q_extend.shape[2], v_extend.shape[2], mle)
-    if stream is None:
-        stream = torch.cuda.current_stream(q_extend.device)
+                                  q_extend.shape[2], v_extend.shape[2], mle, stream)
     sm = 0.0 if sm_scale is None else float(sm_scale)
     if custom_mask is not None:
         cm = custom_mask if custom_mask.dtype == torch.uint8 else custom_mask.view(torch.uint8)
@@ -177,11 +193,12 @@ def verify_splitkv_paged_fwd(q, o, k_cache, v_cache, block_table, seq_lens, page
     raises ValueError when the library rejects the arguments."""
     bs = seq_lens.shape[0]
     mle = int(max_len_extend)
-    if workspace is None:
-        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
-        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle,
+                                  stream)
     sm = 0.0 if sm_scale is None else float(sm_scale)
     ok = _native.lib().verify_splitkv_paged_fwd(
         _ref(q), _ref(o), _ref(k_cache), _ref(v_cache), _ref(block_table), _ref(seq_lens), int(page_size), mle,
@@ -200,12 +217,12 @@ def verify_splitkv_write_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v
     when the library rejects the arguments."""
     bs = qo_indptr.shape[0] - 1
     mle = int(max_len_extend)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_extend.device)
     if workspace is None:
         mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
         workspace = get_workspace(q_extend.device, mb, q_extend.shape[1], k_extend.shape[1], q_extend.shape[2],
-                                  v_extend.shape[2], mle)
-    if stream is None:
-        stream = torch.cuda.current_stream(q_extend.device)
+                                  v_extend.shape[2], mle, stream)
     sm = 0.0 if sm_scale is None else float(sm_scale)
     ok = _native.lib().verify_splitkv_write_fwd(
         _ref(q_extend), _ref(k_extend), _ref(v_extend), _ref(o_extend), _ref(k_buffer), _ref(v_buffer),
@@ -224,11 +241,12 @@ def verify_splitkv_paged_write_fwd(q, k_new, v_new, o, k_cache, v_cache, block_t
     the same launch; the attention uses the stored values."""
     bs = seq_lens.shape[0]
     mle = int(max_len_extend)
-    if workspace is None:
-        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
-        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        mb = bs if (max_bs is None or max_bs < bs) else int(max_bs)
+        workspace = get_workspace(q.device, mb, q.shape[1], k_cache.shape[1], q.shape[2], v_cache.shape[2], mle,
+                                  stream)
     sm = 0.0 if sm_scale is None else float(sm_scale)
     ok = _native.lib().verify_splitkv_paged_write_fwd(
         _ref(q), _ref(k_new), _ref(v_new), _ref(o), _ref(k_cache), _ref(v_cache), _ref(block_table), _ref(seq_lens),
@@ -239,13 +257,15 @@ def verify_splitkv_paged_write_fwd(q, k_new, v_new, o, k_cache, v_cache, block_t
 
 
 def read_error_flags(workspace=None, stream=None) -> int:
-    """Device error word of a workspace (synchronises; for tests/debugging)."""
-    if workspace is None:
-        with _WS_LOCK:
-            ws = next(iter(_WS.values()), None) if _WS else None
-        workspace = ws
+    """Device error word of a workspace (synchronises; for tests/debugging).
+    Default: the cached workspace of ``stream`` (the current stream) on the
+    current device."""
     if stream is None:
         stream = torch.cuda.current_stream()
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        with _WS_LOCK:
+            workspace = _WS.get((dev, int(stream.cuda_stream)))
     flags = ctypes.c_uint32(0)
     ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     if not _native.lib().vsk_read_error_flags(ptr, ctypes.c_void_p(stream.cuda_stream), ctypes.byref(flags)):

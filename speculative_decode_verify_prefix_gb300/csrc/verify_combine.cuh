@@ -4,8 +4,8 @@
 // (o, log-sum-exp) partial per CTA piece of a sequence's prefix and merges
 // them with the log-sum-exp rule; the verify step then continues the same
 // softmax over the causal draft-draft block (verify_splitkv.py page,
-// `_verify_prefix_stage1` / `_verify_merge_with_extend`: the prefix partials
-// are merged with the extend block's scores).
+// `_verify_combine_stage2`: the prefix splits are merged by log-sum-exp, then
+// merged again with the causal draft-draft block's scores).
 //
 // When this kernel starts, the stream launch before it on the same stream has
 // written every piece's partial, so no ticket or arrival order is needed: one

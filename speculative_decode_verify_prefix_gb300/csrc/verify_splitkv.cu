@@ -1943,6 +1943,9 @@ void* internal_workspace(int dev, size_t need, cudaStream_t stream, size_t* byte
   return p;
 }
 
+// device address of the allocation-free entry point's built-in scratch
+void* static_scratch(int dev);
+
 }  // namespace vsk
 
 using namespace vsk;
@@ -2020,11 +2023,16 @@ int vsk_read_error_flags(void* workspace, void* stream, uint32_t* flags) {
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail("cudaStreamSynchronize: %s", cudaGetErrorString(e));
   void* ws = workspace;
-  if (!ws) {
+  if (!ws || ws == VSK_NOALLOC_SCRATCH) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail("no CUDA device");
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (static_cast<int>(g_ws.size()) > dev) ws = g_ws[dev].ptr;
+    if (ws == VSK_NOALLOC_SCRATCH) {
+      ws = static_scratch(dev);
+      if (!ws) return 0;
+    } else {
+      std::lock_guard<std::mutex> lk(g_ws_mu);
+      if (static_cast<int>(g_ws.size()) > dev) ws = g_ws[dev].ptr;
+    }
   }
   if (!ws) {
     *flags = 0;
@@ -2074,79 +2082,113 @@ const char* vsk_version(void) { return VSK_VERSION; }
 }  // extern "C"
 
 namespace vsk {
-// Plans the CTA shape for these sizes, sizes and checks the workspace, fills
-// the plan-dependent fields of p and launches the kernel.
-static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
-                            void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
-  const bool use_tc = tc_eligible(h_q, h_kv, D, L);
-  const bool use_cs = !use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
-  const bool use_sl = !use_tc && !use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
-  Plan pl;
-  if ((use_tc || use_cs) ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
-                         : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
-                                      use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0))
-    return 0;
+// Everything the launches of one call need, decided from static shapes only
+// (no device read): the form (one launch, or a stream then the combine
+// kernel), the CTA shape, the kernels, the grid, the share floor and the
+// workspace layout.  Every entry point plans a call with plan_call and
+// enqueues it with enqueue_call, so the workspace a caller (or the built-in
+// scratch of the allocation-free entry point) is checked against is the one
+// the kernels use.
+struct CallPlan {
+  bool use_tc = false, use_cs = false, use_sl = false;
+  Plan pl{};
   StreamPlan sp{};
-  if (use_cs && !make_cs_stream_plan(pl, D, fp8, sp)) return 0;
+  KernelFn fn = nullptr, fn_comb = nullptr;
+  int threads = 0;
+  size_t smem = 0;
+  long long n_cta = 0, n_comb = 0, w_min = 0;
+  WsLayout wl{};
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  int D = 0;
+};
+
+static int plan_call(long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
+                     long long mean_len, CallPlan& cp) {
+  cp.D = static_cast<int>(D);
+  cp.use_tc = tc_eligible(h_q, h_kv, D, L);
+  cp.use_cs = !cp.use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_sl = !cp.use_tc && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
+  Plan& pl = cp.pl;
+  if ((cp.use_tc || cp.use_cs)
+          ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
+          : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
+                       cp.use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0))
+    return 0;
+  if (cp.use_cs && !make_cs_stream_plan(pl, D, fp8, cp.sp)) return 0;
+  cudaError_t e = cudaGetDevice(&cp.dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
-  const int sms = device_sms(dev);
-  if (sms <= 0) return fail("cannot query the SM count of device %d", dev);
+  const int sms = device_sms(cp.dev);
+  if (sms <= 0) return fail("cannot query the SM count of device %d", cp.dev);
   // the streaming kernel (the whole call on the one-launch path; the prefix
   // stream on the two-launch paths, followed by the combine kernel)
-  KernelFn fn = nullptr, fn_comb = nullptr;
-  int threads = pl.threads;
-  size_t smem = pl.smem;
+  cp.threads = pl.threads;
+  cp.smem = pl.smem;
   int per_sm = pl.ctas_per_sm;
-  if (use_tc) {
+  if (cp.use_tc) {
     const int rm = 16 * pl.MT;
-    fn = pick_tc_kernel(fp8, rm);
-    fn_comb = pick_combine_kernel(256, fp8);
-    if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("tensor-memory kernels unavailable");
+    cp.fn = pick_tc_kernel(fp8, rm);
+    cp.fn_comb = pick_combine_kernel(256, fp8);
+    if (!prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("tensor-memory kernels unavailable");
     int ne = 0;
     if (fp8)
-      rm == 16 ? tc_smem<true, 16>(ne, smem) : tc_smem<true, 32>(ne, smem);
+      rm == 16 ? tc_smem<true, 16>(ne, cp.smem) : tc_smem<true, 32>(ne, cp.smem);
     else
-      rm == 16 ? tc_smem<false, 16>(ne, smem) : tc_smem<false, 32>(ne, smem);
+      rm == 16 ? tc_smem<false, 16>(ne, cp.smem) : tc_smem<false, 32>(ne, cp.smem);
     if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
     pl.nst = ne;
-    threads = tc::kThreads;
-  } else if (use_cs) {
-    fn = pick_cs_kernel(fp8);
-    fn_comb = pick_combine_kernel(256, fp8);
-    if (!prepare_kernel(fn) || !prepare_kernel(fn_comb)) return fail("column-split kernels unavailable");
-    threads = sp.threads;
-    smem = sp.smem;
-    per_sm = sp.per_sm;
-  } else if (use_sl) {
-    fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW);
-    fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
-    if (!fn || !fn_comb || !prepare_kernel(fn) || !prepare_kernel(fn_comb))
+    cp.threads = tc::kThreads;
+  } else if (cp.use_cs) {
+    cp.fn = pick_cs_kernel(fp8);
+    cp.fn_comb = pick_combine_kernel(256, fp8);
+    if (!prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("column-split kernels unavailable");
+    cp.threads = cp.sp.threads;
+    cp.smem = cp.sp.smem;
+    per_sm = cp.sp.per_sm;
+  } else if (cp.use_sl) {
+    cp.fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW);
+    cp.fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
+    if (!cp.fn || !cp.fn_comb || !prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb))
       return fail("stream-only kernels for head_dim %lld unavailable", D);
   } else {
-    fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
-    if (!fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
+    cp.fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
+    if (!cp.fn || !prepare_kernel(cp.fn)) return fail("kernel for head_dim %lld unavailable", D);
   }
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), threads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(cp.fn), cp.threads, cp.smem);
   if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
   per_sm = std::min(occ, per_sm);
-  const long long n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
-  const WsLayout wl = ws_layout(n_cta, B, pl, D);
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  size_t ws_bytes = workspace_bytes;
-  if (!ws) {
-    ws = static_cast<unsigned char*>(internal_workspace(dev, wl.total, st, &ws_bytes));
-    if (!ws) return fail("cannot allocate a %zu-byte workspace", wl.total);
-  } else if (workspace_bytes < wl.total) {
-    return fail("workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes, wl.total);
-  } else if (!aligned(ws, 256)) {
-    return fail("workspace must be 256-byte aligned");
+  cp.n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
+  cp.wl = ws_layout(cp.n_cta, B, pl, D);
+  if (cp.fn_comb) {
+    // one combine CTA per (segment, 16-row tile, 32-column slice)
+    cp.n_comb = B * pl.n_hg * pl.HC * pl.MT * (D / cmb::kCols);
+    if (cp.n_comb > 0x7FFFFFFFLL) return fail("combine grid of %lld CTAs too large", cp.n_comb);
   }
+  // Smallest CTA share, from static shapes only (no device read, graph
+  // safe): at least 64 tokens and, for small batches where the shares get
+  // short, at least the mean prefix / 24 in whole stages, which bounds the
+  // pieces a segment's finisher merges.  The two-launch forms (partials
+  // folded by the combine launch) do best with every CTA busy: mean prefix / 48.
+  if (g_min_tokens > 0) {
+    cp.w_min = g_min_tokens;
+  } else {
+    const long long per = (cp.use_cs || cp.use_sl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
+    const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
+    cp.w_min = std::max(kDefaultMinTokens, wp);
+  }
+  return 1;
+}
 
+// Fills the plan-dependent fields of p and enqueues the call's launches on
+// st, with ws (ws_bytes bytes, 256-byte aligned, at least cp.wl.total) as the
+// workspace.  Tickets sit in the last cp.wl.cnt_bytes of the buffer; the
+// one-launch kernel leaves every ticket it draws at zero, so the last
+// kTicketBytes of a buffer are zero between calls, but a call whose ticket
+// region is larger (very large batches) first clears the part beyond them,
+// where an earlier call may have left partials.
+static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L, unsigned char* ws, size_t ws_bytes,
+                        cudaStream_t st) {
+  const Plan& pl = cp.pl;
   p.B = static_cast<int>(B);
   p.L = static_cast<int>(L);
   p.gq = pl.gq;
@@ -2160,54 +2202,75 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
   p.head_bytes = pl.head_bytes;
   p.misc_off = pl.misc_off;
   p.misc_bytes = pl.misc_bytes;
-  // Smallest CTA share, from static shapes only (no device read, graph
-  // safe): at least 64 tokens and, for small batches where the shares get
-  // short, at least the mean prefix / 24 in whole stages, which bounds the
-  // pieces a segment's finisher merges.  The two-launch forms (partials
-  // folded by the combine launch) do best with every CTA busy: mean prefix / 48.
-  if (g_min_tokens > 0) {
-    p.w_min = g_min_tokens;
-  } else {
-    const long long per = (use_cs || use_sl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
-    const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
-    p.w_min = std::max(kDefaultMinTokens, wp);
-  }
+  p.w_min = cp.w_min;
+  const size_t cnt_off = (ws_bytes & ~static_cast<size_t>(255)) - cp.wl.cnt_bytes;
   p.err = reinterpret_cast<unsigned*>(ws);
-  p.cnt = reinterpret_cast<int*>(ws + ((ws_bytes & ~static_cast<size_t>(255)) - wl.cnt_bytes));
+  p.cnt = reinterpret_cast<int*>(ws + cnt_off);
   p.nseg = B * pl.n_hg;
-  p.plse = reinterpret_cast<float*>(ws + wl.lse_off);
-  p.po = reinterpret_cast<float*>(ws + wl.o_off);
-  p.n_stream = static_cast<int>(n_cta);
-  void* args[] = {&p};
-  if (use_cs) {
+  p.plse = reinterpret_cast<float*>(ws + cp.wl.lse_off);
+  p.po = reinterpret_cast<float*>(ws + cp.wl.o_off);
+  p.n_stream = static_cast<int>(cp.n_cta);
+  if (cp.use_cs) {
     p.nwc = 2 * pl.MT;
-    p.nst = sp.nst;
-    p.ring_off = sp.ring_off;
-    p.head_bytes = sp.head_bytes;
-    p.misc_off = sp.misc_off;
-    p.misc_bytes = sp.misc_bytes;
+    p.nst = cp.sp.nst;
+    p.ring_off = cp.sp.ring_off;
+    p.head_bytes = cp.sp.head_bytes;
+    p.misc_off = cp.sp.misc_off;
+    p.misc_bytes = cp.sp.misc_bytes;
   }
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(n_cta)), dim3(threads), args,
-                       smem, st);
+  cudaError_t e;
+  if (!cp.fn_comb && cp.wl.cnt_bytes > static_cast<size_t>(kTicketBytes)) {
+    e = cudaMemsetAsync(ws + cnt_off, 0, cp.wl.cnt_bytes - kTicketBytes, st);
+    if (e != cudaSuccess) return fail("cudaMemsetAsync of the ticket region: %s", cudaGetErrorString(e));
+  }
+  void* args[] = {&p};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(cp.fn), dim3(static_cast<unsigned>(cp.n_cta)), dim3(cp.threads),
+                       args, cp.smem, st);
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
-  if (fn_comb) {
-    // one CTA per (segment, 16-row tile, 32-column slice); the share floor and
-    // n_stream let it find the pieces the stream launch wrote
-    const long long n_comb = B * pl.n_hg * pl.HC * pl.MT * (D / cmb::kCols);
-    if (n_comb > 0x7FFFFFFFLL) return fail("combine grid of %lld CTAs too large", n_comb);
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn_comb), dim3(static_cast<unsigned>(n_comb)),
-                         dim3(cmb::kThreads), args, combine_smem(static_cast<int>(D)), st);
+  if (cp.fn_comb) {
+    // the share floor and n_stream let the combine kernel find the pieces the
+    // stream launch wrote
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(cp.fn_comb), dim3(static_cast<unsigned>(cp.n_comb)),
+                         dim3(cmb::kThreads), args, combine_smem(cp.D), st);
     if (e != cudaSuccess) return fail("combine kernel launch failed: %s", cudaGetErrorString(e));
   }
   return 1;
 }
 
-// Shared body of the entry points; cm / mi select tree verify (both null: causal drafts).
-static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
-                      const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
-                      const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
-                      float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
-                      const vsk_tensor* mi, const vsk_tensor* ocl = nullptr) {
+// Plans the call, resolves the workspace (NULL: the library-owned per-device
+// buffer) and enqueues the launches.
+static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
+                            void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
+  CallPlan cp;
+  if (!plan_call(B, h_q, h_kv, D, L, fp8, mean_len, cp)) return 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  size_t ws_bytes = workspace_bytes;
+  if (!ws) {
+    ws = static_cast<unsigned char*>(internal_workspace(cp.dev, cp.wl.total, st, &ws_bytes));
+    if (!ws) return fail("cannot allocate a %zu-byte workspace", cp.wl.total);
+  } else if (workspace_bytes < cp.wl.total) {
+    return fail("workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes, cp.wl.total);
+  } else if (!aligned(ws, 256)) {
+    return fail("workspace must be 256-byte aligned");
+  }
+  return enqueue_call(p, cp, B, L, ws, ws_bytes, st);
+}
+
+// The checks and the parameter block shared by the flat entry points (causal,
+// tree, fused store, allocation-free); cm / mi select tree verify (both null:
+// causal drafts), ocl the fused store.  Returns the static shapes the plan
+// needs.
+struct CallShape {
+  long long B, h_q, h_kv, D, L, mean_len;
+  bool fp8;
+};
+
+static int prepare_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                          const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                          const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                          float sm_scale, const vsk_tensor* cm, const vsk_tensor* mi, const vsk_tensor* ocl, Params& p,
+                          CallShape& cs) {
   if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
   if (!check_3d(o, "o_extend")) return 0;
   if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
@@ -2217,7 +2280,6 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
     return fail("o_extend must be 4-byte aligned with even strides");
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return fail("k_scale and v_scale must be finite");
 
-  Params p;
   memset(&p, 0, sizeof p);
   p.q = static_cast<const __nv_bfloat16*>(q->data);
   p.q_s0 = q->stride[0];
@@ -2271,9 +2333,29 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
     p.kq = k_scale;
     p.vq = v_scale;
   }
-  const long long B = qo->shape[0] - 1;
-  return launch_with_plan(p, B, q->shape[1], ke->shape[1], D, max_len_extend, kb->dtype == VSK_DTYPE_FP8E4M3,
-                          workspace, workspace_bytes, stream, kvi->shape[0] / B);
+  cs.B = qo->shape[0] - 1;
+  cs.h_q = q->shape[1];
+  cs.h_kv = ke->shape[1];
+  cs.D = D;
+  cs.L = max_len_extend;
+  cs.fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
+  cs.mean_len = kvi->shape[0] / cs.B;
+  return 1;
+}
+
+// Shared body of the workspace entry points.
+static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const vsk_tensor* o,
+                      const vsk_tensor* kb, const vsk_tensor* vb, const vsk_tensor* qo, const vsk_tensor* kvp,
+                      const vsk_tensor* kvi, int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
+                      float sm_scale, void* workspace, size_t workspace_bytes, void* stream, const vsk_tensor* cm,
+                      const vsk_tensor* mi, const vsk_tensor* ocl = nullptr) {
+  Params p;
+  CallShape cs;
+  if (!prepare_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale, sm_scale, cm,
+                      mi, ocl, p, cs))
+    return 0;
+  return launch_with_plan(p, cs.B, cs.h_q, cs.h_kv, cs.D, cs.L, cs.fp8, workspace, workspace_bytes, stream,
+                          cs.mean_len);
 }
 
 bool check_2d(const vsk_tensor* t, const char* name) {
@@ -2476,14 +2558,13 @@ int verify_splitkv_tree_fwd(const vsk_tensor* q, const vsk_tensor* ke, const vsk
 static __device__ __align__(256) unsigned char g_vsk_static_scratch[VSK_NOALLOC_SCRATCH_BYTES];
 
 namespace vsk {
-namespace {
 
 std::mutex g_static_mu;
 std::vector<void*> g_static_addr;  // per device: device address of g_vsk_static_scratch
 
-// Device address of the scratch array on the current device.  The host-side
-// name is only a stand-in, so the address is asked from the runtime once per
-// device (with that device current) and cached.
+// Device address of the scratch array on device dev, which must be the
+// current device.  The host-side name is only a stand-in, so the address is
+// asked from the runtime once per device and cached.
 void* static_scratch(int dev) {
   std::lock_guard<std::mutex> lk(g_static_mu);
   if (static_cast<int>(g_static_addr.size()) <= dev) g_static_addr.resize(dev + 1, nullptr);
@@ -2499,7 +2580,6 @@ void* static_scratch(int dev) {
   return g_static_addr[dev];
 }
 
-}  // namespace
 }  // namespace vsk
 
 extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve,
@@ -2508,41 +2588,27 @@ extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor*
                                           int is_causal, int64_t max_len_extend, float k_scale, float v_scale,
                                           float sm_scale, void* stream) {
   g_err.clear();
-  if (!gate(q, ke, ve, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, -1, 0, 0.f, -1)) return 0;
-  if (!check_3d(o, "o_extend")) return 0;
-  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != q->shape[1] ||
-      o->shape[2] != ve->shape[2])
-    return fail("o_extend must be bf16 [B*l_ext, h_q, v_head_dim]");
-  const long long B = qo->shape[0] - 1;
-  const long long h_q = q->shape[1], h_kv = ke->shape[1], D = q->shape[2];
-  const bool fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
-  Plan pl;
-  if (!make_plan(h_q, h_kv, D, max_len_extend, fp8, pl, (kvi->shape[0] / B) * B, 0)) return 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
-  const int sms = device_sms(dev);
-  KernelFn fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
-  if (sms <= 0 || !fn || !prepare_kernel(fn)) return fail("kernel for head_dim %lld unavailable", D);
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), pl.threads, pl.smem);
-  if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
-  const long long n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * std::min(occ, pl.ctas_per_sm);
-  const size_t need = ws_layout(n_cta, B, pl, D).total;
-  if (need > static_cast<size_t>(VSK_NOALLOC_SCRATCH_BYTES))
+  Params p;
+  CallShape cs;
+  if (!prepare_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale, sm_scale,
+                      nullptr, nullptr, nullptr, p, cs))
+    return 0;
+  // the same plan (form, grid, workspace layout) verify_splitkv_fwd would use
+  CallPlan cp;
+  if (!plan_call(cs.B, cs.h_q, cs.h_kv, cs.D, cs.L, cs.fp8, cs.mean_len, cp)) return 0;
+  if (cp.wl.total > static_cast<size_t>(VSK_NOALLOC_SCRATCH_BYTES))
     return fail("this problem needs %zu bytes of scratch, more than the %d bytes built into the library for "
                 "verify_splitkv_fwd_noalloc; use verify_splitkv_fwd with a caller workspace",
-                need, VSK_NOALLOC_SCRATCH_BYTES);
-  unsigned char* scratch = static_cast<unsigned char*>(static_scratch(dev));
+                cp.wl.total, VSK_NOALLOC_SCRATCH_BYTES);
+  unsigned char* scratch = static_cast<unsigned char*>(static_scratch(cp.dev));
   if (!scratch) return 0;
   // The array keeps whatever the previous call left: zero the error word and
-  // the per-segment tickets before this call's kernel runs.
-  const WsLayout wl = ws_layout(n_cta, B, pl, D);
-  e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));  // the error word
-  if (e == cudaSuccess)  // the tickets, at the end of the array
-    e = cudaMemsetAsync(scratch + VSK_NOALLOC_SCRATCH_BYTES - wl.cnt_bytes, 0, wl.cnt_bytes,
-                        static_cast<cudaStream_t>(stream));
+  // this call's whole ticket span (at the end of the array) before its
+  // kernels run.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 256, st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(scratch + VSK_NOALLOC_SCRATCH_BYTES - cp.wl.cnt_bytes, 0, cp.wl.cnt_bytes, st);
   if (e != cudaSuccess) return fail("cudaMemsetAsync on the built-in scratch: %s", cudaGetErrorString(e));
-  return verify_splitkv_fwd(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale,
-                            sm_scale, scratch, VSK_NOALLOC_SCRATCH_BYTES, stream);
+  return enqueue_call(p, cp, cs.B, cs.L, scratch, VSK_NOALLOC_SCRATCH_BYTES, st);
 }

@@ -4,6 +4,15 @@ Tolerance: atol 2e-2, rtol 1e-2 on the bf16 output against the oracle's fp64
 value (the parity tolerance of the "test_verify_splitkv.py" page); integer
 index handling is checked bit-exactly (int32 vs int64 indices, pool-slot
 permutations, repeated calls).
+
+At long prefixes the outputs are small (a softmax-weighted mean of thousands
+of N(0, 1) rows: |o| of order 1/sqrt(n)), so the page's absolute tolerance
+alone would pass an output that is off by tens of percent.  The long-context
+cases therefore also bound the error by a fraction of the output's magnitude:
+max |err| <= SCALED * max |ref|.  The kernels' own error is bf16 rounding of
+the output (at most 2^-9 of |o|) and of the softmax weights, about 0.3 % of
+max |ref| at most, so SCALED = 1e-2 leaves room for rounding and none for a
+wrong result (a dropped piece, a wrong scale).
 """
 import numpy as np
 import pytest
@@ -15,6 +24,7 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 ATOL, RTOL = 2e-2, 1e-2
+SCALED = 1e-2  # max |err| <= SCALED * max |ref| on the long-context cases
 
 
 @pytest.fixture(scope="module")
@@ -46,7 +56,10 @@ def oracle_o(prob, **kw):
     return oracle.verify_forward(workloads.to_oracle_arrays(prob), **kw)["o"]
 
 
-def check(got, ref, atol=ATOL, rtol=RTOL, rows=None):
+def check(got, ref, atol=ATOL, rtol=RTOL, rows=None, scaled=None):
+    """The page's tolerance element by element and, with ``scaled``, also
+    max |err| <= scaled * max |ref| (the bound scaled to the output's
+    magnitude).  Returns the largest absolute error."""
     g = got.float().cpu().numpy().astype(np.float64)
     if rows is not None:
         g, ref = g[rows], ref[rows]
@@ -54,7 +67,32 @@ def check(got, ref, atol=ATOL, rtol=RTOL, rows=None):
     err = np.abs(g - ref)
     bad = err > atol + rtol * np.abs(ref)
     assert not bad.any(), f"{bad.sum()} elements out of tolerance; max abs err {err.max():.3e}"
+    if scaled is not None:
+        bound = scaled * float(np.abs(ref).max())
+        assert err.max() <= bound, f"max abs err {err.max():.3e} above {scaled:g} x max|ref| = {bound:.3e}"
     return float(err.max())
+
+
+def check_every_sequence(p, o, scaled=SCALED, planted_seq=None):
+    """Every sequence of a large batch (all heads, all draft rows) against the
+    oracle, one sequence at a time (its referenced pool rows gathered to the
+    host), each with the magnitude-scaled bound.  With ``planted_seq``, that
+    sequence's oracle output is also scaled by 1.1 (a mistake planted in the
+    oracle's result, on the CPU) and the check must reject it, which shows the
+    scaled bound sees a 10 % error the page's absolute tolerance lets through.
+    Returns the largest error relative to max |ref| over the batch."""
+    worst = 0.0
+    for b in range(len(p["prefix_lens"])):
+        sub, (s, e) = _subproblem(p, b)
+        ref = oracle_o(sub, nthreads=0)
+        err = check(o[s:e], ref, scaled=scaled)
+        worst = max(worst, err / float(np.abs(ref).max()))
+        if b == planted_seq:
+            planted = ref * 1.1
+            check(o[s:e], planted)  # the page's tolerance alone: passes
+            with pytest.raises(AssertionError):
+                check(o[s:e], planted, scaled=scaled)
+    return worst
 
 
 def gpu_problem(spec, **over):
@@ -72,19 +110,19 @@ def test_tiny(vsk):
 
 def test_head_dim_256(vsk):
     p = gpu_problem(workloads.D256)
-    check(run_gpu(vsk, p), oracle_o(p))
+    check(run_gpu(vsk, p), oracle_o(p), scaled=SCALED)
 
 
 @pytest.mark.parametrize("spec", workloads.gqa_sweep(), ids=lambda s: s.name)
 def test_gqa_extend_sweep(vsk, spec):
     p = gpu_problem(spec)
-    check(run_gpu(vsk, p), oracle_o(p))
+    check(run_gpu(vsk, p), oracle_o(p), scaled=SCALED)
 
 
 def test_fp8_pool_with_scales(vsk):
     p = gpu_problem(workloads.FP8)
     o, ref = run_gpu(vsk, p), oracle_o(p)
-    err = check(o, ref)
+    err = check(o, ref, scaled=SCALED)
     assert err < 2e-3  # fp8 decode is exact on both sides; outputs are ~v_scale/sqrt(n)
 
 
@@ -106,18 +144,17 @@ def _subproblem(prob, b):
     return sub, (s, e)
 
 
-def test_serving_scale_sampled(vsk):
-    """Full serving-scale batch in the benchmark's launch configuration; the
-    oracle checks three whole sequences (all heads, all draft rows)."""
+def test_serving_scale_every_sequence(vsk):
+    """Full serving-scale batch (64 sequences, prefixes U[8192, 32768]) in the
+    benchmark's launch configuration; the oracle checks every sequence (all
+    heads, all draft rows) with the page's tolerance and the magnitude-scaled
+    bound, and a 10 % error planted in the oracle's result is rejected."""
     p = gpu_problem(workloads.SERVING)
     o = run_gpu(vsk, p)
-    g = o.float()
-    assert torch.isfinite(g).all()
-    for b in (0, 31, 63):
-        sub, (s, e) = _subproblem(p, b)
-        ref = oracle_o(sub, nthreads=0)
-        check(o[s:e], ref)
+    assert torch.isfinite(o.float()).all()
     assert vsk.read_error_flags() == 0
+    worst = check_every_sequence(p, o, planted_seq=0)
+    assert worst < 5e-3, worst  # bf16 rounding only
     del p
     torch.cuda.empty_cache()
 
@@ -145,10 +182,13 @@ EDGE = [
 ]
 
 
+LONG_EDGE = {"rows128", "bf16_scales", "single_seq_long", "one_200k_prefix"}
+
+
 @pytest.mark.parametrize("spec", EDGE, ids=lambda s: s.name)
 def test_edge_cases(vsk, spec):
     p = gpu_problem(spec)
-    check(run_gpu(vsk, p), oracle_o(p))
+    check(run_gpu(vsk, p), oracle_o(p), scaled=SCALED if spec.name in LONG_EDGE else None)
     assert vsk.read_error_flags() == 0
 
 
@@ -586,6 +626,43 @@ def test_one_workspace_serves_calls_of_any_shape(vsk):
                 vsk.set_tuning(0, 0)
             assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (i, spec.name)
     assert vsk.read_error_flags(shared) == 0
+
+
+def test_large_ticket_region_on_a_reused_buffer(vsk):
+    """A one-launch call with more than 16,384 tickets (decode, l_ext = 1,
+    h_q / h_kv = 32 / 8, 9,000 short prefixes: two per segment plus one per
+    CTA) on a buffer whose bytes before its last 64 KiB are not zero, as an
+    earlier call's partials leave them: the part of the ticket region beyond
+    the last 64 KiB is cleared by the call itself.  Checked against the
+    oracle on two calls in a row, the first after a head_dim 256 call with a
+    large partial region on the same buffer."""
+    rng = np.random.default_rng(801)
+    spec = workloads.Spec("tickets_9000", tuple(int(x) for x in rng.integers(0, 9, 9000)), 1, 32, 8, 128, 128,
+                          perm=True, seed=801)
+    big = workloads.Spec("tickets_first", None, 4, 16, 2, 256, 256, perm=True, batch=48, len_range=(2000, 6000),
+                         seed=802)
+    p = gpu_problem(spec)
+    B = len(spec.prefix_lens)
+    need = vsk.workspace_size(B, 32, 8, 128, 128, 1)
+    assert need > 0
+    shared = torch.full((need + (1 << 20),), 0x5A, dtype=torch.uint8, device="cuda")
+    shared[:256] = 0        # the error word
+    shared[-65536:] = 0     # the tail every call leaves at zero
+    ref = oracle_o(p)
+    vsk.set_tuning_split_launch(0)  # the one-launch kernel: the form that draws tickets
+    vsk.set_tuning_colsplit(0)
+    try:
+        assert vsk.launches_per_call(B, 32, 8, 128, 1, p["kv_indices"].shape[0]) == 1
+        pb = gpu_problem(big)
+        ob = run_gpu(vsk, pb, workspace=shared)
+        for _ in range(2):
+            o = run_gpu(vsk, p, workspace=shared)
+            check(o, ref)
+        assert vsk.read_error_flags(shared) == 0
+    finally:
+        vsk.set_tuning_split_launch(1)
+        vsk.set_tuning_colsplit(1)
+    check(ob, oracle_o(pb), scaled=SCALED)
 
 
 TILES = [
