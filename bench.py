@@ -46,7 +46,7 @@ import workloads  # noqa: E402
 METRIC = "verify-attn KV GB/s (fraction of GB300 HBM peak) and µs/call, 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_DIR = os.path.join(ROOT, "speculative_decode_verify_prefix_gb300", "csrc")
-KERNEL_SRCS = ("verify_splitkv.cu", "verify_combine.cuh", "verify_tc.cuh")  # every kernel of a call
+KERNEL_SRCS = ("verify_kernel.cuh", "verify_combine.cuh", "verify_tc.cuh")  # every kernel of a call
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 

@@ -1,6 +1,6 @@
 """Split-KV verify attention for EAGLE target-verify (topk = 1) on GB300.
 
-The computation runs in the CUDA library built from ``csrc/verify_splitkv.cu``
+The computation runs in the CUDA library built from ``csrc/*.cu``
 (C ABI: ``include/verify_splitkv.h``); this package is its Python binding.
 """
 from .api import (as_vsk, can_handle, get_workspace, launches_per_call, read_error_flags, set_tuning,

@@ -1,8 +1,10 @@
 """Build and load the in-tree CUDA library (libverify_splitkv.so, sm_103a).
 
-The library is compiled from ``csrc/verify_splitkv.cu`` with nvcc into
-``_build/`` next to this file.  Loading never falls back to anything: if the
-library is missing or fails to load, callers get an exception.
+The library is compiled from ``csrc/*.cu`` with nvcc into ``_build/`` next to
+this file: every translation unit (the host side, and the kernels of each
+head_dim) in parallel, then linked into one shared library.  Loading never
+falls back to anything: if the library is missing or fails to load, callers
+get an exception.
 """
 from __future__ import annotations
 
@@ -13,11 +15,14 @@ import subprocess
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(_HERE, "csrc", "verify_splitkv.cu")
+CSRC = os.path.join(_HERE, "csrc")
+SRCS = sorted(os.path.join(CSRC, n) for n in os.listdir(CSRC) if n.endswith(".cu"))
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "verify_splitkv.h")
 BUILD_DIR = os.path.join(_HERE, "_build")
+OBJ_DIR = os.path.join(BUILD_DIR, f"obj_{platform.machine()}")
 LIB_PATH = os.path.join(BUILD_DIR, f"libverify_splitkv_{platform.machine()}.so")
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = [*NVCC_ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
 
 
 def nvcc_path() -> str:
@@ -28,19 +33,38 @@ def nvcc_path() -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the CUDA library for sm_103a (no-op when up to date)."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    deps = [SRC, HEADER] + [os.path.join(_HERE, "csrc", n) for n in os.listdir(os.path.join(_HERE, "csrc"))
-                            if n.endswith((".cu", ".cuh"))]
+    """Compile the CUDA library for sm_103a (no-op when up to date): each
+    translation unit in parallel, then one link.  ``verbose`` passes
+    ``-Xptxas=-v`` (registers, spills, shared memory per kernel)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    headers = [HEADER] + [os.path.join(CSRC, n) for n in os.listdir(CSRC) if n.endswith(".cuh")]
+    newest_header = max(os.path.getmtime(h) for h in headers)
     if not force and os.path.exists(LIB_PATH):
-        if os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps):
+        if os.path.getmtime(LIB_PATH) >= max(newest_header, *(os.path.getmtime(s) for s in SRCS)):
             return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-shared", SRC, "-o", tmp]
+    nvcc = nvcc_path()
+
+    def compile_one(src):
+        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(newest_header, os.path.getmtime(src)):
+            return obj, ""
+        tmp = obj + f".tmp{os.getpid()}"
+        cmd = [nvcc, *NVCC_FLAGS, *(["-Xptxas=-v"] if verbose else []), "-c", src, "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+        os.replace(tmp, obj)
+        return obj, r.stderr
+
+    with ThreadPoolExecutor(len(SRCS)) as ex:
+        results = list(ex.map(compile_one, SRCS))
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+        for _, log in results:
+            print(log, end="")
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run([nvcc, *NVCC_ARCH, "-shared", *[o for o, _ in results], "-o", tmp], check=True)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 
