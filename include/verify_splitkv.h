@@ -73,10 +73,11 @@ typedef struct vsk_tensor {
  *   sliding_window_size > 0, has_sinks != 0, logit_cap > 0 and
  *   xai_temperature_len > 0 are features this kernel does not implement:
  *   any of them makes the gate return 0.
- * Build limits: D == Dv in {64, 128, 256}; (h_q/h_kv) * l_ext <= 128
- * (<= 64 when D = 256); pool rows 16-byte aligned (data pointer and the
- * byte strides of both leading dimensions); q/k_extend/v_extend 4-byte aligned
- * with even strides.  On 0, vsk_last_error() names the first failed check. */
+ * Build limits: D and Dv in {64, 128, 256} (D != Dv is served by the
+ * one-launch kernel); (h_q/h_kv) * l_ext <= 128 (<= 64 when D or Dv is 256);
+ * pool rows 16-byte aligned (data pointer and the byte strides of both
+ * leading dimensions); q/k_extend/v_extend 4-byte aligned with even strides.
+ * On 0, vsk_last_error() names the first failed check. */
 int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend,
                    const vsk_tensor* v_extend, const vsk_tensor* k_buffer,
                    const vsk_tensor* v_buffer, const vsk_tensor* qo_indptr,
@@ -161,14 +162,14 @@ int verify_splitkv_tree_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_exte
  * drafts included (they come from the same cache).  With l_ext = 1 this is
  * the plain paged decode step.
  *   q            [B*l_ext, h_q, D] bf16, sequence b's drafts at rows b*l_ext ..
- *   o            [B*l_ext, h_q, D] bf16 output (written, never read)
- *   k_cache, v_cache  [n_pages*page_size, h_kv, D] bf16 or fp8 e4m3 (same
- *                dtype), rows 16-byte aligned
+ *   o            [B*l_ext, h_q, Dv] bf16 output (written, never read)
+ *   k_cache, v_cache  [n_pages*page_size, h_kv, D] and [.., h_kv, Dv], bf16
+ *                or fp8 e4m3 (same dtype), rows 16-byte aligned
  *   block_table  [B, max_blocks] int32 page ids, rows contiguous; only the
  *                columns covering positions < seq_lens[b] + l_ext are read
  *   seq_lens     [B] int32 cached tokens before the drafts
  *   page_size    tokens per page (>= 1); max_blocks*page_size must cover l_ext
- * D in {64, 128, 256}; (h_q/h_kv)*l_ext within the limits of
+ * D, Dv in {64, 128, 256}; (h_q/h_kv)*l_ext within the limits of
  * verify_splitkv_fwd, whose workspace rules, workspace size and return value
  * apply unchanged.  Device-side checks: a page id whose rows fall outside the
  * cache sets error bit 1 and those keys are left out; seq_lens[b] < 0 or
@@ -208,15 +209,16 @@ int verify_splitkv_write_fwd(const vsk_tensor* q_extend, const vsk_tensor* k_ext
                              void* stream);
 
 /* verify_splitkv_paged_fwd with the drafts' K/V stored by the same launch:
- * k_new / v_new row b*l_ext + t ([B*l_ext, h_kv, D] bf16) goes to cache
- * position seq_lens[b] + t of k_cache / v_cache (block-table addressing as in
- * verify_splitkv_paged_fwd), stored as the cache dtype's round-to-nearest-even
- * of x / k_scale (x / v_scale) in binary32, e4m3 saturating to +-448.  The
- * attention then equals verify_splitkv_paged_fwd run after that store: the
- * drafts enter it as stored (dequantised with k_scale / v_scale).  The draft
- * positions must not be prefix positions of any sequence of the batch; a
- * draft position whose page id is outside the cache is neither written nor
- * attended and sets error bit 1.  k_scale, v_scale must be > 0. */
+ * k_new / v_new row b*l_ext + t ([B*l_ext, h_kv, D] / [B*l_ext, h_kv, Dv]
+ * bf16) goes to cache position seq_lens[b] + t of k_cache / v_cache (block-
+ * table addressing as in verify_splitkv_paged_fwd), stored as the cache
+ * dtype's round-to-nearest-even of x / k_scale (x / v_scale) in binary32,
+ * e4m3 saturating to +-448.  The attention then equals
+ * verify_splitkv_paged_fwd run after that store: the drafts enter it as
+ * stored (dequantised with k_scale / v_scale).  The draft positions must not
+ * be prefix positions of any sequence of the batch; a draft position whose
+ * page id is outside the cache is neither written nor attended and sets
+ * error bit 1.  k_scale, v_scale must be > 0. */
 int verify_splitkv_paged_write_fwd(const vsk_tensor* q, const vsk_tensor* k_new,
                                    const vsk_tensor* v_new, const vsk_tensor* o,
                                    const vsk_tensor* k_cache, const vsk_tensor* v_cache,
@@ -323,8 +325,9 @@ void vsk_set_tuning_split_launch(int mode);
  * then the combine kernel); 0 for shapes no entry point accepts.
  * `prefix_tokens` is what the entry point sees: the length of kv_indices for
  * the flat entry points, batch x block-table columns x page_size for the paged
- * ones.  Host only (no device call); for CUDA-graph bookkeeping and launch
- * counts. */
+ * ones.  For head_dim == v_head_dim; a call with v_head_dim != head_dim makes
+ * one launch.  Host only (no device call); for CUDA-graph bookkeeping and
+ * launch counts. */
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens);
 

@@ -538,6 +538,10 @@ template <int D>
 struct MaxWarps {
   static constexpr int value = (D > 128) ? 4 : 8;
 };
+template <int A, int B>
+struct MaxOf {
+  static constexpr int value = A > B ? A : B;
+};
 
 // SO (stream only): the kernel ends once its pieces' partials are written; the
 // combine kernel folds them in its own launch.  CS = 2 (head_dim 256, one KV
@@ -545,20 +549,27 @@ struct MaxWarps {
 // shared by a pair of warps that split the QK contraction (exchanging their
 // scaled partial scores through shared memory) and own half of the output
 // columns each.  Half the accumulator registers per warp, so three CTAs per SM.
-template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2)>
-__global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS == 2 ? 3 : 1)
+// DV: the value head_dim (output columns), D the query / key head_dim.
+template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D>
+__global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
-  constexpr int NT = D / 8;        // n-tiles of the output row
+  constexpr int NT = DV / 8;       // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
-  static_assert(CS == 1 || (CS == 2 && D == 256 && MTW == 1 && SO), "column split: head_dim 256 stream only");
-  constexpr int DH = D / CS;       // output columns (and contraction length) of one warp
+  static_assert(CS == 1 || (CS == 2 && D == 256 && DV == 256 && MTW == 1 && SO),
+                "column split: head_dim 256 stream only");
+  static_assert(D == DV || (MTW == 1 && CS == 1 && !SO), "head_dim != v_head_dim: one-launch kernel, one tile per warp");
+  constexpr int DH = D / CS;       // contraction length of one warp
+  constexpr int DVH = DV / CS;     // output columns of one warp
   constexpr int NTH = NT / CS;     // its n-tiles
   constexpr int KSH = KS / CS;     // its k-steps
-  constexpr int ROWB = D * EK;     // bytes of one head's K (or V) row
-  constexpr int CPR = ROWB / 16;   // 16-byte chunks per row
-  constexpr int STAGE_B = 2 * kStageTokens * ROWB;
+  constexpr int KSV = DV / 16 / CS;  // its 16-wide output blocks (e4m3 PV)
+  constexpr int ROWB = D * EK;     // bytes of one head's K row
+  constexpr int VROWB = DV * EK;   // bytes of one head's V row
+  constexpr int CPR = ROWB / 16;   // 16-byte chunks per K row
+  constexpr int VCPR = VROWB / 16;  // ... per V row
+  constexpr int STAGE_B = kStageTokens * (ROWB + VROWB);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -644,40 +655,80 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
     const uint32_t slot = ring_s + static_cast<uint32_t>(dslot) * STAGE_B;
     // lane -> (token group, 16-byte chunk): LPT lanes cover one row, so each
     // lane computes a token's K and V addresses once and issues both copies
-    constexpr int LPT = CPR < 32 ? CPR : 32;  // lanes per row
-    constexpr int TSTEP = 32 / LPT;          // tokens covered per pass of the warp
-    constexpr int CPL = CPR / LPT;           // chunks of a row per lane
-    const int cl = lane % LPT;
-    auto copy_token = [&](int t, long long loc) {
-      const bool v = (mask >> t) & 1u;
-      // an absent token is zero-filled (nothing read); q is a valid, never-empty address
-      const unsigned char* ks = v ? kbase + loc * p.kb_s0 : reinterpret_cast<const unsigned char*>(p.q);
-      const unsigned char* vs = v ? vbase + loc * p.vb_s0 : reinterpret_cast<const unsigned char*>(p.q);
+    if constexpr (D == DV) {
+      constexpr int LPT = CPR < 32 ? CPR : 32;  // lanes per row
+      constexpr int TSTEP = 32 / LPT;          // tokens covered per pass of the warp
+      constexpr int CPL = CPR / LPT;           // chunks of a row per lane
+      const int cl = lane % LPT;
+      auto copy_token = [&](int t, long long loc) {
+        const bool v = (mask >> t) & 1u;
+        // an absent token is zero-filled (nothing read); q is a valid, never-empty address
+        const unsigned char* ks = v ? kbase + loc * p.kb_s0 : reinterpret_cast<const unsigned char*>(p.q);
+        const unsigned char* vs = v ? vbase + loc * p.vb_s0 : reinterpret_cast<const unsigned char*>(p.q);
 #pragma unroll
-      for (int cj = 0; cj < CPL; ++cj) {
-        const int cir = cl + LPT * cj;
-        const int pc = cir ^ chunk_swz<CPR>(t);
-        const uint32_t d = slot + static_cast<uint32_t>(t * ROWB + pc * 16);
-        cp_async_16_zfill(d, v ? ks + cir * 16 : ks, v, pol);
-        cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
+        for (int cj = 0; cj < CPL; ++cj) {
+          const int cir = cl + LPT * cj;
+          const int pc = cir ^ chunk_swz<CPR>(t);
+          const uint32_t d = slot + static_cast<uint32_t>(t * ROWB + pc * 16);
+          cp_async_16_zfill(d, v ? ks + cir * 16 : ks, v, pol);
+          cp_async_16_zfill(d + 16 * ROWB, v ? vs + cir * 16 : vs, v, pol);
+        }
+      };
+      if (WPHC == 1) {
+        // the warp copies the whole stage (token indices known at compile time)
+#pragma unroll
+        for (int t = lane / LPT; t < kStageTokens; t += TSTEP) copy_token(t, __shfl_sync(0xffffffffu, myloc, t));
+      } else {
+        // the warps of the head split the stage: tokens [cw * tpw, cw * tpw + tpw)
+        const int tpw = kStageTokens / WPHC;
+#pragma unroll
+        for (int i = 0; i < kStageTokens / TSTEP; ++i) {
+          if (i * TSTEP >= tpw) break;  // uniform across the warp
+          const int tw = lane / LPT + i * TSTEP;
+          const bool act = tw < tpw;    // false only when fewer tokens than one pass of the warp
+          const int t = cw * tpw + (act ? tw : 0);
+          const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+          if (act) copy_token(t, loc);
+        }
       }
-    };
-    if (WPHC == 1) {
-      // the warp copies the whole stage (token indices known at compile time)
-#pragma unroll
-      for (int t = lane / LPT; t < kStageTokens; t += TSTEP) copy_token(t, __shfl_sync(0xffffffffu, myloc, t));
     } else {
-      // the warps of the head split the stage: tokens [cw * tpw, cw * tpw + tpw)
-      const int tpw = kStageTokens / WPHC;
+      // K rows and V rows of different sizes: one pass over the stage's K
+      // rows, then one over its V rows (region after the 16 K rows)
+      auto copy_rows = [&](auto rb_tag, const unsigned char* base, long long s0, uint32_t region) {
+        constexpr int RB = decltype(rb_tag)::value;  // row bytes
+        constexpr int CP = RB / 16;
+        constexpr int LP = CP < 32 ? CP : 32;
+        constexpr int TS = 32 / LP;
+        constexpr int CL = CP / LP;
+        const int cl = lane % LP;
+        auto one = [&](int t, long long loc) {
+          const bool v = (mask >> t) & 1u;
+          const unsigned char* src = v ? base + loc * s0 : reinterpret_cast<const unsigned char*>(p.q);
 #pragma unroll
-      for (int i = 0; i < kStageTokens / TSTEP; ++i) {
-        if (i * TSTEP >= tpw) break;  // uniform across the warp
-        const int tw = lane / LPT + i * TSTEP;
-        const bool act = tw < tpw;    // false only when fewer tokens than one pass of the warp
-        const int t = cw * tpw + (act ? tw : 0);
-        const long long loc = __shfl_sync(0xffffffffu, myloc, t);
-        if (act) copy_token(t, loc);
-      }
+          for (int cj = 0; cj < CL; ++cj) {
+            const int cir = cl + LP * cj;
+            const uint32_t d = region + static_cast<uint32_t>(t * RB + (cir ^ chunk_swz<CP>(t)) * 16);
+            cp_async_16_zfill(d, v ? src + cir * 16 : src, v, pol);
+          }
+        };
+        if (WPHC == 1) {
+#pragma unroll
+          for (int t = lane / LP; t < kStageTokens; t += TS) one(t, __shfl_sync(0xffffffffu, myloc, t));
+        } else {
+          const int tpw = kStageTokens / WPHC;
+#pragma unroll
+          for (int i = 0; i < kStageTokens / TS; ++i) {
+            if (i * TS >= tpw) break;
+            const int tw = lane / LP + i * TS;
+            const bool act = tw < tpw;
+            const int t = cw * tpw + (act ? tw : 0);
+            const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+            if (act) one(t, loc);
+          }
+        }
+      };
+      copy_rows(std::integral_constant<int, ROWB>{}, kbase, p.kb_s0, slot);
+      copy_rows(std::integral_constant<int, VROWB>{}, vbase, p.vb_s0, slot + 16 * ROWB);
     }
   };
 
@@ -727,7 +778,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
   // The next piece's query fragments are loaded into registers while the
   // current piece streams (head_dim <= 128, one tile per warp), so a piece
   // boundary costs no global round trip.
-  constexpr bool kQAhead = D <= 128 && MTW == 1;
+  constexpr bool kQAhead = D <= 128 && DV <= 128 && MTW == 1;
   uint32_t qf[MTW][KSH][4];  // this warp's columns of the query (all of them unless CS = 2)
   uint32_t qn[kQAhead ? KSH : 1][4];
   // bf16 pool: bf16 q fragments; e4m3 pool: f16 q fragments scaled by 2^-sh
@@ -820,7 +871,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
       // (lane & 15) and chunk 2kk2 + (lane >> 4), so one x4 load gives both
       // 8-key tiles of two 16-wide d blocks.
       const uint32_t kbase = smem_u32(slotp) + (FP8 ? f_key : k_key) * ROWB;
-      const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * ROWB;
+      const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * VROWB;
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys per 16-row tile.
       // Independent accumulator chains per n-tile (k-step mod NCH) cut the
@@ -988,10 +1039,10 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
         // column g <-> d 2g) and O (odd d, column g <-> d 2g+1) of a 16-wide
         // block.  acc[2*blk] is E, acc[2*blk+1] is O.
 #pragma unroll
-        for (int c2 = 0; c2 < KSH / 2; ++c2) {
-          const int c = 2 * (csi * (KSH / 2) + c2) + (lane >> 4);
+        for (int c2 = 0; c2 < KSV / 2; ++c2) {
+          const int c = 2 * (csi * (KSV / 2) + c2) + (lane >> 4);
           uint32_t r[4];
-          ldsm_x4_t(vbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r[0], r[1], r[2], r[3]);
+          ldsm_x4_t(vbase + ((c ^ chunk_swz<VCPR>(f_key)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);      // keys 2j, 2j+1
@@ -1027,7 +1078,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
     {
       const long long slot_self = c_self + static_cast<long long>(s.b) * p.n_hg + s.hg;
       float* lse_p = p.plse + (slot_self * p.HC + hc) * RM;
-      float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * D;
+      float* o_p = p.po + ((slot_self * p.HC + hc) * RM) * DV;
       const uint64_t keep = policy_evict_last();
 #pragma unroll
       for (int t = 0; t < MTW; ++t) {
@@ -1039,12 +1090,12 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
           st_keep(lse_p + r0, s0 > 0.f ? m0[t] + log2f(s0) : NEG_INF, keep);
           st_keep(lse_p + r1, s1 > 0.f ? m1[t] + log2f(s1) : NEG_INF, keep);
         }
-        float* o0p = o_p + r0 * D + csi * DH;  // this warp's columns
-        float* o1p = o_p + r1 * D + csi * DH;
+        float* o0p = o_p + r0 * DV + csi * DVH;  // this warp's columns
+        float* o1p = o_p + r1 * DV + csi * DVH;
         if constexpr (FP8) {
           // n-tiles E / O of block blk hold d = 16 blk + 4j + {0, 2} / {1, 3}
 #pragma unroll
-          for (int blk = 0; blk < KSH; ++blk) {
+          for (int blk = 0; blk < KSV; ++blk) {
             const float* e = acc[t][2 * blk];
             const float* o = acc[t][2 * blk + 1];
             st_keep4(o0p + blk * 16 + 4 * j, e[0] * inv0, o[0] * inv0, e[1] * inv0, o[1] * inv0, keep);
@@ -1130,16 +1181,16 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
     }
     const float ms0 = (m0 == NEG_INF) ? 0.f : m0;
     const float ms1 = (m1 == NEG_INF) ? 0.f : m1;
-#pragma unroll(D <= 128 ? 2 : 1)
+#pragma unroll(DV <= 128 ? 2 : 1)
     for (long long i = 0; i < count; ++i) {
       const long long sl = slot0 + i * stride;
       const float* lq = p.plse + (sl * p.HC + hc) * RM;
-      const float* oq = p.po + ((sl * p.HC + hc) * RM) * D;
+      const float* oq = p.po + ((sl * p.HC + hc) * RM) * DV;
       const float w0 = exp2f(__ldcg(lq + r0) - ms0), w1 = exp2f(__ldcg(lq + r1) - ms1);
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * D + n * 8 + 2 * j));
-        const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * D + n * 8 + 2 * j));
+        const float2 x0 = __ldcg(reinterpret_cast<const float2*>(oq + r0 * DV + n * 8 + 2 * j));
+        const float2 x1 = __ldcg(reinterpret_cast<const float2*>(oq + r1 * DV + n * 8 + 2 * j));
         if (w0 > 0.f) {
           acc[n][0] = fmaf(x0.x, w0, acc[n][0]);
           acc[n][1] = fmaf(x0.y, w0, acc[n][1]);
@@ -1175,7 +1226,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
         // the group partial replaces the partial of the group's first piece
         const long long sl = gfirst + s_idx;
         float* lse_p = p.plse + (sl * p.HC + hc) * RM;
-        float* o_p = p.po + ((sl * p.HC + hc) * RM) * D;
+        float* o_p = p.po + ((sl * p.HC + hc) * RM) * DV;
 #pragma unroll 1
         for (int t = 0; t < MTW; ++t) {
           const int r0 = r0s[t], r1 = r1s[t];
@@ -1187,8 +1238,8 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
           }
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
-            *reinterpret_cast<float2*>(o_p + r0 * D + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
-            *reinterpret_cast<float2*>(o_p + r1 * D + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+            *reinterpret_cast<float2*>(o_p + r0 * DV + n * 8 + 2 * j) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+            *reinterpret_cast<float2*>(o_p + r1 * DV + n * 8 + 2 * j) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
           }
         }
         __threadfence();
@@ -1208,23 +1259,24 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
       if (first_tile && !p.paged) {
         const int a = p.qo ? __ldg(p.qo + sg.b) : sg.b * p.L;
         if (a >= 0 && static_cast<long long>(a) + p.L <= p.n_rows) {
-          constexpr int LINES = D * 2 / 128;  // 128-byte lines per row
-          for (int i = lane; i < p.L * LINES * 2; i += 32) {
-            const int t = i / (2 * LINES), rest = i % (2 * LINES);
-            const __nv_bfloat16* base = (rest < LINES) ? p.ke + (static_cast<long long>(a) + t) * p.ke_s0
-                                                       : p.ve + (static_cast<long long>(a) + t) * p.ve_s0;
-            prefetch_l2(base + static_cast<long long>(kvh) * (rest < LINES ? p.ke_s1 : p.ve_s1) + (rest % LINES) * 64);
+          constexpr int KL = D * 2 / 128, VL = DV * 2 / 128;  // 128-byte lines of a K / V row
+          for (int i = lane; i < p.L * (KL + VL); i += 32) {
+            const int t = i / (KL + VL), rest = i % (KL + VL);
+            const bool isk = rest < KL;
+            const __nv_bfloat16* base = isk ? p.ke + (static_cast<long long>(a) + t) * p.ke_s0
+                                            : p.ve + (static_cast<long long>(a) + t) * p.ve_s0;
+            prefetch_l2(base + static_cast<long long>(kvh) * (isk ? p.ke_s1 : p.ve_s1) + (isk ? rest : rest - KL) * 64);
           }
         }
       }
       int s_b = 0;
-      if constexpr (D <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
+      if constexpr (D <= 128 && DV <= 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
       // the pieces (or, for a two-level merge, the group partials) in slot order
       if (tree)
         fold(c_first + s_idx, kGroup, ng, r0, r1);
       else
         fold(c_first + s_idx, 1, npc, r0, r1);
-      if constexpr (D > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
+      if constexpr (D > 128 || DV > 128) s_b = load_q<KS>(p, sg, hc, r0, r1, j, flagger && first_tile, qe);
       // ------------- causal draft keys: continue the same online softmax -------------
       const int i0 = r0 / p.gq, i1 = r1 / p.gq;  // draft index of each row
       // tree verify: this sequence's mask rows (row-major [L][P+L], only the
@@ -1251,42 +1303,38 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
         // once, store the codes into the cache (the head's first tile) and
         // keep the dequantised values in the warp's idle ring, where the
         // fragment loads below read them
-        unsigned char* stK = smem + p.ring_off + warp * (32 * D);
+        unsigned char* stK = smem + p.ring_off + warp * (16 * (D + DV));
         unsigned char* stV = stK + 8 * D * 2;
         if (p.wmode == 2) {
-          constexpr int PR = D / 2;  // bf16 pairs per row
+          constexpr int PRK = D / 2, PRV = DV / 2;  // bf16 pairs per K / V row
 #pragma unroll 1
-          for (int idx = lane; idx < 8 * PR; idx += 32) {
-            const int kl = idx / PR, c = (idx % PR) * 2;
+          for (int idx = lane; idx < 8 * (PRK + PRV); idx += 32) {
+            const bool isk = idx < 8 * PRK;
+            const int kl = isk ? idx / PRK : (idx - 8 * PRK) / PRV;
+            const int c = (isk ? idx % PRK : (idx - 8 * PRK) % PRV) * 2;
             const int key = td * 8 + kl;
             if (key >= p.L) continue;
             const long long row = paged_row(p, sg.b, sg.P + key);
             if (row < 0) continue;
             const long long src = static_cast<long long>(s_b) + key;
-            const float2 xk = unpack_bf16(ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + c));
-            const float2 xv = unpack_bf16(ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c));
-            unsigned char* kd = p.kw + row * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1;
-            unsigned char* vd = p.vw + row * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
-            uint32_t dk, dv;
+            const float2 x = unpack_bf16(isk ? ld_u32(p.ke + src * p.ke_s0 + static_cast<long long>(kvh) * p.ke_s1 + c)
+                                             : ld_u32(p.ve + src * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + c));
+            unsigned char* dst = isk ? p.kw + row * p.kb_s0 + static_cast<long long>(kvh) * p.kb_s1
+                                     : p.vw + row * p.vb_s0 + static_cast<long long>(kvh) * p.vb_s1;
+            const float sc = isk ? p.kq : p.vq;
+            uint32_t dq;
             if constexpr (FP8) {
-              const unsigned short ck = store_e4m3x2(xk.x, xk.y, p.kq);
-              const unsigned short cv = store_e4m3x2(xv.x, xv.y, p.vq);
-              dk = e4m3x2_to_bf16x2(ck);
-              dv = e4m3x2_to_bf16x2(cv);
-              if (first_tile) {
-                *reinterpret_cast<unsigned short*>(kd + c) = ck;
-                *reinterpret_cast<unsigned short*>(vd + c) = cv;
-              }
+              const unsigned short cq = store_e4m3x2(x.x, x.y, sc);
+              dq = e4m3x2_to_bf16x2(cq);
+              if (first_tile) *reinterpret_cast<unsigned short*>(dst + c) = cq;
             } else {
-              dk = store_bf16x2(xk.x, xk.y, p.kq);
-              dv = store_bf16x2(xv.x, xv.y, p.vq);
-              if (first_tile) {
-                *reinterpret_cast<uint32_t*>(kd + c * 2) = dk;
-                *reinterpret_cast<uint32_t*>(vd + c * 2) = dv;
-              }
+              dq = store_bf16x2(x.x, x.y, sc);
+              if (first_tile) *reinterpret_cast<uint32_t*>(dst + c * 2) = dq;
             }
-            *reinterpret_cast<uint32_t*>(stK + (kl * D + c) * 2) = dk;
-            *reinterpret_cast<uint32_t*>(stV + (kl * D + c) * 2) = dv;
+            if (isk)
+              *reinterpret_cast<uint32_t*>(stK + (kl * D + c) * 2) = dq;
+            else
+              *reinterpret_cast<uint32_t*>(stV + (kl * DV + c) * 2) = dq;
           }
           __syncwarp();
         }
@@ -1388,7 +1436,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
         }
         // fp32 weighted sum of the draft values of this tile
         bool v_done = false;
-        if constexpr (D <= 128) {
+        if constexpr (DV <= 128) {
           if (!p.paged && p.wmode == 0) {
             // drafts from v_extend: four keys' value rows per load round trip
 #pragma unroll
@@ -1433,7 +1481,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<D>::value * 32, CS ==
             const float w1 = __shfl_sync(0xffffffffu, pd[2 + e], g * 4 + js) * p.dvs;
             if (p.wmode == 2) {
               if (paged_row(p, sg.b, sg.P + key) < 0) continue;  // uniform; its weight is 0
-              const unsigned char* vr = stV + ((key - td * 8) * D + 2 * j) * 2;
+              const unsigned char* vr = stV + ((key - td * 8) * DV + 2 * j) * 2;
 #pragma unroll
               for (int n = 0; n < NT; ++n) {
                 const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(vr + n * 16));

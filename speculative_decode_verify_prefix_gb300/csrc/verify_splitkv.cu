@@ -62,13 +62,15 @@ int floor_pow2(int x) {
 // Chooses the CTA shape: HC KV heads per CTA x MT 16-row tiles per head; a
 // consumer warp owns MTW tiles (two at head_dim <= 128 when a head has more
 // than one tile, so its K / V fragments feed both); ring depth from the
-// shared-memory budget.
+// shared-memory budget.  DV: the value head_dim (0: the same as D).
 bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl,
-               long long total_tokens, int tiles) {
+               long long total_tokens, int tiles, long long DV = 0) {
+  if (DV == 0) DV = D;
   if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
   const long long R = (h_q / h_kv) * L;
-  const int maxw = D > 128 ? 4 : 8;
-  if (R > 16LL * maxw) return fail("packed rows (h_q/h_kv)*l_ext = %lld exceed %d for head_dim %lld", R, 16 * maxw, D);
+  const long long DM = std::max(D, DV);
+  const int maxw = DM > 128 ? 4 : 8;
+  if (R > 16LL * maxw) return fail("packed rows (h_q/h_kv)*l_ext = %lld exceed %d for head_dim %lld", R, 16 * maxw, DM);
   pl.gq = static_cast<int>(h_q / h_kv);
   pl.R = static_cast<int>(R);
   int mt = 1;
@@ -78,7 +80,7 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   // small problems are latency bound and want more, lighter warps
   if (tiles == 0) tiles = g_tiles;
   if (tiles == 0) tiles = total_tokens >= kTwoTileMinTokens ? 2 : 1;
-  pl.MTW = (D <= 128 && mt >= 2 && tiles == 2) ? 2 : 1;
+  pl.MTW = (DM <= 128 && D == DV && mt >= 2 && tiles == 2) ? 2 : 1;
   const int wph = mt / pl.MTW;  // warps per head
   int hc = 1;
   const int hc_cap = g_max_heads > 0 ? g_max_heads : maxw;
@@ -90,7 +92,7 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.ek = fp8 ? 1 : 2;
   // per head: nst stages of 16 K rows + 16 V rows; per warp: the index ring,
   // the mask ring and (two-tile warps; e4m3 pools at head_dim 256) the query tiles
-  pl.stage_bytes = 2 * kStageTokens * static_cast<int>(D) * pl.ek;
+  pl.stage_bytes = kStageTokens * static_cast<int>(D + DV) * pl.ek;
   const int qsm_tiles = (fp8 && D == 256) ? 1 : (pl.MTW == 2 ? 2 : 0);  // query tiles kept in shared memory
   const int fixed = kIdxRing * 128 + 128 + qsm_tiles * 16 * static_cast<int>(D) * 2;
   // CTAs per SM: as many as keep about 8 warps per SM with a ring of at
@@ -113,8 +115,9 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.head_bytes = pl.nst * pl.stage_bytes;
   pl.misc_bytes = fixed;
   pl.ring_off = kCtlBytes;
-  // the ring region also holds each warp's staged drafts (32 * D bytes) after streaming
-  const int rings = std::max(pl.HC * pl.head_bytes, pl.nwc * 32 * static_cast<int>(D));
+  // the ring region also holds each warp's staged drafts (8 K rows and 8 V
+  // rows of bf16, 16 (D + DV) bytes) after streaming
+  const int rings = std::max(pl.HC * pl.head_bytes, pl.nwc * 16 * static_cast<int>(D + DV));
   pl.misc_off = pl.ring_off + rings;
   pl.smem = static_cast<size_t>(pl.misc_off) + static_cast<size_t>(pl.nwc) * pl.misc_bytes;
   if (pl.smem > static_cast<size_t>(kSmemPerCTAMax)) return fail("shared memory plan of %zu bytes too large", pl.smem);
@@ -215,7 +218,7 @@ struct WsLayout {
   size_t lse_off, o_off, cnt_bytes, total;
 };
 
-WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
+WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long DV) {
   WsLayout w;
   const long long segs = B * pl.n_hg;
   const long long slots = n_cta + segs;
@@ -223,7 +226,7 @@ WsLayout ws_layout(long long n_cta, long long B, const Plan& pl, long long D) {
   w.lse_off = 256;
   w.o_off = w.lse_off + align256(4 * static_cast<size_t>(rows));
   w.cnt_bytes = std::max(static_cast<size_t>(kTicketBytes), align256(4 * static_cast<size_t>(segs + slots)));
-  w.total = align256(w.o_off + 4 * static_cast<size_t>(rows) * static_cast<size_t>(D)) + w.cnt_bytes;
+  w.total = align256(w.o_off + 4 * static_cast<size_t>(rows) * static_cast<size_t>(DV)) + w.cnt_bytes;
   return w;
 }
 
@@ -301,8 +304,8 @@ bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const
   if (ke->shape[0] != q->shape[0] || ve->shape[0] != q->shape[0]) return fail("k_extend/v_extend rows differ from q_extend");
   if (kb->shape[0] != vb->shape[0]) return fail("k_buffer and v_buffer pools differ in size");
   // this build's limits
-  if (D != Dv) return fail("head_dim (%lld) != v_head_dim (%lld) is not built", D, Dv);
   if (D != 64 && D != 128 && D != 256) return fail("head_dim %lld not in {64, 128, 256}", D);
+  if (Dv != 64 && Dv != 128 && Dv != 256) return fail("v_head_dim %lld not in {64, 128, 256}", Dv);
   if (q->dtype != VSK_DTYPE_BF16 || ke->dtype != VSK_DTYPE_BF16 || ve->dtype != VSK_DTYPE_BF16)
     return fail("q_extend, k_extend and v_extend must be bf16");
   if (kb->dtype != vb->dtype || (kb->dtype != VSK_DTYPE_BF16 && kb->dtype != VSK_DTYPE_FP8E4M3))
@@ -310,7 +313,7 @@ bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const
   if (qo->dtype != VSK_DTYPE_I32 || kvp->dtype != VSK_DTYPE_I32) return fail("indptr arrays must be int32");
   if (kvi->dtype != VSK_DTYPE_I32 && kvi->dtype != VSK_DTYPE_I64) return fail("kv_indices must be int32 or int64");
   const long long R = (h_q / h_kv) * mle;
-  const long long maxR = D > 128 ? 64 : 128;
+  const long long maxR = std::max(D, Dv) > 128 ? 64 : 128;
   if (R > maxR) return fail("(h_q/h_kv)*max_len_extend = %lld exceeds %lld", R, maxR);
   const size_t ek = kb->dtype == VSK_DTYPE_BF16 ? 2 : 1;
   for (const vsk_tensor* t : {kb, vb}) {
@@ -324,7 +327,8 @@ bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const
   return true;
 }
 
-KernelFn pick_kernel(int D, bool fp8, int mtw) {
+KernelFn pick_kernel(int D, bool fp8, int mtw, int DV = 0) {
+  if (DV != 0 && DV != D) return mtw == 1 ? kernel_dv(D, DV, fp8) : nullptr;
   switch (D) {
     case 64: return kernel_d64(fp8, mtw, false);
     case 128: return kernel_d128(fp8, mtw, false);
@@ -418,19 +422,21 @@ int vsk_can_handle(const vsk_tensor* q_extend, const vsk_tensor* k_extend, const
 
 size_t vsk_workspace_size_for_sms(int num_sms, int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t head_dim,
                                   int64_t v_head_dim, int64_t max_len_extend) {
-  if (num_sms <= 0 || max_bs < 1 || head_dim != v_head_dim || max_len_extend < 1) return 0;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
+  if (num_sms <= 0 || max_bs < 1 || max_len_extend < 1) return 0;
+  for (const int64_t d : {head_dim, v_head_dim})
+    if (d != 64 && d != 128 && d != 256) return 0;
   const long long n_cta = static_cast<long long>(num_sms) * 4;  // bound on CTAs per SM
   size_t need = 0;
   for (int fp8 = 0; fp8 < 2; ++fp8) {
     for (int tiles = 1; tiles <= 2; ++tiles) {
       Plan pl;
-      if (!make_plan(h_q, h_kv, head_dim, max_len_extend, fp8 != 0, pl, 0, tiles)) return 0;
-      need = std::max(need, ws_layout(n_cta, max_bs, pl, head_dim).total);
+      if (!make_plan(h_q, h_kv, head_dim, max_len_extend, fp8 != 0, pl, 0, tiles, v_head_dim)) return 0;
+      need = std::max(need, ws_layout(n_cta, max_bs, pl, v_head_dim).total);
     }
   }
   Plan tp;
-  if (head_dim == 256 && (h_q / h_kv) * max_len_extend <= 32 && make_tc_plan(h_q, h_kv, head_dim, max_len_extend, false, tp))
+  if (head_dim == 256 && v_head_dim == 256 && (h_q / h_kv) * max_len_extend <= 32 &&
+      make_tc_plan(h_q, h_kv, head_dim, max_len_extend, false, tp))
     need = std::max(need, ws_layout(n_cta, max_bs, tp, head_dim).total);
   return need;
 }
@@ -445,13 +451,13 @@ size_t vsk_workspace_size(int64_t max_bs, int64_t h_q, int64_t h_kv, int64_t hea
   if (g_num_ctas > 4 * sms) {
     for (int tiles = 1; tiles <= 2; ++tiles) {
       Plan pl;
-      if (make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl, 0, tiles)) {
-        const size_t t = ws_layout(g_num_ctas, max_bs, pl, head_dim).total;
+      if (make_plan(h_q, h_kv, head_dim, max_len_extend, false, pl, 0, tiles, v_head_dim)) {
+        const size_t t = ws_layout(g_num_ctas, max_bs, pl, v_head_dim).total;
         if (t > need) need = t;
       }
     }
     Plan tp;
-    if (head_dim == 256 && h_kv > 0 && h_q % h_kv == 0 && (h_q / h_kv) * max_len_extend <= 32 &&
+    if (head_dim == 256 && v_head_dim == 256 && h_kv > 0 && h_q % h_kv == 0 && (h_q / h_kv) * max_len_extend <= 32 &&
         make_tc_plan(h_q, h_kv, head_dim, max_len_extend, false, tp)) {
       const size_t t = ws_layout(g_num_ctas, max_bs, tp, head_dim).total;
       if (t > need) need = t;
@@ -554,17 +560,19 @@ struct CallPlan {
   int D = 0;
 };
 
-static int plan_call(long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
+static int plan_call(long long B, long long h_q, long long h_kv, long long D, long long DV, long long L, bool fp8,
                      long long mean_len, CallPlan& cp) {
   cp.D = static_cast<int>(D);
-  cp.use_tc = tc_eligible(h_q, h_kv, D, L);
-  cp.use_cs = !cp.use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
-  cp.use_sl = !cp.use_tc && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
+  // the two-launch forms are built for head_dim == v_head_dim only
+  const bool same = D == DV;
+  cp.use_tc = same && tc_eligible(h_q, h_kv, D, L);
+  cp.use_cs = same && !cp.use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_sl = same && !cp.use_tc && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan& pl = cp.pl;
   if ((cp.use_tc || cp.use_cs)
           ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
           : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
-                       cp.use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0))
+                       cp.use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0, DV))
     return 0;
   if (cp.use_cs && !make_cs_stream_plan(pl, D, fp8, cp.sp)) return 0;
   cudaError_t e = cudaGetDevice(&cp.dev);
@@ -602,15 +610,16 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     if (!cp.fn || !cp.fn_comb || !prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb))
       return fail("stream-only kernels for head_dim %lld unavailable", D);
   } else {
-    cp.fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW);
-    if (!cp.fn || !prepare_kernel(cp.fn)) return fail("kernel for head_dim %lld unavailable", D);
+    cp.fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW, static_cast<int>(DV));
+    if (!cp.fn || !prepare_kernel(cp.fn))
+      return fail("kernel for head_dim %lld, v_head_dim %lld unavailable", D, DV);
   }
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(cp.fn), cp.threads, cp.smem);
   if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
   per_sm = std::min(occ, per_sm);
   cp.n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
-  cp.wl = ws_layout(cp.n_cta, B, pl, D);
+  cp.wl = ws_layout(cp.n_cta, B, pl, DV);
   if (cp.fn_comb) {
     // one combine CTA per (segment, 16-row tile, 32-column slice)
     cp.n_comb = B * pl.n_hg * pl.HC * pl.MT * (D / cmb::kCols);
@@ -691,10 +700,10 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
 
 // Plans the call, resolves the workspace (NULL: the library-owned per-device
 // buffer) and enqueues the launches.
-static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long L, bool fp8,
-                            void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
+static int launch_with_plan(Params& p, long long B, long long h_q, long long h_kv, long long D, long long DV, long long L,
+                            bool fp8, void* workspace, size_t workspace_bytes, void* stream, long long mean_len) {
   CallPlan cp;
-  if (!plan_call(B, h_q, h_kv, D, L, fp8, mean_len, cp)) return 0;
+  if (!plan_call(B, h_q, h_kv, D, DV, L, fp8, mean_len, cp)) return 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   size_t ws_bytes = workspace_bytes;
@@ -714,7 +723,7 @@ static int launch_with_plan(Params& p, long long B, long long h_q, long long h_k
 // causal drafts), ocl the fused store.  Returns the static shapes the plan
 // needs.
 struct CallShape {
-  long long B, h_q, h_kv, D, L, mean_len;
+  long long B, h_q, h_kv, D, DV, L, mean_len;
   bool fp8;
 };
 
@@ -789,6 +798,7 @@ static int prepare_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_t
   cs.h_q = q->shape[1];
   cs.h_kv = ke->shape[1];
   cs.D = D;
+  cs.DV = ve->shape[2];
   cs.L = max_len_extend;
   cs.fp8 = kb->dtype == VSK_DTYPE_FP8E4M3;
   cs.mean_len = kvi->shape[0] / cs.B;
@@ -806,7 +816,7 @@ static int run_verify(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tenso
   if (!prepare_verify(q, ke, ve, o, kb, vb, qo, kvp, kvi, is_causal, max_len_extend, k_scale, v_scale, sm_scale, cm,
                       mi, ocl, p, cs))
     return 0;
-  return launch_with_plan(p, cs.B, cs.h_q, cs.h_kv, cs.D, cs.L, cs.fp8, workspace, workspace_bytes, stream,
+  return launch_with_plan(p, cs.B, cs.h_q, cs.h_kv, cs.D, cs.DV, cs.L, cs.fp8, workspace, workspace_bytes, stream,
                           cs.mean_len);
 }
 
@@ -843,24 +853,25 @@ static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor*
   const long long h_q = q->shape[1], h_kv = kc->shape[1], D = q->shape[2];
   if (h_kv == 0 || h_q % h_kv != 0) return fail("h_q (%lld) is not a multiple of h_kv (%lld)", h_q, h_kv);
   if (vc->shape[1] != h_kv) return fail("KV head count mismatch between k_cache and v_cache");
+  const long long DV = vc->shape[2];
   if (kc->shape[2] != D) return fail("head_dim mismatch between q and k_cache");
-  if (vc->shape[2] != D) return fail("v_head_dim (%lld) != head_dim (%lld) is not built", vc->shape[2], D);
   if (D != 64 && D != 128 && D != 256) return fail("head_dim %lld not in {64, 128, 256}", D);
+  if (DV != 64 && DV != 128 && DV != 256) return fail("v_head_dim %lld not in {64, 128, 256}", DV);
   if (kc->shape[0] != vc->shape[0]) return fail("k_cache and v_cache pools differ in size");
   if (kc->shape[0] % page_size != 0) return fail("cache rows (%lld) are not a whole number of pages", kc->shape[0]);
   if (q->dtype != VSK_DTYPE_BF16) return fail("q must be bf16");
   if (kc->dtype != vc->dtype || (kc->dtype != VSK_DTYPE_BF16 && kc->dtype != VSK_DTYPE_FP8E4M3))
     return fail("k_cache and v_cache must both be bf16 or both fp8 e4m3");
   const long long R = (h_q / h_kv) * mle;
-  const long long maxR = D > 128 ? 64 : 128;
+  const long long maxR = std::max(D, DV) > 128 ? 64 : 128;
   if (R > maxR) return fail("(h_q/h_kv)*max_len_extend = %lld exceeds %lld", R, maxR);
   const size_t ek = kc->dtype == VSK_DTYPE_BF16 ? 2 : 1;
   for (const vsk_tensor* t : {kc, vc}) {
     if (!aligned(t->data, 16) || (t->stride[0] * ek) % 16 != 0 || (t->stride[1] * ek) % 16 != 0)
       return fail("K/V cache rows must be 16-byte aligned");
   }
-  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != h_q || o->shape[2] != D)
-    return fail("o must be bf16 [B*l_ext, h_q, head_dim]");
+  if (o->dtype != VSK_DTYPE_BF16 || o->shape[0] != q->shape[0] || o->shape[1] != h_q || o->shape[2] != DV)
+    return fail("o must be bf16 [B*l_ext, h_q, v_head_dim]");
   for (const vsk_tensor* t : {q, o}) {
     if (!aligned(t->data, 4) || (t->stride[0] % 2) != 0 || (t->stride[1] % 2) != 0)
       return fail("q and o must be 4-byte aligned with even strides");
@@ -910,8 +921,8 @@ static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor*
     if (!check_3d(k_new, "k_new") || !check_3d(v_new, "v_new")) return 0;
     if (k_new->dtype != VSK_DTYPE_BF16 || v_new->dtype != VSK_DTYPE_BF16) return fail("k_new and v_new must be bf16");
     if (k_new->shape[0] != q->shape[0] || v_new->shape[0] != q->shape[0] || k_new->shape[1] != h_kv ||
-        v_new->shape[1] != h_kv || k_new->shape[2] != D || v_new->shape[2] != D)
-      return fail("k_new / v_new must be [B*l_ext, h_kv, head_dim]");
+        v_new->shape[1] != h_kv || k_new->shape[2] != D || v_new->shape[2] != DV)
+      return fail("k_new / v_new must be [B*l_ext, h_kv, head_dim / v_head_dim]");
     for (const vsk_tensor* t : {k_new, v_new}) {
       if (!aligned(t->data, 4) || (t->stride[0] % 2) != 0 || (t->stride[1] % 2) != 0)
         return fail("k_new and v_new must be 4-byte aligned with even strides");
@@ -930,7 +941,7 @@ static int run_paged(const vsk_tensor* q, const vsk_tensor* o, const vsk_tensor*
     p.vq = v_scale;
   }
   // the block table bounds every sequence's length: its capacity stands in for the mean
-  return launch_with_plan(p, bs, h_q, h_kv, D, mle, kc->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes,
+  return launch_with_plan(p, bs, h_q, h_kv, D, DV, mle, kc->dtype == VSK_DTYPE_FP8E4M3, workspace, workspace_bytes,
                           stream, bt->shape[1] * page_size);
 }
 }  // namespace vsk
@@ -1047,7 +1058,7 @@ extern "C" int verify_splitkv_fwd_noalloc(const vsk_tensor* q, const vsk_tensor*
     return 0;
   // the same plan (form, grid, workspace layout) verify_splitkv_fwd would use
   CallPlan cp;
-  if (!plan_call(cs.B, cs.h_q, cs.h_kv, cs.D, cs.L, cs.fp8, cs.mean_len, cp)) return 0;
+  if (!plan_call(cs.B, cs.h_q, cs.h_kv, cs.D, cs.DV, cs.L, cs.fp8, cs.mean_len, cp)) return 0;
   if (cp.wl.total > static_cast<size_t>(VSK_NOALLOC_SCRATCH_BYTES))
     return fail("this problem needs %zu bytes of scratch, more than the %d bytes built into the library for "
                 "verify_splitkv_fwd_noalloc; use verify_splitkv_fwd with a caller workspace",

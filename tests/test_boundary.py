@@ -82,11 +82,16 @@ def test_rejects_unbuilt_dtypes_and_sizes():
     p = workloads.make_problem(spec, "cpu")
     assert not vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
                               p["kv_indptr"], p["kv_indices"], None, True, None, 4)
-    # D != Dv
+    # D != Dv: built for D, Dv in {64, 128, 256}; any other v_head_dim is not
     spec = workloads.Spec("dne", (20,), 4, 4, 1, 64, 128, seed=4)
+    p = workloads.make_problem(spec, "cpu")
+    assert vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
+                          p["kv_indptr"], p["kv_indices"], None, True, None, 4)
+    spec = workloads.Spec("dv96", (20,), 4, 4, 1, 64, 96, seed=4)
     p = workloads.make_problem(spec, "cpu")
     assert not vsk.can_handle(p["q"], p["k_ext"], p["v_ext"], p["k_buffer"], p["v_buffer"], p["qo_indptr"],
                               p["kv_indptr"], p["kv_indices"], None, True, None, 4)
+    assert "v_head_dim" in vsk.last_error()
 
 
 def test_packed_row_limit():
@@ -131,6 +136,11 @@ def test_workspace_bound_for_sms():
     a = lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 128, 128, 4)
     b = lib.vsk_workspace_size_for_sms(152, 128, 32, 8, 128, 128, 4)
     assert 0 < a < b
+    # head_dim != v_head_dim: the partials hold v_head_dim columns
+    c = lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 128, 64, 4)
+    d = lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 128, 256, 4)
+    assert 0 < c < a < d
+    assert lib.vsk_workspace_size_for_sms(152, 64, 32, 8, 128, 96, 4) == 0
     # serving shape: partial slots (4 CTAs/SM bound + one per segment) x 8 heads x 16 rows x (128 + 1) fp32
     slots = 4 * 152 + 64
     assert a >= slots * 8 * 16 * 129 * 4

@@ -126,6 +126,35 @@ def test_fp8_pool_with_scales(vsk):
     assert err < 2e-3  # fp8 decode is exact on both sides; outputs are ~v_scale/sqrt(n)
 
 
+DV_PAIRS = [(64, 128), (64, 256), (128, 64), (128, 256), (256, 64), (256, 128)]
+
+
+@pytest.mark.parametrize("pool", ["bf16", "e4m3"])
+@pytest.mark.parametrize("d,dv", DV_PAIRS, ids=lambda x: str(x))
+def test_head_dim_differs_from_v_head_dim(vsk, d, dv, pool):
+    """head_dim != v_head_dim (the value rows, the partials and the output
+    have v_head_dim columns), one launch; empty, short and multi-piece
+    prefixes, permuted pool slots, scales on the e4m3 pool."""
+    fp8 = pool == "e4m3"
+    spec = workloads.Spec(f"dv_{d}_{dv}_{pool}", (0, 17, 300, 2500), 4, 16, 2, d, dv, pool=pool, perm=True,
+                          pool_extra=20, k_scale=0.5 if fp8 else 1.0, v_scale=0.75 if fp8 else 1.0,
+                          seed=900 + d + dv + (7 if fp8 else 0))
+    p = gpu_problem(spec)
+    assert vsk.launches_per_call(4, 16, 2, d, 4, p["kv_indices"].shape[0]) >= 1
+    vsk.read_error_flags()
+    o = run_gpu(vsk, p)
+    assert o.shape[2] == dv
+    check(o, oracle_o(p), scaled=SCALED)
+    assert vsk.read_error_flags() == 0
+    # the split of the prefix across CTAs changes the rounding order only
+    vsk.set_tuning(7, 16)
+    try:
+        o2 = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning(0, 0)
+    check(o2, oracle_o(p), scaled=SCALED)
+
+
 def _subproblem(prob, b):
     """Sequence b alone, with its referenced pool rows gathered to the host."""
     kvp, qo = prob["kv_indptr"].cpu(), prob["qo_indptr"].cpu()
@@ -320,6 +349,7 @@ TREES = [
     workloads.Spec("tree_rand_d256_fp8", (700, 90), 6, 16, 2, 256, 256, pool="e4m3", perm=True, tree="random",
                    k_scale=0.5, v_scale=0.25, seed=203),
     workloads.Spec("tree_rand_d64_l16", (129, 64), 16, 8, 1, 64, 64, perm=True, tree="random", seed=204),
+    workloads.Spec("tree_rand_d256_dv128", (500, 33), 6, 8, 2, 256, 128, perm=True, tree="random", seed=205),
 ]
 
 
@@ -396,13 +426,18 @@ PAGED = [
     workloads.Spec("paged_ps24_fp8", (23, 24, 25, 3000), 4, 8, 2, 128, 128, pool="e4m3", perm=True, page_size=24,
                    k_scale=0.75, v_scale=1.25, seed=312),
     workloads.Spec("paged_ps100_d64", (99, 100, 101, 1234), 5, 16, 8, 64, 64, perm=True, page_size=100, seed=313),
+    # head_dim != v_head_dim
+    workloads.Spec("paged_ps16_d128_dv64", (300, 0, 1500), 4, 16, 2, 128, 64, perm=True, page_size=16, seed=314),
+    workloads.Spec("paged_ps8_d64_dv256_fp8", (77, 900), 2, 16, 4, 64, 256, pool="e4m3", perm=True, page_size=8,
+                   k_scale=0.5, v_scale=1.5, seed=315),
 ]
 
 
 def run_paged(vsk, prob, o=None, **kw):
     q = prob["q"]
     if o is None:
-        o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=q.device)
+        o = torch.full((q.shape[0], q.shape[1], prob["v_buffer"].shape[2]), float("nan"), dtype=torch.bfloat16,
+                       device=q.device)
     vsk.verify_splitkv_paged_fwd(q, o, prob["k_buffer"], prob["v_buffer"], prob["block_table"], prob["seq_lens"],
                                  prob["page_size"], prob["max_len_extend"], prob["k_scale"], prob["v_scale"],
                                  sm_scale=prob["sm_scale"], **kw)
@@ -517,6 +552,8 @@ WRITE_FLAT = [
                    k_scale=2.0, v_scale=0.75, seed=403),
     workloads.Spec("write_bf16_scaled", (500,), 3, 32, 8, 128, 128, perm=True, pool_extra=8, k_scale=1.5,
                    v_scale=0.5, seed=404),
+    workloads.Spec("write_fp8_d128_dv256", (400, 7), 4, 16, 2, 128, 256, pool="e4m3", perm=True, pool_extra=40,
+                   k_scale=0.5, v_scale=0.25, seed=405),
 ]
 
 
@@ -563,6 +600,8 @@ PAGED_WRITE = [
                    v_scale=1.25, seed=414),
     workloads.Spec("pwrite_ps16_bf16_poison", (40, 0, 129), 4, 8, 2, 128, 128, perm=True, page_size=16,
                    pool_extra=200, poison=True, k_scale=1.25, v_scale=2.0, seed=415),
+    workloads.Spec("pwrite_ps16_d256_dv64_fp8", (600, 3), 4, 16, 2, 256, 64, pool="e4m3", perm=True, page_size=16,
+                   k_scale=0.5, v_scale=0.75, seed=416),
 ]
 
 
@@ -582,7 +621,8 @@ def test_fused_store_paged(vsk, spec):
     k_new = torch.randn(p["k_ext"].shape, generator=g, device="cuda").to(torch.bfloat16)
     v_new = torch.randn(p["v_ext"].shape, generator=g, device="cuda").to(torch.bfloat16)
     kc, vc = p["k_buffer"].clone(), p["v_buffer"].clone()
-    o = torch.full(p["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = torch.full((p["q"].shape[0], p["q"].shape[1], vc.shape[2]), float("nan"), dtype=torch.bfloat16,
+                   device="cuda")
     vsk.read_error_flags()
     vsk.verify_splitkv_paged_write_fwd(p["q"], k_new, v_new, o, kc, vc, p["block_table"], p["seq_lens"],
                                        p["page_size"], p["max_len_extend"], p["k_scale"], p["v_scale"],
