@@ -320,6 +320,31 @@ void vsk_set_tuning_colsplit(int mode);
  * rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_split_launch(int mode);
 
+/* Tuning switch, for A/B runs and tests: the cluster form.  One
+ * thread-block cluster of up to 16 CTAs per (sequence, KV head) segment
+ * streams that segment's prefix, then, after a cluster barrier, the
+ * cluster's CTAs fold the segment's partials, add the draft block and write
+ * o: one launch, no tickets, no second kernel.  It serves head_dim ==
+ * v_head_dim, at most 32 draft rows per sequence and at most 512 segments.
+ * Mode 1 (the default) takes it when the call's prefix tokens (kv_indices
+ * entries, or block-table capacity for the paged entry points) times h_kv are
+ * fewer than 2,048 (the smallest calls, where it measured faster than the
+ * one-launch kernel on GB300; above that the stream + combine launches are
+ * faster); mode 2 takes it wherever it applies; mode 0 never.
+ * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
+ * up to rounding order.  Process-wide; not thread-safe. */
+void vsk_set_tuning_cluster(int mode);
+
+/* Tuning switch, for A/B runs: mode 1 launches the combine kernel of the
+ * two-launch forms as a programmatic dependent of the prefix stream
+ * (cudaLaunchAttributeProgrammaticStreamSerialization): its CTAs may start
+ * while the stream runs, read the call's inputs (lengths, drafts, queries)
+ * and wait for the stream grid before reading its partials.  Mode 0 (the
+ * default; measured faster on GB300 for all but the smallest calls) launches
+ * it after the stream in plain stream order.  The result is the same either
+ * way.  Process-wide; not thread-safe. */
+void vsk_set_tuning_pdl(int mode);
+
 /* Kernel launches a call of these static shapes makes on its stream under the
  * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
  * then the combine kernel); 0 for shapes no entry point accepts.

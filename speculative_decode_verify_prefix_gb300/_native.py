@@ -126,6 +126,10 @@ def _bind(lib):
     lib.vsk_set_tuning_colsplit.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_split_launch.restype = None
     lib.vsk_set_tuning_split_launch.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_cluster.restype = None
+    lib.vsk_set_tuning_cluster.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_pdl.restype = None
+    lib.vsk_set_tuning_pdl.argtypes = [ctypes.c_int]
     lib.vsk_launches_per_call.restype = ctypes.c_int
     lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
     lib.vsk_set_tuning_shape.restype = None

@@ -309,6 +309,20 @@ def set_tuning_split_launch(mode: int = 1) -> None:
     _native.lib().vsk_set_tuning_split_launch(int(mode))
 
 
+def set_tuning_cluster(mode: int = 1) -> None:
+    """The cluster form (one launch; one thread-block cluster per (sequence,
+    KV head) folds its own partials): for small calls (1, the default), wherever
+    it applies (2) or never (0); for A/B runs and tests."""
+    _native.lib().vsk_set_tuning_cluster(int(mode))
+
+
+def set_tuning_pdl(enabled: bool = False) -> None:
+    """Launch the combine kernel of the two-launch forms as a programmatic
+    dependent of the prefix stream, or in plain stream order (the default);
+    for A/B runs."""
+    _native.lib().vsk_set_tuning_pdl(1 if enabled else 0)
+
+
 def launches_per_call(batch: int, h_q: int, h_kv: int, head_dim: int, max_len_extend: int,
                       prefix_tokens: int) -> int:
     """Kernel launches one call of these shapes makes (1 or 2; 0 if no entry

@@ -48,23 +48,33 @@ struct Geo {
 };
 }  // namespace cmb
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid_constant__ Params p) {
+// One unit of the combine: segment s_idx, KV head hc of the segment, 16-row
+// tile `tile`, 32-column slice ch, served by 128 threads (tid 0..127) with
+// the shared-memory region smem (Geo<D>::kSmem bytes).  CL = false: the
+// combine kernel, which finds the segment's pieces by the stream launch's cut
+// of the work (a block scan) and synchronises with __syncthreads.  CL = true:
+// the cluster form, whose pieces are slot0 .. slot0 + npc - 1 and whose
+// threads meet at named barrier `bar` (128 threads).
+template <int D, bool FP8, bool CL>
+__device__ __forceinline__ void combine_unit(const Params& p, unsigned char* smem, const int tid, const int bar,
+                                             const long long s_idx, const int hc, const int tile, const int ch,
+                                             long long slot0, long long npc) {
   using namespace cmb;
   using G = Geo<D>;
-  constexpr int kSlices = G::kSlices, kKPitch = G::kKPitch;
+  constexpr int kKPitch = G::kKPitch;
   constexpr int kScanOff = G::kScanOff, kSrcOff = G::kSrcOff, kDstOff = G::kDstOff, kKOff = G::kKOff;
   constexpr int kVOff = G::kVOff, kFoldOff = G::kFoldOff, kAccOff = G::kAccOff, kScOff = G::kScOff;
   constexpr int DW = D / 4;    // head dimensions of one warp's part of the draft scores
   constexpr int KSW = DW / 16;  // its k-steps
-  extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, j = lane & 3;
-  const int ch = static_cast<int>(blockIdx.x % kSlices);
-  const int tile = static_cast<int>((blockIdx.x / kSlices) % p.MT);
-  const int hc = static_cast<int>((blockIdx.x / (kSlices * p.MT)) % p.HC);
-  const long long s_idx = static_cast<long long>(blockIdx.x) / (kSlices * p.MT * p.HC);
   const int RM = 16 * p.MT;
+  auto sync = [&]() {
+    if constexpr (CL)
+      named_bar_sync(bar, kThreads);
+    else
+      __syncthreads();
+  };
   const float NEG_INF = -INFINITY;
   Seg sg;
   sg.b = static_cast<int>(s_idx / p.n_hg);
@@ -79,7 +89,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
   // block sums of the virtual segment lengths: all of them and those before b
   // (issued first: nothing else waits on fewer loads)
   long long* scan = reinterpret_cast<long long*>(smem + kScanOff);
-  {
+  if constexpr (!CL) {
     long long tot_t = 0, bef_t = 0;
     for (int bb = tid; bb < p.B; bb += kThreads) {
       int P_;
@@ -132,15 +142,17 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     ksrc[key] = src;
     kdst[key] = dst;
   }
-  __syncthreads();  // also publishes ksrc / kdst
-  const long long tot = (scan[0] + scan[1] + scan[2] + scan[3]) * p.n_hg;
-  const long long before = scan[4] + scan[5] + scan[6] + scan[7];
-  long long W = (tot + p.n_stream - 1) / p.n_stream;
-  if (W < p.w_min) W = p.w_min;
-  const long long off = before * p.n_hg + static_cast<long long>(sg.hg) * sg.len;
-  const long long c_first = off / W, c_last = (off + sg.len - 1) / W;
-  const long long npc = c_last - c_first + 1;  // pieces of the segment
-  const long long slot0 = c_first + s_idx;  // partial of piece i, this head: (slot0 + i) HC + hc
+  sync();  // also publishes ksrc / kdst
+  if constexpr (!CL) {
+    const long long tot = (scan[0] + scan[1] + scan[2] + scan[3]) * p.n_hg;
+    const long long before = scan[4] + scan[5] + scan[6] + scan[7];
+    long long W = (tot + p.n_stream - 1) / p.n_stream;
+    if (W < p.w_min) W = p.w_min;
+    const long long off = before * p.n_hg + static_cast<long long>(sg.hg) * sg.len;
+    const long long c_first = off / W, c_last = (off + sg.len - 1) / W;
+    npc = c_last - c_first + 1;  // pieces of the segment
+    slot0 = c_first + s_idx;     // partial of piece i, this head: (slot0 + i) HC + hc
+  }
 
   // ---- stage the draft K rows (whole head dimension) and this slice of V ----
   // Plain drafts (k_extend / v_extend, no store) go by cp.async and land while
@@ -237,6 +249,13 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     load_q<KSW>(p, sg, hc, r0, r0 + 8, j, false, qf, DW * warp);
   }
 
+  // Everything above reads only the call's inputs.  The combine kernel is
+  // launched as a programmatic dependent of the stream launch, so it may have
+  // started while the stream still runs: wait for that grid to complete (and
+  // its partials to be visible) before reading them.  Without such a launch
+  // the wait returns at once.
+  if constexpr (!CL) asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // ---- fold: warp w takes pieces w, w + 4, ...; lane = (row, 16 columns) ----
   const int fr = lane >> 1, fc = (lane & 1) * 16;
   float fm = NEG_INF, fl = 0.f, fa[16];
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     *reinterpret_cast<float4*>(sm_a + fr * kCols + fc + 4 * k) =
         make_float4(fa[4 * k], fa[4 * k + 1], fa[4 * k + 2], fa[4 * k + 3]);
   cp_async_wait<0>();
-  __syncthreads();  // staged drafts, fold partials
+  sync();  // staged drafts, fold partials
 
   // ---- draft scores: this warp's DW-wide part of q . k for every 8-key group ----
   float* scp = reinterpret_cast<float*>(smem + kScOff) + warp * 16 * kScPitch;
@@ -307,7 +326,7 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     scp[(g + 8) * kScPitch + nt * 8 + 2 * j] = sd[2];
     scp[(g + 8) * kScPitch + nt * 8 + 2 * j + 1] = sd[3];
   }
-  __syncthreads();
+  sync();
 
   // ---- per thread: row r of the tile, 4 output columns ----
   const int r = tid >> 3, c4 = (tid & 7) * 4;
@@ -384,4 +403,15 @@ __global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid
     *reinterpret_cast<uint32_t*>(op) = pack_bf16(acc[0] * inv, acc[1] * inv);
     *reinterpret_cast<uint32_t*>(op + 2) = pack_bf16(acc[2] * inv, acc[3] * inv);
   }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(cmb::kThreads) vsk_combine_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int kSlices = cmb::Geo<D>::kSlices;
+  const int ch = static_cast<int>(blockIdx.x % kSlices);
+  const int tile = static_cast<int>((blockIdx.x / kSlices) % p.MT);
+  const int hc = static_cast<int>((blockIdx.x / (kSlices * p.MT)) % p.HC);
+  const long long s_idx = static_cast<long long>(blockIdx.x) / (kSlices * p.MT * p.HC);
+  combine_unit<D, FP8, false>(p, smem, static_cast<int>(threadIdx.x), 0, s_idx, hc, tile, ch, 0, 0);
 }

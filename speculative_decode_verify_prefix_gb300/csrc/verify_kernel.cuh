@@ -60,6 +60,10 @@ constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_di
 constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
 constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
 constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... up to which they do (at most 16 packed rows)
+constexpr long long kClMaxWork = 2047;  // prefix tokens x KV heads up to which calls take the cluster form
+constexpr long long kClMaxSeg = 512;         // ... with at most this many (sequence, KV head) segments
+constexpr long long kClTokensPerCta = 64;    // prefix tokens per CTA the cluster size aims at
+constexpr int kClMax = 16;                   // CTAs per cluster at most (8 where 16 do not fit an SM group)
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
@@ -110,6 +114,8 @@ struct Params {
   float kq, vq;       // dequantisation scales the stored codes are divided by
   long long w_min;
   int n_stream;  // CTAs of the stream launch (read by the combine kernel of the two-launch forms)
+  int cl;        // cluster form: CTAs per cluster (one cluster per segment); 0 otherwise
+  int cl_smem;   // cluster form: shared-memory bytes of one combine group (128 threads)
   const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
   const void* mindptr;
   int mindptr64;
@@ -517,6 +523,54 @@ __device__ __forceinline__ bool cta_share(const Params& p, unsigned char* smem, 
   return true;
 }
 
+#include "verify_combine.cuh"
+
+// ---------------------------------------------------------------------------
+// Cluster form: one thread-block cluster per segment (b, hg), of p.cl CTAs.
+// CTA r of the cluster streams tokens [r w, r w + w) of the segment, w = the
+// segment's (virtual) length over p.cl in whole stages, and writes its
+// partial to slot k (p.cl + 1) + r (k = the cluster, the segment's index);
+// after the cluster barrier the cluster's CTAs fold the segment's pieces,
+// add the draft block and write o (the combine, in the same launch).  Every
+// thread calls it; false: this CTA streams nothing (it still joins the
+// barrier and the combine).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool cluster_share(const Params& p, long long& start, long long& end, Seg& seg0,
+                                              long long& slot0, long long& npc) {
+  // (also called after streaming, for slot0 / npc alone: recomputing them is
+  // cheaper than keeping them in registers across the stream)
+  const int C = p.cl;
+  const long long k = blockIdx.x / C;
+  const int r = static_cast<int>(blockIdx.x % C);
+  seg0.b = static_cast<int>(k / p.n_hg);
+  seg0.hg = static_cast<int>(k % p.n_hg);
+  const bool ok = seq_info(p, seg0.b, seg0.P, seg0.kv0);
+  if (!ok && r == 0 && seg0.hg == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadKvIndptr);
+  seg0.len = max(seg0.P, 1);
+  seg0.off = 0;
+  long long w = (seg0.len + C - 1) / C;
+  w = (w + kStageTokens - 1) / kStageTokens * kStageTokens;
+  npc = (seg0.len + w - 1) / w;
+  slot0 = k * (C + 1);
+  start = r * w;
+  end = min(static_cast<long long>(seg0.len), start + w);
+  return start < seg0.len;
+}
+
+// The cluster form's combine unit as a call of its own: its registers are
+// allocated apart from the stream's, which are dead by then.
+template <int D, bool FP8>
+__device__ __noinline__ void combine_unit_cl(const Params& p, unsigned char* smem, int tid, int bar, long long s_idx,
+                                             int hc, int tile, int ch, long long slot0, long long npc) {
+  combine_unit<D, FP8, true>(p, smem, tid, bar, s_idx, hc, tile, ch, slot0, npc);
+}
+
+// Every thread of every CTA of the cluster: what each wrote to global memory
+// before is visible to all of them after (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // Shared memory map (bytes):
@@ -550,7 +604,9 @@ struct MaxOf {
 // scaled partial scores through shared memory) and own half of the output
 // columns each.  Half the accumulator registers per warp, so three CTAs per SM.
 // DV: the value head_dim (output columns), D the query / key head_dim.
-template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D>
+// CL: the cluster form (stream only, then the combine of the segment by the
+// cluster's CTAs after a cluster barrier; one launch, no tickets).
+template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D, bool CL = false>
 __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -560,6 +616,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   static_assert(CS == 1 || (CS == 2 && D == 256 && DV == 256 && MTW == 1 && SO),
                 "column split: head_dim 256 stream only");
   static_assert(D == DV || (MTW == 1 && CS == 1 && !SO), "head_dim != v_head_dim: one-launch kernel, one tile per warp");
+  static_assert(!CL || (SO && MTW == 1 && D == DV), "cluster form: stream-only, one tile per warp");
   constexpr int DH = D / CS;       // contraction length of one warp
   constexpr int DVH = DV / CS;     // output columns of one warp
   constexpr int NTH = NT / CS;     // its n-tiles
@@ -577,10 +634,24 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + 16);  // [2]
   const int nst = p.nst;
 
+  // The stream-only launches are followed by the combine kernel, launched as
+  // a programmatic dependent: let it start (its prologue reads only the
+  // call's inputs; it waits for this grid before reading any partial).
+  if constexpr (SO && !CL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- prologue: this CTA's share of the flattened space and its first segment ----
-  long long start, end, W;
+  long long start = 0, end = 0, W = 0;
   Seg seg0;
-  if (!cta_share(p, smem, start, end, W, seg0)) return;  // uniform: the whole CTA has no work
+  if constexpr (CL) {
+    long long slot0_, npc_;
+    // no range (start = end = 0: the stream loop below does nothing) for a
+    // CTA past the segment's end
+    if (!cluster_share(p, start, end, seg0, slot0_, npc_)) {
+      start = 0;
+      end = 0;
+    }
+  } else {
+    if (!cta_share(p, smem, start, end, W, seg0)) return;  // uniform: the whole CTA has no work
+  }
 
   // ============================ per-warp pipeline ============================
   // Warp w serves KV head hc = w / WPH of the group and MTW 16-row tiles
@@ -592,7 +663,12 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   // ring.
   const int WPH = p.MT / MTW;  // warp groups per KV head; each owns MTW 16-row tiles
   const int WPHC = WPH * CS;   // warps per KV head
-  const int hc = warp / WPHC;
+  // Cluster form at head_dim <= 128: warps beyond the streaming ones are
+  // there only for the combine (it takes four); they take head HC - 1's
+  // indices and issue no copy.  (The head_dim 256 cluster form streams with
+  // all four warps.)  The range itself stays uniform across the CTA.
+  const int hc = (CL && CS == 1) ? min(warp / WPHC, p.HC - 1) : warp / WPHC;
+  const bool streamer = !(CL && CS == 1) || warp < p.nwc;
   const int mt = (warp / CS) % WPH;
   const int csi = CS == 2 ? (warp & 1) : 0;  // column half of this warp
   const int cw = warp % WPHC;                // this warp's share of the head's copies
@@ -619,7 +695,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   {
   int dslot = 0;  // ring slot of the next data job (job % nst, kept without a division)
   auto issue_idx = [&](const StageIt& it, long long job) {
-    if (it.valid && lane < min(kStageTokens, it.te - it.tok)) {
+    if (streamer && it.valid && lane < min(kStageTokens, it.te - it.tok)) {
       const long long n = it.s.kv0 + it.tok + lane;
       const uint32_t dst = idx_s + static_cast<uint32_t>(job % kIdxRing) * 128u + lane * 8u;
       if (p.paged)  // page id of cache position tok + lane
@@ -631,7 +707,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
     }
   };
   auto issue_data = [&](const StageIt& it, long long job) {
-    if (!it.valid) return;
+    if (!streamer || !it.valid) return;
     const int n = min(kStageTokens, it.te - it.tok);
     const unsigned char* ie = idx_ring + static_cast<int>(job % kIdxRing) * 128;
     long long myloc = -1;
@@ -699,13 +775,13 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
         constexpr int CP = RB / 16;
         constexpr int LP = CP < 32 ? CP : 32;
         constexpr int TS = 32 / LP;
-        constexpr int CL = CP / LP;
+        constexpr int NCL = CP / LP;
         const int cl = lane % LP;
         auto one = [&](int t, long long loc) {
           const bool v = (mask >> t) & 1u;
           const unsigned char* src = v ? base + loc * s0 : reinterpret_cast<const unsigned char*>(p.q);
 #pragma unroll
-          for (int cj = 0; cj < CL; ++cj) {
+          for (int cj = 0; cj < NCL; ++cj) {
             const int cir = cl + LP * cj;
             const uint32_t d = region + static_cast<uint32_t>(t * RB + (cir ^ chunk_swz<CP>(t)) * 16);
             cp_async_16_zfill(d, v ? src + cir * 16 : src, v, pol);
@@ -838,7 +914,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   int kslot = 0;  // ring slot of stage k (k % nst, kept without a division)
 
 #pragma unroll 1
-  while (seg_live(p, s, end)) {
+  while (streamer && seg_live(p, s, end)) {
     const int t0 = static_cast<int>(max(start, s.off) - s.off);
     const int te = piece_real_end(s, end);
     float acc[MTW][NTH][4];  // this warp's output columns
@@ -1133,6 +1209,29 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   }  // streaming
   if constexpr (SO) {
     cp_async_wait<0>();  // stream only: the partials are folded by the combine kernel
+    if constexpr (CL) {
+      // the cluster's pieces are all written: fold them here, 128 threads per
+      // (KV head, 16-row tile, 32-column slice) unit, the ring region reused
+      // as each group's shared memory
+      cluster_sync_all();
+      long long cl_slot0, cl_npc, s_, e_;
+      Seg g_;
+      cluster_share(p, s_, e_, g_, cl_slot0, cl_npc);
+      constexpr int kSl = cmb::Geo<D>::kSlices;
+      const int C = p.cl;
+      const int rank = static_cast<int>(blockIdx.x % C);
+      const long long k_seg = blockIdx.x / C;
+      const int units = p.HC * p.MT * kSl;
+      const int groups = static_cast<int>(blockDim.x) / cmb::kThreads;
+      const int gid = warp / (cmb::kThreads / 32);
+      unsigned char* gsm = smem + gid * p.cl_smem;
+#pragma unroll 1
+      for (int u = rank + C * gid; u < units; u += C * groups) {
+        const int ch = u % kSl, tile = (u / kSl) % p.MT, hcu = u / (kSl * p.MT);
+        combine_unit_cl<D, FP8>(p, gsm, tid % cmb::kThreads, 12 + gid, k_seg, hcu, tile, ch, cl_slot0, cl_npc);
+        named_bar_sync(12 + gid, cmb::kThreads);  // the group's shared memory is reused by its next unit
+      }
+    }
   } else {
 
   // ================= epilogue: tickets, log-sum-exp merges, drafts, output =================
@@ -1568,16 +1667,17 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
 }
 
 #include "verify_tc.cuh"
-#include "verify_combine.cuh"
 
 // Kernel entry points, instantiated per head_dim in vsk_inst_*.cu (nullptr:
 // not built).
 using KernelFn = void (*)(Params);
 // head_dim 64 / 128 (D = Dv): the one-launch kernel (so = false) or the
-// stream-only kernel of the two-launch form (so = true), with 1 or 2 tiles per warp
-KernelFn kernel_d64(bool fp8, int mtw, bool so);
-KernelFn kernel_d128(bool fp8, int mtw, bool so);
-// head_dim 256 (D = Dv): one-launch kernel (variant 0) or column-split stream (variant 1)
+// stream-only kernel of the two-launch form (so = true), with 1 or 2 tiles
+// per warp; cl = true: the cluster form (one tile per warp)
+KernelFn kernel_d64(bool fp8, int mtw, bool so, bool cl = false);
+KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl = false);
+// head_dim 256 (D = Dv): one-launch kernel (variant 0), column-split stream
+// (variant 1) or the cluster form streaming by column split (variant 2)
 KernelFn kernel_d256(bool fp8, int variant);
 // tensor-memory stream, head_dim 256, rm = 16 or 32 packed rows
 KernelFn kernel_tc(bool fp8, int rm);

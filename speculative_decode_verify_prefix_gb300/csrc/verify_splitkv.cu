@@ -45,6 +45,8 @@ int g_tiles = 0;  // tiles per warp override (0 = default)
 int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
+int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
+int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
 
 struct Plan {
   int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
@@ -64,7 +66,7 @@ int floor_pow2(int x) {
 // than one tile, so its K / V fragments feed both); ring depth from the
 // shared-memory budget.  DV: the value head_dim (0: the same as D).
 bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8, Plan& pl,
-               long long total_tokens, int tiles, long long DV = 0) {
+               long long total_tokens, int tiles, long long DV = 0, int hc_cap = 0) {
   if (DV == 0) DV = D;
   if (h_kv <= 0 || h_q % h_kv != 0) return fail("h_q (%lld) must be a positive multiple of h_kv (%lld)", h_q, h_kv);
   const long long R = (h_q / h_kv) * L;
@@ -83,8 +85,8 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   pl.MTW = (DM <= 128 && D == DV && mt >= 2 && tiles == 2) ? 2 : 1;
   const int wph = mt / pl.MTW;  // warps per head
   int hc = 1;
-  const int hc_cap = g_max_heads > 0 ? g_max_heads : maxw;
-  while (hc * 2 * wph <= maxw && hc * 2 <= hc_cap && h_kv % (hc * 2) == 0) hc *= 2;
+  const int hcc = hc_cap > 0 ? hc_cap : (g_max_heads > 0 ? g_max_heads : maxw);
+  while (hc * 2 * wph <= maxw && hc * 2 <= hcc && h_kv % (hc * 2) == 0) hc *= 2;
   pl.HC = hc;
   pl.n_hg = static_cast<int>(h_kv / hc);
   pl.nwc = hc * wph;
@@ -185,6 +187,19 @@ bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long l
   const long long cap = (h_q / h_kv) * L <= 16 ? kSplitLaunchMaxWork16 : kSplitLaunchMaxWork;
   return work >= kSplitLaunchMinWork && work <= cap;
 }
+// Cluster form (one launch: one thread-block cluster per (sequence, KV head)
+// segment streams it, then folds its pieces, adds the draft block and writes
+// o after a cluster barrier; no tickets, no second launch): small calls,
+// where the latency of the other forms' chains of launches and memory round
+// trips is what the call costs.  At most cmb::kMaxL drafts, head_dim ==
+// v_head_dim, from static shapes.
+bool cl_eligible(long long B, long long h_q, long long h_kv, long long D, long long DV, long long L,
+                 long long total_tokens) {
+  if (g_cl == 0 || D != DV || h_kv <= 0 || h_q % h_kv != 0 || L > cmb::kMaxL || B * h_kv > kClMaxSeg) return false;
+  if (D == 256 && (h_q / h_kv) * L > 32) return false;  // head_dim 256 streams by column split: <= 32 rows
+  return g_cl == 2 || total_tokens * h_kv <= kClMaxWork;
+}
+
 struct StreamPlan {
   int threads, nst, ring_off, head_bytes, misc_off, misc_bytes, per_sm;
   size_t smem;
@@ -516,11 +531,18 @@ void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode 
 
 void vsk_set_tuning_split_launch(int mode) { g_sl = (mode == 0 || mode == 2) ? mode : 1; }
 
+void vsk_set_tuning_cluster(int mode) { g_cl = (mode == 0 || mode == 2) ? mode : 1; }
+
+void vsk_set_tuning_pdl(int mode) { g_pdl = mode == 0 ? 0 : 1; }
+
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens) {
   if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
   const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
+  if (!tc_eligible(h_q, h_kv, head_dim, max_len_extend) &&
+      cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens))
+    return 1;
   return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) ||
           cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens) ||
           sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
@@ -548,7 +570,8 @@ namespace vsk {
 // scratch of the allocation-free entry point) is checked against is the one
 // the kernels use.
 struct CallPlan {
-  bool use_tc = false, use_cs = false, use_sl = false;
+  bool use_tc = false, use_cs = false, use_sl = false, use_cl = false;
+  int cl = 0, cl_smem = 0;  // cluster form: CTAs per cluster, shared memory of one combine group
   Plan pl{};
   StreamPlan sp{};
   KernelFn fn = nullptr, fn_comb = nullptr;
@@ -563,17 +586,31 @@ struct CallPlan {
 static int plan_call(long long B, long long h_q, long long h_kv, long long D, long long DV, long long L, bool fp8,
                      long long mean_len, CallPlan& cp) {
   cp.D = static_cast<int>(D);
-  // the two-launch forms are built for head_dim == v_head_dim only
+  // the two-launch forms and the cluster form are built for head_dim == v_head_dim only
   const bool same = D == DV;
   cp.use_tc = same && tc_eligible(h_q, h_kv, D, L);
-  cp.use_cs = same && !cp.use_tc && cs_eligible(h_q, h_kv, D, L, mean_len * B);
-  cp.use_sl = same && !cp.use_tc && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_cl = !cp.use_tc && cl_eligible(B, h_q, h_kv, D, DV, L, mean_len * B);
+  cp.use_cs = same && !cp.use_tc && !cp.use_cl && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_sl = same && !cp.use_tc && !cp.use_cl && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan& pl = cp.pl;
-  if ((cp.use_tc || cp.use_cs)
-          ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
-          : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
-                       cp.use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0, DV))
+  if (cp.use_cl && D == 256) {
+    // one KV head per cluster, streamed by the column split (two warps per
+    // tile) in two 16-row tiles whatever the packed rows (the second empty at
+    // <= 16): all four warps stream, the four the combine takes
+    if (!make_tc_plan(h_q, h_kv, D, L, fp8, pl)) return 0;
+    pl.MT = 2;
+    pl.nwc = 2;
+    pl.threads = 64;
+    if (!make_cs_stream_plan(pl, D, fp8, cp.sp)) return 0;
+  } else if (cp.use_cl) {
+    // one KV head per cluster, one 16-row tile per warp
+    if (!make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 1, DV, 1)) return 0;
+  } else if ((cp.use_tc || cp.use_cs)
+                 ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
+                 : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
+                              cp.use_sl && g_tiles == 0 ? (mean_len * B >= kSplitTwoTileMinTokens ? 2 : 1) : 0, DV)) {
     return 0;
+  }
   if (cp.use_cs && !make_cs_stream_plan(pl, D, fp8, cp.sp)) return 0;
   cudaError_t e = cudaGetDevice(&cp.dev);
   if (e != cudaSuccess) return fail("cudaGetDevice: %s", cudaGetErrorString(e));
@@ -604,6 +641,46 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     cp.threads = cp.sp.threads;
     cp.smem = cp.sp.smem;
     per_sm = cp.sp.per_sm;
+  } else if (cp.use_cl) {
+    cp.fn = D == 64 ? kernel_d64(fp8, 1, true, true) : D == 128 ? kernel_d128(fp8, 1, true, true) : kernel_d256(fp8, 2);
+    if (!cp.fn || !prepare_kernel(cp.fn)) return fail("cluster-form kernel for head_dim %lld unavailable", D);
+    // at least one 128-thread combine group; the ring region is reused as the
+    // groups' shared memory after streaming
+    const int nw = D == 256 ? cp.sp.threads / 32 : pl.nwc;  // streaming warps
+    const int groups = std::max(nw, 4) / 4;
+    cp.threads = groups * cmb::kThreads;
+    cp.cl_smem = (combine_smem(static_cast<int>(D)) + 127) & ~127;
+    // every warp of the CTA (streaming or not) has its index / mask / query region
+    const size_t misc_end = D == 256 ? static_cast<size_t>(cp.sp.misc_off) + 4 * groups * cp.sp.misc_bytes
+                                     : static_cast<size_t>(pl.misc_off) + 4 * groups * pl.misc_bytes;
+    cp.smem = std::max({D == 256 ? cp.sp.smem : cp.smem, misc_end, static_cast<size_t>(groups) * cp.cl_smem});
+    if (cp.smem > static_cast<size_t>(kSmemPerCTAMax)) return fail("cluster-form shared memory plan too large");
+    const long long n_seg = B * pl.n_hg;
+    long long c = (mean_len + kClTokensPerCta - 1) / kClTokensPerCta;
+    c = std::max(1LL, std::min<long long>(c, kClMax));
+    while (c > 1 && n_seg * c > 4LL * sms) --c;  // the workspace bound: at most 4 CTAs per SM
+    if (c > 8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(cp.fn),
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      c = 8;
+    for (;; c = c > 8 ? 8 : c - 1) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = static_cast<unsigned>(c);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(c));
+      cfg.blockDim = dim3(cp.threads);
+      cfg.dynamicSmemBytes = cp.smem;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int ncl = 0;
+      const cudaError_t ce = cudaOccupancyMaxActiveClusters(&ncl, reinterpret_cast<const void*>(cp.fn), &cfg);
+      if (ce == cudaSuccess && ncl >= 1) break;
+      cudaGetLastError();  // clear the error the query left
+      if (c == 1) return fail("cluster-form kernel does not fit (%s)", cudaGetErrorString(ce));
+    }
+    cp.cl = static_cast<int>(c);
   } else if (cp.use_sl) {
     cp.fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW);
     cp.fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
@@ -618,7 +695,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(cp.fn), cp.threads, cp.smem);
   if (e != cudaSuccess || occ < 1) return fail("kernel does not fit an SM (%s)", cudaGetErrorString(e));
   per_sm = std::min(occ, per_sm);
-  cp.n_cta = g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
+  cp.n_cta = cp.use_cl ? B * pl.n_hg * cp.cl : g_num_ctas > 0 ? g_num_ctas : static_cast<long long>(sms) * per_sm;
   cp.wl = ws_layout(cp.n_cta, B, pl, DV);
   if (cp.fn_comb) {
     // one combine CTA per (segment, 16-row tile, 32-column slice)
@@ -633,7 +710,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   if (g_min_tokens > 0) {
     cp.w_min = g_min_tokens;
   } else {
-    const long long per = (cp.use_cs || cp.use_sl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
+    const long long per = (cp.use_cs || cp.use_sl || cp.use_cl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
     const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
     cp.w_min = std::max(kDefaultMinTokens, wp);
   }
@@ -671,7 +748,9 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
   p.plse = reinterpret_cast<float*>(ws + cp.wl.lse_off);
   p.po = reinterpret_cast<float*>(ws + cp.wl.o_off);
   p.n_stream = static_cast<int>(cp.n_cta);
-  if (cp.use_cs) {
+  p.cl = cp.use_cl ? cp.cl : 0;
+  p.cl_smem = cp.cl_smem;
+  if (cp.use_cs || (cp.use_cl && cp.D == 256)) {  // the column-split stream
     p.nwc = 2 * pl.MT;
     p.nst = cp.sp.nst;
     p.ring_off = cp.sp.ring_off;
@@ -685,14 +764,42 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
     if (e != cudaSuccess) return fail("cudaMemsetAsync of the ticket region: %s", cudaGetErrorString(e));
   }
   void* args[] = {&p};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(cp.fn), dim3(static_cast<unsigned>(cp.n_cta)), dim3(cp.threads),
-                       args, cp.smem, st);
+  if (cp.use_cl) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(cp.cl);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(cp.n_cta));
+    cfg.blockDim = dim3(cp.threads);
+    cfg.dynamicSmemBytes = cp.smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(cp.fn), args);
+  } else {
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(cp.fn), dim3(static_cast<unsigned>(cp.n_cta)), dim3(cp.threads),
+                         args, cp.smem, st);
+  }
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
   if (cp.fn_comb) {
     // the share floor and n_stream let the combine kernel find the pieces the
-    // stream launch wrote
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(cp.fn_comb), dim3(static_cast<unsigned>(cp.n_comb)),
-                         dim3(cmb::kThreads), args, combine_smem(cp.D), st);
+    // stream launch wrote.  With vsk_set_tuning_pdl(1) it is launched as a
+    // programmatic dependent of the stream: its CTAs may start (and read the
+    // call's inputs) before the stream ends, and wait for it before reading
+    // the partials (measured slower than plain stream order on mid-size calls).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(cp.n_comb));
+    cfg.blockDim = dim3(cmb::kThreads);
+    cfg.dynamicSmemBytes = combine_smem(cp.D);
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = g_pdl ? 1 : 0;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(cp.fn_comb), args);
     if (e != cudaSuccess) return fail("combine kernel launch failed: %s", cudaGetErrorString(e));
   }
   return 1;

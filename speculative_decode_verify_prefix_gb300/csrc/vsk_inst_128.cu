@@ -4,7 +4,9 @@
 
 namespace vsk {
 
-KernelFn kernel_d128(bool fp8, int mtw, bool so) {
+KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl) {
+  if (cl) return fp8 ? static_cast<KernelFn>(vsk_kernel<128, true, 1, 1, true, 128, true>)
+                     : static_cast<KernelFn>(vsk_kernel<128, false, 1, 1, true, 128, true>);
   if (so) {
     if (mtw == 2) return fp8 ? static_cast<KernelFn>(vsk_kernel<128, true, 2, 1, true>)
                              : static_cast<KernelFn>(vsk_kernel<128, false, 2, 1, true>);

@@ -246,9 +246,23 @@ def test_launches_per_call_follows_the_form_switches():
     KV heads (mode 1), always (mode 2) or never (mode 0); the tensor-memory
     switch takes precedence.  Head_dim 64 / 128 with at most 32 drafts takes the
     stream-only kernel plus the combine launch inside its own size window.
+    The cluster form (one launch) takes small calls first when it is on.
     Everything else is one launch."""
     f = vsk.launches_per_call
     try:
+        vsk.set_tuning_cluster(1)
+        # the cluster form (one launch): fewer than 2,048 token-heads, at most 512 segments
+        assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
+        assert f(4, 16, 2, 128, 4, 1020) == 1                       # 2,040 token-heads
+        assert f(4, 16, 2, 128, 4, 1028) == 2                       # 2,056: stream + combine
+        assert f(3, 16, 2, 256, 4, 1536) == 2                       # 3,072: column split + combine
+        assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128 at head_dim 256: one-launch kernel
+        assert f(300, 16, 2, 128, 4, 3000) == 2                     # 600 segments: past 512
+        vsk.set_tuning_cluster(2)
+        assert f(3, 16, 2, 256, 4, 1536) == 1                       # mode 2: wherever it applies
+        assert f(64, 32, 8, 128, 4, 64 * 20000) == 1
+        assert f(2, 64, 2, 256, 4, 100) == 1                        # (one-launch kernel: R = 128 at 256)
+        vsk.set_tuning_cluster(0)
         vsk.set_tuning_colsplit(1)
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1                 # head_dim 128
         assert f(3, 16, 2, 256, 4, 1536) == 2                       # R = 32, 3,072 token-heads
@@ -282,6 +296,7 @@ def test_launches_per_call_follows_the_form_switches():
         vsk.set_tuning_tc(False)
         vsk.set_tuning_colsplit(1)
         vsk.set_tuning_split_launch(1)
+        vsk.set_tuning_cluster(1)
     assert f(0, 16, 2, 256, 4, 10) == 0                             # no sequences
     assert f(2, 15, 2, 256, 4, 10) == 0                             # h_q not a multiple of h_kv
     assert f(2, 16, 2, 96, 4, 10) == 0                              # head_dim not built

@@ -6,10 +6,14 @@ beside each:
 - "colsplit": the column-split mma.sync stream (two warps per 16-row query
   tile, each holding half the head dimension), head_dim 256;
 - "split": the stream-only mma.sync kernel at head_dim 64 and 128 (every case
-  below rewritten to one of them, chosen by a hash of its name).
+  below rewritten to one of them, chosen by a hash of its name);
+- "cluster": the cluster form (one launch: a thread-block cluster per
+  (sequence, KV head) streams it and folds its own partials after a cluster
+  barrier), at head_dim 64, 128 or 256 (chosen by a hash of the case's name).
 
 All serve at most 32 packed query rows per KV head (head_dim 256) or 32 drafts
-(64 / 128) and fold their partials in a second launch.  Same tolerance as the other parity tests
+(64 / 128) and fold their partials after the stream: in a second launch, or
+(the cluster form) in the same one.  Same tolerance as the other parity tests
 (atol 2e-2, rtol 1e-2 on the bf16 output); stored cache codes and repeated /
 graph-replayed calls are compared bit for bit.  Every call also checks the
 device error word, whose timeout bit would report a pipeline wait that gave up.
@@ -35,10 +39,14 @@ FORM = {"name": "tc"}
 
 def _adapt(spec):
     """The case as the form under test serves it: the "split" form runs it at
-    head_dim 64 or 128."""
-    if FORM["name"] != "split":
+    head_dim 64 or 128, the "cluster" form at 64, 128 or 256."""
+    h = zlib.crc32(spec.name.encode()) % 3
+    if FORM["name"] == "split":
+        d = 64 if h == 0 else 128
+    elif FORM["name"] == "cluster":
+        d = (64, 128, 256)[h]
+    else:
         return spec
-    d = 64 if zlib.crc32(spec.name.encode()) % 3 == 0 else 128
     return workloads.replace(spec, d=d, dv=d)
 
 
@@ -50,9 +58,10 @@ def _select(m, form):
     m.set_tuning_tc(form == "tc")
     m.set_tuning_colsplit(2 if form == "colsplit" else 0)
     m.set_tuning_split_launch(2 if form == "split" else 0)
+    m.set_tuning_cluster(2 if form == "cluster" else 0)
 
 
-@pytest.fixture(scope="module", params=["tc", "colsplit", "split"])
+@pytest.fixture(scope="module", params=["tc", "colsplit", "split", "cluster"])
 def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 
@@ -65,6 +74,7 @@ def vsk(request):
     m.set_tuning_tc(False)
     m.set_tuning_colsplit(1)
     m.set_tuning_split_launch(1)
+    m.set_tuning_cluster(1)
     FORM["name"] = "tc"
 
 
@@ -328,6 +338,26 @@ def test_form_poisoned_unreferenced_slots(vsk):
     p = gpu_problem(spec)
     check(run_gpu(vsk, p), oracle_o(p))
     assert vsk.read_error_flags() == 0
+
+
+@pytest.mark.parametrize("spec", TC[:4] + TC[9:10], ids=lambda s: s.name)
+def test_form_with_programmatic_dependent_launch(vsk, spec):
+    """The two-launch forms with the combine kernel launched as a
+    programmatic dependent of the stream (it starts early and waits for the
+    stream grid before reading partials): the same result as in stream order."""
+    p = gpu_problem(spec)
+    vsk.read_error_flags()
+    a = run_gpu(vsk, p)
+    vsk.set_tuning_pdl(True)
+    try:
+        b = run_gpu(vsk, p)
+        c = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning_pdl(False)
+    assert vsk.read_error_flags() == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+    check(b, oracle_o(p))
 
 
 def test_form_out_of_range_index_is_flagged_not_read(vsk):

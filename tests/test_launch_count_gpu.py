@@ -25,6 +25,7 @@ def vsk():
     yield m
     m.set_tuning_colsplit(1)
     m.set_tuning_split_launch(1)
+    m.set_tuning_cluster(1)
 
 
 def _kernels_of_one_call(vsk, p):
@@ -42,20 +43,23 @@ def _kernels_of_one_call(vsk, p):
 
 
 CASES = [
-    # (spec, colsplit mode, split-launch mode)
-    (workloads.TINY, 1, 1),                                                   # tiny: one launch
-    (workloads.D256, 1, 1),                                                   # column split + combine
-    (workloads.D256, 0, 1),                                                   # forced one launch
-    (S("lc_gqa", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 1),  # stream + combine
-    (S("lc_gqa_one", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 0),
+    # (spec, colsplit mode, split-launch mode, cluster mode)
+    (workloads.TINY, 1, 1, 1),                                                # tiny: the cluster form, one launch
+    (workloads.TINY, 1, 1, 0),                                                # tiny without it: one launch
+    (workloads.D256, 1, 1, 1),                                                # the cluster form
+    (workloads.D256, 1, 1, 0),                                                # column split + combine
+    (workloads.D256, 0, 1, 0),                                                # forced one launch
+    (S("lc_gqa", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 1, 0),  # stream + combine
+    (S("lc_gqa_one", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 0, 0),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}_cs{c[1]}_sl{c[2]}")
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}_cs{c[1]}_sl{c[2]}_cl{c[3]}")
 def test_reported_launches_match_the_profiled_kernels(vsk, case):
-    spec, cs, sl = case
+    spec, cs, sl, cl = case
     vsk.set_tuning_colsplit(cs)
     vsk.set_tuning_split_launch(sl)
+    vsk.set_tuning_cluster(cl)
     p = gpu_problem(spec)
     B = len(p["prefix_lens"])
     want = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, p["max_len_extend"], p["kv_indices"].shape[0])

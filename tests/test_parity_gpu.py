@@ -232,13 +232,15 @@ def test_poisoned_unreferenced_slots(vsk):
 def test_split_count_independence(vsk, num_ctas, min_tok):
     spec = workloads.Spec("splits", (2000, 5, 0, 777, 64), 4, 16, 4, 128, 128, perm=True, seed=113)
     p = gpu_problem(spec)
-    vsk.set_tuning(0, 0)
-    base = run_gpu(vsk, p).float()
-    vsk.set_tuning(num_ctas, min_tok)
+    vsk.set_tuning_cluster(0)  # the forms whose split the CTA count sets
     try:
+        vsk.set_tuning(0, 0)
+        base = run_gpu(vsk, p).float()
+        vsk.set_tuning(num_ctas, min_tok)
         o = run_gpu(vsk, p)
     finally:
         vsk.set_tuning(0, 0)
+        vsk.set_tuning_cluster(1)
     check(o, oracle_o(p))
     assert (o.float() - base).abs().max().item() < 1e-3 * 8  # a few bf16 ulps at |o| < 1
 
@@ -467,11 +469,13 @@ def test_paged_bf16_unit_scales_is_bitwise_the_flat_path(vsk):
     spec = workloads.Spec("paged_vs_flat", (900, 3, 0, 2500), 4, 32, 8, 128, 128, perm=True, page_size=16, seed=307)
     p = gpu_problem(spec)
     vsk.set_tuning(0, 256)  # the same split for both (their default floors come from different static shapes)
+    vsk.set_tuning_cluster(0)  # (the cluster form sizes its clusters from the static shapes too)
     try:
         a = run_paged(vsk, p)
         b = run_gpu(vsk, p)
     finally:
         vsk.set_tuning(0, 0)
+        vsk.set_tuning_cluster(1)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
@@ -481,10 +485,12 @@ def test_paged_split_count_independence(vsk):
     ref = oracle_o(p)
     for n in (1, 7, 1000):
         vsk.set_tuning(n, 16)
+        vsk.set_tuning_cluster(0)  # the forms whose split the CTA count sets
         try:
             o = run_paged(vsk, p)
         finally:
             vsk.set_tuning(0, 0)
+            vsk.set_tuning_cluster(1)
         check(o, ref)
 
 
@@ -654,16 +660,18 @@ def test_one_workspace_serves_calls_of_any_shape(vsk):
         workloads.Spec("ws_c", (2000, 5, 0, 777, 64), 4, 16, 4, 128, 128, perm=True, seed=503),
     ]
     shared = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
-    plan = [(0, 0), (1000, 16), (64, 16), (0, 0), (7, 16), (300, 16)]
-    for i, (nc, mt) in enumerate(plan):
+    plan = [(0, 0, 0), (1000, 16, 0), (64, 16, 0), (0, 0, 1), (7, 16, 0), (300, 16, 0)]
+    for i, (nc, mt, cl) in enumerate(plan):
         for spec in specs:
             p = gpu_problem(spec)
             vsk.set_tuning(nc, mt)
+            vsk.set_tuning_cluster(cl)  # mostly the forms with tickets or a second launch
             try:
                 got = run_gpu(vsk, p, workspace=shared)
                 fresh = run_gpu(vsk, p, workspace=torch.zeros_like(shared))
             finally:
                 vsk.set_tuning(0, 0)
+                vsk.set_tuning_cluster(1)
             assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (i, spec.name)
     assert vsk.read_error_flags(shared) == 0
 
@@ -691,6 +699,7 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     ref = oracle_o(p)
     vsk.set_tuning_split_launch(0)  # the one-launch kernel: the form that draws tickets
     vsk.set_tuning_colsplit(0)
+    vsk.set_tuning_cluster(0)
     try:
         assert vsk.launches_per_call(B, 32, 8, 128, 1, p["kv_indices"].shape[0]) == 1
         pb = gpu_problem(big)
@@ -702,6 +711,7 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     finally:
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_colsplit(1)
+        vsk.set_tuning_cluster(1)
     check(ob, oracle_o(pb), scaled=SCALED)
 
 

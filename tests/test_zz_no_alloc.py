@@ -10,8 +10,8 @@ call and keeping whatever the previous call left.
 These tests call it through the C ABI several times in a row, with problems
 of different shapes and forms in turn (a head_dim 256 e4m3 call served by a
 column-split stream plus a combine launch, a head_dim 128 stream plus combine,
-a one-launch call), so each call runs on what a differently shaped call left
-in the array.  Each result is compared with the fp64 oracle (the page's
+a cluster-form call and a one-launch call with tickets), so each call runs on
+what a differently shaped call left in the array.  Each result is compared with the fp64 oracle (the page's
 tolerance and the magnitude-scaled bound of the other parity tests) and with
 verify_splitkv_fwd given a caller workspace.  The device's free memory must
 not change across the calls.  This file is collected last on purpose.
@@ -89,42 +89,65 @@ def _check(got, ref):
     assert err.max() <= SCALED * np.abs(ref).max(), f"max abs err {err.max():.3e} vs max|ref| {np.abs(ref).max():.3e}"
 
 
-# three shapes and forms, called in turn: each call finds the array as a call
-# of another shape (another workspace layout) left it
+# four shapes and forms, called in turn: each call finds the array as a call
+# of another shape (another workspace layout) left it.  Form switches:
+# (cluster, column split, stream + combine) modes.
 SPECS = [
-    workloads.Spec("noalloc_fp8_d256", (4096, 1500), 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
-                   v_scale=0.25, seed=202),
-    workloads.Spec("noalloc_bf16_d128", (3000, 4000, 10, 0, 777), 4, 32, 8, 128, 128, perm=True, seed=201),
-    workloads.Spec("noalloc_tiny", (64, 96), 4, 4, 1, 64, 64, seed=204),
+    (workloads.Spec("noalloc_fp8_d256", (4096, 1500), 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
+                    v_scale=0.25, seed=202), (0, 1, 1), 2),    # column split + combine
+    (workloads.Spec("noalloc_bf16_d128", (3000, 4000, 10, 0, 777), 4, 32, 8, 128, 128, perm=True, seed=201),
+     (0, 1, 1), 2),                                            # stream + combine
+    (workloads.Spec("noalloc_tiny", (64, 96), 4, 4, 1, 64, 64, seed=204), (1, 1, 1), 1),  # the cluster form
+    (workloads.Spec("noalloc_one_launch", (2500, 33, 700), 4, 16, 2, 128, 128, perm=True, seed=206),
+     (0, 1, 0), 1),                                            # one launch: tickets in the array
 ]
+
+
+def _form(modes):
+    import speculative_decode_verify_prefix_gb300 as vsk
+
+    cl, cs, sl = modes
+    vsk.set_tuning_cluster(cl)
+    vsk.set_tuning_colsplit(cs)
+    vsk.set_tuning_split_launch(sl)
 
 
 def test_noalloc_matches_oracle_across_shapes(lib):
     import speculative_decode_verify_prefix_gb300 as vsk
 
-    probs = [workloads.make_problem(spec, "cuda") for spec in SPECS]
-    launches = [vsk.launches_per_call(len(p["prefix_lens"]), s.h_q, s.h_kv, s.d, s.l_ext, p["kv_indices"].shape[0])
-                for s, p in zip(SPECS, probs)]
-    assert launches == [2, 2, 1]  # column split + combine, stream + combine, one launch
-    refs = [oracle.verify_forward(workloads.to_oracle_arrays(p))["o"] for p in probs]
-    with_ws = [_with_workspace(p).float().cpu().numpy() for p in probs]
-    outs = [torch.empty(p["q"].shape[0], p["q"].shape[1], p["v_ext"].shape[2], dtype=torch.bfloat16,
-                        device="cuda") for p in probs]
-    # one round first: the library's module and kernels are loaded
-    for p, o in zip(probs, outs):
-        assert _noalloc(lib, p, o) == 1, lib.vsk_last_error().decode()
-    torch.cuda.synchronize()
-    for rnd in range(2):
-        for i in (0, 1, 2) if rnd == 0 else (2, 1, 0):
-            outs[i].fill_(float("nan"))
-            torch.cuda.synchronize()
-            free0 = torch.cuda.mem_get_info()[0]
-            assert _noalloc(lib, probs[i], outs[i]) == 1, lib.vsk_last_error().decode()
-            torch.cuda.synchronize()
-            assert torch.cuda.mem_get_info()[0] == free0, "device memory was allocated"
-            _check(outs[i], refs[i])
-            np.testing.assert_allclose(outs[i].float().cpu().numpy(), with_ws[i], atol=ATOL, rtol=RTOL)
-            assert _noalloc_flags(lib) == 0
+    probs = [workloads.make_problem(spec, "cuda") for spec, _, _ in SPECS]
+    try:
+        for (spec, modes, launches), p in zip(SPECS, probs):
+            _form(modes)
+            assert vsk.launches_per_call(len(p["prefix_lens"]), spec.h_q, spec.h_kv, spec.d, spec.l_ext,
+                                         p["kv_indices"].shape[0]) == launches, spec.name
+        refs = [oracle.verify_forward(workloads.to_oracle_arrays(p))["o"] for p in probs]
+        with_ws = []
+        for (_, modes, _), p in zip(SPECS, probs):
+            _form(modes)
+            with_ws.append(_with_workspace(p).float().cpu().numpy())
+        outs = [torch.empty(p["q"].shape[0], p["q"].shape[1], p["v_ext"].shape[2], dtype=torch.bfloat16,
+                            device="cuda") for p in probs]
+        # one round first: the library's module and kernels are loaded
+        for (_, modes, _), p, o in zip(SPECS, probs, outs):
+            _form(modes)
+            assert _noalloc(lib, p, o) == 1, lib.vsk_last_error().decode()
+        torch.cuda.synchronize()
+        n = len(SPECS)
+        for rnd in range(2):
+            for i in range(n) if rnd == 0 else reversed(range(n)):
+                _form(SPECS[i][1])
+                outs[i].fill_(float("nan"))
+                torch.cuda.synchronize()
+                free0 = torch.cuda.mem_get_info()[0]
+                assert _noalloc(lib, probs[i], outs[i]) == 1, lib.vsk_last_error().decode()
+                torch.cuda.synchronize()
+                assert torch.cuda.mem_get_info()[0] == free0, "device memory was allocated"
+                _check(outs[i], refs[i])
+                np.testing.assert_allclose(outs[i].float().cpu().numpy(), with_ws[i], atol=ATOL, rtol=RTOL)
+                assert _noalloc_flags(lib) == 0
+    finally:
+        _form((1, 1, 1))
 
 
 def test_noalloc_flags_an_out_of_range_index(lib):
