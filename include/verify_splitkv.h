@@ -345,6 +345,14 @@ void vsk_set_tuning_cluster(int mode);
  * way.  Process-wide; not thread-safe. */
 void vsk_set_tuning_pdl(int mode);
 
+/* Tuning switch, for A/B runs: mode 1 (the default) runs the head_dim 256
+ * one-launch kernel with software-pipelined stages (the softmax and PV
+ * products of a 16-token stage are computed after the QK products of the
+ * next stage are issued, so each warp interleaves two stages' work); mode 0
+ * runs one stage after the other.  The result is the same either way.
+ * Process-wide; not thread-safe. */
+void vsk_set_tuning_pipe(int mode);
+
 /* Kernel launches a call of these static shapes makes on its stream under the
  * current tuning switches: 1 (the one-launch kernel) or 2 (a prefix stream,
  * then the combine kernel); 0 for shapes no entry point accepts.

@@ -130,6 +130,8 @@ def _bind(lib):
     lib.vsk_set_tuning_cluster.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_pdl.restype = None
     lib.vsk_set_tuning_pdl.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_pipe.restype = None
+    lib.vsk_set_tuning_pipe.argtypes = [ctypes.c_int]
     lib.vsk_launches_per_call.restype = ctypes.c_int
     lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
     lib.vsk_set_tuning_shape.restype = None

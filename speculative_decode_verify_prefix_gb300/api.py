@@ -323,6 +323,12 @@ def set_tuning_pdl(enabled: bool = False) -> None:
     _native.lib().vsk_set_tuning_pdl(1 if enabled else 0)
 
 
+def set_tuning_pipe(enabled: bool = True) -> None:
+    """Head_dim 256 one-launch kernel with software-pipelined stages (the
+    default) or one stage after the other; for A/B runs."""
+    _native.lib().vsk_set_tuning_pipe(1 if enabled else 0)
+
+
 def launches_per_call(batch: int, h_q: int, h_kv: int, head_dim: int, max_len_extend: int,
                       prefix_tokens: int) -> int:
     """Kernel launches one call of these shapes makes (1 or 2; 0 if no entry

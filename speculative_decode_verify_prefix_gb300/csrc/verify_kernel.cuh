@@ -64,6 +64,7 @@ constexpr long long kClMaxWork = 2047;  // prefix tokens x KV heads up to which 
 constexpr long long kClMaxSeg = 512;         // ... with at most this many (sequence, KV head) segments
 constexpr long long kClTokensPerCta = 64;    // prefix tokens per CTA the cluster size aims at
 constexpr int kClMax = 16;                   // CTAs per cluster at most (8 where 16 do not fit an SM group)
+constexpr float kLazy = 8.f;          // log2 headroom before a running maximum is raised
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
 constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
@@ -208,6 +209,25 @@ __device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, uint32_t b0
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D(16x8 fp32) = A(16x16 f16, row) * B(16x8 f16, col): a chain's first product
+// (accumulator input zero, no zero-fill of the registers needed)
+__device__ __forceinline__ void mma_f16_z(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// D(16x8 fp32) = A(16x16 bf16, row) * B(16x8 bf16, col), accumulator input zero
+__device__ __forceinline__ void mma_bf16_z(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 // D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
@@ -606,7 +626,9 @@ struct MaxOf {
 // DV: the value head_dim (output columns), D the query / key head_dim.
 // CL: the cluster form (stream only, then the combine of the segment by the
 // cluster's CTAs after a cluster barrier; one launch, no tickets).
-template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D, bool CL = false>
+// PIPE: software-pipelined stages (the softmax and PV of stage k run after
+// the QK products of stage k + 1 are issued; needs a ring of >= 3 stages).
+template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D, bool CL = false, bool PIPE = false>
 __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>::value * 32, CS == 2 ? 3 : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -617,6 +639,7 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
                 "column split: head_dim 256 stream only");
   static_assert(D == DV || (MTW == 1 && CS == 1 && !SO), "head_dim != v_head_dim: one-launch kernel, one tile per warp");
   static_assert(!CL || (SO && MTW == 1 && D == DV), "cluster form: stream-only, one tile per warp");
+  static_assert(!PIPE || CS == 1, "pipelined stages: not with the column split");
   constexpr int DH = D / CS;       // contraction length of one warp
   constexpr int DVH = DV / CS;     // output columns of one warp
   constexpr int NTH = NT / CS;     // its n-tiles
@@ -729,6 +752,59 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
     const unsigned char* kbase = p.kb + head * p.kb_s1;
     const unsigned char* vbase = p.vb + head * p.vb_s1;
     const uint32_t slot = ring_s + static_cast<uint32_t>(dslot) * STAGE_B;
+    // Two warps per KV head (the head's stage split in 8 tokens per warp):
+    // four lanes serve each token (eight tokens a pass), lane s of a token
+    // copying chunks s, s + 4, ... of
+    // its K row and of its V row, so each copy instruction reads runs of 64
+    // bytes (smaller runs measured far slower).  A lane forms its token's row
+    // addresses once; every further source offset is a compile-time
+    // constant, and the swizzled destinations repeat in groups of min(8,
+    // chunks per row) chunks, so up to two precomputed bases plus constants
+    // cover them.
+    auto fast_copy = [&](auto tpw_tag) {
+      constexpr int TPW = decltype(tpw_tag)::value;  // tokens this warp copies
+      constexpr int LPN = 4;                         // lanes per token
+      constexpr int NPASS = TPW / (32 / LPN);
+      const int sl = lane % LPN;
+      // all of this warp's tokens present (the common case): no selects
+      const unsigned wmask = ((1u << TPW) - 1u) << (cw * TPW);
+      const bool full = (mask & wmask) == wmask;
+#pragma unroll
+      for (int pass = 0; pass < NPASS; ++pass) {
+        const int t = cw * TPW + pass * (32 / LPN) + lane / LPN;
+        const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+        const bool v = (mask >> t) & 1u;
+        auto rows = [&](auto rb_tag, const unsigned char* base, long long s0, uint32_t region) {
+          constexpr int RB = decltype(rb_tag)::value;  // row bytes
+          constexpr int CP = RB / 16;                 // chunks per row
+          constexpr int G = CP < 8 ? CP : 8;          // chunks a swizzle permutes together
+          constexpr int Q = G / LPN;                  // distinct destination bases
+          static_assert(CP % LPN == 0 && G % LPN == 0, "lanes per token divide the row");
+          const int x = chunk_swz<CP>(t);
+          uint32_t db[Q];
+#pragma unroll
+          for (int q = 0; q < Q; ++q) db[q] = region + static_cast<uint32_t>(t * RB + (((q * LPN + sl) ^ x) << 4));
+          const unsigned char* src = v ? base + loc * s0 + sl * 16 : reinterpret_cast<const unsigned char*>(p.q);
+          if (full) {
+#pragma unroll
+            for (int r = 0; r < CP / LPN; ++r)
+              cp_async_16_zfill(db[r % Q] + ((r * LPN) / G) * G * 16, src + r * LPN * 16, true, pol);
+          } else {
+#pragma unroll
+            for (int r = 0; r < CP / LPN; ++r)
+              cp_async_16_zfill(db[r % Q] + ((r * LPN) / G) * G * 16, v ? src + r * LPN * 16 : src, v, pol);
+          }
+        };
+        rows(std::integral_constant<int, ROWB>{}, kbase, p.kb_s0, slot);
+        rows(std::integral_constant<int, VROWB>{}, vbase, p.vb_s0, slot + 16 * ROWB);
+      }
+    };
+    // (one warp per head keeps the whole-row copies below: with 16 tokens a
+    // warp they measured faster than this mapping)
+    if (WPHC == 2) {
+      fast_copy(std::integral_constant<int, 8>{});
+      return;
+    }
     // lane -> (token group, 16-byte chunk): LPT lanes cover one row, so each
     // lane computes a token's K and V addresses once and issues both copies
     if constexpr (D == DV) {
@@ -837,8 +913,10 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   cp_async_commit();
   cp_async_wait<0>();
   __syncwarp();
+  // stages in flight ahead of the one being consumed: nst - 1, or nst - 2
+  // when pipelined (the ring then also holds the stage whose PV is pending)
 #pragma unroll 1
-  for (int a = 0; a < nst - 1; ++a) {
+  for (int a = 0; a < nst - 1 - (PIPE ? 1 : 0); ++a) {
     step_data();
     step_idx();
     cp_async_commit();
@@ -850,6 +928,22 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   const int v_key = (((lane >> 3) & 1) << 3) + (lane & 7);
   const int v_chk = lane >> 4;
   const int f_key = lane & 15;  // e4m3 pools: key row of this lane's ldmatrix address
+  // This lane's swizzled 16-byte chunk offsets of its ldmatrix rows: the
+  // chunk index XOR the row's swizzle only touches the low 3 bits (the low 2
+  // with 4-chunk rows), so within each group of four consecutive loads the
+  // offsets repeat and the group adds 128 bytes: offset of load i =
+  // koff[i & 3] + 128 (i >> 2).
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    if constexpr (FP8) {
+      koff[r] = static_cast<uint32_t>(((2 * r + (lane >> 4)) ^ chunk_swz<CPR>(f_key)) << 4);
+      voff[r] = static_cast<uint32_t>(((2 * r + (lane >> 4)) ^ chunk_swz<VCPR>(f_key)) << 4);
+    } else {
+      koff[r] = static_cast<uint32_t>(((2 * r + k_chk) ^ (k_key & 7)) << 4);
+      voff[r] = static_cast<uint32_t>(((2 * r + v_chk) ^ (v_key & 7)) << 4);
+    }
+  }
 
   // The next piece's query fragments are loaded into registers while the
   // current piece streams (head_dim <= 128, one tile per warp), so a piece
@@ -895,6 +989,10 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
   };
   const int q_row = (lane & 7) + (((lane >> 3) & 1) << 3);
   const uint32_t q_lane = smem_u32(qsm) + q_row * (2 * DH);
+  // swizzled chunk offsets of this lane's query-fragment loads (as koff)
+  uint32_t qoff[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) qoff[r] = static_cast<uint32_t>(((2 * r + (lane >> 4)) ^ (q_row & 7)) << 4);
   // CS = 2: this warp's score exchange buffer (after its query tiles) and the
   // offset, in floats, to its partner's
   float* xbuf = reinterpret_cast<float*>(qsm + (kQSmem ? MTW * 32 * DH : 0));
@@ -930,126 +1028,40 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
     }
 
     // ---------------- prefix: online softmax over this CTA's piece ----------------
-#pragma unroll 1
-    for (int tok = t0; tok < te; tok += kStageTokens, ++k, kslot = (kslot + 1 == nst) ? 0 : kslot + 1) {
-      cp_async_wait_dyn(nst - 2);  // stage k has landed (this lane's copies)
-      __syncwarp();                // ... and every other lane's
-      // ... and the other warps' of this head: after this barrier no warp of
-      // the head still reads the slot of stage k - 1, which step_data refills
-      if (WPHC > 1) named_bar_sync(2 + hc, WPHC * 32);
-      step_data();                 // refill the slot stage k-1 used
-      step_idx();
-      cp_async_commit();
-      const unsigned mask = mask_ring[k % 16];
-      unsigned char* slotp = ring + kslot * STAGE_B;
-      // ldmatrix row addresses.  bf16: lanes 0-15 / 16-31 take keys 0-7, 8-15
-      // of k-chunk 2kk / 2kk+1 ... (k_key, k_chk); e4m3: lane takes key
-      // (lane & 15) and chunk 2kk2 + (lane >> 4), so one x4 load gives both
-      // 8-key tiles of two 16-wide d blocks.
-      const uint32_t kbase = smem_u32(slotp) + (FP8 ? f_key : k_key) * ROWB;
-      const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * VROWB;
-
-      // S = Q K^T for 16 keys: two n-tiles of 8 keys per 16-row tile.
-      // Independent accumulator chains per n-tile (k-step mod NCH) cut the
-      // dependent mma latency; summed afterwards.  With two tiles per warp the
-      // tiles themselves are independent chains.
-      constexpr int NCH = MTW == 1 ? 4 : 1;
-      float sc[MTW][2][4];
-      float sx[MTW][NCH > 1 ? NCH - 1 : 1][2][4];
-#pragma unroll
-      for (int t = 0; t < MTW; ++t) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[t][u][e] = 0.f;
-#pragma unroll
-            for (int c = 0; c < NCH - 1; ++c) sx[t][c][u][e] = 0.f;
-          }
-        }
-      }
-      auto qk_step = [&](int kk, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-        const int ch = kk % NCH;
-#pragma unroll
-        for (int t = 0; t < MTW; ++t) {
-          float* c0 = ch == 0 ? sc[t][0] : sx[t][ch - 1][0];
-          float* c1 = ch == 0 ? sc[t][1] : sx[t][ch - 1][1];
-          if constexpr (kQSmem) {
-            uint32_t a[4];
-            ldsm_x4(q_lane + t * 32 * DH + (((2 * kk + (lane >> 4)) ^ (q_row & 7)) << 4), a[0], a[1], a[2], a[3]);
-            if constexpr (FP8) {
-              mma_f16(c0, a, b0, b1);
-              mma_f16(c1, a, b2, b3);
-            } else {
-              mma_bf16(c0, a, b0, b1);
-              mma_bf16(c1, a, b2, b3);
-            }
-          } else if constexpr (FP8) {
-            mma_f16(c0, qf[t][kk], b0, b1);
-            mma_f16(c1, qf[t][kk], b2, b3);
-          } else {
-            mma_bf16(c0, qf[t][kk], b0, b1);
-            mma_bf16(c1, qf[t][kk], b2, b3);
-          }
-        }
-      };
-      if constexpr (FP8) {
-        // each 32-bit register holds 4 consecutive e4m3 d values of one key:
-        // low pair -> b0, high pair -> b1 of the permuted contraction order
-#pragma unroll
-        for (int kk2 = 0; kk2 < KSH / 2; ++kk2) {
-          const int c = 2 * (csi * (KSH / 2) + kk2) + (lane >> 4);
-          uint32_t r0k, r1k, r2k, r3k;
-          ldsm_x4(kbase + ((c ^ chunk_swz<CPR>(f_key)) << 4), r0k, r1k, r2k, r3k);
-          qk_step(2 * kk2, e4m3x2_to_f16x2(r0k & 0xFFFF), e4m3x2_to_f16x2(r0k >> 16), e4m3x2_to_f16x2(r1k & 0xFFFF),
-                  e4m3x2_to_f16x2(r1k >> 16));
-          qk_step(2 * kk2 + 1, e4m3x2_to_f16x2(r2k & 0xFFFF), e4m3x2_to_f16x2(r2k >> 16),
-                  e4m3x2_to_f16x2(r3k & 0xFFFF), e4m3x2_to_f16x2(r3k >> 16));
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < KSH; ++kk) {
-          uint32_t b0, b1, b2, b3;
-          const int lc = (csi * KSH + kk) * 2 + k_chk;
-          ldsm_x4(kbase + ((lc ^ (k_key & 7)) << 4), b0, b1, b2, b3);
-          qk_step(kk, b0, b1, b2, b3);
-        }
-      }
+    // Pipelined: the previous stage's raw scores, valid-key mask and V rows,
+    // finished (softmax, PV) after this stage's QK products are issued.
+    [[maybe_unused]] float s_prev[MTW][2][4];
+    [[maybe_unused]] unsigned mask_prev = 0u;
+    [[maybe_unused]] uint32_t vbase_prev = 0u;
+    [[maybe_unused]] bool have_prev = false;
+    // softmax of one stage's scores (scaled into the log2 domain here) and its
+    // PV products; `sfin` holds the raw QK sums of the stage
+    auto finish = [&](float (&sfin)[MTW][2][4], const unsigned mask, const uint32_t vbase) {
       uint32_t pa[MTW][4];
 #pragma unroll
       for (int t = 0; t < MTW; ++t) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x = sc[t][u][e];
-            if constexpr (NCH == 4) {
-              x += (sx[t][0][u][e] + sx[t][1][u][e]) + sx[t][2][u][e];
-            } else {
-#pragma unroll
-              for (int c = 0; c < NCH - 1; ++c) x += sx[t][c][u][e];
-            }
-            // scale into the log2 domain
-            sc[t][u][e] = x * qsc[t];
-          }
+          for (int e = 0; e < 4; ++e) sfin[t][u][e] *= qsc[t];  // scale into the log2 domain
         }
         if constexpr (CS == 2) {
           // the pair's partial scores (each in the log2 domain already) summed
           // by both warps alike; the buffer alternates with the stage parity
           float* xo = xbuf + static_cast<int>(k & 1) * 256 + lane * 8;
-          *reinterpret_cast<float4*>(xo) = make_float4(sc[t][0][0], sc[t][0][1], sc[t][0][2], sc[t][0][3]);
-          *reinterpret_cast<float4*>(xo + 4) = make_float4(sc[t][1][0], sc[t][1][1], sc[t][1][2], sc[t][1][3]);
+          *reinterpret_cast<float4*>(xo) = make_float4(sfin[t][0][0], sfin[t][0][1], sfin[t][0][2], sfin[t][0][3]);
+          *reinterpret_cast<float4*>(xo + 4) = make_float4(sfin[t][1][0], sfin[t][1][1], sfin[t][1][2], sfin[t][1][3]);
           named_bar_sync(10 + (warp >> 1), 64);
           const float* xp = xo + xpair;
           const float4 y0 = *reinterpret_cast<const float4*>(xp), y1 = *reinterpret_cast<const float4*>(xp + 4);
-          sc[t][0][0] += y0.x;
-          sc[t][0][1] += y0.y;
-          sc[t][0][2] += y0.z;
-          sc[t][0][3] += y0.w;
-          sc[t][1][0] += y1.x;
-          sc[t][1][1] += y1.y;
-          sc[t][1][2] += y1.z;
-          sc[t][1][3] += y1.w;
+          sfin[t][0][0] += y0.x;
+          sfin[t][0][1] += y0.y;
+          sfin[t][0][2] += y0.z;
+          sfin[t][0][3] += y0.w;
+          sfin[t][1][0] += y1.x;
+          sfin[t][1][1] += y1.y;
+          sfin[t][1][2] += y1.z;
+          sfin[t][1][3] += y1.w;
         }
         // mask absent keys (tail / dropped) only when the stage is not full
         // (the mask is uniform across the warp)
@@ -1059,22 +1071,26 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int key = u * 8 + 2 * j + (e & 1);
-              if (!((mask >> key) & 1u)) sc[t][u][e] = NEG_INF;
+              if (!((mask >> key) & 1u)) sfin[t][u][e] = NEG_INF;
             }
           }
         }
-        const float mx0 = quad_max(fmaxf(fmaxf(sc[t][0][0], sc[t][0][1]), fmaxf(sc[t][1][0], sc[t][1][1])));
-        const float mx1 = quad_max(fmaxf(fmaxf(sc[t][0][2], sc[t][0][3]), fmaxf(sc[t][1][2], sc[t][1][3])));
-        const float mn0 = fmaxf(m0[t], mx0), mn1 = fmaxf(m1[t], mx1);
+        const float mx0 = quad_max(fmaxf(fmaxf(sfin[t][0][0], sfin[t][0][1]), fmaxf(sfin[t][1][0], sfin[t][1][1])));
+        const float mx1 = quad_max(fmaxf(fmaxf(sfin[t][0][2], sfin[t][0][3]), fmaxf(sfin[t][1][2], sfin[t][1][3])));
+        // The running maximum is raised only when a stage exceeds it by more
+        // than kLazy (log2 units): the weights 2^(s - m) then stay below
+        // 2^kLazy, and most stages need no rescale of the accumulator.  The
+        // result is the same (weights and sum share the reference m).
+        const float mn0 = mx0 > m0[t] + kLazy ? mx0 : m0[t], mn1 = mx1 > m1[t] + kLazy ? mx1 : m1[t];
         const float ms0 = (mn0 == NEG_INF) ? 0.f : mn0;
         const float ms1 = (mn1 == NEG_INF) ? 0.f : mn1;
         float pr[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          pr[u][0] = fast_exp2(sc[t][u][0] - ms0);
-          pr[u][1] = fast_exp2(sc[t][u][1] - ms0);
-          pr[u][2] = fast_exp2(sc[t][u][2] - ms1);
-          pr[u][3] = fast_exp2(sc[t][u][3] - ms1);
+          pr[u][0] = fast_exp2(sfin[t][u][0] - ms0);
+          pr[u][1] = fast_exp2(sfin[t][u][1] - ms0);
+          pr[u][2] = fast_exp2(sfin[t][u][2] - ms1);
+          pr[u][3] = fast_exp2(sfin[t][u][3] - ms1);
         }
         const float ps0 = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
         const float ps1 = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
@@ -1114,11 +1130,12 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
         // regroups them by d, so each register feeds two n-tiles: E (even d,
         // column g <-> d 2g) and O (odd d, column g <-> d 2g+1) of a 16-wide
         // block.  acc[2*blk] is E, acc[2*blk+1] is O.
+        static_assert(KSV / 2 <= 2 || (KSV / 2) % 4 == 0, "offset groups of four");
+        const uint32_t vb = vbase + static_cast<uint32_t>(csi * (KSV / 2) / 4) * 128u;
 #pragma unroll
         for (int c2 = 0; c2 < KSV / 2; ++c2) {
-          const int c = 2 * (csi * (KSV / 2) + c2) + (lane >> 4);
           uint32_t r[4];
-          ldsm_x4_t(vbase + ((c ^ chunk_swz<VCPR>(f_key)) << 4), r[0], r[1], r[2], r[3]);
+          ldsm_x4_t(vb + voff[c2 & 3] + (c2 >> 2) * 128, r[0], r[1], r[2], r[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);      // keys 2j, 2j+1
@@ -1135,11 +1152,12 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
         }
       } else {
         // O += P V for 16 keys
+        static_assert((NTH / 2) % 4 == 0, "offset groups of four");
+        const uint32_t vb = vbase + static_cast<uint32_t>(csi * (NTH / 2) / 4) * 128u;
 #pragma unroll
         for (int n2 = 0; n2 < NTH / 2; ++n2) {
           uint32_t b0, b1, b2, b3;
-          const int lc = (csi * (NTH / 2) + n2) * 2 + v_chk;
-          ldsm_x4_t(vbase + ((lc ^ (v_key & 7)) << 4), b0, b1, b2, b3);
+          ldsm_x4_t(vb + voff[n2 & 3] + (n2 >> 2) * 128, b0, b1, b2, b3);
 #pragma unroll
           for (int t = 0; t < MTW; ++t) {
             mma_bf16(acc[t][2 * n2], pa[t], b0, b1);
@@ -1147,6 +1165,129 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
           }
         }
       }
+    };
+#pragma unroll 1
+    for (int tok = t0; tok < te; tok += kStageTokens, ++k, kslot = (kslot + 1 == nst) ? 0 : kslot + 1) {
+      cp_async_wait_dyn(nst - 2 - (PIPE ? 1 : 0));  // stage k has landed (this lane's copies)
+      __syncwarp();                // ... and every other lane's
+      // ... and the other warps' of this head: after this barrier no warp of
+      // the head still reads the slot of stage k - 1 (k - 2 when pipelined),
+      // which step_data refills
+      if (WPHC > 1) named_bar_sync(2 + hc, WPHC * 32);
+      step_data();                 // refill the freed slot
+      step_idx();
+      cp_async_commit();
+      const unsigned mask = mask_ring[k % 16];
+      unsigned char* slotp = ring + kslot * STAGE_B;
+      // ldmatrix row addresses.  bf16: lanes 0-15 / 16-31 take keys 0-7, 8-15
+      // of k-chunk 2kk / 2kk+1 ... (k_key, k_chk); e4m3: lane takes key
+      // (lane & 15) and chunk 2kk2 + (lane >> 4), so one x4 load gives both
+      // 8-key tiles of two 16-wide d blocks.
+      const uint32_t kbase = smem_u32(slotp) + (FP8 ? f_key : k_key) * ROWB;
+      const uint32_t vbase = smem_u32(slotp) + 16 * ROWB + (FP8 ? f_key : v_key) * VROWB;
+
+      // S = Q K^T for 16 keys: two n-tiles of 8 keys per 16-row tile.
+      // Independent accumulator chains per n-tile (k-step mod NCH) cut the
+      // dependent mma latency; summed afterwards.  With two tiles per warp the
+      // tiles themselves are independent chains.
+      constexpr int NCH = (MTW == 1 && !PIPE) ? 4 : 1;
+      // (a chain's first product takes a zero accumulator input: nothing to clear)
+      float sc[MTW][2][4];
+      float sx[MTW][NCH > 1 ? NCH - 1 : 1][2][4];
+      auto qk_step = [&](int kk, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+        const int ch = kk % NCH;
+        const bool first = kk < NCH;  // known at compile time in the unrolled loops
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) {
+          float* c0 = ch == 0 ? sc[t][0] : sx[t][ch - 1][0];
+          float* c1 = ch == 0 ? sc[t][1] : sx[t][ch - 1][1];
+          uint32_t a[4];
+          if constexpr (kQSmem) {
+            ldsm_x4(q_lane + t * 32 * DH + qoff[kk & 3] + (kk >> 2) * 128, a[0], a[1], a[2], a[3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = qf[t][kk][i];
+          }
+          if constexpr (FP8) {
+            if (first) {
+              mma_f16_z(c0, a, b0, b1);
+              mma_f16_z(c1, a, b2, b3);
+            } else {
+              mma_f16(c0, a, b0, b1);
+              mma_f16(c1, a, b2, b3);
+            }
+          } else {
+            if (first) {
+              mma_bf16_z(c0, a, b0, b1);
+              mma_bf16_z(c1, a, b2, b3);
+            } else {
+              mma_bf16(c0, a, b0, b1);
+              mma_bf16(c1, a, b2, b3);
+            }
+          }
+        }
+      };
+      if constexpr (FP8) {
+        // each 32-bit register holds 4 consecutive e4m3 d values of one key:
+        // low pair -> b0, high pair -> b1 of the permuted contraction order
+        static_assert(KSH / 2 <= 2 || (KSH / 2) % 4 == 0, "offset groups of four");
+        const uint32_t kb = kbase + static_cast<uint32_t>(csi * (KSH / 2) / 4) * 128u;
+#pragma unroll
+        for (int kk2 = 0; kk2 < KSH / 2; ++kk2) {
+          uint32_t r0k, r1k, r2k, r3k;
+          ldsm_x4(kb + koff[kk2 & 3] + (kk2 >> 2) * 128, r0k, r1k, r2k, r3k);
+          qk_step(2 * kk2, e4m3x2_to_f16x2(r0k & 0xFFFF), e4m3x2_to_f16x2(r0k >> 16), e4m3x2_to_f16x2(r1k & 0xFFFF),
+                  e4m3x2_to_f16x2(r1k >> 16));
+          qk_step(2 * kk2 + 1, e4m3x2_to_f16x2(r2k & 0xFFFF), e4m3x2_to_f16x2(r2k >> 16),
+                  e4m3x2_to_f16x2(r3k & 0xFFFF), e4m3x2_to_f16x2(r3k >> 16));
+        }
+      } else {
+        static_assert(KSH % 4 == 0, "offset groups of four");
+        const uint32_t kb = kbase + static_cast<uint32_t>(csi * KSH / 4) * 128u;
+#pragma unroll
+        for (int kk = 0; kk < KSH; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + koff[kk & 3] + (kk >> 2) * 128, b0, b1, b2, b3);
+          qk_step(kk, b0, b1, b2, b3);
+        }
+      }
+      // the stage's raw scores: its accumulation chains summed
+      float sr[MTW][2][4];
+#pragma unroll
+      for (int t = 0; t < MTW; ++t) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = sc[t][u][e];
+            if constexpr (NCH == 4) {
+              x += (sx[t][0][u][e] + sx[t][1][u][e]) + sx[t][2][u][e];
+            } else {
+#pragma unroll
+              for (int c = 0; c < NCH - 1; ++c) x += sx[t][c][u][e];
+            }
+            sr[t][u][e] = x;
+          }
+        }
+      }
+      if constexpr (PIPE) {
+        // this stage's QK products are in flight: finish the previous stage
+        if (have_prev) finish(s_prev, mask_prev, vbase_prev);
+#pragma unroll
+        for (int t = 0; t < MTW; ++t)
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s_prev[t][u][e] = sr[t][u][e];
+        mask_prev = mask;
+        vbase_prev = vbase;
+        have_prev = true;
+      } else {
+        finish(sr, mask, vbase);
+      }
+    }
+    if constexpr (PIPE) {
+      if (have_prev) finish(s_prev, mask_prev, vbase_prev);
     }
 
     // ---------------- piece end: write the partial and keep streaming ----------------
@@ -1677,7 +1818,8 @@ using KernelFn = void (*)(Params);
 KernelFn kernel_d64(bool fp8, int mtw, bool so, bool cl = false);
 KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl = false);
 // head_dim 256 (D = Dv): one-launch kernel (variant 0), column-split stream
-// (variant 1) or the cluster form streaming by column split (variant 2)
+// (variant 1), the cluster form streaming by column split (variant 2) or the
+// one-launch kernel with pipelined stages (variant 3)
 KernelFn kernel_d256(bool fp8, int variant);
 // tensor-memory stream, head_dim 256, rm = 16 or 32 packed rows
 KernelFn kernel_tc(bool fp8, int rm);

@@ -46,6 +46,7 @@ int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the def
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
+int g_pipe = 1;   // head_dim 256 one-launch kernel with pipelined stages (1) or not (0)
 int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
 
 struct Plan {
@@ -342,12 +343,14 @@ bool gate(const vsk_tensor* q, const vsk_tensor* ke, const vsk_tensor* ve, const
   return true;
 }
 
-KernelFn pick_kernel(int D, bool fp8, int mtw, int DV = 0) {
+KernelFn pick_kernel(int D, bool fp8, int mtw, int DV = 0, int nst = 0) {
   if (DV != 0 && DV != D) return mtw == 1 ? kernel_dv(D, DV, fp8) : nullptr;
   switch (D) {
     case 64: return kernel_d64(fp8, mtw, false);
     case 128: return kernel_d128(fp8, mtw, false);
-    case 256: return mtw == 1 ? kernel_d256(fp8, 0) : nullptr;
+    // pipelined stages (faster for e4m3 pools; measured slower for bf16 ones)
+    // need a ring of at least three
+    case 256: return mtw == 1 ? kernel_d256(fp8, g_pipe && fp8 && nst >= 3 ? 3 : 0) : nullptr;
     default: return nullptr;
   }
 }
@@ -535,6 +538,8 @@ void vsk_set_tuning_cluster(int mode) { g_cl = (mode == 0 || mode == 2) ? mode :
 
 void vsk_set_tuning_pdl(int mode) { g_pdl = mode == 0 ? 0 : 1; }
 
+void vsk_set_tuning_pipe(int mode) { g_pipe = mode == 0 ? 0 : 1; }
+
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens) {
   if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
@@ -687,7 +692,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     if (!cp.fn || !cp.fn_comb || !prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb))
       return fail("stream-only kernels for head_dim %lld unavailable", D);
   } else {
-    cp.fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW, static_cast<int>(DV));
+    cp.fn = pick_kernel(static_cast<int>(D), fp8, pl.MTW, static_cast<int>(DV), pl.nst);
     if (!cp.fn || !prepare_kernel(cp.fn))
       return fail("kernel for head_dim %lld, v_head_dim %lld unavailable", D, DV);
   }
