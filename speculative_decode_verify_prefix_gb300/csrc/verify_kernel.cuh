@@ -752,58 +752,76 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
     const unsigned char* kbase = p.kb + head * p.kb_s1;
     const unsigned char* vbase = p.vb + head * p.vb_s1;
     const uint32_t slot = ring_s + static_cast<uint32_t>(dslot) * STAGE_B;
-    // Two warps per KV head (the head's stage split in 8 tokens per warp):
-    // four lanes serve each token (eight tokens a pass), lane s of a token
-    // copying chunks s, s + 4, ... of
-    // its K row and of its V row, so each copy instruction reads runs of 64
-    // bytes (smaller runs measured far slower).  A lane forms its token's row
+    // Two, four or eight warps per KV head (the head's stage split in 8, 4 or
+    // 2 tokens per warp): LPN = 32 / TPW lanes serve each token (4, 8 or
+    // 16), lane s of a token copying chunks s, s + LPN, ... of its K row and
+    // of its V row, so each copy instruction reads runs of 64 bytes or more
+    // (smaller runs measured far slower).  A lane forms its token's row
     // addresses once; every further source offset is a compile-time
-    // constant, and the swizzled destinations repeat in groups of min(8,
-    // chunks per row) chunks, so up to two precomputed bases plus constants
-    // cover them.
-    auto fast_copy = [&](auto tpw_tag) {
+    // constant.  The swizzle permutes chunks in groups of G = min(8, chunks
+    // per row): with LPN < G the lane's destinations repeat every G / LPN
+    // chunks (that many precomputed bases plus constants), with LPN >= G one
+    // base plus constants covers them.
+    auto fast_copy = [&](auto tpw_tag, auto lpn_tag) {
       constexpr int TPW = decltype(tpw_tag)::value;  // tokens this warp copies
-      constexpr int LPN = 4;                         // lanes per token
-      constexpr int NPASS = TPW / (32 / LPN);
+      constexpr int LPN = decltype(lpn_tag)::value;  // lanes per token
+      constexpr int NPASS = TPW * LPN / 32;          // tokens a lane serves
       const int sl = lane % LPN;
       // all of this warp's tokens present (the common case): no selects
       const unsigned wmask = ((1u << TPW) - 1u) << (cw * TPW);
       const bool full = (mask & wmask) == wmask;
 #pragma unroll
       for (int pass = 0; pass < NPASS; ++pass) {
-        const int t = cw * TPW + pass * (32 / LPN) + lane / LPN;
-        const long long loc = __shfl_sync(0xffffffffu, myloc, t);
-        const bool v = (mask >> t) & 1u;
-        auto rows = [&](auto rb_tag, const unsigned char* base, long long s0, uint32_t region) {
-          constexpr int RB = decltype(rb_tag)::value;  // row bytes
-          constexpr int CP = RB / 16;                 // chunks per row
-          constexpr int G = CP < 8 ? CP : 8;          // chunks a swizzle permutes together
-          constexpr int Q = G / LPN;                  // distinct destination bases
-          static_assert(CP % LPN == 0 && G % LPN == 0, "lanes per token divide the row");
-          const int x = chunk_swz<CP>(t);
-          uint32_t db[Q];
+      const int t = cw * TPW + pass * (32 / LPN) + lane / LPN;
+      const long long loc = __shfl_sync(0xffffffffu, myloc, t);
+      const bool v = (mask >> t) & 1u;
+      auto rows = [&](auto rb_tag, const unsigned char* base, long long s0, uint32_t region) {
+        constexpr int RB = decltype(rb_tag)::value;  // row bytes
+        constexpr int CP = RB / 16;                 // chunks per row
+        constexpr int G = CP < 8 ? CP : 8;          // chunks a swizzle permutes together
+        constexpr int Q = LPN < G ? G / LPN : 1;    // distinct destination bases
+        static_assert(CP % LPN == 0, "lanes per token divide the row");
+        const int x = chunk_swz<CP>(t);
+        uint32_t db[Q];
 #pragma unroll
-          for (int q = 0; q < Q; ++q) db[q] = region + static_cast<uint32_t>(t * RB + (((q * LPN + sl) ^ x) << 4));
-          const unsigned char* src = v ? base + loc * s0 + sl * 16 : reinterpret_cast<const unsigned char*>(p.q);
-          if (full) {
-#pragma unroll
-            for (int r = 0; r < CP / LPN; ++r)
-              cp_async_16_zfill(db[r % Q] + ((r * LPN) / G) * G * 16, src + r * LPN * 16, true, pol);
-          } else {
-#pragma unroll
-            for (int r = 0; r < CP / LPN; ++r)
-              cp_async_16_zfill(db[r % Q] + ((r * LPN) / G) * G * 16, v ? src + r * LPN * 16 : src, v, pol);
-          }
+        for (int q = 0; q < Q; ++q) db[q] = region + static_cast<uint32_t>(t * RB + (((q * LPN + sl) ^ x) << 4));
+        const unsigned char* src = v ? base + loc * s0 + sl * 16 : reinterpret_cast<const unsigned char*>(p.q);
+        // destination of the lane's r-th chunk (chunk r LPN + sl)
+        auto dst = [&](int r) -> uint32_t {
+          return LPN < G ? db[r % Q] + ((r * LPN) / G) * G * 16 : db[0] + r * LPN * 16;
         };
-        rows(std::integral_constant<int, ROWB>{}, kbase, p.kb_s0, slot);
-        rows(std::integral_constant<int, VROWB>{}, vbase, p.vb_s0, slot + 16 * ROWB);
+        if (full) {
+#pragma unroll
+          for (int r = 0; r < CP / LPN; ++r) cp_async_16_zfill(dst(r), src + r * LPN * 16, true, pol);
+        } else {
+#pragma unroll
+          for (int r = 0; r < CP / LPN; ++r) cp_async_16_zfill(dst(r), v ? src + r * LPN * 16 : src, v, pol);
+        }
+      };
+      rows(std::integral_constant<int, ROWB>{}, kbase, p.kb_s0, slot);
+      rows(std::integral_constant<int, VROWB>{}, vbase, p.vb_s0, slot + 16 * ROWB);
       }
     };
     // (one warp per head keeps the whole-row copies below: with 16 tokens a
     // warp they measured faster than this mapping)
     if (WPHC == 2) {
-      fast_copy(std::integral_constant<int, 8>{});
+      // head_dim 256 bf16 rows: eight lanes per token (128-byte runs, two
+      // passes) measured 5 % faster; e4m3 rows and the other sizes keep four
+      constexpr int LPN2 = (!FP8 && D == 256 && DV == 256) ? 8 : 4;
+      fast_copy(std::integral_constant<int, 8>{}, std::integral_constant<int, LPN2>{});
       return;
+    }
+    if constexpr (CPR % 8 == 0 && VCPR % 8 == 0) {
+      if (WPHC == 4) {
+        fast_copy(std::integral_constant<int, 4>{}, std::integral_constant<int, 8>{});
+        return;
+      }
+    }
+    if constexpr (CPR % 16 == 0 && VCPR % 16 == 0) {
+      if (WPHC == 8) {
+        fast_copy(std::integral_constant<int, 2>{}, std::integral_constant<int, 16>{});
+        return;
+      }
     }
     // lane -> (token group, 16-byte chunk): LPT lanes cover one row, so each
     // lane computes a token's K and V addresses once and issues both copies
@@ -1190,7 +1208,8 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
       // Independent accumulator chains per n-tile (k-step mod NCH) cut the
       // dependent mma latency; summed afterwards.  With two tiles per warp the
       // tiles themselves are independent chains.
-      constexpr int NCH = (MTW == 1 && !PIPE) ? 4 : 1;
+      // (two chains measured faster than four for head_dim 256 bf16 only)
+      constexpr int NCH = (MTW == 1 && !PIPE) ? ((D == 256 && !FP8 && CS == 1) ? 2 : 4) : 1;
       // (a chain's first product takes a zero accumulator input: nothing to clear)
       float sc[MTW][2][4];
       float sx[MTW][NCH > 1 ? NCH - 1 : 1][2][4];
