@@ -110,6 +110,7 @@ WORKLOADS = {
     # the e4m3 head_dim 256 shape with 8 sequences (~0.17 GB > L2): multi-pass ncu captures
     "fp8_b8": workloads.Spec("fp8_b8_p8k_32k", None, 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
                              v_scale=0.25, batch=8, len_range=(8192, 32768), seed=1240),
+    "fp8_cfg": workloads.FP8,
 }
 
 

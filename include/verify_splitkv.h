@@ -308,6 +308,19 @@ void vsk_set_tuning_tc(int mode);
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
 
+/* Tuning switch, for A/B runs and tests, over head_dim 256 calls with 17 to 32
+ * packed query rows per KV head: the column-split stream with both 16-row
+ * tiles in each warp (one warp pair per KV head, each warp half of the head
+ * dimension for both tiles, so every K / V element is loaded and, for an
+ * e4m3 pool, converted once per head), then the combine kernel in a second
+ * launch.  Mode 1 (the default) takes it, for e4m3 pools with at least
+ * 131,072 prefix tokens x KV heads, where the one-tile split of
+ * vsk_set_tuning_colsplit would serve the call (it measured faster there;
+ * smaller calls keep the one-tile split, longer ones the one-launch kernel);
+ * mode 2 takes it wherever it applies, any pool and size; mode 0 never.  All forms compute the same result up to rounding order.
+ * Process-wide; not thread-safe. */
+void vsk_set_tuning_colsplit2(int mode);
+
 /* Tuning switch, for A/B runs and tests, over head_dim 64 and 128 calls with at
  * most 32 draft rows per sequence: the prefix is streamed by a stream-only
  * instance of the mma.sync kernel and the per-piece partials are folded, the

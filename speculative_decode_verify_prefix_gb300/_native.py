@@ -132,6 +132,8 @@ def _bind(lib):
     lib.vsk_set_tuning_pdl.argtypes = [ctypes.c_int]
     lib.vsk_set_tuning_pipe.restype = None
     lib.vsk_set_tuning_pipe.argtypes = [ctypes.c_int]
+    lib.vsk_set_tuning_colsplit2.restype = None
+    lib.vsk_set_tuning_colsplit2.argtypes = [ctypes.c_int]
     lib.vsk_launches_per_call.restype = ctypes.c_int
     lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
     lib.vsk_set_tuning_shape.restype = None

@@ -302,6 +302,13 @@ def set_tuning_colsplit(mode: int = 1) -> None:
     _native.lib().vsk_set_tuning_colsplit(int(mode))
 
 
+def set_tuning_colsplit2(mode: int = 1) -> None:
+    """Head_dim 256 calls with 17-32 packed rows per KV head: the column split
+    with both tiles in each warp for e4m3 pools past the one-tile split's window
+    (1, the default), wherever it applies (2) or never (0); for A/B runs and tests."""
+    _native.lib().vsk_set_tuning_colsplit2(int(mode))
+
+
 def set_tuning_split_launch(mode: int = 1) -> None:
     """Head_dim 64 / 128 calls (at most 32 drafts): stream-only kernel plus a
     combine launch for small calls (1, the default), always (2) or never (0);

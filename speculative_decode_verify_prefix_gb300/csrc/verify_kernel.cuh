@@ -56,6 +56,7 @@ constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
 constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
+constexpr long long kColSplit2MinWork = 1LL << 17;  // ... from which e4m3 pools take the two-tile split instead
 constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
 constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
 constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
@@ -628,14 +629,18 @@ struct MaxOf {
 // cluster's CTAs after a cluster barrier; one launch, no tickets).
 // PIPE: software-pipelined stages (the softmax and PV of stage k run after
 // the QK products of stage k + 1 are issued; needs a ring of >= 3 stages).
+// The column split with MTW = 2: one warp pair per KV head holding both
+// 16-row tiles, each warp half the columns (every K / V element converted
+// and loaded once per head); 64-thread CTAs, four per SM.
 template <int D, bool FP8, int MTW, int CS = 1, bool SO = (CS == 2), int DV = D, bool CL = false, bool PIPE = false>
-__global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>::value * 32, CS == 2 ? 3 : 1)
+__global__ void __launch_bounds__(CS == 2 ? (MTW == 2 ? 64 : 128) : MaxWarps<MaxOf<D, DV>::value>::value * 32,
+                                  CS == 2 ? (MTW == 2 ? 4 : 3) : 1)
     vsk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int EK = FP8 ? 1 : 2;  // pool element bytes
   constexpr int NT = DV / 8;       // n-tiles of the output row
   constexpr int KS = D / 16;       // k-steps of the QK contraction
-  static_assert(CS == 1 || (CS == 2 && D == 256 && DV == 256 && MTW == 1 && SO),
+  static_assert(CS == 1 || (CS == 2 && D == 256 && DV == 256 && SO),
                 "column split: head_dim 256 stream only");
   static_assert(D == DV || (MTW == 1 && CS == 1 && !SO), "head_dim != v_head_dim: one-launch kernel, one tile per warp");
   static_assert(!CL || (SO && MTW == 1 && D == DV), "cluster form: stream-only, one tile per warp");
@@ -1057,20 +1062,27 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
     auto finish = [&](float (&sfin)[MTW][2][4], const unsigned mask, const uint32_t vbase) {
       uint32_t pa[MTW][4];
 #pragma unroll
-      for (int t = 0; t < MTW; ++t) {
+      for (int t = 0; t < MTW; ++t)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sfin[t][u][e] *= qsc[t];  // scale into the log2 domain
+      if constexpr (CS == 2) {
+        // the pair's partial scores (each in the log2 domain already) summed
+        // by both warps alike, every tile through one barrier; the buffer
+        // alternates with the stage parity
+        float* xo = xbuf + static_cast<int>(k & 1) * (256 * MTW) + lane * 8;
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) {
+          *reinterpret_cast<float4*>(xo + t * 256) =
+              make_float4(sfin[t][0][0], sfin[t][0][1], sfin[t][0][2], sfin[t][0][3]);
+          *reinterpret_cast<float4*>(xo + t * 256 + 4) =
+              make_float4(sfin[t][1][0], sfin[t][1][1], sfin[t][1][2], sfin[t][1][3]);
         }
-        if constexpr (CS == 2) {
-          // the pair's partial scores (each in the log2 domain already) summed
-          // by both warps alike; the buffer alternates with the stage parity
-          float* xo = xbuf + static_cast<int>(k & 1) * 256 + lane * 8;
-          *reinterpret_cast<float4*>(xo) = make_float4(sfin[t][0][0], sfin[t][0][1], sfin[t][0][2], sfin[t][0][3]);
-          *reinterpret_cast<float4*>(xo + 4) = make_float4(sfin[t][1][0], sfin[t][1][1], sfin[t][1][2], sfin[t][1][3]);
-          named_bar_sync(10 + (warp >> 1), 64);
-          const float* xp = xo + xpair;
+        named_bar_sync(10 + (warp >> 1), 64);
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) {
+          const float* xp = xo + t * 256 + xpair;
           const float4 y0 = *reinterpret_cast<const float4*>(xp), y1 = *reinterpret_cast<const float4*>(xp + 4);
           sfin[t][0][0] += y0.x;
           sfin[t][0][1] += y0.y;
@@ -1081,6 +1093,9 @@ __global__ void __launch_bounds__(CS == 2 ? 128 : MaxWarps<MaxOf<D, DV>::value>:
           sfin[t][1][2] += y1.z;
           sfin[t][1][3] += y1.w;
         }
+      }
+#pragma unroll
+      for (int t = 0; t < MTW; ++t) {
         // mask absent keys (tail / dropped) only when the stage is not full
         // (the mask is uniform across the warp)
         if (mask != 0xFFFFu) {
@@ -1837,8 +1852,9 @@ using KernelFn = void (*)(Params);
 KernelFn kernel_d64(bool fp8, int mtw, bool so, bool cl = false);
 KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl = false);
 // head_dim 256 (D = Dv): one-launch kernel (variant 0), column-split stream
-// (variant 1), the cluster form streaming by column split (variant 2) or the
-// one-launch kernel with pipelined stages (variant 3)
+// (variant 1), the cluster form streaming by column split (variant 2), the
+// one-launch kernel with pipelined stages (variant 3) or the column-split
+// stream with two tiles per warp (variant 4)
 KernelFn kernel_d256(bool fp8, int variant);
 // tensor-memory stream, head_dim 256, rm = 16 or 32 packed rows
 KernelFn kernel_tc(bool fp8, int rm);

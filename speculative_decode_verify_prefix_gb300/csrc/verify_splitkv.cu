@@ -45,6 +45,7 @@ int g_tiles = 0;  // tiles per warp override (0 = default)
 int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
+int g_cs2 = 1;    // two-tile column split at head_dim 256: 1 e4m3 pools past kColSplitMaxWork, 2 always, 0 never
 int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
 int g_pipe = 1;   // head_dim 256 one-launch kernel with pipelined stages (1) or not (0)
 int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
@@ -173,6 +174,21 @@ bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long l
   if (g_cs == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0 || (h_q / h_kv) * L > 32) return false;
   return g_cs == 2 || total_tokens * h_kv <= kColSplitMaxWork;
 }
+// Column-split stream with both 16-row tiles in each warp of the pair
+// (vsk_kernel<256, ., 2, 2>): head_dim 256 with 17 to 32 packed rows per KV
+// head.  Each K / V element is converted (e4m3 pools) and loaded from shared
+// memory once per head instead of once per tile, at the price of the pair's
+// score exchange each stage; by default taken for e4m3 pools inside the
+// one-tile split's size window (instead of it) from kColSplit2MinWork prefix
+// tokens x KV heads, where it measured faster (smaller calls: the one-tile
+// split's lighter CTAs are faster).
+bool cs2_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens, bool fp8) {
+  if (g_cs2 == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
+  const long long R = (h_q / h_kv) * L;
+  if (R <= 16 || R > 32) return false;
+  const long long work = total_tokens * h_kv;
+  return g_cs2 == 2 || (fp8 && g_cs != 0 && work >= kColSplit2MinWork && (g_cs == 2 || work <= kColSplitMaxWork));
+}
 // Stream-only vsk_kernel then the combine kernel, for head_dim 64 / 128 calls
 // with at most cmb::kMaxL drafts: small and mid-size calls, where the
 // one-launch kernel's tail (tickets, a two-level fold of the pieces, the
@@ -216,6 +232,31 @@ bool make_cs_stream_plan(const Plan& pl, long long D, bool fp8, StreamPlan& sp) 
   sp.nst = std::min(kMaxStages, (budget - kCtlBytes - nwc * sp.misc_bytes) / stage_bytes);
   if (g_max_stages > 0) sp.nst = std::min(sp.nst, g_max_stages);
   if (sp.nst < 2) return fail("column-split stage of %d bytes does not fit shared memory", stage_bytes);
+  sp.ring_off = kCtlBytes;
+  sp.head_bytes = sp.nst * stage_bytes;
+  sp.misc_off = sp.ring_off + sp.head_bytes;
+  sp.smem = static_cast<size_t>(sp.misc_off) + static_cast<size_t>(nwc) * sp.misc_bytes;
+  return true;
+}
+
+// Two-tile column split: one warp pair per CTA (both tiles of one KV head),
+// four CTAs per SM (three if the ring would be shallower than 3 stages).
+bool make_cs2_stream_plan(const Plan& pl, long long D, bool fp8, StreamPlan& sp) {
+  if (pl.MT != 2) return fail("two-tile column split needs two 16-row tiles (got %d)", pl.MT);
+  const int nwc = 2;
+  sp.threads = nwc * 32;
+  const int stage_bytes = 2 * kStageTokens * static_cast<int>(D) * (fp8 ? 1 : 2);
+  // per warp: index ring, mask ring, both query tiles (16 rows x D/2, f16 / bf16),
+  // score exchange buffer (2 stage parities x 2 tiles x 1 KB)
+  sp.misc_bytes = kIdxRing * 128 + 128 + 2 * 16 * static_cast<int>(D / 2) * 2 + 2 * 2 * 1024;
+  sp.nst = 0;
+  for (sp.per_sm = 4; sp.per_sm >= 3; --sp.per_sm) {
+    const int budget = std::min(kSmemPerCTAMax, kSmemPerSM / sp.per_sm - kReservedPerCTA);
+    sp.nst = std::min(kMaxStages, (budget - kCtlBytes - nwc * sp.misc_bytes) / stage_bytes);
+    if (g_max_stages > 0) sp.nst = std::min(sp.nst, g_max_stages);
+    if (sp.nst >= 3) break;
+  }
+  if (sp.nst < 2) return fail("two-tile column-split stage of %d bytes does not fit shared memory", stage_bytes);
   sp.ring_off = kCtlBytes;
   sp.head_bytes = sp.nst * stage_bytes;
   sp.misc_off = sp.ring_off + sp.head_bytes;
@@ -540,6 +581,8 @@ void vsk_set_tuning_pdl(int mode) { g_pdl = mode == 0 ? 0 : 1; }
 
 void vsk_set_tuning_pipe(int mode) { g_pipe = mode == 0 ? 0 : 1; }
 
+void vsk_set_tuning_colsplit2(int mode) { g_cs2 = (mode == 0 || mode == 2) ? mode : 1; }
+
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens) {
   if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
@@ -548,7 +591,10 @@ int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
   if (!tc_eligible(h_q, h_kv, head_dim, max_len_extend) &&
       cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens))
     return 1;
+  // (the two-tile column split takes by default only calls the one-tile
+  // split would take: the same two launches)
   return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) ||
+          cs2_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) ||
           cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens) ||
           sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
              ? 2
@@ -575,7 +621,7 @@ namespace vsk {
 // scratch of the allocation-free entry point) is checked against is the one
 // the kernels use.
 struct CallPlan {
-  bool use_tc = false, use_cs = false, use_sl = false, use_cl = false;
+  bool use_tc = false, use_cs = false, use_sl = false, use_cl = false, use_cs2 = false;
   int cl = 0, cl_smem = 0;  // cluster form: CTAs per cluster, shared memory of one combine group
   Plan pl{};
   StreamPlan sp{};
@@ -595,8 +641,10 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   const bool same = D == DV;
   cp.use_tc = same && tc_eligible(h_q, h_kv, D, L);
   cp.use_cl = !cp.use_tc && cl_eligible(B, h_q, h_kv, D, DV, L, mean_len * B);
-  cp.use_cs = same && !cp.use_tc && !cp.use_cl && cs_eligible(h_q, h_kv, D, L, mean_len * B);
-  cp.use_sl = same && !cp.use_tc && !cp.use_cl && !cp.use_cs && sl_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_cs2 = same && !cp.use_tc && !cp.use_cl && cs2_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
+  cp.use_cs = same && !cp.use_tc && !cp.use_cl && !cp.use_cs2 && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_sl = same && !cp.use_tc && !cp.use_cl && !cp.use_cs && !cp.use_cs2 &&
+              sl_eligible(h_q, h_kv, D, L, mean_len * B);
   Plan& pl = cp.pl;
   if (cp.use_cl && D == 256) {
     // one KV head per cluster, streamed by the column split (two warps per
@@ -610,6 +658,8 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   } else if (cp.use_cl) {
     // one KV head per cluster, one 16-row tile per warp
     if (!make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B, 1, DV, 1)) return 0;
+  } else if (cp.use_cs2) {
+    if (!make_tc_plan(h_q, h_kv, D, L, fp8, pl) || !make_cs2_stream_plan(pl, D, fp8, cp.sp)) return 0;
   } else if ((cp.use_tc || cp.use_cs)
                  ? !make_tc_plan(h_q, h_kv, D, L, fp8, pl)
                  : !make_plan(h_q, h_kv, D, L, fp8, pl, mean_len * B,
@@ -639,10 +689,10 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
     pl.nst = ne;
     cp.threads = tc::kThreads;
-  } else if (cp.use_cs) {
-    cp.fn = pick_cs_kernel(fp8);
+  } else if (cp.use_cs || cp.use_cs2) {
+    cp.fn = cp.use_cs2 ? kernel_d256(fp8, 4) : pick_cs_kernel(fp8);
     cp.fn_comb = pick_combine_kernel(256, fp8);
-    if (!prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("column-split kernels unavailable");
+    if (!cp.fn || !prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("column-split kernels unavailable");
     cp.threads = cp.sp.threads;
     cp.smem = cp.sp.smem;
     per_sm = cp.sp.per_sm;
@@ -715,7 +765,8 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   if (g_min_tokens > 0) {
     cp.w_min = g_min_tokens;
   } else {
-    const long long per = (cp.use_cs || cp.use_sl || cp.use_cl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
+    const long long per =
+        (cp.use_cs || cp.use_cs2 || cp.use_sl || cp.use_cl) ? kPiecesPerSegmentColSplit : kPiecesPerSegment;
     const long long wp = (mean_len / per + kStageTokens - 1) / kStageTokens * kStageTokens;
     cp.w_min = std::max(kDefaultMinTokens, wp);
   }
@@ -755,8 +806,8 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
   p.n_stream = static_cast<int>(cp.n_cta);
   p.cl = cp.use_cl ? cp.cl : 0;
   p.cl_smem = cp.cl_smem;
-  if (cp.use_cs || (cp.use_cl && cp.D == 256)) {  // the column-split stream
-    p.nwc = 2 * pl.MT;
+  if (cp.use_cs || cp.use_cs2 || (cp.use_cl && cp.D == 256)) {  // the column-split streams
+    p.nwc = cp.sp.threads / 32;
     p.nst = cp.sp.nst;
     p.ring_off = cp.sp.ring_off;
     p.head_bytes = cp.sp.head_bytes;

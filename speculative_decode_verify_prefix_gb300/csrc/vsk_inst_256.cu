@@ -6,6 +6,8 @@
 namespace vsk {
 
 KernelFn kernel_d256(bool fp8, int variant) {
+  if (variant == 4) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 2, 2>)
+                               : static_cast<KernelFn>(vsk_kernel<256, false, 2, 2>);
   if (variant == 3) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, false, 256, false, true>)
                                : static_cast<KernelFn>(vsk_kernel<256, false, 1, 1, false, 256, false, true>);
   if (variant == 2) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 2, true, 256, true>)

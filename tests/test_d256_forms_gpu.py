@@ -7,6 +7,9 @@ beside each:
   tile, each holding half the head dimension), head_dim 256;
 - "split": the stream-only mma.sync kernel at head_dim 64 and 128 (every case
   below rewritten to one of them, chosen by a hash of its name);
+- "colsplit2": the column-split stream with both 16-row tiles in each warp
+  of the pair (head_dim 256, 17 to 32 packed rows; cases with fewer rows take
+  the one-tile split);
 - "cluster": the cluster form (one launch: a thread-block cluster per
   (sequence, KV head) streams it and folds its own partials after a cluster
   barrier), at head_dim 64, 128 or 256 (chosen by a hash of the case's name).
@@ -56,12 +59,13 @@ def gpu_problem(spec, **over):
 
 def _select(m, form):
     m.set_tuning_tc(form == "tc")
-    m.set_tuning_colsplit(2 if form == "colsplit" else 0)
+    m.set_tuning_colsplit(2 if form in ("colsplit", "colsplit2") else 0)
+    m.set_tuning_colsplit2(2 if form == "colsplit2" else 0)
     m.set_tuning_split_launch(2 if form == "split" else 0)
     m.set_tuning_cluster(2 if form == "cluster" else 0)
 
 
-@pytest.fixture(scope="module", params=["tc", "colsplit", "split", "cluster"])
+@pytest.fixture(scope="module", params=["tc", "colsplit", "colsplit2", "split", "cluster"])
 def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 
@@ -73,6 +77,7 @@ def vsk(request):
     m.set_tuning(0, 0)
     m.set_tuning_tc(False)
     m.set_tuning_colsplit(1)
+    m.set_tuning_colsplit2(1)
     m.set_tuning_split_launch(1)
     m.set_tuning_cluster(1)
     FORM["name"] = "tc"
