@@ -132,6 +132,10 @@ def parse_args(argv=None):
                          "two launches per call: vtc_kernel, then the combine kernel)")
     ap.add_argument("--report-configs", action="store_true",
                     help="print a per-configuration table (tiny, d256, GQA sweep, fp8, serving) instead of the JSON line")
+    ap.add_argument("--config-calls", type=int, default=0, metavar="N",
+                    help="call every small parity configuration (tiny, d256, GQA sweep, fp8) N times in its default "
+                         "form and print the kernel launches per call, nothing timed: the command an ncu launch list "
+                         "of those configurations runs")
     return ap.parse_args(argv)
 
 
@@ -623,10 +627,38 @@ def report_configs(args) -> str:
     return "\n".join(rows)
 
 
+def config_calls(n: int) -> None:
+    """Every small parity configuration, n calls each in its default form (in
+    the order tiny, d256, GQA sweep, fp8), one line per configuration with the
+    kernel launches each call makes: the launch list of an ncu run over this
+    command maps back to the configurations by those counts."""
+    import speculative_decode_verify_prefix_gb300 as vsk
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for spec in [workloads.TINY, workloads.D256] + workloads.gqa_sweep() + [workloads.FP8]:
+        prob = workloads.make_problem(spec, dev)
+        B = len(prob["prefix_lens"])
+        o = torch.empty(prob["q"].shape[0], spec.h_q, spec.dv, dtype=torch.bfloat16, device=dev)
+        ws = vsk.get_workspace(dev, B, spec.h_q, spec.h_kv, spec.d, spec.dv, spec.l_ext)
+        for _ in range(n):
+            assert _call(vsk, prob, o, ws), vsk.last_error()
+        torch.cuda.synchronize()
+        if vsk.read_error_flags(ws):
+            raise RuntimeError(f"device error flags after {spec.name}")
+        print(spec.name, vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, spec.l_ext,
+                                               prob["kv_indices"].shape[0]), flush=True)
+        del prob, o
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.report_configs:
         print(report_configs(args), flush=True)
+        return
+    if args.config_calls > 0:
+        config_calls(args.config_calls)
         return
     dist = Dist()
     try:

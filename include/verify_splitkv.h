@@ -351,19 +351,21 @@ void vsk_set_tuning_cluster(int mode);
 /* Tuning switch, for A/B runs: mode 1 launches the combine kernel of the
  * two-launch forms as a programmatic dependent of the prefix stream
  * (cudaLaunchAttributeProgrammaticStreamSerialization): its CTAs may start
- * while the stream runs, read the call's inputs (lengths, drafts, queries)
- * and wait for the stream grid before reading its partials.  Mode 0 (the
+ * while the stream runs, read the call's lengths, qo_indptr and draft-row
+ * locations, and wait for the stream grid before reading anything else.  Mode 0 (the
  * default; measured faster on GB300 for all but the smallest calls) launches
  * it after the stream in plain stream order.  The result is the same either
  * way.  Process-wide; not thread-safe. */
 void vsk_set_tuning_pdl(int mode);
 
 /* Tuning switch, for A/B runs: mode 1 (the default) runs the head_dim 256
- * one-launch kernel with software-pipelined stages (the softmax and PV
- * products of a 16-token stage are computed after the QK products of the
- * next stage are issued, so each warp interleaves two stages' work); mode 0
- * runs one stage after the other.  The result is the same either way.
- * Process-wide; not thread-safe. */
+ * one-launch kernel over fp8 e4m3 pools (ring of at least three stages) with
+ * software-pipelined stages (the softmax and PV products of a 16-token stage
+ * are computed after the QK products of the next stage are issued, so each
+ * warp interleaves two stages' work); mode 0 runs one stage after the other.
+ * bf16 pools always run one stage after the other (pipelining measured no
+ * faster there).  The result is the same either way.  Process-wide; not
+ * thread-safe. */
 void vsk_set_tuning_pipe(int mode);
 
 /* Kernel launches a call of these static shapes makes on its stream under the

@@ -331,8 +331,9 @@ def set_tuning_pdl(enabled: bool = False) -> None:
 
 
 def set_tuning_pipe(enabled: bool = True) -> None:
-    """Head_dim 256 one-launch kernel with software-pipelined stages (the
-    default) or one stage after the other; for A/B runs."""
+    """Head_dim 256 one-launch kernel over e4m3 pools with software-pipelined
+    stages (the default) or one stage after the other (bf16 pools always run
+    one stage after the other); for A/B runs."""
     _native.lib().vsk_set_tuning_pipe(1 if enabled else 0)
 
 

@@ -10,11 +10,15 @@
 // When this kernel starts, the stream launch before it on the same stream has
 // written every piece's partial, so no ticket or arrival order is needed: one
 // CTA per (segment, KV head of the segment, 16-row query tile, 32-column
-// slice of the output) reads the segment's pieces straight away.  Its four
-// warps split the pieces (each keeps a running maximum, sum and weighted
-// 16 x 32 block), meet in shared memory, and then compute the draft scores of
-// the tile (each warp a quarter of the head dimension, summed in a fixed
-// order), continue the softmax and write their 16 x 32 block of o.  The fused-store forms store the new
+// slice of the output) reads the segment's pieces straight away.  Thread t
+// owns row t / 8 of the tile and four output columns.  The pieces' 16 x 32
+// blocks are staged in shared memory by cp.async, nb pieces a batch with two
+// batches in flight (each thread copies the 16 bytes it will fold, each warp
+// the log-sum-exps of its four rows, so the fold needs no block barrier), and
+// every thread folds its columns with a running maximum and sum.  The CTA
+// then computes the draft scores of the tile (each warp a quarter of the head
+// dimension, summed in a fixed order), continues the softmax and writes its
+// 16 x 32 block of o.  The fused-store forms store the new
 // draft rows here too: tile 0's CTAs, each its 32-column slice of every row,
 // so every stored element has exactly one writer.
 //
@@ -29,6 +33,9 @@ constexpr int kThreads = 128;              // four warps
 constexpr int kCols = 32;                  // output columns per CTA
 constexpr int kMaxL = 32;                  // draft keys served
 constexpr int kScPitch = kMaxL + 1;
+constexpr int kPieceBytes = 16 * kCols * 4;  // one piece's staged 16 x 32 fp32 block
+constexpr int kPieceLseBytes = 16 * 4;       // ... and its 16 log-sum-exps
+constexpr int kBatchMax = 32;                // pieces per batch at most (one log-sum-exp copy per lane)
 // Shared-memory map of the head_dim D instance (bytes).
 template <int D>
 struct Geo {
@@ -39,18 +46,18 @@ struct Geo {
   static constexpr int kDstOff = kSrcOff + kMaxL * 8;    // [kMaxL] i64: row it is stored to (-1: none)
   static constexpr int kKOff = kDstOff + kMaxL * 8;      // [kMaxL][kKPitch] draft K rows
   static constexpr int kVOff = kKOff + kMaxL * kKPitch;  // [kMaxL][kCols] bf16 draft V slice
-  static constexpr int kFoldOff = kVOff + kMaxL * kCols * 2;  // per warp m[16], then l[16]
-  static constexpr int kAccOff = kFoldOff + 4 * 32 * 4;       // per warp [16][kCols] weighted sums
-  static constexpr int kScOff = kAccOff + 4 * 16 * kCols * 4;  // per warp [16][kScPitch] partial scores
-  static constexpr int kSmem = kScOff + 4 * 16 * kScPitch * 4;
-  static_assert(kSmem <= 48 * 1024, "combine kernel fits the default shared-memory window");
-  static_assert(kKOff % 16 == 0 && kVOff % 16 == 0 && kAccOff % 16 == 0, "16-byte aligned regions");
+  static constexpr int kScOff = kVOff + kMaxL * kCols * 2;     // per warp [16][kScPitch] partial scores
+  static constexpr int kStageOff = (kScOff + 4 * 16 * kScPitch * 4 + 127) & ~127;
+  // staged pieces: 2 nb blocks [16][kCols] fp32, then 2 nb x 16 log-sum-exps
+  static constexpr int smem(int nb) { return kStageOff + 2 * nb * (kPieceBytes + kPieceLseBytes); }
+  static_assert(smem(kBatchMax) <= 227 * 1024, "combine kernel fits an SM");
+  static_assert(kKOff % 16 == 0 && kVOff % 16 == 0 && kStageOff % 16 == 0, "16-byte aligned regions");
 };
 }  // namespace cmb
 
 // One unit of the combine: segment s_idx, KV head hc of the segment, 16-row
 // tile `tile`, 32-column slice ch, served by 128 threads (tid 0..127) with
-// the shared-memory region smem (Geo<D>::kSmem bytes).  CL = false: the
+// the shared-memory region smem (Geo<D>::smem(p.cmb_nb) bytes).  CL = false: the
 // combine kernel, which finds the segment's pieces by the stream launch's cut
 // of the work (a block scan) and synchronises with __syncthreads.  CL = true:
 // the cluster form, whose pieces are slot0 .. slot0 + npc - 1 and whose
@@ -63,7 +70,7 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
   using G = Geo<D>;
   constexpr int kKPitch = G::kKPitch;
   constexpr int kScanOff = G::kScanOff, kSrcOff = G::kSrcOff, kDstOff = G::kDstOff, kKOff = G::kKOff;
-  constexpr int kVOff = G::kVOff, kFoldOff = G::kFoldOff, kAccOff = G::kAccOff, kScOff = G::kScOff;
+  constexpr int kVOff = G::kVOff, kScOff = G::kScOff, kStageOff = G::kStageOff;
   constexpr int DW = D / 4;    // head dimensions of one warp's part of the draft scores
   constexpr int KSW = DW / 16;  // its k-steps
   const int lane = tid & 31, warp = tid >> 5;
@@ -79,15 +86,18 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
   Seg sg;
   sg.b = static_cast<int>(s_idx / p.n_hg);
   sg.hg = static_cast<int>(s_idx % p.n_hg);
+  // Every load below depends on the segment index alone: all are issued
+  // before any of them is used, so they cost one memory round trip together.
+  int qa, qe;  // the sequence's draft rows in q / k_ext / v_ext / o (qo_indptr)
+  if (p.qo) {
+    qa = __ldg(p.qo + sg.b);
+    qe = __ldg(p.qo + sg.b + 1);
+  } else {
+    qa = sg.b * p.L;
+    qe = qa + p.L;
+  }
   load_seq(p, sg.b, sg.P, sg.kv0);
-  sg.len = max(sg.P, 1);
-  const int kvh = sg.hg * p.HC + hc;
-  const int col0 = ch * kCols;
-  const bool writer = tile == 0;  // stores this CTA's column slice of the new drafts
-  const bool flagger = tid == 0 && ch == 0 && tile == 0 && hc == 0;
-
   // block sums of the virtual segment lengths: all of them and those before b
-  // (issued first: nothing else waits on fewer loads)
   long long* scan = reinterpret_cast<long long*>(smem + kScanOff);
   if constexpr (!CL) {
     long long tot_t = 0, bef_t = 0;
@@ -109,13 +119,16 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
       scan[4 + warp] = bef_t;
     }
   }
-  // the sequence's draft rows in q / k_ext / v_ext / o (qo_indptr, validated)
+  sg.len = max(sg.P, 1);
+  const int kvh = sg.hg * p.HC + hc;
+  const int col0 = ch * kCols;
+  const bool writer = tile == 0;  // stores this CTA's column slice of the new drafts
+  const bool flagger = tid == 0 && ch == 0 && tile == 0 && hc == 0;
   int s_b;
   {
-    const int a = p.qo ? __ldg(p.qo + sg.b) : sg.b * p.L, e = p.qo ? __ldg(p.qo + sg.b + 1) : (sg.b + 1) * p.L;
-    const bool ok = a >= 0 && e - a == p.L && static_cast<long long>(a) + p.L <= p.n_rows;
+    const bool ok = qa >= 0 && qe - qa == p.L && static_cast<long long>(qa) + p.L <= p.n_rows;
     if (!ok && flagger) atomicOr(p.err, kErrBadQoIndptr);
-    s_b = ok ? a : sg.b * p.L;
+    s_b = ok ? qa : sg.b * p.L;
   }
   // per draft key: the row it is read from and the row it is stored to
   long long* ksrc = reinterpret_cast<long long*>(smem + kSrcOff);
@@ -154,13 +167,54 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
     slot0 = c_first + s_idx;     // partial of piece i, this head: (slot0 + i) HC + hc
   }
 
+  // Everything above reads only the call's inputs.  The combine kernel is
+  // launched as a programmatic dependent of the stream launch, so it may have
+  // started while the stream still runs: wait for that grid to complete (and
+  // its partials to be visible) before reading them.  Without such a launch
+  // the wait returns at once.
+  if constexpr (!CL) asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- stage the pieces: batch k (pieces k nb .. k nb + nb - 1) into half k % 2 ----
+  // Thread t copies (and later folds) row t / 8, 16-byte chunk t % 8 of every
+  // piece's 16 x 32 block; lane u < n of each warp copies piece u's four
+  // log-sum-exps of the warp's rows.  One cp.async group per batch.  The
+  // cluster form's pieces (at most 2 nb: its CTAs) go in one batch.
+  const int nb = p.cmb_nb;
+  const long long nbatch = CL ? 1 : (npc + nb - 1) / nb;
+  unsigned char* blk = smem + kStageOff;
+  unsigned char* lse_st = blk + 2 * nb * kPieceBytes;
+  const int fr = tid >> 3, fch = tid & 7;  // row of the tile, 16-byte chunk of the 32 columns
+  auto batch_n = [&](long long k) -> int {
+    return CL ? static_cast<int>(npc) : static_cast<int>(min(static_cast<long long>(nb), npc - k * nb));
+  };
+  auto batch_h0 = [&](long long k) -> int { return CL ? 0 : static_cast<int>(k & 1) * nb; };
+  auto issue = [&](long long k) {
+    const long long i0 = k * nb;
+    const int n = batch_n(k);
+    const int h0 = batch_h0(k);
+    for (int u = 0; u < n; ++u) {
+      const long long sl = (slot0 + i0 + u) * p.HC + hc;
+      cp_async_16(smem_u32(blk + (h0 + u) * kPieceBytes + fr * (kCols * 4) + fch * 16),
+                  p.po + (sl * RM + 16 * tile + fr) * D + col0 + fch * 4);
+    }
+    if (lane < n) {
+      const long long sl = (slot0 + i0 + lane) * p.HC + hc;
+      cp_async_16(smem_u32(lse_st + (h0 + lane) * kPieceLseBytes + warp * 16), p.plse + sl * RM + 16 * tile + 4 * warp);
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  if (nbatch > 1) issue(1);
+
   // ---- stage the draft K rows (whole head dimension) and this slice of V ----
-  // Plain drafts (k_extend / v_extend, no store) go by cp.async and land while
-  // the pieces are folded; the cache and store forms convert in registers.
+  // Plain drafts (k_extend / v_extend, no store) go by cp.async, one group
+  // committed after the first two batches, and land while the pieces are
+  // folded; the cache and store forms convert in registers.
   const int LK = (p.L + 7) & ~7;  // whole 8-key groups (keys past L staged as zero)
   unsigned char* kst = smem + kKOff;
   unsigned char* vst = smem + kVOff;
-  if (!p.paged && p.wmode == 0) {
+  const bool plain_drafts = !p.paged && p.wmode == 0;
+  if (plain_drafts) {
     for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
       const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
       unsigned char* dk = kst + key * kKPitch + d * 2;
@@ -175,7 +229,9 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
                  p.ve + ksrc[key] * p.ve_s0 + static_cast<long long>(kvh) * p.ve_s1 + col0 + c);
     }
     cp_async_commit();
-  } else {
+  }
+
+  if (!plain_drafts) {
     for (int idx = tid; idx < LK * (D / 2); idx += kThreads) {
       const int key = idx / (D / 2), d = (idx % (D / 2)) * 2;
       uint32_t val = 0u;
@@ -249,65 +305,44 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
     load_q<KSW>(p, sg, hc, r0, r0 + 8, j, false, qf, DW * warp);
   }
 
-  // Everything above reads only the call's inputs.  The combine kernel is
-  // launched as a programmatic dependent of the stream launch, so it may have
-  // started while the stream still runs: wait for that grid to complete (and
-  // its partials to be visible) before reading them.  Without such a launch
-  // the wait returns at once.
-  if constexpr (!CL) asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- fold: warp w takes pieces w, w + 4, ...; lane = (row, 16 columns) ----
-  const int fr = lane >> 1, fc = (lane & 1) * 16;
-  float fm = NEG_INF, fl = 0.f, fa[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) fa[k] = 0.f;
-  auto fold_one = [&](float x, const float4 (&v)[4]) {
-    if (x == NEG_INF) return;  // a piece with nothing visible
-    const float mn = fmaxf(fm, x);
-    const float sc = exp2f(fm - mn);  // 0 while fm is -inf
-    const float w = exp2f(x - mn);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      fa[4 * k + 0] = fmaf(fa[4 * k + 0], sc, w * v[k].x);
-      fa[4 * k + 1] = fmaf(fa[4 * k + 1], sc, w * v[k].y);
-      fa[4 * k + 2] = fmaf(fa[4 * k + 2], sc, w * v[k].z);
-      fa[4 * k + 3] = fmaf(fa[4 * k + 3], sc, w * v[k].w);
-    }
-    fl = fmaf(fl, sc, w);
-    fm = mn;
-  };
-  {
-    const int prow = 16 * tile + fr;
+  // ---- fold: this thread's row and four columns over every piece, in piece order ----
+  float fm = NEG_INF, fl = 0.f, fa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-    for (long long i = warp; i < npc; i += 8) {
-      const bool two = i + 4 < npc;  // uniform across the warp
-      const long long sa = (slot0 + i) * p.HC + hc, sb = (slot0 + (two ? i + 4 : i)) * p.HC + hc;
-      const float xa = __ldcg(p.plse + sa * RM + prow);
-      const float xb = __ldcg(p.plse + sb * RM + prow);
-      const float4* oa = reinterpret_cast<const float4*>(p.po + (sa * RM + prow) * D + col0 + fc);
-      const float4* ob = reinterpret_cast<const float4*>(p.po + (sb * RM + prow) * D + col0 + fc);
-      float4 va[4], vb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        va[k] = __ldcg(oa + k);
-        vb[k] = __ldcg(ob + k);
+  for (long long k = 0; k < nbatch; ++k) {
+    // groups committed after batch k: batch k + 1 (if any) and, for k < 2,
+    // the plain drafts' group (committed after batch 1)
+    cp_async_wait_dyn((k + 1 < nbatch ? 1 : 0) + (k < 2 && plain_drafts ? 1 : 0));
+    __syncwarp();  // the warp's log-sum-exp copies
+    const int n = batch_n(k);
+    const int h0 = batch_h0(k);
+#pragma unroll 1
+    for (int u = 0; u < n; ++u) {
+      const float x = *reinterpret_cast<const float*>(lse_st + (h0 + u) * kPieceLseBytes + fr * 4);
+      if (x == NEG_INF) continue;  // a piece with nothing visible
+      const float4 v = *reinterpret_cast<const float4*>(blk + (h0 + u) * kPieceBytes + fr * (kCols * 4) + fch * 16);
+      if (x > fm) {
+        const float sc = exp2f(fm - x);  // 0 while fm is -inf
+        fa[0] *= sc;
+        fa[1] *= sc;
+        fa[2] *= sc;
+        fa[3] *= sc;
+        fl *= sc;
+        fm = x;
       }
-      fold_one(xa, va);
-      if (two) fold_one(xb, vb);
+      const float w = exp2f(x - fm);
+      fa[0] = fmaf(w, v.x, fa[0]);
+      fa[1] = fmaf(w, v.y, fa[1]);
+      fa[2] = fmaf(w, v.z, fa[2]);
+      fa[3] = fmaf(w, v.w, fa[3]);
+      fl += w;
+    }
+    if constexpr (!CL) {
+      __syncwarp();  // every lane is done with half k % 2 before it is refilled
+      if (k + 2 < nbatch) issue(k + 2);
     }
   }
-  float* sm_m = reinterpret_cast<float*>(smem + kFoldOff) + warp * 32;
-  float* sm_a = reinterpret_cast<float*>(smem + kAccOff) + warp * 16 * kCols;
-  if ((lane & 1) == 0) {
-    sm_m[fr] = fm;
-    sm_m[16 + fr] = fl;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    *reinterpret_cast<float4*>(sm_a + fr * kCols + fc + 4 * k) =
-        make_float4(fa[4 * k], fa[4 * k + 1], fa[4 * k + 2], fa[4 * k + 3]);
   cp_async_wait<0>();
-  sync();  // staged drafts, fold partials
+  sync();  // staged drafts
 
   // ---- draft scores: this warp's DW-wide part of q . k for every 8-key group ----
   float* scp = reinterpret_cast<float*>(smem + kScOff) + warp * 16 * kScPitch;
@@ -328,28 +363,12 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
   }
   sync();
 
-  // ---- per thread: row r of the tile, 4 output columns ----
-  const int r = tid >> 3, c4 = (tid & 7) * 4;
+  // ---- per thread: row r of the tile, 4 output columns (the fold's own) ----
+  const int r = fr, c4 = fch * 4;
   const int prow = 16 * tile + r;
-  const float* fm_all = reinterpret_cast<const float*>(smem + kFoldOff);
-  const float* fa_all = reinterpret_cast<const float*>(smem + kAccOff);
-  float M = NEG_INF;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) M = fmaxf(M, fm_all[w * 32 + r]);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float l = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float mw = fm_all[w * 32 + r];
-    if (mw == NEG_INF) continue;
-    const float s = exp2f(mw - M);
-    l = fmaf(fm_all[w * 32 + 16 + r], s, l);
-    const float4 a = *reinterpret_cast<const float4*>(fa_all + (w * 16 + r) * kCols + c4);
-    acc[0] = fmaf(a.x, s, acc[0]);
-    acc[1] = fmaf(a.y, s, acc[1]);
-    acc[2] = fmaf(a.z, s, acc[2]);
-    acc[3] = fmaf(a.w, s, acc[3]);
-  }
+  const float M = fm;
+  float acc[4] = {fa[0], fa[1], fa[2], fa[3]};
+  float l = fl;
   // draft visibility: causal, or the tree mask rows (row-major [L][P+L], only
   // the draft columns are read; inconsistent offsets fall back to causal)
   long long mbase = -1;

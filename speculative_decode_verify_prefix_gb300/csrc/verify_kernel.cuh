@@ -118,6 +118,7 @@ struct Params {
   int n_stream;  // CTAs of the stream launch (read by the combine kernel of the two-launch forms)
   int cl;        // cluster form: CTAs per cluster (one cluster per segment); 0 otherwise
   int cl_smem;   // cluster form: shared-memory bytes of one combine group (128 threads)
+  int cmb_nb;    // combine: pieces staged per batch (two batches in flight), 1 .. 32
   const unsigned char* cmask;  // tree verify: per-sequence [L][P+L] draft visibility (nullptr: causal)
   const void* mindptr;
   int mindptr64;
@@ -164,6 +165,10 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// 16-byte global -> shared copy through L2 only
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }

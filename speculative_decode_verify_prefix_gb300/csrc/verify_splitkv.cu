@@ -47,7 +47,7 @@ int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxW
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 int g_cs2 = 1;    // two-tile column split at head_dim 256: 1 e4m3 pools past kColSplitMaxWork, 2 always, 0 never
 int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
-int g_pipe = 1;   // head_dim 256 one-launch kernel with pipelined stages (1) or not (0)
+int g_pipe = 1;   // head_dim 256 one-launch kernel over e4m3 pools with pipelined stages (1) or not (0)
 int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
 
 struct Plan {
@@ -410,8 +410,9 @@ KernelFn pick_so_kernel(int D, bool fp8, int mtw) {
 
 KernelFn pick_combine_kernel(int D, bool fp8) { return kernel_combine(D, fp8); }
 
-int combine_smem(int D) {
-  return D == 64 ? cmb::Geo<64>::kSmem : D == 128 ? cmb::Geo<128>::kSmem : cmb::Geo<256>::kSmem;
+// Shared memory of one combine unit staging nb pieces a batch.
+int combine_smem(int D, int nb) {
+  return D == 64 ? cmb::Geo<64>::smem(nb) : D == 128 ? cmb::Geo<128>::smem(nb) : cmb::Geo<256>::smem(nb);
 }
 
 
@@ -623,6 +624,7 @@ namespace vsk {
 struct CallPlan {
   bool use_tc = false, use_cs = false, use_sl = false, use_cl = false, use_cs2 = false;
   int cl = 0, cl_smem = 0;  // cluster form: CTAs per cluster, shared memory of one combine group
+  int cmb_nb = 8;           // combine units: pieces staged per batch (two batches in flight)
   Plan pl{};
   StreamPlan sp{};
   KernelFn fn = nullptr, fn_comb = nullptr;
@@ -704,16 +706,19 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     const int nw = D == 256 ? cp.sp.threads / 32 : pl.nwc;  // streaming warps
     const int groups = std::max(nw, 4) / 4;
     cp.threads = groups * cmb::kThreads;
-    cp.cl_smem = (combine_smem(static_cast<int>(D)) + 127) & ~127;
+    const long long n_seg = B * pl.n_hg;
+    long long c = (mean_len + kClTokensPerCta - 1) / kClTokensPerCta;
+    c = std::max(1LL, std::min<long long>(c, kClMax));
+    while (c > 1 && n_seg * c > 4LL * sms) --c;  // the workspace bound: at most 4 CTAs per SM
+    // a segment's pieces are the cluster's CTAs: two batches of ceil(c / 2)
+    // hold them all (the checks below only lower c)
+    cp.cmb_nb = static_cast<int>((c + 1) / 2);
+    cp.cl_smem = (combine_smem(static_cast<int>(D), cp.cmb_nb) + 127) & ~127;
     // every warp of the CTA (streaming or not) has its index / mask / query region
     const size_t misc_end = D == 256 ? static_cast<size_t>(cp.sp.misc_off) + 4 * groups * cp.sp.misc_bytes
                                      : static_cast<size_t>(pl.misc_off) + 4 * groups * pl.misc_bytes;
     cp.smem = std::max({D == 256 ? cp.sp.smem : cp.smem, misc_end, static_cast<size_t>(groups) * cp.cl_smem});
     if (cp.smem > static_cast<size_t>(kSmemPerCTAMax)) return fail("cluster-form shared memory plan too large");
-    const long long n_seg = B * pl.n_hg;
-    long long c = (mean_len + kClTokensPerCta - 1) / kClTokensPerCta;
-    c = std::max(1LL, std::min<long long>(c, kClMax));
-    while (c > 1 && n_seg * c > 4LL * sms) --c;  // the workspace bound: at most 4 CTAs per SM
     if (c > 8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(cp.fn),
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       c = 8;
@@ -756,6 +761,10 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     // one combine CTA per (segment, 16-row tile, 32-column slice)
     cp.n_comb = B * pl.n_hg * pl.HC * pl.MT * (D / cmb::kCols);
     if (cp.n_comb > 0x7FFFFFFFLL) return fail("combine grid of %lld CTAs too large", cp.n_comb);
+    // pieces in flight per CTA against CTAs per SM: a grid of at most two
+    // CTAs per SM stages 2 x 16 pieces (two CTAs fit an SM), up to three
+    // CTAs per SM 2 x 8, larger grids 2 x 4
+    cp.cmb_nb = cp.n_comb <= 2LL * sms ? 16 : cp.n_comb <= 3LL * sms ? 8 : 4;
   }
   // Smallest CTA share, from static shapes only (no device read, graph
   // safe): at least 64 tokens and, for small batches where the shares get
@@ -806,6 +815,7 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
   p.n_stream = static_cast<int>(cp.n_cta);
   p.cl = cp.use_cl ? cp.cl : 0;
   p.cl_smem = cp.cl_smem;
+  p.cmb_nb = cp.cmb_nb;
   if (cp.use_cs || cp.use_cs2 || (cp.use_cl && cp.D == 256)) {  // the column-split streams
     p.nwc = cp.sp.threads / 32;
     p.nst = cp.sp.nst;
@@ -851,7 +861,7 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(cp.n_comb));
     cfg.blockDim = dim3(cmb::kThreads);
-    cfg.dynamicSmemBytes = combine_smem(cp.D);
+    cfg.dynamicSmemBytes = combine_smem(cp.D, cp.cmb_nb);
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = g_pdl ? 1 : 0;
