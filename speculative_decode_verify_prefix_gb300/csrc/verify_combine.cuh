@@ -179,7 +179,12 @@ __device__ __forceinline__ void combine_unit(const Params& p, unsigned char* sme
   // piece's 16 x 32 block; lane u < n of each warp copies piece u's four
   // log-sum-exps of the warp's rows.  One cp.async group per batch.  The
   // cluster form's pieces (at most 2 nb: its CTAs) go in one batch.
-  const int nb = p.cmb_nb;
+  const int nb = max(1, min(p.cmb_nb, kBatchMax));  // the host's choice, within what the copies serve
+  if (CL && npc > 2 * nb) {
+    // the host sizes the cluster form's slots for its cluster: never taken
+    if (flagger) atomicOr(p.err, kErrBadKvIndptr);
+    npc = 2 * nb;
+  }
   const long long nbatch = CL ? 1 : (npc + nb - 1) / nb;
   unsigned char* blk = smem + kStageOff;
   unsigned char* lse_st = blk + 2 * nb * kPieceBytes;

@@ -715,6 +715,32 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     check(ob, oracle_o(pb), scaled=SCALED)
 
 
+def _combine_grid_specs():
+    # The combine kernel stages 2 x nb pieces per CTA, nb chosen by its grid
+    # (16 up to two CTAs per SM, 8 up to three, 4 beyond).  With 32 combine
+    # CTAs per sequence at both shapes below, 8 / 12 / 20 sequences fall in the
+    # three classes on a 152-SM GB300; lengths up to 3,000 tokens give
+    # segments of tens of pieces, so several batches run per CTA.
+    rng = np.random.default_rng(811)
+    out = []
+    for B in (8, 12, 20):
+        lens = tuple(int(x) for x in rng.integers(100, 3000, B))
+        out.append(workloads.Spec(f"combine_b{B}_d128", lens, 4, 32, 8, 128, 128, perm=True, seed=811 + B))
+        out.append(workloads.Spec(f"combine_b{B}_d256_fp8", lens, 4, 16, 2, 256, 256, pool="e4m3", perm=True,
+                                  k_scale=0.5, v_scale=0.25, seed=831 + B))
+    return out
+
+
+@pytest.mark.parametrize("spec", _combine_grid_specs(), ids=lambda s: s.name)
+def test_combine_kernel_grid_sizes(vsk, spec):
+    """Two-launch calls whose combine grids take each staging batch size."""
+    p = gpu_problem(spec)
+    B = len(spec.prefix_lens)
+    assert vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, spec.l_ext, p["kv_indices"].shape[0]) == 2
+    check(run_gpu(vsk, p), oracle_o(p), scaled=SCALED)
+    assert vsk.read_error_flags() == 0
+
+
 TILES = [
     workloads.Spec("tiles_r32", (700, 0, 2100), 4, 16, 2, 128, 128, perm=True, seed=601),
     workloads.Spec("tiles_r64_fp8", (333, 1500), 8, 8, 1, 128, 128, pool="e4m3", perm=True, k_scale=0.5,
