@@ -451,6 +451,7 @@ def run_ours(args, dist: Dist) -> dict:
     vsk.set_tuning_tc(tc)
     vsk.set_tuning_colsplit(0 if args.one_launch else 1)
     vsk.set_tuning_split_launch(0 if args.one_launch else 1)
+    vsk.set_tuning_cluster(0 if args.one_launch else 1)
     prob = workloads.make_problem(spec, dev)
     B = len(prob["prefix_lens"])
     nbytes = workloads.algorithmic_bytes(prob)
@@ -477,10 +478,13 @@ def run_ours(args, dist: Dist) -> dict:
     else:
         tokens = prob["kv_indices"].shape[0]
     launches = vsk.launches_per_call(B, spec.h_q, spec.h_kv, spec.d, prob["max_len_extend"], tokens)
-    kernel = ("vtc_kernel (+ vsk_combine_kernel)" if tc else
-              "vsk_kernel column-split stream (+ vsk_combine_kernel)" if launches == 2 and spec.d == 256 else
-              "vsk_kernel stream only (+ vsk_combine_kernel)" if launches == 2 else
-              "vsk_kernel<128,false>" if spec.d == 128 and spec.pool == "bf16" else "vsk_kernel")
+    form = vsk.call_form(B, spec.h_q, spec.h_kv, spec.d, spec.dv, prob["max_len_extend"], tokens,
+                         spec.pool == "e4m3")
+    kernel = {"tensor_memory": "vtc_kernel (+ vsk_combine_kernel)",
+              "column_split": "vsk_kernel column-split stream (+ vsk_combine_kernel)",
+              "column_split_two_tiles": "vsk_kernel two-tile column-split stream (+ vsk_combine_kernel)",
+              "stream_only": "vsk_kernel stream only (+ vsk_combine_kernel)",
+              "cluster": "vsk_kernel cluster form"}.get(form, f"vsk_kernel<{spec.d},{str(spec.pool == 'e4m3').lower()}>")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),

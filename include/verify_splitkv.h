@@ -302,10 +302,12 @@ void vsk_set_tuning_tc(int mode);
  * a second launch on the same stream (the combine kernel: one CTA per
  * segment, 16-row tile and 32-column slice).  Mode 1 (the default) takes that
  * form when the call's prefix tokens (kv_indices entries, or block-table
- * capacity for the paged entry points) times h_kv are at most 1,048,576, where
- * it is the faster one on GB300; mode 2 always takes it; mode 0 never does.
- * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
- * up to rounding order.  Process-wide; not thread-safe. */
+ * capacity for the paged entry points) times h_kv are below 262,144 (bf16
+ * pools) or 131,072 (e4m3), where it is the faster one on GB300 (from there
+ * the stream-only kernel of vsk_set_tuning_split_launch takes over); mode 2
+ * always takes it; mode 0 never does.  vsk_set_tuning_tc(1) takes
+ * precedence.  All forms compute the same result up to rounding order.
+ * Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
 
 /* Tuning switch, for A/B runs and tests, over head_dim 256 calls with 17 to 32
@@ -313,24 +315,26 @@ void vsk_set_tuning_colsplit(int mode);
  * tiles in each warp (one warp pair per KV head, each warp half of the head
  * dimension for both tiles, so every K / V element is loaded and, for an
  * e4m3 pool, converted once per head), then the combine kernel in a second
- * launch.  Mode 1 (the default) takes it, for e4m3 pools with at least
- * 131,072 prefix tokens x KV heads, where the one-tile split of
- * vsk_set_tuning_colsplit would serve the call (it measured faster there;
- * smaller calls keep the one-tile split, longer ones the one-launch kernel);
- * mode 2 takes it wherever it applies, any pool and size; mode 0 never.  All forms compute the same result up to rounding order.
- * Process-wide; not thread-safe. */
+ * launch.  Mode 2 takes it wherever it applies, any pool and size; modes 0
+ * and 1 (the default) never do: it beat the one-tile split on mid-size e4m3
+ * calls, but the stream-only kernel of vsk_set_tuning_split_launch measured
+ * faster still there.  All forms compute the same result up to rounding
+ * order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit2(int mode);
 
-/* Tuning switch, for A/B runs and tests, over head_dim 64 and 128 calls with at
- * most 32 draft rows per sequence: the prefix is streamed by a stream-only
- * instance of the mma.sync kernel and the per-piece partials are folded, the
- * draft block added and o written by the combine kernel in a second launch on
- * the same stream (instead of the one-launch kernel's ticketed tail).  Mode 1
- * (the default) takes that form when the call's prefix tokens times h_kv are
- * at least 2,048 and at most 4,194,304 (8,388,608 when (h_q / h_kv) *
- * max_len_extend <= 16), where it measured faster on GB300; mode 2 always
- * takes it; mode 0 never does.  All forms compute the same result up to
- * rounding order.  Process-wide; not thread-safe. */
+/* Tuning switch, for A/B runs and tests, over calls with at most 32 draft
+ * rows per sequence (head_dim == v_head_dim): the prefix is streamed by a
+ * stream-only instance of the mma.sync kernel and the per-piece partials are
+ * folded, the draft block added and o written by the combine kernel in a
+ * second launch on the same stream (instead of the one-launch kernel's
+ * ticketed tail).  Mode 1 (the default) takes that form where it measured
+ * faster on GB300: at head_dim 64 / 128 when the call's prefix tokens times
+ * h_kv are at least 2,048 and at most 4,194,304 (8,388,608 when (h_q / h_kv) *
+ * max_len_extend <= 16); at head_dim 256 with at most 32 packed rows per KV
+ * head from where the column split stops (262,144 bf16, 131,072 e4m3; 2,048
+ * with the column split off) up to 8,388,608.  Mode 2 always takes it; mode 0
+ * never does.  All forms compute the same result up to rounding order.
+ * Process-wide; not thread-safe. */
 void vsk_set_tuning_split_launch(int mode);
 
 /* Tuning switch, for A/B runs and tests: the cluster form.  One
@@ -378,6 +382,16 @@ void vsk_set_tuning_pipe(int mode);
  * launch counts. */
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens);
+
+/* The form a call of these static shapes takes under the current tuning
+ * switches, as a static string: "one_launch" (the persistent kernel, tickets
+ * for the merge), "cluster" (one launch of thread-block clusters),
+ * "column_split", "column_split_two_tiles", "stream_only" or "tensor_memory"
+ * (each a prefix stream, then the combine kernel), or "" for shapes no entry
+ * point accepts.  fp8_pool: nonzero for an e4m3 K/V pool (some cut-overs
+ * depend on it).  prefix_tokens as for vsk_launches_per_call.  Host only. */
+const char* vsk_call_form(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t v_head_dim,
+                          int64_t max_len_extend, int64_t prefix_tokens, int fp8_pool);
 
 /* Size, in bytes, of the scratch array built into the library for
  * verify_splitkv_fwd_noalloc (32 MiB). */

@@ -136,6 +136,8 @@ def _bind(lib):
     lib.vsk_set_tuning_colsplit2.argtypes = [ctypes.c_int]
     lib.vsk_launches_per_call.restype = ctypes.c_int
     lib.vsk_launches_per_call.argtypes = [ctypes.c_int64] * 6
+    lib.vsk_call_form.restype = ctypes.c_char_p
+    lib.vsk_call_form.argtypes = [ctypes.c_int64] * 7 + [ctypes.c_int]
     lib.vsk_set_tuning_shape.restype = None
     lib.vsk_set_tuning_shape.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.vsk_last_error.restype = ctypes.c_char_p

@@ -304,15 +304,16 @@ def set_tuning_colsplit(mode: int = 1) -> None:
 
 def set_tuning_colsplit2(mode: int = 1) -> None:
     """Head_dim 256 calls with 17-32 packed rows per KV head: the column split
-    with both tiles in each warp for e4m3 pools past the one-tile split's window
-    (1, the default), wherever it applies (2) or never (0); for A/B runs and tests."""
+    with both tiles in each warp wherever it applies (2) or never (0 and 1, the
+    default: the stream-only kernel measured faster); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_colsplit2(int(mode))
 
 
 def set_tuning_split_launch(mode: int = 1) -> None:
-    """Head_dim 64 / 128 calls (at most 32 drafts): stream-only kernel plus a
-    combine launch for small calls (1, the default), always (2) or never (0);
-    for A/B runs and tests."""
+    """Calls with at most 32 drafts: stream-only kernel plus a combine launch
+    (head_dim 64 / 128: small and mid-size calls; head_dim 256: from where the
+    column split stops up to 2^23 prefix tokens x KV heads) by size (1, the
+    default), always (2) or never (0); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_split_launch(int(mode))
 
 
@@ -344,6 +345,16 @@ def launches_per_call(batch: int, h_q: int, h_kv: int, head_dim: int, max_len_ex
     block-table columns x page_size for the paged entry points."""
     return int(_native.lib().vsk_launches_per_call(int(batch), int(h_q), int(h_kv), int(head_dim),
                                                    int(max_len_extend), int(prefix_tokens)))
+
+
+def call_form(batch: int, h_q: int, h_kv: int, head_dim: int, v_head_dim: int, max_len_extend: int,
+              prefix_tokens: int, fp8_pool: bool = False) -> str:
+    """The form a call of these shapes takes ("one_launch", "cluster",
+    "column_split", "column_split_two_tiles", "stream_only", "tensor_memory";
+    "" if no entry point accepts them); ``prefix_tokens`` as for
+    ``launches_per_call``."""
+    return _native.lib().vsk_call_form(int(batch), int(h_q), int(h_kv), int(head_dim), int(v_head_dim),
+                                       int(max_len_extend), int(prefix_tokens), 1 if fp8_pool else 0).decode()
 
 
 def version() -> str:

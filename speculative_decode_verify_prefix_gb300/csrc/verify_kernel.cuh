@@ -55,8 +55,9 @@ constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
 constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
-constexpr long long kColSplitMaxWork = 1LL << 20;  // prefix tokens x KV heads up to which head_dim 256 splits columns
-constexpr long long kColSplit2MinWork = 1LL << 17;  // ... from which e4m3 pools take the two-tile split instead
+constexpr long long kColSplitEndBf16 = 1LL << 18;  // prefix tokens x KV heads below which head_dim 256 splits columns (bf16)
+constexpr long long kColSplitEndE4m3 = 1LL << 17;  // ... (e4m3 pools); from there the stream-only kernel + combine
+constexpr long long kSplit256MaxWork = 1LL << 23;   // ... up to which head_dim 256 takes the stream-only kernel + combine
 constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
 constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
 constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
@@ -1858,8 +1859,9 @@ KernelFn kernel_d64(bool fp8, int mtw, bool so, bool cl = false);
 KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl = false);
 // head_dim 256 (D = Dv): one-launch kernel (variant 0), column-split stream
 // (variant 1), the cluster form streaming by column split (variant 2), the
-// one-launch kernel with pipelined stages (variant 3) or the column-split
-// stream with two tiles per warp (variant 4)
+// one-launch kernel with pipelined stages (variant 3), the column-split
+// stream with two tiles per warp (variant 4), the stream-only kernel of the
+// two-launch form (variant 5; variant 6: e4m3 pools with pipelined stages)
 KernelFn kernel_d256(bool fp8, int variant);
 // tensor-memory stream, head_dim 256, rm = 16 or 32 packed rows
 KernelFn kernel_tc(bool fp8, int rm);

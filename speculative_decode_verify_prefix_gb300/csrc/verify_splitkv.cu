@@ -43,9 +43,9 @@ int g_max_stages = 0;
 int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
 int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
-int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitMaxWork, 2 always, 0 never
+int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitEnd*, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
-int g_cs2 = 1;    // two-tile column split at head_dim 256: 1 e4m3 pools past kColSplitMaxWork, 2 always, 0 never
+int g_cs2 = 1;    // two-tile column split at head_dim 256: 2 always; 0 and 1 (the default) never
 int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
 int g_pipe = 1;   // head_dim 256 one-launch kernel over e4m3 pools with pipelined stages (1) or not (0)
 int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
@@ -166,41 +166,46 @@ bool make_tc_plan(long long h_q, long long h_kv, long long D, long long L, bool 
 // most 32 packed rows per KV head.  The workspace / epilogue plan is the
 // tensor-memory one (one KV head per segment, MT = RM / 16, the epilogue in
 // MT warps); the stream runs 2 MT warps per CTA, three CTAs per SM.  Lighter
-// warps, more CTAs and the ticket-free combine launch shorten small calls; on
-// long ones the pair exchange costs more than it saves, so by default only
-// calls of at most kColSplitMaxWork prefix tokens x KV heads (from static
-// shapes) take it.
-bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
+// warps and more CTAs shorten small calls; from kColSplitEndBf16 (bf16) or
+// kColSplitEndE4m3 (e4m3) prefix tokens x KV heads (static shapes) the
+// stream-only one-tile kernel with the combine launch measured faster, so by
+// default only smaller calls take it.
+long long col_split_end(bool fp8) { return fp8 ? kColSplitEndE4m3 : kColSplitEndBf16; }
+bool cs_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens, bool fp8) {
   if (g_cs == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0 || (h_q / h_kv) * L > 32) return false;
-  return g_cs == 2 || total_tokens * h_kv <= kColSplitMaxWork;
+  return g_cs == 2 || total_tokens * h_kv < col_split_end(fp8);
 }
 // Column-split stream with both 16-row tiles in each warp of the pair
 // (vsk_kernel<256, ., 2, 2>): head_dim 256 with 17 to 32 packed rows per KV
 // head.  Each K / V element is converted (e4m3 pools) and loaded from shared
 // memory once per head instead of once per tile, at the price of the pair's
-// score exchange each stage; by default taken for e4m3 pools inside the
-// one-tile split's size window (instead of it) from kColSplit2MinWork prefix
-// tokens x KV heads, where it measured faster (smaller calls: the one-tile
-// split's lighter CTAs are faster).
-bool cs2_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens, bool fp8) {
-  if (g_cs2 == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
+// score exchange each stage.  It beat the one-tile split on mid-size e4m3
+// calls, but the stream-only one-tile kernel with the combine launch
+// measured faster still there, so only mode 2 takes it.
+bool cs2_eligible(long long h_q, long long h_kv, long long D, long long L) {
+  if (g_cs2 != 2 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
   const long long R = (h_q / h_kv) * L;
-  if (R <= 16 || R > 32) return false;
-  const long long work = total_tokens * h_kv;
-  return g_cs2 == 2 || (fp8 && g_cs != 0 && work >= kColSplit2MinWork && (g_cs == 2 || work <= kColSplitMaxWork));
+  return R > 16 && R <= 32;
 }
-// Stream-only vsk_kernel then the combine kernel, for head_dim 64 / 128 calls
-// with at most cmb::kMaxL drafts: small and mid-size calls, where the
-// one-launch kernel's tail (tickets, a two-level fold of the pieces, the
-// draft block) is a chain of memory round trips that the combine launch
-// shortens.  Not for the very smallest (the second launch costs more than it
-// saves), nor for long batches, where the one-launch kernel's finishers hide
-// its tail behind other CTAs' streaming.  Warps take two tiles (more than 16
-// packed rows) from kSplitTwoTileMinTokens prefix tokens.
-bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens) {
-  if (g_sl == 0 || (D != 64 && D != 128) || h_kv <= 0 || h_q % h_kv != 0 || L > cmb::kMaxL) return false;
+// Stream-only vsk_kernel then the combine kernel, for calls with at most
+// cmb::kMaxL drafts: small and mid-size calls, where the one-launch kernel's
+// tail (tickets, a two-level fold of the pieces, the draft block) is a chain
+// of memory round trips that the combine launch shortens.  Not for the very
+// smallest (the second launch costs more than it saves), nor, at head_dim 64
+// / 128, for long batches, where the one-launch kernel's finishers hide its
+// tail behind other CTAs' streaming; at head_dim 256 it measured faster up to
+// the 64-sequence batches (from where the column split stops; capped at
+// kSplit256MaxWork).  Warps take two tiles (more than 16 packed rows, head_dim
+// 64 / 128) from kSplitTwoTileMinTokens prefix tokens.
+bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens, bool fp8) {
+  if (g_sl == 0 || (D != 64 && D != 128 && D != 256) || h_kv <= 0 || h_q % h_kv != 0 || L > cmb::kMaxL) return false;
   if (g_sl == 2) return true;
   const long long work = total_tokens * h_kv;
+  if (D == 256) {
+    // measured for at most 32 packed rows (more stay on the one-launch kernel)
+    if ((h_q / h_kv) * L > 32) return false;
+    return work >= (g_cs != 0 ? col_split_end(fp8) : kSplitLaunchMinWork) && work <= kSplit256MaxWork;
+  }
   const long long cap = (h_q / h_kv) * L <= 16 ? kSplitLaunchMaxWork16 : kSplitLaunchMaxWork;
   return work >= kSplitLaunchMinWork && work <= cap;
 }
@@ -400,10 +405,13 @@ KernelFn pick_tc_kernel(bool fp8, int rm) { return kernel_tc(fp8, rm); }
 
 KernelFn pick_cs_kernel(bool fp8) { return kernel_d256(fp8, 1); }
 
-KernelFn pick_so_kernel(int D, bool fp8, int mtw) {
+KernelFn pick_so_kernel(int D, bool fp8, int mtw, int nst) {
   switch (D) {
     case 64: return kernel_d64(fp8, mtw, true);
     case 128: return kernel_d128(fp8, mtw, true);
+    // head_dim 256: one tile per warp; e4m3 pools pipeline the stages as the
+    // one-launch kernel does
+    case 256: return mtw == 1 ? kernel_d256(fp8, g_pipe && fp8 && nst >= 3 ? 6 : 5) : nullptr;
     default: return nullptr;
   }
 }
@@ -592,14 +600,30 @@ int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
   if (!tc_eligible(h_q, h_kv, head_dim, max_len_extend) &&
       cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens))
     return 1;
-  // (the two-tile column split takes by default only calls the one-tile
-  // split would take: the same two launches)
-  return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) ||
-          cs2_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) ||
-          cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens) ||
-          sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens))
+  // (the pool dtype moves only the boundary between two-launch forms: the
+  // bf16 thresholds give the same count)
+  return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) || cs2_eligible(h_q, h_kv, head_dim, max_len_extend) ||
+          cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) ||
+          sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false))
              ? 2
              : 1;
+}
+
+const char* vsk_call_form(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t v_head_dim,
+                          int64_t max_len_extend, int64_t prefix_tokens, int fp8_pool) {
+  if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return "";
+  auto ok = [](int64_t d) { return d == 64 || d == 128 || d == 256; };
+  if (!ok(head_dim) || !ok(v_head_dim)) return "";
+  if (head_dim != v_head_dim) return "one_launch";
+  const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
+  const bool fp8 = fp8_pool != 0;
+  // the same order as the planner's
+  if (tc_eligible(h_q, h_kv, head_dim, max_len_extend)) return "tensor_memory";
+  if (cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens)) return "cluster";
+  if (cs2_eligible(h_q, h_kv, head_dim, max_len_extend)) return "column_split_two_tiles";
+  if (cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, fp8)) return "column_split";
+  if (sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, fp8)) return "stream_only";
+  return "one_launch";
 }
 
 void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta) {
@@ -643,10 +667,10 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   const bool same = D == DV;
   cp.use_tc = same && tc_eligible(h_q, h_kv, D, L);
   cp.use_cl = !cp.use_tc && cl_eligible(B, h_q, h_kv, D, DV, L, mean_len * B);
-  cp.use_cs2 = same && !cp.use_tc && !cp.use_cl && cs2_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
-  cp.use_cs = same && !cp.use_tc && !cp.use_cl && !cp.use_cs2 && cs_eligible(h_q, h_kv, D, L, mean_len * B);
+  cp.use_cs2 = same && !cp.use_tc && !cp.use_cl && cs2_eligible(h_q, h_kv, D, L);
+  cp.use_cs = same && !cp.use_tc && !cp.use_cl && !cp.use_cs2 && cs_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
   cp.use_sl = same && !cp.use_tc && !cp.use_cl && !cp.use_cs && !cp.use_cs2 &&
-              sl_eligible(h_q, h_kv, D, L, mean_len * B);
+              sl_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
   Plan& pl = cp.pl;
   if (cp.use_cl && D == 256) {
     // one KV head per cluster, streamed by the column split (two warps per
@@ -742,7 +766,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     }
     cp.cl = static_cast<int>(c);
   } else if (cp.use_sl) {
-    cp.fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW);
+    cp.fn = pick_so_kernel(static_cast<int>(D), fp8, pl.MTW, pl.nst);
     cp.fn_comb = pick_combine_kernel(static_cast<int>(D), fp8);
     if (!cp.fn || !cp.fn_comb || !prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb))
       return fail("stream-only kernels for head_dim %lld unavailable", D);

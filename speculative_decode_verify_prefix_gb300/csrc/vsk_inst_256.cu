@@ -1,11 +1,14 @@
 // head_dim 256 kernels of the split-KV verify attention: the one-launch
-// kernel, the column-split stream, the tensor-memory stream, and the combine
-// kernel of the two-launch forms at every head_dim.
+// kernel, the stream-only kernel, the column-split stream, the tensor-memory
+// stream, and the combine kernel of the two-launch forms at every head_dim.
 #include "verify_kernel.cuh"
 
 namespace vsk {
 
 KernelFn kernel_d256(bool fp8, int variant) {
+  if (variant == 6 && fp8) return static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, true, 256, false, true>);
+  if (variant >= 5) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, true>)
+                               : static_cast<KernelFn>(vsk_kernel<256, false, 1, 1, true>);
   if (variant == 4) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 2, 2>)
                                : static_cast<KernelFn>(vsk_kernel<256, false, 2, 2>);
   if (variant == 3) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, false, 256, false, true>)

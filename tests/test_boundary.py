@@ -240,10 +240,37 @@ def test_paged_entry_rejects_bad_arguments(change, msg):
     assert msg in vsk.last_error(), vsk.last_error()
 
 
+def test_call_form_names_the_form_of_each_shape():
+    """vsk_call_form: the form the planner takes for static shapes and the
+    pool dtype (default switches), consistent with vsk_launches_per_call."""
+    f = vsk.call_form
+    cases = [
+        ((2, 4, 1, 64, 64, 4, 160, False), "cluster"),                  # the tiny case
+        ((4, 16, 2, 128, 128, 4, 1028, False), "stream_only"),          # 2,056 token-heads
+        ((64, 32, 8, 128, 128, 4, 64 * 20000, False), "one_launch"),    # the serving batch
+        ((3, 16, 2, 256, 256, 4, 1536, False), "column_split"),         # 3,072 token-heads
+        ((2, 16, 2, 256, 256, 4, 72000, False), "column_split"),        # 144,000: below 2^18 (bf16)
+        ((2, 16, 2, 256, 256, 4, 72000, True), "stream_only"),          # ... from 2^17 (e4m3)
+        ((8, 8, 2, 256, 256, 4, 8 * 20000, False), "stream_only"),
+        ((64, 16, 2, 256, 256, 4, 64 * 20000, True), "stream_only"),    # the long head_dim 256 batch
+        ((64, 16, 2, 256, 256, 4, 64 * 65537, False), "one_launch"),    # past 2^23 token-heads
+        ((2, 64, 2, 256, 256, 4, 100, False), "one_launch"),            # R = 128
+        ((2, 16, 2, 128, 256, 4, 1000, False), "one_launch"),           # head_dim != v_head_dim
+        ((2, 16, 2, 96, 96, 4, 1000, False), ""),                       # not built
+    ]
+    for args, want in cases:
+        assert f(*args) == want, (args, f(*args))
+        b, hq, hkv, d, dv, l, t, _ = args
+        if want and d == dv:
+            assert vsk.launches_per_call(b, hq, hkv, d, l, t) == (1 if want in ("cluster", "one_launch") else 2)
+
+
 def test_launches_per_call_follows_the_form_switches():
-    """Head_dim 256 with at most 32 packed rows per KV head takes the
-    column-split stream plus the combine launch up to 1,048,576 prefix tokens x
-    KV heads (mode 1), always (mode 2) or never (mode 0); the tensor-memory
+    """Head_dim 256 with at most 32 packed rows per KV head takes two launches
+    up to 2^23 prefix tokens x KV heads: the column-split stream below 2^18
+    (bf16; 2^17 for e4m3 pools, which the host-only query does not know), the
+    stream-only kernel from there, each followed by the combine launch; with
+    the column split off, the stream-only form from 2,048.  The tensor-memory
     switch takes precedence.  Head_dim 64 / 128 with at most 32 drafts takes the
     stream-only kernel plus the combine launch inside its own size window.
     The cluster form (one launch) takes small calls first when it is on.
@@ -265,12 +292,13 @@ def test_launches_per_call_follows_the_form_switches():
         vsk.set_tuning_cluster(0)
         vsk.set_tuning_colsplit(1)
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1                 # head_dim 128
-        assert f(3, 16, 2, 256, 4, 1536) == 2                       # R = 32, 3,072 token-heads
-        assert f(8, 8, 2, 256, 4, 8 * 20000) == 2                   # R = 16
-        assert f(16, 16, 2, 256, 4, 524288) == 2                    # exactly 1,048,576 token-heads
-        assert f(16, 16, 2, 256, 4, 524304) == 1                    # one token past it per sequence
-        assert f(64, 16, 2, 256, 4, 64 * 20000) == 1                # the long batch
-        assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: no column split
+        assert f(3, 16, 2, 256, 4, 1536) == 2                       # R = 32, 3,072 token-heads: column split
+        assert f(8, 8, 2, 256, 4, 8 * 20000) == 2                   # R = 16, 320,000: stream only
+        assert f(16, 16, 2, 256, 4, 524288) == 2                    # 1,048,576: stream only
+        assert f(64, 16, 2, 256, 4, 64 * 20000) == 2                # the long batch: stream only
+        assert f(64, 16, 2, 256, 4, 64 * 65536) == 2                # exactly 2^23 token-heads
+        assert f(64, 16, 2, 256, 4, 64 * 65537) == 1                # one token past it per sequence
+        assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: one-launch kernel
         # head_dim 64 / 128: stream + combine from 2,048 token-heads up to 2^22 (R > 16) or 2^23 (R <= 16)
         assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
         assert f(2, 16, 2, 128, 4, 1024) == 2                       # exactly 2,048 token-heads
@@ -289,7 +317,11 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1
         vsk.set_tuning_colsplit(0)
-        assert f(3, 16, 2, 256, 4, 1536) == 1
+        assert f(3, 16, 2, 256, 4, 1536) == 2                       # stream only from 2,048 token-heads
+        assert f(2, 16, 2, 256, 4, 1000) == 1                       # 2,000: one launch
+        vsk.set_tuning_split_launch(0)
+        assert f(3, 16, 2, 256, 4, 1536) == 1                       # both off: one launch
+        vsk.set_tuning_split_launch(1)
         vsk.set_tuning_tc(True)
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
     finally:

@@ -7,6 +7,8 @@ beside each:
   tile, each holding half the head dimension), head_dim 256;
 - "split": the stream-only mma.sync kernel at head_dim 64 and 128 (every case
   below rewritten to one of them, chosen by a hash of its name);
+- "split256": the stream-only mma.sync kernel at head_dim 256 (one tile per
+  warp; e4m3 pools with pipelined stages);
 - "colsplit2": the column-split stream with both 16-row tiles in each warp
   of the pair (head_dim 256, 17 to 32 packed rows; cases with fewer rows take
   the one-tile split);
@@ -61,11 +63,11 @@ def _select(m, form):
     m.set_tuning_tc(form == "tc")
     m.set_tuning_colsplit(2 if form in ("colsplit", "colsplit2") else 0)
     m.set_tuning_colsplit2(2 if form == "colsplit2" else 0)
-    m.set_tuning_split_launch(2 if form == "split" else 0)
+    m.set_tuning_split_launch(2 if form in ("split", "split256") else 0)
     m.set_tuning_cluster(2 if form == "cluster" else 0)
 
 
-@pytest.fixture(scope="module", params=["tc", "colsplit", "colsplit2", "split", "cluster"])
+@pytest.fixture(scope="module", params=["tc", "colsplit", "colsplit2", "split", "split256", "cluster"])
 def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 

@@ -48,7 +48,9 @@ CASES = [
     (workloads.TINY, 1, 1, 0),                                                # tiny without it: one launch
     (workloads.D256, 1, 1, 1),                                                # the cluster form
     (workloads.D256, 1, 1, 0),                                                # column split + combine
-    (workloads.D256, 0, 1, 0),                                                # forced one launch
+    (workloads.D256, 0, 1, 0),                                                # column split off: stream only + combine
+    (workloads.D256, 0, 0, 0),                                                # both off: one launch
+    (workloads.D256, 0, 2, 0),                                                # stream-only head_dim 256 + combine
     (S("lc_gqa", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 1, 0),  # stream + combine
     (S("lc_gqa_one", (3000, 2500), 4, 16, 2, 128, 128, perm=True, seed=790), 1, 0, 0),
 ]
@@ -68,3 +70,5 @@ def test_reported_launches_match_the_profiled_kernels(vsk, case):
     assert len(got) == want, got
     if want == 2:
         assert any("vsk_combine_kernel" in n for n in got)
+    if spec.d == 256 and cs == 0 and sl == 2:
+        assert any("vsk_kernel<256, false, 1, 1, true" in n for n in got), got

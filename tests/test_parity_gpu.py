@@ -715,6 +715,25 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     check(ob, oracle_o(pb), scaled=SCALED)
 
 
+def test_head_dim_256_stream_only_with_64_packed_rows(vsk):
+    """The stream-only head_dim 256 kernel with four 16-row tiles per KV head
+    (h_q / h_kv = 16, 4 drafts), forced on, then the combine kernel."""
+    spec = workloads.Spec("so256_r64", (3000, 0, 1700, 65), 4, 16, 1, 256, 256, perm=True, seed=851)
+    p = gpu_problem(spec)
+    vsk.set_tuning_colsplit(0)
+    vsk.set_tuning_split_launch(2)
+    vsk.set_tuning_cluster(0)
+    try:
+        assert vsk.launches_per_call(4, 16, 1, 256, 4, p["kv_indices"].shape[0]) == 2
+        o = run_gpu(vsk, p)
+    finally:
+        vsk.set_tuning_colsplit(1)
+        vsk.set_tuning_split_launch(1)
+        vsk.set_tuning_cluster(1)
+    check(o, oracle_o(p), scaled=SCALED)
+    assert vsk.read_error_flags() == 0
+
+
 def _combine_grid_specs():
     # The combine kernel stages 2 x nb pieces per CTA, nb chosen by its grid
     # (16 up to two CTAs per SM, 8 up to three, 4 beyond).  With 32 combine
