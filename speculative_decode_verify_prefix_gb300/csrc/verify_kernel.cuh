@@ -1861,7 +1861,7 @@ KernelFn kernel_d128(bool fp8, int mtw, bool so, bool cl = false);
 // (variant 1), the cluster form streaming by column split (variant 2), the
 // one-launch kernel with pipelined stages (variant 3), the column-split
 // stream with two tiles per warp (variant 4), the stream-only kernel of the
-// two-launch form (variant 5; variant 6: e4m3 pools with pipelined stages)
+// two-launch form (variant 5)
 KernelFn kernel_d256(bool fp8, int variant);
 // tensor-memory stream, head_dim 256, rm = 16 or 32 packed rows
 KernelFn kernel_tc(bool fp8, int rm);

@@ -6,8 +6,7 @@
 namespace vsk {
 
 KernelFn kernel_d256(bool fp8, int variant) {
-  if (variant == 6 && fp8) return static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, true, 256, false, true>);
-  if (variant >= 5) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, true>)
+  if (variant == 5) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 1, 1, true>)
                                : static_cast<KernelFn>(vsk_kernel<256, false, 1, 1, true>);
   if (variant == 4) return fp8 ? static_cast<KernelFn>(vsk_kernel<256, true, 2, 2>)
                                : static_cast<KernelFn>(vsk_kernel<256, false, 2, 2>);
