@@ -352,14 +352,16 @@ void vsk_set_tuning_split_launch(int mode);
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_cluster(int mode);
 
-/* Tuning switch, for A/B runs: mode 1 launches the combine kernel of the
- * two-launch forms as a programmatic dependent of the prefix stream
- * (cudaLaunchAttributeProgrammaticStreamSerialization): its CTAs may start
+/* Tuning switch, for A/B runs: how the combine kernel of the two-launch forms
+ * follows the prefix stream.  As a programmatic dependent
+ * (cudaLaunchAttributeProgrammaticStreamSerialization) its CTAs may start
  * while the stream runs, read the call's lengths, qo_indptr and draft-row
- * locations, and wait for the stream grid before reading anything else.  Mode 0 (the
- * default; measured faster on GB300 for all but the smallest calls) launches
- * it after the stream in plain stream order.  The result is the same either
- * way.  Process-wide; not thread-safe. */
+ * locations, and wait for the stream grid before reading anything else;
+ * otherwise it starts after the stream in plain stream order.  Mode 1 (the
+ * default) takes the programmatic form for calls of at most 65,536 prefix
+ * tokens x KV heads (about 2 us faster there on GB300; neutral to slower on
+ * mid-size calls), mode 2 always, mode 0 never.  The result is the same
+ * either way.  Process-wide; not thread-safe. */
 void vsk_set_tuning_pdl(int mode);
 
 /* Tuning switch, for A/B runs: mode 1 (the default) runs the head_dim 256

@@ -324,11 +324,11 @@ def set_tuning_cluster(mode: int = 1) -> None:
     _native.lib().vsk_set_tuning_cluster(int(mode))
 
 
-def set_tuning_pdl(enabled: bool = False) -> None:
-    """Launch the combine kernel of the two-launch forms as a programmatic
-    dependent of the prefix stream, or in plain stream order (the default);
-    for A/B runs."""
-    _native.lib().vsk_set_tuning_pdl(1 if enabled else 0)
+def set_tuning_pdl(mode: int = 1) -> None:
+    """The combine kernel of the two-launch forms as a programmatic dependent
+    of the prefix stream for small calls (1, the default), always (2) or
+    never (0: plain stream order); for A/B runs."""
+    _native.lib().vsk_set_tuning_pdl(int(mode))
 
 
 def set_tuning_pipe(enabled: bool = True) -> None:

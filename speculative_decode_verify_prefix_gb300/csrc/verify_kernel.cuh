@@ -58,6 +58,7 @@ constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from 
 constexpr long long kColSplitEndBf16 = 1LL << 18;  // prefix tokens x KV heads below which head_dim 256 splits columns (bf16)
 constexpr long long kColSplitEndE4m3 = 1LL << 17;  // ... (e4m3 pools); from there the stream-only kernel + combine
 constexpr long long kSplit256MaxWork = 1LL << 23;   // ... up to which head_dim 256 takes the stream-only kernel + combine
+constexpr long long kPdlMaxWork = 1LL << 16;  // prefix tokens x KV heads up to which the combine launch is a programmatic dependent
 constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
 constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
 constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
@@ -1229,8 +1230,8 @@ __global__ void __launch_bounds__(CS == 2 ? (MTW == 2 ? 64 : 128) : MaxWarps<Max
       // Independent accumulator chains per n-tile (k-step mod NCH) cut the
       // dependent mma latency; summed afterwards.  With two tiles per warp the
       // tiles themselves are independent chains.
-      // (two chains measured faster than four for head_dim 256 bf16 only)
-      constexpr int NCH = (MTW == 1 && !PIPE) ? ((D == 256 && !FP8 && CS == 1) ? 2 : 4) : 1;
+      // (two chains measured faster than four at head_dim 256, both pools)
+      constexpr int NCH = (MTW == 1 && !PIPE) ? ((D == 256 && CS == 1) ? 2 : 4) : 1;
       // (a chain's first product takes a zero accumulator input: nothing to clear)
       float sc[MTW][2][4];
       float sx[MTW][NCH > 1 ? NCH - 1 : 1][2][4];

@@ -48,7 +48,7 @@ int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kS
 int g_cs2 = 1;    // two-tile column split at head_dim 256: 2 always; 0 and 1 (the default) never
 int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
 int g_pipe = 1;   // head_dim 256 one-launch kernel over e4m3 pools with pipelined stages (1) or not (0)
-int g_pdl = 0;    // combine kernel launched as a programmatic dependent of the stream (1) or not (0, the default)
+int g_pdl = 1;    // combine kernel as a programmatic dependent of the stream: 1 up to kPdlMaxWork, 2 always, 0 never
 
 struct Plan {
   int gq, R, MT, MTW, HC, n_hg, nwc, threads, ek;
@@ -586,7 +586,7 @@ void vsk_set_tuning_split_launch(int mode) { g_sl = (mode == 0 || mode == 2) ? m
 
 void vsk_set_tuning_cluster(int mode) { g_cl = (mode == 0 || mode == 2) ? mode : 1; }
 
-void vsk_set_tuning_pdl(int mode) { g_pdl = mode == 0 ? 0 : 1; }
+void vsk_set_tuning_pdl(int mode) { g_pdl = (mode == 0 || mode == 2) ? mode : 1; }
 
 void vsk_set_tuning_pipe(int mode) { g_pipe = mode == 0 ? 0 : 1; }
 
@@ -649,6 +649,7 @@ struct CallPlan {
   bool use_tc = false, use_cs = false, use_sl = false, use_cl = false, use_cs2 = false;
   int cl = 0, cl_smem = 0;  // cluster form: CTAs per cluster, shared memory of one combine group
   int cmb_nb = 8;           // combine units: pieces staged per batch (two batches in flight)
+  bool pdl = false;         // combine kernel launched as a programmatic dependent of the stream
   Plan pl{};
   StreamPlan sp{};
   KernelFn fn = nullptr, fn_comb = nullptr;
@@ -789,6 +790,10 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
     // CTAs per SM stages 2 x 16 pieces (two CTAs fit an SM), up to three
     // CTAs per SM 2 x 8, larger grids 2 x 4
     cp.cmb_nb = cp.n_comb <= 2LL * sms ? 16 : cp.n_comb <= 3LL * sms ? 8 : 4;
+    // small calls: the combine kernel's CTAs start while the stream ends (about
+    // one microsecond less per call); on mid-size calls that measured neutral
+    // to slower, so only up to kPdlMaxWork prefix tokens x KV heads
+    cp.pdl = g_pdl == 2 || (g_pdl == 1 && mean_len * B * h_kv <= kPdlMaxWork);
   }
   // Smallest CTA share, from static shapes only (no device read, graph
   // safe): at least 64 tokens and, for small batches where the shares get
@@ -875,10 +880,10 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
   if (e != cudaSuccess) return fail("kernel launch failed: %s", cudaGetErrorString(e));
   if (cp.fn_comb) {
     // the share floor and n_stream let the combine kernel find the pieces the
-    // stream launch wrote.  With vsk_set_tuning_pdl(1) it is launched as a
-    // programmatic dependent of the stream: its CTAs may start (and read the
-    // call's inputs) before the stream ends, and wait for it before reading
-    // the partials (measured slower than plain stream order on mid-size calls).
+    // stream launch wrote.  Small calls (cp.pdl) launch it as a programmatic
+    // dependent of the stream: its CTAs may start (and read the call's
+    // lengths) before the stream ends, and wait for it before reading anything
+    // it wrote.
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -888,7 +893,7 @@ static int enqueue_call(Params& p, const CallPlan& cp, long long B, long long L,
     cfg.dynamicSmemBytes = combine_smem(cp.D, cp.cmb_nb);
     cfg.stream = st;
     cfg.attrs = at;
-    cfg.numAttrs = g_pdl ? 1 : 0;
+    cfg.numAttrs = cp.pdl ? 1 : 0;
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(cp.fn_comb), args);
     if (e != cudaSuccess) return fail("combine kernel launch failed: %s", cudaGetErrorString(e));
   }

@@ -351,16 +351,18 @@ def test_form_poisoned_unreferenced_slots(vsk):
 def test_form_with_programmatic_dependent_launch(vsk, spec):
     """The two-launch forms with the combine kernel launched as a
     programmatic dependent of the stream (it starts early and waits for the
-    stream grid before reading partials): the same result as in stream order."""
+    stream grid before reading partials), forced on: bitwise the result of
+    plain stream order, forced off."""
     p = gpu_problem(spec)
     vsk.read_error_flags()
-    a = run_gpu(vsk, p)
-    vsk.set_tuning_pdl(True)
+    vsk.set_tuning_pdl(0)
     try:
+        a = run_gpu(vsk, p)
+        vsk.set_tuning_pdl(2)
         b = run_gpu(vsk, p)
         c = run_gpu(vsk, p)
     finally:
-        vsk.set_tuning_pdl(False)
+        vsk.set_tuning_pdl(1)
     assert vsk.read_error_flags() == 0
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
