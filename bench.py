@@ -451,7 +451,7 @@ def run_ours(args, dist: Dist) -> dict:
     vsk.set_tuning_tc(tc)
     vsk.set_tuning_colsplit(0 if args.one_launch else 1)
     vsk.set_tuning_split_launch(0 if args.one_launch else 1)
-    vsk.set_tuning_cluster(0 if args.one_launch else 1)
+    vsk.set_tuning_cluster(0)
     prob = workloads.make_problem(spec, dev)
     B = len(prob["prefix_lens"])
     nbytes = workloads.algorithmic_bytes(prob)

@@ -329,10 +329,10 @@ void vsk_set_tuning_colsplit2(int mode);
  * second launch on the same stream (instead of the one-launch kernel's
  * ticketed tail).  Mode 1 (the default) takes that form where it measured
  * faster on GB300: at head_dim 64 / 128 when the call's prefix tokens times
- * h_kv are at least 2,048 and at most 4,194,304 (8,388,608 when (h_q / h_kv) *
- * max_len_extend <= 16); at head_dim 256 with at most 32 packed rows per KV
- * head from where the column split stops (262,144 bf16, 131,072 e4m3; 2,048
- * with the column split off) up to 8,388,608.  Mode 2 always takes it; mode 0
+ * h_kv are at most 4,194,304 (8,388,608 when (h_q / h_kv) * max_len_extend <=
+ * 16); at head_dim 256 with at most 32 packed rows per KV head from where the
+ * column split stops (262,144 bf16, 131,072 e4m3; any size with the column
+ * split off) up to 8,388,608.  Mode 2 always takes it; mode 0
  * never does.  All forms compute the same result up to rounding order.
  * Process-wide; not thread-safe. */
 void vsk_set_tuning_split_launch(int mode);
@@ -343,11 +343,12 @@ void vsk_set_tuning_split_launch(int mode);
  * cluster's CTAs fold the segment's partials, add the draft block and write
  * o: one launch, no tickets, no second kernel.  It serves head_dim ==
  * v_head_dim, at most 32 draft rows per sequence and at most 512 segments.
- * Mode 1 (the default) takes it when the call's prefix tokens (kv_indices
- * entries, or block-table capacity for the paged entry points) times h_kv are
- * fewer than 2,048 (the smallest calls, where it measured faster than the
- * one-launch kernel on GB300; above that the stream + combine launches are
- * faster); mode 2 takes it wherever it applies; mode 0 never.
+ * Mode 0 (the default) never takes it: the stream-only kernel with the
+ * combine kernel launched as a programmatic dependent measured faster on
+ * GB300 at every size (the tiny case 18.3 -> 16.3 us, warm).  Mode 1 takes
+ * it when the call's prefix tokens (kv_indices entries, or block-table
+ * capacity for the paged entry points) times h_kv are fewer than 2,048, where
+ * it beat the one-launch kernel before that; mode 2 wherever it applies.
  * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_cluster(int mode);

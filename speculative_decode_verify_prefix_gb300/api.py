@@ -317,10 +317,10 @@ def set_tuning_split_launch(mode: int = 1) -> None:
     _native.lib().vsk_set_tuning_split_launch(int(mode))
 
 
-def set_tuning_cluster(mode: int = 1) -> None:
+def set_tuning_cluster(mode: int = 0) -> None:
     """The cluster form (one launch; one thread-block cluster per (sequence,
-    KV head) folds its own partials): for small calls (1, the default), wherever
-    it applies (2) or never (0); for A/B runs and tests."""
+    KV head) folds its own partials): never (0, the default), for small calls
+    (1) or wherever it applies (2); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_cluster(int(mode))
 
 

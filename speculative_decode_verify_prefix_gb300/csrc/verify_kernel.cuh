@@ -54,25 +54,9 @@ constexpr int kSmemPerSM = 233472;   // 228 KB per SM
 constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
 constexpr int kReservedPerCTA = 1024;
 constexpr int kTicketBytes = 65536;   // minimum ticket region at the end of a workspace
-constexpr long long kTwoTileMinTokens = 65536;  // prefix tokens of a call from which warps take two tiles
-constexpr long long kColSplitEndBf16 = 1LL << 18;  // prefix tokens x KV heads below which head_dim 256 splits columns (bf16)
-constexpr long long kColSplitEndE4m3 = 1LL << 17;  // ... (e4m3 pools); from there the stream-only kernel + combine
-constexpr long long kSplit256MaxWork = 1LL << 23;   // ... up to which head_dim 256 takes the stream-only kernel + combine
-constexpr long long kPdlMaxWork = 1LL << 16;  // prefix tokens x KV heads up to which the combine launch is a programmatic dependent
-constexpr long long kSplitLaunchMinWork = 2048;        // ... from which head_dim 64 / 128 calls take two launches
-constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // ... up to which they do (more than 16 packed rows)
-constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
-constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... up to which they do (at most 16 packed rows)
-constexpr long long kClMaxWork = 2047;  // prefix tokens x KV heads up to which calls take the cluster form
-constexpr long long kClMaxSeg = 512;         // ... with at most this many (sequence, KV head) segments
-constexpr long long kClTokensPerCta = 64;    // prefix tokens per CTA the cluster size aims at
-constexpr int kClMax = 16;                   // CTAs per cluster at most (8 where 16 do not fit an SM group)
 constexpr float kLazy = 8.f;          // log2 headroom before a running maximum is raised
 constexpr int kGroup = 4;             // pieces per group of a two-level merge
 constexpr int kTreeMin = 6;           // segments of more pieces merge in two levels
-constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
-constexpr long long kPiecesPerSegment = 24;    // ... and at least the mean prefix over this many
-constexpr long long kPiecesPerSegmentColSplit = 48;  // ... this many for the column-split stream
 
 enum : unsigned {
   kErrBadIndex = 1u,

@@ -21,6 +21,25 @@
 #define VSK_VERSION "verify_splitkv-gb300 0.2"
 
 namespace vsk {
+
+// Host-side policy of the planner: which form a call takes and how it is cut
+// (prefix tokens x KV heads are from static shapes: kv_indices entries, or
+// block-table capacity, times h_kv).
+constexpr long long kTwoTileMinTokens = 65536;  // one-launch kernel: prefix tokens from which warps take two tiles
+constexpr long long kDefaultMinTokens = 64;  // smallest CTA share of the flattened token space
+constexpr long long kPiecesPerSegment = 24;    // ... and at least the mean prefix over this many (one launch)
+constexpr long long kPiecesPerSegmentColSplit = 48;  // ... over this many for the two-launch and cluster forms
+constexpr long long kColSplitEndBf16 = 1LL << 18;  // head_dim 256: column split below this many token-heads (bf16)
+constexpr long long kColSplitEndE4m3 = 1LL << 17;  // ... (e4m3 pools); from there the stream-only kernel + combine
+constexpr long long kSplit256MaxWork = 1LL << 23;   // ... up to which head_dim 256 takes the stream-only kernel + combine
+constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // head_dim 64 / 128: stream-only + combine up to (R > 16)
+constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... (at most 16 packed rows)
+constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
+constexpr long long kPdlMaxWork = 1LL << 16;  // token-heads up to which the combine launch is a programmatic dependent
+constexpr long long kClMaxWork = 2047;  // cluster form, mode 1: token-heads up to which calls take it
+constexpr long long kClMaxSeg = 512;         // ... with at most this many (sequence, KV head) segments
+constexpr long long kClTokensPerCta = 64;    // prefix tokens per CTA the cluster size aims at
+constexpr int kClMax = 16;                   // CTAs per cluster at most (8 where 16 do not fit an SM group)
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
@@ -46,7 +65,7 @@ int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the def
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitEnd*, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 int g_cs2 = 1;    // two-tile column split at head_dim 256: 2 always; 0 and 1 (the default) never
-int g_cl = 1;     // cluster form: 1 up to kClMaxWork, 2 always (where it applies), 0 never
+int g_cl = 0;     // cluster form: 0 never (the default), 1 up to kClMaxWork, 2 always (where it applies)
 int g_pipe = 1;   // head_dim 256 one-launch kernel over e4m3 pools with pipelined stages (1) or not (0)
 int g_pdl = 1;    // combine kernel as a programmatic dependent of the stream: 1 up to kPdlMaxWork, 2 always, 0 never
 
@@ -190,8 +209,8 @@ bool cs2_eligible(long long h_q, long long h_kv, long long D, long long L) {
 // Stream-only vsk_kernel then the combine kernel, for calls with at most
 // cmb::kMaxL drafts: small and mid-size calls, where the one-launch kernel's
 // tail (tickets, a two-level fold of the pieces, the draft block) is a chain
-// of memory round trips that the combine launch shortens.  Not for the very
-// smallest (the second launch costs more than it saves), nor, at head_dim 64
+// of memory round trips that the combine launch shortens (the smallest ones
+// with the combine launch as a programmatic dependent).  Not, at head_dim 64
 // / 128, for long batches, where the one-launch kernel's finishers hide its
 // tail behind other CTAs' streaming; at head_dim 256 it measured faster up to
 // the 64-sequence batches (from where the column split stops; capped at
@@ -204,10 +223,10 @@ bool sl_eligible(long long h_q, long long h_kv, long long D, long long L, long l
   if (D == 256) {
     // measured for at most 32 packed rows (more stay on the one-launch kernel)
     if ((h_q / h_kv) * L > 32) return false;
-    return work >= (g_cs != 0 ? col_split_end(fp8) : kSplitLaunchMinWork) && work <= kSplit256MaxWork;
+    return (g_cs == 0 || work >= col_split_end(fp8)) && work <= kSplit256MaxWork;
   }
   const long long cap = (h_q / h_kv) * L <= 16 ? kSplitLaunchMaxWork16 : kSplitLaunchMaxWork;
-  return work >= kSplitLaunchMinWork && work <= cap;
+  return work <= cap;
 }
 // Cluster form (one launch: one thread-block cluster per (sequence, KV head)
 // segment streams it, then folds its pieces, adds the draft block and writes
@@ -584,7 +603,7 @@ void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode 
 
 void vsk_set_tuning_split_launch(int mode) { g_sl = (mode == 0 || mode == 2) ? mode : 1; }
 
-void vsk_set_tuning_cluster(int mode) { g_cl = (mode == 0 || mode == 2) ? mode : 1; }
+void vsk_set_tuning_cluster(int mode) { g_cl = (mode == 1 || mode == 2) ? mode : 0; }
 
 void vsk_set_tuning_pdl(int mode) { g_pdl = (mode == 0 || mode == 2) ? mode : 1; }
 

@@ -245,7 +245,7 @@ def test_call_form_names_the_form_of_each_shape():
     pool dtype (default switches), consistent with vsk_launches_per_call."""
     f = vsk.call_form
     cases = [
-        ((2, 4, 1, 64, 64, 4, 160, False), "cluster"),                  # the tiny case
+        ((2, 4, 1, 64, 64, 4, 160, False), "stream_only"),              # the tiny case
         ((4, 16, 2, 128, 128, 4, 1028, False), "stream_only"),          # 2,056 token-heads
         ((64, 32, 8, 128, 128, 4, 64 * 20000, False), "one_launch"),    # the serving batch
         ((3, 16, 2, 256, 256, 4, 1536, False), "column_split"),         # 3,072 token-heads
@@ -273,8 +273,8 @@ def test_launches_per_call_follows_the_form_switches():
     the column split off, the stream-only form from 2,048.  The tensor-memory
     switch takes precedence.  Head_dim 64 / 128 with at most 32 drafts takes the
     stream-only kernel plus the combine launch inside its own size window.
-    The cluster form (one launch) takes small calls first when it is on.
-    Everything else is one launch."""
+    The cluster form (one launch; off by default) takes small calls first when
+    it is on.  Everything else is one launch."""
     f = vsk.launches_per_call
     try:
         vsk.set_tuning_cluster(1)
@@ -299,9 +299,9 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(64, 16, 2, 256, 4, 64 * 65536) == 2                # exactly 2^23 token-heads
         assert f(64, 16, 2, 256, 4, 64 * 65537) == 1                # one token past it per sequence
         assert f(2, 64, 2, 256, 4, 100) == 1                        # R = 128: one-launch kernel
-        # head_dim 64 / 128: stream + combine from 2,048 token-heads up to 2^22 (R > 16) or 2^23 (R <= 16)
-        assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
-        assert f(2, 16, 2, 128, 4, 1024) == 2                       # exactly 2,048 token-heads
+        # head_dim 64 / 128: stream + combine up to 2^22 (R > 16) or 2^23 (R <= 16) token-heads
+        assert f(2, 4, 1, 64, 4, 160) == 2                          # the tiny case
+        assert f(2, 16, 2, 128, 4, 1024) == 2                       # 2,048 token-heads
         assert f(16, 16, 2, 128, 4, 2097152) == 2                   # R = 32, 2^22
         assert f(16, 16, 2, 128, 4, 2097168) == 1
         assert f(16, 32, 8, 128, 4, 1048576) == 2                   # R = 16, 2^23
@@ -317,8 +317,8 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
         assert f(64, 32, 8, 128, 4, 64 * 20000) == 1
         vsk.set_tuning_colsplit(0)
-        assert f(3, 16, 2, 256, 4, 1536) == 2                       # stream only from 2,048 token-heads
-        assert f(2, 16, 2, 256, 4, 1000) == 1                       # 2,000: one launch
+        assert f(3, 16, 2, 256, 4, 1536) == 2                       # stream only at any size
+        assert f(2, 16, 2, 256, 4, 1000) == 2
         vsk.set_tuning_split_launch(0)
         assert f(3, 16, 2, 256, 4, 1536) == 1                       # both off: one launch
         vsk.set_tuning_split_launch(1)
@@ -328,7 +328,7 @@ def test_launches_per_call_follows_the_form_switches():
         vsk.set_tuning_tc(False)
         vsk.set_tuning_colsplit(1)
         vsk.set_tuning_split_launch(1)
-        vsk.set_tuning_cluster(1)
+        vsk.set_tuning_cluster(0)
     assert f(0, 16, 2, 256, 4, 10) == 0                             # no sequences
     assert f(2, 15, 2, 256, 4, 10) == 0                             # h_q not a multiple of h_kv
     assert f(2, 16, 2, 96, 4, 10) == 0                              # head_dim not built

@@ -81,7 +81,7 @@ def vsk(request):
     m.set_tuning_colsplit(1)
     m.set_tuning_colsplit2(1)
     m.set_tuning_split_launch(1)
-    m.set_tuning_cluster(1)
+    m.set_tuning_cluster(0)
     FORM["name"] = "tc"
 
 

@@ -25,7 +25,7 @@ def vsk():
     yield m
     m.set_tuning_colsplit(1)
     m.set_tuning_split_launch(1)
-    m.set_tuning_cluster(1)
+    m.set_tuning_cluster(0)
 
 
 def _kernels_of_one_call(vsk, p):
@@ -44,9 +44,10 @@ def _kernels_of_one_call(vsk, p):
 
 CASES = [
     # (spec, colsplit mode, split-launch mode, cluster mode)
-    (workloads.TINY, 1, 1, 1),                                                # tiny: the cluster form, one launch
-    (workloads.TINY, 1, 1, 0),                                                # tiny without it: one launch
-    (workloads.D256, 1, 1, 1),                                                # the cluster form
+    (workloads.TINY, 1, 1, 1),                                                # tiny: the cluster form (mode 1), one launch
+    (workloads.TINY, 1, 1, 0),                                                # tiny by default: stream only + combine
+    (workloads.TINY, 1, 0, 0),                                                # tiny, both off: one launch
+    (workloads.D256, 1, 1, 1),                                                # past the cluster form's window
     (workloads.D256, 1, 1, 0),                                                # column split + combine
     (workloads.D256, 0, 1, 0),                                                # column split off: stream only + combine
     (workloads.D256, 0, 0, 0),                                                # both off: one launch

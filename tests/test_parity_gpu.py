@@ -240,7 +240,7 @@ def test_split_count_independence(vsk, num_ctas, min_tok):
         o = run_gpu(vsk, p)
     finally:
         vsk.set_tuning(0, 0)
-        vsk.set_tuning_cluster(1)
+        vsk.set_tuning_cluster(0)
     check(o, oracle_o(p))
     assert (o.float() - base).abs().max().item() < 1e-3 * 8  # a few bf16 ulps at |o| < 1
 
@@ -475,7 +475,7 @@ def test_paged_bf16_unit_scales_is_bitwise_the_flat_path(vsk):
         b = run_gpu(vsk, p)
     finally:
         vsk.set_tuning(0, 0)
-        vsk.set_tuning_cluster(1)
+        vsk.set_tuning_cluster(0)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
@@ -490,7 +490,7 @@ def test_paged_split_count_independence(vsk):
             o = run_paged(vsk, p)
         finally:
             vsk.set_tuning(0, 0)
-            vsk.set_tuning_cluster(1)
+            vsk.set_tuning_cluster(0)
         check(o, ref)
 
 
@@ -671,7 +671,7 @@ def test_one_workspace_serves_calls_of_any_shape(vsk):
                 fresh = run_gpu(vsk, p, workspace=torch.zeros_like(shared))
             finally:
                 vsk.set_tuning(0, 0)
-                vsk.set_tuning_cluster(1)
+                vsk.set_tuning_cluster(0)
             assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (i, spec.name)
     assert vsk.read_error_flags(shared) == 0
 
@@ -711,7 +711,7 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     finally:
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_colsplit(1)
-        vsk.set_tuning_cluster(1)
+        vsk.set_tuning_cluster(0)
     check(ob, oracle_o(pb), scaled=SCALED)
 
 
@@ -729,7 +729,7 @@ def test_head_dim_256_stream_only_with_64_packed_rows(vsk):
     finally:
         vsk.set_tuning_colsplit(1)
         vsk.set_tuning_split_launch(1)
-        vsk.set_tuning_cluster(1)
+        vsk.set_tuning_cluster(0)
     check(o, oracle_o(p), scaled=SCALED)
     assert vsk.read_error_flags() == 0
 

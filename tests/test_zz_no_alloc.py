@@ -147,7 +147,7 @@ def test_noalloc_matches_oracle_across_shapes(lib):
                 np.testing.assert_allclose(outs[i].float().cpu().numpy(), with_ws[i], atol=ATOL, rtol=RTOL)
                 assert _noalloc_flags(lib) == 0
     finally:
-        _form((1, 1, 1))
+        _form((0, 1, 1))
 
 
 def test_noalloc_flags_an_out_of_range_index(lib):
