@@ -111,6 +111,11 @@ WORKLOADS = {
     "fp8_b8": workloads.Spec("fp8_b8_p8k_32k", None, 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
                              v_scale=0.25, batch=8, len_range=(8192, 32768), seed=1240),
     "fp8_cfg": workloads.FP8,
+    # the serving batch over an e4m3 cache (k_scale 0.5, v_scale 0.25): half the bytes per token
+    "serving_fp8": workloads.replace(workloads.SERVING, name="serving_fp8_b64_p8k_32k", pool="e4m3", k_scale=0.5,
+                                     v_scale=0.25),
+    "serving_fp8_b8": workloads.replace(workloads.SERVING, name="serving_fp8_b8_p8k_32k", batch=8, pool="e4m3",
+                                        k_scale=0.5, v_scale=0.25),
 }
 
 

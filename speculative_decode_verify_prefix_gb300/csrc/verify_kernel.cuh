@@ -46,9 +46,13 @@ namespace vsk {
 // Constants shared by the host plan and the kernel.
 // ---------------------------------------------------------------------------
 constexpr int kStageTokens = 16;     // prefix tokens per pipeline stage (one mma k-step)
-constexpr int kMaxStages = 5;        // ring depth cap (kIdxAhead >= stages - 1)
-constexpr int kIdxAhead = 4;         // stages of kv_indices prefetched ahead of the copies
+constexpr int kMaxStages = 7;        // ring depth cap (kIdxAhead >= stages - 1)
+constexpr int kIdxAhead = 6;         // stages of kv_indices prefetched ahead of the copies (< kIdxRing)
 constexpr int kIdxRing = 8;          // per-warp index ring entries (> kIdxAhead)
+// the index of a stage lands before its copies are issued (kIdxAhead >= the
+// stages in flight), its ring entry lives until then (kIdxRing > kIdxAhead),
+// and the 16-entry valid-token mask ring covers every stage in flight
+static_assert(kIdxAhead >= kMaxStages - 1 && kIdxRing > kIdxAhead && kMaxStages <= 16, "ring invariants");
 constexpr int kCtlBytes = 256;       // control block before the warp regions
 constexpr int kSmemPerSM = 233472;   // 228 KB per SM
 constexpr int kSmemPerCTAMax = 232448;  // 227 KB opt-in per CTA
