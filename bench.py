@@ -132,9 +132,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--one-launch", action="store_true",
                     help="keep every call on the one-launch kernel (no column split, no stream + combine launches)")
-    ap.add_argument("--tc", action="store_true",
-                    help="head_dim 256 calls stream the prefix with the tensor-memory kernel (tcgen05; "
-                         "two launches per call: vtc_kernel, then the combine kernel)")
+    ap.add_argument("--tc", type=int, nargs="?", const=1, default=0, metavar="MODE",
+                    help="head_dim 256 calls stream the prefix with a tensor-memory kernel (tcgen05; two "
+                         "launches per call, then the combine kernel): 1 (the bare flag) vtc_kernel, keys "
+                         "on the MMAs' M side; 2 vtr_kernel, packed query rows on M")
     ap.add_argument("--report-configs", action="store_true",
                     help="print a per-configuration table (tiny, d256, GQA sweep, fp8, serving) instead of the JSON line")
     ap.add_argument("--config-calls", type=int, default=0, metavar="N",
@@ -452,7 +453,7 @@ def run_ours(args, dist: Dist) -> dict:
     dev = torch.device("cuda", dist.local_rank)
     spec = WORKLOADS[args.workload]
     # the tensor-memory stream serves head_dim 256 with at most 32 packed rows per KV head
-    tc = bool(args.tc) and spec.d == 256 and (spec.h_q // spec.h_kv) * spec.l_ext <= 32
+    tc = int(args.tc) if spec.d == 256 and (spec.h_q // spec.h_kv) * spec.l_ext <= 32 else 0
     vsk.set_tuning_tc(tc)
     vsk.set_tuning_colsplit(0 if args.one_launch else 1)
     vsk.set_tuning_split_launch(0 if args.one_launch else 1)
@@ -486,6 +487,7 @@ def run_ours(args, dist: Dist) -> dict:
     form = vsk.call_form(B, spec.h_q, spec.h_kv, spec.d, spec.dv, prob["max_len_extend"], tokens,
                          spec.pool == "e4m3")
     kernel = {"tensor_memory": "vtc_kernel (+ vsk_combine_kernel)",
+              "tensor_memory_rows": "vtr_kernel (+ vsk_combine_kernel)",
               "column_split": "vsk_kernel column-split stream (+ vsk_combine_kernel)",
               "column_split_two_tiles": "vsk_kernel two-tile column-split stream (+ vsk_combine_kernel)",
               "stream_only": "vsk_kernel stream only (+ vsk_combine_kernel)",

@@ -288,11 +288,12 @@ def set_tuning_tiles(tiles_per_warp: int = 0) -> None:
     _native.lib().vsk_set_tuning_tiles(int(tiles_per_warp))
 
 
-def set_tuning_tc(enabled: bool = False) -> None:
-    """Route head_dim 256 calls (at most 32 packed rows per KV head) through the
-    tensor-memory stream (``enabled=True``) or through the mma.sync kernel (the
-    default, faster on GB300 at these shapes); for A/B runs and tests."""
-    _native.lib().vsk_set_tuning_tc(1 if enabled else 0)
+def set_tuning_tc(mode: int = 0) -> None:
+    """Route head_dim 256 calls (at most 32 packed rows per KV head) through a
+    tensor-memory stream: 1 (or ``True``) the one with the keys on the MMAs' M
+    side, 2 the one with the packed query rows on M; 0 (or ``False``, the
+    default) keeps them on the mma.sync kernels.  For A/B runs and tests."""
+    _native.lib().vsk_set_tuning_tc(int(mode))
 
 
 def set_tuning_colsplit(mode: int = 1) -> None:

@@ -17,6 +17,7 @@
 
 #include "../../include/verify_splitkv.h"
 #include "verify_kernel.cuh"
+#include "verify_tr.cuh"
 
 #define VSK_VERSION "verify_splitkv-gb300 0.2"
 
@@ -61,7 +62,7 @@ long long g_min_tokens = 0;
 int g_max_stages = 0;
 int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
-int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 on, 0 off (the default: slower here)
+int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 keys on M, 2 rows on M, 0 off (the default)
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitEnd*, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 int g_cs2 = 1;    // two-tile column split at head_dim 256: 2 always; 0 and 1 (the default) never
@@ -150,7 +151,7 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
 // The tensor-memory stream (vtc_kernel) serves head_dim 256 with at most 32
 // packed query rows per KV head.
 bool tc_eligible(long long h_q, long long h_kv, long long D, long long L) {
-  if (g_tc != 1 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
+  if (g_tc == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
   return (h_q / h_kv) * L <= 32;
 }
 
@@ -453,6 +454,16 @@ void tc_smem(int& ne, size_t& smem) {
   smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::ENT;
 }
 
+// Ring entries and shared memory of vtr_kernel (e4m3 pools: an even number,
+// so that V rows always sit in odd entries).
+template <bool FP8>
+void tr_smem(int& ne, size_t& smem) {
+  using G = tr::Geo<FP8>;
+  ne = std::min(tr::kMaxNE, (kSmemPerCTAMax - G::ring_off) / G::ENT);
+  if (FP8) ne &= ~1;
+  smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::ENT;
+}
+
 int prepare_kernel(KernelFn fn) {
   // the attribute is per function and context; set it before every launch
   // configuration query (cheap, idempotent)
@@ -597,7 +608,7 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
 
 void vsk_set_tuning_tiles(int tiles_per_warp) { g_tiles = tiles_per_warp == 1 || tiles_per_warp == 2 ? tiles_per_warp : 0; }
 
-void vsk_set_tuning_tc(int mode) { g_tc = mode == 1 ? 1 : 0; }
+void vsk_set_tuning_tc(int mode) { g_tc = (mode == 1 || mode == 2) ? mode : 0; }
 
 void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode : 1; }
 
@@ -637,7 +648,7 @@ const char* vsk_call_form(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
   const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
   const bool fp8 = fp8_pool != 0;
   // the same order as the planner's
-  if (tc_eligible(h_q, h_kv, head_dim, max_len_extend)) return "tensor_memory";
+  if (tc_eligible(h_q, h_kv, head_dim, max_len_extend)) return g_tc == 2 ? "tensor_memory_rows" : "tensor_memory";
   if (cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens)) return "cluster";
   if (cs2_eligible(h_q, h_kv, head_dim, max_len_extend)) return "column_split_two_tiles";
   if (cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, fp8)) return "column_split";
@@ -724,17 +735,20 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   int per_sm = pl.ctas_per_sm;
   if (cp.use_tc) {
     const int rm = 16 * pl.MT;
-    cp.fn = pick_tc_kernel(fp8, rm);
+    const bool rows_m = g_tc == 2;  // the rows-on-M stream (vtr_kernel)
+    cp.fn = rows_m ? kernel_tr(fp8, rm) : pick_tc_kernel(fp8, rm);
     cp.fn_comb = pick_combine_kernel(256, fp8);
     if (!prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("tensor-memory kernels unavailable");
     int ne = 0;
-    if (fp8)
+    if (rows_m)
+      fp8 ? tr_smem<true>(ne, cp.smem) : tr_smem<false>(ne, cp.smem);
+    else if (fp8)
       rm == 16 ? tc_smem<true, 16>(ne, cp.smem) : tc_smem<true, 32>(ne, cp.smem);
     else
       rm == 16 ? tc_smem<false, 16>(ne, cp.smem) : tc_smem<false, 32>(ne, cp.smem);
     if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
     pl.nst = ne;
-    cp.threads = tc::kThreads;
+    cp.threads = rows_m ? tr::kThreads : tc::kThreads;
   } else if (cp.use_cs || cp.use_cs2) {
     cp.fn = cp.use_cs2 ? kernel_d256(fp8, 4) : pick_cs_kernel(fp8);
     cp.fn_comb = pick_combine_kernel(256, fp8);

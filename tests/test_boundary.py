@@ -263,6 +263,16 @@ def test_call_form_names_the_form_of_each_shape():
         b, hq, hkv, d, dv, l, t, _ = args
         if want and d == dv:
             assert vsk.launches_per_call(b, hq, hkv, d, l, t) == (1 if want in ("cluster", "one_launch") else 2)
+    # the tensor-memory switch takes every head_dim 256 call of <= 32 packed rows
+    try:
+        for mode, want in ((1, "tensor_memory"), (2, "tensor_memory_rows")):
+            vsk.set_tuning_tc(mode)
+            assert f(64, 16, 2, 256, 256, 4, 64 * 20000, True) == want
+            assert f(3, 16, 2, 256, 256, 4, 1536, False) == want
+            assert f(2, 64, 2, 256, 256, 4, 100, False) == "one_launch"   # R = 128
+            assert f(64, 32, 8, 128, 128, 4, 64 * 20000, False) == "one_launch"
+    finally:
+        vsk.set_tuning_tc(0)
 
 
 def test_launches_per_call_follows_the_form_switches():
@@ -323,6 +333,8 @@ def test_launches_per_call_follows_the_form_switches():
         assert f(3, 16, 2, 256, 4, 1536) == 1                       # both off: one launch
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_tc(True)
+        assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
+        vsk.set_tuning_tc(2)
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
     finally:
         vsk.set_tuning_tc(False)

@@ -2,7 +2,10 @@
 kernel), against the fp64 oracle, with the one-launch mma.sync kernel checked
 beside each:
 
-- "tc": the tensor-memory stream (tcgen05.mma, accumulators in TMEM), head_dim 256;
+- "tc": the tensor-memory stream (tcgen05.mma, accumulators in TMEM), head_dim 256,
+  keys on the MMAs' M side;
+- "tcr": the tensor-memory stream with the packed query rows on M (e4m3
+  queries split into two exact e4m3 terms), head_dim 256;
 - "colsplit": the column-split mma.sync stream (two warps per 16-row query
   tile, each holding half the head dimension), head_dim 256;
 - "split": the stream-only mma.sync kernel at head_dim 64 and 128 (every case
@@ -60,14 +63,14 @@ def gpu_problem(spec, **over):
 
 
 def _select(m, form):
-    m.set_tuning_tc(form == "tc")
+    m.set_tuning_tc(2 if form == "tcr" else 1 if form == "tc" else 0)
     m.set_tuning_colsplit(2 if form in ("colsplit", "colsplit2") else 0)
     m.set_tuning_colsplit2(2 if form == "colsplit2" else 0)
     m.set_tuning_split_launch(2 if form in ("split", "split256") else 0)
     m.set_tuning_cluster(2 if form == "cluster" else 0)
 
 
-@pytest.fixture(scope="module", params=["tc", "colsplit", "colsplit2", "split", "split256", "cluster"])
+@pytest.fixture(scope="module", params=["tc", "tcr", "colsplit", "colsplit2", "split", "split256", "cluster"])
 def vsk(request):
     import speculative_decode_verify_prefix_gb300 as m
 
@@ -77,7 +80,7 @@ def vsk(request):
     _select(m, m.form)
     yield m
     m.set_tuning(0, 0)
-    m.set_tuning_tc(False)
+    m.set_tuning_tc(0)
     m.set_tuning_colsplit(1)
     m.set_tuning_colsplit2(1)
     m.set_tuning_split_launch(1)
