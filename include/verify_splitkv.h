@@ -251,8 +251,8 @@ int vsk_workspace_init(void* workspace, size_t bytes, void* stream);
  * word holds the flags of the most recent such call there).  Bits: 1 = a kv_indices value outside [0, pool); 2 = kv_indptr
  * not non-decreasing or beyond kv_indices; 4 = qo_indptr inconsistent with
  * l_ext; 8 = a pipeline wait that gave up after one second (only the
- * tensor-memory form of the stream, selected by vsk_set_tuning_tc(1), has
- * such waits: its CTA then stops streaming, frees its tensor memory and
+ * tensor-memory forms of the stream, selected by vsk_set_tuning_tc(1 or 2), have
+ * such waits: the CTA then stops streaming, frees its tensor memory and
  * exits, and that call's output is not valid; the default kernel has no
  * waits that can time out); 16 = a mask_indptr entry of
  * verify_splitkv_tree_fwd outside custom_mask.  Returns 1 on success, 0 on a
@@ -283,15 +283,18 @@ void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta);
  * result.  Process-wide; not thread-safe. */
 void vsk_set_tuning_tiles(int tiles_per_warp);
 
-/* Tuning switch, for A/B runs and tests: mode 1 sends head_dim 256 calls with
- * at most 32 packed query rows per KV head ((h_q / h_kv) * max_len_extend <=
- * 32) through the tensor-memory form of the prefix stream (tcgen05.mma with
- * accumulators in TMEM, one launch) followed by the combine kernel (a second
- * launch on the same stream: it folds the per-piece partials, adds the draft
- * block and writes o); any other value (and the
- * default) keeps every call on the mma.sync kernel, which is the faster of the
- * two on GB300 at these shapes.  Both forms compute the same result up to
- * rounding order.  Process-wide; not thread-safe. */
+/* Tuning switch, for A/B runs and tests: modes 1 and 2 send head_dim 256
+ * calls with at most 32 packed query rows per KV head ((h_q / h_kv) *
+ * max_len_extend <= 32) through a tensor-memory form of the prefix stream
+ * (tcgen05.mma with accumulators in TMEM, one launch) followed by the combine
+ * kernel (a second launch on the same stream: it folds the per-piece
+ * partials, adds the draft block and writes o).  Mode 1 puts the keys on the
+ * MMAs' M side (vtc_kernel), mode 2 the packed query rows (vtr_kernel: for an
+ * e4m3 pool the queries split exactly into two e4m3 terms so the scores come
+ * straight from the e4m3 K rows).  Any other value (and the default) keeps
+ * every call on the mma.sync kernels, which measured faster on GB300 at these
+ * shapes.  All forms compute the same result up to rounding order.
+ * Process-wide; not thread-safe. */
 void vsk_set_tuning_tc(int mode);
 
 /* Tuning switch, for A/B runs and tests, over head_dim 256 calls with at most
@@ -305,7 +308,7 @@ void vsk_set_tuning_tc(int mode);
  * capacity for the paged entry points) times h_kv are below 262,144 (bf16
  * pools) or 131,072 (e4m3), where it is the faster one on GB300 (from there
  * the stream-only kernel of vsk_set_tuning_split_launch takes over); mode 2
- * always takes it; mode 0 never does.  vsk_set_tuning_tc(1) takes
+ * always takes it; mode 0 never does.  vsk_set_tuning_tc(1 or 2) takes
  * precedence.  All forms compute the same result up to rounding order.
  * Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
@@ -349,7 +352,7 @@ void vsk_set_tuning_split_launch(int mode);
  * it when the call's prefix tokens (kv_indices entries, or block-table
  * capacity for the paged entry points) times h_kv are fewer than 2,048, where
  * it beat the one-launch kernel before that; mode 2 wherever it applies.
- * vsk_set_tuning_tc(1) takes precedence.  All forms compute the same result
+ * vsk_set_tuning_tc(1 or 2) takes precedence.  All forms compute the same result
  * up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_cluster(int mode);
 
