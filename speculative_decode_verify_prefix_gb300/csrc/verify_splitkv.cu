@@ -454,14 +454,16 @@ void tc_smem(int& ne, size_t& smem) {
   smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::ENT;
 }
 
-// Ring entries and shared memory of vtr_kernel (e4m3 pools: an even number,
-// so that V rows always sit in odd entries).
+// Ring of vtr_kernel: tile slots (K rows, then V rows of a 64-key tile) for
+// e4m3 pools, alternating K and V entries for bf16 pools; and its shared
+// memory.
 template <bool FP8>
 void tr_smem(int& ne, size_t& smem) {
   using G = tr::Geo<FP8>;
-  ne = std::min(tr::kMaxNE, (kSmemPerCTAMax - G::ring_off) / G::ENT);
-  if (FP8) ne &= ~1;
-  smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::ENT;
+  ne = std::min(tr::kMaxNE, (kSmemPerCTAMax - G::ring_off) / G::RING_UNIT);
+  // loaders publish a tile's key mask at most ring tiles + 2 ahead of its reader
+  ne = std::min(ne, FP8 ? tr::kMaskRing - 3 : 2 * (tr::kMaskRing - 3));
+  smem = static_cast<size_t>(G::ring_off) + static_cast<size_t>(ne) * G::RING_UNIT;
 }
 
 int prepare_kernel(KernelFn fn) {
@@ -746,7 +748,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
       rm == 16 ? tc_smem<true, 16>(ne, cp.smem) : tc_smem<true, 32>(ne, cp.smem);
     else
       rm == 16 ? tc_smem<false, 16>(ne, cp.smem) : tc_smem<false, 32>(ne, cp.smem);
-    if (ne < 4) return fail("tensor-memory ring of %d entries is too shallow", ne);
+    if (ne < (rows_m && fp8 ? 2 : 4)) return fail("tensor-memory ring of %d entries is too shallow", ne);
     pl.nst = ne;
     cp.threads = rows_m ? tr::kThreads : tc::kThreads;
   } else if (cp.use_cs || cp.use_cs2) {

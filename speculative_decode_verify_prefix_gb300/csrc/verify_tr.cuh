@@ -62,7 +62,10 @@ template <bool FP8>
 __device__ __forceinline__ int loader_index(int warp) {  // -1: not a loader
   return warp >= 9 ? warp - (FP8 ? 9 : 5) : (!FP8 && warp >= 4 && warp < 8 ? warp - 4 : -1);
 }
-constexpr int kMaxNE = 10;                 // ring entries at most
+// The ring: for e4m3 pools tile slots (K rows, then V rows of a 64-key tile,
+// freed once QK is done and V widened); for bf16 pools separate K and V
+// entries (a V entry stays until PV has read it in place), alternating.
+constexpr int kMaxNE = 10;                 // ring slots (e4m3) or entries (bf16) at most
 constexpr float kThr = 8.f;                // log2 headroom before the running maximum is raised
 constexpr int NCS = 1;                     // accumulation chains of S
 constexpr int kColO = 2 * NCS * KT;        // TMEM column of O; S buffer b, chain c at (b NCS + c) KT
@@ -75,21 +78,23 @@ constexpr int kAbortOff = 644;
 constexpr int kRedOff = 1024;              // per-warp largest |q| bits
 constexpr int kMaskOff = 2048;             // [kMaskRing][kMaskWords] valid-key words: tile + 1 (high half), key bits (low)
 constexpr int kMaskWords = 11;             // one per loader warp (at most 11)
-constexpr int kMaskRing = 8;               // > the tiles the loaders can run ahead of the softmax (kMaxNE / 2 + 2)
+constexpr int kMaskRing = 8;               // > the tiles the loaders can run ahead of the softmax
 constexpr int kDataOff = 3072;
 constexpr int kBFull = 0, kBEmpty = kMaxNE, kBSFull = 2 * kMaxNE, kBSEmpty = kBSFull + 2, kBPFull = kBSEmpty + 2,
               kBPEmpty = kBPFull + 2, kBV16Full = kBPEmpty + 2, kBV16Empty = kBV16Full + 2, kBQFull = kBV16Empty + 2,
               kNumBars = kBQFull + 1;
 static_assert(kBarOff + 8 * kNumBars <= kTmemOff, "barriers overlap");
 static_assert(kMaskOff + kMaskRing * kMaskWords * 8 <= kDataOff, "masks overlap");
-static_assert(kMaxNE / 2 + 3 <= kMaskRing, "mask ring too short");
+static_assert(kMaxNE / 2 + 3 <= kMaskRing, "mask ring too short (bf16 entries; e4m3 slots are capped on the host)");
 
 template <bool FP8>
 struct Geo {
   static constexpr int D = 256;
   static constexpr int ROWB = D * (FP8 ? 1 : 2);  // one K (or V) row of one head
   static constexpr int CPR = ROWB / 16;           // its 16-byte chunks
-  static constexpr int ENT = KT * ROWB;           // one ring entry: K or V rows of a tile
+  static constexpr int ENT = KT * ROWB;           // K (or V) rows of a tile
+  static constexpr int TILEB = 2 * ENT;           // one e4m3 ring slot: K rows, then V rows
+  static constexpr int RING_UNIT = FP8 ? TILEB : ENT;  // bytes per ring slot (e4m3) or entry (bf16)
   static constexpr int QB = 64 * ROWB;            // Qs
   static constexpr int PB = 64 * 128;             // one P buffer
   static constexpr int V16B = FP8 ? 4 * KT * 128 : 0;  // one widened V tile
@@ -99,14 +104,14 @@ struct Geo {
   static constexpr int ring_off = v16_off + 2 * V16B;
 };
 
-// Position of a ring entry: slot and lap (entries e, e + 2, e + 4, ...).
+// Position in the ring: slot and lap.
 struct RingPos {
   int slot;
   uint32_t lap;
-  __device__ __forceinline__ void step2(int ne) {
-    slot += 2;
-    if (slot >= ne) {
-      slot -= ne;
+  __device__ __forceinline__ void step(int n, int by = 1) {
+    slot += by;
+    if (slot >= n) {
+      slot -= n;
       ++lap;
     }
   }
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
   constexpr int ENT = G::ENT;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NE = p.nst;
+  const int NE = p.nst;  // ring slots (e4m3) or entries (bf16)
 
   long long start, end, W;
   Seg seg0;
@@ -333,9 +338,10 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < NE; ++i) {
-      mbar_init(bar(tr::kBFull + i), NL * 32);  // every loader lane copies part of each entry
-      // e4m3 pools: odd entries hold V rows, released by the four widening warps
-      mbar_init(bar(tr::kBEmpty + i), (FP8 && (i & 1)) ? 4 : 1);
+      mbar_init(bar(tr::kBFull + i), NL * 32);  // every loader lane copies part of each slot / entry
+      // e4m3: released by the QK products' commit and the four widening
+      // warps; bf16: by the commit of the products that read the entry
+      mbar_init(bar(tr::kBEmpty + i), FP8 ? 1 + 4 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(tr::kBSFull + b), 1);
@@ -377,8 +383,8 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
     const int tlo = KT * lw / NL, cnt = KT * (lw + 1) / NL - tlo;  // this warp's tokens of a tile
     tr::RingPos pos{0, 0u};
     uint32_t tile = 0;  // tiles issued
-    // one tile: its two ring entries (K rows, then V rows) from the pool rows
-    // of this warp's cnt tokens (lane j < cnt holds token tlo + j's row)
+    // one tile: its ring slot (K rows, then V rows) from the pool rows of
+    // this warp's cnt tokens (lane j < cnt holds token tlo + j's row)
     auto load_tile = [&](const TileIt& it, long long raw) {
       const int t = it.tok + tlo + lane;
       const long long loc = tile_loc(p, it, tlo + lane, raw);
@@ -386,16 +392,17 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
       if (lane < cnt && t < it.te && !ok) atomicOr(p.err, kErrBadIndex);
       const unsigned m = __ballot_sync(0xffffffffu, ok);
       const long long head = it.s.hg;
+      const unsigned char* kbase = p.kb + head * p.kb_s1;
+      const unsigned char* vbase = p.vb + head * p.vb_s1;
 #pragma unroll 1
-      for (int kv = 0; kv < 2; ++kv) {
+      for (int kv = 0; kv < (FP8 ? 1 : 2); ++kv) {
+        // e4m3: one slot for K and V; bf16: the K entry, then the V entry
         const int slot = pos.slot;
         tr::wait_warp(bar(tr::kBEmpty + slot), (pos.lap & 1u) ^ 1u, abort_flag, p.err);
         if (kv == 0 && lane == 0)
           // this warp's valid keys of the tile (token tlo + j: bit j), tagged
           maskq[(tile % tr::kMaskRing) * tr::kMaskWords + lw] = (static_cast<unsigned long long>(tile + 1) << 32) | m;
-        const unsigned char* base = (kv ? p.vb + head * p.vb_s1 : p.kb + head * p.kb_s1);
-        const long long s0 = kv ? p.vb_s0 : p.kb_s0;
-        const uint32_t dst0 = ring_s + static_cast<uint32_t>(slot) * ENT;
+        const uint32_t d0 = ring_s + static_cast<uint32_t>(slot) * G::RING_UNIT;
 #pragma unroll
         for (int i = 0; i < (TPW + TSTEP - 1) / TSTEP; ++i) {
           const int tl = i * TSTEP + lane / LPT;  // token among this warp's cnt
@@ -403,20 +410,20 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
           if (tl < cnt) {
             const bool v = (m >> tl) & 1u;
             const int tt = tlo + tl;  // token within the tile
-            const unsigned char* srow = v ? base + lc * s0 : reinterpret_cast<const unsigned char*>(p.q);
+            const unsigned char* q0 = reinterpret_cast<const unsigned char*>(p.q);
+            const unsigned char* sk = v ? (kv ? vbase + lc * p.vb_s0 : kbase + lc * p.kb_s0) : q0;
+            const unsigned char* sv = v && FP8 ? vbase + lc * p.vb_s0 : q0;
 #pragma unroll
             for (int cj = 0; cj < CPL; ++cj) {
               const int c = lane % LPT + LPT * cj;
-              const uint32_t d = dst0 + (c >> 3) * (KT * 128) + tt * 128 + (((c & 7) ^ (tt & 7)) << 4);
-              cp_async_16_zfill(d, v ? srow + c * 16 : srow, v, pol);
+              const uint32_t d = (c >> 3) * (KT * 128) + tt * 128 + (((c & 7) ^ (tt & 7)) << 4);
+              cp_async_16_zfill(d0 + d, v ? sk + c * 16 : sk, v, pol);
+              if constexpr (FP8) cp_async_16_zfill(d0 + ENT + d, v ? sv + c * 16 : sv, v, pol);
             }
           }
         }
         cp_async_arrive_noinc(bar(tr::kBFull + slot));
-        if (++pos.slot == NE) {
-          pos.slot = 0;
-          ++pos.lap;
-        }
+        pos.step(NE);
       }
       ++tile;
     };
@@ -455,7 +462,8 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
       // descriptors of the operands' bases; an offset is added in 16-byte units
       const uint64_t dq0 = sdesc(q_s, 16, 1024), dk0 = sdesc(ring_s, 16, 1024), dp0 = sdesc(p_s, 16, 1024);
       const uint64_t dv0 = sdesc(FP8 ? v16_s : ring_s, KT * 128, 1024);
-      tr::RingPos kpos{0, 0u}, vpos{1, 0u};  // K entry of the next QK tile, V entry of the next PV tile
+      // ring positions of the next QK tile and the next PV tile (bf16: its V entry)
+      tr::RingPos kpos{0, 0u}, vpos{FP8 ? 0 : 1, 0u};
       long long u = 0, qp = 0;
       long long pu = -1;  // tile whose PV is pending
       bool pfirst = false;
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
           tr::wait(bar(tr::kBV16Full + (w & 1)), static_cast<uint32_t>((w >> 1) & 1), abort_flag, p.err);
         else
           tr::wait(bar(tr::kBFull + slotV), vpos.lap & 1u, abort_flag, p.err);
-        vpos.step2(NE);
+        vpos.step(NE, FP8 ? 1 : 2);
         fence_proxy_async();
         tc_fence_after();
         const uint64_t pd = dp0 + static_cast<uint64_t>(((w & 1) * G::PB) >> 4);
@@ -496,11 +504,11 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
           for (int tok0 = t0; tok0 < te; tok0 += KT, ++u) {
             const int slotK = kpos.slot;
             tr::wait(bar(tr::kBFull + slotK), kpos.lap & 1u, abort_flag, p.err);
-            kpos.step2(NE);
+            kpos.step(NE, FP8 ? 1 : 2);
             tr::wait(bar(tr::kBSEmpty + (u & 1)), static_cast<uint32_t>(((u >> 1) & 1) ^ 1), abort_flag, p.err);
             fence_proxy_async();
             tc_fence_after();
-            const uint64_t kd = dk0 + static_cast<uint64_t>((slotK * ENT) >> 4);
+            const uint64_t kd = dk0 + static_cast<uint64_t>((slotK * G::RING_UNIT) >> 4);
             const uint32_t sS = tmem + static_cast<uint32_t>((u & 1) * tr::NCS * KT);
 #pragma unroll
             for (int ks = 0; ks < NKS; ++ks) {
@@ -535,13 +543,13 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
       it.te = piece_real_end(seg0, end);
       tile_settle(p, it, end);
       long long u = 0;
-      tr::RingPos vpos{1, 0u};
+      tr::RingPos vpos{0, 0u};
       while (it.valid) {
         const int slotV = vpos.slot;
         tr::wait_warp(bar(tr::kBFull + slotV), vpos.lap & 1u, abort_flag, p.err);
-        vpos.step2(NE);
+        vpos.step(NE);
         tr::wait_warp(bar(tr::kBV16Empty + (u & 1)), static_cast<uint32_t>(((u >> 1) & 1) ^ 1), abort_flag, p.err);
-        const unsigned char* raw = smem + G::ring_off + slotV * ENT;
+        const unsigned char* raw = smem + G::ring_off + slotV * G::TILEB + ENT;
         unsigned char* v16 = smem + G::v16_off + (u & 1) * G::V16B;
 #pragma unroll
         for (int i = 0; i < KT * CPR / 128; ++i) {
