@@ -427,30 +427,33 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
       }
       ++tile;
     };
-    // pool rows are read kPF tiles before their tile is copied
-    constexpr int kPF = 4;
+    // pool rows are read four tiles before their tile is copied, rotating
+    // through registers (one copy of the tile code: a small instruction
+    // footprint beside the other roles)
     TileIt cur;
     cur.s = seg0;
     cur.tok = static_cast<int>(start - seg0.off);
     cur.te = piece_real_end(seg0, end);
     tile_settle(p, cur, end);
     TileIt ahead = cur;
-    long long rows[kPF];
-#pragma unroll
-    for (int k = 0; k < kPF; ++k) {
-      rows[k] = tile_raw(p, ahead, lane < cnt ? tlo + lane : KT);
-      tile_next(p, ahead, end);
-    }
+    const int jl = lane < cnt ? tlo + lane : KT;
+    long long r0 = tile_raw(p, ahead, jl);
+    tile_next(p, ahead, end);
+    long long r1 = tile_raw(p, ahead, jl);
+    tile_next(p, ahead, end);
+    long long r2 = tile_raw(p, ahead, jl);
+    tile_next(p, ahead, end);
+    long long r3 = tile_raw(p, ahead, jl);
+    tile_next(p, ahead, end);
+#pragma unroll 1
     while (cur.valid) {
-#pragma unroll
-      for (int k = 0; k < kPF; ++k) {
-        if (cur.valid) {
-          load_tile(cur, rows[k]);
-          rows[k] = tile_raw(p, ahead, lane < cnt ? tlo + lane : KT);
-          tile_next(p, ahead, end);
-          tile_next(p, cur, end);
-        }
-      }
+      load_tile(cur, r0);
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
+      r3 = tile_raw(p, ahead, jl);
+      tile_next(p, ahead, end);
+      tile_next(p, cur, end);
     }
     cp_async_wait<0>();
   } else if (warp == tr::kWarpMma) {
