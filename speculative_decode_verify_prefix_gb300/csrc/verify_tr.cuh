@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
           // this warp's valid keys of the tile (token tlo + j: bit j), tagged
           maskq[(tile % tr::kMaskRing) * tr::kMaskWords + lw] = (static_cast<unsigned long long>(tile + 1) << 32) | m;
         const uint32_t d0 = ring_s + static_cast<uint32_t>(slot) * G::RING_UNIT;
-#pragma unroll
+#pragma unroll 1
         for (int i = 0; i < (TPW + TSTEP - 1) / TSTEP; ++i) {
           const int tl = i * TSTEP + lane / LPT;  // token among this warp's cnt
           const long long lc = __shfl_sync(0xffffffffu, loc, tl & 31);
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
         tr::wait_warp(bar(tr::kBV16Empty + (u & 1)), static_cast<uint32_t>(((u >> 1) & 1) ^ 1), abort_flag, p.err);
         const unsigned char* raw = smem + G::ring_off + slotV * G::TILEB + ENT;
         unsigned char* v16 = smem + G::v16_off + (u & 1) * G::V16B;
-#pragma unroll
+#pragma unroll 2
         for (int i = 0; i < KT * CPR / 128; ++i) {
           const int ci = ct + 128 * i;
           const int tt = ci / CPR, c = ci % CPR;
