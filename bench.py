@@ -46,7 +46,7 @@ import workloads  # noqa: E402
 METRIC = "verify-attn KV GB/s (fraction of GB300 HBM peak) and µs/call, 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_DIR = os.path.join(ROOT, "speculative_decode_verify_prefix_gb300", "csrc")
-KERNEL_SRCS = ("verify_kernel.cuh", "verify_combine.cuh", "verify_tc.cuh")  # every kernel of a call
+KERNEL_SRCS = ("verify_kernel.cuh", "verify_combine.cuh", "verify_tc.cuh", "verify_tr.cuh")  # every kernel of a call
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
@@ -132,10 +132,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--one-launch", action="store_true",
                     help="keep every call on the one-launch kernel (no column split, no stream + combine launches)")
-    ap.add_argument("--tc", type=int, nargs="?", const=1, default=0, metavar="MODE",
-                    help="head_dim 256 calls stream the prefix with a tensor-memory kernel (tcgen05; two "
-                         "launches per call, then the combine kernel): 1 (the bare flag) vtc_kernel, keys "
-                         "on the MMAs' M side; 2 vtr_kernel, packed query rows on M")
+    ap.add_argument("--tc", type=int, nargs="?", const=2, default=None, metavar="MODE",
+                    help="head_dim 256 tensor-memory streams (tcgen05; two launches per call, then the "
+                         "combine kernel): 2 (the bare flag) vtr_kernel, packed query rows on the MMAs' M side, "
+                         "wherever it applies; 1 vtc_kernel, keys on M; 0 neither; unset: the library's "
+                         "default (vtr_kernel where it measured faster)")
     ap.add_argument("--report-configs", action="store_true",
                     help="print a per-configuration table (tiny, d256, GQA sweep, fp8, serving) instead of the JSON line")
     ap.add_argument("--config-calls", type=int, default=0, metavar="N",
@@ -453,8 +454,7 @@ def run_ours(args, dist: Dist) -> dict:
     dev = torch.device("cuda", dist.local_rank)
     spec = WORKLOADS[args.workload]
     # the tensor-memory stream serves head_dim 256 with at most 32 packed rows per KV head
-    tc = int(args.tc) if spec.d == 256 and (spec.h_q // spec.h_kv) * spec.l_ext <= 32 else 0
-    vsk.set_tuning_tc(tc)
+    vsk.set_tuning_tc(0 if args.one_launch else (3 if args.tc is None else int(args.tc)))
     vsk.set_tuning_colsplit(0 if args.one_launch else 1)
     vsk.set_tuning_split_launch(0 if args.one_launch else 1)
     vsk.set_tuning_cluster(0)

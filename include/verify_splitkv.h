@@ -283,18 +283,21 @@ void vsk_set_tuning_shape(int max_ring_stages, int max_kv_heads_per_cta);
  * result.  Process-wide; not thread-safe. */
 void vsk_set_tuning_tiles(int tiles_per_warp);
 
-/* Tuning switch, for A/B runs and tests: modes 1 and 2 send head_dim 256
- * calls with at most 32 packed query rows per KV head ((h_q / h_kv) *
- * max_len_extend <= 32) through a tensor-memory form of the prefix stream
- * (tcgen05.mma with accumulators in TMEM, one launch) followed by the combine
- * kernel (a second launch on the same stream: it folds the per-piece
- * partials, adds the draft block and writes o).  Mode 1 puts the keys on the
- * MMAs' M side (vtc_kernel), mode 2 the packed query rows (vtr_kernel: for an
- * e4m3 pool the queries split exactly into two e4m3 terms so the scores come
- * straight from the e4m3 K rows).  Any other value (and the default) keeps
- * every call on the mma.sync kernels, which measured faster on GB300 at these
- * shapes.  All forms compute the same result up to rounding order.
- * Process-wide; not thread-safe. */
+/* Tuning switch over head_dim 256 calls with at most 32 packed query rows
+ * per KV head ((h_q / h_kv) * max_len_extend <= 32): the tensor-memory forms
+ * of the prefix stream (tcgen05.mma with accumulators in TMEM, one launch),
+ * each followed by the combine kernel (a second launch on the same stream: it
+ * folds the per-piece partials, adds the draft block and writes o).
+ * vtr_kernel puts the packed query rows on the MMAs' M side (for an e4m3 pool
+ * the queries split exactly into two e4m3 terms, so the scores come straight
+ * from the e4m3 K rows); vtc_kernel puts the keys there.  Mode 3 (the
+ * default) takes vtr_kernel where it measured faster on GB300: e4m3 pools with
+ * 17-32 packed rows, or up to 16 rows below 1,048,576 prefix tokens x h_kv;
+ * bf16 pools with up to 16 rows, or 17-32 rows below 786,432; never past
+ * 8,388,608 (the one-launch kernel there).  Mode 2 takes vtr_kernel wherever
+ * it applies, mode 1 vtc_kernel, mode 0 neither (the mma.sync forms only);
+ * other values select mode 3.  All forms compute the same result up to
+ * rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_tc(int mode);
 
 /* Tuning switch, for A/B runs and tests, over head_dim 256 calls with at most

@@ -288,11 +288,13 @@ def set_tuning_tiles(tiles_per_warp: int = 0) -> None:
     _native.lib().vsk_set_tuning_tiles(int(tiles_per_warp))
 
 
-def set_tuning_tc(mode: int = 0) -> None:
-    """Route head_dim 256 calls (at most 32 packed rows per KV head) through a
-    tensor-memory stream: 1 (or ``True``) the one with the keys on the MMAs' M
-    side, 2 the one with the packed query rows on M; 0 (or ``False``, the
-    default) keeps them on the mma.sync kernels.  For A/B runs and tests."""
+def set_tuning_tc(mode: int = 3) -> None:
+    """Head_dim 256 calls (at most 32 packed rows per KV head) and the
+    tensor-memory streams: 3 (the default) the one with the packed query rows
+    on the MMAs' M side where it measured faster (by pool dtype, packed rows and
+    size), 2 that one wherever it applies, 1 (or ``True``) the one with the keys
+    on M wherever it applies, 0 (or ``False``) never (the mma.sync kernels
+    only).  For A/B runs and tests."""
     _native.lib().vsk_set_tuning_tc(int(mode))
 
 

@@ -33,6 +33,12 @@ constexpr long long kPiecesPerSegmentColSplit = 48;  // ... over this many for t
 constexpr long long kColSplitEndBf16 = 1LL << 18;  // head_dim 256: column split below this many token-heads (bf16)
 constexpr long long kColSplitEndE4m3 = 1LL << 17;  // ... (e4m3 pools); from there the stream-only kernel + combine
 constexpr long long kSplit256MaxWork = 1LL << 23;   // ... up to which head_dim 256 takes the stream-only kernel + combine
+// head_dim 256, <= 32 packed rows: the rows-on-M tensor-memory stream + combine
+// (measured faster) for e4m3 pools with 17-32 rows, or <= 16 rows below
+// kRowsMR16EndE4m3; for bf16 pools with <= 16 rows, or 17-32 rows below
+// kRowsMEndBf16; never past kSplit256MaxWork (the one-launch kernel there)
+constexpr long long kRowsMR16EndE4m3 = 1LL << 20;
+constexpr long long kRowsMEndBf16 = 3LL << 18;
 constexpr long long kSplitLaunchMaxWork = 1LL << 22;   // head_dim 64 / 128: stream-only + combine up to (R > 16)
 constexpr long long kSplitLaunchMaxWork16 = 1LL << 23;  // ... (at most 16 packed rows)
 constexpr long long kSplitTwoTileMinTokens = 1LL << 18;  // prefix tokens from which their warps take two tiles
@@ -62,7 +68,7 @@ long long g_min_tokens = 0;
 int g_max_stages = 0;
 int g_max_heads = 0;
 int g_tiles = 0;  // tiles per warp override (0 = default)
-int g_tc = 0;     // tensor-memory stream for head_dim 256: 1 keys on M, 2 rows on M, 0 off (the default)
+int g_tc = 3;     // tensor-memory stream for head_dim 256: 3 rows on M by pool and size (default), 2 / 1 rows / keys on M always, 0 never
 int g_cs = 1;     // column-split stream for head_dim 256: 1 below kColSplitEnd*, 2 always, 0 never
 int g_sl = 1;     // stream + combine launches for head_dim 64 / 128: 1 below kSplitLaunchMaxWork, 2 always, 0 never
 int g_cs2 = 1;    // two-tile column split at head_dim 256: 2 always; 0 and 1 (the default) never
@@ -148,11 +154,18 @@ bool make_plan(long long h_q, long long h_kv, long long D, long long L, bool fp8
   return true;
 }
 
-// The tensor-memory stream (vtc_kernel) serves head_dim 256 with at most 32
-// packed query rows per KV head.
-bool tc_eligible(long long h_q, long long h_kv, long long D, long long L) {
+// The tensor-memory streams (vtc_kernel, vtr_kernel) serve head_dim 256 with
+// at most 32 packed query rows per KV head; by default (mode 3) the rows-on-M
+// one takes the calls where it measured faster (total_tokens: prefix tokens
+// from static shapes).
+bool tc_eligible(long long h_q, long long h_kv, long long D, long long L, long long total_tokens, bool fp8) {
   if (g_tc == 0 || D != 256 || h_kv <= 0 || h_q % h_kv != 0) return false;
-  return (h_q / h_kv) * L <= 32;
+  const long long R = (h_q / h_kv) * L;
+  if (R > 32) return false;
+  if (g_tc != 3) return true;
+  const long long work = total_tokens * h_kv;
+  if (work > kSplit256MaxWork) return false;
+  return fp8 ? (R > 16 || work < kRowsMR16EndE4m3) : (R <= 16 || work < kRowsMEndBf16);
 }
 
 // Plan fields of a two-launch call (tensor-memory or column-split stream,
@@ -610,7 +623,7 @@ void vsk_set_tuning(int num_ctas, int min_tokens_per_cta) {
 
 void vsk_set_tuning_tiles(int tiles_per_warp) { g_tiles = tiles_per_warp == 1 || tiles_per_warp == 2 ? tiles_per_warp : 0; }
 
-void vsk_set_tuning_tc(int mode) { g_tc = (mode == 1 || mode == 2) ? mode : 0; }
+void vsk_set_tuning_tc(int mode) { g_tc = (mode >= 0 && mode <= 2) ? mode : 3; }
 
 void vsk_set_tuning_colsplit(int mode) { g_cs = (mode == 0 || mode == 2) ? mode : 1; }
 
@@ -629,12 +642,12 @@ int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
   if (batch < 1 || h_kv <= 0 || h_q % h_kv != 0 || max_len_extend < 1 || prefix_tokens < 0) return 0;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
   const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
-  if (!tc_eligible(h_q, h_kv, head_dim, max_len_extend) &&
+  if (!tc_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) &&
       cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens))
     return 1;
   // (the pool dtype moves only the boundary between two-launch forms: the
   // bf16 thresholds give the same count)
-  return (tc_eligible(h_q, h_kv, head_dim, max_len_extend) || cs2_eligible(h_q, h_kv, head_dim, max_len_extend) ||
+  return (tc_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) || cs2_eligible(h_q, h_kv, head_dim, max_len_extend) ||
           cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false) ||
           sl_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, false))
              ? 2
@@ -650,7 +663,7 @@ const char* vsk_call_form(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head
   const long long tokens = prefix_tokens / batch * batch;  // the entry points' static estimate
   const bool fp8 = fp8_pool != 0;
   // the same order as the planner's
-  if (tc_eligible(h_q, h_kv, head_dim, max_len_extend)) return g_tc == 2 ? "tensor_memory_rows" : "tensor_memory";
+  if (tc_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, fp8)) return g_tc == 1 ? "tensor_memory" : "tensor_memory_rows";
   if (cl_eligible(batch, h_q, h_kv, head_dim, head_dim, max_len_extend, tokens)) return "cluster";
   if (cs2_eligible(h_q, h_kv, head_dim, max_len_extend)) return "column_split_two_tiles";
   if (cs_eligible(h_q, h_kv, head_dim, max_len_extend, tokens, fp8)) return "column_split";
@@ -698,7 +711,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   cp.D = static_cast<int>(D);
   // the two-launch forms and the cluster form are built for head_dim == v_head_dim only
   const bool same = D == DV;
-  cp.use_tc = same && tc_eligible(h_q, h_kv, D, L);
+  cp.use_tc = same && tc_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
   cp.use_cl = !cp.use_tc && cl_eligible(B, h_q, h_kv, D, DV, L, mean_len * B);
   cp.use_cs2 = same && !cp.use_tc && !cp.use_cl && cs2_eligible(h_q, h_kv, D, L);
   cp.use_cs = same && !cp.use_tc && !cp.use_cl && !cp.use_cs2 && cs_eligible(h_q, h_kv, D, L, mean_len * B, fp8);
@@ -737,7 +750,7 @@ static int plan_call(long long B, long long h_q, long long h_kv, long long D, lo
   int per_sm = pl.ctas_per_sm;
   if (cp.use_tc) {
     const int rm = 16 * pl.MT;
-    const bool rows_m = g_tc == 2;  // the rows-on-M stream (vtr_kernel)
+    const bool rows_m = g_tc != 1;  // the rows-on-M stream (vtr_kernel), else vtc_kernel
     cp.fn = rows_m ? kernel_tr(fp8, rm) : pick_tc_kernel(fp8, rm);
     cp.fn_comb = pick_combine_kernel(256, fp8);
     if (!prepare_kernel(cp.fn) || !prepare_kernel(cp.fn_comb)) return fail("tensor-memory kernels unavailable");

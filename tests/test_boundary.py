@@ -242,51 +242,75 @@ def test_paged_entry_rejects_bad_arguments(change, msg):
 
 def test_call_form_names_the_form_of_each_shape():
     """vsk_call_form: the form the planner takes for static shapes and the
-    pool dtype (default switches), consistent with vsk_launches_per_call."""
+    pool dtype (default switches), consistent with vsk_launches_per_call; then
+    the head_dim 256 forms with the tensor-memory streams switched off, and
+    with each of them forced."""
     f = vsk.call_form
-    cases = [
+
+    def check(cases):
+        for args, want in cases:
+            assert f(*args) == want, (args, f(*args))
+            b, hq, hkv, d, dv, l, t, _ = args
+            if want and d == dv:
+                assert vsk.launches_per_call(b, hq, hkv, d, l, t) == (1 if want in ("cluster", "one_launch") else 2)
+
+    rows = "tensor_memory_rows"
+    check([
         ((2, 4, 1, 64, 64, 4, 160, False), "stream_only"),              # the tiny case
         ((4, 16, 2, 128, 128, 4, 1028, False), "stream_only"),          # 2,056 token-heads
         ((64, 32, 8, 128, 128, 4, 64 * 20000, False), "one_launch"),    # the serving batch
-        ((3, 16, 2, 256, 256, 4, 1536, False), "column_split"),         # 3,072 token-heads
-        ((2, 16, 2, 256, 256, 4, 72000, False), "column_split"),        # 144,000: below 2^18 (bf16)
-        ((2, 16, 2, 256, 256, 4, 72000, True), "stream_only"),          # ... from 2^17 (e4m3)
-        ((8, 8, 2, 256, 256, 4, 8 * 20000, False), "stream_only"),
-        ((64, 16, 2, 256, 256, 4, 64 * 20000, True), "stream_only"),    # the long head_dim 256 batch
-        ((64, 16, 2, 256, 256, 4, 64 * 65537, False), "one_launch"),    # past 2^23 token-heads
+        ((3, 16, 2, 256, 256, 4, 1536, False), rows),                   # 3,072 token-heads
+        ((2, 16, 2, 256, 256, 4, 72000, True), rows),                   # e4m3, R = 32: any size up to 2^23
+        ((64, 16, 2, 256, 256, 4, 64 * 20000, True), rows),             # the long e4m3 batch
+        ((1, 16, 2, 256, 256, 4, 393215, False), rows),                 # bf16, R = 32: below 786,432 token-heads
+        ((1, 16, 2, 256, 256, 4, 393216, False), "stream_only"),        # ... from there
+        ((64, 16, 2, 256, 256, 4, 64 * 20000, False), "stream_only"),   # the long bf16 batch
+        ((8, 8, 2, 256, 256, 4, 8 * 20000, False), rows),               # bf16, R = 16: any size up to 2^23
+        ((1, 8, 2, 256, 256, 4, 524287, True), rows),                   # e4m3, R = 16: below 2^20
+        ((1, 8, 2, 256, 256, 4, 524288, True), "stream_only"),          # ... from there
+        ((64, 16, 2, 256, 256, 4, 64 * 65536, True), rows),             # exactly 2^23 token-heads
+        ((64, 16, 2, 256, 256, 4, 64 * 65537, True), "one_launch"),     # past 2^23 token-heads
+        ((64, 16, 2, 256, 256, 4, 64 * 65537, False), "one_launch"),
         ((2, 64, 2, 256, 256, 4, 100, False), "one_launch"),            # R = 128
         ((2, 16, 2, 128, 256, 4, 1000, False), "one_launch"),           # head_dim != v_head_dim
         ((2, 16, 2, 96, 96, 4, 1000, False), ""),                       # not built
-    ]
-    for args, want in cases:
-        assert f(*args) == want, (args, f(*args))
-        b, hq, hkv, d, dv, l, t, _ = args
-        if want and d == dv:
-            assert vsk.launches_per_call(b, hq, hkv, d, l, t) == (1 if want in ("cluster", "one_launch") else 2)
-    # the tensor-memory switch takes every head_dim 256 call of <= 32 packed rows
+    ])
     try:
-        for mode, want in ((1, "tensor_memory"), (2, "tensor_memory_rows")):
+        vsk.set_tuning_tc(0)  # the mma.sync forms only
+        check([
+            ((3, 16, 2, 256, 256, 4, 1536, False), "column_split"),     # 3,072 token-heads
+            ((2, 16, 2, 256, 256, 4, 72000, False), "column_split"),    # 144,000: below 2^18 (bf16)
+            ((2, 16, 2, 256, 256, 4, 72000, True), "stream_only"),      # ... from 2^17 (e4m3)
+            ((8, 8, 2, 256, 256, 4, 8 * 20000, False), "stream_only"),
+            ((64, 16, 2, 256, 256, 4, 64 * 20000, True), "stream_only"),
+            ((64, 16, 2, 256, 256, 4, 64 * 65537, False), "one_launch"),
+        ])
+        # a forced tensor-memory stream takes every head_dim 256 call of <= 32 packed rows
+        for mode, want in ((1, "tensor_memory"), (2, rows)):
             vsk.set_tuning_tc(mode)
-            assert f(64, 16, 2, 256, 256, 4, 64 * 20000, True) == want
+            assert f(64, 16, 2, 256, 256, 4, 64 * 20000, False) == want
+            assert f(64, 16, 2, 256, 256, 4, 64 * 65537, True) == want
             assert f(3, 16, 2, 256, 256, 4, 1536, False) == want
             assert f(2, 64, 2, 256, 256, 4, 100, False) == "one_launch"   # R = 128
             assert f(64, 32, 8, 128, 128, 4, 64 * 20000, False) == "one_launch"
     finally:
-        vsk.set_tuning_tc(0)
+        vsk.set_tuning_tc()
 
 
 def test_launches_per_call_follows_the_form_switches():
     """Head_dim 256 with at most 32 packed rows per KV head takes two launches
-    up to 2^23 prefix tokens x KV heads: the column-split stream below 2^18
+    up to 2^23 prefix tokens x KV heads, whichever stream serves it: with the
+    tensor-memory streams off (as here), the column-split stream below 2^18
     (bf16; 2^17 for e4m3 pools, which the host-only query does not know), the
     stream-only kernel from there, each followed by the combine launch; with
     the column split off, the stream-only form from 2,048.  The tensor-memory
-    switch takes precedence.  Head_dim 64 / 128 with at most 32 drafts takes the
+    switch takes precedence (by default within the same 2^23 window).  Head_dim 64 / 128 with at most 32 drafts takes the
     stream-only kernel plus the combine launch inside its own size window.
     The cluster form (one launch; off by default) takes small calls first when
     it is on.  Everything else is one launch."""
     f = vsk.launches_per_call
     try:
+        vsk.set_tuning_tc(0)
         vsk.set_tuning_cluster(1)
         # the cluster form (one launch): fewer than 2,048 token-heads, at most 512 segments
         assert f(2, 4, 1, 64, 4, 160) == 1                          # the tiny case
@@ -334,10 +358,15 @@ def test_launches_per_call_follows_the_form_switches():
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_tc(True)
         assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
+        assert f(3, 16, 2, 256, 4, 1536) == 2                       # over the one-launch switches
         vsk.set_tuning_tc(2)
-        assert f(64, 16, 2, 256, 4, 64 * 20000) == 2
+        assert f(64, 16, 2, 256, 4, 64 * 65537) == 2
+        vsk.set_tuning_tc()                                          # the default: the 2^23 window
+        assert f(3, 16, 2, 256, 4, 1536) == 2
+        assert f(64, 16, 2, 256, 4, 64 * 65536) == 2
+        assert f(64, 16, 2, 256, 4, 64 * 65537) == 1
     finally:
-        vsk.set_tuning_tc(False)
+        vsk.set_tuning_tc()
         vsk.set_tuning_colsplit(1)
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_cluster(0)

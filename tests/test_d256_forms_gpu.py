@@ -80,7 +80,7 @@ def vsk(request):
     _select(m, m.form)
     yield m
     m.set_tuning(0, 0)
-    m.set_tuning_tc(0)
+    m.set_tuning_tc()
     m.set_tuning_colsplit(1)
     m.set_tuning_colsplit2(1)
     m.set_tuning_split_launch(1)

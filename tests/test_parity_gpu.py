@@ -700,6 +700,7 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
     vsk.set_tuning_split_launch(0)  # the one-launch kernel: the form that draws tickets
     vsk.set_tuning_colsplit(0)
     vsk.set_tuning_cluster(0)
+    vsk.set_tuning_tc(0)
     try:
         assert vsk.launches_per_call(B, 32, 8, 128, 1, p["kv_indices"].shape[0]) == 1
         pb = gpu_problem(big)
@@ -712,6 +713,7 @@ def test_large_ticket_region_on_a_reused_buffer(vsk):
         vsk.set_tuning_split_launch(1)
         vsk.set_tuning_colsplit(1)
         vsk.set_tuning_cluster(0)
+        vsk.set_tuning_tc()
     check(ob, oracle_o(pb), scaled=SCALED)
 
 

@@ -8,8 +8,8 @@ scratch is an array built into the library's device image, shared by every
 call and keeping whatever the previous call left.
 
 These tests call it through the C ABI several times in a row, with problems
-of different shapes and forms in turn (a head_dim 256 e4m3 call served by a
-column-split stream plus a combine launch, a head_dim 128 stream plus combine,
+of different shapes and forms in turn (a head_dim 256 e4m3 call served by the
+rows-on-M tensor-memory stream plus a combine launch, a head_dim 128 stream plus combine,
 a cluster-form call and a one-launch call with tickets), so each call runs on
 what a differently shaped call left in the array.  Each result is compared with the fp64 oracle (the page's
 tolerance and the magnitude-scaled bound of the other parity tests) and with
@@ -94,7 +94,7 @@ def _check(got, ref):
 # (cluster, column split, stream + combine) modes.
 SPECS = [
     (workloads.Spec("noalloc_fp8_d256", (4096, 1500), 4, 16, 2, 256, 256, pool="e4m3", perm=True, k_scale=0.5,
-                    v_scale=0.25, seed=202), (0, 1, 1), 2),    # column split + combine
+                    v_scale=0.25, seed=202), (0, 1, 1), 2),    # rows-on-M tensor-memory stream + combine
     (workloads.Spec("noalloc_bf16_d128", (3000, 4000, 10, 0, 777), 4, 32, 8, 128, 128, perm=True, seed=201),
      (0, 1, 1), 2),                                            # stream + combine
     (workloads.Spec("noalloc_tiny", (64, 96), 4, 4, 1, 64, 64, seed=204), (1, 1, 1), 1),  # the cluster form
