@@ -478,7 +478,9 @@ def run_ours(args, dist: Dist) -> dict:
     value = aggregate(nbytes * args.steps, region_s, dist.world) / 1e9
     peak, peak_kind = hbm_peak()
     achieved = nbytes / launch_s / 1e9
-    traffic = traffic_per_launch(args.workload + ("_tc" if tc else ""))
+    # the committed ncu figures are for the default forms only
+    default_form = not args.one_launch and args.tc in (None, 3)
+    traffic = traffic_per_launch(args.workload) if default_form else None
     if prob.get("block_table") is not None:
         tokens = B * prob["block_table"].shape[1] * prob["page_size"]
     else:
