@@ -314,6 +314,9 @@ __global__ void __launch_bounds__(tr::kThreads, 1) vtr_kernel(const __grid_const
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NE = p.nst;  // ring slots (e4m3) or entries (bf16)
+  // the combine kernel, when launched as a programmatic dependent, may start
+  // its CTAs now (its griddepcontrol.wait still waits for this whole grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   long long start, end, W;
   Seg seg0;
