@@ -387,17 +387,19 @@ void vsk_set_tuning_pipe(int mode);
  * `prefix_tokens` is what the entry point sees: the length of kv_indices for
  * the flat entry points, batch x block-table columns x page_size for the paged
  * ones.  For head_dim == v_head_dim; a call with v_head_dim != head_dim makes
- * one launch.  Host only (no device call); for CUDA-graph bookkeeping and
- * launch counts. */
+ * one launch.  The count does not depend on the pool dtype (the pool-dependent
+ * cut-overs all lie between two-launch forms).  Host only (no device call);
+ * for CUDA-graph bookkeeping and launch counts. */
 int vsk_launches_per_call(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t max_len_extend,
                           int64_t prefix_tokens);
 
 /* The form a call of these static shapes takes under the current tuning
  * switches, as a static string: "one_launch" (the persistent kernel, tickets
  * for the merge), "cluster" (one launch of thread-block clusters),
- * "column_split", "column_split_two_tiles", "stream_only" or "tensor_memory"
- * (each a prefix stream, then the combine kernel), or "" for shapes no entry
- * point accepts.  fp8_pool: nonzero for an e4m3 K/V pool (some cut-overs
+ * "column_split", "column_split_two_tiles", "stream_only",
+ * "tensor_memory_rows" (vtr_kernel) or "tensor_memory" (vtc_kernel) (each a
+ * prefix stream, then the combine kernel), or "" for shapes no entry point
+ * accepts.  fp8_pool: nonzero for an e4m3 K/V pool (some cut-overs
  * depend on it).  prefix_tokens as for vsk_launches_per_call.  Host only. */
 const char* vsk_call_form(int64_t batch, int64_t h_q, int64_t h_kv, int64_t head_dim, int64_t v_head_dim,
                           int64_t max_len_extend, int64_t prefix_tokens, int fp8_pool);
