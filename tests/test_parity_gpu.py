@@ -188,6 +188,23 @@ def test_serving_scale_every_sequence(vsk):
     torch.cuda.empty_cache()
 
 
+def test_head_dim_256_long_every_sequence(vsk):
+    """The bf16 head_dim 256 benchmark shape (64 sequences, prefixes
+    U[8192, 32768], h_q/h_kv 16/2, 4 drafts) in its default form; the oracle
+    checks every sequence with the page's tolerance and the magnitude-scaled
+    bound, and a 10 % error planted in the oracle's result is rejected."""
+    spec = workloads.Spec("d256_b64_p8k_32k", None, 4, 16, 2, 256, 256, perm=True, batch=64,
+                          len_range=(8192, 32768), seed=1239)
+    p = gpu_problem(spec)
+    o = run_gpu(vsk, p)
+    assert torch.isfinite(o.float()).all()
+    assert vsk.read_error_flags() == 0
+    worst = check_every_sequence(p, o, planted_seq=0)
+    assert worst < 5e-3, worst  # bf16 rounding only
+    del p
+    torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------- edge cases
 EDGE = [
     workloads.Spec("mixed_ragged_empty", (0, 1, 15, 16, 17, 300, 0, 1000), 3, 8, 2, 128, 128, perm=True,
