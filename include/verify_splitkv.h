@@ -311,8 +311,9 @@ void vsk_set_tuning_tc(int mode);
  * capacity for the paged entry points) times h_kv are below 262,144 (bf16
  * pools) or 131,072 (e4m3), where it is the faster one on GB300 (from there
  * the stream-only kernel of vsk_set_tuning_split_launch takes over); mode 2
- * always takes it; mode 0 never does.  vsk_set_tuning_tc(1 or 2) takes
- * precedence.  All forms compute the same result up to rounding order.
+ * always takes it; mode 0 never does.  The tensor-memory streams of
+ * vsk_set_tuning_tc take precedence (by default the rows-on-M one takes most
+ * such calls).  All forms compute the same result up to rounding order.
  * Process-wide; not thread-safe. */
 void vsk_set_tuning_colsplit(int mode);
 
@@ -355,8 +356,8 @@ void vsk_set_tuning_split_launch(int mode);
  * it when the call's prefix tokens (kv_indices entries, or block-table
  * capacity for the paged entry points) times h_kv are fewer than 2,048, where
  * it beat the one-launch kernel before that; mode 2 wherever it applies.
- * vsk_set_tuning_tc(1 or 2) takes precedence.  All forms compute the same result
- * up to rounding order.  Process-wide; not thread-safe. */
+ * The tensor-memory streams of vsk_set_tuning_tc take precedence.  All forms
+ * compute the same result up to rounding order.  Process-wide; not thread-safe. */
 void vsk_set_tuning_cluster(int mode);
 
 /* Tuning switch, for A/B runs: how the combine kernel of the two-launch forms

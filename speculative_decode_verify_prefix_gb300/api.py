@@ -299,7 +299,8 @@ def set_tuning_tc(mode: int = 3) -> None:
 
 
 def set_tuning_colsplit(mode: int = 1) -> None:
-    """Head_dim 256 calls (at most 32 packed rows per KV head): stream with the
+    """Head_dim 256 calls (at most 32 packed rows per KV head) that no
+    tensor-memory stream takes (``set_tuning_tc``): stream with the
     column-split mma.sync kernel plus a combine launch for small calls (1, the
     default), always (2) or never (0); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_colsplit(int(mode))
@@ -315,8 +316,9 @@ def set_tuning_colsplit2(mode: int = 1) -> None:
 def set_tuning_split_launch(mode: int = 1) -> None:
     """Calls with at most 32 drafts: stream-only kernel plus a combine launch
     (head_dim 64 / 128: small and mid-size calls; head_dim 256: from where the
-    column split stops up to 2^23 prefix tokens x KV heads) by size (1, the
-    default), always (2) or never (0); for A/B runs and tests."""
+    column split stops up to 2^23 prefix tokens x KV heads, where no
+    tensor-memory stream takes the call) by size (1, the default), always (2)
+    or never (0); for A/B runs and tests."""
     _native.lib().vsk_set_tuning_split_launch(int(mode))
 
 

@@ -24,26 +24,33 @@
 // so O's row of packed row 8 w + j is lane j of sub-partition w.
 //
 // Roles (16 warps of 128 registers, one CTA per SM):
-//   warps 0-3   softmax: warp w reads sub-partition w.  Lanes j and j + 8
-//               exchange half of their scores (shfl_xor 8): lane j then holds
-//               the full scores of keys 0-31 of packed row 8 w + j, lane
-//               j + 8 those of keys 32-63.  Online softmax in the log2 domain
-//               with a running maximum raised only when a score exceeds it by
-//               more than 2^8 (the pair agrees through one more shuffle; O is
+//   warps 0-3   softmax: warp w reads sub-partition w in the 16-lane fragment
+//               shape (tcgen05.ld 16x256b), which hands each thread lanes g
+//               and g + 8, i.e. both terms of packed row 8 w + g, for 16 of
+//               the tile's keys; the four threads of a quad share the row.
+//               Online softmax in the log2 domain with a running maximum
+//               raised only when a score exceeds it by more than 2^8 (O is
 //               then rescaled in TMEM); P (f16 for e4m3 pools, bf16
 //               otherwise) into shared memory; the partial at a piece's end.
 //               They also load each piece's queries.
-//   warps 4-7   e4m3 pools: widen each V tile exactly to f16 (PV's B operand).
+//   warps 4-7   e4m3 pools: widen each V tile exactly to f16 (PV's B operand);
+//               bf16 pools: loaders.
 //   warp 8      TMEM allocation; lane 0 issues every MMA.
-//   warps 9-15  loaders: kv_indices / page ids, 16-byte cp.async gathers of
-//               the K and V rows into a ring of 64-key entries (K, V
-//               alternating), completion by cp.async.mbarrier.arrive.noinc.
+//   warps 9-15  loaders (with 4-7 for bf16 pools): kv_indices / page ids,
+//               16-byte cp.async gathers of the K and V rows into a ring
+//               (e4m3: one slot per 64-key tile, K rows then V rows; bf16:
+//               alternating K and V entries, a V entry being read in place by
+//               PV), completion by cp.async.mbarrier.arrive.noinc; each warp
+//               publishes its keys' validity in a tagged 8-byte word.
 // Operands in shared memory use the 128-byte swizzled canonical layouts:
 //   Qs (A), K tile (B)   K-major   [128-byte column block][row][128 B]
 //   P (A)                K-major   [row][128 B] (64 keys of 16 bits)
 //   V tile (B)           MN-major  [64-dv block][key][128 B]
 // Every mbarrier wait is bounded (one second); a wait that gives up sets the
 // CTA's abort flag and error bit 8, and the CTA drains, frees TMEM and exits.
+// Each role keeps a small code footprint (loops rolled, one copy of the
+// loader's tile code): four roles share every SM sub-partition's instruction
+// cache, and fetch stalls bounded an earlier version.
 #pragma once
 #include "verify_kernel.cuh"
 
